@@ -1,0 +1,129 @@
+/*
+ * ks_oracle.h — C interface of the CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY. The oracle is a plain, slow, per-lane CPU
+ * interpreter of the PTX subset that the GPU interpreter executes. Only the
+ * test suite, the package's smoke() check and bench.py's CPU-baseline /
+ * reference legs may load it. It shares no code, header, table or helper
+ * with the GPU path: its parser, its post-dominator computation and its
+ * instruction semantics are written separately here.
+ *
+ * Output formats that must match the GPU path byte for byte (written
+ * independently on each side):
+ *   - per-warp statistics record, 96 bytes (orc_warp_stats below);
+ *   - per-warp trace slot: 16-byte header {u32 n_events, u8 format=1,
+ *     u8 bytes_per_event=4, u16 n_dropped, u64 warp_cycles} followed by
+ *     max_ts 4-byte records, slot size rounded up to 8 bytes
+ *     (CuTeDSL IKET 浅析, §2 "buffer 是怎么定形的": warp_slot =
+ *     align8(16B header + maxTsCntPerWarp × bytes_per_event)).
+ */
+#ifndef KS_ORACLE_H
+#define KS_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (same numbering as the library's device statuses). */
+#define ORC_OK 0
+#define ORC_ERR_PARSE (-1)
+#define ORC_ERR_UNSUPPORTED (-2)
+#define ORC_ERR_ARG (-3)
+#define ORC_ERR_NOT_FOUND (-5)
+#define ORC_ST_OOB 1
+#define ORC_ST_MISALIGNED 2
+#define ORC_ST_STEP_LIMIT 3
+#define ORC_ST_SIMT_STACK 4
+#define ORC_ST_TIMEOUT 5
+#define ORC_ST_INJECTED 6
+
+/* Latency classes (index into orc_config.lat). */
+#define ORC_LAT_ALU 0 /* int/f32 add, sub, mul, mad, logic, shifts, cvt, mov, setp, selp, ld.param */
+#define ORC_LAT_FMA 1 /* fma.rn.f32 */
+#define ORC_LAT_LDG 2 /* ld.global */
+#define ORC_LAT_STG 3 /* st.global */
+#define ORC_LAT_BRA 4 /* bra */
+#define ORC_LAT_SFU 5 /* div.rn.f32, sqrt.rn.f32 */
+#define ORC_LAT_RET 6 /* ret, exit */
+#define ORC_NUM_LAT 8 /* slot 7 is reserved */
+
+/* Simulated global buffer: caller-chosen simulated base address (4 KiB
+ * aligned, non-overlapping) backed by host memory. */
+typedef struct {
+  uint64_t sim_base;
+  void* host;
+  uint64_t bytes;
+} orc_buffer;
+
+/* Run modes. */
+#define ORC_MODE_WARP 0       /* warp-level SIMT with the reconvergence stack (the method) */
+#define ORC_MODE_PER_THREAD 1 /* every thread alone, scalar (memory and status only) */
+
+typedef struct {
+  uint32_t lat[ORC_NUM_LAT];
+  uint32_t max_ts_per_warp;
+  uint32_t stack_depth;     /* SIMT stack entries per warp, base entry included */
+  uint64_t step_limit;      /* max issued instructions per warp (per thread in per-thread mode) */
+  int64_t inject_warp;      /* global warp id that posts ORC_ST_INJECTED, -1 = off */
+  uint64_t inject_step;     /* ...when its issued-instruction count reaches this value */
+  uint32_t mode;            /* ORC_MODE_* */
+  uint32_t threads;         /* host worker threads, 0 = all hardware threads */
+  uint32_t race_check;      /* 1 = shadow-memory race checker (forces one thread) */
+  uint32_t n_warp_list;     /* 0 = every warp of the grid */
+  const uint32_t* warp_list;/* global warp ids to run when n_warp_list > 0 */
+} orc_config;
+
+/* Per-warp statistics record, 96 bytes. */
+typedef struct {
+  uint64_t cycles;
+  uint64_t warp_insts;
+  uint64_t thread_insts;
+  uint64_t ld_req;
+  uint64_t ld_sectors;
+  uint64_t st_req;
+  uint64_t st_sectors;
+  uint64_t ld_lines;
+  uint64_t st_lines;
+  int32_t status;
+  uint32_t max_stack_depth;
+  uint64_t reserved[2];
+} orc_warp_stats;
+
+/* Race checker result bits. */
+#define ORC_RACE_CROSS_THREAD 1u
+
+/* Fill cfg with the defaults: latency table {4,4,400,20,8,36,1,0},
+ * max_ts 0, stack depth 32, step limit 2^26, no injection, warp mode. */
+void orc_config_default(orc_config* cfg);
+
+/* Interpret `kernel` of the PTX module text over grid x block threads.
+ * stats: W records (W = grid * ceil(block/32)), indexed by global warp id;
+ *        only the warps that run are written.
+ * trace: NULL, or W slots of align8(16 + 4*max_ts) bytes.
+ * *status: status of the first warp (in run order) that stopped on an error.
+ * Returns ORC_OK or a negative code with a message in err. */
+int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+            const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+            uint32_t n_bufs, const orc_config* cfg, void* stats, void* trace,
+            int32_t* status, uint32_t* race_flags, char* err, uint64_t errlen);
+
+/* Immediate post-dominator of every program entry (instructions and trace
+ * pseudo-ops, in program order); the virtual exit is n (= *n_out). */
+int orc_ipdom(const char* ptx, const char* kernel, int32_t* out, uint32_t cap,
+              uint32_t* n_out, char* err, uint64_t errlen);
+
+/* Parameter layout: offsets/sizes in declaration order, total block size. */
+int orc_params(const char* ptx, const char* kernel, uint32_t* offsets,
+               uint32_t* sizes, uint32_t cap, uint32_t* n_params,
+               uint32_t* param_bytes, char* err, uint64_t errlen);
+
+/* Event table: kinds (0 mark, 1 range_start, 2 range_end) in id order. */
+int orc_events(const char* ptx, const char* kernel, uint32_t* kinds,
+               uint32_t cap, uint32_t* n_events, char* err, uint64_t errlen);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
