@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 warp-level SIMT PTX interpreter.
+
+Metric: simulated thread-instructions per second (sum over issued simulated
+instructions of the active lanes, divided by device time). One step is one
+pass of the whole hot path over the FFMA latency-probe pair (grid 132 x
+block 128, 4096 outer iterations of 32 fma.rn.f32, one dependent-chain
+kernel and one with 8 rotating accumulators), i.e. two interpreter launches.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload ffma_pair|vector_add|gather_sS|divergent_kK|fuzz]
+
+Prints one JSON line (rank 0). N > 1 runs N independent replicas, one per
+GPU (weak scaling; the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "simulated thread-instructions/sec"
+UNIT = "thread-inst/s"
+KERNEL_SRC = os.path.join(ROOT, "simt_ptx_interpretation_gb300", "csrc", "ks_interp.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_SM_MHZ = 2070.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="ffma_pair")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def workloads(name: str):
+    from simt_ptx_interpretation_gb300 import workloads as wl
+    if name == "ffma_pair":
+        return [wl.ffma(acc=1), wl.ffma(acc=8)], {
+            "workload": "ffma_probe_pair", "grid": 132, "block": 128, "iters": 4096, "fma_per_iter": 32,
+            "accumulators": [1, 8], "seed": 2}
+    if name == "vector_add":
+        return [wl.vector_add()], {"workload": "vector_add", "n": 4000, "grid": 16, "block": 256, "seed": 0}
+    if name.startswith("gather_s"):
+        s = int(name[len("gather_s"):])
+        return [wl.gather(s)], {"workload": name, "n_out": 1 << 24, "stride": s, "block": 256, "seed": 1}
+    if name.startswith("divergent_k"):
+        k = int(name[len("divergent_k"):])
+        return [wl.divergent(k)], {"workload": name, "threads": 1 << 20, "block": 128, "k": k, "seed": 3}
+    if name == "fuzz":
+        return [wl.fuzz(i) for i in range(64)], {"workload": "fuzz64", "grid": 1024, "block": 256, "kernels": 64,
+                                                 "seed": "1000+i, data 4"}
+    raise SystemExit(f"unknown workload {name}")
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_sha() -> str:
+    return hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+
+
+def traffic_for(workload: str):
+    """DRAM bytes per launch from the committed ncu capture, if it was taken
+    on the current kernel source; else None."""
+    try:
+        t = json.load(open(TRAFFIC_FILE))
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_sha") != kernel_sha():
+        return None
+    return t.get("workloads", {}).get(workload)
+
+
+def sm_peak_mhz():
+    try:
+        return float(json.load(open(PEAKS_FILE)).get("sm_max_mhz", FALLBACK_SM_MHZ)), "measured"
+    except (OSError, ValueError):
+        return FALLBACK_SM_MHZ, "fallback"
+
+
+# ---------------------------------------------------------------- ours ----
+
+def run_ours(args, world, rank, local):
+    import torch
+    import simt_ptx_interpretation_gb300 as ks
+    from simt_ptx_interpretation_gb300 import _build
+
+    if not _build.up_to_date():
+        _build.build_native()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ws, config = workloads(args.workload)
+    stream = torch.cuda.current_stream(dev)
+
+    # inputs resident in HBM; outputs preallocated
+    jobs = []
+    for w in ws:
+        mod = ks.Module(w.ptx)
+        host = [b.data for b in w.fresh_buffers()]
+        bufs = [(b.sim_base, torch.from_numpy(h.view(np.uint8)).to(dev)) for b, h in zip(w.buffers, host)]
+        cfg = ks.Config(max_ts=w.max_ts)
+        st = torch.empty(ks.stats_bytes(w.grid, w.block), dtype=torch.uint8, device=dev)
+        tr = torch.empty(ks.trace_bytes(w.grid, w.block, w.max_ts), dtype=torch.uint8, device=dev) if w.max_ts else None
+        jobs.append(dict(w=w, mod=mod, bufs=bufs, cfg=cfg, st=st, tr=tr))
+
+    def step():
+        for j in jobs:
+            w = j["w"]
+            ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"], stream)
+
+    # work per step (deterministic): one run, reduce totals, check statuses
+    step()
+    insts, launch_insts = 0, []
+    for j in jobs:
+        t = ks.read_stats(j["st"], j["w"].warps, stream)
+        if t.status != 0:
+            raise SystemExit(f"simulation status {t.status} on {j['w'].name}")
+        insts += t.thread_insts
+        launch_insts.append(t.thread_insts)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+
+    n_launch = len(jobs)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            evs[k][0].record(stream)
+            for i, j in enumerate(jobs):
+                w = j["w"]
+                ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"],
+                            stream)
+                evs[k][i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    step_ms = [evs[k][0].elapsed_time(evs[k][n_launch]) for k in range(args.steps)]
+    launch_ms = [[evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i in range(n_launch)]
+    dev_s = sum(step_ms) / 1e3
+    dev_s = max_over_ranks(dev_s, world)
+    value = insts * args.steps * world / dev_s
+    clocks = clk.summary()
+
+    # roofline of the interpreter kernel (every launch is ks_interp_kernel)
+    mhz, peak_src = sm_peak_mhz()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * 4 * 32 * mhz * 1e6 / 1e9  # G thread-inst/s: 4 warp-issues per SM per clock, 32 lanes
+    mean_launch_s = sum(sum(x) for x in launch_ms) / (args.steps * n_launch) / 1e3
+    achieved = (insts / n_launch) / mean_launch_s / 1e9
+    traffic = traffic_for(config["workload"])
+    roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "Gthread-inst/s",
+                "frac": round(achieved / peak, 5), "traffic": traffic,
+                "peak_source": f"{sms} SMs x 4 issue/clk x 32 lanes x {mhz:.0f} MHz ({peak_src})",
+                "algorithmic_units_per_launch": [int(x) for x in launch_insts],
+                "launch_ms_mean": [round(sum(x) / len(x), 4) for x in launch_ms]}
+
+    # end to end through the public API with pinned host buffers
+    e2e = run_e2e(args, jobs, insts, dev, stream)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sum(step_ms) / len(step_ms), 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)", "data": "synthetic (seeded)",
+        "config": dict(config, l2="flushed between steps (256 MiB write)", parallelism=f"replicas{world}"),
+        "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * n_launch, "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 3), "kernel_sha": kernel_sha(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(ws, sample_warps=None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, jobs, insts, dev, stream):
+    import torch
+    import simt_ptx_interpretation_gb300 as ks
+    pinned_in, pinned_out = [], []
+    h2d = d2h = 0
+    for j in jobs:
+        ins, outs = [], []
+        for b, (_, t) in zip(j["w"].buffers, j["bufs"]):
+            h = torch.from_numpy(b.data.view(np.uint8)).pin_memory()
+            if b.output:
+                outs.append((t, torch.empty_like(h).pin_memory()))
+                d2h += h.numel()
+            else:
+                ins.append((h, t))
+                h2d += h.numel()
+        outs.append((j["st"], torch.empty(j["st"].numel(), dtype=torch.uint8).pin_memory()))
+        d2h += j["st"].numel()
+        if j["tr"] is not None:
+            outs.append((j["tr"], torch.empty(j["tr"].numel(), dtype=torch.uint8).pin_memory()))
+            d2h += j["tr"].numel()
+        pinned_in.append(ins)
+        pinned_out.append(outs)
+    times = []
+    for k in range(args.e2e_steps):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for j, ins, outs in zip(jobs, pinned_in, pinned_out):
+                for h, t in ins:
+                    t.copy_(h, non_blocking=True)
+                w = j["w"]
+                ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"],
+                            stream)
+                for t, h in outs:
+                    h.copy_(t, non_blocking=True)
+        stream.synchronize()
+        times.append(time.perf_counter() - t0)
+    mean = sum(times) / len(times)
+    return {"value": round(insts / mean, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+
+
+def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None):
+    """The oracle, as it stands, on the host cores over a bounded sample of the
+    workload: the first `n` warps of every kernel."""
+    import oracle
+    cores = os.cpu_count() or 1
+    n = max_warps_per_kernel or 40 * cores
+    total_i, total_s, desc = 0, 0.0, []
+    for w in ws:
+        warps = list(range(min(n, w.warps)))
+        bufs = w.fresh_buffers()
+        t0 = time.perf_counter()
+        r = oracle.run(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in bufs],
+                       max_ts=w.max_ts, trace=bool(w.max_ts), warps=warps, threads=cores)
+        total_s += time.perf_counter() - t0
+        total_i += int(r.stats["thread_insts"][warps].sum())
+        desc.append(f"{w.name}: warps 0..{len(warps) - 1} of {w.warps}")
+    return {"value": round(total_i / total_s, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "; ".join(desc), "thread_insts": total_i, "seconds": round(total_s, 3)}
+
+
+# ----------------------------------------------------------- reference ----
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    ws, config = workloads(args.workload)
+    cores = os.cpu_count() or 1
+    per = max(4, min(64, 2 * cores))
+    for _ in range(args.warmup):
+        cpu_baseline(ws, max_warps_per_kernel=4)
+    times, insts = [], 0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        b = cpu_baseline(ws, max_warps_per_kernel=per)
+        times.append(time.perf_counter() - t0)
+        insts = b["thread_insts"]
+    value = insts * len(times) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)",
+        "data": "synthetic (seeded)", "config": dict(config, sample_warps_per_kernel=per),
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"first {per} warps of each kernel per step"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_init()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

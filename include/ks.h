@@ -1,0 +1,227 @@
+/*
+ * ks.h — C ABI of libks, a GB300 (sm_103a) warp-level SIMT PTX interpreter.
+ *
+ * What the library computes (KernelScope backend doc, simulator/engine.py and
+ * simulator/models.py — PtxSimulator, Thread, Warp, Block, TraceEvent): it
+ * steps every simulated warp of a simulated grid in lockstep over a decoded
+ * PTX program, one real GPU lane per simulated lane, and produces
+ *   1. the simulated global memory (the caller's device buffers, updated in
+ *      place by the simulated stores);
+ *   2. per-warp cycle counts from a fixed per-class latency table and an
+ *      in-order scoreboard (KernelScope backend doc, latency/model.py);
+ *   3. per-warp counts of 32-byte sectors and 128-byte lines touched by each
+ *      ld/st request (KernelScope backend doc, simulator/engine.py —
+ *      analyze_global_memory_access);
+ *   4. per-warp trace slots in the IKET layout (CuTeDSL IKET 浅析, §2:
+ *      16-byte header u32+u8+u8+u16+u64 then maxTsCntPerWarp 4-byte records,
+ *      slot size rounded up to 8 bytes, one slot per warp, no atomics).
+ *
+ * Supported PTX subset: add/sub (.u32 .s32 .u64 .s64 .f32), mul.lo/mad.lo
+ * (integers), mul.f32, fma.rn.f32, div.rn.f32, sqrt.rn.f32, and/or/xor
+ * (.b32 .b64 .pred), shl (.b32 .b64), shr (.b32 .b64 .u32 .u64 .s32 .s64),
+ * cvt (int<->int, .rn f32<-int, .rni/.rzi/.rmi/.rpi int<-f32), mov, setp
+ * (eq ne lt le gt ge, lo ls hi hs), selp, bra, ld.param, ld.global,
+ * st.global (4- and 8-byte), ret/exit; registers .b32 .u32 .s32 .f32 .b64
+ * .u64 .s64 .pred; special registers %tid %ntid %ctaid %nctaid (.x; .y/.z
+ * read 0 or 1) and %laneid; trace pseudo-ops written as comments
+ * `//@iket mark NAME`, `//@iket range_start NAME`, `//@iket range_end NAME`.
+ *
+ * Semantics fixed where the pages are silent:
+ *   - %tid.x is the thread's index in its CTA; lanes whose %tid.x >= block
+ *     are inactive from the start.
+ *   - Divergence: immediate post-dominator reconvergence stack; the
+ *     fall-through path runs first; `ret` removes its lanes from every entry.
+ *   - Cycles: t = max(t_next, ready[sources], ready[guard], ready[dests]);
+ *     dests ready at t + lat; bra/ret set t_next = t + lat, others t + 1;
+ *     a store completes at t + lat; cycles = max(last issue + 1, max ready,
+ *     last store completion). Trace pseudo-ops cost nothing and are not
+ *     counted. Guarded-off instructions still issue.
+ *   - thread_insts adds the number of active lanes of every issued
+ *     instruction; sectors are distinct addr>>5, lines distinct addr>>7, over
+ *     the lanes that execute the access; a request counts when at least one
+ *     lane executes it.
+ *   - f32: IEEE binary32 round-to-nearest-even with subnormals; every NaN
+ *     produced by add/sub/mul/fma/div/sqrt is stored as 0x7FFFFFFF.
+ *   - Two lanes of one st.global writing the same address: the highest lane's
+ *     value lands. Stores from different warps to the same address, or a load
+ *     of a word another warp stores, are undefined (warps run concurrently).
+ *   - Registers start at zero, predicates false.
+ */
+#ifndef KS_H
+#define KS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes (host errors are negative) ---------------------------- */
+#define KS_OK 0
+#define KS_ERR_PARSE (-1)       /* malformed PTX */
+#define KS_ERR_UNSUPPORTED (-2) /* valid PTX outside the supported subset */
+#define KS_ERR_ARG (-3)         /* bad argument (null pointer, size, shape) */
+#define KS_ERR_CUDA (-4)        /* a CUDA runtime call failed */
+#define KS_ERR_NOT_FOUND (-5)   /* no such kernel / index */
+#define KS_ERR_LIMIT (-6)       /* program or register file too large */
+
+/* ---- per-warp device statuses (positive, in ks_warp_stats.status) ------- */
+#define KS_ST_OOB 1          /* an address outside every buffer */
+#define KS_ST_MISALIGNED 2   /* address not a multiple of the access size */
+#define KS_ST_STEP_LIMIT 3   /* the warp tried to issue more than step_limit */
+#define KS_ST_SIMT_STACK 4   /* reconvergence stack deeper than allowed */
+#define KS_ST_TIMEOUT 5      /* a bounded wait inside the interpreter ran out */
+#define KS_ST_INJECTED 6     /* the debug injection point was reached */
+
+/* ---- latency classes (index of ks_config.lat) --------------------------- */
+#define KS_NUM_LAT_CLASSES 8
+#define KS_LAT_ALU 0 /* int & f32 add/sub/mul/mad, logic, shifts, cvt, mov, setp, selp, ld.param */
+#define KS_LAT_FMA 1 /* fma.rn.f32 */
+#define KS_LAT_LDG 2 /* ld.global */
+#define KS_LAT_STG 3 /* st.global */
+#define KS_LAT_BRA 4 /* bra */
+#define KS_LAT_SFU 5 /* div.rn.f32, sqrt.rn.f32 */
+#define KS_LAT_RET 6 /* ret, exit */
+/* class 7 is reserved */
+
+#define KS_MAX_BUFFERS 8
+#define KS_MAX_PARAM_BYTES 256
+#define KS_MAX_STACK 32
+
+typedef struct ks_module ks_module; /* opaque; owned by the library */
+
+/* A simulated global buffer: the caller picks sim_base (4 KiB aligned,
+ * buffers non-overlapping); simulated pointers passed in the kernel
+ * parameters are sim_base-relative virtual addresses. dev_ptr is caller-owned
+ * device memory of `bytes` bytes that the simulated loads read and the
+ * simulated stores write. */
+typedef struct {
+  uint64_t sim_base;
+  void* dev_ptr;
+  uint64_t bytes;
+} ks_buffer;
+
+typedef struct {
+  uint32_t lat[KS_NUM_LAT_CLASSES]; /* cycles per latency class */
+  uint32_t max_ts_per_warp;         /* trace records per warp slot */
+  uint32_t simt_stack_depth;        /* 1..32 entries, base entry included */
+  uint64_t step_limit;              /* max issued instructions per warp */
+  int64_t inject_warp;              /* debug: global warp id that posts KS_ST_INJECTED; -1 off */
+  uint64_t inject_step;             /* ...when its issued-instruction count reaches this */
+  uint32_t flags;                   /* reserved, 0 */
+  uint32_t reserved;
+} ks_config;
+
+/* Per-warp statistics record (96 bytes), indexed by global warp id
+ * (ctaid * ceil(block/32) + warp index in the CTA). */
+typedef struct {
+  uint64_t cycles;
+  uint64_t warp_insts;   /* issued instructions */
+  uint64_t thread_insts; /* sum over issued instructions of the active lanes */
+  uint64_t ld_req;
+  uint64_t ld_sectors;
+  uint64_t st_req;
+  uint64_t st_sectors;
+  uint64_t ld_lines;
+  uint64_t st_lines;
+  int32_t status;           /* 0 or a KS_ST_* code */
+  uint32_t max_stack_depth; /* deepest reconvergence stack reached */
+  uint64_t reserved[2];     /* written as 0 */
+} ks_warp_stats;
+
+/* Launch totals reduced over every warp record. */
+typedef struct {
+  uint64_t cycles_max;
+  uint64_t cycles_sum;
+  uint64_t warp_insts;
+  uint64_t thread_insts;
+  uint64_t ld_req;
+  uint64_t ld_sectors;
+  uint64_t st_req;
+  uint64_t st_sectors;
+  uint64_t ld_lines;
+  uint64_t st_lines;
+  uint64_t n_warps;
+  uint64_t n_failed;          /* warps with a nonzero status */
+  int64_t first_failed_warp;  /* lowest failing warp id, -1 if none */
+  int32_t status;             /* status of first_failed_warp, 0 if none */
+  uint32_t max_stack_depth;
+} ks_totals;
+
+/* Fills the defaults: lat = {4, 4, 400, 20, 8, 36, 1, 0}, max_ts 0,
+ * stack depth 32, step limit 2^26, injection off. */
+void ks_config_default(ks_config* cfg);
+
+/* Parses and decodes a PTX module (host only; no GPU work). `len` bytes of
+ * `ptx` (need not be NUL-terminated). On success *out owns the module; free
+ * it with ks_free_module. On failure returns KS_ERR_PARSE /
+ * KS_ERR_UNSUPPORTED / KS_ERR_LIMIT / KS_ERR_ARG with a message in err
+ * (NUL-terminated, truncated to errlen). */
+int ks_load_module(const char* ptx, size_t len, ks_module** out, char* err, size_t errlen);
+
+/* Frees the module and the device copies of its programs (which are created
+ * lazily, once per device, by the first ks_simulate on that device). */
+void ks_free_module(ks_module* mod);
+
+/* Kernel introspection. Any output pointer may be NULL. */
+int ks_kernel_info(const ks_module* mod, const char* kernel, uint32_t* n_params,
+                   uint32_t* param_bytes, uint32_t* n_events, uint32_t* n_insns,
+                   uint32_t* n_reg_slots);
+/* Parameter `index` in declaration order: byte offset in the parameter block
+ * (natural alignment), size in bytes, name (owned by the module). */
+int ks_kernel_param(const ks_module* mod, const char* kernel, uint32_t index,
+                    uint32_t* offset, uint32_t* size, const char** name);
+/* Event `id`: kind 0 mark, 1 range_start, 2 range_end; ids number the
+ * distinct (kind, name) pairs in order of first appearance. */
+int ks_kernel_event(const ks_module* mod, const char* kernel, uint32_t id, uint32_t* kind,
+                    const char** name);
+/* Reconvergence point (immediate post-dominator) of every program entry
+ * (instructions and pseudo-ops in order); the virtual exit is *n_out. */
+int ks_kernel_ipdom(const ks_module* mod, const char* kernel, int32_t* out, uint32_t cap,
+                    uint32_t* n_out);
+
+/* Sizes of the caller-owned output buffers:
+ * trace = W * align8(16 + 4 * max_ts_per_warp), stats = W * 96, where
+ * W = grid * ceil(block / 32). */
+size_t ks_trace_bytes(uint32_t grid, uint32_t block, uint32_t max_ts_per_warp);
+size_t ks_stats_bytes(uint32_t grid, uint32_t block);
+
+/* Enqueues the interpretation of `kernel` over grid x block simulated
+ * threads on `stream` (a cudaStream_t; NULL = the legacy default stream) of
+ * the current device, and returns without waiting.
+ *   params      host pointer to the kernel's parameter block (layout from
+ *               ks_kernel_param), param_bytes >= the kernel's block size,
+ *               at most KS_MAX_PARAM_BYTES; copied at launch.
+ *   bufs        host array of n_bufs <= 8 buffer descriptors (device memory).
+ *   trace_buf   device buffer of trace_bytes >= ks_trace_bytes(...), or NULL
+ *               (then no trace is written). Every byte of every slot is
+ *               written (unused records as zero).
+ *   stats_buf   device buffer of stats_bytes >= ks_stats_bytes(...); every
+ *               record is written.
+ *   cfg         host pointer; NULL = defaults.
+ * Simulated faults do not fail the call: they are reported per warp in the
+ * stats records (read them with ks_read_stats). Host-side errors: KS_ERR_ARG
+ * (shapes, sizes, buffer table, undersized outputs), KS_ERR_NOT_FOUND,
+ * KS_ERR_LIMIT (shared memory), KS_ERR_CUDA. The first call on a device
+ * uploads the module's program there (one allocation per module per device).
+ * Simulations that share output or store-target buffers must not overlap in
+ * time. */
+int ks_simulate(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block,
+                const void* params, size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs,
+                void* trace_buf, size_t trace_bytes, void* stats_buf, size_t stats_bytes,
+                const ks_config* cfg, void* stream);
+
+/* Reduces n_warps stats records (device pointer) on `stream`, waits for the
+ * stream, and writes the totals to *out (host). Uses a small device
+ * accumulator that the library allocates once per device; calls are
+ * serialised inside the library. */
+int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_totals* out);
+
+/* Text for any KS_* return code or status. */
+const char* ks_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KS_H */

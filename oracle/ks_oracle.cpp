@@ -1145,6 +1145,7 @@ void run_warp(const Launch& X, Memory& M, uint32_t gwarp) {
   while (!stack.empty()) {
     Entry& top = stack.back();
     if (top.pc == top.rpc || top.mask == 0) { stack.pop_back(); continue; }
+    if (top.pc >= n) { top.mask = 0; continue; }  // virtual exit: remaining lanes finish
     const int pc = top.pc;
     const Inst& in = K.code[(size_t)pc];
 

@@ -1,0 +1,74 @@
+"""ctypes declarations of libks (include/ks.h). Loading fails loudly: there is
+no fallback path."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libks.so")
+
+
+class KsBuffer(ctypes.Structure):
+    _fields_ = [("sim_base", ctypes.c_uint64), ("dev_ptr", ctypes.c_void_p), ("bytes", ctypes.c_uint64)]
+
+
+class KsConfig(ctypes.Structure):
+    _fields_ = [
+        ("lat", ctypes.c_uint32 * 8),
+        ("max_ts_per_warp", ctypes.c_uint32),
+        ("simt_stack_depth", ctypes.c_uint32),
+        ("step_limit", ctypes.c_uint64),
+        ("inject_warp", ctypes.c_int64),
+        ("inject_step", ctypes.c_uint64),
+        ("flags", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
+    ]
+
+
+class KsTotals(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "cycles_max", "cycles_sum", "warp_insts", "thread_insts", "ld_req", "ld_sectors", "st_req",
+        "st_sectors", "ld_lines", "st_lines", "n_warps", "n_failed")] + [
+        ("first_failed_warp", ctypes.c_int64), ("status", ctypes.c_int32), ("max_stack_depth", ctypes.c_uint32)]
+
+
+EXPORTS = {
+    "ks_config_default": (None, [ctypes.POINTER(KsConfig)]),
+    "ks_load_module": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p),
+                                      ctypes.c_char_p, ctypes.c_size_t]),
+    "ks_free_module": (None, [ctypes.c_void_p]),
+    "ks_kernel_info": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p] + [ctypes.POINTER(ctypes.c_uint32)] * 5),
+    "ks_kernel_param": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32,
+                                       ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32),
+                                       ctypes.POINTER(ctypes.c_char_p)]),
+    "ks_kernel_event": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32,
+                                       ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_char_p)]),
+    "ks_kernel_ipdom": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
+    "ks_trace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]),
+    "ks_stats_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32]),
+    "ks_simulate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
+                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(KsBuffer), ctypes.c_uint32,
+                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,
+                                   ctypes.POINTER(KsConfig), ctypes.c_void_p]),
+    "ks_read_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.POINTER(KsTotals)]),
+    "ks_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libks; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib

@@ -1,0 +1,198 @@
+"""Python face of libks: argument marshalling around the C ABI only.
+
+Device memory and streams come from PyTorch; every step of the simulation
+runs in the library's sm_103a kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import _native
+
+STATS_DTYPE = np.dtype(
+    [("cycles", "<u8"), ("warp_insts", "<u8"), ("thread_insts", "<u8"), ("ld_req", "<u8"),
+     ("ld_sectors", "<u8"), ("st_req", "<u8"), ("st_sectors", "<u8"), ("ld_lines", "<u8"),
+     ("st_lines", "<u8"), ("status", "<i4"), ("max_stack_depth", "<u4"), ("reserved", "<u8", (2,))])
+DEFAULT_LAT = (4, 4, 400, 20, 8, 36, 1, 0)
+
+ST_OOB, ST_MISALIGNED, ST_STEP_LIMIT, ST_SIMT_STACK, ST_TIMEOUT, ST_INJECTED = 1, 2, 3, 4, 5, 6
+
+
+class KsError(RuntimeError):
+    def __init__(self, code: int, msg: str = ""):
+        text = _native.lib().ks_status_string(code).decode()
+        super().__init__(f"libks error {code} ({text}){': ' + msg if msg else ''}")
+        self.code = code
+
+
+def _check(rc: int, msg: str = ""):
+    if rc != 0:
+        raise KsError(rc, msg)
+
+
+@dataclass
+class Config:
+    lat: tuple = DEFAULT_LAT
+    max_ts: int = 0
+    stack_depth: int = 32
+    step_limit: int = 1 << 26
+    inject_warp: int = -1
+    inject_step: int = 0
+
+    def to_c(self) -> _native.KsConfig:
+        c = _native.KsConfig()
+        _native.lib().ks_config_default(ctypes.byref(c))
+        for i in range(8):
+            c.lat[i] = self.lat[i] if i < len(self.lat) else 0
+        c.max_ts_per_warp = self.max_ts
+        c.simt_stack_depth = self.stack_depth
+        c.step_limit = self.step_limit
+        c.inject_warp = self.inject_warp
+        c.inject_step = self.inject_step
+        return c
+
+
+@dataclass
+class Totals:
+    cycles_max: int
+    cycles_sum: int
+    warp_insts: int
+    thread_insts: int
+    ld_req: int
+    ld_sectors: int
+    st_req: int
+    st_sectors: int
+    ld_lines: int
+    st_lines: int
+    n_warps: int
+    n_failed: int
+    first_failed_warp: int
+    status: int
+    max_stack_depth: int
+
+
+class Module:
+    """A decoded PTX module (ks_load_module)."""
+
+    def __init__(self, ptx: str):
+        L = _native.lib()
+        self._h = ctypes.c_void_p()
+        err = ctypes.create_string_buffer(1024)
+        data = ptx.encode()
+        rc = L.ks_load_module(data, len(data), ctypes.byref(self._h), err, len(err))
+        _check(rc, err.value.decode(errors="replace"))
+
+    def close(self):
+        if self._h:
+            _native.lib().ks_free_module(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self, kernel: str) -> dict:
+        v = [ctypes.c_uint32() for _ in range(5)]
+        _check(_native.lib().ks_kernel_info(self._h, kernel.encode(), *[ctypes.byref(x) for x in v]))
+        return dict(zip(("n_params", "param_bytes", "n_events", "n_insns", "n_reg_slots"), (x.value for x in v)))
+
+    def params(self, kernel: str) -> list[tuple[str, int, int]]:
+        out = []
+        for i in range(self.info(kernel)["n_params"]):
+            off, size, name = ctypes.c_uint32(), ctypes.c_uint32(), ctypes.c_char_p()
+            _check(_native.lib().ks_kernel_param(self._h, kernel.encode(), i, ctypes.byref(off), ctypes.byref(size),
+                                                 ctypes.byref(name)))
+            out.append((name.value.decode(), off.value, size.value))
+        return out
+
+    def events(self, kernel: str) -> list[tuple[int, str]]:
+        out = []
+        for i in range(self.info(kernel)["n_events"]):
+            kind, name = ctypes.c_uint32(), ctypes.c_char_p()
+            _check(_native.lib().ks_kernel_event(self._h, kernel.encode(), i, ctypes.byref(kind), ctypes.byref(name)))
+            out.append((kind.value, name.value.decode()))
+        return out
+
+    def ipdom(self, kernel: str) -> list[int]:
+        n = self.info(kernel)["n_insns"]
+        arr = (ctypes.c_int32 * max(1, n))()
+        cnt = ctypes.c_uint32()
+        _check(_native.lib().ks_kernel_ipdom(self._h, kernel.encode(), arr, n, ctypes.byref(cnt)))
+        return [arr[i] for i in range(cnt.value)]
+
+
+def stats_bytes(grid: int, block: int) -> int:
+    return int(_native.lib().ks_stats_bytes(grid, block))
+
+
+def trace_bytes(grid: int, block: int, max_ts: int) -> int:
+    return int(_native.lib().ks_trace_bytes(grid, block, max_ts))
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def simulate(module: Module, kernel: str, grid: int, block: int, params: bytes, buffers, stats: torch.Tensor,
+             trace: torch.Tensor | None = None, config: Config | None = None, stream=None) -> None:
+    """Enqueues one simulation (ks_simulate). buffers: [(sim_base, cuda tensor)];
+    stats / trace: uint8 cuda tensors of stats_bytes / trace_bytes."""
+    bufs = (_native.KsBuffer * max(1, len(buffers)))()
+    for i, (base, t) in enumerate(buffers):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("buffers must be contiguous CUDA tensors")
+        bufs[i].sim_base = base
+        bufs[i].dev_ptr = t.data_ptr()
+        bufs[i].bytes = t.numel() * t.element_size()
+    cfg = (config or Config()).to_c()
+    pbuf = ctypes.create_string_buffer(bytes(params), max(1, len(params)))
+    rc = _native.lib().ks_simulate(
+        module.handle, kernel.encode(), grid, block, ctypes.cast(pbuf, ctypes.c_void_p), len(params), bufs,
+        len(buffers), trace.data_ptr() if trace is not None else None,
+        trace.numel() if trace is not None else 0, stats.data_ptr(), stats.numel(), ctypes.byref(cfg),
+        _stream_handle(stream))
+    _check(rc)
+
+
+def read_stats(stats: torch.Tensor, n_warps: int, stream=None) -> Totals:
+    """Launch totals (ks_read_stats); waits for the stream."""
+    t = _native.KsTotals()
+    _check(_native.lib().ks_read_stats(stats.data_ptr(), n_warps, _stream_handle(stream), ctypes.byref(t)))
+    return Totals(**{f: getattr(t, f) for f, _ in _native.KsTotals._fields_})
+
+
+def stats_array(stats: torch.Tensor) -> np.ndarray:
+    """Per-warp records as a numpy structured array (copies to the host)."""
+    return stats.cpu().numpy().view(STATS_DTYPE)
+
+
+@dataclass
+class Run:
+    stats: torch.Tensor
+    trace: torch.Tensor | None
+    totals: Totals
+    buffers: list = field(default_factory=list)
+
+
+def run(module: Module, kernel: str, grid: int, block: int, params: bytes, buffers, config: Config | None = None,
+        trace: bool = False, stream=None) -> Run:
+    """Allocates the outputs, simulates, and reduces the totals."""
+    config = config or Config()
+    dev = buffers[0][1].device if buffers else torch.device("cuda")
+    st = torch.empty(stats_bytes(grid, block), dtype=torch.uint8, device=dev)
+    tr = torch.empty(trace_bytes(grid, block, config.max_ts), dtype=torch.uint8, device=dev) if trace else None
+    simulate(module, kernel, grid, block, params, buffers, st, tr, config, stream)
+    n = grid * ((block + 31) // 32)
+    return Run(st, tr, read_stats(st, n, stream), list(buffers))

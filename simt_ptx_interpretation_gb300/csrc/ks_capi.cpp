@@ -1,0 +1,338 @@
+// ks_capi.cpp — the extern "C" boundary of libks (declared in include/ks.h).
+//
+// Host work only: argument checks, the module registry, one lazy upload of
+// each kernel's program image per device, the real launch shape, and the
+// stats-reduction call. Every step of the simulation itself runs in
+// ks_interp.cu on the GPU.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "ks_internal.h"
+
+struct ks_module {
+  std::vector<ks::KsKernel> kernels;
+  std::mutex mu;
+  std::map<std::pair<size_t, int>, void*> images;  // (kernel index, device) -> device copy
+};
+
+namespace {
+
+void put_err(const std::string& m, char* err, size_t errlen) {
+  if (!err || errlen == 0) return;
+  size_t n = std::min(m.size(), errlen - 1);
+  std::memcpy(err, m.data(), n);
+  err[n] = 0;
+}
+
+const ks::KsKernel* find_kernel(const ks_module* mod, const char* name, size_t* index) {
+  if (!mod || !name) return nullptr;
+  for (size_t i = 0; i < mod->kernels.size(); i++)
+    if (mod->kernels[i].name == name) {
+      if (index) *index = i;
+      return &mod->kernels[i];
+    }
+  return nullptr;
+}
+
+struct DevInfo {
+  int sms = 0;
+  int max_smem = 0;
+};
+
+std::mutex g_dev_mu;
+std::map<int, DevInfo> g_dev;
+
+int device_info(DevInfo* out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KS_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) {
+    DevInfo d;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KS_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return KS_ERR_CUDA;
+    it = g_dev.emplace(dev, d).first;
+  }
+  *out = it->second;
+  *dev_out = dev;
+  return KS_OK;
+}
+
+// Device accumulator for ks_read_stats, one per device, allocated once.
+std::mutex g_acc_mu;
+std::map<int, void*> g_acc;
+constexpr size_t ACC_WORDS = 13;
+
+uint64_t warps_of(uint32_t grid, uint32_t block) { return (uint64_t)grid * ((block + 31u) / 32u); }
+
+}  // namespace
+
+extern "C" {
+
+void ks_config_default(ks_config* cfg) {
+  if (!cfg) return;
+  std::memset(cfg, 0, sizeof *cfg);
+  const uint32_t lat[KS_NUM_LAT_CLASSES] = {4, 4, 400, 20, 8, 36, 1, 0};
+  std::memcpy(cfg->lat, lat, sizeof lat);
+  cfg->max_ts_per_warp = 0;
+  cfg->simt_stack_depth = 32;
+  cfg->step_limit = 1ull << 26;
+  cfg->inject_warp = -1;
+  cfg->inject_step = 0;
+}
+
+int ks_load_module(const char* ptx, size_t len, ks_module** out, char* err, size_t errlen) {
+  if (!ptx || !out) {
+    put_err("null argument", err, errlen);
+    return KS_ERR_ARG;
+  }
+  *out = nullptr;
+  std::vector<ks::KsKernel> ks;
+  std::string msg;
+  int rc = ks::decode_module(ptx, len, &ks, &msg);
+  if (rc != KS_OK) {
+    put_err(msg, err, errlen);
+    return rc;
+  }
+  ks_module* m = new ks_module;
+  m->kernels = std::move(ks);
+  *out = m;
+  put_err("", err, errlen);
+  return KS_OK;
+}
+
+void ks_free_module(ks_module* mod) {
+  if (!mod) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  for (auto& kv : mod->images) {
+    cudaSetDevice(kv.first.second);
+    cudaFree(kv.second);
+  }
+  if (cur >= 0 && !mod->images.empty()) cudaSetDevice(cur);
+  delete mod;
+}
+
+int ks_kernel_info(const ks_module* mod, const char* kernel, uint32_t* n_params, uint32_t* param_bytes,
+                   uint32_t* n_events, uint32_t* n_insns, uint32_t* n_reg_slots) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  if (n_params) *n_params = (uint32_t)k->params.size();
+  if (param_bytes) *param_bytes = k->param_bytes;
+  if (n_events) *n_events = (uint32_t)k->events.size();
+  if (n_insns) *n_insns = (uint32_t)k->code.size();
+  if (n_reg_slots) *n_reg_slots = k->n_slots;
+  return KS_OK;
+}
+
+int ks_kernel_param(const ks_module* mod, const char* kernel, uint32_t index, uint32_t* offset, uint32_t* size,
+                    const char** name) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  if (index >= k->params.size()) return KS_ERR_NOT_FOUND;
+  if (offset) *offset = k->params[index].offset;
+  if (size) *size = k->params[index].size;
+  if (name) *name = k->params[index].name.c_str();
+  return KS_OK;
+}
+
+int ks_kernel_event(const ks_module* mod, const char* kernel, uint32_t id, uint32_t* kind, const char** name) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  if (id >= k->events.size()) return KS_ERR_NOT_FOUND;
+  if (kind) *kind = k->events[id].kind;
+  if (name) *name = k->events[id].name.c_str();
+  return KS_OK;
+}
+
+int ks_kernel_ipdom(const ks_module* mod, const char* kernel, int32_t* out, uint32_t cap, uint32_t* n_out) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  if (n_out) *n_out = (uint32_t)k->ipdom.size();
+  if (out)
+    for (size_t i = 0; i < k->ipdom.size() && i < cap; i++) out[i] = k->ipdom[i];
+  return KS_OK;
+}
+
+size_t ks_trace_bytes(uint32_t grid, uint32_t block, uint32_t max_ts_per_warp) {
+  const uint64_t slot = (16ull + 4ull * max_ts_per_warp + 7ull) / 8ull * 8ull;
+  return (size_t)(warps_of(grid, block) * slot);
+}
+
+size_t ks_stats_bytes(uint32_t grid, uint32_t block) {
+  return (size_t)(warps_of(grid, block) * sizeof(ks_warp_stats));
+}
+
+int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t block, const void* params,
+                size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf, size_t trace_bytes,
+                void* stats_buf, size_t stats_bytes, const ks_config* cfg_in, void* stream) {
+  ks_module* mod = const_cast<ks_module*>(mod_c);
+  size_t kidx = 0;
+  const ks::KsKernel* k = find_kernel(mod, kernel, &kidx);
+  if (!mod || !kernel) return KS_ERR_ARG;
+  if (!k) return KS_ERR_NOT_FOUND;
+  ks_config cfg;
+  if (cfg_in) cfg = *cfg_in; else ks_config_default(&cfg);
+
+  // ---- argument checks ----
+  if (grid == 0 || block == 0 || block > 1024) return KS_ERR_ARG;
+  const uint64_t W = warps_of(grid, block);
+  if (W >= (1ull << 31)) return KS_ERR_ARG;
+  if (param_bytes < k->param_bytes || param_bytes > KS_MAX_PARAM_BYTES) return KS_ERR_ARG;
+  if (k->param_bytes && !params) return KS_ERR_ARG;
+  if (n_bufs > KS_MAX_BUFFERS || (n_bufs && !bufs)) return KS_ERR_ARG;
+  for (uint32_t i = 0; i < n_bufs; i++) {
+    const ks_buffer& b = bufs[i];
+    if (b.sim_base % 4096 != 0 || b.bytes == 0 || !b.dev_ptr) return KS_ERR_ARG;
+    if (b.sim_base + b.bytes < b.sim_base) return KS_ERR_ARG;
+    for (uint32_t j = 0; j < i; j++) {
+      const ks_buffer& o = bufs[j];
+      if (!(b.sim_base + b.bytes <= o.sim_base || o.sim_base + o.bytes <= b.sim_base)) return KS_ERR_ARG;
+    }
+  }
+  if (!stats_buf || stats_bytes < W * sizeof(ks_warp_stats)) return KS_ERR_ARG;
+  if (cfg.simt_stack_depth == 0 || cfg.simt_stack_depth > KS_MAX_STACK) return KS_ERR_ARG;
+  if (cfg.max_ts_per_warp > (1u << 24)) return KS_ERR_ARG;
+  const uint64_t slot = (16ull + 4ull * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
+  if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
+
+  DevInfo di;
+  int dev = 0;
+  if (device_info(&di, &dev) != KS_OK) return KS_ERR_CUDA;
+
+  // ---- program image on this device (uploaded once) ----
+  void* image = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mod->mu);
+    auto key = std::make_pair(kidx, dev);
+    auto it = mod->images.find(key);
+    if (it == mod->images.end()) {
+      if (cudaMalloc(&image, k->image.size()) != cudaSuccess) return KS_ERR_CUDA;
+      if (cudaMemcpy(image, k->image.data(), k->image.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(image);
+        return KS_ERR_CUDA;
+      }
+      mod->images[key] = image;
+    } else {
+      image = it->second;
+    }
+  }
+
+  // ---- launch block ----
+  ks::KsLaunch L;
+  std::memset(&L, 0, sizeof L);
+  L.image = static_cast<const uint8_t*>(image);
+  L.image_bytes = (uint32_t)k->image.size();
+  L.n_insn = (uint32_t)k->code.size();
+  L.n_slots = k->n_slots;
+  L.grid = grid;
+  L.block = block;
+  L.wpc = (block + 31u) / 32u;
+  L.n_warps = (uint32_t)W;
+  std::memcpy(L.lat, cfg.lat, sizeof L.lat);
+  L.max_ts = cfg.max_ts_per_warp;
+  L.stack_depth = cfg.simt_stack_depth;
+  L.step_limit = cfg.step_limit;
+  L.inject_warp = cfg.inject_warp;
+  L.inject_step = cfg.inject_step;
+  L.n_bufs = n_bufs;
+  for (uint32_t i = 0; i < n_bufs; i++) {
+    L.bufs[i].sim_base = bufs[i].sim_base;
+    L.bufs[i].bytes = bufs[i].bytes;
+    L.bufs[i].ptr = static_cast<uint8_t*>(bufs[i].dev_ptr);
+  }
+  L.trace = static_cast<uint8_t*>(trace_buf);
+  L.slot_bytes = slot;
+  L.stats = static_cast<uint8_t*>(stats_buf);
+  L.param_bytes = (uint32_t)param_bytes;
+  if (param_bytes) std::memcpy(L.params, params, param_bytes);
+
+  // ---- real launch shape: as many real warps as simulated warps, up to the
+  // resident capacity; CTAs small enough that every SM gets work ----
+  uint32_t wpc_real = 8;
+  while (wpc_real > 1 && (W + wpc_real - 1) / wpc_real < 2ull * (uint64_t)di.sms) wpc_real /= 2;
+  while (wpc_real > 1 && ks::interp_smem_bytes(L.image_bytes, L.n_slots, wpc_real) > (size_t)di.max_smem)
+    wpc_real /= 2;
+  const size_t smem = ks::interp_smem_bytes(L.image_bytes, L.n_slots, wpc_real);
+  if (smem > (size_t)di.max_smem) return KS_ERR_LIMIT;
+  int per_sm = 0;
+  if (ks::interp_occupancy(wpc_real, smem, &per_sm) != 0) return KS_ERR_CUDA;
+  if (per_sm < 1) return KS_ERR_LIMIT;
+  const uint64_t want = (W + wpc_real - 1) / wpc_real;
+  const uint64_t cap = (uint64_t)di.sms * (uint64_t)per_sm;
+  const uint32_t ctas = (uint32_t)std::min(want, cap);
+  if (ks::launch_interp(L, wpc_real, ctas, stream) != 0) return KS_ERR_CUDA;
+  return KS_OK;
+}
+
+int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_totals* out) {
+  if (!stats_buf || !out || n_warps == 0) return KS_ERR_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KS_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_acc_mu);
+  void*& acc = g_acc[dev];
+  if (!acc && cudaMalloc(&acc, ACC_WORDS * sizeof(uint64_t)) != cudaSuccess) {
+    acc = nullptr;
+    return KS_ERR_CUDA;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(acc, 0, ACC_WORDS * sizeof(uint64_t), s) != cudaSuccess) return KS_ERR_CUDA;
+  if (ks::launch_reduce_stats(stats_buf, n_warps, acc, stream) != 0) return KS_ERR_CUDA;
+  uint64_t h[ACC_WORDS];
+  if (cudaMemcpyAsync(h, acc, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return KS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KS_ERR_CUDA;
+  std::memset(out, 0, sizeof *out);
+  out->cycles_max = h[0];
+  out->cycles_sum = h[1];
+  out->warp_insts = h[2];
+  out->thread_insts = h[3];
+  out->ld_req = h[4];
+  out->ld_sectors = h[5];
+  out->st_req = h[6];
+  out->st_sectors = h[7];
+  out->ld_lines = h[8];
+  out->st_lines = h[9];
+  out->n_warps = n_warps;
+  out->n_failed = h[10];
+  out->max_stack_depth = (uint32_t)h[12];
+  out->first_failed_warp = -1;
+  out->status = 0;
+  if (h[10]) {
+    const uint64_t w = ~0ull - h[11];
+    out->first_failed_warp = (int64_t)w;
+    int32_t st = 0;
+    const char* p = static_cast<const char*>(stats_buf) + w * sizeof(ks_warp_stats) + offsetof(ks_warp_stats, status);
+    if (cudaMemcpyAsync(&st, p, sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess) return KS_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KS_ERR_CUDA;
+    out->status = st;
+  }
+  return KS_OK;
+}
+
+const char* ks_status_string(int code) {
+  switch (code) {
+    case KS_OK: return "ok";
+    case KS_ERR_PARSE: return "malformed PTX";
+    case KS_ERR_UNSUPPORTED: return "PTX outside the supported subset";
+    case KS_ERR_ARG: return "bad argument";
+    case KS_ERR_CUDA: return "CUDA runtime error";
+    case KS_ERR_NOT_FOUND: return "not found";
+    case KS_ERR_LIMIT: return "program or register file too large";
+    case KS_ST_OOB: return "simulated address outside every buffer";
+    case KS_ST_MISALIGNED: return "simulated address not aligned to the access size";
+    case KS_ST_STEP_LIMIT: return "warp exceeded the step limit";
+    case KS_ST_SIMT_STACK: return "reconvergence stack overflow";
+    case KS_ST_TIMEOUT: return "bounded wait ran out";
+    case KS_ST_INJECTED: return "injected fault";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

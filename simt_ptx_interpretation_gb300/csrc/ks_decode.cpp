@@ -1,0 +1,992 @@
+// ks_decode.cpp — host PTX-subset lexer, parser and decoder.
+//
+// Lowers the supported subset (KernelScope backend doc, "PTX Parser":
+// directives, .entry/.param/.reg, instructions with an optional @%p / @!%p
+// guard, opcode, modifier chain and operands) into the packed 32-byte KsInsn
+// array the sm_103a interpreter executes, and computes each branch's
+// reconvergence pc as its immediate post-dominator (Cooper, Harvey and
+// Kennedy's iterative dominator algorithm run on the reversed CFG).
+//
+// Register allocation: a 32-bit register takes one 32-bit slot of the
+// interpreter's shared-memory register file, a 64-bit register two
+// consecutive slots; slots and predicate indices are assigned in order of
+// first use. Immediates go to a per-kernel constant pool.
+#include <algorithm>
+#include <cctype>
+#include <cstring>
+#include <map>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "ks_internal.h"
+
+namespace ks {
+namespace {
+
+struct Fail {
+  int code;
+  std::string msg;
+};
+
+[[noreturn]] void fail(int code, int line, const std::string& m) {
+  throw Fail{code, "line " + std::to_string(line) + ": " + m};
+}
+
+// ------------------------------------------------------------------ lexer --
+
+enum TokKind { TK_NAME, TK_NUM, TK_PUNCT, TK_PSEUDO, TK_EOF };
+
+struct Tok {
+  TokKind kind;
+  std::string text;
+  int line;
+};
+
+bool name_start(unsigned char c) { return std::isalpha(c) || c == '_' || c == '$' || c == '%' || c == '.'; }
+bool name_char(unsigned char c) { return std::isalnum(c) || c == '_' || c == '$' || c == '.'; }
+
+std::vector<Tok> lex(const char* p, size_t n) {
+  std::vector<Tok> out;
+  int line = 1;
+  size_t i = 0;
+  while (i < n) {
+    unsigned char c = (unsigned char)p[i];
+    if (c == '\n') { line++; i++; continue; }
+    if (std::isspace(c)) { i++; continue; }
+    if (c == '/' && i + 1 < n && p[i + 1] == '*') {
+      size_t j = i + 2;
+      while (j + 1 < n && !(p[j] == '*' && p[j + 1] == '/')) { if (p[j] == '\n') line++; j++; }
+      if (j + 1 >= n) fail(KS_ERR_PARSE, line, "unterminated block comment");
+      i = j + 2;
+      continue;
+    }
+    if (c == '/' && i + 1 < n && p[i + 1] == '/') {
+      size_t j = i + 2;
+      while (j < n && p[j] != '\n') j++;
+      std::string body(p + i + 2, j - i - 2);
+      size_t a = 0;
+      while (a < body.size() && std::isspace((unsigned char)body[a])) a++;
+      if (body.compare(a, 5, "@iket") == 0) out.push_back({TK_PSEUDO, body.substr(a + 5), line});
+      i = j;
+      continue;
+    }
+    if (std::isdigit(c)) {
+      size_t j = i;
+      while (j < n && (std::isalnum((unsigned char)p[j]) || p[j] == '.' || p[j] == '_')) j++;
+      out.push_back({TK_NUM, std::string(p + i, j - i), line});
+      i = j;
+      continue;
+    }
+    if (name_start(c)) {
+      size_t j = i + 1;
+      while (j < n && name_char((unsigned char)p[j])) j++;
+      out.push_back({TK_NAME, std::string(p + i, j - i), line});
+      i = j;
+      continue;
+    }
+    if (std::strchr(",;:[](){}+-<>@!", (int)c)) {
+      out.push_back({TK_PUNCT, std::string(1, (char)c), line});
+      i++;
+      continue;
+    }
+    fail(KS_ERR_PARSE, line, std::string("unexpected character '") + (char)c + "'");
+  }
+  out.push_back({TK_EOF, "", line});
+  return out;
+}
+
+// ------------------------------------------------------------- literals ----
+
+struct Lit {
+  bool neg = false;
+  uint64_t mag = 0;
+  bool is_f32 = false;  // 0fXXXXXXXX
+};
+
+bool hexval(char ch, unsigned* v) {
+  if (ch >= '0' && ch <= '9') { *v = (unsigned)(ch - '0'); return true; }
+  if (ch >= 'a' && ch <= 'f') { *v = (unsigned)(ch - 'a' + 10); return true; }
+  if (ch >= 'A' && ch <= 'F') { *v = (unsigned)(ch - 'A' + 10); return true; }
+  return false;
+}
+
+bool parse_number(const std::string& s, Lit* out) {
+  if (s.size() == 10 && s[0] == '0' && (s[1] == 'f' || s[1] == 'F')) {
+    uint64_t v = 0;
+    for (size_t i = 2; i < 10; i++) {
+      unsigned d;
+      if (!hexval(s[i], &d)) return false;
+      v = (v << 4) | d;
+    }
+    out->mag = v;
+    out->is_f32 = true;
+    return true;
+  }
+  std::string t = s;
+  if (!t.empty() && (t.back() == 'U' || t.back() == 'u')) t.pop_back();
+  if (t.empty()) return false;
+  uint64_t v = 0;
+  if (t.size() > 2 && t[0] == '0' && (t[1] == 'x' || t[1] == 'X')) {
+    if (t.size() > 18) return false;
+    for (size_t i = 2; i < t.size(); i++) {
+      unsigned d;
+      if (!hexval(t[i], &d)) return false;
+      v = (v << 4) | d;
+    }
+  } else {
+    for (char ch : t) {
+      if (ch < '0' || ch > '9') return false;
+      uint64_t d = (uint64_t)(ch - '0');
+      if (v > (~0ull - d) / 10) return false;
+      v = v * 10 + d;
+    }
+  }
+  out->mag = v;
+  return true;
+}
+
+bool is_ident(const std::string& s) {
+  if (s.empty()) return false;
+  unsigned char c0 = (unsigned char)s[0];
+  if (!(std::isalpha(c0) || c0 == '_' || c0 == '$')) return false;
+  for (unsigned char c : s)
+    if (!(std::isalnum(c) || c == '_' || c == '$')) return false;
+  return true;
+}
+
+// --------------------------------------------------------------- types ----
+
+enum PType { PT_BAD, PT_U32, PT_S32, PT_B32, PT_F32, PT_U64, PT_S64, PT_B64, PT_PRED };
+
+PType ptype(const std::string& s) {
+  static const std::map<std::string, PType> m = {
+      {"u32", PT_U32}, {"s32", PT_S32}, {"b32", PT_B32}, {"f32", PT_F32},
+      {"u64", PT_U64}, {"s64", PT_S64}, {"b64", PT_B64}, {"pred", PT_PRED}};
+  auto it = m.find(s);
+  return it == m.end() ? PT_BAD : it->second;
+}
+unsigned bits(PType t) {
+  switch (t) {
+    case PT_U32: case PT_S32: case PT_B32: case PT_F32: return 32;
+    case PT_U64: case PT_S64: case PT_B64: return 64;
+    case PT_PRED: return 1;
+    default: return 0;
+  }
+}
+bool integer(PType t) { return t == PT_U32 || t == PT_S32 || t == PT_U64 || t == PT_S64; }
+bool is_signed(PType t) { return t == PT_S32 || t == PT_S64; }
+
+// ------------------------------------------------------------ operands ----
+
+struct Operand {
+  enum Kind { NONE, REG, LIT, SPECIAL, MEM, PARAM, LABEL } kind = NONE;
+  std::string name;  // register / label / param / base register
+  Lit lit;           // LIT
+  int special = 0;
+  int64_t offset = 0;
+};
+
+struct RegDecl {
+  unsigned width;   // 32, 64 or 1 (predicate)
+  int index = -1;   // slot (first slot for 64-bit) or predicate index, -1 until used
+};
+
+// A statement of the kernel body after parsing.
+struct Stmt {
+  int line;
+  bool pseudo = false;
+  std::string pseudo_kind, pseudo_name;
+  std::string guard;  // predicate register name, empty if none
+  bool guard_neg = false;
+  std::string opcode;                 // base opcode
+  std::vector<std::string> mods;      // modifiers after the base
+  std::vector<Operand> ops;
+};
+
+struct KernelText {
+  std::string name;
+  int line;
+  std::vector<std::pair<std::string, PType>> params;
+  std::map<std::string, RegDecl> regs;
+  std::vector<Stmt> body;
+  std::map<std::string, size_t> labels;  // label -> index into body
+};
+
+// --------------------------------------------------------------- parser ----
+
+class Parser {
+ public:
+  explicit Parser(std::vector<Tok> t) : toks_(std::move(t)) {}
+
+  std::vector<KernelText> module() {
+    std::vector<KernelText> ks;
+    while (cur().kind != TK_EOF) {
+      const Tok& t = cur();
+      if (t.kind != TK_NAME) fail(KS_ERR_UNSUPPORTED, t.line, "unsupported top-level token '" + t.text + "'");
+      if (t.text == ".version" || t.text == ".target") {
+        skip_line();
+      } else if (t.text == ".loc" || t.text == ".file") {
+        skip_line();
+      } else if (t.text == ".address_size") {
+        int ln = t.line;
+        pos_++;
+        if (cur().kind != TK_NUM || cur().text != "64") fail(KS_ERR_UNSUPPORTED, ln, "only .address_size 64 is supported");
+        pos_++;
+      } else if (t.text == ".visible") {
+        pos_++;
+      } else if (t.text == ".entry") {
+        ks.push_back(entry());
+      } else {
+        fail(KS_ERR_UNSUPPORTED, t.line, "unsupported top-level statement " + t.text);
+      }
+    }
+    return ks;
+  }
+
+ private:
+  std::vector<Tok> toks_;
+  size_t pos_ = 0;
+
+  const Tok& cur() const { return toks_[pos_]; }
+  const Tok& peek(size_t k = 1) const { return toks_[std::min(pos_ + k, toks_.size() - 1)]; }
+  bool is(const char* punct) const { return cur().kind == TK_PUNCT && cur().text == punct; }
+  void expect(const char* punct) {
+    if (!is(punct)) fail(KS_ERR_PARSE, cur().line, std::string("expected '") + punct + "'");
+    pos_++;
+  }
+  std::string name() {
+    if (cur().kind != TK_NAME) fail(KS_ERR_PARSE, cur().line, "expected a name");
+    return toks_[pos_++].text;
+  }
+  void skip_line() {
+    int ln = cur().line;
+    while (cur().kind != TK_EOF && cur().line == ln) pos_++;
+  }
+
+  KernelText entry() {
+    KernelText k;
+    k.line = cur().line;
+    pos_++;  // .entry
+    k.name = name();
+    if (!is_ident(k.name)) fail(KS_ERR_PARSE, k.line, "bad kernel name");
+    expect("(");
+    std::set<std::string> seen;
+    if (!is(")")) {
+      while (true) {
+        int ln = cur().line;
+        if (cur().kind != TK_NAME || cur().text != ".param") fail(KS_ERR_UNSUPPORTED, ln, "unsupported parameter declaration");
+        pos_++;
+        std::string ty = name();
+        PType t = ty.size() > 1 && ty[0] == '.' ? ptype(ty.substr(1)) : PT_BAD;
+        if (t == PT_BAD || t == PT_PRED) fail(KS_ERR_UNSUPPORTED, ln, "unsupported parameter type " + ty);
+        std::string pn = name();
+        if (!is_ident(pn)) fail(KS_ERR_PARSE, ln, "bad parameter name");
+        if (!seen.insert(pn).second) fail(KS_ERR_PARSE, ln, "parameter declared twice");
+        k.params.push_back({pn, t});
+        if (is(",")) { pos_++; continue; }
+        if (!is(")")) fail(KS_ERR_UNSUPPORTED, ln, "unsupported parameter declaration");
+        break;
+      }
+    }
+    expect(")");
+    while (cur().kind != TK_EOF && !is("{")) pos_++;  // performance directives are ignored
+    expect("{");
+    std::vector<std::string> pending;
+    while (true) {
+      const Tok& t = cur();
+      if (t.kind == TK_EOF) fail(KS_ERR_PARSE, t.line, "missing '}'");
+      if (t.kind == TK_PUNCT && t.text == "}") { pos_++; break; }
+      if (t.kind == TK_PUNCT && t.text == "{") fail(KS_ERR_UNSUPPORTED, t.line, "nested blocks are not supported");
+      if (t.kind == TK_PSEUDO) {
+        Stmt s;
+        s.line = t.line;
+        s.pseudo = true;
+        std::vector<std::string> w;
+        std::string word;
+        for (char ch : t.text + " ") {
+          if (std::isspace((unsigned char)ch)) { if (!word.empty()) w.push_back(word); word.clear(); }
+          else word += ch;
+        }
+        if (w.size() != 2) fail(KS_ERR_PARSE, t.line, "bad //@iket pseudo-op");
+        s.pseudo_kind = w[0];
+        s.pseudo_name = w[1];
+        attach(k, pending, std::move(s));
+        pos_++;
+        continue;
+      }
+      if (t.kind == TK_NAME && (t.text == ".loc" || t.text == ".file")) { skip_line(); continue; }
+      if (t.kind == TK_NAME && t.text == ".reg") { reg_decl(k); continue; }
+      if (t.kind == TK_NAME && t.text[0] == '.') fail(KS_ERR_UNSUPPORTED, t.line, "unsupported directive in kernel body: " + t.text);
+      if (t.kind == TK_NAME && peek().kind == TK_PUNCT && peek().text == ":" && is_ident(t.text)) {
+        if (k.labels.count(t.text) || std::count(pending.begin(), pending.end(), t.text))
+          fail(KS_ERR_PARSE, t.line, "label defined twice: " + t.text);
+        pending.push_back(t.text);
+        pos_ += 2;
+        continue;
+      }
+      attach(k, pending, instruction());
+    }
+    if (!pending.empty()) fail(KS_ERR_PARSE, k.line, "label at the end of the kernel: " + pending[0]);
+    return k;
+  }
+
+  static void attach(KernelText& k, std::vector<std::string>& pending, Stmt s) {
+    for (const std::string& l : pending) k.labels[l] = k.body.size();
+    pending.clear();
+    k.body.push_back(std::move(s));
+  }
+
+  void reg_decl(KernelText& k) {
+    int ln = cur().line;
+    pos_++;
+    std::string ty = name();
+    PType t = ty.size() > 1 && ty[0] == '.' ? ptype(ty.substr(1)) : PT_BAD;
+    if (t == PT_BAD) fail(KS_ERR_UNSUPPORTED, ln, "unsupported register type " + ty);
+    while (true) {
+      std::string rn = name();
+      if (rn.size() < 2 || rn[0] != '%' || !is_ident(rn.substr(1))) fail(KS_ERR_PARSE, ln, "bad register name " + rn);
+      std::vector<std::string> names;
+      if (is("<")) {
+        pos_++;
+        Lit n;
+        if (cur().kind != TK_NUM || !parse_number(cur().text, &n) || n.is_f32 || n.mag == 0 || n.mag > 4096)
+          fail(KS_ERR_PARSE, ln, "bad register count");
+        pos_++;
+        expect(">");
+        for (uint64_t i = 0; i < n.mag; i++) names.push_back(rn + std::to_string(i));
+      } else {
+        names.push_back(rn);
+      }
+      for (const std::string& r : names) {
+        if (k.regs.count(r)) fail(KS_ERR_PARSE, ln, "register declared twice: " + r);
+        k.regs[r] = RegDecl{bits(t)};
+      }
+      if (is(",")) { pos_++; continue; }
+      break;
+    }
+    expect(";");
+  }
+
+  Stmt instruction() {
+    Stmt s;
+    s.line = cur().line;
+    if (is("@")) {
+      pos_++;
+      if (is("!")) { s.guard_neg = true; pos_++; }
+      s.guard = name();
+      if (s.guard[0] != '%') fail(KS_ERR_PARSE, s.line, "bad guard");
+    }
+    std::string op = name();
+    if (op[0] == '%' || op[0] == '.') fail(KS_ERR_PARSE, s.line, "expected an opcode");
+    size_t dot = op.find('.');
+    s.opcode = op.substr(0, dot);
+    while (dot != std::string::npos) {
+      size_t nd = op.find('.', dot + 1);
+      s.mods.push_back(op.substr(dot + 1, nd == std::string::npos ? std::string::npos : nd - dot - 1));
+      dot = nd;
+    }
+    if (!is(";")) {
+      while (true) {
+        s.ops.push_back(operand());
+        if (is(",")) { pos_++; continue; }
+        break;
+      }
+    }
+    expect(";");
+    return s;
+  }
+
+  Operand operand() {
+    Operand o;
+    int ln = cur().line;
+    if (is("[")) {
+      pos_++;
+      o.name = name();
+      o.kind = o.name[0] == '%' ? Operand::MEM : Operand::PARAM;
+      if (is("+") || is("-")) {
+        int sign = is("-") ? -1 : 1;
+        pos_++;
+        if (is("-")) { sign = -sign; pos_++; }
+        Lit l;
+        if (cur().kind != TK_NUM || !parse_number(cur().text, &l) || l.is_f32 || l.mag > 0x7FFFFFFFull)
+          fail(KS_ERR_PARSE, ln, "bad address offset");
+        pos_++;
+        o.offset = sign * (int64_t)l.mag;
+      }
+      expect("]");
+      return o;
+    }
+    if (is("-")) {
+      pos_++;
+      if (cur().kind != TK_NUM || !parse_number(cur().text, &o.lit) || o.lit.is_f32) fail(KS_ERR_PARSE, ln, "bad literal");
+      o.lit.neg = true;
+      o.kind = Operand::LIT;
+      pos_++;
+      return o;
+    }
+    if (cur().kind == TK_NUM) {
+      if (!parse_number(cur().text, &o.lit)) fail(KS_ERR_PARSE, ln, "bad literal " + cur().text);
+      o.kind = Operand::LIT;
+      pos_++;
+      return o;
+    }
+    std::string n = name();
+    if (n[0] == '%') {
+      static const std::map<std::string, int> sp = {
+          {"%tid.x", SP_TID}, {"%ntid.x", SP_NTID}, {"%ctaid.x", SP_CTAID}, {"%nctaid.x", SP_NCTAID},
+          {"%laneid", SP_LANEID}, {"%tid.y", SP_ZERO}, {"%tid.z", SP_ZERO}, {"%ctaid.y", SP_ZERO},
+          {"%ctaid.z", SP_ZERO}, {"%ntid.y", SP_ONE}, {"%ntid.z", SP_ONE}, {"%nctaid.y", SP_ONE},
+          {"%nctaid.z", SP_ONE}};
+      auto it = sp.find(n);
+      if (it != sp.end()) { o.kind = Operand::SPECIAL; o.special = it->second; return o; }
+      o.kind = Operand::REG;
+      o.name = n;
+      return o;
+    }
+    if (!is_ident(n)) fail(KS_ERR_PARSE, ln, "bad operand " + n);
+    o.kind = Operand::LABEL;
+    o.name = n;
+    return o;
+  }
+};
+
+// -------------------------------------------------------------- decoder ----
+
+class Decoder {
+ public:
+  Decoder(KernelText& t, KsKernel& k) : T(t), K(k) {}
+
+  void run() {
+    K.name = T.name;
+    uint32_t off = 0;
+    for (auto& p : T.params) {
+      uint32_t sz = bits(p.second) / 8;
+      off = (off + sz - 1) / sz * sz;
+      K.params.push_back({p.first, off, sz});
+      off += sz;
+    }
+    K.param_bytes = off;
+    if (T.body.empty()) fail(KS_ERR_PARSE, T.line, "empty kernel");
+    if (T.body.size() > KS_MAX_INSNS) fail(KS_ERR_LIMIT, T.line, "kernel longer than 2048 entries");
+    for (Stmt& s : T.body) K.code.push_back(s.pseudo ? event(s) : insn(s));
+    // branch targets
+    for (size_t i = 0; i < T.body.size(); i++) {
+      const Stmt& s = T.body[i];
+      if (s.pseudo || s.opcode != "bra") continue;
+      auto it = T.labels.find(s.ops[0].name);
+      if (it == T.labels.end()) fail(KS_ERR_PARSE, s.line, "undefined label " + s.ops[0].name);
+      K.code[i].target = (uint32_t)it->second;
+    }
+    const KsInsn& last = K.code.back();
+    if (!((last.op == OP_RET || last.op == OP_BRA) && last.guard == KS_NO_GUARD))
+      fail(KS_ERR_PARSE, T.body.back().line, "control can fall off the end of the kernel");
+    K.n_slots = next_slot_;
+    K.n_preds = next_pred_;
+    postdominators();
+    for (size_t i = 0; i < K.code.size(); i++)
+      if (K.code[i].op == OP_BRA) K.code[i].rpc = (uint32_t)K.ipdom[i];
+    build_image();
+  }
+
+ private:
+  KernelText& T;
+  KsKernel& K;
+  uint32_t next_slot_ = 0, next_pred_ = 0;
+  std::map<uint64_t, uint32_t> consts_;
+  std::map<std::pair<uint32_t, std::string>, uint32_t> event_ids_;
+
+  KsInsn blank() {
+    KsInsn in;
+    std::memset(&in, 0, sizeof in);
+    in.guard = KS_NO_GUARD;
+    in.hd = in.ha = in.hb = in.hc = in.hg = KS_HZ_NONE;
+    in.lat = KS_LAT_ALU;
+    return in;
+  }
+
+  KsInsn event(const Stmt& s) {
+    uint32_t kind;
+    if (s.pseudo_kind == "mark") kind = 0;
+    else if (s.pseudo_kind == "range_start") kind = 1;
+    else if (s.pseudo_kind == "range_end") kind = 2;
+    else fail(KS_ERR_PARSE, s.line, "unknown //@iket kind " + s.pseudo_kind);
+    if (!is_ident(s.pseudo_name)) fail(KS_ERR_PARSE, s.line, "bad event name");
+    auto key = std::make_pair(kind, s.pseudo_name);
+    auto it = event_ids_.find(key);
+    uint32_t id;
+    if (it == event_ids_.end()) {
+      id = (uint32_t)K.events.size();
+      if (id >= 256) fail(KS_ERR_UNSUPPORTED, s.line, "more than 256 events");
+      event_ids_[key] = id;
+      K.events.push_back({s.pseudo_name, kind});
+    } else {
+      id = it->second;
+    }
+    KsInsn in = blank();
+    in.op = OP_EVENT;
+    in.event = (uint16_t)id;
+    return in;
+  }
+
+  RegDecl& reg(const std::string& n, int line) {
+    auto it = T.regs.find(n);
+    if (it == T.regs.end()) fail(KS_ERR_PARSE, line, "undeclared register " + n);
+    RegDecl& r = it->second;
+    if (r.index < 0) {
+      if (r.width == 1) {
+        if (next_pred_ >= KS_MAX_PREDS) fail(KS_ERR_LIMIT, line, "more than 31 predicate registers in use");
+        r.index = (int)next_pred_++;
+      } else {
+        uint32_t need = r.width / 32;
+        if (next_slot_ + need > KS_MAX_SLOTS) fail(KS_ERR_LIMIT, line, "more than 96 register slots in use");
+        r.index = (int)next_slot_;
+        next_slot_ += need;
+      }
+    }
+    return r;
+  }
+
+  uint8_t constant(uint64_t v, int line) {
+    auto it = consts_.find(v);
+    if (it != consts_.end()) return (uint8_t)(KS_CONST_BIT | it->second);
+    if (K.cpool.size() >= KS_MAX_CONSTS) fail(KS_ERR_LIMIT, line, "more than 128 distinct immediates");
+    uint32_t i = (uint32_t)K.cpool.size();
+    K.cpool.push_back(v);
+    consts_[v] = i;
+    return (uint8_t)(KS_CONST_BIT | i);
+  }
+
+  // Predicate operand: returns the predicate index, sets the hazard index.
+  uint8_t pred(const Operand& o, int line, uint8_t* hz) {
+    if (o.kind != Operand::REG) fail(KS_ERR_PARSE, line, "predicate register expected");
+    RegDecl& r = reg(o.name, line);
+    if (r.width != 1) fail(KS_ERR_PARSE, line, "predicate register expected");
+    *hz = (uint8_t)(KS_HZ_PRED0 + r.index);
+    return (uint8_t)r.index;
+  }
+
+  // Destination register of `width` bits.
+  uint8_t dest(const Operand& o, unsigned width, int line, uint8_t* hz) {
+    if (o.kind != Operand::REG) fail(KS_ERR_PARSE, line, "register operand expected");
+    RegDecl& r = reg(o.name, line);
+    if (r.width != width) fail(KS_ERR_PARSE, line, "register width does not match the instruction type");
+    *hz = (uint8_t)r.index;
+    return (uint8_t)r.index;
+  }
+
+  // Source operand. allow: 'r' register only, 'v' register or literal,
+  // 'm' register, literal or special register (mov).
+  uint8_t source(const Operand& o, unsigned width, PType ty, char allow, int line, uint8_t* hz, int* special) {
+    *hz = KS_HZ_NONE;
+    switch (o.kind) {
+      case Operand::REG: {
+        RegDecl& r = reg(o.name, line);
+        if (r.width != width) fail(KS_ERR_PARSE, line, "register width does not match the instruction type");
+        *hz = (uint8_t)r.index;
+        return (uint8_t)r.index;
+      }
+      case Operand::SPECIAL:
+        if (allow != 'm' || width != 32) fail(KS_ERR_PARSE, line, "special register only allowed as a 32-bit mov source");
+        *special = o.special;
+        return 0;
+      case Operand::LIT: {
+        if (allow == 'r') fail(KS_ERR_PARSE, line, "register operand expected");
+        uint64_t v;
+        if (o.lit.is_f32) {
+          if (!(ty == PT_F32 || ty == PT_B32)) fail(KS_ERR_PARSE, line, "f32 literal on a non-32-bit-float operand");
+          v = o.lit.mag;
+        } else {
+          if (ty == PT_F32) fail(KS_ERR_PARSE, line, "f32 operands take 0fXXXXXXXX literals only");
+          if (width == 32) {
+            if (o.lit.neg ? o.lit.mag > 0x80000000ull : o.lit.mag > 0xFFFFFFFFull)
+              fail(KS_ERR_PARSE, line, "literal does not fit 32 bits");
+            v = (o.lit.neg ? (0 - o.lit.mag) : o.lit.mag) & 0xFFFFFFFFull;
+          } else {
+            if (o.lit.neg && o.lit.mag > 0x8000000000000000ull) fail(KS_ERR_PARSE, line, "literal does not fit 64 bits");
+            v = o.lit.neg ? (0 - o.lit.mag) : o.lit.mag;
+          }
+        }
+        return constant(v, line);
+      }
+      default:
+        fail(KS_ERR_PARSE, line, "bad operand kind");
+    }
+  }
+
+  KsInsn insn(const Stmt& s) {
+    KsInsn in = blank();
+    const int ln = s.line;
+    if (!s.guard.empty()) {
+      RegDecl& g = reg(s.guard, ln);
+      if (g.width != 1) fail(KS_ERR_PARSE, ln, "guard must be a predicate");
+      in.guard = (uint8_t)g.index;
+      in.gneg = s.guard_neg ? 1 : 0;
+      in.hg = (uint8_t)(KS_HZ_PRED0 + g.index);
+    }
+    const std::string& op = s.opcode;
+    const std::vector<std::string>& m = s.mods;
+    const std::vector<Operand>& o = s.ops;
+    auto unsupported = [&]() -> void {
+      std::string full = op;
+      for (const std::string& x : m) full += "." + x;
+      fail(KS_ERR_UNSUPPORTED, ln, "unsupported instruction form: " + full);
+    };
+    auto arity = [&](size_t n) {
+      if (o.size() != n) fail(KS_ERR_PARSE, ln, op + ": expected " + std::to_string(n) + " operands");
+    };
+    int sp = -1;
+
+    if (op == "add" || op == "sub" || op == "mul" || op == "mad" || op == "fma" || op == "div" || op == "sqrt") {
+      bool rn = false, lo = false;
+      PType t = PT_BAD;
+      for (const std::string& x : m) {
+        if (x == "rn" && !rn) rn = true;
+        else if (x == "lo" && !lo) lo = true;
+        else if (t == PT_BAD && ptype(x) != PT_BAD) t = ptype(x);
+        else unsupported();
+      }
+      if (t == PT_BAD) unsupported();
+      bool f = (t == PT_F32);
+      size_t nops = 3;
+      if (op == "add" || op == "sub") {
+        if (lo || (!f && (!integer(t) || rn))) unsupported();
+        in.op = f ? (op == "add" ? OP_FADD : OP_FSUB)
+                  : bits(t) == 32 ? (op == "add" ? OP_ADD32 : OP_SUB32) : (op == "add" ? OP_ADD64 : OP_SUB64);
+      } else if (op == "mul") {
+        if (f ? lo : (!integer(t) || !lo || rn)) unsupported();
+        in.op = f ? OP_FMUL : bits(t) == 32 ? OP_MUL32 : OP_MUL64;
+      } else if (op == "mad") {
+        if (!integer(t) || !lo || rn) unsupported();
+        in.op = bits(t) == 32 ? OP_MAD32 : OP_MAD64;
+        nops = 4;
+      } else if (op == "fma") {
+        if (!f || !rn || lo) unsupported();
+        in.op = OP_FFMA;
+        in.lat = KS_LAT_FMA;
+        nops = 4;
+      } else if (op == "div") {
+        if (!f || !rn || lo) unsupported();
+        in.op = OP_FDIV;
+        in.lat = KS_LAT_SFU;
+      } else {
+        if (!f || !rn || lo) unsupported();
+        in.op = OP_FSQRT;
+        in.lat = KS_LAT_SFU;
+        nops = 2;
+      }
+      arity(nops);
+      unsigned w = bits(t);
+      in.d = dest(o[0], w, ln, &in.hd);
+      in.a = source(o[1], w, t, 'v', ln, &in.ha, &sp);
+      if (nops > 2) in.b = source(o[2], w, t, 'v', ln, &in.hb, &sp);
+      if (nops > 3) in.c = source(o[3], w, t, 'v', ln, &in.hc, &sp);
+      return in;
+    }
+    if (op == "and" || op == "or" || op == "xor") {
+      if (m.size() != 1) unsupported();
+      PType t = ptype(m[0]);
+      if (!(t == PT_B32 || t == PT_B64 || t == PT_PRED)) unsupported();
+      arity(3);
+      int k = op == "and" ? 0 : op == "or" ? 1 : 2;
+      if (t == PT_PRED) {
+        in.op = (uint8_t)(OP_ANDP + k);
+        uint8_t hz;
+        in.d = pred(o[0], ln, &in.hd);
+        in.a = pred(o[1], ln, &hz); in.ha = hz;
+        in.b = pred(o[2], ln, &hz); in.hb = hz;
+      } else {
+        in.op = (uint8_t)((t == PT_B32 ? OP_AND32 : OP_AND64) + k);
+        unsigned w = bits(t);
+        in.d = dest(o[0], w, ln, &in.hd);
+        in.a = source(o[1], w, t, 'v', ln, &in.ha, &sp);
+        in.b = source(o[2], w, t, 'v', ln, &in.hb, &sp);
+      }
+      return in;
+    }
+    if (op == "shl" || op == "shr") {
+      if (m.size() != 1) unsupported();
+      PType t = ptype(m[0]);
+      if (op == "shl") {
+        if (!(t == PT_B32 || t == PT_B64)) unsupported();
+        in.op = t == PT_B32 ? OP_SHL32 : OP_SHL64;
+      } else {
+        if (!(t == PT_B32 || t == PT_B64 || integer(t))) unsupported();
+        bool w32 = bits(t) == 32;
+        in.op = is_signed(t) ? (w32 ? OP_SHR32S : OP_SHR64S) : (w32 ? OP_SHR32U : OP_SHR64U);
+      }
+      arity(3);
+      unsigned w = bits(t);
+      in.d = dest(o[0], w, ln, &in.hd);
+      in.a = source(o[1], w, t, 'v', ln, &in.ha, &sp);
+      in.b = source(o[2], 32, PT_U32, 'v', ln, &in.hb, &sp);
+      return in;
+    }
+    if (op == "cvt") {
+      std::vector<std::string> mm = m;
+      int rnd = -1;  // -1 none, 4 = rn, else RND_*
+      if (!mm.empty()) {
+        if (mm[0] == "rn") rnd = 4;
+        else if (mm[0] == "rni") rnd = RND_RNI;
+        else if (mm[0] == "rzi") rnd = RND_RZI;
+        else if (mm[0] == "rmi") rnd = RND_RMI;
+        else if (mm[0] == "rpi") rnd = RND_RPI;
+        if (rnd >= 0) mm.erase(mm.begin());
+      }
+      if (mm.size() != 2) unsupported();
+      PType dt = ptype(mm[0]), st = ptype(mm[1]);
+      arity(2);
+      if (integer(dt) && integer(st)) {
+        if (rnd >= 0) unsupported();
+        unsigned dw = bits(dt), sw = bits(st);
+        in.d = dest(o[0], dw, ln, &in.hd);
+        in.a = source(o[1], sw, st, 'r', ln, &in.ha, &sp);
+        if (dw == sw) in.op = dw == 32 ? OP_MOV32 : OP_MOV64;
+        else if (dw == 64) in.op = is_signed(st) ? OP_CVT_SX : OP_CVT_ZX;
+        else in.op = OP_MOV32;  // 64 -> 32 keeps the low slot
+        return in;
+      }
+      if (dt == PT_F32 && integer(st)) {
+        if (rnd != 4) unsupported();
+        in.op = st == PT_U32 ? OP_CVT_F32_U32 : st == PT_S32 ? OP_CVT_F32_S32 : st == PT_U64 ? OP_CVT_F32_U64 : OP_CVT_F32_S64;
+        in.d = dest(o[0], 32, ln, &in.hd);
+        in.a = source(o[1], bits(st), st, 'r', ln, &in.ha, &sp);
+        return in;
+      }
+      if (integer(dt) && st == PT_F32) {
+        if (rnd < 0 || rnd == 4) unsupported();
+        in.op = OP_CVT_F2I;
+        uint8_t dk = dt == PT_S32 ? CVT_S32 : dt == PT_U32 ? CVT_U32 : dt == PT_S64 ? CVT_S64 : CVT_U64;
+        in.flags = (uint8_t)(dk | (rnd << 4));
+        in.d = dest(o[0], bits(dt), ln, &in.hd);
+        in.a = source(o[1], 32, st, 'r', ln, &in.ha, &sp);
+        return in;
+      }
+      unsupported();
+    }
+    if (op == "mov") {
+      if (m.size() != 1) unsupported();
+      PType t = ptype(m[0]);
+      if (t == PT_BAD || t == PT_PRED) unsupported();
+      arity(2);
+      unsigned w = bits(t);
+      in.d = dest(o[0], w, ln, &in.hd);
+      in.a = source(o[1], w, t, 'm', ln, &in.ha, &sp);
+      if (sp >= 0) {
+        in.op = OP_MOVSP;
+        in.imm = (uint64_t)sp;
+      } else {
+        in.op = w == 32 ? OP_MOV32 : OP_MOV64;
+      }
+      return in;
+    }
+    if (op == "setp") {
+      if (m.size() != 2) unsupported();
+      const std::string& c = m[0];
+      PType t = ptype(m[1]);
+      bool uname = (c == "lo" || c == "ls" || c == "hi" || c == "hs");
+      uint8_t cmp;
+      if (c == "eq") cmp = CMP_EQ;
+      else if (c == "ne") cmp = CMP_NE;
+      else if (c == "lt" || c == "lo") cmp = CMP_LT;
+      else if (c == "le" || c == "ls") cmp = CMP_LE;
+      else if (c == "gt" || c == "hi") cmp = CMP_GT;
+      else if (c == "ge" || c == "hs") cmp = CMP_GE;
+      else unsupported();
+      if (t == PT_B32 || t == PT_B64) { if (!(cmp == CMP_EQ || cmp == CMP_NE)) unsupported(); }
+      else if (t == PT_U32 || t == PT_U64) { }
+      else if (t == PT_S32 || t == PT_S64 || t == PT_F32) { if (uname) unsupported(); }
+      else unsupported();
+      in.op = t == PT_F32 ? OP_SETP_F32
+              : t == PT_S32 ? OP_SETP_S32
+              : t == PT_S64 ? OP_SETP_S64
+              : bits(t) == 32 ? OP_SETP_U32 : OP_SETP_U64;
+      in.flags = cmp;
+      arity(3);
+      unsigned w = bits(t);
+      in.d = pred(o[0], ln, &in.hd);
+      in.a = source(o[1], w, t, 'v', ln, &in.ha, &sp);
+      in.b = source(o[2], w, t, 'v', ln, &in.hb, &sp);
+      return in;
+    }
+    if (op == "selp") {
+      if (m.size() != 1) unsupported();
+      PType t = ptype(m[0]);
+      if (t == PT_BAD || t == PT_PRED) unsupported();
+      arity(4);
+      unsigned w = bits(t);
+      in.op = w == 32 ? OP_SELP32 : OP_SELP64;
+      in.d = dest(o[0], w, ln, &in.hd);
+      in.a = source(o[1], w, t, 'v', ln, &in.ha, &sp);
+      in.b = source(o[2], w, t, 'v', ln, &in.hb, &sp);
+      in.c = pred(o[3], ln, &in.hc);
+      return in;
+    }
+    if (op == "bra") {
+      if (!(m.empty() || (m.size() == 1 && m[0] == "uni"))) unsupported();
+      arity(1);
+      if (o[0].kind != Operand::LABEL) fail(KS_ERR_PARSE, ln, "bra needs a label");
+      in.op = OP_BRA;
+      in.lat = KS_LAT_BRA;
+      return in;
+    }
+    if (op == "ret" || op == "exit") {
+      if (!m.empty()) unsupported();
+      arity(0);
+      in.op = OP_RET;
+      in.lat = KS_LAT_RET;
+      return in;
+    }
+    if (op == "ld" || op == "st") {
+      if (m.size() != 2) unsupported();
+      PType t = ptype(m[1]);
+      if (t == PT_BAD || t == PT_PRED) unsupported();
+      unsigned w = bits(t);
+      arity(2);
+      if (op == "ld" && m[0] == "global") {
+        in.op = w == 32 ? OP_LDG32 : OP_LDG64;
+        in.lat = KS_LAT_LDG;
+        in.d = dest(o[0], w, ln, &in.hd);
+        address(o[1], ln, &in);
+        return in;
+      }
+      if (op == "ld" && m[0] == "param") {
+        in.op = w == 32 ? OP_LDP32 : OP_LDP64;
+        in.d = dest(o[0], w, ln, &in.hd);
+        if (o[1].kind != Operand::PARAM) fail(KS_ERR_PARSE, ln, "ld.param needs [param(+offset)]");
+        const KsParam* p = nullptr;
+        for (const KsParam& q : K.params) if (q.name == o[1].name) p = &q;
+        if (!p) fail(KS_ERR_PARSE, ln, "unknown parameter " + o[1].name);
+        int64_t at = (int64_t)p->offset + o[1].offset;
+        int64_t sz = w / 8;
+        if (at < 0 || at + sz > (int64_t)K.param_bytes || at % sz) fail(KS_ERR_PARSE, ln, "ld.param outside the parameter block or misaligned");
+        in.imm = (uint64_t)at;
+        return in;
+      }
+      if (op == "st" && m[0] == "global") {
+        in.op = w == 32 ? OP_STG32 : OP_STG64;
+        in.lat = KS_LAT_STG;
+        address(o[0], ln, &in);
+        in.b = source(o[1], w, t, 'r', ln, &in.hb, &sp);
+        return in;
+      }
+      unsupported();
+    }
+    fail(KS_ERR_UNSUPPORTED, ln, "unsupported opcode " + op);
+  }
+
+  void address(const Operand& o, int ln, KsInsn* in) {
+    if (o.kind != Operand::MEM) fail(KS_ERR_PARSE, ln, "global access needs [64-bit register(+offset)]");
+    RegDecl& r = reg(o.name, ln);
+    if (r.width != 64) fail(KS_ERR_PARSE, ln, "global access needs [64-bit register(+offset)]");
+    in->a = (uint8_t)r.index;
+    in->ha = (uint8_t)r.index;
+    in->imm = (uint64_t)o.offset;  // sign-extended
+  }
+
+  // Immediate post-dominators by Cooper-Harvey-Kennedy on the reverse CFG,
+  // rooted at the virtual exit. Entries that cannot reach the exit
+  // reconverge at the exit.
+  void postdominators() {
+    const int n = (int)K.code.size();
+    const int EXIT = n;
+    std::vector<std::vector<int>> succ((size_t)n + 1), pred((size_t)n + 1);
+    for (int i = 0; i < n; i++) {
+      const KsInsn& in = K.code[(size_t)i];
+      bool guarded = in.guard != KS_NO_GUARD;
+      std::vector<int>& s = succ[(size_t)i];
+      if (in.op == OP_BRA) {
+        s.push_back((int)in.target);
+        if (guarded && (int)in.target != i + 1) s.push_back(i + 1);
+      } else if (in.op == OP_RET) {
+        s.push_back(EXIT);
+        if (guarded) s.push_back(i + 1);
+      } else {
+        s.push_back(i + 1);
+      }
+      for (int x : s) pred[(size_t)x].push_back(i);
+    }
+    // postorder of the reverse graph (edges exit -> predecessors), iterative DFS
+    std::vector<int> order, po_num((size_t)n + 1, -1);
+    std::vector<char> seen((size_t)n + 1, 0);
+    std::vector<std::pair<int, size_t>> stack;
+    stack.push_back({EXIT, 0});
+    seen[(size_t)EXIT] = 1;
+    while (!stack.empty()) {
+      auto& top = stack.back();
+      const std::vector<int>& nb = pred[(size_t)top.first];
+      if (top.second < nb.size()) {
+        int v = nb[top.second++];
+        if (!seen[(size_t)v]) { seen[(size_t)v] = 1; stack.push_back({v, 0}); }
+      } else {
+        po_num[(size_t)top.first] = (int)order.size();
+        order.push_back(top.first);
+        stack.pop_back();
+      }
+    }
+    std::vector<int> idom((size_t)n + 1, -1);
+    idom[(size_t)EXIT] = EXIT;
+    auto intersect = [&](int a, int b) {
+      while (a != b) {
+        while (po_num[(size_t)a] < po_num[(size_t)b]) a = idom[(size_t)a];
+        while (po_num[(size_t)b] < po_num[(size_t)a]) b = idom[(size_t)b];
+      }
+      return a;
+    };
+    bool changed = true;
+    while (changed) {
+      changed = false;
+      for (int k = (int)order.size() - 1; k >= 0; k--) {  // reverse postorder
+        int v = order[(size_t)k];
+        if (v == EXIT) continue;
+        int nd = -1;
+        for (int s : succ[(size_t)v]) {  // predecessors in the reverse graph
+          if (idom[(size_t)s] < 0) continue;
+          nd = nd < 0 ? s : intersect(s, nd);
+        }
+        if (nd >= 0 && idom[(size_t)v] != nd) { idom[(size_t)v] = nd; changed = true; }
+      }
+    }
+    K.ipdom.assign((size_t)n, EXIT);
+    for (int i = 0; i < n; i++)
+      if (seen[(size_t)i] && idom[(size_t)i] >= 0) K.ipdom[(size_t)i] = idom[(size_t)i];
+  }
+
+  void build_image() {
+    size_t ib = K.code.size() * sizeof(KsInsn);
+    size_t cb = K.cpool.size() * sizeof(uint64_t);
+    size_t total = (ib + cb + 15) / 16 * 16;
+    K.image.assign(total, 0);
+    std::memcpy(K.image.data(), K.code.data(), ib);
+    if (cb) std::memcpy(K.image.data() + ib, K.cpool.data(), cb);
+  }
+};
+
+}  // namespace
+
+int decode_module(const char* text, size_t len, std::vector<KsKernel>* out, std::string* err) {
+  try {
+    Parser P(lex(text, len));
+    std::vector<KernelText> kts = P.module();
+    out->clear();
+    for (KernelText& kt : kts) {
+      for (const KsKernel& k : *out)
+        if (k.name == kt.name) fail(KS_ERR_PARSE, kt.line, "kernel defined twice: " + kt.name);
+      KsKernel k;
+      Decoder D(kt, k);
+      D.run();
+      out->push_back(std::move(k));
+    }
+    if (out->empty()) fail(KS_ERR_PARSE, 0, "no .entry in the module");
+    err->clear();
+    return KS_OK;
+  } catch (const Fail& f) {
+    *err = f.msg;
+    return f.code;
+  } catch (const std::exception& e) {
+    *err = e.what();
+    return KS_ERR_PARSE;
+  }
+}
+
+}  // namespace ks

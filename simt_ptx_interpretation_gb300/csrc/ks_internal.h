@@ -1,0 +1,144 @@
+// ks_internal.h — decoded program format and launch block shared by the host
+// decoder (ks_decode.cpp), the C ABI (ks_capi.cpp) and the sm_103a
+// interpreter (ks_interp.cu).
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/ks.h"
+
+namespace ks {
+
+// Handler opcodes of the decoded program. Type and operand width are folded
+// into the opcode so the interpreter dispatches once per instruction.
+enum Op : uint8_t {
+  OP_EVENT = 0,  // trace pseudo-op, zero cost
+  OP_RET,
+  OP_BRA,
+  OP_LDP32, OP_LDP64,  // ld.param
+  OP_LDG32, OP_LDG64,  // ld.global
+  OP_STG32, OP_STG64,  // st.global
+  OP_MOV32, OP_MOV64, OP_MOVSP,
+  OP_ADD32, OP_SUB32, OP_MUL32, OP_MAD32,
+  OP_ADD64, OP_SUB64, OP_MUL64, OP_MAD64,
+  OP_AND32, OP_OR32, OP_XOR32, OP_AND64, OP_OR64, OP_XOR64,
+  OP_ANDP, OP_ORP, OP_XORP,
+  OP_SHL32, OP_SHR32U, OP_SHR32S, OP_SHL64, OP_SHR64U, OP_SHR64S,
+  OP_FADD, OP_FSUB, OP_FMUL, OP_FFMA, OP_FDIV, OP_FSQRT,
+  OP_SETP_U32, OP_SETP_S32, OP_SETP_U64, OP_SETP_S64, OP_SETP_F32,
+  OP_SELP32, OP_SELP64,
+  OP_CVT_F32_U32, OP_CVT_F32_S32, OP_CVT_F32_U64, OP_CVT_F32_S64,
+  OP_CVT_F2I,          // flags: KS_CVT_* destination | rounding << 4
+  OP_CVT_ZX, OP_CVT_SX,  // 32 -> 64 zero / sign extension
+  OP_COUNT
+};
+
+// setp comparison in KsInsn::flags
+enum Cmp : uint8_t { CMP_EQ = 0, CMP_NE, CMP_LT, CMP_LE, CMP_GT, CMP_GE };
+// cvt float->int destination (low nibble) and rounding (high nibble)
+enum CvtDst : uint8_t { CVT_S32 = 0, CVT_U32, CVT_S64, CVT_U64 };
+enum CvtRnd : uint8_t { RND_RNI = 0, RND_RZI, RND_RMI, RND_RPI };
+// special registers (KsInsn::imm of OP_MOVSP)
+enum Special : uint8_t { SP_TID = 0, SP_NTID, SP_CTAID, SP_NCTAID, SP_LANEID, SP_ZERO, SP_ONE };
+
+// Operand encoding: 0..KS_MAX_SLOTS-1 register slot (32-bit; a 64-bit
+// register uses slots s and s+1), KS_CONST_BIT|i constant-pool entry i.
+// Predicate operands are predicate indices 0..KS_MAX_PREDS-1.
+constexpr uint32_t KS_MAX_SLOTS = 96;
+constexpr uint32_t KS_MAX_PREDS = 31;
+constexpr uint32_t KS_MAX_CONSTS = 128;
+constexpr uint8_t KS_CONST_BIT = 0x80;
+// Scoreboard (ready-time table) indices: slots 0..95, predicates 96..126,
+// 127 never written (always ready).
+constexpr uint32_t KS_HZ_PRED0 = 96;
+constexpr uint8_t KS_HZ_NONE = 127;
+constexpr uint32_t KS_HZ_ENTRIES = 128;
+constexpr uint8_t KS_NO_GUARD = 0xFF;
+constexpr uint32_t KS_MAX_INSNS = 2048;
+
+// One decoded instruction, 32 bytes (two 16-byte shared-memory loads).
+struct alignas(16) KsInsn {
+  uint8_t op;
+  uint8_t lat;     // latency class
+  uint8_t guard;   // predicate index or KS_NO_GUARD
+  uint8_t gneg;    // 1: guard negated
+  uint8_t d, a, b, c;
+  uint8_t hd, ha, hb, hc;  // scoreboard indices of dest and sources
+  uint8_t hg;              // scoreboard index of the guard
+  uint8_t flags;
+  uint16_t event;          // trace event id
+  uint64_t imm;            // address offset / param offset / special id
+  uint32_t target;         // branch target
+  uint32_t rpc;            // reconvergence pc of a branch
+};
+static_assert(sizeof(KsInsn) == 32, "KsInsn must be 32 bytes");
+
+struct KsParam {
+  std::string name;
+  uint32_t offset, size;
+};
+
+struct KsEvent {
+  std::string name;
+  uint32_t kind;  // 0 mark, 1 range_start, 2 range_end
+};
+
+struct KsKernel {
+  std::string name;
+  std::vector<KsParam> params;
+  uint32_t param_bytes = 0;
+  std::vector<KsEvent> events;
+  std::vector<KsInsn> code;
+  std::vector<uint64_t> cpool;
+  uint32_t n_slots = 0;
+  uint32_t n_preds = 0;
+  std::vector<int32_t> ipdom;
+  // [insns | constant pool] padded to 16 bytes, as uploaded to the device
+  std::vector<uint8_t> image;
+};
+
+// Decoder entry point (ks_decode.cpp). Returns KS_OK or a KS_ERR_* code and
+// fills `err` with a message.
+int decode_module(const char* text, size_t len, std::vector<KsKernel>* out, std::string* err);
+
+struct KsBufDev {
+  uint64_t sim_base;
+  uint64_t bytes;
+  uint8_t* ptr;
+};
+
+// Everything one interpreter launch needs, passed by value as the kernel
+// argument (about 0.6 KB).
+struct KsLaunch {
+  const uint8_t* image;  // device: insns then constants
+  uint32_t image_bytes;  // multiple of 16
+  uint32_t n_insn;
+  uint32_t n_slots;
+  uint32_t grid, block, wpc;  // simulated grid, block, warps per simulated CTA
+  uint32_t n_warps;           // grid * wpc
+  uint32_t lat[KS_NUM_LAT_CLASSES];
+  uint32_t max_ts;
+  uint32_t stack_depth;
+  uint64_t step_limit;
+  int64_t inject_warp;
+  uint64_t inject_step;
+  uint32_t n_bufs;
+  uint32_t param_bytes;
+  KsBufDev bufs[KS_MAX_BUFFERS];
+  uint8_t* trace;  // may be null
+  uint64_t slot_bytes;
+  uint8_t* stats;
+  alignas(16) uint8_t params[KS_MAX_PARAM_BYTES];
+};
+
+// Shared-memory footprint of one real CTA of `warps` warps.
+size_t interp_smem_bytes(uint32_t image_bytes, uint32_t n_slots, uint32_t warps);
+
+// Launchers (ks_interp.cu). Return a cudaError_t value.
+int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);
+int interp_occupancy(uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
+int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream);
+
+}  // namespace ks

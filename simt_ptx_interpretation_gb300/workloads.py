@@ -664,6 +664,7 @@ class _FuzzGen:
     def program(self, name: str) -> str:
         r = self.rng
         s_perm = 1 << r.randrange(0, 7)  # 1..64
+        self.s_perm = s_perm
         body_start = len(self.lines)
         # prologue: gtid, buffer pointers, perm_s(gtid), register pool init
         pro = [
@@ -720,25 +721,37 @@ class _FuzzGen:
                          f"    .param .u64 fz_out\n)\n{{\n{decl}\n\n{body}\n}}\n")
 
 
-def fuzz_ptx(seed: int, n_static: int = 256, budget: int = 20000, early_exit: bool = True) -> str:
-    """A random program named fuzz_<seed>; redrawn (with a derived stream)
-    until its static bound on per-thread issued instructions fits `budget`."""
+def fuzz_program(seed: int, n_static: int = 256, budget: int = 20000, early_exit: bool = True):
+    """A random program named fuzz_<seed>, redrawn (with a derived stream)
+    until its static bound on per-thread issued instructions fits `budget`.
+    Returns (ptx, s) where s is the lane-interleave stride of its stores."""
     for attempt in range(100):
         g = _FuzzGen(seed * 1000 + attempt, n_static, budget, early_exit)
         text = g.program(f"fuzz_{seed}")
         if g.dynamic <= budget:
-            return text
+            return text, g.s_perm
     raise RuntimeError("fuzz generator could not meet the dynamic budget")
+
+
+def fuzz_ptx(seed: int, n_static: int = 256, budget: int = 20000, early_exit: bool = True) -> str:
+    return fuzz_program(seed, n_static, budget, early_exit)[0]
+
+
+def fuzz_store_words(gtid: np.ndarray, s_perm: int) -> np.ndarray:
+    """The four `out` words thread gtid may store to (perm_s(gtid) + T*k)."""
+    g = gtid.astype(np.int64)
+    perm = (g & ~(32 * s_perm - 1)) | ((g & 31) * s_perm) | ((g >> 5) & (s_perm - 1))
+    return (perm[:, None] + FUZZ_T * np.arange(4)[None, :]).reshape(-1)
 
 
 def fuzz(i: int, grid: int = 1024, block: int = 256, data_seed: int = 4, max_ts: int = 64,
          n_static: int = 256, early_exit: bool = True) -> Workload:
     seed = 1000 + i
-    ptx = fuzz_ptx(seed, n_static=n_static, early_exit=early_exit)
+    ptx, s_perm = fuzz_program(seed, n_static=n_static, early_exit=early_exit)
     inf = uniform_f32(FUZZ_N, -2.0, 2.0, data_seed)
     inu = random_u32(FUZZ_N, data_seed + 1)
     out = np.zeros(FUZZ_N, dtype=np.uint32)
     bufs = place([("inF", inf, False), ("inU", inu, False), ("out", out, True)])
     params = pack_params([("u64", bufs[0].sim_base), ("u64", bufs[1].sim_base), ("u64", bufs[2].sim_base)])
     return Workload(f"fuzz_{seed}", ptx, f"fuzz_{seed}", grid, block, params, bufs, max_ts=max_ts,
-                    meta={"seed": seed})
+                    meta={"seed": seed, "s_perm": s_perm})

@@ -1,0 +1,280 @@
+"""GPU parity: the sm_103a interpreter (called through the C ABI) against the
+oracle, byte for byte — simulated memory, per-warp statistics records, trace
+slots and statuses — on the seeded workloads, at small sizes over every warp
+and at the headline sizes over sampled warps. Plus single-instruction
+semantics, error statuses, launch totals, and a cross-check of the simulated
+memory against the same PTX run natively by the driver JIT."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import simt_ptx_interpretation_gb300 as ks
+from simt_ptx_interpretation_gb300 import workloads as wl
+from tests import _jit, _parity
+from tests import test_oracle_control as toc
+from tests import test_oracle_semantics as tos
+from tests._kernels import op_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for -m gpu tests")
+    from simt_ptx_interpretation_gb300 import _build
+    _build.build_native()
+
+
+# ---------------------------------------------------------- vector_add ----
+
+@pytest.mark.parametrize("n", [4000, 4010, 1, 31, 33, 8192])
+def test_vector_add_parity(n):
+    w = wl.vector_add(n=n)
+    g, o = _parity.assert_parity(w)
+    a, b, c = (x.view(np.float32) for x in g.buffers)
+    assert np.array_equal(c, (a + b).astype(np.float32))
+
+
+def test_vector_add_headline_values():
+    w = wl.vector_add()
+    g = _parity.gpu_run(w)
+    assert tuple(int(g.stats[0][k]) for k in ("cycles", "warp_insts", "thread_insts")) == (463, 20, 640)
+    assert tuple(int(g.stats[127][k]) for k in ("cycles", "warp_insts", "thread_insts")) == (27, 11, 352)
+
+
+def test_vector_add_odd_block_and_no_trace():
+    w = wl.vector_add(n=1000, block=100)
+    _parity.assert_parity(w)
+    g = _parity.gpu_run(w, trace=False)
+    o, _ = _parity.oracle_run(w, trace=False)
+    assert np.array_equal(g.stats.view(np.uint8), o.stats.view(np.uint8))
+
+
+# ---------------------------------------------------------------- ffma ----
+
+@pytest.mark.parametrize("acc", [1, 2, 4, 8, 16])
+def test_ffma_parity_small(acc):
+    _parity.assert_parity(wl.ffma(acc=acc, iters=40, grid=6, block=128))
+
+
+@pytest.mark.parametrize("acc", [1, 8])
+def test_ffma_parity_headline_sampled(acc):
+    """Grid 132 x block 128, 4096 x 32 FFMA per thread: sampled warps."""
+    w = wl.ffma(acc=acc)
+    warps = [0, 1, 2, 3, 130, 263, 264, 400, 524, 525, 526, 527]
+    tids = _parity.thread_ids(w, warps)
+    g, o = _parity.assert_parity(w, warps=warps, out_words={"out": tids})
+    slope = 141 if acc == 1 else 48
+    icept = 446 if acc == 1 else 474
+    assert set(g.stats["cycles"].tolist()) == {icept + slope * 4096}
+
+
+# -------------------------------------------------------------- gather ----
+
+@pytest.mark.parametrize("s", [1, 2, 4, 8, 16, 32])
+def test_gather_parity_small(s):
+    w = wl.gather(s, n_out=1 << 14)
+    g, _ = _parity.assert_parity(w)
+    assert set(g.stats["ld_sectors"].tolist()) == {min(32, 4 * s)}
+
+
+@pytest.mark.parametrize("s", [1, 32])
+def test_gather_parity_headline_sampled(s):
+    w = wl.gather(s)
+    warps = _parity.sample_warps(w, n=48, seed=s)
+    g, _ = _parity.assert_parity(w, warps=warps, out_words={"out": _parity.thread_ids(w, warps)})
+    assert set(g.stats["ld_sectors"].tolist()) == {min(32, 4 * s)}
+    out, src = g.buffers[1].view(np.float32), g.buffers[0].view(np.float32)
+    assert np.array_equal(out, src[::s])
+
+
+# ----------------------------------------------------------- divergent ----
+
+@pytest.mark.parametrize("k", [2, 4, 32])
+def test_divergent_parity_small(k):
+    _parity.assert_parity(wl.divergent(k, n=1 << 14))
+
+
+@pytest.mark.parametrize("k", [2, 4, 32])
+def test_divergent_parity_headline(k):
+    w = wl.divergent(k)
+    warps = _parity.sample_warps(w, n=256, seed=k)
+    g, _ = _parity.assert_parity(w, warps=warps, out_words={"out": _parity.thread_ids(w, warps)})
+    trips = w.buffer("in").data
+    assert np.array_equal(g.buffers[1].view(np.uint32), toc.numpy_divergent(trips, k))
+
+
+# ---------------------------------------------------------------- fuzz ----
+
+@pytest.mark.parametrize("i", range(64))
+def test_fuzz_parity_small(i):
+    _parity.assert_parity(wl.fuzz(i, grid=8))
+
+
+@pytest.mark.parametrize("i", range(0, 64, 8))
+def test_fuzz_parity_headline_sampled(i):
+    w = wl.fuzz(i)
+    warps = _parity.sample_warps(w, n=24, seed=i)
+    words = wl.fuzz_store_words(_parity.thread_ids(w, warps), w.meta["s_perm"])
+    _parity.assert_parity(w, warps=warps, out_words={"out": words})
+
+
+# --------------------------------------------------- single instructions ----
+
+OPS = [
+    ("add.rn.f32", "ff", "f", "f"), ("sub.rn.f32", "ff", "f", "f"), ("mul.rn.f32", "ff", "f", "f"),
+    ("div.rn.f32", "ff", "f", "f"), ("fma.rn.f32", "fff", "f", "f"), ("sqrt.rn.f32", "f", "f", "f"),
+    ("add.u32", "uu", "u", "u"), ("sub.s64", "ww", "w", "w"), ("mul.lo.s32", "uu", "u", "u"),
+    ("mul.lo.u64", "ww", "w", "w"), ("mad.lo.s32", "uuu", "u", "u"), ("mad.lo.u64", "www", "w", "w"),
+    ("and.b32", "uu", "u", "u"), ("xor.b64", "ww", "w", "w"), ("shl.b32", "uu", "u", "u"),
+    ("shr.s32", "uu", "u", "u"), ("shr.u64", "wu", "w", "w"), ("shr.s64", "wu", "w", "w"),
+    ("setp.lt.f32", "ff", "p", "f"), ("setp.ne.f32", "ff", "p", "f"), ("setp.ge.s32", "uu", "p", "u"),
+    ("setp.hi.u64", "ww", "p", "w"), ("selp.b64", "wwp", "w", "w"), ("selp.f32", "ffp", "f", "f"),
+    ("cvt.rn.f32.u32", "u", "f", "u"), ("cvt.rn.f32.s64", "w", "f", "w"), ("cvt.rni.s32.f32", "f", "u", "f"),
+    ("cvt.rzi.u64.f32", "f", "w", "f"), ("cvt.rmi.s64.f32", "f", "w", "f"), ("cvt.rpi.u32.f32", "f", "u", "f"),
+    ("cvt.s64.s32", "u", "w", "u"), ("cvt.u32.u64", "w", "u", "w"), ("and.pred", "pp", "p", "p"),
+    ("xor.pred", "pp", "p", "p"),
+]
+
+
+def operands(kind, seed):
+    if kind == "f":
+        return tos.f32_operands(seed)
+    if kind == "u":
+        return tos.int_operands(seed, 32)
+    if kind == "w":
+        return tos.int_operands(seed, 64)
+    return [x & 1 for x in tos.int_operands(seed, 32)]
+
+
+@pytest.mark.parametrize("op,srcs,dst,kind", OPS)
+def test_single_instruction_parity(op, srcs, dst, kind):
+    ins = [operands(k if k != "p" else "p", 50 + j) for j, k in enumerate(srcs)]
+    while len(ins) < 3:
+        ins.append(None)
+    w = op_workload("k_" + op.replace(".", "_"), op, srcs, dst, *[np.array(x, dtype=np.uint64) if x else None for x in ins])
+    _parity.assert_parity(w)
+
+
+# ------------------------------------------------------------- statuses ----
+
+def test_error_statuses_match_the_oracle():
+    base = 0x60000000
+    buf = np.zeros(1024, dtype=np.uint8)
+    cases = [
+        (toc.access_kernel("mul.lo.u32 %r2, %r1, 64;\n    cvt.u64.u32 %rd2, %r2;\n    add.s64 %rd3, %rd1, %rd2;\n"
+                           "    ld.global.u32 %r3, [%rd3];"), 1),
+        (toc.access_kernel("ld.global.u32 %r3, [%rd1+2];"), 2),
+        (toc.access_kernel("ld.global.u64 %rd2, [%rd1+2044];"), 2),
+        (toc.access_kernel("mul.lo.u32 %r2, %r1, 2048;\n    add.u32 %r2, %r2, 2;\n    cvt.u64.u32 %rd2, %r2;\n"
+                           "    add.s64 %rd3, %rd1, %rd2;\n    st.global.u32 [%rd3], %r1;"), 2),
+    ]
+    import struct
+    for ptx, want in cases:
+        w = wl.Workload("bad", ptx, "bad", 2, 64, struct.pack("<Q", base), wl.place([("buf", buf.copy(), True)]))
+        w.buffers[0].sim_base = base
+        g, o = _parity.assert_parity(w, cfg=ks.Config())
+        assert g.totals.status == want and g.totals.first_failed_warp == 0 and g.totals.n_failed == 4
+
+
+def test_step_limit_stack_and_injection_match_the_oracle():
+    ptx = toc.cfg_kernel(toc.HAND_CFGS["endless"][0])
+    w = wl.Workload("cfg", ptx, "cfg", 3, 64, b"", [])
+    g, _ = _parity.assert_parity(w, cfg=ks.Config(step_limit=777))
+    assert g.totals.status == 3 and set(g.stats["warp_insts"].tolist()) == {777}
+    body = """
+    mov.u32 %r1, %tid.x;
+    and.b32 %r2, %r1, 1;
+    setp.eq.u32 %p1, %r2, 0;
+    @%p1 bra ELSE;
+    add.u32 %r3, %r3, 1;
+    bra.uni JOIN;
+ELSE:
+    add.u32 %r3, %r3, 2;
+JOIN:
+    ret;"""
+    w = wl.Workload("cfg", toc.cfg_kernel(body), "cfg", 2, 64, b"", [])
+    g, _ = _parity.assert_parity(w, cfg=ks.Config(stack_depth=2))
+    assert g.totals.status == 4
+    g, _ = _parity.assert_parity(w, cfg=ks.Config(stack_depth=3))
+    assert g.totals.status == 0 and g.totals.max_stack_depth == 3
+    v = wl.vector_add()
+    g, _ = _parity.assert_parity(v, cfg=ks.Config(max_ts=8, inject_warp=5, inject_step=7))
+    assert g.totals.status == 6 and g.totals.first_failed_warp == 5 and g.totals.n_failed == 1
+
+
+def test_divergence_examples_match_the_oracle():
+    for name in sorted(toc.HAND_CFGS):
+        if name == "endless":
+            continue
+        body, _ = toc.HAND_CFGS[name]
+        w = wl.Workload("cfg", toc.cfg_kernel(body), "cfg", 2, 96, b"", [])
+        _parity.assert_parity(w, cfg=ks.Config(max_ts=4))
+
+
+# --------------------------------------------------------------- totals ----
+
+def test_read_stats_totals_reduce_every_record():
+    w = wl.divergent(4, n=1 << 14)
+    g = _parity.gpu_run(w)
+    s = g.stats
+    t = g.totals
+    assert t.cycles_max == int(s["cycles"].max()) and t.cycles_sum == int(s["cycles"].sum())
+    for f in ("warp_insts", "thread_insts", "ld_req", "ld_sectors", "st_req", "st_sectors", "ld_lines", "st_lines"):
+        assert getattr(t, f) == int(s[f].sum()), f
+    assert t.n_warps == w.warps and t.n_failed == 0 and t.first_failed_warp == -1 and t.status == 0
+    assert t.max_stack_depth == int(s["max_stack_depth"].max())
+
+
+# -------------------------------------------------- driver-JIT cross-check ----
+
+def jit_memory(w: wl.Workload):
+    layout, _ = oracle.params_layout(w.ptx, w.kernel)
+    vals = _jit.unpack_params(w.params, layout)
+    bufs = w.fresh_buffers()
+    dev = [torch.from_numpy(b.data.view(np.uint8)).cuda() for b in bufs]
+    real = {b.sim_base: t.data_ptr() for b, t in zip(bufs, dev)}
+    vals = [real.get(v, v) if size == 8 else v for v, (off, size) in zip(vals, layout)]
+    _jit.run_native(w.ptx, w.kernel, w.grid, w.block, layout, vals)
+    return [t.cpu().numpy() for t in dev]
+
+
+def nan_equivalent(a: np.ndarray, b: np.ndarray) -> bool:
+    a32, b32 = a.view(np.uint32), b.view(np.uint32)
+    same = a32 == b32
+    fa, fb = a.view(np.float32), b.view(np.float32)
+    return bool(np.all(same | (np.isnan(fa) & np.isnan(fb))))
+
+
+@pytest.mark.parametrize("make", [lambda: wl.vector_add(n=4010), lambda: wl.ffma(acc=8, iters=64, grid=4),
+                                  lambda: wl.gather(8, n_out=1 << 14), lambda: wl.divergent(4, n=1 << 14)])
+def test_jit_crosscheck_workloads(make):
+    w = make()
+    sim = _parity.gpu_run(w).buffers
+    nat = jit_memory(w)
+    for b, x, y in zip(w.buffers, sim, nat):
+        assert np.array_equal(x, y), b.name
+
+
+@pytest.mark.parametrize("i", range(0, 64, 4))
+def test_jit_crosscheck_fuzz(i):
+    w = wl.fuzz(i, grid=8)
+    sim = _parity.gpu_run(w).buffers
+    nat = jit_memory(w)
+    assert nan_equivalent(sim[2], nat[2])
+
+
+@pytest.mark.parametrize("op,srcs,dst,kind", OPS[:18] + OPS[24:32])
+def test_jit_crosscheck_single_instructions(op, srcs, dst, kind):
+    ins = [operands(k, 50 + j) for j, k in enumerate(srcs)]
+    while len(ins) < 3:
+        ins.append(None)
+    w = op_workload("k_" + op.replace(".", "_"), op, srcs, dst, *[np.array(x, dtype=np.uint64) if x else None for x in ins])
+    sim = _parity.gpu_run(w).buffers[0]
+    nat = jit_memory(w)[0]
+    if dst == "f":
+        assert nan_equivalent(sim, nat)
+    else:
+        assert np.array_equal(sim, nat)

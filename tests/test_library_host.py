@@ -1,0 +1,139 @@
+"""Host-side checks of libks that need no GPU: the shared library loads and
+exports every function include/ks.h declares; the decoder accepts exactly the
+programs the oracle accepts and agrees on parameter layout, event tables and
+reconvergence points; output sizes follow the IKET slot rule."""
+import ctypes
+import os
+import random
+import re
+
+import pytest
+
+import oracle
+from simt_ptx_interpretation_gb300 import _build, _native
+from simt_ptx_interpretation_gb300 import api as ks
+from simt_ptx_interpretation_gb300 import workloads as wl
+from tests import test_oracle_control as toc
+from tests._kernels import op_kernel
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build_native()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ks.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(ks_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_function_is_exported():
+    names = declared_functions()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(_native.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_native.EXPORTS)
+
+
+def test_output_sizes_follow_the_slot_rule():
+    for grid, block, ts in [(16, 256, 8), (1024, 256, 64), (3, 33, 0), (1, 1, 1), (7, 100, 3)]:
+        W = grid * ((block + 31) // 32)
+        assert ks.stats_bytes(grid, block) == W * 96
+        assert ks.trace_bytes(grid, block, ts) == W * ((16 + 4 * ts + 7) // 8 * 8)
+
+
+def corpus():
+    progs = [("vector_add", wl.vector_add_ptx()), ("gather", wl.gather_ptx()), ("divergent", wl.divergent_ptx())]
+    for acc in (1, 8):
+        progs.append((f"ffma_acc{acc}", wl.ffma_ptx(acc)))
+    for i in range(0, 64, 3):
+        progs.append((f"fuzz_{1000 + i}", wl.fuzz_ptx(1000 + i)))
+    for name, (body, _) in toc.HAND_CFGS.items():
+        progs.append(("cfg", toc.cfg_kernel(body)))
+    for name, body in toc.BAD_PROGRAMS:
+        progs.append(("k", wl.HEADER + (".visible .entry k()\n{\n    .reg .pred %p<2>;\n    .reg .b32 %r<4>;\n"
+                                        "    .reg .f32 %f<4>;\n    .reg .b64 %rd<4>;\n    " + body + "\n}\n")))
+    for op, srcs, dst in [("add.u32", "uu", "u"), ("fma.rn.f32", "fff", "f"), ("setp.lt.f32", "ff", "p"),
+                          ("selp.b64", "wwp", "w"), ("cvt.rzi.s64.f32", "f", "w"), ("shr.s64", "wu", "w")]:
+        progs.append(("k_op", op_kernel("k_op", op, srcs, dst)))
+    return progs
+
+
+@pytest.mark.parametrize("idx", range(len(corpus())))
+def test_decoder_accepts_what_the_oracle_accepts(idx):
+    kernel, ptx = corpus()[idx]
+    ocode, _ = oracle.parse_check(ptx, kernel)
+    try:
+        m = ks.Module(ptx)
+        dcode = 0
+    except ks.KsError as e:
+        dcode = e.code
+    assert (ocode == 0) == (dcode == 0), (ocode, dcode)
+    if dcode:
+        return
+    layout, total = oracle.params_layout(ptx, kernel)
+    assert [(o, s) for _, o, s in m.params(kernel)] == layout
+    assert m.info(kernel)["param_bytes"] == total
+    assert [k for k, _ in m.events(kernel)] == oracle.events(ptx, kernel)
+    assert m.ipdom(kernel) == oracle.ipdom(ptx, kernel)
+
+
+@pytest.mark.parametrize("name", sorted(toc.HAND_CFGS))
+def test_decoder_ipdom_hand_drawn(name):
+    body, want = toc.HAND_CFGS[name]
+    assert ks.Module(toc.cfg_kernel(body)).ipdom("cfg") == want
+
+
+def test_decoder_ipdom_random_cfgs_against_brute_force():
+    rng = random.Random(78)
+    for _ in range(200):
+        m = rng.randrange(2, 30)
+        body, succ = toc.random_cfg(rng, m)
+        assert ks.Module(toc.cfg_kernel(body)).ipdom("cfg") == toc.brute_ipdom(succ), body
+
+
+def test_resource_limits_are_reported():
+    regs = "\n".join(f"    add.u32 %r{i}, %r{i}, 1;" for i in range(100))
+    ptx = wl.HEADER + ".visible .entry big()\n{\n    .reg .b32 %r<100>;\n" + regs + "\n    ret;\n}\n"
+    with pytest.raises(ks.KsError) as e:
+        ks.Module(ptx)
+    assert e.value.code == -6
+    consts = "\n".join(f"    add.u32 %r1, %r1, {i + 1000};" for i in range(130))
+    ptx = wl.HEADER + ".visible .entry big()\n{\n    .reg .b32 %r<2>;\n" + consts + "\n    ret;\n}\n"
+    with pytest.raises(ks.KsError) as e:
+        ks.Module(ptx)
+    assert e.value.code == -6
+
+
+def test_unknown_kernel_and_bad_arguments():
+    m = ks.Module(wl.vector_add_ptx())
+    with pytest.raises(ks.KsError) as e:
+        m.info("nope")
+    assert e.value.code == -5
+    L = _native.lib()
+    assert L.ks_load_module(None, 0, None, None, 0) == -3
+    assert L.ks_simulate(None, b"x", 1, 32, None, 0, None, 0, None, 0, None, 0, None, None) == -3
+    # shape and size checks happen before any GPU work
+    stats = ctypes.create_string_buffer(96 * 8)
+    args = dict(grid=0, block=32)
+    assert L.ks_simulate(m.handle, b"vector_add", 0, 32, None, 0, None, 0, None, 0, stats, 96 * 8, None, None) == -3
+    assert L.ks_simulate(m.handle, b"vector_add", 1, 2000, None, 0, None, 0, None, 0, stats, 96 * 8, None, None) == -3
+    p = ctypes.create_string_buffer(28)
+    # too small a stats buffer
+    assert L.ks_simulate(m.handle, b"vector_add", 16, 256, p, 28, None, 0, None, 0, stats, 96, None, None) == -3
+    # parameter block smaller than the kernel's
+    assert L.ks_simulate(m.handle, b"vector_add", 1, 32, p, 8, None, 0, None, 0, stats, 96, None, None) == -3
+    # overlapping buffers
+    bufs = (_native.KsBuffer * 2)()
+    bufs[0].sim_base, bufs[0].dev_ptr, bufs[0].bytes = 0x10000000, 1, 8192
+    bufs[1].sim_base, bufs[1].dev_ptr, bufs[1].bytes = 0x10001000, 1, 8192
+    assert L.ks_simulate(m.handle, b"vector_add", 1, 32, p, 28, bufs, 2, None, 0, stats, 96, None, None) == -3
+    # unaligned simulated base
+    bufs[1].sim_base = 0x20000010
+    assert L.ks_simulate(m.handle, b"vector_add", 1, 32, p, 28, bufs, 2, None, 0, stats, 96, None, None) == -3
+    for code in (0, -1, -2, -3, -4, -5, -6, 1, 2, 3, 4, 5, 6):
+        assert L.ks_status_string(code)
