@@ -103,7 +103,7 @@ typedef struct {
 } ks_buffer;
 
 typedef struct {
-  uint32_t lat[KS_NUM_LAT_CLASSES]; /* cycles per latency class */
+  uint32_t lat[KS_NUM_LAT_CLASSES]; /* cycles per latency class, each <= 2^24 */
   uint32_t max_ts_per_warp;         /* trace records per warp slot */
   uint32_t simt_stack_depth;        /* 1..32 entries, base entry included */
   uint64_t step_limit;              /* max issued instructions per warp */

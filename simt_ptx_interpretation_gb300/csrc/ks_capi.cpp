@@ -200,6 +200,8 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   if (!stats_buf || stats_bytes < W * sizeof(ks_warp_stats)) return KS_ERR_ARG;
   if (cfg.simt_stack_depth == 0 || cfg.simt_stack_depth > KS_MAX_STACK) return KS_ERR_ARG;
   if (cfg.max_ts_per_warp > (1u << 24)) return KS_ERR_ARG;
+  for (uint32_t i = 0; i < KS_NUM_LAT_CLASSES; i++)
+    if (cfg.lat[i] > ks::KS_MAX_LATENCY) return KS_ERR_ARG;
   const uint64_t slot = (16ull + 4ull * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
   if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
 
@@ -230,8 +232,11 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   std::memset(&L, 0, sizeof L);
   L.image = static_cast<const uint8_t*>(image);
   L.image_bytes = (uint32_t)k->image.size();
+  L.prog_bytes = k->prog_bytes;
   L.n_insn = (uint32_t)k->code.size();
   L.n_slots = k->n_slots;
+  L.n_crows = k->layout.n_crows;
+  L.layout = k->layout;
   L.grid = grid;
   L.block = block;
   L.wpc = (block + 31u) / 32u;
@@ -256,11 +261,12 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
 
   // ---- real launch shape: as many real warps as simulated warps, up to the
   // resident capacity; CTAs small enough that every SM gets work ----
+  const uint32_t region = k->layout.region_bytes;
   uint32_t wpc_real = 8;
   while (wpc_real > 1 && (W + wpc_real - 1) / wpc_real < 2ull * (uint64_t)di.sms) wpc_real /= 2;
-  while (wpc_real > 1 && ks::interp_smem_bytes(L.image_bytes, L.n_slots, wpc_real) > (size_t)di.max_smem)
+  while (wpc_real > 1 && ks::interp_smem_bytes(L.image_bytes, region, wpc_real) > (size_t)di.max_smem)
     wpc_real /= 2;
-  const size_t smem = ks::interp_smem_bytes(L.image_bytes, L.n_slots, wpc_real);
+  const size_t smem = ks::interp_smem_bytes(L.image_bytes, region, wpc_real);
   if (smem > (size_t)di.max_smem) return KS_ERR_LIMIT;
   int per_sm = 0;
   if (ks::interp_occupancy(wpc_real, smem, &per_sm) != 0) return KS_ERR_CUDA;

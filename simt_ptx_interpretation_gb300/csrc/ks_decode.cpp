@@ -952,13 +952,180 @@ class Decoder {
       if (seen[(size_t)i] && idom[(size_t)i] >= 0) K.ipdom[(size_t)i] = idom[(size_t)i];
   }
 
+  // Width in bits of the row operand at position `pos` (0 a, 1 b, 2 c, 3 d)
+  // of a decoded op, or 0 if that position holds no register/constant row.
+  static unsigned row_width(const KsInsn& in, int pos) {
+    const unsigned op = in.op;
+    auto w = [&](unsigned a, unsigned b, unsigned c, unsigned d) {
+      const unsigned v[4] = {a, b, c, d};
+      return v[pos];
+    };
+    switch (op) {
+      case OP_LDP32: return w(0, 0, 0, 32);
+      case OP_LDP64: return w(0, 0, 0, 64);
+      case OP_LDG32: return w(64, 0, 0, 32);
+      case OP_LDG64: return w(64, 0, 0, 64);
+      case OP_STG32: return w(64, 32, 0, 0);
+      case OP_STG64: return w(64, 64, 0, 0);
+      case OP_MOV32: return w(32, 0, 0, 32);
+      case OP_MOV64: return w(64, 0, 0, 64);
+      case OP_MOVSP: return w(0, 0, 0, 32);
+      case OP_ADD32: case OP_SUB32: case OP_MUL32: case OP_AND32: case OP_OR32: case OP_XOR32:
+      case OP_SHL32: case OP_SHR32U: case OP_SHR32S: case OP_FADD: case OP_FSUB: case OP_FMUL:
+      case OP_FDIV: case OP_SELP32:
+        return w(32, 32, 0, 32);
+      case OP_MAD32: case OP_FFMA: return w(32, 32, 32, 32);
+      case OP_ADD64: case OP_SUB64: case OP_MUL64: case OP_AND64: case OP_OR64: case OP_XOR64:
+      case OP_SELP64:
+        return w(64, 64, 0, 64);
+      case OP_MAD64: return w(64, 64, 64, 64);
+      case OP_SHL64: case OP_SHR64U: case OP_SHR64S: return w(64, 32, 0, 64);
+      case OP_FSQRT: case OP_CVT_F32_U32: case OP_CVT_F32_S32: return w(32, 0, 0, 32);
+      case OP_CVT_F32_U64: case OP_CVT_F32_S64: return w(64, 0, 0, 32);
+      case OP_CVT_F2I: return w(32, 0, 0, ((in.flags & 15) == CVT_S64 || (in.flags & 15) == CVT_U64) ? 64 : 32);
+      case OP_CVT_ZX: case OP_CVT_SX: return w(32, 0, 0, 64);
+      case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_F32: return w(32, 32, 0, 0);
+      case OP_SETP_U64: case OP_SETP_S64: return w(64, 64, 0, 0);
+      default: return 0;  // events, control, predicate logic
+    }
+  }
+
+  // Routing constants of the unified datapaths (added to the pool on demand).
+  static bool fpu_family(uint8_t op) { return op == OP_FADD || op == OP_FSUB || op == OP_FMUL || op == OP_FFMA; }
+  static bool imad_family(uint8_t op) {
+    return op == OP_ADD32 || op == OP_SUB32 || op == OP_MUL32 || op == OP_MAD32 || op == OP_MOV32;
+  }
+
+  static unsigned routed_width(const KsInsn& in, int pos) {
+    if (fpu_family(in.op) || imad_family(in.op)) return 32;
+    return row_width(in, pos);
+  }
+
+  int in_line(size_t) const { return T.line; }
+
+  // Lays out the warp region and emits the device image.
   void build_image() {
-    size_t ib = K.code.size() * sizeof(KsInsn);
-    size_t cb = K.cpool.size() * sizeof(uint64_t);
-    size_t total = (ib + cb + 15) / 16 * 16;
-    K.image.assign(total, 0);
-    std::memcpy(K.image.data(), K.code.data(), ib);
-    if (cb) std::memcpy(K.image.data() + ib, K.cpool.data(), cb);
+    const size_t n = K.code.size();
+    // rewrite the unified-datapath families onto (a, b, c) of fma / mad
+    struct Route { uint8_t a, b, c; uint32_t aux; };
+    std::vector<Route> route(n);
+    for (size_t i = 0; i < n; i++) {
+      const KsInsn& in = K.code[i];
+      Route r{in.a, in.b, in.c, 0};
+      if (fpu_family(in.op)) {
+        if (in.op == OP_FADD || in.op == OP_FSUB) {
+          r.b = constant(0x3F800000ull, in_line(i));
+          r.c = in.b;
+          r.aux = in.op == OP_FSUB ? 0x80000000u : 0u;
+        } else if (in.op == OP_FMUL) {
+          r.c = constant(0x80000000ull, in_line(i));
+        }
+      } else if (imad_family(in.op)) {
+        if (in.op == OP_ADD32 || in.op == OP_SUB32) {
+          r.b = constant(1ull, in_line(i));
+          r.c = in.b;
+          r.aux = in.op == OP_SUB32 ? 0xFFFFFFFFu : 0u;
+        } else if (in.op == OP_MUL32) {
+          r.c = constant(0ull, in_line(i));
+        } else if (in.op == OP_MOV32) {
+          r.b = constant(1ull, in_line(i));
+          r.c = constant(0ull, in_line(i));
+        }
+      }
+      route[i] = r;
+    }
+    // constant rows: one per constant, two if any use is 64-bit
+    std::vector<unsigned> cwidth(K.cpool.size(), 32);
+    for (size_t i = 0; i < n; i++) {
+      const KsInsn& in = K.code[i];
+      const uint8_t ops[4] = {route[i].a, route[i].b, route[i].c, in.d};
+      for (int p = 0; p < 4; p++) {
+        const unsigned w = routed_width(in, p);
+        if (w && (ops[p] & KS_CONST_BIT)) cwidth[ops[p] & 0x7F] = std::max(cwidth[ops[p] & 0x7F], w);
+      }
+    }
+    std::vector<uint32_t> crow(K.cpool.size()), rowval;
+    for (size_t k = 0; k < K.cpool.size(); k++) {
+      crow[k] = (uint32_t)rowval.size();
+      rowval.push_back((uint32_t)K.cpool[k]);
+      if (cwidth[k] == 64) rowval.push_back((uint32_t)(K.cpool[k] >> 32));
+    }
+    DevLayout& Y = K.layout;
+    Y.n_slots = K.n_slots;
+    Y.n_crows = (uint32_t)rowval.size();
+    Y.const_off = K.n_slots * 128u;
+    Y.zero_off = Y.const_off + Y.n_crows * 128u;
+    Y.ready_off = Y.zero_off + 128u;
+    const uint32_t entries = K.n_slots + 32u + 1u;
+    Y.sink_off = Y.ready_off + (K.n_slots + 32u) * 4u;
+    Y.stack_off = Y.ready_off + (entries * 4u + 127u) / 128u * 128u;
+    Y.region_bytes = Y.stack_off + KS_MAX_STACK * 8u;
+
+    auto row_of = [&](uint8_t o) -> uint32_t {
+      return (o & KS_CONST_BIT) ? Y.const_off + crow[o & 0x7F] * 128u : (uint32_t)o * 128u;
+    };
+    auto hz = [&](uint8_t h) -> uint32_t {
+      if (h == KS_HZ_NONE) return Y.pred_entry(31);
+      if (h >= KS_HZ_PRED0) return Y.pred_entry(h - KS_HZ_PRED0);
+      return Y.ready_off + (uint32_t)h * 4u;
+    };
+    std::vector<DevInsn> dev(n + 1);
+    for (size_t i = 0; i <= n; i++) {
+      DevInsn& o = dev[i];
+      std::memset(&o, 0, sizeof o);
+      o.guard = 31;
+      o.a = o.b = o.c = o.d = Y.zero_off;
+      o.ha = o.hb = o.hc = Y.pred_entry(31);
+      o.hd = Y.sink_off;
+      if (i == n) {  // exit sentinel
+        o.op = OP_EXIT;
+        continue;
+      }
+      const KsInsn& in = K.code[i];
+      o.op = fpu_family(in.op) ? DOP_FPU : imad_family(in.op) ? DOP_IMAD : in.op;
+      o.inc = in.op == OP_EVENT ? 0u : 1u;
+      if (in.guard != KS_NO_GUARD) {
+        o.guard = in.guard;
+        o.gneg = in.gneg ? 0xFFFFFFFFu : 0u;
+      }
+      const uint8_t ops[4] = {route[i].a, route[i].b, route[i].c, in.d};
+      uint32_t* rows[4] = {&o.a, &o.b, &o.c, &o.d};
+      for (int p = 0; p < 4; p++)
+        if (routed_width(in, p)) *rows[p] = row_of(ops[p]);
+      if (o.op == DOP_FPU || o.op == DOP_IMAD) o.aux = route[i].aux;
+      if (in.op != OP_EVENT) {
+        o.ha = hz(in.ha);
+        o.hb = hz(in.hb);
+        o.hc = hz(in.hc);
+        o.hd = in.hd == KS_HZ_NONE ? Y.sink_off : hz(in.hd);
+        o.wlat = (uint32_t)in.lat;
+        if (in.hd != KS_HZ_NONE) o.wlat |= DEV_HAS_DEST;
+        if (in.op == OP_STG32 || in.op == OP_STG64) o.wlat |= DEV_IS_STORE;
+        if (in.op == OP_BRA || in.op == OP_RET) o.wlat |= DEV_IS_CTRL;
+      }
+      switch (in.op) {
+        case OP_EVENT: o.aux = in.event; break;
+        case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64:
+        case OP_LDP32: case OP_LDP64: case OP_MOVSP:
+          o.aux = (uint32_t)in.imm;
+          break;
+        case OP_CVT_F2I: o.aux = in.flags; break;
+        case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32:
+          o.aux = (uint32_t)in.flags | ((uint32_t)in.d << 8);
+          break;
+        case OP_ANDP: case OP_ORP: case OP_XORP:
+          o.aux = (uint32_t)in.a | ((uint32_t)in.b << 8) | ((uint32_t)in.d << 16);
+          break;
+        case OP_SELP32: case OP_SELP64: o.aux = in.c; break;
+        case OP_BRA: o.aux = (in.target & 0xFFFFu) | ((in.rpc & 0xFFFFu) << 16); break;
+        default: break;
+      }
+    }
+    K.prog_bytes = (uint32_t)((n + 1) * sizeof(DevInsn));
+    const size_t cb = rowval.size() * 4;
+    K.image.assign((K.prog_bytes + cb + 15) / 16 * 16, 0);
+    std::memcpy(K.image.data(), dev.data(), K.prog_bytes);
+    if (cb) std::memcpy(K.image.data() + K.prog_bytes, rowval.data(), cb);
   }
 };
 

@@ -57,6 +57,8 @@ constexpr uint8_t KS_HZ_NONE = 127;
 constexpr uint32_t KS_HZ_ENTRIES = 128;
 constexpr uint8_t KS_NO_GUARD = 0xFF;
 constexpr uint32_t KS_MAX_INSNS = 2048;
+// Largest latency a class may have (keeps the 32-bit epoch-relative clock exact).
+constexpr uint32_t KS_MAX_LATENCY = 1u << 24;
 
 // One decoded instruction, 32 bytes (two 16-byte shared-memory loads).
 struct alignas(16) KsInsn {
@@ -74,6 +76,54 @@ struct alignas(16) KsInsn {
   uint32_t rpc;            // reconvergence pc of a branch
 };
 static_assert(sizeof(KsInsn) == 32, "KsInsn must be 32 bytes");
+
+// ---- device program format ---------------------------------------------
+// The host resolves every KsInsn into a 64-byte DevInsn whose operand fields
+// are byte offsets inside a warp's shared-memory region, so the interpreter
+// reads each operand with one shared load at (lane base + offset):
+//
+//   warp region: [register rows: n_slots x 128 B]   row s = slot s, word l = lane l
+//                [constant rows: n_crows x 128 B]   the constant replicated per lane
+//                [zero row: 128 B]                  operand "none"
+//                [ready table: n_slots + 32 + 1 u32, padded to 128 B]
+//                    entry s: slot s; n_slots + p: predicate p (p = 31 is the
+//                    always-true predicate and stays 0); last: write sink
+//                [reconvergence stack: 32 x 8 B]
+//
+// A 64-bit register or constant uses two consecutive rows (low word first),
+// so its high word is at offset + 128.
+struct alignas(16) DevInsn {
+  uint32_t op;
+  uint32_t guard;  // predicate lane 0..30, or 31 (always true)
+  uint32_t gneg;   // 0 or 0xFFFFFFFF
+  uint32_t inc;    // 1 for an issued instruction, 0 for a trace pseudo-op or the exit sentinel
+  uint32_t a, b, c, d;       // operand row offsets (region-relative)
+  uint32_t ha, hb, hc, hd;   // ready-table entry offsets (region-relative); hd = sink if no dest
+  uint32_t wlat;   // in the image: latency class | flags (below); patched to dest latency
+  uint32_t dlat;   // patched: store completion latency (0 if not a store)
+  uint32_t nlat;   // patched: issue-clock advance (latency for bra/ret, 1 otherwise, 0 if inc == 0)
+  uint32_t aux;    // offset / param offset / special / event / cvt / cmp|pred / target|rpc<<16 / pred idx
+};
+static_assert(sizeof(DevInsn) == 64, "DevInsn must be 64 bytes");
+
+// flags in DevInsn::wlat of the uploaded image
+constexpr uint32_t DEV_HAS_DEST = 1u << 8;
+constexpr uint32_t DEV_IS_STORE = 1u << 9;
+constexpr uint32_t DEV_IS_CTRL = 1u << 10;
+constexpr uint32_t OP_EXIT = 0xFE;  // sentinel at index n_insn: the remaining lanes finish
+// Unified datapaths selected at resolve time (DevInsn::op only):
+//   DOP_FPU:  d = fma.rn(a, b, c ^ aux)      add: b = 1.0, c = y;  sub: b = 1.0, c = y, aux = sign bit;
+//                                            mul: c = -0.0;        fma: as is
+//   DOP_IMAD: d = a * b + ((c ^ aux) - aux)  add: b = 1, c = y;    sub: aux = ~0;  mul: c = 0;
+//                                            mad: as is;           mov: b = 1, c = 0
+constexpr uint32_t DOP_FPU = 0x40;
+constexpr uint32_t DOP_IMAD = 0x41;
+
+struct DevLayout {
+  uint32_t n_slots, n_crows;
+  uint32_t const_off, zero_off, ready_off, sink_off, stack_off, region_bytes;
+  uint32_t pred_entry(uint32_t p) const { return ready_off + (n_slots + p) * 4u; }
+};
 
 struct KsParam {
   std::string name;
@@ -95,8 +145,10 @@ struct KsKernel {
   uint32_t n_slots = 0;
   uint32_t n_preds = 0;
   std::vector<int32_t> ipdom;
-  // [insns | constant pool] padded to 16 bytes, as uploaded to the device
+  // [DevInsn x (n_insn + 1) | constant row values (u32 each), padded to 16]
   std::vector<uint8_t> image;
+  DevLayout layout{};
+  uint32_t prog_bytes = 0;  // DevInsn part of the image
 };
 
 // Decoder entry point (ks_decode.cpp). Returns KS_OK or a KS_ERR_* code and
@@ -112,10 +164,13 @@ struct KsBufDev {
 // Everything one interpreter launch needs, passed by value as the kernel
 // argument (about 0.6 KB).
 struct KsLaunch {
-  const uint8_t* image;  // device: insns then constants
+  const uint8_t* image;  // device: DevInsn program then constant row values
   uint32_t image_bytes;  // multiple of 16
+  uint32_t prog_bytes;   // DevInsn part
   uint32_t n_insn;
   uint32_t n_slots;
+  uint32_t n_crows;
+  DevLayout layout;
   uint32_t grid, block, wpc;  // simulated grid, block, warps per simulated CTA
   uint32_t n_warps;           // grid * wpc
   uint32_t lat[KS_NUM_LAT_CLASSES];
@@ -134,7 +189,9 @@ struct KsLaunch {
 };
 
 // Shared-memory footprint of one real CTA of `warps` warps.
-size_t interp_smem_bytes(uint32_t image_bytes, uint32_t n_slots, uint32_t warps);
+size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t warps);
+// Offset of the first warp region in shared memory.
+uint32_t interp_region0(uint32_t image_bytes);
 
 // Launchers (ks_interp.cu). Return a cudaError_t value.
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);

@@ -8,18 +8,28 @@
 // while the simulated grid and block only change what %tid/%ctaid read.
 //
 // Per real CTA, shared memory holds
-//   [program image | mbarrier | parameter block | latency table]
-//   [register file: slot-major, one 32-bit word per real thread per slot]
-//   [per warp: 128-entry ready-time table | 32-entry reconvergence stack].
-// The program image (decoded instructions + constant pool) is staged once per
-// CTA with one cp.async.bulk global->shared copy completing on an mbarrier;
-// the wait is bounded and reports KS_ST_TIMEOUT instead of hanging.
+//   [program: 64-byte DevInsn records | constant row values]
+//   [parameter block | mbarrier]
+//   [one region per warp: register rows | constant rows | zero row |
+//    ready-time table | reconvergence stack]   (layout in ks_internal.h)
+// The program image is staged once per CTA with one cp.async.bulk
+// global->shared copy completing on an mbarrier; the wait is bounded and
+// reports KS_ST_TIMEOUT instead of hanging. The launch's latency table is then
+// patched into the staged instructions.
+//
+// Every operand field of an instruction is the offset of a 128-byte row of the
+// warp's region, so lane l reads an operand with one shared load at
+// (region + offset + 4l): registers, constants (replicated across the row) and
+// "no operand" (the zero row) look the same. All operand and ready-time loads
+// of an instruction are issued together right after the fetch.
 //
 // Warp-uniform state (pc, active mask, scoreboard clock, counters) lives in
 // registers, identical in every lane; values every lane must agree on (ready
 // times, stack entries) are written by all lanes with the same value, so each
 // lane only ever reads back its own store. Predicates are per-warp ballot
-// masks, predicate p held by lane p and read with a shuffle.
+// masks, predicate p held by lane p (lane 31 holds the always-true predicate)
+// and read with a shuffle. The scoreboard clock is 32-bit relative to a 64-bit
+// epoch that moves forward before any clock reaches 2^31.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -31,10 +41,6 @@ namespace ks {
 namespace {
 
 constexpr uint32_t FULL = 0xFFFFFFFFu;
-constexpr uint32_t HDR_BYTES = 384;  // mbarrier 16 + params 256 + latency table 32, padded
-constexpr uint32_t HDR_PARAMS = 16;
-constexpr uint32_t HDR_LAT = 16 + KS_MAX_PARAM_BYTES;
-constexpr uint32_t STACK_ENTRIES = KS_MAX_STACK;
 constexpr uint32_t WAIT_SPINS = 1u << 22;
 
 __device__ __forceinline__ uint32_t cvta_shared(const void* p) {
@@ -85,8 +91,6 @@ __device__ __forceinline__ bool wait_staged(uint64_t* bar) {
 __device__ __forceinline__ uint32_t fbits(float f) {
   return (f != f) ? 0x7FFFFFFFu : __float_as_uint(f);  // canonical NaN
 }
-
-__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
 __device__ __forceinline__ uint64_t f2i(float f, uint32_t flags) {
   if (f != f) return 0;
@@ -162,6 +166,24 @@ __device__ __forceinline__ int translate(const KsLaunch& L, uint64_t va, uint32_
   return KS_ST_OOB;
 }
 
+// Predicated 32-bit shared store (no branch around the per-lane condition).
+__device__ __forceinline__ void st_shared_if(bool p, uint32_t addr, uint32_t v) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t@q st.shared.u32 [%1], %2;\n\t}" ::"r"((uint32_t)p),
+      "r"(addr), "r"(v)
+      : "memory");
+}
+
+#define SM32(off) (*reinterpret_cast<uint32_t*>(smem + (off)))
+#define SM64(off) (*reinterpret_cast<uint64_t*>(smem + (off)))
+
+constexpr uint32_t REBASE_AT = 1u << 30;
+constexpr uint64_t BUDGET_CHUNK = 1ull << 30;
+
+__host__ __device__ __forceinline__ uint32_t region0(uint32_t image_bytes) {
+  return (image_bytes + KS_MAX_PARAM_BYTES + 16u + 127u) / 128u * 128u;
+}
+
 __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32_t mask) {
   return (uint64_t)(pc & 0xFFFFu) | ((uint64_t)(rpc & 0xFFFFu) << 16) | ((uint64_t)mask << 32);
 }
@@ -173,15 +195,14 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
   const uint32_t nwarps = blockDim.x >> 5;
-  const uint32_t stride = blockDim.x;  // register-file slot stride (words)
+  const DevLayout& Y = L.layout;
 
-  uint8_t* s_image = smem;
-  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.image_bytes);
-  uint8_t* s_params = smem + L.image_bytes + HDR_PARAMS;
-  uint32_t* s_lat = reinterpret_cast<uint32_t*>(smem + L.image_bytes + HDR_LAT);
-  uint32_t* s_rf = reinterpret_cast<uint32_t*>(smem + L.image_bytes + HDR_BYTES);
-  uint64_t* s_ready = reinterpret_cast<uint64_t*>(s_rf + (size_t)L.n_slots * stride);
-  uint64_t* s_stack = s_ready + (size_t)nwarps * KS_HZ_ENTRIES;
+  uint8_t* s_params = smem + L.image_bytes;
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.image_bytes + KS_MAX_PARAM_BYTES);
+  const uint32_t wb = region0(L.image_bytes) + wid * Y.region_bytes;  // this warp's region
+  const uint32_t lb = wb + lane * 4u;                                  // this lane's column in it
+  const uint32_t pg = wb + Y.ready_off + Y.n_slots * 4u;                // predicate ready entries
+  const uint32_t s_lane = cvta_shared(smem) + lb;                       // shared-window address of lb
 
   // ---- stage the program once per CTA (a1) ----
   if (threadIdx.x == 0) {
@@ -191,33 +212,31 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
   __syncthreads();
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(s_bar, L.image_bytes);
-    bulk_copy_g2s(s_image, L.image, L.image_bytes, s_bar);
+    bulk_copy_g2s(smem, L.image, L.image_bytes, s_bar);
   }
   for (uint32_t i = threadIdx.x; i < KS_MAX_PARAM_BYTES / 4; i += blockDim.x)
     reinterpret_cast<uint32_t*>(s_params)[i] = reinterpret_cast<const uint32_t*>(L.params)[i];
-  if (threadIdx.x < KS_NUM_LAT_CLASSES) s_lat[threadIdx.x] = L.lat[threadIdx.x];
   const bool staged = __all_sync(FULL, wait_staged(s_bar));
   __syncthreads();
+  // patch this launch's latencies into the program
+  if (staged) {
+    for (uint32_t i = threadIdx.x; i <= L.n_insn; i += blockDim.x) {
+      DevInsn* p = reinterpret_cast<DevInsn*>(smem) + i;
+      const uint32_t f = p->wlat, lat = L.lat[f & 0xFFu];
+      p->wlat = (f & DEV_HAS_DEST) ? lat : 0u;
+      p->dlat = (f & DEV_IS_STORE) ? lat : 0u;
+      p->nlat = p->inc ? ((f & DEV_IS_CTRL) ? lat : 1u) : 0u;
+    }
+  }
+  // constant rows and the zero row of this warp's region (read-only afterwards)
+  {
+    const uint32_t* vals = reinterpret_cast<const uint32_t*>(smem + L.prog_bytes);
+    for (uint32_t r = 0; r < Y.n_crows; r++) SM32(lb + Y.const_off + r * 128u) = vals[r];
+    SM32(lb + Y.zero_off) = 0u;
+  }
+  __syncthreads();
 
-  const KsInsn* prog = reinterpret_cast<const KsInsn*>(s_image);
-  const uint64_t* cpool = reinterpret_cast<const uint64_t*>(s_image + (size_t)L.n_insn * sizeof(KsInsn));
-  uint32_t* rf = s_rf + threadIdx.x;
-  uint64_t* ready = s_ready + (size_t)wid * KS_HZ_ENTRIES;
-  uint64_t* stk = s_stack + (size_t)wid * STACK_ENTRIES;
   const uint32_t exit_pc = L.n_insn;
-
-#define RD32(o) (((o) & KS_CONST_BIT) ? (uint32_t)cpool[(o) & 0x7Fu] : rf[(uint32_t)(o) * stride])
-#define RD64(o)                                                   \
-  (((o) & KS_CONST_BIT) ? cpool[(o) & 0x7Fu]                      \
-                        : ((uint64_t)rf[(uint32_t)(o) * stride] | \
-                           ((uint64_t)rf[((uint32_t)(o) + 1u) * stride] << 32)))
-#define WR32(o, v) (rf[(uint32_t)(o) * stride] = (v))
-#define WR64(o, v)                                         \
-  do {                                                     \
-    const uint64_t v_ = (v);                               \
-    rf[(uint32_t)(o) * stride] = (uint32_t)v_;             \
-    rf[((uint32_t)(o) + 1u) * stride] = (uint32_t)(v_ >> 32); \
-  } while (0)
 
   for (uint32_t gw = blockIdx.x * nwarps + wid; gw < L.n_warps; gw += gridDim.x * nwarps) {
     const uint32_t cta = gw / L.wpc;
@@ -225,122 +244,175 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
     const uint32_t tid_sim = wic * 32u + lane;
 
     // ---- warp set-up (a1): registers zero, predicates false, clock 0 ----
-    for (uint32_t s = 0; s < L.n_slots; s++) rf[s * stride] = 0u;
-    for (uint32_t i = lane; i < KS_HZ_ENTRIES; i += 32) ready[i] = 0ull;
-    uint32_t my_pred = 0;
+    for (uint32_t s = 0; s < Y.n_slots; s++) SM32(lb + s * 128u) = 0u;
+    for (uint32_t i = lane; i < Y.n_slots + 33u; i += 32u) SM32(wb + Y.ready_off + i * 4u) = 0u;
+    __syncwarp();
+    uint32_t my_pred = (lane == 31u) ? 0xFFFFFFFFu : 0u;  // predicate 31 is always true
     uint32_t pc = 0, rpc = exit_pc;
     uint32_t mask = __ballot_sync(FULL, tid_sim < L.block);
     uint32_t depth = 1, max_depth = 1;
-    uint64_t t_next = 0, t_last = 0, max_ready = 0, drain = 0;
-    uint64_t warp_insts = 0, thread_insts = 0;
+    uint64_t epoch = 0;
+    uint32_t t_next = 0, t_last = 0, max_ready = 0, drain = 0;
+    uint64_t thread_insts = 0;
     uint64_t ld_req = 0, ld_sec = 0, st_req = 0, st_sec = 0, ld_lin = 0, st_lin = 0;
     uint32_t n_events = 0, n_rec = 0, n_dropped = 0;
     int status = staged ? 0 : KS_ST_TIMEOUT;
     uint8_t* slot = L.trace ? L.trace + (uint64_t)gw * L.slot_bytes : nullptr;
+    const bool injected = L.inject_warp >= 0 && (uint64_t)L.inject_warp == gw;
+    const uint64_t stop_at = (injected && L.inject_step < L.step_limit) ? L.inject_step : L.step_limit;
+    // Issued-instruction accounting: `budget` counts down the instructions
+    // that may issue before the next check point (chunks of at most 2^30),
+    // `left` those after it; issued = stop_at - left - budget. thread_insts
+    // is accumulated at every active-mask change from the instructions issued
+    // since `mark` (a budget value) times the lanes of the mask they ran with.
+    uint32_t budget = (uint32_t)(stop_at < BUDGET_CHUNK ? stop_at : BUDGET_CHUNK);
+    uint64_t left = stop_at - budget;
+    uint32_t mark = budget;
+#define FLUSH_THREADS()                                            \
+  do {                                                             \
+    thread_insts += (uint64_t)(mark - budget) * (uint64_t)__popc(mask); \
+    mark = budget;                                                 \
+  } while (0)
 
-    while (status == 0) {
-      // pop finished entries (a6)
-      if (pc == rpc || mask == 0) {
+    if (status == 0) for (;;) {
+      // pop finished entries (a6); every control condition below is warp-uniform
+      // in value, and the votes make that visible to the compiler
+      if (__any_sync(FULL, pc == rpc || mask == 0)) {
+        FLUSH_THREADS();
         if (depth == 1) break;
         depth--;
-        const uint64_t e = stk[depth - 1];
+        const uint64_t e = SM64(wb + Y.stack_off + (depth - 1) * 8u);
         pc = (uint32_t)(e & 0xFFFFu);
         rpc = (uint32_t)((e >> 16) & 0xFFFFu);
         mask = (uint32_t)(e >> 32);
         continue;
       }
-      if (pc >= exit_pc) {  // reached the virtual exit: the remaining lanes finish
-        mask = 0;
+      // fetch (a2) and every operand / ready-time load of the instruction at once
+      const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
+      const uint4 q0 = ip[0], q1 = ip[1], q2 = ip[2], q3 = ip[3];
+      const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q0.y, gneg = q0.z, inc = q0.w;
+      const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q1.w;
+      const uint32_t aux = q3.w;
+      const uint32_t a0 = SM32(lb + A), b0 = SM32(lb + B), c0 = SM32(lb + C);
+      const uint32_t ra = SM32(wb + q2.x), rb = SM32(wb + q2.y), rc = SM32(wb + q2.z), rd = SM32(wb + q2.w);
+      const uint32_t rg = SM32(pg + guard * 4u);
+      const uint32_t pm = __shfl_sync(FULL, my_pred, guard);
+
+      if (__any_sync(FULL, inc == 0u || budget == 0u || t_next >= REBASE_AT)) {  // rare path
+        if (op == OP_EVENT) {  // trace record (a7), zero cost
+          if (n_events != 0xFFFFFFFFu) n_events++;
+          if (n_rec < L.max_ts) {
+            if (slot && lane == 0)
+              *reinterpret_cast<uint32_t*>(slot + 16 + 4 * n_rec) =
+                  ((aux & 0xFFu) << 24) | (((uint32_t)epoch + t_next) & 0xFFFFFFu);
+            n_rec++;
+          } else if (n_dropped < 0xFFFFu) {
+            n_dropped++;
+          }
+          pc++;
+          continue;
+        }
+        if (op == OP_EXIT) {  // reached the virtual exit: the remaining lanes finish
+          FLUSH_THREADS();
+          mask = 0;
+          continue;
+        }
+        if (t_next >= REBASE_AT) {  // keep every clock below 2^31: move the epoch to t_last
+          const uint32_t delta = t_last;
+          for (uint32_t i = lane; i < Y.n_slots + 33u; i += 32u) {
+            const uint32_t e = SM32(wb + Y.ready_off + i * 4u);
+            SM32(wb + Y.ready_off + i * 4u) = e > delta ? e - delta : 0u;
+          }
+          __syncwarp();
+          epoch += delta;
+          t_last = 0;
+          t_next -= delta;
+          max_ready = max_ready > delta ? max_ready - delta : 0u;
+          drain = drain > delta ? drain - delta : 0u;
+          continue;  // reload the ready times
+        }
+        // budget == 0: a stop, or the next chunk
+        FLUSH_THREADS();
+        if (left == 0) {
+          status = (injected && stop_at - left - budget == L.inject_step) ? KS_ST_INJECTED : KS_ST_STEP_LIMIT;
+          break;
+        }
+        budget = (uint32_t)(left < BUDGET_CHUNK ? left : BUDGET_CHUNK);
+        left -= budget;
+        mark = budget;
         continue;
       }
-      // fetch (a2)
-      const uint4 w0 = reinterpret_cast<const uint4*>(prog + pc)[0];
-      const uint4 w1 = reinterpret_cast<const uint4*>(prog + pc)[1];
-      const uint32_t op = w0.x & 0xFFu;
-      if (op == OP_EVENT) {  // trace record (a7), zero cost
-        const uint32_t ev = w0.w >> 16;
-        if (n_events != 0xFFFFFFFFu) n_events++;
-        if (n_rec < L.max_ts) {
-          if (slot && lane == 0)
-            *reinterpret_cast<uint32_t*>(slot + 16 + 4 * n_rec) =
-                ((ev & 0xFFu) << 24) | (uint32_t)(t_next & 0xFFFFFFull);
-          n_rec++;
-        } else if (n_dropped < 0xFFFFu) {
-          n_dropped++;
-        }
+
+      // issue: in-order scoreboard (a3), epoch-relative 32-bit clock
+      uint32_t t = max(max(max(t_next, ra), max(rb, rc)), max(rd, rg));
+      const uint32_t wr = t + q3.x;
+      SM32(wb + q2.w) = wr;
+      max_ready = max(max_ready, wr);
+      drain = max(drain, t + q3.y);
+      t_last = t;
+      t_next = t + q3.z;
+      budget--;
+
+      // guard (a2)
+      const uint32_t exec = mask & (pm ^ gneg);
+      const bool on = (exec >> lane) & 1u;
+      // high words of 64-bit operands, loaded by the handlers that need them
+#define A64() ((uint64_t)a0 | ((uint64_t)SM32(lb + A + 128u) << 32))
+#define B64() ((uint64_t)b0 | ((uint64_t)SM32(lb + B + 128u) << 32))
+#define C64() ((uint64_t)c0 | ((uint64_t)SM32(lb + C + 128u) << 32))
+
+#define W32(v) st_shared_if(on, s_lane + D, (v))
+#define W64(v)                                           \
+  do {                                                   \
+    const uint64_t v_ = (v);                             \
+    st_shared_if(on, s_lane + D, (uint32_t)v_);          \
+    st_shared_if(on, s_lane + D + 128u, (uint32_t)(v_ >> 32)); \
+  } while (0)
+
+      // unified datapaths, no dispatch branch (routing chosen by the decoder)
+      if (__all_sync(FULL, op == DOP_FPU)) {
+        W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))));
         pc++;
         continue;
       }
-      if (L.inject_warp >= 0 && (uint64_t)L.inject_warp == gw && warp_insts == L.inject_step) {
-        status = KS_ST_INJECTED;
-        break;
+      if (__all_sync(FULL, op == DOP_IMAD)) {
+        W32(a0 * b0 + ((c0 ^ aux) - aux));
+        pc++;
+        continue;
       }
-      if (warp_insts == L.step_limit) {
-        status = KS_ST_STEP_LIMIT;
-        break;
-      }
-      const uint32_t latc = (w0.x >> 8) & 0xFFu;
-      const uint32_t guard = (w0.x >> 16) & 0xFFu;
-      const uint32_t gneg = w0.x >> 24;
-      const uint32_t d = w0.y & 0xFFu, a = (w0.y >> 8) & 0xFFu, b = (w0.y >> 16) & 0xFFu, c = w0.y >> 24;
-      const uint32_t hd = w0.z & 0xFFu;
-      const uint32_t flags = (w0.w >> 8) & 0xFFu;
-      const uint64_t imm = (uint64_t)w1.x | ((uint64_t)w1.y << 32);
-
-      // issue: in-order scoreboard (a3)
-      uint64_t t = t_next;
-      t = umax64(t, ready[(w0.z >> 8) & 0xFFu]);
-      t = umax64(t, ready[(w0.z >> 16) & 0xFFu]);
-      t = umax64(t, ready[w0.z >> 24]);
-      t = umax64(t, ready[w0.w & 0xFFu]);
-      t = umax64(t, ready[hd]);
-      const uint64_t lat = s_lat[latc];
-      if (hd != KS_HZ_NONE) {
-        ready[hd] = t + lat;
-        max_ready = umax64(max_ready, t + lat);
-      }
-      if (op == OP_STG32 || op == OP_STG64) drain = umax64(drain, t + lat);
-      t_last = t;
-      t_next = (op == OP_BRA || op == OP_RET) ? t + lat : t + 1;
-      warp_insts++;
-      thread_insts += (uint64_t)__popc(mask);
-
-      // guard (a2)
-      uint32_t exec = mask;
-      if (guard != KS_NO_GUARD) {
-        const uint32_t pm = __shfl_sync(FULL, my_pred, guard);
-        exec &= gneg ? ~pm : pm;
-      }
-      const bool on = (exec >> lane) & 1u;
 
       switch (op) {
         // ---- control (a6) ----
         case OP_BRA: {
-          const uint32_t target = w1.z, R = w1.w;
+          const uint32_t target = aux & 0xFFFFu, R = aux >> 16;
           const uint32_t taken = exec, fall = mask & ~exec;
           if (fall == 0) {
             pc = target;
           } else if (taken == 0) {
             pc = pc + 1;
           } else {
-            uint32_t n = depth;  // entries after the top is resolved, all in shared memory
+            FLUSH_THREADS();
+            const uint32_t sbase = wb + Y.stack_off;
+            uint32_t n = depth;  // entries held in shared memory once the top is resolved
             if (rpc == R) {
               n = depth - 1;  // the top already waits at R below: replace it
             } else {
-              stk[depth - 1] = pack_entry(R, rpc, mask);
+              SM64(sbase + (depth - 1) * 8u) = pack_entry(R, rpc, mask);
             }
             if (target != R) {
               if (n >= L.stack_depth) { status = KS_ST_SIMT_STACK; break; }
-              stk[n++] = pack_entry(target, R, taken);
+              SM64(sbase + n * 8u) = pack_entry(target, R, taken);
+              n++;
             }
             if (pc + 1 != R) {
               if (n >= L.stack_depth) { status = KS_ST_SIMT_STACK; break; }
-              stk[n++] = pack_entry(pc + 1, R, fall);
+              SM64(sbase + n * 8u) = pack_entry(pc + 1, R, fall);
+              n++;
             }
             if (n == 0) { depth = 1; pc = rpc = exit_pc; mask = 0; break; }
             depth = n;
             max_depth = max(max_depth, depth);
-            const uint64_t e = stk[depth - 1];
+            const uint64_t e = SM64(sbase + (depth - 1) * 8u);
             pc = (uint32_t)(e & 0xFFFFu);
             rpc = (uint32_t)((e >> 16) & 0xFFFFu);
             mask = (uint32_t)(e >> 32);
@@ -348,29 +420,23 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
           break;
         }
         case OP_RET: {
-          for (uint32_t i = 0; i + 1 < depth; i++) stk[i] &= ~((uint64_t)exec << 32);
+          FLUSH_THREADS();
+          for (uint32_t i = 0; i + 1 < depth; i++) {
+            const uint32_t at = wb + Y.stack_off + i * 8u;
+            SM64(at) = SM64(at) & ~((uint64_t)exec << 32);
+          }
           mask &= ~exec;
           pc++;
           break;
         }
         // ---- memory (a5) ----
-        case OP_LDP32: {
-          const uint32_t v = *reinterpret_cast<const uint32_t*>(s_params + imm);
-          if (on) WR32(d, v);
-          pc++;
-          break;
-        }
-        case OP_LDP64: {
-          const uint64_t v = *reinterpret_cast<const uint64_t*>(s_params + imm);
-          if (on) WR64(d, v);
-          pc++;
-          break;
-        }
+        case OP_LDP32: W32(*reinterpret_cast<const uint32_t*>(s_params + aux)); pc++; break;
+        case OP_LDP64: W64(*reinterpret_cast<const uint64_t*>(s_params + aux)); pc++; break;
         case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64: {
           const bool wide = (op == OP_LDG64 || op == OP_STG64);
           const bool is_ld = (op == OP_LDG32 || op == OP_LDG64);
           const uint32_t size = wide ? 8u : 4u;
-          const uint64_t va = RD64(a) + imm;
+          const uint64_t va = A64() + (uint64_t)(int64_t)(int32_t)aux;
           uint8_t* ptr = nullptr;
           int err = 0;
           if (on) err = translate(L, va, size, &ptr);
@@ -389,26 +455,31 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
           }
           if (is_ld) {
             if (on) {
-              if (wide) WR64(d, *reinterpret_cast<const uint64_t*>(ptr));
-              else WR32(d, *reinterpret_cast<const uint32_t*>(ptr));
+              if (wide) {
+                const uint64_t v = *reinterpret_cast<const uint64_t*>(ptr);
+                SM32(lb + D) = (uint32_t)v;
+                SM32(lb + D + 128u) = (uint32_t)(v >> 32);
+              } else {
+                SM32(lb + D) = *reinterpret_cast<const uint32_t*>(ptr);
+              }
             }
           } else {
             // the highest lane writing an address wins
             const uint32_t mv = __match_any_sync(FULL, on ? va : ~0ull);
             if (on && (31u - __clz(mv)) == lane) {
-              if (wide) *reinterpret_cast<uint64_t*>(ptr) = RD64(b);
-              else *reinterpret_cast<uint32_t*>(ptr) = RD32(b);
+              if (wide) *reinterpret_cast<uint64_t*>(ptr) = B64();
+              else *reinterpret_cast<uint32_t*>(ptr) = b0;
             }
           }
           pc++;
           break;
         }
         // ---- moves and integer ALU (a4) ----
-        case OP_MOV32: { const uint32_t v = RD32(a); if (on) WR32(d, v); pc++; break; }
-        case OP_MOV64: { const uint64_t v = RD64(a); if (on) WR64(d, v); pc++; break; }
+        case OP_MOV32: W32(a0); pc++; break;
+        case OP_MOV64: W64(A64()); pc++; break;
         case OP_MOVSP: {
           uint32_t v;
-          switch ((uint32_t)imm) {
+          switch (aux) {
             case SP_TID: v = tid_sim; break;
             case SP_NTID: v = L.block; break;
             case SP_CTAID: v = cta; break;
@@ -417,118 +488,116 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
             case SP_ONE: v = 1; break;
             default: v = 0; break;
           }
-          if (on) WR32(d, v);
+          W32(v);
           pc++;
           break;
         }
-        case OP_ADD32: { const uint32_t v = RD32(a) + RD32(b); if (on) WR32(d, v); pc++; break; }
-        case OP_SUB32: { const uint32_t v = RD32(a) - RD32(b); if (on) WR32(d, v); pc++; break; }
-        case OP_MUL32: { const uint32_t v = RD32(a) * RD32(b); if (on) WR32(d, v); pc++; break; }
-        case OP_MAD32: { const uint32_t v = RD32(a) * RD32(b) + RD32(c); if (on) WR32(d, v); pc++; break; }
-        case OP_ADD64: { const uint64_t v = RD64(a) + RD64(b); if (on) WR64(d, v); pc++; break; }
-        case OP_SUB64: { const uint64_t v = RD64(a) - RD64(b); if (on) WR64(d, v); pc++; break; }
-        case OP_MUL64: { const uint64_t v = RD64(a) * RD64(b); if (on) WR64(d, v); pc++; break; }
-        case OP_MAD64: { const uint64_t v = RD64(a) * RD64(b) + RD64(c); if (on) WR64(d, v); pc++; break; }
-        case OP_AND32: { const uint32_t v = RD32(a) & RD32(b); if (on) WR32(d, v); pc++; break; }
-        case OP_OR32: { const uint32_t v = RD32(a) | RD32(b); if (on) WR32(d, v); pc++; break; }
-        case OP_XOR32: { const uint32_t v = RD32(a) ^ RD32(b); if (on) WR32(d, v); pc++; break; }
-        case OP_AND64: { const uint64_t v = RD64(a) & RD64(b); if (on) WR64(d, v); pc++; break; }
-        case OP_OR64: { const uint64_t v = RD64(a) | RD64(b); if (on) WR64(d, v); pc++; break; }
-        case OP_XOR64: { const uint64_t v = RD64(a) ^ RD64(b); if (on) WR64(d, v); pc++; break; }
-        case OP_SHL32: { const uint32_t s = RD32(b); const uint32_t v = s >= 32u ? 0u : RD32(a) << s; if (on) WR32(d, v); pc++; break; }
-        case OP_SHR32U: { const uint32_t s = RD32(b); const uint32_t v = s >= 32u ? 0u : RD32(a) >> s; if (on) WR32(d, v); pc++; break; }
-        case OP_SHR32S: {
-          const uint32_t s = RD32(b);
-          const int32_t x = (int32_t)RD32(a);
-          const uint32_t v = (uint32_t)(s >= 32u ? (x >> 31) : (x >> s));
-          if (on) WR32(d, v);
-          pc++;
-          break;
-        }
-        case OP_SHL64: { const uint32_t s = RD32(b); const uint64_t v = s >= 64u ? 0ull : RD64(a) << s; if (on) WR64(d, v); pc++; break; }
-        case OP_SHR64U: { const uint32_t s = RD32(b); const uint64_t v = s >= 64u ? 0ull : RD64(a) >> s; if (on) WR64(d, v); pc++; break; }
+        case OP_ADD32: W32(a0 + b0); pc++; break;
+        case OP_SUB32: W32(a0 - b0); pc++; break;
+        case OP_MUL32: W32(a0 * b0); pc++; break;
+        case OP_MAD32: W32(a0 * b0 + c0); pc++; break;
+        case OP_ADD64: W64(A64() + B64()); pc++; break;
+        case OP_SUB64: W64(A64() - B64()); pc++; break;
+        case OP_MUL64: W64(A64() * B64()); pc++; break;
+        case OP_MAD64: W64(A64() * B64() + C64()); pc++; break;
+        case OP_AND32: W32(a0 & b0); pc++; break;
+        case OP_OR32: W32(a0 | b0); pc++; break;
+        case OP_XOR32: W32(a0 ^ b0); pc++; break;
+        case OP_AND64: W64(A64() & B64()); pc++; break;
+        case OP_OR64: W64(A64() | B64()); pc++; break;
+        case OP_XOR64: W64(A64() ^ B64()); pc++; break;
+        case OP_SHL32: W32(b0 >= 32u ? 0u : a0 << b0); pc++; break;
+        case OP_SHR32U: W32(b0 >= 32u ? 0u : a0 >> b0); pc++; break;
+        case OP_SHR32S: W32((uint32_t)(b0 >= 32u ? ((int32_t)a0 >> 31) : ((int32_t)a0 >> b0))); pc++; break;
+        case OP_SHL64: W64(b0 >= 64u ? 0ull : A64() << b0); pc++; break;
+        case OP_SHR64U: W64(b0 >= 64u ? 0ull : A64() >> b0); pc++; break;
         case OP_SHR64S: {
-          const uint32_t s = RD32(b);
-          const int64_t x = (int64_t)RD64(a);
-          const uint64_t v = (uint64_t)(s >= 64u ? (x >> 63) : (x >> s));
-          if (on) WR64(d, v);
+          const int64_t x = (int64_t)A64();
+          W64((uint64_t)(b0 >= 64u ? (x >> 63) : (x >> b0)));
           pc++;
           break;
         }
         // ---- f32 (a4), IEEE round-to-nearest-even, canonical NaN ----
-        case OP_FADD: { const uint32_t v = fbits(__fadd_rn(__uint_as_float(RD32(a)), __uint_as_float(RD32(b)))); if (on) WR32(d, v); pc++; break; }
-        case OP_FSUB: { const uint32_t v = fbits(__fsub_rn(__uint_as_float(RD32(a)), __uint_as_float(RD32(b)))); if (on) WR32(d, v); pc++; break; }
-        case OP_FMUL: { const uint32_t v = fbits(__fmul_rn(__uint_as_float(RD32(a)), __uint_as_float(RD32(b)))); if (on) WR32(d, v); pc++; break; }
-        case OP_FFMA: {
-          const uint32_t v = fbits(__fmaf_rn(__uint_as_float(RD32(a)), __uint_as_float(RD32(b)), __uint_as_float(RD32(c))));
-          if (on) WR32(d, v);
+        case OP_FADD: W32(fbits(__fadd_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
+        case OP_FSUB: W32(fbits(__fsub_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
+        case OP_FMUL: W32(fbits(__fmul_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
+        case OP_FFMA:
+          W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0))));
           pc++;
           break;
-        }
-        case OP_FDIV: { const uint32_t v = fbits(__fdiv_rn(__uint_as_float(RD32(a)), __uint_as_float(RD32(b)))); if (on) WR32(d, v); pc++; break; }
-        case OP_FSQRT: { const uint32_t v = fbits(__fsqrt_rn(__uint_as_float(RD32(a)))); if (on) WR32(d, v); pc++; break; }
+        case OP_FDIV: W32(fbits(__fdiv_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
+        case OP_FSQRT: W32(fbits(__fsqrt_rn(__uint_as_float(a0)))); pc++; break;
         // ---- predicates ----
         case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32: {
+          const uint32_t cmp = aux & 0xFFu, pd = (aux >> 8) & 0xFFu;
           bool r;
-          if (op == OP_SETP_U32) r = cmp_u(RD32(a), RD32(b), flags);
-          else if (op == OP_SETP_S32) r = cmp_s((int32_t)RD32(a), (int32_t)RD32(b), flags);
-          else if (op == OP_SETP_U64) r = cmp_u(RD64(a), RD64(b), flags);
-          else if (op == OP_SETP_S64) r = cmp_s((int64_t)RD64(a), (int64_t)RD64(b), flags);
-          else r = cmp_f(__uint_as_float(RD32(a)), __uint_as_float(RD32(b)), flags);
+          if (op == OP_SETP_U32) r = cmp_u(a0, b0, cmp);
+          else if (op == OP_SETP_S32) r = cmp_s((int32_t)a0, (int32_t)b0, cmp);
+          else if (op == OP_SETP_U64) r = cmp_u(A64(), B64(), cmp);
+          else if (op == OP_SETP_S64) r = cmp_s((int64_t)A64(), (int64_t)B64(), cmp);
+          else r = cmp_f(__uint_as_float(a0), __uint_as_float(b0), cmp);
           const uint32_t bal = __ballot_sync(FULL, r);
-          const uint32_t old = __shfl_sync(FULL, my_pred, d);
-          if (lane == d) my_pred = (old & ~exec) | (bal & exec);
+          const uint32_t old = __shfl_sync(FULL, my_pred, pd);
+          if (lane == pd) my_pred = (old & ~exec) | (bal & exec);
           pc++;
           break;
         }
         case OP_ANDP: case OP_ORP: case OP_XORP: {
-          const uint32_t pa = __shfl_sync(FULL, my_pred, a);
-          const uint32_t pb = __shfl_sync(FULL, my_pred, b);
-          const uint32_t old = __shfl_sync(FULL, my_pred, d);
+          const uint32_t pa = __shfl_sync(FULL, my_pred, aux & 0xFFu);
+          const uint32_t pb = __shfl_sync(FULL, my_pred, (aux >> 8) & 0xFFu);
+          const uint32_t pd = (aux >> 16) & 0xFFu;
+          const uint32_t old = __shfl_sync(FULL, my_pred, pd);
           const uint32_t r = op == OP_ANDP ? (pa & pb) : op == OP_ORP ? (pa | pb) : (pa ^ pb);
-          if (lane == d) my_pred = (old & ~exec) | (r & exec);
+          if (lane == pd) my_pred = (old & ~exec) | (r & exec);
           pc++;
           break;
         }
         case OP_SELP32: {
-          const uint32_t pm = __shfl_sync(FULL, my_pred, c);
-          const uint32_t v = ((pm >> lane) & 1u) ? RD32(a) : RD32(b);
-          if (on) WR32(d, v);
+          const uint32_t sel = __shfl_sync(FULL, my_pred, aux);
+          W32(((sel >> lane) & 1u) ? a0 : b0);
           pc++;
           break;
         }
         case OP_SELP64: {
-          const uint32_t pm = __shfl_sync(FULL, my_pred, c);
-          const uint64_t v = ((pm >> lane) & 1u) ? RD64(a) : RD64(b);
-          if (on) WR64(d, v);
+          const uint32_t sel = __shfl_sync(FULL, my_pred, aux);
+          W64(((sel >> lane) & 1u) ? A64() : B64());
           pc++;
           break;
         }
         // ---- conversions ----
-        case OP_CVT_F32_U32: { const uint32_t v = __float_as_uint(__uint2float_rn(RD32(a))); if (on) WR32(d, v); pc++; break; }
-        case OP_CVT_F32_S32: { const uint32_t v = __float_as_uint(__int2float_rn((int32_t)RD32(a))); if (on) WR32(d, v); pc++; break; }
-        case OP_CVT_F32_U64: { const uint32_t v = __float_as_uint(__ull2float_rn(RD64(a))); if (on) WR32(d, v); pc++; break; }
-        case OP_CVT_F32_S64: { const uint32_t v = __float_as_uint(__ll2float_rn((long long)RD64(a))); if (on) WR32(d, v); pc++; break; }
+        case OP_CVT_F32_U32: W32(__float_as_uint(__uint2float_rn(a0))); pc++; break;
+        case OP_CVT_F32_S32: W32(__float_as_uint(__int2float_rn((int32_t)a0))); pc++; break;
+        case OP_CVT_F32_U64: W32(__float_as_uint(__ull2float_rn(A64()))); pc++; break;
+        case OP_CVT_F32_S64: W32(__float_as_uint(__ll2float_rn((long long)A64()))); pc++; break;
         case OP_CVT_F2I: {
-          const uint64_t v = f2i(__uint_as_float(RD32(a)), flags);
-          const uint32_t kind = flags & 15u;
-          if (on) {
-            if (kind == CVT_S64 || kind == CVT_U64) WR64(d, v);
-            else WR32(d, (uint32_t)v);
-          }
+          const uint64_t v = f2i(__uint_as_float(a0), aux);
+          const uint32_t kind = aux & 15u;
+          if (kind == CVT_S64 || kind == CVT_U64) W64(v);
+          else W32((uint32_t)v);
           pc++;
           break;
         }
-        case OP_CVT_ZX: { const uint64_t v = (uint64_t)RD32(a); if (on) WR64(d, v); pc++; break; }
-        case OP_CVT_SX: { const uint64_t v = (uint64_t)(int64_t)(int32_t)RD32(a); if (on) WR64(d, v); pc++; break; }
+        case OP_CVT_ZX: W64((uint64_t)a0); pc++; break;
+        case OP_CVT_SX: W64((uint64_t)(int64_t)(int32_t)a0); pc++; break;
         default:
           pc++;
           break;
       }
+#undef W32
+#undef W64
+#undef A64
+#undef B64
+#undef C64
+      if (status != 0) {
+        FLUSH_THREADS();
+        break;
+      }
     }
+#undef FLUSH_THREADS
+    const uint64_t warp_insts = stop_at - left - budget;
 
     // ---- write-back (a9) ----
-    const uint64_t cycles = warp_insts ? umax64(umax64(t_last + 1, max_ready), drain) : 0ull;
+    const uint64_t cycles = warp_insts ? epoch + (uint64_t)max(max(t_last + 1u, max_ready), drain) : 0ull;
     {
       uint64_t v = 0;
       switch (lane) {
@@ -557,11 +626,8 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
       }
       for (uint32_t i = 4 + n_rec + lane; i < words; i += 32) sw[i] = 0u;
     }
+    __syncwarp();
   }
-#undef RD32
-#undef RD64
-#undef WR32
-#undef WR64
   // Leave no copy in flight: if staging timed out, wait once more (bounded).
   if (!staged) (void)wait_staged(s_bar);
 }
@@ -608,9 +674,10 @@ __global__ void ks_reduce_kernel(const ks_warp_stats* __restrict__ s, uint64_t n
   }
 }
 
-size_t interp_smem_bytes(uint32_t image_bytes, uint32_t n_slots, uint32_t warps) {
-  return (size_t)image_bytes + HDR_BYTES + (size_t)n_slots * warps * 32 * 4 +
-         (size_t)warps * (KS_HZ_ENTRIES + STACK_ENTRIES) * 8;
+uint32_t interp_region0(uint32_t image_bytes) { return region0(image_bytes); }
+
+size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t warps) {
+  return (size_t)region0(image_bytes) + (size_t)region_bytes * warps;
 }
 
 static int g_attr_done[64];
@@ -639,7 +706,7 @@ int interp_occupancy(uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm)
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream) {
   int e = ensure_attr();
   if (e) return e;
-  const size_t smem = interp_smem_bytes(L.image_bytes, L.n_slots, real_warps_per_cta);
+  const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, real_warps_per_cta);
   ks_interp_kernel<<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
   return (int)cudaGetLastError();
 }

@@ -276,5 +276,15 @@ def test_jit_crosscheck_single_instructions(op, srcs, dst, kind):
     nat = jit_memory(w)[0]
     if dst == "f":
         assert nan_equivalent(sim, nat)
-    else:
-        assert np.array_equal(sim, nat)
+        return
+    if op.startswith("cvt.r") and op.endswith(("s64.f32", "u64.f32")):
+        # PTX ISA: float-to-integer conversion of NaN gives 0, which the
+        # simulator implements; the GB300 returns 0x8000000000000000 for NaN
+        # converted to a 64-bit integer (32-bit destinations give 0). Every
+        # other input must agree with the hardware.
+        isnan = np.isnan(np.array(ins[0], dtype=np.uint64).astype(np.uint32).view(np.float32))
+        s64, n64 = sim.view(np.uint64), nat.view(np.uint64)
+        assert np.all(s64[isnan] == 0)
+        assert np.array_equal(s64[~isnan], n64[~isnan])
+        return
+    assert np.array_equal(sim, nat)
