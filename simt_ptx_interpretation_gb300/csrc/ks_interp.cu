@@ -275,6 +275,40 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
   } while (0)
 
     if (status == 0) for (;;) {
+      // ---- fast path: runs of routed FPU / IMAD instructions with nothing
+      // pending (no reconvergence, no stop, no rebase). One basic block per
+      // instruction; the next instruction is fetched while this one executes.
+      {
+        const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
+        uint4 q0 = ip[0], q1 = ip[1], q2 = ip[2], q3 = ip[3];
+        while (__all_sync(FULL, (q0.x == DOP_FPU || q0.x == DOP_IMAD) && pc != rpc && mask != 0u && budget != 0u &&
+                                    t_next < REBASE_AT)) {
+          const uint32_t a0 = SM32(lb + q1.x), b0 = SM32(lb + q1.y), c0 = SM32(lb + q1.z);
+          const uint32_t ra = SM32(wb + q2.x), rb = SM32(wb + q2.y), rc = SM32(wb + q2.z), rd = SM32(wb + q2.w);
+          const uint32_t rg = SM32(pg + q0.y * 4u);
+          const uint32_t pm = __shfl_sync(FULL, my_pred, q0.y);
+          const uint4 n0 = ip[4], n1 = ip[5], n2 = ip[6], n3 = ip[7];  // instruction pc + 1 (<= sentinel)
+          const uint32_t t = max(max(max(t_next, ra), max(rb, rc)), max(rd, rg));
+          const uint32_t wr = t + q3.x;
+          SM32(wb + q2.w) = wr;
+          max_ready = max(max_ready, wr);
+          drain = max(drain, t + q3.y);
+          t_last = t;
+          t_next = t + q3.z;
+          budget--;
+          const bool on = ((mask & (pm ^ q0.z)) >> lane) & 1u;
+          const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ q3.w)));
+          const uint32_t ri = a0 * b0 + ((c0 ^ q3.w) - q3.w);
+          st_shared_if(on, s_lane + q1.w, q0.x == DOP_FPU ? rf : ri);
+          pc++;
+          ip += 4;
+          q0 = n0;
+          q1 = n1;
+          q2 = n2;
+          q3 = n3;
+        }
+      }
+      // ---- general path ----
       // pop finished entries (a6); every control condition below is warp-uniform
       // in value, and the votes make that visible to the compiler
       if (__any_sync(FULL, pc == rpc || mask == 0)) {
