@@ -1053,21 +1053,20 @@ class Decoder {
     DevLayout& Y = K.layout;
     Y.n_slots = K.n_slots;
     Y.n_crows = (uint32_t)rowval.size();
-    Y.const_off = K.n_slots * 128u;
-    Y.zero_off = Y.const_off + Y.n_crows * 128u;
-    Y.ready_off = Y.zero_off + 128u;
-    const uint32_t entries = K.n_slots + 32u + 1u;
-    Y.sink_off = Y.ready_off + (K.n_slots + 32u) * 4u;
-    Y.stack_off = Y.ready_off + (entries * 4u + 127u) / 128u * 128u;
+    Y.const_off = K.n_slots * ROW_BYTES;
+    Y.zero_off = Y.const_off + Y.n_crows * ROW_BYTES;
+    Y.pred_off = Y.zero_off + ROW_BYTES;
+    Y.stack_off = Y.pred_off + 256u;
     Y.region_bytes = Y.stack_off + KS_MAX_STACK * 8u;
 
     auto row_of = [&](uint8_t o) -> uint32_t {
-      return (o & KS_CONST_BIT) ? Y.const_off + crow[o & 0x7F] * 128u : (uint32_t)o * 128u;
+      return (o & KS_CONST_BIT) ? Y.const_off + crow[o & 0x7F] * ROW_BYTES : (uint32_t)o * ROW_BYTES;
     };
-    auto hz = [&](uint8_t h) -> uint32_t {
-      if (h == KS_HZ_NONE) return Y.pred_entry(31);
-      if (h >= KS_HZ_PRED0) return Y.pred_entry(h - KS_HZ_PRED0);
-      return Y.ready_off + (uint32_t)h * 4u;
+    // predicate hazards live in the predicate table; register hazards travel
+    // with the register rows themselves
+    auto phz = [&](uint8_t h) -> uint32_t {
+      if (h != KS_HZ_NONE && h >= KS_HZ_PRED0) return Y.pred_entry(h - KS_HZ_PRED0);
+      return Y.pred_entry(31);
     };
     std::vector<DevInsn> dev(n + 1);
     for (size_t i = 0; i <= n; i++) {
@@ -1075,15 +1074,14 @@ class Decoder {
       std::memset(&o, 0, sizeof o);
       o.guard = 31;
       o.a = o.b = o.c = o.d = Y.zero_off;
-      o.ha = o.hb = o.hc = Y.pred_entry(31);
-      o.hd = Y.sink_off;
+      o.ha = o.hb = o.hc = o.hd = Y.pred_entry(31);
       if (i == n) {  // exit sentinel
         o.op = OP_EXIT;
         continue;
       }
       const KsInsn& in = K.code[i];
       o.op = fpu_family(in.op) ? DOP_FPU : imad_family(in.op) ? DOP_IMAD : in.op;
-      o.inc = in.op == OP_EVENT ? 0u : 1u;
+      o.inc = in.op == OP_EVENT ? 0u : INC_ISSUE;
       if (in.guard != KS_NO_GUARD) {
         o.guard = in.guard;
         o.gneg = in.gneg ? 0xFFFFFFFFu : 0u;
@@ -1094,10 +1092,14 @@ class Decoder {
         if (routed_width(in, p)) *rows[p] = row_of(ops[p]);
       if (o.op == DOP_FPU || o.op == DOP_IMAD) o.aux = route[i].aux;
       if (in.op != OP_EVENT) {
-        o.ha = hz(in.ha);
-        o.hb = hz(in.hb);
-        o.hc = hz(in.hc);
-        o.hd = in.hd == KS_HZ_NONE ? Y.sink_off : hz(in.hd);
+        o.ha = phz(in.ha);
+        o.hb = phz(in.hb);
+        o.hc = phz(in.hc);
+        if (in.hd != KS_HZ_NONE && in.hd >= KS_HZ_PRED0) {
+          o.hd = Y.pred_entry(in.hd - KS_HZ_PRED0);
+          o.inc |= INC_PDEST;
+        }
+        if (routed_width(in, 3)) o.inc |= INC_RDEST;
         o.wlat = (uint32_t)in.lat;
         if (in.hd != KS_HZ_NONE) o.wlat |= DEV_HAS_DEST;
         if (in.op == OP_STG32 || in.op == OP_STG64) o.wlat |= DEV_IS_STORE;

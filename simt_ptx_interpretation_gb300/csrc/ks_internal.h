@@ -79,26 +79,30 @@ static_assert(sizeof(KsInsn) == 32, "KsInsn must be 32 bytes");
 
 // ---- device program format ---------------------------------------------
 // The host resolves every KsInsn into a 64-byte DevInsn whose operand fields
-// are byte offsets inside a warp's shared-memory region, so the interpreter
-// reads each operand with one shared load at (lane base + offset):
+// are byte offsets of rows inside a warp's shared-memory region. A row holds
+// one 8-byte pair per lane: (value, ready), where `ready` is the simulated
+// cycle at which the register becomes available (the same in every lane), so
+// one 64-bit shared load returns both an operand and its scoreboard entry:
 //
-//   warp region: [register rows: n_slots x 128 B]   row s = slot s, word l = lane l
-//                [constant rows: n_crows x 128 B]   the constant replicated per lane
-//                [zero row: 128 B]                  operand "none"
-//                [ready table: n_slots + 32 + 1 u32, padded to 128 B]
-//                    entry s: slot s; n_slots + p: predicate p (p = 31 is the
-//                    always-true predicate and stays 0); last: write sink
+//   warp region: [register rows: n_slots x 256 B]   row s = slot s
+//                [constant rows: n_crows x 256 B]   (constant, 0) in every lane
+//                [zero row: 256 B]                  operand "none": (0, 0), never written
+//                [predicate ready table: 32 u32, padded to 256 B]
+//                    entry p: predicate p (p = 31 is the always-true predicate and stays 0)
 //                [reconvergence stack: 32 x 8 B]
 //
 // A 64-bit register or constant uses two consecutive rows (low word first),
-// so its high word is at offset + 128.
+// so its high word is at row offset + 256.
+constexpr uint32_t ROW_BYTES = 256;
+
 struct alignas(16) DevInsn {
   uint32_t op;
   uint32_t guard;  // predicate lane 0..30, or 31 (always true)
   uint32_t gneg;   // 0 or 0xFFFFFFFF
-  uint32_t inc;    // 1 for an issued instruction, 0 for a trace pseudo-op or the exit sentinel
-  uint32_t a, b, c, d;       // operand row offsets (region-relative)
-  uint32_t ha, hb, hc, hd;   // ready-table entry offsets (region-relative); hd = sink if no dest
+  uint32_t inc;    // bit 0: issued (0 for a trace pseudo-op or the exit sentinel);
+                   // bit 1: has a register destination; bit 2: has a predicate destination
+  uint32_t a, b, c, d;       // row offsets (region-relative); the zero row if absent
+  uint32_t ha, hb, hc, hd;   // predicate-table offsets of predicate sources / destination (entry 31 if absent)
   uint32_t wlat;   // in the image: latency class | flags (below); patched to dest latency
   uint32_t dlat;   // patched: store completion latency (0 if not a store)
   uint32_t nlat;   // patched: issue-clock advance (latency for bra/ret, 1 otherwise, 0 if inc == 0)
@@ -110,6 +114,8 @@ static_assert(sizeof(DevInsn) == 64, "DevInsn must be 64 bytes");
 constexpr uint32_t DEV_HAS_DEST = 1u << 8;
 constexpr uint32_t DEV_IS_STORE = 1u << 9;
 constexpr uint32_t DEV_IS_CTRL = 1u << 10;
+// bits of DevInsn::inc
+constexpr uint32_t INC_ISSUE = 1u, INC_RDEST = 2u, INC_PDEST = 4u;
 constexpr uint32_t OP_EXIT = 0xFE;  // sentinel at index n_insn: the remaining lanes finish
 // Unified datapaths selected at resolve time (DevInsn::op only):
 //   DOP_FPU:  d = fma.rn(a, b, c ^ aux)      add: b = 1.0, c = y;  sub: b = 1.0, c = y, aux = sign bit;
@@ -121,8 +127,8 @@ constexpr uint32_t DOP_IMAD = 0x41;
 
 struct DevLayout {
   uint32_t n_slots, n_crows;
-  uint32_t const_off, zero_off, ready_off, sink_off, stack_off, region_bytes;
-  uint32_t pred_entry(uint32_t p) const { return ready_off + (n_slots + p) * 4u; }
+  uint32_t const_off, zero_off, pred_off, stack_off, region_bytes;
+  uint32_t pred_entry(uint32_t p) const { return pred_off + p * 4u; }
 };
 
 struct KsParam {

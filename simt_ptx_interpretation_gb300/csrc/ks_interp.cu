@@ -174,7 +174,19 @@ __device__ __forceinline__ void st_shared_if(bool p, uint32_t addr, uint32_t v) 
       : "memory");
 }
 
+// Stores (value, ready) for a lane that executes and only `ready` for one
+// that does not (the scoreboard entry is written in every lane).
+__device__ __forceinline__ void st_pair(bool on, uint32_t addr, uint32_t v, uint32_t ready) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t"
+      "@q st.shared.v2.u32 [%1], {%2, %3};\n\t"
+      "@!q st.shared.u32 [%1+4], %3;\n\t}" ::"r"((uint32_t)on),
+      "r"(addr), "r"(v), "r"(ready)
+      : "memory");
+}
+
 #define SM32(off) (*reinterpret_cast<uint32_t*>(smem + (off)))
+#define SM2(off) (*reinterpret_cast<const uint2*>(smem + (off)))
 #define SM64(off) (*reinterpret_cast<uint64_t*>(smem + (off)))
 
 constexpr uint32_t REBASE_AT = 1u << 30;
@@ -190,7 +202,7 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 
 }  // namespace
 
-__global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ KsLaunch L) {
+__global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant__ KsLaunch L) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
@@ -200,9 +212,9 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
   uint8_t* s_params = smem + L.image_bytes;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.image_bytes + KS_MAX_PARAM_BYTES);
   const uint32_t wb = region0(L.image_bytes) + wid * Y.region_bytes;  // this warp's region
-  const uint32_t lb = wb + lane * 4u;                                  // this lane's column in it
-  const uint32_t pg = wb + Y.ready_off + Y.n_slots * 4u;                // predicate ready entries
-  const uint32_t s_lane = cvta_shared(smem) + lb;                       // shared-window address of lb
+  const uint32_t lb = wb + lane * 8u;                                  // this lane's pair in row 0
+  const uint32_t pg = wb + Y.pred_off;                                 // predicate ready table
+  const uint32_t s_lane = cvta_shared(smem) + lb;                      // shared-window address of lb
 
   // ---- stage the program once per CTA (a1) ----
   if (threadIdx.x == 0) {
@@ -231,8 +243,8 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
   // constant rows and the zero row of this warp's region (read-only afterwards)
   {
     const uint32_t* vals = reinterpret_cast<const uint32_t*>(smem + L.prog_bytes);
-    for (uint32_t r = 0; r < Y.n_crows; r++) SM32(lb + Y.const_off + r * 128u) = vals[r];
-    SM32(lb + Y.zero_off) = 0u;
+    for (uint32_t r = 0; r < Y.n_crows; r++) SM64(lb + Y.const_off + r * ROW_BYTES) = (uint64_t)vals[r];
+    SM64(lb + Y.zero_off) = 0ull;
   }
   __syncthreads();
 
@@ -244,8 +256,8 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
     const uint32_t tid_sim = wic * 32u + lane;
 
     // ---- warp set-up (a1): registers zero, predicates false, clock 0 ----
-    for (uint32_t s = 0; s < Y.n_slots; s++) SM32(lb + s * 128u) = 0u;
-    for (uint32_t i = lane; i < Y.n_slots + 33u; i += 32u) SM32(wb + Y.ready_off + i * 4u) = 0u;
+    for (uint32_t s = 0; s < Y.n_slots; s++) SM64(lb + s * ROW_BYTES) = 0ull;
+    SM32(pg + lane * 4u) = 0u;
     __syncwarp();
     uint32_t my_pred = (lane == 31u) ? 0xFFFFFFFFu : 0u;  // predicate 31 is always true
     uint32_t pc = 0, rpc = exit_pc;
@@ -268,43 +280,41 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
     uint32_t budget = (uint32_t)(stop_at < BUDGET_CHUNK ? stop_at : BUDGET_CHUNK);
     uint64_t left = stop_at - budget;
     uint32_t mark = budget;
-#define FLUSH_THREADS()                                            \
-  do {                                                             \
+#define FLUSH_THREADS()                                                 \
+  do {                                                                  \
     thread_insts += (uint64_t)(mark - budget) * (uint64_t)__popc(mask); \
-    mark = budget;                                                 \
+    mark = budget;                                                      \
   } while (0)
 
     if (status == 0) for (;;) {
       // ---- fast path: runs of routed FPU / IMAD instructions with nothing
       // pending (no reconvergence, no stop, no rebase). One basic block per
       // instruction; the next instruction is fetched while this one executes.
-      {
+      if (__all_sync(FULL, mask != 0u)) {
         const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
-        uint4 q0 = ip[0], q1 = ip[1], q2 = ip[2], q3 = ip[3];
-        while (__all_sync(FULL, (q0.x == DOP_FPU || q0.x == DOP_IMAD) && pc != rpc && mask != 0u && budget != 0u &&
+        uint4 q0 = ip[0], q1 = ip[1], q3 = ip[3];
+        while (__all_sync(FULL, (q0.x == DOP_FPU || q0.x == DOP_IMAD) && pc != rpc && budget != 0u &&
                                     t_next < REBASE_AT)) {
-          const uint32_t a0 = SM32(lb + q1.x), b0 = SM32(lb + q1.y), c0 = SM32(lb + q1.z);
-          const uint32_t ra = SM32(wb + q2.x), rb = SM32(wb + q2.y), rc = SM32(wb + q2.z), rd = SM32(wb + q2.w);
+          const uint2 a = SM2(lb + q1.x), b = SM2(lb + q1.y), c = SM2(lb + q1.z);
+          const uint32_t rd = SM32(lb + q1.w + 4u);
           const uint32_t rg = SM32(pg + q0.y * 4u);
           const uint32_t pm = __shfl_sync(FULL, my_pred, q0.y);
-          const uint4 n0 = ip[4], n1 = ip[5], n2 = ip[6], n3 = ip[7];  // instruction pc + 1 (<= sentinel)
-          const uint32_t t = max(max(max(t_next, ra), max(rb, rc)), max(rd, rg));
+          const uint4 n0 = ip[4], n1 = ip[5], n3 = ip[7];  // instruction pc + 1 (<= sentinel)
+          const uint32_t t = max(max(max(t_next, a.y), max(b.y, c.y)), max(rd, rg));
           const uint32_t wr = t + q3.x;
-          SM32(wb + q2.w) = wr;
           max_ready = max(max_ready, wr);
           drain = max(drain, t + q3.y);
           t_last = t;
           t_next = t + q3.z;
           budget--;
           const bool on = ((mask & (pm ^ q0.z)) >> lane) & 1u;
-          const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ q3.w)));
-          const uint32_t ri = a0 * b0 + ((c0 ^ q3.w) - q3.w);
-          st_shared_if(on, s_lane + q1.w, q0.x == DOP_FPU ? rf : ri);
+          const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(c.x ^ q3.w)));
+          const uint32_t ri = a.x * b.x + ((c.x ^ q3.w) - q3.w);
+          st_pair(on, s_lane + q1.w, q0.x == DOP_FPU ? rf : ri, wr);
           pc++;
           ip += 4;
           q0 = n0;
           q1 = n1;
-          q2 = n2;
           q3 = n3;
         }
       }
@@ -327,12 +337,14 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
       const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q0.y, gneg = q0.z, inc = q0.w;
       const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q1.w;
       const uint32_t aux = q3.w;
-      const uint32_t a0 = SM32(lb + A), b0 = SM32(lb + B), c0 = SM32(lb + C);
-      const uint32_t ra = SM32(wb + q2.x), rb = SM32(wb + q2.y), rc = SM32(wb + q2.z), rd = SM32(wb + q2.w);
+      const uint2 pa = SM2(lb + A), pb = SM2(lb + B), pcc = SM2(lb + C);
+      const uint32_t a0 = pa.x, b0 = pb.x, c0 = pcc.x;
+      const uint32_t rd = SM32(lb + D + 4u);
+      const uint32_t h0 = SM32(wb + q2.x), h1 = SM32(wb + q2.y), h2 = SM32(wb + q2.z), h3 = SM32(wb + q2.w);
       const uint32_t rg = SM32(pg + guard * 4u);
       const uint32_t pm = __shfl_sync(FULL, my_pred, guard);
 
-      if (__any_sync(FULL, inc == 0u || budget == 0u || t_next >= REBASE_AT)) {  // rare path
+      if (__any_sync(FULL, (inc & INC_ISSUE) == 0u || budget == 0u || t_next >= REBASE_AT)) {  // rare path
         if (op == OP_EVENT) {  // trace record (a7), zero cost
           if (n_events != 0xFFFFFFFFu) n_events++;
           if (n_rec < L.max_ts) {
@@ -353,9 +365,13 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
         }
         if (t_next >= REBASE_AT) {  // keep every clock below 2^31: move the epoch to t_last
           const uint32_t delta = t_last;
-          for (uint32_t i = lane; i < Y.n_slots + 33u; i += 32u) {
-            const uint32_t e = SM32(wb + Y.ready_off + i * 4u);
-            SM32(wb + Y.ready_off + i * 4u) = e > delta ? e - delta : 0u;
+          for (uint32_t r = 0; r < Y.n_slots; r++) {
+            const uint32_t e = SM32(lb + r * ROW_BYTES + 4u);
+            SM32(lb + r * ROW_BYTES + 4u) = e > delta ? e - delta : 0u;
+          }
+          {
+            const uint32_t e = SM32(pg + lane * 4u);
+            SM32(pg + lane * 4u) = e > delta ? e - delta : 0u;
           }
           __syncwarp();
           epoch += delta;
@@ -378,9 +394,11 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
       }
 
       // issue: in-order scoreboard (a3), epoch-relative 32-bit clock
-      uint32_t t = max(max(max(t_next, ra), max(rb, rc)), max(rd, rg));
+      const uint32_t t = max(max(max(max(t_next, pa.y), max(pb.y, pcc.y)), max(rd, rg)),
+                             max(max(h0, h1), max(h2, h3)));
       const uint32_t wr = t + q3.x;
-      SM32(wb + q2.w) = wr;
+      if (inc & INC_RDEST) SM32(lb + D + 4u) = wr;  // register destination
+      if (inc & INC_PDEST) SM32(wb + q2.w) = wr;    // predicate destination
       max_ready = max(max_ready, wr);
       drain = max(drain, t + q3.y);
       t_last = t;
@@ -391,16 +409,15 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
       const uint32_t exec = mask & (pm ^ gneg);
       const bool on = (exec >> lane) & 1u;
       // high words of 64-bit operands, loaded by the handlers that need them
-#define A64() ((uint64_t)a0 | ((uint64_t)SM32(lb + A + 128u) << 32))
-#define B64() ((uint64_t)b0 | ((uint64_t)SM32(lb + B + 128u) << 32))
-#define C64() ((uint64_t)c0 | ((uint64_t)SM32(lb + C + 128u) << 32))
-
+#define A64() ((uint64_t)a0 | ((uint64_t)SM32(lb + A + ROW_BYTES) << 32))
+#define B64() ((uint64_t)b0 | ((uint64_t)SM32(lb + B + ROW_BYTES) << 32))
+#define C64() ((uint64_t)c0 | ((uint64_t)SM32(lb + C + ROW_BYTES) << 32))
 #define W32(v) st_shared_if(on, s_lane + D, (v))
-#define W64(v)                                           \
-  do {                                                   \
-    const uint64_t v_ = (v);                             \
-    st_shared_if(on, s_lane + D, (uint32_t)v_);          \
-    st_shared_if(on, s_lane + D + 128u, (uint32_t)(v_ >> 32)); \
+#define W64(v)                                                  \
+  do {                                                          \
+    const uint64_t v_ = (v);                                    \
+    st_shared_if(on, s_lane + D, (uint32_t)v_);                 \
+    st_shared_if(on, s_lane + D + ROW_BYTES, (uint32_t)(v_ >> 32)); \
   } while (0)
 
       // unified datapaths, no dispatch branch (routing chosen by the decoder)
@@ -492,7 +509,7 @@ __global__ void __launch_bounds__(256) ks_interp_kernel(const __grid_constant__ 
               if (wide) {
                 const uint64_t v = *reinterpret_cast<const uint64_t*>(ptr);
                 SM32(lb + D) = (uint32_t)v;
-                SM32(lb + D + 128u) = (uint32_t)(v >> 32);
+                SM32(lb + D + ROW_BYTES) = (uint32_t)(v >> 32);
               } else {
                 SM32(lb + D) = *reinterpret_cast<const uint32_t*>(ptr);
               }
