@@ -1081,6 +1081,7 @@ class Decoder {
       }
       const KsInsn& in = K.code[i];
       o.op = fpu_family(in.op) ? DOP_FPU : imad_family(in.op) ? DOP_IMAD : in.op;
+      if ((o.op == DOP_FPU || o.op == DOP_IMAD) && in.guard != KS_NO_GUARD) o.op |= DOP_GUARDED;
       o.inc = in.op == OP_EVENT ? 0u : INC_ISSUE;
       if (in.guard != KS_NO_GUARD) {
         o.guard = in.guard;
@@ -1090,7 +1091,7 @@ class Decoder {
       uint32_t* rows[4] = {&o.a, &o.b, &o.c, &o.d};
       for (int p = 0; p < 4; p++)
         if (routed_width(in, p)) *rows[p] = row_of(ops[p]);
-      if (o.op == DOP_FPU || o.op == DOP_IMAD) o.aux = route[i].aux;
+      if ((o.op & ~DOP_GUARDED) == DOP_FPU || (o.op & ~DOP_GUARDED) == DOP_IMAD) o.aux = route[i].aux;
       if (in.op != OP_EVENT) {
         o.ha = phz(in.ha);
         o.hb = phz(in.hb);

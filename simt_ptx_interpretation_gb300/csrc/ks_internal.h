@@ -122,8 +122,10 @@ constexpr uint32_t OP_EXIT = 0xFE;  // sentinel at index n_insn: the remaining l
 //                                            mul: c = -0.0;        fma: as is
 //   DOP_IMAD: d = a * b + ((c ^ aux) - aux)  add: b = 1, c = y;    sub: aux = ~0;  mul: c = 0;
 //                                            mad: as is;           mov: b = 1, c = 0
+// Unguarded forms run in the interpreter's fast path; guarded ones add DOP_GUARDED.
 constexpr uint32_t DOP_FPU = 0x40;
 constexpr uint32_t DOP_IMAD = 0x41;
+constexpr uint32_t DOP_GUARDED = 0x02;
 
 struct DevLayout {
   uint32_t n_slots, n_crows;

@@ -287,35 +287,51 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
   } while (0)
 
     if (status == 0) for (;;) {
-      // ---- fast path: runs of routed FPU / IMAD instructions with nothing
-      // pending (no reconvergence, no stop, no rebase). One basic block per
-      // instruction; the next instruction is fetched while this one executes.
+      // ---- fast path: runs of unguarded routed FPU / IMAD instructions with
+      // nothing pending. `fuel` = instructions that may run before the
+      // reconvergence pc or the end of the step budget; pc, budget and t_last
+      // are rebuilt when the run ends. One basic block per instruction,
+      // unrolled by two; the next instruction is fetched while this one executes.
       if (__all_sync(FULL, mask != 0u)) {
+        const uint32_t dist = rpc >= pc ? rpc - pc : 0xFFFFFFFFu;
+        uint32_t fuel = min(budget, dist);
+        const uint32_t fuel0 = fuel;
+        const bool on_all = (mask >> lane) & 1u;
         const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
         uint4 q0 = ip[0], q1 = ip[1], q3 = ip[3];
-        while (__all_sync(FULL, (q0.x == DOP_FPU || q0.x == DOP_IMAD) && pc != rpc && budget != 0u &&
-                                    t_next < REBASE_AT)) {
-          const uint2 a = SM2(lb + q1.x), b = SM2(lb + q1.y), c = SM2(lb + q1.z);
-          const uint32_t rd = SM32(lb + q1.w + 4u);
-          const uint32_t rg = SM32(pg + q0.y * 4u);
-          const uint32_t pm = __shfl_sync(FULL, my_pred, q0.y);
-          const uint4 n0 = ip[4], n1 = ip[5], n3 = ip[7];  // instruction pc + 1 (<= sentinel)
-          const uint32_t t = max(max(max(t_next, a.y), max(b.y, c.y)), max(rd, rg));
-          const uint32_t wr = t + q3.x;
-          max_ready = max(max_ready, wr);
-          drain = max(drain, t + q3.y);
-          t_last = t;
-          t_next = t + q3.z;
-          budget--;
-          const bool on = ((mask & (pm ^ q0.z)) >> lane) & 1u;
-          const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(c.x ^ q3.w)));
-          const uint32_t ri = a.x * b.x + ((c.x ^ q3.w) - q3.w);
-          st_pair(on, s_lane + q1.w, q0.x == DOP_FPU ? rf : ri, wr);
-          pc++;
-          ip += 4;
-          q0 = n0;
-          q1 = n1;
-          q3 = n3;
+        uint4 n0, n1, n3;
+#define FAST_OK(x0) (fuel != 0u && ((x0).x | 1u) == DOP_IMAD && t_next < REBASE_AT)
+#define FAST_STEP(x0, x1, x3, y0, y1, y3)                                                         \
+  {                                                                                             \
+    const uint2 a = SM2(lb + x1.x), b = SM2(lb + x1.y), c = SM2(lb + x1.z);                     \
+    const uint32_t rd = SM32(lb + x1.w + 4u);                                                   \
+    y0 = ip[4];                                                                                 \
+    y1 = ip[5];                                                                                 \
+    y3 = ip[7]; /* instruction pc + 1 (<= sentinel) */                                          \
+    const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));                           \
+    const uint32_t wr = t + x3.x;                                                               \
+    max_ready = max(max_ready, wr);                                                             \
+    t_next = t + 1u;                                                                            \
+    const uint32_t cx = c.x ^ x3.w;                                                             \
+    const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx))); \
+    const uint32_t ri = a.x * b.x + (cx - x3.w);                                                \
+    st_pair(on_all, s_lane + x1.w, x0.x == DOP_FPU ? rf : ri, wr);                              \
+    fuel--;                                                                                     \
+    ip += 4;                                                                                    \
+  }
+        for (;;) {
+          if (!__all_sync(FULL, FAST_OK(q0))) break;
+          FAST_STEP(q0, q1, q3, n0, n1, n3)
+          if (!__all_sync(FULL, FAST_OK(n0))) break;
+          FAST_STEP(n0, n1, n3, q0, q1, q3)
+        }
+#undef FAST_OK
+#undef FAST_STEP
+        const uint32_t steps = fuel0 - fuel;
+        if (steps) {
+          pc += steps;
+          budget -= steps;
+          t_last = t_next - 1u;
         }
       }
       // ---- general path ----
@@ -421,12 +437,12 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
   } while (0)
 
       // unified datapaths, no dispatch branch (routing chosen by the decoder)
-      if (__all_sync(FULL, op == DOP_FPU)) {
+      if (__all_sync(FULL, (op & ~DOP_GUARDED) == DOP_FPU)) {
         W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))));
         pc++;
         continue;
       }
-      if (__all_sync(FULL, op == DOP_IMAD)) {
+      if (__all_sync(FULL, (op & ~DOP_GUARDED) == DOP_IMAD)) {
         W32(a0 * b0 + ((c0 ^ aux) - aux));
         pc++;
         continue;
