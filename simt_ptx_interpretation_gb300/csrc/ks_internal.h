@@ -96,17 +96,19 @@ static_assert(sizeof(KsInsn) == 32, "KsInsn must be 32 bytes");
 constexpr uint32_t ROW_BYTES = 256;
 
 struct alignas(16) DevInsn {
+  // first 16 bytes + next 16: everything the fast path reads
   uint32_t op;
-  uint32_t guard;  // predicate lane 0..30, or 31 (always true)
-  uint32_t gneg;   // 0 or 0xFFFFFFFF
+  uint32_t wlat;   // in the image: latency class | flags (below); patched to dest latency
+  uint32_t aux;    // offset / param offset / special / event / cvt / cmp|pred / target|rpc<<16 / pred idx
+  uint32_t d;      // destination row offset (the zero row if absent)
+  uint32_t a, b, c;  // source row offsets (region-relative; the zero row if absent)
   uint32_t inc;    // bit 0: issued (0 for a trace pseudo-op or the exit sentinel);
                    // bit 1: has a register destination; bit 2: has a predicate destination
-  uint32_t a, b, c, d;       // row offsets (region-relative); the zero row if absent
+  uint32_t guard;  // predicate lane 0..30, or 31 (always true)
+  uint32_t gneg;   // 0 or 0xFFFFFFFF
   uint32_t ha, hb, hc, hd;   // predicate-table offsets of predicate sources / destination (entry 31 if absent)
-  uint32_t wlat;   // in the image: latency class | flags (below); patched to dest latency
   uint32_t dlat;   // patched: store completion latency (0 if not a store)
   uint32_t nlat;   // patched: issue-clock advance (latency for bra/ret, 1 otherwise, 0 if inc == 0)
-  uint32_t aux;    // offset / param offset / special / event / cvt / cmp|pred / target|rpc<<16 / pred idx
 };
 static_assert(sizeof(DevInsn) == 64, "DevInsn must be 64 bytes");
 

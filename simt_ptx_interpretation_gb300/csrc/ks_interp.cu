@@ -290,43 +290,58 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       // ---- fast path: runs of unguarded routed FPU / IMAD instructions with
       // nothing pending. `fuel` = instructions that may run before the
       // reconvergence pc or the end of the step budget; pc, budget and t_last
-      // are rebuilt when the run ends. One basic block per instruction,
-      // unrolled by two; the next instruction is fetched while this one executes.
+      // are rebuilt when the run ends. Software-pipelined: while instruction k
+      // executes, the rows of instruction k+1 are loaded and the record of k+2
+      // fetched; k+1's rows may predate k's store, so k's result and ready time
+      // are forwarded into any of them that is k's destination.
       if (__all_sync(FULL, mask != 0u)) {
         const uint32_t dist = rpc >= pc ? rpc - pc : 0xFFFFFFFFu;
         uint32_t fuel = min(budget, dist);
         const uint32_t fuel0 = fuel;
         const bool on_all = (mask >> lane) & 1u;
         const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
-        uint4 q0 = ip[0], q1 = ip[1], q3 = ip[3];
-        uint4 n0, n1, n3;
-#define FAST_OK(x0) (fuel != 0u && ((x0).x | 1u) == DOP_IMAD && t_next < REBASE_AT)
-#define FAST_STEP(x0, x1, x3, y0, y1, y3)                                                         \
-  {                                                                                             \
-    const uint2 a = SM2(lb + x1.x), b = SM2(lb + x1.y), c = SM2(lb + x1.z);                     \
-    const uint32_t rd = SM32(lb + x1.w + 4u);                                                   \
-    y0 = ip[4];                                                                                 \
-    y1 = ip[5];                                                                                 \
-    y3 = ip[7]; /* instruction pc + 1 (<= sentinel) */                                          \
-    const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));                           \
-    const uint32_t wr = t + x3.x;                                                               \
-    max_ready = max(max_ready, wr);                                                             \
-    t_next = t + 1u;                                                                            \
-    const uint32_t cx = c.x ^ x3.w;                                                             \
-    const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx))); \
-    const uint32_t ri = a.x * b.x + (cx - x3.w);                                                \
-    st_pair(on_all, s_lane + x1.w, x0.x == DOP_FPU ? rf : ri, wr);                              \
-    fuel--;                                                                                     \
-    ip += 4;                                                                                    \
-  }
+        // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
+        uint4 ka = ip[0], kb = ip[1];
+        uint2 a = SM2(lb + kb.x), b = SM2(lb + kb.y), c = SM2(lb + kb.z);
+        uint32_t rd = SM32(lb + ka.w + 4u);
+        // instruction k+1 (the last instruction is never a fast op, so k+1 and
+        // k+2 stay within the program and its exit sentinel)
+        uint4 na = ip[4], nb = ip[5];
         for (;;) {
-          if (!__all_sync(FULL, FAST_OK(q0))) break;
-          FAST_STEP(q0, q1, q3, n0, n1, n3)
-          if (!__all_sync(FULL, FAST_OK(n0))) break;
-          FAST_STEP(n0, n1, n3, q0, q1, q3)
+          if (!__all_sync(FULL, fuel != 0u && (ka.x | 1u) == DOP_IMAD && t_next < REBASE_AT)) break;
+          uint2 a1 = SM2(lb + nb.x), b1 = SM2(lb + nb.y), c1 = SM2(lb + nb.z);
+          uint32_t rd1 = SM32(lb + na.w + 4u);
+          const uint4 ma = ip[8], mb = ip[9];
+          const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));
+          const uint32_t wr = t + ka.y;
+          max_ready = max(max_ready, wr);
+          t_next = t + 1u;
+          const uint32_t cx = c.x ^ ka.z;
+          const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
+          const uint32_t ri = a.x * b.x + (cx - ka.z);
+          const uint32_t res = ka.x == DOP_FPU ? rf : ri;
+          st_pair(on_all, s_lane + ka.w, res, wr);
+          // forward k into k+1
+          const uint32_t dk = ka.w;
+          const bool fa = nb.x == dk, fb = nb.y == dk, fc = nb.z == dk;
+          a1.x = (fa && on_all) ? res : a1.x;
+          a1.y = fa ? wr : a1.y;
+          b1.x = (fb && on_all) ? res : b1.x;
+          b1.y = fb ? wr : b1.y;
+          c1.x = (fc && on_all) ? res : c1.x;
+          c1.y = fc ? wr : c1.y;
+          rd1 = na.w == dk ? wr : rd1;
+          ka = na;
+          kb = nb;
+          na = ma;
+          nb = mb;
+          a = a1;
+          b = b1;
+          c = c1;
+          rd = rd1;
+          fuel--;
+          ip += 4;
         }
-#undef FAST_OK
-#undef FAST_STEP
         const uint32_t steps = fuel0 - fuel;
         if (steps) {
           pc += steps;
@@ -350,13 +365,13 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       // fetch (a2) and every operand / ready-time load of the instruction at once
       const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
       const uint4 q0 = ip[0], q1 = ip[1], q2 = ip[2], q3 = ip[3];
-      const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q0.y, gneg = q0.z, inc = q0.w;
-      const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q1.w;
-      const uint32_t aux = q3.w;
+      const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q2.x, gneg = q2.y, inc = q1.w;
+      const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q0.w;
+      const uint32_t aux = q0.z;
       const uint2 pa = SM2(lb + A), pb = SM2(lb + B), pcc = SM2(lb + C);
       const uint32_t a0 = pa.x, b0 = pb.x, c0 = pcc.x;
       const uint32_t rd = SM32(lb + D + 4u);
-      const uint32_t h0 = SM32(wb + q2.x), h1 = SM32(wb + q2.y), h2 = SM32(wb + q2.z), h3 = SM32(wb + q2.w);
+      const uint32_t h0 = SM32(wb + q2.z), h1 = SM32(wb + q2.w), h2 = SM32(wb + q3.x), h3 = SM32(wb + q3.y);
       const uint32_t rg = SM32(pg + guard * 4u);
       const uint32_t pm = __shfl_sync(FULL, my_pred, guard);
 
@@ -412,13 +427,13 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       // issue: in-order scoreboard (a3), epoch-relative 32-bit clock
       const uint32_t t = max(max(max(max(t_next, pa.y), max(pb.y, pcc.y)), max(rd, rg)),
                              max(max(h0, h1), max(h2, h3)));
-      const uint32_t wr = t + q3.x;
+      const uint32_t wr = t + q0.y;
       if (inc & INC_RDEST) SM32(lb + D + 4u) = wr;  // register destination
-      if (inc & INC_PDEST) SM32(wb + q2.w) = wr;    // predicate destination
+      if (inc & INC_PDEST) SM32(wb + q3.y) = wr;    // predicate destination
       max_ready = max(max_ready, wr);
-      drain = max(drain, t + q3.y);
+      drain = max(drain, t + q3.z);
       t_last = t;
-      t_next = t + q3.z;
+      t_next = t + q3.w;
       budget--;
 
       // guard (a2)
