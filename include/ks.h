@@ -212,6 +212,29 @@ int ks_simulate(const ks_module* mod, const char* kernel, uint32_t grid, uint32_
                 void* trace_buf, size_t trace_bytes, void* stats_buf, size_t stats_bytes,
                 const ks_config* cfg, void* stream);
 
+/* Allocation-free variant of ks_simulate. The pages have no counterpart: it
+ * exists for callers that cannot let a library allocate device memory —
+ * code running during CUDA graph capture, programs that give all device
+ * memory to their own allocator, embedders with a fixed budget. Instead of the
+ * per-module device copy that ks_simulate allocates, the kernel's program
+ * image (its decoded instructions and constant rows: 64 bytes per program
+ * entry plus 4 per constant row) is copied with cudaMemcpyAsync on `stream`
+ * into one file-scope device array of KS_STATIC_IMAGE_BYTES bytes, which every
+ * GPU that loads the library holds until the process exits. Arguments,
+ * outputs and errors are those of ks_simulate, plus KS_ERR_LIMIT when the
+ * image exceeds KS_STATIC_IMAGE_BYTES (checked before any GPU work). The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * and the device limits; make that first call before any stream capture.
+ * Nothing in the array has to start at zero: each call writes every byte the
+ * kernel reads. All calls share the array and it keeps the last call's image,
+ * so calls whose copies and kernels overlap on the GPU (for example on two
+ * streams) race: order them on one stream or synchronise between them. */
+#define KS_STATIC_IMAGE_BYTES (64u * 1024u)
+int ks_simulate_static(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block,
+                       const void* params, size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs,
+                       void* trace_buf, size_t trace_bytes, void* stats_buf, size_t stats_bytes,
+                       const ks_config* cfg, void* stream);
+
 /* Reduces n_warps stats records (device pointer) on `stream`, waits for the
  * stream, and writes the totals to *out (host). Uses a small device
  * accumulator that the library allocates once per device; calls are

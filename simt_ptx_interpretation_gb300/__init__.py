@@ -7,7 +7,7 @@ produces the simulated memory, per-warp cycles from an in-order scoreboard,
 is include/ks.h (libks.so); this package marshals arguments to it.
 """
 from .api import (DEFAULT_LAT, STATS_DTYPE, Config, KsError, Module, Run, Totals, read_stats, run, simulate,
-                  stats_array, stats_bytes, trace_bytes)
+                  simulate_static, stats_array, stats_bytes, trace_bytes)
 
 __all__ = ["DEFAULT_LAT", "STATS_DTYPE", "Config", "KsError", "Module", "Run", "Totals", "read_stats", "run",
-           "simulate", "stats_array", "stats_bytes", "trace_bytes"]
+           "simulate", "simulate_static", "stats_array", "stats_bytes", "trace_bytes"]

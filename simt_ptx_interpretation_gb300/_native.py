@@ -52,6 +52,10 @@ EXPORTS = {
                                    ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(KsBuffer), ctypes.c_uint32,
                                    ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,
                                    ctypes.POINTER(KsConfig), ctypes.c_void_p]),
+    "ks_simulate_static": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(KsBuffer),
+                                          ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.POINTER(KsConfig), ctypes.c_void_p]),
     "ks_read_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.POINTER(KsTotals)]),
     "ks_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }

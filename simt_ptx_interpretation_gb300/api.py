@@ -166,6 +166,28 @@ def simulate(module: Module, kernel: str, grid: int, block: int, params: bytes, 
     _check(rc)
 
 
+def simulate_static(module: Module, kernel: str, grid: int, block: int, params: bytes, buffers, stats: torch.Tensor,
+                    trace: torch.Tensor | None = None, config: Config | None = None, stream=None) -> None:
+    """ks_simulate_static: like simulate(), but the library allocates no device
+    memory (the program image goes to one fixed-size static device array shared
+    by all calls; calls that overlap on the GPU race)."""
+    bufs = (_native.KsBuffer * max(1, len(buffers)))()
+    for i, (base, t) in enumerate(buffers):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("buffers must be contiguous CUDA tensors")
+        bufs[i].sim_base = base
+        bufs[i].dev_ptr = t.data_ptr()
+        bufs[i].bytes = t.numel() * t.element_size()
+    cfg = (config or Config()).to_c()
+    pbuf = ctypes.create_string_buffer(bytes(params), max(1, len(params)))
+    rc = _native.lib().ks_simulate_static(
+        module.handle, kernel.encode(), grid, block, ctypes.cast(pbuf, ctypes.c_void_p), len(params), bufs,
+        len(buffers), trace.data_ptr() if trace is not None else None,
+        trace.numel() if trace is not None else 0, stats.data_ptr(), stats.numel(), ctypes.byref(cfg),
+        _stream_handle(stream))
+    _check(rc)
+
+
 def read_stats(stats: torch.Tensor, n_warps: int, stream=None) -> Totals:
     """Launch totals (ks_read_stats); waits for the stream."""
     t = _native.KsTotals()

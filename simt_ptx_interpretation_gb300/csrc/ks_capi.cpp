@@ -74,6 +74,10 @@ uint64_t warps_of(uint32_t grid, uint32_t block) { return (uint64_t)grid * ((blo
 
 }  // namespace
 
+namespace ks {
+const KsKernel* module_kernel(const ks_module* mod, const char* name) { return find_kernel(mod, name, nullptr); }
+}  // namespace ks
+
 extern "C" {
 
 void ks_config_default(ks_config* cfg) {

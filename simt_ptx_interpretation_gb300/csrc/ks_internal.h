@@ -203,6 +203,9 @@ size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t w
 // Offset of the first warp region in shared memory.
 uint32_t interp_region0(uint32_t image_bytes);
 
+// Kernel lookup by name in a module (ks_capi.cpp); nullptr if absent.
+const KsKernel* module_kernel(const ks_module* mod, const char* name);
+
 // Launchers (ks_interp.cu). Return a cudaError_t value.
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);
 int interp_occupancy(uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
