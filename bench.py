@@ -47,15 +47,17 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="ffma_pair")
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--iters", type=int, default=4096, help="FFMA outer iterations (smaller cases for profiling)")
     return p.parse_args()
 
 
-def workloads(name: str):
+def workloads(name: str, iters: int = 4096):
     from simt_ptx_interpretation_gb300 import workloads as wl
     if name == "ffma_pair":
-        return [wl.ffma(acc=1), wl.ffma(acc=8)], {
-            "workload": "ffma_probe_pair", "grid": 132, "block": 128, "iters": 4096, "fma_per_iter": 32,
+        return [wl.ffma(acc=1, iters=iters), wl.ffma(acc=8, iters=iters)], {
+            "workload": "ffma_probe_pair", "grid": 132, "block": 128, "iters": iters, "fma_per_iter": 32,
             "accumulators": [1, 8], "seed": 2}
     if name == "vector_add":
         return [wl.vector_add()], {"workload": "vector_add", "n": 4000, "grid": 16, "block": 256, "seed": 0}
@@ -191,7 +193,7 @@ def run_ours(args, world, rank, local):
         _build.build_native()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    ws, config = workloads(args.workload)
+    ws, config = workloads(args.workload, args.iters)
     stream = torch.cuda.current_stream(dev)
 
     # inputs resident in HBM; outputs preallocated
@@ -264,7 +266,7 @@ def run_ours(args, world, rank, local):
                 "launch_ms_mean": [round(sum(x) / len(x), 4) for x in launch_ms]}
 
     # end to end through the public API with pinned host buffers
-    e2e = run_e2e(args, jobs, insts, dev, stream)
+    e2e = None if args.no_e2e else run_e2e(args, jobs, insts, dev, stream)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -347,7 +349,7 @@ def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    ws, config = workloads(args.workload)
+    ws, config = workloads(args.workload, args.iters)
     cores = os.cpu_count() or 1
     per = max(4, min(64, 2 * cores))
     for _ in range(args.warmup):
