@@ -1101,6 +1101,23 @@ class Decoder {
           o.inc |= INC_PDEST;
         }
         if (routed_width(in, 3)) o.inc |= INC_RDEST;
+        const bool pred_operand = (in.ha >= KS_HZ_PRED0 && in.ha != KS_HZ_NONE) ||
+                                  (in.hb >= KS_HZ_PRED0 && in.hb != KS_HZ_NONE) ||
+                                  (in.hc >= KS_HZ_PRED0 && in.hc != KS_HZ_NONE) || (o.inc & INC_PDEST);
+        if (pred_operand) o.inc |= INC_PHAZ;
+        switch (in.op) {
+          case OP_LDP32: case OP_LDP64: case OP_MOV64: case OP_MOVSP:
+          case OP_ADD64: case OP_SUB64: case OP_MUL64: case OP_MAD64:
+          case OP_AND32: case OP_OR32: case OP_XOR32: case OP_AND64: case OP_OR64: case OP_XOR64:
+          case OP_SHL32: case OP_SHR32U: case OP_SHR32S: case OP_SHL64: case OP_SHR64U: case OP_SHR64S:
+          case OP_FDIV: case OP_FSQRT:
+          case OP_CVT_F32_U32: case OP_CVT_F32_S32: case OP_CVT_F32_U64: case OP_CVT_F32_S64:
+          case OP_CVT_F2I: case OP_CVT_ZX: case OP_CVT_SX:
+            if (in.guard == KS_NO_GUARD && !pred_operand) o.inc |= INC_MID;
+            break;
+          default:
+            break;
+        }
         o.wlat = (uint32_t)in.lat;
         if (in.hd != KS_HZ_NONE) o.wlat |= DEV_HAS_DEST;
         if (in.op == OP_STG32 || in.op == OP_STG64) o.wlat |= DEV_IS_STORE;

@@ -118,6 +118,10 @@ constexpr uint32_t DEV_IS_STORE = 1u << 9;
 constexpr uint32_t DEV_IS_CTRL = 1u << 10;
 // bits of DevInsn::inc
 constexpr uint32_t INC_ISSUE = 1u, INC_RDEST = 2u, INC_PDEST = 4u;
+// INC_MID: unguarded register-to-register op with no predicate operand, no
+//          memory access and no control transfer (runs in the mid loop)
+// INC_PHAZ: has a predicate source or destination (its ready entries matter)
+constexpr uint32_t INC_MID = 8u, INC_PHAZ = 16u;
 constexpr uint32_t OP_EXIT = 0xFE;  // sentinel at index n_insn: the remaining lanes finish
 // Unified datapaths selected at resolve time (DevInsn::op only):
 //   DOP_FPU:  d = fma.rn(a, b, c ^ aux)      add: b = 1.0, c = y;  sub: b = 1.0, c = y, aux = sign bit;
@@ -182,6 +186,7 @@ struct KsLaunch {
   uint32_t n_crows;
   DevLayout layout;
   uint32_t grid, block, wpc;  // simulated grid, block, warps per simulated CTA
+  uint32_t gw_step_cta, gw_step_wic;  // the real-warp stride split into (CTAs, warps) of the simulated grid
   uint32_t n_warps;           // grid * wpc
   uint32_t lat[KS_NUM_LAT_CLASSES];
   uint32_t max_ts;

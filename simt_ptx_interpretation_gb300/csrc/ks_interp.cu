@@ -250,9 +250,16 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
 
   const uint32_t exit_pc = L.n_insn;
 
-  for (uint32_t gw = blockIdx.x * nwarps + wid; gw < L.n_warps; gw += gridDim.x * nwarps) {
-    const uint32_t cta = gw / L.wpc;
-    const uint32_t wic = gw - cta * L.wpc;
+  // simulated (CTA, warp-in-CTA) of this real warp's first simulated warp, and
+  // the real-warp stride split the same way (no division per simulated warp)
+  const uint32_t gw_stride = gridDim.x * nwarps;
+  const uint32_t step_cta = gw_stride / L.wpc, step_wic = gw_stride - step_cta * L.wpc;
+  uint32_t cta = (blockIdx.x * nwarps + wid) / L.wpc;
+  uint32_t wic = (blockIdx.x * nwarps + wid) - cta * L.wpc;
+  uint32_t hint = 0;  // buffer of the last simulated access (tried first)
+
+  for (uint32_t gw = blockIdx.x * nwarps + wid; gw < L.n_warps;
+       gw += gw_stride, cta += step_cta, wic += step_wic, cta += (wic >= L.wpc), wic -= (wic >= L.wpc) ? L.wpc : 0u) {
     const uint32_t tid_sim = wic * 32u + lane;
 
     // ---- warp set-up (a1): registers zero, predicates false, clock 0 ----
@@ -349,6 +356,91 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           t_last = t_next - 1u;
         }
       }
+      // ---- mid path: runs of the other unguarded register-to-register ops
+      // (64-bit arithmetic, logic, shifts, conversions, specials, ld.param,
+      // div, sqrt), bounded by `fuel` like the fast path, dispatched with one
+      // uniform jump per instruction.
+      if (__all_sync(FULL, mask != 0u)) {
+        const uint32_t dist = rpc >= pc ? rpc - pc : 0xFFFFFFFFu;
+        uint32_t fuel = min(budget, dist);
+        const uint32_t fuel0 = fuel;
+        const bool on = (mask >> lane) & 1u;
+        const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
+        for (;;) {
+          const uint4 ka = ip[0], kb = ip[1];
+          if (!__all_sync(FULL, fuel != 0u && (kb.w & INC_MID) != 0u && t_next < REBASE_AT)) break;
+          const uint2 pa = SM2(lb + kb.x), pb = SM2(lb + kb.y), pcc = SM2(lb + kb.z);
+          const uint32_t rd = SM32(lb + ka.w + 4u);
+          const uint32_t t = max(max(t_next, pa.y), max(max(pb.y, pcc.y), rd));
+          const uint32_t wr = t + ka.y;
+          max_ready = max(max_ready, wr);
+          t_next = t + 1u;
+          const uint32_t a0 = pa.x, b0 = pb.x, D = ka.w, aux = ka.z;
+          const uint32_t A = kb.x, B = kb.y;
+          uint32_t lo = 0, hi = 0;
+          bool wide = false;
+#define MA64() ((uint64_t)a0 | ((uint64_t)SM32(lb + A + ROW_BYTES) << 32))
+#define MB64() ((uint64_t)b0 | ((uint64_t)SM32(lb + B + ROW_BYTES) << 32))
+#define R64(v) do { const uint64_t v_ = (v); lo = (uint32_t)v_; hi = (uint32_t)(v_ >> 32); wide = true; } while (0)
+          switch (__shfl_sync(FULL, ka.x, 0)) {
+            case OP_LDP32: lo = *reinterpret_cast<const uint32_t*>(s_params + aux); break;
+            case OP_LDP64: R64(*reinterpret_cast<const uint64_t*>(s_params + aux)); break;
+            case OP_MOV64: R64(MA64()); break;
+            case OP_MOVSP:
+              lo = aux == SP_TID ? tid_sim : aux == SP_NTID ? L.block : aux == SP_CTAID ? cta
+                 : aux == SP_NCTAID ? L.grid : aux == SP_LANEID ? lane : aux == SP_ONE ? 1u : 0u;
+              break;
+            case OP_ADD64: R64(MA64() + MB64()); break;
+            case OP_SUB64: R64(MA64() - MB64()); break;
+            case OP_MUL64: R64(MA64() * MB64()); break;
+            case OP_MAD64: R64(MA64() * MB64() + ((uint64_t)pcc.x | ((uint64_t)SM32(lb + kb.z + ROW_BYTES) << 32))); break;
+            case OP_AND32: lo = a0 & b0; break;
+            case OP_OR32: lo = a0 | b0; break;
+            case OP_XOR32: lo = a0 ^ b0; break;
+            case OP_AND64: R64(MA64() & MB64()); break;
+            case OP_OR64: R64(MA64() | MB64()); break;
+            case OP_XOR64: R64(MA64() ^ MB64()); break;
+            case OP_SHL32: lo = b0 >= 32u ? 0u : a0 << b0; break;
+            case OP_SHR32U: lo = b0 >= 32u ? 0u : a0 >> b0; break;
+            case OP_SHR32S: lo = (uint32_t)(b0 >= 32u ? ((int32_t)a0 >> 31) : ((int32_t)a0 >> b0)); break;
+            case OP_SHL64: R64(b0 >= 64u ? 0ull : MA64() << b0); break;
+            case OP_SHR64U: R64(b0 >= 64u ? 0ull : MA64() >> b0); break;
+            case OP_SHR64S: {
+              const int64_t x = (int64_t)MA64();
+              R64((uint64_t)(b0 >= 64u ? (x >> 63) : (x >> b0)));
+              break;
+            }
+            case OP_FDIV: lo = fbits(__fdiv_rn(__uint_as_float(a0), __uint_as_float(b0))); break;
+            case OP_FSQRT: lo = fbits(__fsqrt_rn(__uint_as_float(a0))); break;
+            case OP_CVT_F32_U32: lo = __float_as_uint(__uint2float_rn(a0)); break;
+            case OP_CVT_F32_S32: lo = __float_as_uint(__int2float_rn((int32_t)a0)); break;
+            case OP_CVT_F32_U64: lo = __float_as_uint(__ull2float_rn(MA64())); break;
+            case OP_CVT_F32_S64: lo = __float_as_uint(__ll2float_rn((long long)MA64())); break;
+            case OP_CVT_F2I: {
+              const uint64_t v = f2i(__uint_as_float(a0), aux);
+              if ((aux & 15u) == CVT_S64 || (aux & 15u) == CVT_U64) R64(v); else lo = (uint32_t)v;
+              break;
+            }
+            case OP_CVT_ZX: R64((uint64_t)a0); break;
+            case OP_CVT_SX: R64((uint64_t)(int64_t)(int32_t)a0); break;
+            default: break;
+          }
+#undef MA64
+#undef MB64
+#undef R64
+          st_pair(on, s_lane + D, lo, wr);
+          st_shared_if(on && wide, s_lane + D + ROW_BYTES, hi);
+          fuel--;
+          ip += 4;
+        }
+        const uint32_t steps = fuel0 - fuel;
+        if (steps) {
+          pc += steps;
+          budget -= steps;
+          t_last = t_next - 1u;
+          continue;  // maybe a fast run follows
+        }
+      }
       // ---- general path ----
       // pop finished entries (a6); every control condition below is warp-uniform
       // in value, and the votes make that visible to the compiler
@@ -371,7 +463,9 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       const uint2 pa = SM2(lb + A), pb = SM2(lb + B), pcc = SM2(lb + C);
       const uint32_t a0 = pa.x, b0 = pb.x, c0 = pcc.x;
       const uint32_t rd = SM32(lb + D + 4u);
-      const uint32_t h0 = SM32(wb + q2.z), h1 = SM32(wb + q2.w), h2 = SM32(wb + q3.x), h3 = SM32(wb + q3.y);
+      uint32_t hmax = 0;
+      if (inc & INC_PHAZ)
+        hmax = max(max(SM32(wb + q2.z), SM32(wb + q2.w)), max(SM32(wb + q3.x), SM32(wb + q3.y)));
       const uint32_t rg = SM32(pg + guard * 4u);
       const uint32_t pm = __shfl_sync(FULL, my_pred, guard);
 
@@ -425,8 +519,7 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       }
 
       // issue: in-order scoreboard (a3), epoch-relative 32-bit clock
-      const uint32_t t = max(max(max(max(t_next, pa.y), max(pb.y, pcc.y)), max(rd, rg)),
-                             max(max(h0, h1), max(h2, h3)));
+      const uint32_t t = max(max(max(t_next, pa.y), max(pb.y, pcc.y)), max(max(rd, rg), hmax));
       const uint32_t wr = t + q0.y;
       if (inc & INC_RDEST) SM32(lb + D + 4u) = wr;  // register destination
       if (inc & INC_PDEST) SM32(wb + q3.y) = wr;    // predicate destination
@@ -451,19 +544,16 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
     st_shared_if(on, s_lane + D + ROW_BYTES, (uint32_t)(v_ >> 32)); \
   } while (0)
 
-      // unified datapaths, no dispatch branch (routing chosen by the decoder)
-      if (__all_sync(FULL, (op & ~DOP_GUARDED) == DOP_FPU)) {
-        W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))));
-        pc++;
-        continue;
-      }
-      if (__all_sync(FULL, (op & ~DOP_GUARDED) == DOP_IMAD)) {
-        W32(a0 * b0 + ((c0 ^ aux) - aux));
-        pc++;
-        continue;
-      }
-
       switch (op) {
+        // ---- the routed datapaths (guarded, or outside a fast run) ----
+        case DOP_FPU: case DOP_FPU | DOP_GUARDED:
+          W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))));
+          pc++;
+          break;
+        case DOP_IMAD: case DOP_IMAD | DOP_GUARDED:
+          W32(a0 * b0 + ((c0 ^ aux) - aux));
+          pc++;
+          break;
         // ---- control (a6) ----
         case OP_BRA: {
           const uint32_t target = aux & 0xFFFFu, R = aux >> 16;
@@ -521,11 +611,25 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           const uint64_t va = A64() + (uint64_t)(int64_t)(int32_t)aux;
           uint8_t* ptr = nullptr;
           int err = 0;
-          if (on) err = translate(L, va, size, &ptr);
-          const uint32_t emask = __ballot_sync(FULL, err != 0);
-          if (emask) {
-            status = __shfl_sync(FULL, err, __ffs(emask) - 1);
-            break;
+          {  // the buffer of the last access first, every buffer if any lane misses it
+            const uint64_t base = L.bufs[hint].sim_base, bytes = L.bufs[hint].bytes;
+            const bool hit = (va & (uint64_t)(size - 1)) == 0 && va >= base && bytes >= size && va - base <= bytes - size;
+            if (__all_sync(FULL, hit || !on)) {
+              ptr = L.bufs[hint].ptr + (va - base);
+            } else {
+              if (on) err = translate(L, va, size, &ptr);
+              const uint32_t emask = __ballot_sync(FULL, err != 0);
+              if (emask) {
+                status = __shfl_sync(FULL, err, __ffs(emask) - 1);
+                break;
+              }
+              uint32_t bi = 0;
+              if (on) {
+                for (uint32_t k = 0; k < L.n_bufs; k++)
+                  if (ptr >= L.bufs[k].ptr && ptr < L.bufs[k].ptr + L.bufs[k].bytes) bi = k;
+              }
+              hint = __shfl_sync(FULL, bi, __ffs(exec ? exec : 1u) - 1);
+            }
           }
           if (exec) {
             const uint32_t ms = __match_any_sync(FULL, on ? (va >> 5) : ~0ull);
@@ -680,22 +784,14 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
 
     // ---- write-back (a9) ----
     const uint64_t cycles = warp_insts ? epoch + (uint64_t)max(max(t_last + 1u, max_ready), drain) : 0ull;
-    {
-      uint64_t v = 0;
-      switch (lane) {
-        case 0: v = cycles; break;
-        case 1: v = warp_insts; break;
-        case 2: v = thread_insts; break;
-        case 3: v = ld_req; break;
-        case 4: v = ld_sec; break;
-        case 5: v = st_req; break;
-        case 6: v = st_sec; break;
-        case 7: v = ld_lin; break;
-        case 8: v = st_lin; break;
-        case 9: v = (uint64_t)(uint32_t)status | ((uint64_t)max_depth << 32); break;
-        default: v = 0; break;
-      }
-      if (lane < 12) reinterpret_cast<uint64_t*>(L.stats + (uint64_t)gw * sizeof(ks_warp_stats))[lane] = v;
+    if (lane == 0) {
+      ulonglong2* r = reinterpret_cast<ulonglong2*>(L.stats + (uint64_t)gw * sizeof(ks_warp_stats));
+      r[0] = make_ulonglong2(cycles, warp_insts);
+      r[1] = make_ulonglong2(thread_insts, ld_req);
+      r[2] = make_ulonglong2(ld_sec, st_req);
+      r[3] = make_ulonglong2(st_sec, ld_lin);
+      r[4] = make_ulonglong2(st_lin, (uint64_t)(uint32_t)status | ((uint64_t)max_depth << 32));
+      r[5] = make_ulonglong2(0ull, 0ull);
     }
     if (slot) {
       uint32_t* sw = reinterpret_cast<uint32_t*>(slot);
