@@ -294,28 +294,46 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
   } while (0)
 
     if (status == 0) for (;;) {
-      // ---- fast path: runs of unguarded routed FPU / IMAD instructions with
-      // nothing pending. `fuel` = instructions that may run before the
-      // reconvergence pc or the end of the step budget; pc, budget and t_last
-      // are rebuilt when the run ends. Software-pipelined: while instruction k
-      // executes, the rows of instruction k+1 are loaded and the record of k+2
-      // fetched; k+1's rows may predate k's store, so k's result and ready time
-      // are forwarded into any of them that is k's destination.
-      if (__all_sync(FULL, mask != 0u)) {
-        const uint32_t dist = rpc >= pc ? rpc - pc : 0xFFFFFFFFu;
-        uint32_t fuel = min(budget, dist);
-        const uint32_t fuel0 = fuel;
+      // pop finished entries (a6); every control condition below is warp-uniform
+      // in value, and the votes make that visible to the compiler
+      if (__any_sync(FULL, pc == rpc || mask == 0)) {
+        FLUSH_THREADS();
+        if (depth == 1) break;
+        depth--;
+        const uint64_t e = SM64(wb + Y.stack_off + (depth - 1) * 8u);
+        pc = (uint32_t)(e & 0xFFFFu);
+        rpc = (uint32_t)((e >> 16) & 0xFFFFu);
+        mask = (uint32_t)(e >> 32);
+        continue;
+      }
+      // fetch (a2): the first half of the record decides the path. The active
+      // mask is not empty and pc is not the reconvergence pc here; `fuel_in` =
+      // instructions that may run before the reconvergence pc or the end of the
+      // step budget.
+      const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
+      const uint4 q0 = ip[0], q1 = ip[1];
+      const uint32_t fuel_in = min(budget, rpc > pc ? rpc - pc : 0xFFFFFFFFu);
+      const bool runnable = fuel_in != 0u && t_next < REBASE_AT;
+
+      // ---- fast path: runs of unguarded routed FPU / IMAD instructions.
+      // pc, budget and t_last are rebuilt when the run ends. Software-pipelined:
+      // while instruction k executes, the rows of instruction k+1 are loaded and
+      // the record of k+2 fetched; k+1's rows may predate k's store, so k's
+      // result and ready time are forwarded into any of them that is k's
+      // destination.
+      if (runnable && (q0.x | 1u) == DOP_IMAD) {
+        uint32_t fuel = fuel_in;
         const bool on_all = (mask >> lane) & 1u;
-        const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
         // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
-        uint4 ka = ip[0], kb = ip[1];
+        uint4 ka = q0, kb = q1;
         uint2 a = SM2(lb + kb.x), b = SM2(lb + kb.y), c = SM2(lb + kb.z);
         uint32_t rd = SM32(lb + ka.w + 4u);
         // instruction k+1 (the last instruction is never a fast op, so k+1 and
         // k+2 stay within the program and its exit sentinel)
         uint4 na = ip[4], nb = ip[5];
         for (;;) {
-          if (!__all_sync(FULL, fuel != 0u && (ka.x | 1u) == DOP_IMAD && t_next < REBASE_AT)) break;
+          // uniform in value; a plain branch is cheaper here than a vote
+          if (!(fuel != 0u && (ka.x | 1u) == DOP_IMAD && t_next < REBASE_AT)) break;
           uint2 a1 = SM2(lb + nb.x), b1 = SM2(lb + nb.y), c1 = SM2(lb + nb.z);
           uint32_t rd1 = SM32(lb + na.w + 4u);
           const uint4 ma = ip[8], mb = ip[9];
@@ -349,26 +367,22 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           fuel--;
           ip += 4;
         }
-        const uint32_t steps = fuel0 - fuel;
-        if (steps) {
-          pc += steps;
-          budget -= steps;
-          t_last = t_next - 1u;
-        }
+        const uint32_t steps = fuel_in - fuel;  // at least 1
+        pc += steps;
+        budget -= steps;
+        t_last = t_next - 1u;
+        continue;
       }
       // ---- mid path: runs of the other unguarded register-to-register ops
       // (64-bit arithmetic, logic, shifts, conversions, specials, ld.param,
       // div, sqrt), bounded by `fuel` like the fast path, dispatched with one
       // uniform jump per instruction.
-      if (__all_sync(FULL, mask != 0u)) {
-        const uint32_t dist = rpc >= pc ? rpc - pc : 0xFFFFFFFFu;
-        uint32_t fuel = min(budget, dist);
-        const uint32_t fuel0 = fuel;
+      if (runnable && (q1.w & INC_MID) != 0u) {
+        uint32_t fuel = fuel_in;
         const bool on = (mask >> lane) & 1u;
-        const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
+        const uint4* mp = ip;
+        uint4 ka = q0, kb = q1;
         for (;;) {
-          const uint4 ka = ip[0], kb = ip[1];
-          if (!__all_sync(FULL, fuel != 0u && (kb.w & INC_MID) != 0u && t_next < REBASE_AT)) break;
           const uint2 pa = SM2(lb + kb.x), pb = SM2(lb + kb.y), pcc = SM2(lb + kb.z);
           const uint32_t rd = SM32(lb + ka.w + 4u);
           const uint32_t t = max(max(t_next, pa.y), max(max(pb.y, pcc.y), rd));
@@ -431,32 +445,19 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           st_pair(on, s_lane + D, lo, wr);
           st_shared_if(on && wide, s_lane + D + ROW_BYTES, hi);
           fuel--;
-          ip += 4;
+          mp += 4;
+          ka = mp[0];
+          kb = mp[1];
+          if (!__all_sync(FULL, fuel != 0u && (kb.w & INC_MID) != 0u && t_next < REBASE_AT)) break;
         }
-        const uint32_t steps = fuel0 - fuel;
-        if (steps) {
-          pc += steps;
-          budget -= steps;
-          t_last = t_next - 1u;
-          continue;  // maybe a fast run follows
-        }
-      }
-      // ---- general path ----
-      // pop finished entries (a6); every control condition below is warp-uniform
-      // in value, and the votes make that visible to the compiler
-      if (__any_sync(FULL, pc == rpc || mask == 0)) {
-        FLUSH_THREADS();
-        if (depth == 1) break;
-        depth--;
-        const uint64_t e = SM64(wb + Y.stack_off + (depth - 1) * 8u);
-        pc = (uint32_t)(e & 0xFFFFu);
-        rpc = (uint32_t)((e >> 16) & 0xFFFFu);
-        mask = (uint32_t)(e >> 32);
+        const uint32_t steps = fuel_in - fuel;  // at least 1
+        pc += steps;
+        budget -= steps;
+        t_last = t_next - 1u;
         continue;
       }
-      // fetch (a2) and every operand / ready-time load of the instruction at once
-      const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
-      const uint4 q0 = ip[0], q1 = ip[1], q2 = ip[2], q3 = ip[3];
+      // ---- general path: one instruction; every operand / ready-time load at once
+      const uint4 q2 = ip[2], q3 = ip[3];
       const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q2.x, gneg = q2.y, inc = q1.w;
       const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q0.w;
       const uint32_t aux = q0.z;
