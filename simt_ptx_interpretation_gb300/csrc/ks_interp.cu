@@ -116,38 +116,15 @@ __device__ __forceinline__ uint64_t f2i(float f, uint32_t flags) {
   }
 }
 
-__device__ __forceinline__ bool cmp_u(uint64_t a, uint64_t b, uint32_t c) {
-  switch (c) {
-    case CMP_EQ: return a == b;
-    case CMP_NE: return a != b;
-    case CMP_LT: return a < b;
-    case CMP_LE: return a <= b;
-    case CMP_GT: return a > b;
-    default: return a >= b;
-  }
-}
-
-__device__ __forceinline__ bool cmp_s(int64_t a, int64_t b, uint32_t c) {
-  switch (c) {
-    case CMP_EQ: return a == b;
-    case CMP_NE: return a != b;
-    case CMP_LT: return a < b;
-    case CMP_LE: return a <= b;
-    case CMP_GT: return a > b;
-    default: return a >= b;
-  }
-}
-
-__device__ __forceinline__ bool cmp_f(float a, float b, uint32_t c) {
-  if (a != a || b != b) return false;  // ordered comparisons
-  switch (c) {
-    case CMP_EQ: return a == b;
-    case CMP_NE: return a != b;
-    case CMP_LT: return a < b;
-    case CMP_LE: return a <= b;
-    case CMP_GT: return a > b;
-    default: return a >= b;
-  }
+// Comparison results from the three relations. Bit c of each mask is the
+// result of comparison code c (eq, ne, lt, le, gt, ge) when that relation holds;
+// an unordered f32 pair holds none of them, so every code is false (ordered
+// comparisons).
+constexpr uint32_t REL_LT = 0x0Eu;  // ne lt le
+constexpr uint32_t REL_EQ = 0x29u;  // eq le ge
+constexpr uint32_t REL_GT = 0x32u;  // ne gt ge
+__device__ __forceinline__ bool rel_result(bool lt, bool eq, bool gt, uint32_t c) {
+  return (((lt ? REL_LT : 0u) | (eq ? REL_EQ : 0u) | (gt ? REL_GT : 0u)) >> c) & 1u;
 }
 
 // Translates a simulated address for a `size`-byte access; 0 or a status.
@@ -295,8 +272,8 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
 
     if (status == 0) for (;;) {
       // pop finished entries (a6); every control condition below is warp-uniform
-      // in value, and the votes make that visible to the compiler
-      if (__any_sync(FULL, pc == rpc || mask == 0)) {
+      // in value
+      if (pc == rpc || mask == 0) {
         FLUSH_THREADS();
         if (depth == 1) break;
         depth--;
@@ -311,7 +288,7 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       // instructions that may run before the reconvergence pc or the end of the
       // step budget.
       const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
-      const uint4 q0 = ip[0], q1 = ip[1];
+      const uint4 q0 = ip[0], q1 = ip[1], q2 = ip[2], q3 = ip[3];
       const uint32_t fuel_in = min(budget, rpc > pc ? rpc - pc : 0xFFFFFFFFu);
       const bool runnable = fuel_in != 0u && t_next < REBASE_AT;
 
@@ -383,6 +360,7 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
         const uint4* mp = ip;
         uint4 ka = q0, kb = q1;
         for (;;) {
+          const uint4 na = mp[4], nb = mp[5];  // the next record, fetched early
           const uint2 pa = SM2(lb + kb.x), pb = SM2(lb + kb.y), pcc = SM2(lb + kb.z);
           const uint32_t rd = SM32(lb + ka.w + 4u);
           const uint32_t t = max(max(t_next, pa.y), max(max(pb.y, pcc.y), rd));
@@ -446,9 +424,9 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           st_shared_if(on && wide, s_lane + D + ROW_BYTES, hi);
           fuel--;
           mp += 4;
-          ka = mp[0];
-          kb = mp[1];
-          if (!__all_sync(FULL, fuel != 0u && (kb.w & INC_MID) != 0u && t_next < REBASE_AT)) break;
+          ka = na;
+          kb = nb;
+          if (!(fuel != 0u && (kb.w & INC_MID) != 0u && t_next < REBASE_AT)) break;
         }
         const uint32_t steps = fuel_in - fuel;  // at least 1
         pc += steps;
@@ -457,7 +435,6 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
         continue;
       }
       // ---- general path: one instruction; every operand / ready-time load at once
-      const uint4 q2 = ip[2], q3 = ip[3];
       const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q2.x, gneg = q2.y, inc = q1.w;
       const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q0.w;
       const uint32_t aux = q0.z;
@@ -470,7 +447,7 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       const uint32_t rg = SM32(pg + guard * 4u);
       const uint32_t pm = __shfl_sync(FULL, my_pred, guard);
 
-      if (__any_sync(FULL, (inc & INC_ISSUE) == 0u || budget == 0u || t_next >= REBASE_AT)) {  // rare path
+      if ((inc & INC_ISSUE) == 0u || budget == 0u || t_next >= REBASE_AT) {  // rare path
         if (op == OP_EVENT) {  // trace record (a7), zero cost
           if (n_events != 0xFFFFFFFFu) n_events++;
           if (n_rec < L.max_ts) {
@@ -717,15 +694,24 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
         // ---- predicates ----
         case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32: {
           const uint32_t cmp = aux & 0xFFu, pd = (aux >> 8) & 0xFFu;
-          bool r;
-          if (op == OP_SETP_U32) r = cmp_u(a0, b0, cmp);
-          else if (op == OP_SETP_S32) r = cmp_s((int32_t)a0, (int32_t)b0, cmp);
-          else if (op == OP_SETP_U64) r = cmp_u(A64(), B64(), cmp);
-          else if (op == OP_SETP_S64) r = cmp_s((int64_t)A64(), (int64_t)B64(), cmp);
-          else r = cmp_f(__uint_as_float(a0), __uint_as_float(b0), cmp);
-          const uint32_t bal = __ballot_sync(FULL, r);
-          const uint32_t old = __shfl_sync(FULL, my_pred, pd);
-          if (lane == pd) my_pred = (old & ~exec) | (bal & exec);
+          bool lt, eq, gt;
+          if (op == OP_SETP_F32) {
+            const float x = __uint_as_float(a0), y = __uint_as_float(b0);
+            lt = x < y; eq = x == y; gt = x > y;
+          } else {
+            // signed order = unsigned order with the sign bits flipped
+            const bool sgn = op == OP_SETP_S32 || op == OP_SETP_S64;
+            uint64_t x, y;
+            if (op == OP_SETP_U64 || op == OP_SETP_S64) { x = A64(); y = B64(); }
+            else if (sgn) { x = (uint64_t)(int64_t)(int32_t)a0; y = (uint64_t)(int64_t)(int32_t)b0; }
+            else { x = a0; y = b0; }
+            const uint64_t flip = sgn ? (1ull << 63) : 0ull;
+            x ^= flip; y ^= flip;
+            lt = x < y; eq = x == y; gt = x > y;
+          }
+          const uint32_t bal = __ballot_sync(FULL, rel_result(lt, eq, gt, cmp));
+          // lane pd holds predicate pd
+          if (lane == pd) my_pred = (my_pred & ~exec) | (bal & exec);
           pc++;
           break;
         }
@@ -733,9 +719,8 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           const uint32_t pa = __shfl_sync(FULL, my_pred, aux & 0xFFu);
           const uint32_t pb = __shfl_sync(FULL, my_pred, (aux >> 8) & 0xFFu);
           const uint32_t pd = (aux >> 16) & 0xFFu;
-          const uint32_t old = __shfl_sync(FULL, my_pred, pd);
           const uint32_t r = op == OP_ANDP ? (pa & pb) : op == OP_ORP ? (pa | pb) : (pa ^ pb);
-          if (lane == pd) my_pred = (old & ~exec) | (r & exec);
+          if (lane == pd) my_pred = (my_pred & ~exec) | (r & exec);
           pc++;
           break;
         }
