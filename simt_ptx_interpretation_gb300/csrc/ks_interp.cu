@@ -609,7 +609,18 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
               hint = __shfl_sync(FULL, bi, __ffs(exec ? exec : 1u) - 1);
             }
           }
-          if (exec) {
+          // Distinct 32-byte sectors and 128-byte lines over the executing lanes.
+          // With every lane executing and addresses non-decreasing in lane order
+          // (the coalesced case), equal sectors are adjacent and each change from
+          // the lane below starts a new one; otherwise lanes are grouped by value.
+          const uint64_t va_up = __shfl_up_sync(FULL, va, 1);
+          const bool sorted = exec == FULL && __all_sync(FULL, lane == 0 || va >= va_up);
+          if (sorted) {
+            const uint32_t sectors = 1u + __popc(__ballot_sync(FULL, lane != 0 && (va >> 5) != (va_up >> 5)));
+            const uint32_t lines = 1u + __popc(__ballot_sync(FULL, lane != 0 && (va >> 7) != (va_up >> 7)));
+            if (is_ld) { ld_req++; ld_sec += sectors; ld_lin += lines; }
+            else { st_req++; st_sec += sectors; st_lin += lines; }
+          } else if (exec) {
             const uint32_t ms = __match_any_sync(FULL, on ? (va >> 5) : ~0ull);
             const uint32_t sectors = __popc(__ballot_sync(FULL, on && (uint32_t)(__ffs(ms) - 1) == lane));
             const uint32_t ml = __match_any_sync(FULL, on ? (va >> 7) : ~0ull);
@@ -628,9 +639,12 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
               }
             }
           } else {
-            // the highest lane writing an address wins
-            const uint32_t mv = __match_any_sync(FULL, on ? va : ~0ull);
-            if (on && (31u - __clz(mv)) == lane) {
+            // the highest lane writing an address wins: in the sorted case the
+            // last lane of each run of equal addresses
+            const uint64_t va_dn = __shfl_down_sync(FULL, va, 1);
+            const bool wins = sorted ? (lane == 31 || va_dn != va)
+                                     : (31u - __clz(__match_any_sync(FULL, on ? va : ~0ull))) == lane;
+            if (on && wins) {
               if (wide) *reinterpret_cast<uint64_t*>(ptr) = B64();
               else *reinterpret_cast<uint32_t*>(ptr) = b0;
             }
