@@ -50,11 +50,15 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--iters", type=int, default=4096, help="FFMA outer iterations (smaller cases for profiling)")
+    p.add_argument("--scale", type=int, default=1,
+                   help="divide the gather outputs, divergent threads or fuzz kernels (smaller cases for profiling)")
     return p.parse_args()
 
 
-def workloads(name: str, iters: int = 4096):
+def workloads(name: str, iters: int = 4096, scale: int = 1):
     from simt_ptx_interpretation_gb300 import workloads as wl
+    if scale < 1 or scale & (scale - 1):
+        raise SystemExit("--scale must be a power of two")
     if name == "ffma_pair":
         return [wl.ffma(acc=1, iters=iters), wl.ffma(acc=8, iters=iters)], {
             "workload": "ffma_probe_pair", "grid": 132, "block": 128, "iters": iters, "fma_per_iter": 32,
@@ -63,13 +67,16 @@ def workloads(name: str, iters: int = 4096):
         return [wl.vector_add()], {"workload": "vector_add", "n": 4000, "grid": 16, "block": 256, "seed": 0}
     if name.startswith("gather_s"):
         s = int(name[len("gather_s"):])
-        return [wl.gather(s)], {"workload": name, "n_out": 1 << 24, "stride": s, "block": 256, "seed": 1}
+        n_out = max(256, (1 << 24) // scale)
+        return [wl.gather(s, n_out=n_out)], {"workload": name, "n_out": n_out, "stride": s, "block": 256, "seed": 1}
     if name.startswith("divergent_k"):
         k = int(name[len("divergent_k"):])
-        return [wl.divergent(k)], {"workload": name, "threads": 1 << 20, "block": 128, "k": k, "seed": 3}
+        n = max(128, (1 << 20) // scale)
+        return [wl.divergent(k, n=n)], {"workload": name, "threads": n, "block": 128, "k": k, "seed": 3}
     if name == "fuzz":
-        return [wl.fuzz(i) for i in range(64)], {"workload": "fuzz64", "grid": 1024, "block": 256, "kernels": 64,
-                                                 "seed": "1000+i, data 4"}
+        nk = max(1, 64 // scale)
+        return [wl.fuzz(i) for i in range(nk)], {"workload": "fuzz64" if nk == 64 else f"fuzz{nk}", "grid": 1024,
+                                                 "block": 256, "kernels": nk, "seed": "1000+i, data 4"}
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -193,7 +200,7 @@ def run_ours(args, world, rank, local):
         _build.build_native()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    ws, config = workloads(args.workload, args.iters)
+    ws, config = workloads(args.workload, args.iters, args.scale)
     stream = torch.cuda.current_stream(dev)
 
     # inputs resident in HBM; outputs preallocated
@@ -349,7 +356,7 @@ def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    ws, config = workloads(args.workload, args.iters)
+    ws, config = workloads(args.workload, args.iters, args.scale)
     cores = os.cpu_count() or 1
     per = max(4, min(64, 2 * cores))
     for _ in range(args.warmup):
