@@ -263,21 +263,10 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   L.param_bytes = (uint32_t)param_bytes;
   if (param_bytes) std::memcpy(L.params, params, param_bytes);
 
-  // ---- real launch shape: as many real warps as simulated warps, up to the
-  // resident capacity; CTAs small enough that every SM gets work ----
-  const uint32_t region = k->layout.region_bytes;
-  uint32_t wpc_real = 8;
-  while (wpc_real > 1 && (W + wpc_real - 1) / wpc_real < 2ull * (uint64_t)di.sms) wpc_real /= 2;
-  while (wpc_real > 1 && ks::interp_smem_bytes(L.image_bytes, region, wpc_real) > (size_t)di.max_smem)
-    wpc_real /= 2;
-  const size_t smem = ks::interp_smem_bytes(L.image_bytes, region, wpc_real);
-  if (smem > (size_t)di.max_smem) return KS_ERR_LIMIT;
-  int per_sm = 0;
-  if (ks::interp_occupancy(wpc_real, smem, &per_sm) != 0) return KS_ERR_CUDA;
-  if (per_sm < 1) return KS_ERR_LIMIT;
-  const uint64_t want = (W + wpc_real - 1) / wpc_real;
-  const uint64_t cap = (uint64_t)di.sms * (uint64_t)per_sm;
-  const uint32_t ctas = (uint32_t)std::min(want, cap);
+  // ---- real launch shape (persistent real warps, see ks::choose_launch) ----
+  uint32_t wpc_real = 0, ctas = 0;
+  const int shape = ks::choose_launch(W, L.image_bytes, k->layout.region_bytes, di.sms, di.max_smem, &wpc_real, &ctas);
+  if (shape != KS_OK) return shape;
   if (ks::launch_interp(L, wpc_real, ctas, stream) != 0) return KS_ERR_CUDA;
   return KS_OK;
 }

@@ -212,6 +212,11 @@ uint32_t interp_region0(uint32_t image_bytes);
 const KsKernel* module_kernel(const ks_module* mod, const char* name);
 
 // Launchers (ks_interp.cu). Return a cudaError_t value.
+// Real launch shape for `n_warps` simulated warps: real warps per CTA (1..8)
+// and real CTAs (persistent). KS_OK, KS_ERR_LIMIT (no shape fits the shared
+// memory) or KS_ERR_CUDA.
+int choose_launch(uint64_t n_warps, uint32_t image_bytes, uint32_t region_bytes, int sms, int max_smem,
+                  uint32_t* real_warps_per_cta, uint32_t* real_ctas);
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);
 int interp_occupancy(uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
 int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream);

@@ -32,6 +32,7 @@
 // epoch that moves forward before any clock reaches 2^31.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "ks_internal.h"
@@ -879,6 +880,40 @@ int interp_occupancy(uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm)
   if (e) return e;
   return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, ks_interp_kernel,
                                                             (int)(real_warps_per_cta * 32), smem);
+}
+
+int choose_launch(uint64_t n_warps, uint32_t image_bytes, uint32_t region_bytes, int sms, int max_smem,
+                  uint32_t* real_warps_per_cta, uint32_t* real_ctas) {
+  // Candidates: 1..8 real warps per CTA. While the simulated grid is small,
+  // keep at least two CTAs per SM so that every SM gets work; among the rest
+  // take the shape with the most resident real warps (shared memory,
+  // registers and the CTA limit all count), then the larger CTA (fewer
+  // program copies).
+  uint32_t best_w = 0, best_ctas = 0;
+  uint64_t best_res = 0;
+  bool any_fit = false;
+  for (uint32_t w = 1; w <= 8; w++) {
+    const size_t smem = interp_smem_bytes(image_bytes, region_bytes, w);
+    if (smem > (size_t)max_smem) break;
+    any_fit = true;
+    const uint64_t want = (n_warps + w - 1) / w;
+    if (w > 1 && want < 2ull * (uint64_t)sms) break;
+    int per_sm = 0;
+    const int e = interp_occupancy(w, smem, &per_sm);
+    if (e) return KS_ERR_CUDA;
+    if (per_sm < 1) continue;
+    const uint64_t cap = (uint64_t)sms * (uint64_t)per_sm;
+    const uint64_t res = std::min<uint64_t>(n_warps, cap * w);
+    if (res >= best_res) {
+      best_res = res;
+      best_w = w;
+      best_ctas = (uint32_t)std::min<uint64_t>(want, cap);
+    }
+  }
+  if (!any_fit || best_w == 0) return KS_ERR_LIMIT;
+  *real_warps_per_cta = best_w;
+  *real_ctas = best_ctas;
+  return KS_OK;
 }
 
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream) {

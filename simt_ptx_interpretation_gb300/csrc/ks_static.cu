@@ -120,19 +120,10 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   L.param_bytes = (uint32_t)param_bytes;
   if (param_bytes) std::memcpy(L.params, params, param_bytes);
 
-  const int sms = g_static_sms[dev], max_smem = g_static_smem[dev];
-  const uint32_t region = k->layout.region_bytes;
-  uint32_t wpc_real = 8;
-  while (wpc_real > 1 && (W + wpc_real - 1) / wpc_real < 2ull * (uint64_t)sms) wpc_real /= 2;
-  while (wpc_real > 1 && ks::interp_smem_bytes(L.image_bytes, region, wpc_real) > (size_t)max_smem) wpc_real /= 2;
-  const size_t smem = ks::interp_smem_bytes(L.image_bytes, region, wpc_real);
-  if (smem > (size_t)max_smem) return KS_ERR_LIMIT;
-  int per_sm = 0;
-  if (ks::interp_occupancy(wpc_real, smem, &per_sm) != 0) return KS_ERR_CUDA;
-  if (per_sm < 1) return KS_ERR_LIMIT;
-  const uint64_t want = (W + wpc_real - 1) / wpc_real;
-  const uint64_t cap = (uint64_t)sms * (uint64_t)per_sm;
-  const uint32_t ctas = (uint32_t)(want < cap ? want : cap);
+  uint32_t wpc_real = 0, ctas = 0;
+  const int shape = ks::choose_launch(W, L.image_bytes, k->layout.region_bytes, g_static_sms[dev],
+                                      g_static_smem[dev], &wpc_real, &ctas);
+  if (shape != KS_OK) return shape;
   if (ks::launch_interp(L, wpc_real, ctas, stream) != 0) return KS_ERR_CUDA;
   return KS_OK;
 }
