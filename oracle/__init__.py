@@ -40,7 +40,10 @@ _lib = None
 
 MODE_WARP = 0
 MODE_PER_THREAD = 1
-DEFAULT_LAT = (4, 4, 400, 20, 8, 36, 1, 0)
+RACE_CROSS_THREAD = 1  # two threads touch one word, at least one writing
+# ALU, FMA, ld.global, st.global, bra, div/sqrt, ret, ld.shared, st.shared,
+# bar.sync, two reserved classes
+DEFAULT_LAT = (4, 4, 400, 20, 8, 36, 1, 23, 23, 20, 0, 0)
 
 STATS_DTYPE = np.dtype(
     [
@@ -55,7 +58,8 @@ STATS_DTYPE = np.dtype(
         ("st_lines", "<u8"),
         ("status", "<i4"),
         ("max_stack_depth", "<u4"),
-        ("reserved", "<u8", (2,)),
+        ("sh_req", "<u8"),
+        ("sh_wavefronts", "<u8"),
     ]
 )
 assert STATS_DTYPE.itemsize == 96
@@ -67,7 +71,7 @@ class _Buffer(ctypes.Structure):
 
 class _Config(ctypes.Structure):
     _fields_ = [
-        ("lat", ctypes.c_uint32 * 8),
+        ("lat", ctypes.c_uint32 * 12),
         ("max_ts_per_warp", ctypes.c_uint32),
         ("stack_depth", ctypes.c_uint32),
         ("step_limit", ctypes.c_uint64),
@@ -165,7 +169,7 @@ def run(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffers, *,
         bufs[i].host = arr.ctypes.data
         bufs[i].bytes = arr.nbytes
     cfg = _Config()
-    for i in range(8):
+    for i in range(12):
         cfg.lat[i] = lat[i] if i < len(lat) else 0
     cfg.max_ts_per_warp = max_ts
     cfg.stack_depth = stack_depth

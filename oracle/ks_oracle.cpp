@@ -22,6 +22,12 @@
  *    latency per instruction class (values supplied by the caller).
  *  - CuTeDSL IKET 浅析 §2 — per-warp slot of a 16-byte header plus
  *    maxTsCntPerWarp records, no cross-warp atomics, overflow counted not lost.
+ *  - KernelScope backend doc, simulator/models.py Block (a 48 KB zeroed shared
+ *    array and a barrier per block), simulator/engine.py step (warps waiting
+ *    at a barrier are skipped) and analyze_shared_memory_access (bank =
+ *    (address / 4) % 32; a bank whose lanes all use one address is a
+ *    broadcast; otherwise its conflict degree is its number of lanes; the
+ *    request's degree, its transactions, is the largest over banks, at least 1).
  *
  * Readings where the pages are silent (each applied identically on the GPU):
  *  - %tid.x is the thread's index in its CTA (the page's `tid % 32` is the lane).
@@ -39,6 +45,20 @@
  *  - Sectors: distinct addr>>5 over the executing lanes; lines: distinct addr>>7.
  *  - f32 arithmetic is IEEE binary32 round-to-nearest-even with subnormals;
  *    every NaN result of add/sub/mul/fma/div/sqrt is written as 0x7FFFFFFF.
+ *  - Barriers are per warp, as the page's Warp.at_barrier: a warp that issues
+ *    bar.sync 0 (any active mask) stops; when every warp of the CTA has
+ *    stopped at a barrier or finished, the stopped warps resume with
+ *    t_next = (latest bar.sync issue cycle among them) + the bar.sync latency.
+ *    A finished warp never holds a barrier. Only barrier 0 without a thread
+ *    count, unguarded.
+ *  - Shared memory: .shared arrays declared in the kernel body, laid out in
+ *    declaration order at their alignment from address 0, at most 48 KiB; a
+ *    shared address is a register (32- or 64-bit, zero-extended) or a symbol,
+ *    plus an offset. Misaligned (checked first) or out-of-range accesses give
+ *    the same statuses as global ones. The bank rule reads each lane's
+ *    address only, for 4- and 8-byte accesses alike. ld.shared results are
+ *    ready at t + the ld.shared latency; a shared store completes at t + the
+ *    st.shared latency. Bank conflicts do not change the timing.
  */
 #include "ks_oracle.h"
 
@@ -100,7 +120,8 @@ bool is_int_ty(Ty t) { return t == TY_U32 || t == TY_S32 || t == TY_U64 || t == 
 
 enum Kind {
   K_ADD, K_SUB, K_MUL, K_MAD, K_FMA, K_DIV, K_SQRT, K_AND, K_OR, K_XOR, K_SHL, K_SHR,
-  K_CVT, K_MOV, K_SETP, K_SELP, K_BRA, K_LDG, K_STG, K_LDP, K_RET, K_EVENT
+  K_CVT, K_MOV, K_SETP, K_SELP, K_BRA, K_LDG, K_STG, K_LDP, K_RET, K_EVENT,
+  K_LDS, K_STS, K_BAR
 };
 
 enum Special { SP_TID_X, SP_TID_Y, SP_TID_Z, SP_NTID_X, SP_NTID_Y, SP_NTID_Z, SP_CTAID_X,
@@ -146,6 +167,11 @@ struct Kernel {
   std::vector<uint32_t> event_kind;   // 0 mark, 1 range_start, 2 range_end
   std::vector<std::string> event_name;
   std::vector<int> ipdom;             // per entry, n = virtual exit
+  std::map<std::string, uint32_t> shared_sym;  // .shared array -> its shared address
+  uint32_t shared_bytes = 0;
+  bool has_bar = false;
+  // CTA by CTA: the warps of a CTA share memory or barriers
+  bool cta_mode() const { return shared_bytes > 0 || has_bar; }
 };
 
 // --------------------------------------------------------------- parsing ----
@@ -310,6 +336,62 @@ struct Parser {
         K.regs.push_back(Reg{r, width_of(t)});
       }
     }
+  }
+
+  // .shared [.align A] .TYPE name[N]  (or a scalar without [N])
+  void declare_shared(const std::string& stmt, int line) {
+    std::vector<std::string> w;
+    for (const std::string& x : split(stmt, ' '))
+      for (const std::string& y : split(x, '\t'))
+        if (!trim(y).empty()) w.push_back(trim(y));
+    size_t i = 1;
+    uint64_t align = 0;
+    if (i + 1 < w.size() && w[i] == ".align") {
+      Lit a = parse_int_literal(w[i + 1]);
+      if (!a.ok || a.neg || a.mag == 0 || (a.mag & (a.mag - 1)) || a.mag > 4096) fail(ORC_ERR_PARSE, line, "bad .align");
+      align = a.mag;
+      i += 2;
+    }
+    if (i + 2 != w.size()) fail(ORC_ERR_UNSUPPORTED, line, "unsupported .shared declaration");
+    static const std::map<std::string, uint32_t> esz = {
+        {".b8", 1}, {".u8", 1}, {".s8", 1}, {".b16", 2}, {".u16", 2}, {".s16", 2},
+        {".b32", 4}, {".u32", 4}, {".s32", 4}, {".f32", 4},
+        {".b64", 8}, {".u64", 8}, {".s64", 8}, {".f64", 8}};
+    auto et = esz.find(w[i]);
+    if (et == esz.end()) fail(ORC_ERR_UNSUPPORTED, line, "unsupported .shared type " + w[i]);
+    std::string nm = w[i + 1];
+    uint64_t count = 1;
+    size_t lb = nm.find('[');
+    if (lb != std::string::npos) {
+      if (nm.back() != ']') fail(ORC_ERR_PARSE, line, "bad .shared array");
+      Lit c = parse_int_literal(nm.substr(lb + 1, nm.size() - lb - 2));
+      if (!c.ok || c.neg || c.mag == 0 || c.mag > (1u << 20)) fail(ORC_ERR_PARSE, line, "bad .shared array size");
+      count = c.mag;
+      nm = nm.substr(0, lb);
+    }
+    if (!valid_ident(nm)) fail(ORC_ERR_PARSE, line, "bad .shared name");
+    if (K.shared_sym.count(nm)) fail(ORC_ERR_PARSE, line, "shared array declared twice: " + nm);
+    if (!align) align = et->second;
+    const uint64_t off = (K.shared_bytes + align - 1) / align * align;
+    const uint64_t end = off + count * et->second;
+    if (end > 49152) fail(ORC_ERR_UNSUPPORTED, line, "more than 48 KiB of shared memory");
+    K.shared_sym[nm] = (uint32_t)off;
+    K.shared_bytes = (uint32_t)end;
+  }
+
+  // A shared address operand: [%r(+off)] with a 32- or 64-bit register, or
+  // [symbol(+off)], which becomes a register-free address.
+  void shared_address(Opnd& o, int line) {
+    if (o.k == Opnd::PARAM) {
+      auto it = K.shared_sym.find(o.label);
+      if (it == K.shared_sym.end()) fail(ORC_ERR_PARSE, line, "unknown shared array " + o.label);
+      o.k = Opnd::MEM;
+      o.reg = -1;
+      o.off += (int64_t)it->second;
+      return;
+    }
+    if (o.k != Opnd::MEM || !(K.regs[o.reg].width == 32 || K.regs[o.reg].width == 64))
+      fail(ORC_ERR_PARSE, line, "shared address must be [register(+offset)] or [array(+offset)]");
   }
 
   void add_entry(Inst in) {
@@ -547,7 +629,16 @@ struct Parser {
       need(2);
       int w = width_of(t);
       in.d = ops[0]; check(in.d, w, 'r', t, line);
-      in.a = ops[1]; check(in.a, w, 'm', t, line);
+      in.a = ops[1];
+      if (in.a.k == Opnd::LABEL) {  // the shared address of an array
+        auto it = K.shared_sym.find(in.a.label);
+        if (it == K.shared_sym.end() || t == TY_F32) fail(ORC_ERR_PARSE, line, "bad mov operand " + in.a.label);
+        in.a.k = Opnd::IMM;
+        in.a.imm = it->second;
+        in.a.spec = 2;
+        in.a.off = it->second;
+      }
+      check(in.a, w, 'm', t, line);
     } else if (op == "setp") {
       in.k = K_SETP;
       if (mods.size() != 2) bad();
@@ -587,6 +678,19 @@ struct Parser {
       need(1);
       if (ops[0].k != Opnd::LABEL) fail(ORC_ERR_PARSE, line, "bra needs a label");
       in.a = ops[0];
+    } else if (op == "bar" || op == "barrier") {
+      // bar.sync 0 / barrier.sync[.aligned] 0: CTA barrier 0 over every thread
+      const bool form = (op == "bar" && mods.size() == 1 && mods[0] == "sync") ||
+                        (op == "barrier" && (mods.size() == 1 || mods.size() == 2) && mods[0] == "sync" &&
+                         (mods.size() == 1 || mods[1] == "aligned"));
+      if (!form) bad();
+      need(1);
+      if (ops[0].k != Opnd::IMM || ops[0].spec != 2 || ops[0].imm != 0)
+        fail(ORC_ERR_UNSUPPORTED, line, "only barrier 0 without a thread count is supported");
+      if (in.guard >= 0) fail(ORC_ERR_UNSUPPORTED, line, "guarded bar.sync is not supported");
+      in.k = K_BAR;
+      in.cls = ORC_LAT_BAR;
+      K.has_bar = true;
     } else if (op == "ret" || op == "exit") {
       in.k = K_RET;
       in.cls = ORC_LAT_RET;
@@ -621,6 +725,14 @@ struct Parser {
         in.k = K_STG; in.cls = ORC_LAT_STG;
         in.a = ops[0];
         if (in.a.k != Opnd::MEM || K.regs[in.a.reg].width != 64) fail(ORC_ERR_PARSE, line, "st.global needs [64-bit register(+offset)]");
+        in.b = ops[1]; check(in.b, w, 'r', t, line);
+      } else if (op == "ld" && mods[0] == "shared") {
+        in.k = K_LDS; in.cls = ORC_LAT_LDS;
+        in.d = ops[0]; check(in.d, w, 'r', t, line);
+        in.a = ops[1]; shared_address(in.a, line);
+      } else if (op == "st" && mods[0] == "shared") {
+        in.k = K_STS; in.cls = ORC_LAT_STS;
+        in.a = ops[0]; shared_address(in.a, line);
         in.b = ops[1]; check(in.b, w, 'r', t, line);
       } else {
         bad();
@@ -675,6 +787,7 @@ struct Parser {
     }
     if (s.empty()) return;
     if (s.compare(0, 4, ".reg") == 0) { declare_regs(s, line); return; }
+    if (s.compare(0, 7, ".shared") == 0) { declare_shared(s, line); return; }
     if (s.compare(0, 5, "@iket") == 0) { event(s, line); return; }
     if (s[0] == '.') fail(ORC_ERR_UNSUPPORTED, line, "unsupported directive in kernel body: " + s);
     instruction(s, line);
@@ -1112,209 +1225,432 @@ struct Launch {
   uint64_t slot_bytes;
 };
 
+// ------------------------------------------------- shared memory (per CTA) ----
+
+struct CtaMem {
+  std::vector<uint8_t> bytes;  // zeroed at the start of the CTA
+  // race checker state per 4-byte word, cleared at every barrier release
+  bool race_on = false;
+  std::vector<int64_t> writer, reader;
+  uint32_t race_flags = 0;
+
+  CtaMem(uint32_t size, bool race) : bytes(size, 0), race_on(race) {
+    if (race_on) {
+      writer.assign(size / 4 + 1, -1);
+      reader.assign(size / 4 + 1, -1);
+    }
+  }
+  void new_interval() {
+    if (!race_on) return;
+    std::fill(writer.begin(), writer.end(), -1);
+    std::fill(reader.begin(), reader.end(), -1);
+  }
+  void note(uint64_t off, uint32_t size, int64_t gtid, bool write) {
+    if (!race_on) return;
+    for (uint64_t w = off / 4; w < (off + size + 3) / 4; w++) {
+      int64_t& wr = writer[(size_t)w];
+      int64_t& rd = reader[(size_t)w];
+      if (write) {
+        if (wr >= 0 && wr != gtid) race_flags |= ORC_RACE_CROSS_THREAD;
+        if (rd != -1 && rd != gtid) race_flags |= ORC_RACE_CROSS_THREAD;
+        wr = gtid;
+      } else {
+        if (wr >= 0 && wr != gtid) race_flags |= ORC_RACE_CROSS_THREAD;
+        if (rd == -1) rd = gtid; else if (rd != gtid) rd = -2;
+      }
+    }
+  }
+};
+
+// The shared address of a lane: register (zero-extended) plus offset.
+uint64_t shared_addr(const Inst& in, const Lane& L) {
+  uint64_t base = in.a.reg >= 0 ? L.v[(size_t)in.a.reg] : 0;
+  return base + (uint64_t)in.a.off;
+}
+
+// 0, or the status of a shared access of `size` bytes at `addr`.
+int shared_check(uint64_t addr, uint32_t size, uint32_t shared_bytes) {
+  if (addr % size != 0) return ORC_ST_MISALIGNED;
+  if (shared_bytes < size || addr > (uint64_t)shared_bytes - size) return ORC_ST_OOB;
+  return 0;
+}
+
+// Bank-conflict degree of one request over the executing lanes (the page's
+// analyze_shared_memory_access, written out): lanes grouped by bank; a bank
+// whose lanes all use one address is a broadcast and counts 1, any other bank
+// counts its lanes; the request's degree is the largest count, at least 1.
+uint32_t bank_degree(const uint64_t* addr, uint32_t exec) {
+  std::map<uint64_t, std::vector<uint64_t>> banks;
+  for (int i = 0; i < 32; i++)
+    if ((exec >> i) & 1) banks[(addr[i] / 4) % 32].push_back(addr[i]);
+  uint32_t worst = 1;
+  for (const auto& kv : banks) {
+    const std::vector<uint64_t>& a = kv.second;
+    const bool broadcast = std::set<uint64_t>(a.begin(), a.end()).size() == 1;
+    if (!broadcast) worst = std::max(worst, (uint32_t)a.size());
+  }
+  return worst;
+}
+
 // ---------------------------------------------------------- warp mode ----
 
 struct Entry { int pc, rpc; uint32_t mask; };
 
-void run_warp(const Launch& X, Memory& M, uint32_t gwarp) {
-  const Kernel& K = *X.K;
-  const orc_config& cfg = *X.cfg;
-  const int n = (int)K.code.size();
-  const uint32_t cta = gwarp / X.warps_per_cta;
-  const uint32_t wic = gwarp % X.warps_per_cta;
-
-  std::vector<Lane> lanes(32);
-  std::vector<LaneCtx> ctx(32);
-  uint32_t mask0 = 0;
-  for (uint32_t i = 0; i < 32; i++) {
-    lanes[i].v.assign(K.regs.size(), 0);
-    ctx[i] = LaneCtx{wic * 32 + i, X.block, cta, X.grid, i};
-    if (wic * 32 + i < X.block) mask0 |= 1u << i;
-  }
+// One simulated warp, resumable at barriers.
+struct WarpRun {
+  const Launch* X;
+  uint32_t gwarp, cta, wic;
+  std::vector<Lane> lanes;
+  std::vector<LaneCtx> ctx;
   std::vector<Entry> stack;
-  stack.push_back(Entry{0, n, mask0});
-
-  std::vector<uint64_t> ready(K.regs.size(), 0);
+  std::vector<uint64_t> ready;
   uint64_t t_next = 0, t_last = 0, max_ready = 0, drain = 0;
   orc_warp_stats st;
-  std::memset(&st, 0, sizeof st);
-  st.max_stack_depth = 1;
   uint32_t n_events = 0, n_dropped = 0;
   std::vector<uint32_t> records;
 
-  while (!stack.empty()) {
-    Entry& top = stack.back();
-    if (top.pc == top.rpc || top.mask == 0) { stack.pop_back(); continue; }
-    if (top.pc >= n) { top.mask = 0; continue; }  // virtual exit: remaining lanes finish
-    const int pc = top.pc;
-    const Inst& in = K.code[(size_t)pc];
-
-    if (in.k == K_EVENT) {  // zero-cost pseudo-op
-      if (n_events != 0xFFFFFFFFu) n_events++;
-      if (records.size() < cfg.max_ts_per_warp)
-        records.push_back(((uint32_t)(in.event & 0xFF) << 24) | (uint32_t)(t_next & 0xFFFFFF));
-      else if (n_dropped < 0xFFFF)
-        n_dropped++;
-      top.pc = pc + 1;
-      continue;
+  WarpRun(const Launch& L, uint32_t gw) : X(&L), gwarp(gw) {
+    const Kernel& K = *X->K;
+    cta = gwarp / X->warps_per_cta;
+    wic = gwarp % X->warps_per_cta;
+    lanes.resize(32);
+    ctx.resize(32);
+    uint32_t mask0 = 0;
+    for (uint32_t i = 0; i < 32; i++) {
+      lanes[i].v.assign(K.regs.size(), 0);
+      ctx[i] = LaneCtx{wic * 32 + i, X->block, cta, X->grid, i};
+      if (wic * 32 + i < X->block) mask0 |= 1u << i;
     }
-    if (cfg.inject_warp >= 0 && (uint64_t)cfg.inject_warp == gwarp && st.warp_insts == cfg.inject_step) {
-      st.status = ORC_ST_INJECTED;
-      break;
-    }
-    if (st.warp_insts == cfg.step_limit) { st.status = ORC_ST_STEP_LIMIT; break; }
+    stack.push_back(Entry{0, (int)K.code.size(), mask0});
+    ready.assign(K.regs.size(), 0);
+    std::memset(&st, 0, sizeof st);
+    st.max_stack_depth = 1;
+  }
 
-    // ---- issue: in-order scoreboard ----
-    std::vector<int> srcs, dsts;
-    auto src = [&](const Opnd& o) { if ((o.k == Opnd::REG || o.k == Opnd::MEM) && o.reg >= 0) srcs.push_back(o.reg); };
-    if (in.k == K_STG) { src(in.a); src(in.b); }
-    else if (in.k != K_BRA && in.k != K_RET) {
-      src(in.a); src(in.b); src(in.c);
-      dsts.push_back(in.d.reg);
-    }
-    if (in.guard >= 0) srcs.push_back(in.guard);
-    uint64_t t = t_next;
-    for (int r : srcs) t = std::max(t, ready[(size_t)r]);
-    for (int r : dsts) t = std::max(t, ready[(size_t)r]);
-    uint64_t lat = cfg.lat[in.cls];
-    for (int r : dsts) { ready[(size_t)r] = t + lat; max_ready = std::max(max_ready, t + lat); }
-    if (in.k == K_STG) drain = std::max(drain, t + lat);
-    t_last = t;
-    t_next = (in.k == K_BRA || in.k == K_RET) ? t + lat : t + 1;
-    st.warp_insts++;
-    st.thread_insts += (uint64_t)popcount32(top.mask);
+  // Interprets until the warp finishes (returns false) or issues bar.sync
+  // (returns true with the issue cycle in *arrival).
+  bool run(Memory& M, CtaMem* S, uint64_t* arrival) {
+    const Kernel& K = *X->K;
+    const orc_config& cfg = *X->cfg;
+    const int n = (int)K.code.size();
+    while (!stack.empty()) {
+      Entry& top = stack.back();
+      if (top.pc == top.rpc || top.mask == 0) { stack.pop_back(); continue; }
+      if (top.pc >= n) { top.mask = 0; continue; }  // virtual exit: remaining lanes finish
+      const int pc = top.pc;
+      const Inst& in = K.code[(size_t)pc];
 
-    // ---- guard ----
-    uint32_t exec = 0;
-    for (int i = 0; i < 32; i++) {
-      if (!((top.mask >> i) & 1)) continue;
-      bool g = true;
-      if (in.guard >= 0) g = (lanes[(size_t)i].v[(size_t)in.guard] != 0) != in.guard_neg;
-      if (g) exec |= 1u << i;
-    }
-
-    // ---- execute ----
-    if (in.k == K_BRA) {
-      uint32_t taken = exec, fall = top.mask & ~exec;
-      if (fall == 0) { top.pc = in.target; }
-      else if (taken == 0) { top.pc = pc + 1; }
-      else {
-        int R = K.ipdom[(size_t)pc];
-        if (top.rpc == R) stack.pop_back(); else top.pc = R;
-        bool overflow = false;
-        if (in.target != R) {
-          if (stack.size() >= cfg.stack_depth) overflow = true;
-          else stack.push_back(Entry{in.target, R, taken});
-        }
-        if (!overflow && pc + 1 != R) {
-          if (stack.size() >= cfg.stack_depth) overflow = true;
-          else stack.push_back(Entry{pc + 1, R, fall});
-        }
-        if (overflow) { st.status = ORC_ST_SIMT_STACK; break; }
-        st.max_stack_depth = std::max(st.max_stack_depth, (uint32_t)stack.size());
+      if (in.k == K_EVENT) {  // zero-cost pseudo-op
+        if (n_events != 0xFFFFFFFFu) n_events++;
+        if (records.size() < cfg.max_ts_per_warp)
+          records.push_back(((uint32_t)(in.event & 0xFF) << 24) | (uint32_t)(t_next & 0xFFFFFF));
+        else if (n_dropped < 0xFFFF)
+          n_dropped++;
+        top.pc = pc + 1;
+        continue;
       }
-      continue;
-    }
-    if (in.k == K_RET) {
-      for (Entry& e : stack) e.mask &= ~exec;
-      stack.back().pc = pc + 1;
-      continue;
-    }
-    if (in.k == K_LDG || in.k == K_STG) {
-      uint32_t size = (uint32_t)width_of(in.ty) / 8;
-      uint64_t addr[32];
-      uint8_t* host[32];
-      int bi[32];
-      uint64_t off[32];
-      int err = 0;
-      for (int i = 0; i < 32 && !err; i++) {
-        if (!((exec >> i) & 1)) continue;
-        addr[i] = lanes[(size_t)i].v[(size_t)in.a.reg] + (uint64_t)in.a.off;
-        err = M.translate(addr[i], size, &host[i], &bi[i], &off[i]);
+      if (cfg.inject_warp >= 0 && (uint64_t)cfg.inject_warp == gwarp && st.warp_insts == cfg.inject_step) {
+        st.status = ORC_ST_INJECTED;
+        return false;
       }
-      if (err) { st.status = err; break; }
-      if (exec) {
-        std::set<uint64_t> sectors, lines;
-        for (int i = 0; i < 32; i++) {
+      if (st.warp_insts == cfg.step_limit) { st.status = ORC_ST_STEP_LIMIT; return false; }
+
+      // ---- issue: in-order scoreboard ----
+      std::vector<int> srcs, dsts;
+      auto src = [&](const Opnd& o) { if ((o.k == Opnd::REG || o.k == Opnd::MEM) && o.reg >= 0) srcs.push_back(o.reg); };
+      if (in.k == K_STG || in.k == K_STS) { src(in.a); src(in.b); }
+      else if (in.k != K_BRA && in.k != K_RET && in.k != K_BAR) {
+        src(in.a); src(in.b); src(in.c);
+        dsts.push_back(in.d.reg);
+      }
+      if (in.guard >= 0) srcs.push_back(in.guard);
+      uint64_t t = t_next;
+      for (int r : srcs) t = std::max(t, ready[(size_t)r]);
+      for (int r : dsts) t = std::max(t, ready[(size_t)r]);
+      uint64_t lat = cfg.lat[in.cls];
+      for (int r : dsts) { ready[(size_t)r] = t + lat; max_ready = std::max(max_ready, t + lat); }
+      if (in.k == K_STG || in.k == K_STS) drain = std::max(drain, t + lat);
+      t_last = t;
+      t_next = (in.k == K_BRA || in.k == K_RET) ? t + lat : t + 1;
+      st.warp_insts++;
+      st.thread_insts += (uint64_t)popcount32(top.mask);
+
+      // ---- guard ----
+      uint32_t exec = 0;
+      for (int i = 0; i < 32; i++) {
+        if (!((top.mask >> i) & 1)) continue;
+        bool g = true;
+        if (in.guard >= 0) g = (lanes[(size_t)i].v[(size_t)in.guard] != 0) != in.guard_neg;
+        if (g) exec |= 1u << i;
+      }
+
+      // ---- execute ----
+      if (in.k == K_BAR) {  // stop here until the CTA's barrier releases
+        top.pc = pc + 1;
+        *arrival = t;
+        return true;
+      }
+      if (in.k == K_BRA) {
+        uint32_t taken = exec, fall = top.mask & ~exec;
+        if (fall == 0) { top.pc = in.target; }
+        else if (taken == 0) { top.pc = pc + 1; }
+        else {
+          int R = K.ipdom[(size_t)pc];
+          if (top.rpc == R) stack.pop_back(); else top.pc = R;
+          bool overflow = false;
+          if (in.target != R) {
+            if (stack.size() >= cfg.stack_depth) overflow = true;
+            else stack.push_back(Entry{in.target, R, taken});
+          }
+          if (!overflow && pc + 1 != R) {
+            if (stack.size() >= cfg.stack_depth) overflow = true;
+            else stack.push_back(Entry{pc + 1, R, fall});
+          }
+          if (overflow) { st.status = ORC_ST_SIMT_STACK; return false; }
+          st.max_stack_depth = std::max(st.max_stack_depth, (uint32_t)stack.size());
+        }
+        continue;
+      }
+      if (in.k == K_RET) {
+        for (Entry& e : stack) e.mask &= ~exec;
+        stack.back().pc = pc + 1;
+        continue;
+      }
+      if (in.k == K_LDG || in.k == K_STG) {
+        uint32_t size = (uint32_t)width_of(in.ty) / 8;
+        uint64_t addr[32];
+        uint8_t* host[32];
+        int bi[32];
+        uint64_t off[32];
+        int err = 0;
+        for (int i = 0; i < 32 && !err; i++) {
           if (!((exec >> i) & 1)) continue;
-          sectors.insert(addr[i] >> 5);
-          lines.insert(addr[i] >> 7);
+          addr[i] = lanes[(size_t)i].v[(size_t)in.a.reg] + (uint64_t)in.a.off;
+          err = M.translate(addr[i], size, &host[i], &bi[i], &off[i]);
         }
-        if (in.k == K_LDG) { st.ld_req++; st.ld_sectors += sectors.size(); st.ld_lines += lines.size(); }
-        else { st.st_req++; st.st_sectors += sectors.size(); st.st_lines += lines.size(); }
-      }
-      for (int i = 0; i < 32; i++) {  // ascending lanes: the highest lane's store lands last
-        if (!((exec >> i) & 1)) continue;
-        int64_t gtid = (int64_t)cta * X.block + ctx[(size_t)i].tid;
-        if (in.k == K_LDG) {
-          M.note(bi[i], off[i], size, gtid, false);
-          lanes[(size_t)i].v[(size_t)in.d.reg] = load_le(host[i], size);
-        } else {
-          M.note(bi[i], off[i], size, gtid, true);
-          store_le(host[i], lanes[(size_t)i].v[(size_t)in.b.reg], size);
+        if (err) { st.status = err; return false; }
+        if (exec) {
+          std::set<uint64_t> sectors, lines;
+          for (int i = 0; i < 32; i++) {
+            if (!((exec >> i) & 1)) continue;
+            sectors.insert(addr[i] >> 5);
+            lines.insert(addr[i] >> 7);
+          }
+          if (in.k == K_LDG) { st.ld_req++; st.ld_sectors += sectors.size(); st.ld_lines += lines.size(); }
+          else { st.st_req++; st.st_sectors += sectors.size(); st.st_lines += lines.size(); }
         }
+        for (int i = 0; i < 32; i++) {  // ascending lanes: the highest lane's store lands last
+          if (!((exec >> i) & 1)) continue;
+          int64_t gtid = (int64_t)cta * X->block + ctx[(size_t)i].tid;
+          if (in.k == K_LDG) {
+            M.note(bi[i], off[i], size, gtid, false);
+            lanes[(size_t)i].v[(size_t)in.d.reg] = load_le(host[i], size);
+          } else {
+            M.note(bi[i], off[i], size, gtid, true);
+            store_le(host[i], lanes[(size_t)i].v[(size_t)in.b.reg], size);
+          }
+        }
+        top.pc = pc + 1;
+        continue;
       }
+      if (in.k == K_LDS || in.k == K_STS) {
+        uint32_t size = (uint32_t)width_of(in.ty) / 8;
+        uint64_t addr[32];
+        int err = 0;
+        for (int i = 0; i < 32 && !err; i++) {
+          if (!((exec >> i) & 1)) continue;
+          addr[i] = shared_addr(in, lanes[(size_t)i]);
+          err = shared_check(addr[i], size, K.shared_bytes);
+        }
+        if (err) { st.status = err; return false; }
+        if (exec) {
+          st.sh_req++;
+          st.sh_wavefronts += bank_degree(addr, exec);
+        }
+        for (int i = 0; i < 32; i++) {  // ascending lanes: the highest lane's store lands last
+          if (!((exec >> i) & 1)) continue;
+          int64_t gtid = (int64_t)cta * X->block + ctx[(size_t)i].tid;
+          uint8_t* p = S->bytes.data() + addr[i];
+          if (in.k == K_LDS) {
+            S->note(addr[i], size, gtid, false);
+            lanes[(size_t)i].v[(size_t)in.d.reg] = load_le(p, size);
+          } else {
+            S->note(addr[i], size, gtid, true);
+            store_le(p, lanes[(size_t)i].v[(size_t)in.b.reg], size);
+          }
+        }
+        top.pc = pc + 1;
+        continue;
+      }
+      for (int i = 0; i < 32; i++)
+        if ((exec >> i) & 1) alu(in, lanes[(size_t)i], ctx[(size_t)i], X->params);
       top.pc = pc + 1;
-      continue;
     }
-    for (int i = 0; i < 32; i++)
-      if ((exec >> i) & 1) alu(in, lanes[(size_t)i], ctx[(size_t)i], X.params);
-    top.pc = pc + 1;
+    return false;
   }
 
-  st.cycles = st.warp_insts ? std::max(std::max(t_last + 1, max_ready), drain) : 0;
-  std::memcpy(X.stats + (uint64_t)gwarp * sizeof(orc_warp_stats), &st, sizeof st);
-  if (X.trace) {
-    uint8_t* slot = X.trace + (uint64_t)gwarp * X.slot_bytes;
-    std::memset(slot, 0, X.slot_bytes);
-    store_le(slot + 0, n_events, 4);
-    slot[4] = 1;
-    slot[5] = 4;
-    store_le(slot + 6, n_dropped, 2);
-    store_le(slot + 8, st.cycles, 8);
-    for (size_t i = 0; i < records.size(); i++) store_le(slot + 16 + 4 * i, records[i], 4);
+  void write_back() const {
+    orc_warp_stats out = st;
+    out.cycles = st.warp_insts ? std::max(std::max(t_last + 1, max_ready), drain) : 0;
+    std::memcpy(X->stats + (uint64_t)gwarp * sizeof(orc_warp_stats), &out, sizeof out);
+    if (X->trace) {
+      uint8_t* slot = X->trace + (uint64_t)gwarp * X->slot_bytes;
+      std::memset(slot, 0, X->slot_bytes);
+      store_le(slot + 0, n_events, 4);
+      slot[4] = 1;
+      slot[5] = 4;
+      store_le(slot + 6, n_dropped, 2);
+      store_le(slot + 8, out.cycles, 8);
+      for (size_t i = 0; i < records.size(); i++) store_le(slot + 16 + 4 * i, records[i], 4);
+    }
   }
+};
+
+// A warp of a kernel with no shared memory and no barrier runs alone.
+void run_warp(const Launch& X, Memory& M, uint32_t gwarp) {
+  WarpRun w(X, gwarp);
+  uint64_t arrival;
+  w.run(M, nullptr, &arrival);
+  w.write_back();
+}
+
+// Every warp of one CTA, barrier interval by barrier interval (the page's
+// step(): warps waiting at the barrier are skipped until all have arrived).
+void run_cta(const Launch& X, Memory& M, uint32_t cta) {
+  const Kernel& K = *X.K;
+  CtaMem S(K.shared_bytes, M.race_on);
+  std::vector<WarpRun> ws;
+  for (uint32_t w = 0; w < X.warps_per_cta; w++) ws.emplace_back(X, cta * X.warps_per_cta + w);
+  std::vector<char> done(ws.size(), 0), waiting(ws.size(), 0);
+  for (;;) {
+    bool any_waiting = false;
+    uint64_t latest = 0;
+    for (size_t w = 0; w < ws.size(); w++) {
+      if (done[w]) continue;
+      uint64_t arrival = 0;
+      if (ws[w].run(M, &S, &arrival)) {
+        waiting[w] = 1;
+        any_waiting = true;
+        latest = std::max(latest, arrival);
+      } else {
+        done[w] = 1;
+      }
+    }
+    if (!any_waiting) break;  // every warp has finished
+    const uint64_t release = latest + X.cfg->lat[ORC_LAT_BAR];
+    for (size_t w = 0; w < ws.size(); w++)
+      if (waiting[w]) { ws[w].t_next = release; waiting[w] = 0; }
+    S.new_interval();
+  }
+  for (const WarpRun& w : ws) w.write_back();
+  M.race_flags |= S.race_flags;
 }
 
 // ---------------------------------------------------- per-thread mode ----
-// Each thread runs alone with scalar control flow. Gives the memory image a
-// race-free program must produce whatever the warp-level masking does.
+// Each thread runs alone with scalar control flow (between barriers, in CTA
+// kernels). Gives the memory image a race-free program must produce whatever
+// the warp-level masking does.
 
-void run_thread_alone(const Launch& X, Memory& M, uint32_t gwarp, uint32_t lane, int32_t* status) {
-  const Kernel& K = *X.K;
-  const uint32_t cta = gwarp / X.warps_per_cta;
-  const uint32_t wic = gwarp % X.warps_per_cta;
+struct ThreadRun {
+  const Launch* X;
+  uint32_t gwarp, lane, cta, wic;
   Lane L;
-  L.v.assign(K.regs.size(), 0);
-  LaneCtx c{wic * 32 + lane, X.block, cta, X.grid, lane};
+  LaneCtx c;
   int pc = 0;
   uint64_t steps = 0;
-  const int n = (int)K.code.size();
-  while (pc < n) {
-    const Inst& in = K.code[(size_t)pc];
-    if (in.k == K_EVENT) { pc++; continue; }
-    if (steps == X.cfg->step_limit) { *status = ORC_ST_STEP_LIMIT; return; }
-    steps++;
-    bool g = true;
-    if (in.guard >= 0) g = (L.v[(size_t)in.guard] != 0) != in.guard_neg;
-    if (in.k == K_BRA) { pc = g ? in.target : pc + 1; continue; }
-    if (in.k == K_RET) { if (g) return; pc++; continue; }
-    if (!g) { pc++; continue; }
-    if (in.k == K_LDG || in.k == K_STG) {
-      uint32_t size = (uint32_t)width_of(in.ty) / 8;
-      uint64_t addr = L.v[(size_t)in.a.reg] + (uint64_t)in.a.off;
-      uint8_t* host;
-      int bi;
-      uint64_t off;
-      int err = M.translate(addr, size, &host, &bi, &off);
-      if (err) { *status = err; return; }
-      if (in.k == K_LDG) L.v[(size_t)in.d.reg] = load_le(host, size);
-      else store_le(host, L.v[(size_t)in.b.reg], size);
+  int32_t status = 0;
+
+  ThreadRun(const Launch& Xl, uint32_t gw, uint32_t ln) : X(&Xl), gwarp(gw), lane(ln) {
+    cta = gwarp / X->warps_per_cta;
+    wic = gwarp % X->warps_per_cta;
+    L.v.assign(X->K->regs.size(), 0);
+    c = LaneCtx{wic * 32 + lane, X->block, cta, X->grid, lane};
+  }
+
+  // Runs until the thread finishes (false) or reaches bar.sync (true).
+  bool run(Memory& M, CtaMem* S) {
+    const Kernel& K = *X->K;
+    const int n = (int)K.code.size();
+    while (pc < n) {
+      const Inst& in = K.code[(size_t)pc];
+      if (in.k == K_EVENT) { pc++; continue; }
+      if (steps == X->cfg->step_limit) { status = ORC_ST_STEP_LIMIT; return false; }
+      steps++;
+      bool g = true;
+      if (in.guard >= 0) g = (L.v[(size_t)in.guard] != 0) != in.guard_neg;
+      if (in.k == K_BAR) { pc++; return true; }
+      if (in.k == K_BRA) { pc = g ? in.target : pc + 1; continue; }
+      if (in.k == K_RET) { if (g) return false; pc++; continue; }
+      if (!g) { pc++; continue; }
+      if (in.k == K_LDG || in.k == K_STG) {
+        uint32_t size = (uint32_t)width_of(in.ty) / 8;
+        uint64_t addr = L.v[(size_t)in.a.reg] + (uint64_t)in.a.off;
+        uint8_t* host;
+        int bi;
+        uint64_t off;
+        int err = M.translate(addr, size, &host, &bi, &off);
+        if (err) { status = err; return false; }
+        if (in.k == K_LDG) L.v[(size_t)in.d.reg] = load_le(host, size);
+        else store_le(host, L.v[(size_t)in.b.reg], size);
+        pc++;
+        continue;
+      }
+      if (in.k == K_LDS || in.k == K_STS) {
+        uint32_t size = (uint32_t)width_of(in.ty) / 8;
+        uint64_t addr = shared_addr(in, L);
+        int err = shared_check(addr, size, K.shared_bytes);
+        if (err) { status = err; return false; }
+        if (in.k == K_LDS) L.v[(size_t)in.d.reg] = load_le(S->bytes.data() + addr, size);
+        else store_le(S->bytes.data() + addr, L.v[(size_t)in.b.reg], size);
+        pc++;
+        continue;
+      }
+      alu(in, L, c, X->params);
       pc++;
-      continue;
     }
-    alu(in, L, c, X.params);
-    pc++;
+    return false;
+  }
+};
+
+// One warp's threads one after another (no shared memory, no barrier); or,
+// in a CTA kernel, every thread of the CTA interval by interval. The status
+// of each warp is that of its first failing thread in lane order.
+void run_threads(const Launch& X, Memory& M, const std::vector<uint32_t>& warps, std::vector<int32_t>* status) {
+  const Kernel& K = *X.K;
+  CtaMem S(K.shared_bytes, false);
+  if (!K.cta_mode()) {  // a failing thread stops its warp's remaining lanes
+    for (size_t k = 0; k < warps.size(); k++) {
+      const uint32_t wic = warps[k] % X.warps_per_cta;
+      for (uint32_t lane = 0; lane < 32 && wic * 32 + lane < X.block; lane++) {
+        ThreadRun t(X, warps[k], lane);
+        t.run(M, &S);
+        if (t.status) { (*status)[k] = t.status; break; }
+      }
+    }
+    return;
+  }
+  std::vector<ThreadRun> ts;
+  std::vector<size_t> owner;
+  for (size_t k = 0; k < warps.size(); k++) {
+    const uint32_t wic = warps[k] % X.warps_per_cta;
+    for (uint32_t lane = 0; lane < 32 && wic * 32 + lane < X.block; lane++) {
+      ts.emplace_back(X, warps[k], lane);
+      owner.push_back(k);
+    }
+  }
+  std::vector<char> done(ts.size(), 0);
+  for (;;) {
+    bool any_waiting = false;
+    for (size_t i = 0; i < ts.size(); i++) {
+      if (done[i]) continue;
+      if (ts[i].run(M, &S)) any_waiting = true;
+      else done[i] = 1;
+    }
+    if (!any_waiting) break;
+  }
+  for (size_t i = 0; i < ts.size(); i++) {
+    int32_t& s = (*status)[owner[i]];
+    if (!s && ts[i].status) s = ts[i].status;
   }
 }
 
@@ -1333,7 +1669,7 @@ extern "C" {
 
 void orc_config_default(orc_config* cfg) {
   std::memset(cfg, 0, sizeof *cfg);
-  const uint32_t lat[ORC_NUM_LAT] = {4, 4, 400, 20, 8, 36, 1, 0};
+  const uint32_t lat[ORC_NUM_LAT] = {4, 4, 400, 20, 8, 36, 1, 23, 23, 20, 0, 0};
   std::memcpy(cfg->lat, lat, sizeof lat);
   cfg->max_ts_per_warp = 0;
   cfg->stack_depth = 32;
@@ -1385,6 +1721,20 @@ int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
     } else {
       for (uint64_t w = 0; w < W; w++) warps.push_back((uint32_t)w);
     }
+    // Kernels with shared memory or barriers run whole CTAs: every warp of a
+    // listed warp's CTA runs (and is written).
+    const bool by_cta = K.cta_mode();
+    std::vector<uint32_t> units;  // warps, or CTAs
+    if (by_cta) {
+      std::set<uint32_t> ctas;
+      for (uint32_t w : warps) ctas.insert(w / X.warps_per_cta);
+      units.assign(ctas.begin(), ctas.end());
+      warps.clear();
+      for (uint32_t c : units)
+        for (uint32_t w = 0; w < X.warps_per_cta; w++) warps.push_back(c * X.warps_per_cta + w);
+    } else {
+      units = warps;
+    }
 
     Memory M;
     M.bufs = bufs;
@@ -1399,35 +1749,36 @@ int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
 
     unsigned nthreads = cfg->threads ? cfg->threads : std::max(1u, std::thread::hardware_concurrency());
     if (cfg->race_check) nthreads = 1;
-    nthreads = (unsigned)std::min<size_t>(nthreads, std::max<size_t>(1, warps.size()));
+    nthreads = (unsigned)std::min<size_t>(nthreads, std::max<size_t>(1, units.size()));
 
-    // per-thread mode keeps one status per warp
-    std::vector<int32_t> pt_status(cfg->mode == ORC_MODE_PER_THREAD ? warps.size() : 0, 0);
     auto work = [&](size_t lo, size_t hi) {
       for (size_t k = lo; k < hi; k++) {
         if (cfg->mode == ORC_MODE_PER_THREAD) {
-          uint32_t gw = warps[k];
-          uint32_t wic = gw % X.warps_per_cta;
-          for (uint32_t lane = 0; lane < 32 && wic * 32 + lane < block; lane++) {
-            run_thread_alone(X, M, gw, lane, &pt_status[k]);
-            if (pt_status[k]) break;
+          std::vector<uint32_t> ws;
+          if (by_cta) for (uint32_t w = 0; w < X.warps_per_cta; w++) ws.push_back(units[k] * X.warps_per_cta + w);
+          else ws.push_back(units[k]);
+          std::vector<int32_t> pst(ws.size(), 0);
+          run_threads(X, M, ws, &pst);
+          for (size_t j = 0; j < ws.size(); j++) {
+            orc_warp_stats st;
+            std::memset(&st, 0, sizeof st);
+            st.status = pst[j];
+            std::memcpy(X.stats + (uint64_t)ws[j] * sizeof st, &st, sizeof st);
           }
-          orc_warp_stats st;
-          std::memset(&st, 0, sizeof st);
-          st.status = pt_status[k];
-          std::memcpy(X.stats + (uint64_t)gw * sizeof st, &st, sizeof st);
+        } else if (by_cta) {
+          run_cta(X, M, units[k]);
         } else {
-          run_warp(X, M, warps[k]);
+          run_warp(X, M, units[k]);
         }
       }
     };
     if (nthreads <= 1) {
-      work(0, warps.size());
+      work(0, units.size());
     } else {
       std::vector<std::thread> pool;
-      size_t chunk = (warps.size() + nthreads - 1) / nthreads;
+      size_t chunk = (units.size() + nthreads - 1) / nthreads;
       for (unsigned t = 0; t < nthreads; t++) {
-        size_t lo = t * chunk, hi = std::min(warps.size(), lo + chunk);
+        size_t lo = t * chunk, hi = std::min(units.size(), lo + chunk);
         if (lo < hi) pool.emplace_back(work, lo, hi);
       }
       for (std::thread& th : pool) th.join();

@@ -8,6 +8,15 @@
  * with the GPU path: its parser, its post-dominator computation and its
  * instruction semantics are written separately here.
  *
+ * Shared memory and barriers (KernelScope backend doc, simulator/models.py
+ * Block: a per-block shared array and a barrier; simulator/engine.py
+ * analyze_shared_memory_access: 32 banks of 4 bytes, broadcast rule;
+ * latency/model.py: ld.shared/st.shared 23, bar.sync 20): a kernel that
+ * declares .shared arrays or uses bar.sync runs CTA by CTA. A warp that issues
+ * bar.sync 0 stops; once every warp of its CTA has stopped there or finished,
+ * the stopped warps resume at (latest issue cycle of the bar.sync) + the
+ * barrier latency. Shared memory starts zeroed for every CTA.
+ *
  * Output formats that must match the GPU path byte for byte (written
  * independently on each side):
  *   - per-warp statistics record, 96 bytes (orc_warp_stats below);
@@ -47,7 +56,10 @@ extern "C" {
 #define ORC_LAT_BRA 4 /* bra */
 #define ORC_LAT_SFU 5 /* div.rn.f32, sqrt.rn.f32 */
 #define ORC_LAT_RET 6 /* ret, exit */
-#define ORC_NUM_LAT 8 /* slot 7 is reserved */
+#define ORC_LAT_LDS 7 /* ld.shared */
+#define ORC_LAT_STS 8 /* st.shared */
+#define ORC_LAT_BAR 9 /* bar.sync: from the last arrival to the release */
+#define ORC_NUM_LAT 12 /* slots 10 and 11 are reserved */
 
 /* Simulated global buffer: caller-chosen simulated base address (4 KiB
  * aligned, non-overlapping) backed by host memory. */
@@ -88,13 +100,16 @@ typedef struct {
   uint64_t st_lines;
   int32_t status;
   uint32_t max_stack_depth;
-  uint64_t reserved[2];
+  uint64_t sh_req;        /* ld/st.shared requests with at least one executing lane */
+  uint64_t sh_wavefronts; /* sum over those requests of the bank-conflict degree */
 } orc_warp_stats;
 
-/* Race checker result bits. */
+/* Race checker result bits: two threads touch one 4-byte word, at least one
+ * writing (global memory: anywhere in the launch; shared memory: within one
+ * barrier interval of one CTA). */
 #define ORC_RACE_CROSS_THREAD 1u
 
-/* Fill cfg with the defaults: latency table {4,4,400,20,8,36,1,0},
+/* Fill cfg with the defaults: latency table {4,4,400,20,8,36,1,23,23,20,0,0},
  * max_ts 0, stack depth 32, step limit 2^26, no injection, warp mode. */
 void orc_config_default(orc_config* cfg);
 

@@ -287,6 +287,80 @@ def gather(stride: int, n_out: int = 1 << 24, block: int = 256, seed: int = 1) -
                     max_ts=0, meta={"stride": stride, "n_out": n_out})
 
 
+# ------------------------------------------------------------ smem_reduce --
+
+def smem_reduce_ptx(block: int) -> str:
+    """Per-CTA u32 sum in shared memory: every thread stores its element,
+    then a tree over halving strides s (threads tid < s add sdata[tid + s]),
+    bar.sync 0 between the steps; thread 0 writes the CTA's sum."""
+    return HEADER + f""".visible .entry smem_reduce(
+    .param .u64 rd_in,
+    .param .u64 rd_out
+)
+{{
+    .reg .pred  %p<3>;
+    .reg .b32   %r<12>;
+    .reg .b64   %rd<6>;
+    .shared .align 4 .b8 sdata[{4 * block}];
+
+    ld.param.u64    %rd1, [rd_in];
+    ld.param.u64    %rd2, [rd_out];
+    mov.u32         %r1, %tid.x;
+    mov.u32         %r2, %ctaid.x;
+    mov.u32         %r3, %ntid.x;
+    mad.lo.s32      %r4, %r2, %r3, %r1;
+    cvt.u64.u32     %rd3, %r4;
+    shl.b64         %rd3, %rd3, 2;
+    add.s64         %rd4, %rd1, %rd3;
+    ld.global.u32   %r5, [%rd4];
+    mov.u32         %r6, sdata;
+    shl.b32         %r7, %r1, 2;
+    add.u32         %r8, %r6, %r7;
+    st.shared.u32   [%r8], %r5;
+    bar.sync 0;
+    shr.u32         %r9, %r3, 1;
+    //@iket range_start tree
+RD_LOOP:
+    setp.eq.u32     %p1, %r9, 0;
+    @%p1 bra        RD_DONE;
+    setp.lt.u32     %p2, %r1, %r9;
+    @!%p2 bra       RD_SKIP;
+    shl.b32         %r10, %r9, 2;
+    add.u32         %r10, %r8, %r10;
+    ld.shared.u32   %r11, [%r10];
+    ld.shared.u32   %r5, [%r8];
+    add.u32         %r5, %r5, %r11;
+    st.shared.u32   [%r8], %r5;
+RD_SKIP:
+    bar.sync 0;
+    shr.u32         %r9, %r9, 1;
+    bra             RD_LOOP;
+RD_DONE:
+    //@iket range_end tree
+    setp.ne.u32     %p1, %r1, 0;
+    @%p1 bra        RD_EXIT;
+    cvt.u64.u32     %rd3, %r2;
+    shl.b64         %rd3, %rd3, 2;
+    add.s64         %rd5, %rd2, %rd3;
+    st.global.u32   [%rd5], %r5;
+RD_EXIT:
+    ret;
+}}
+"""
+
+
+def smem_reduce(n: int = 1 << 22, block: int = 256, seed: int = 5, max_ts: int = 4) -> Workload:
+    """Shared-memory tree reduction: one u32 sum per CTA of `block` threads
+    (block a power of two, at most 256)."""
+    assert block & (block - 1) == 0 and 2 <= block <= 256 and n % block == 0
+    x = randint_u32(n, 0, 1 << 31, seed)
+    out = np.zeros(n // block, dtype=np.uint32)
+    bufs = place([("in", x, False), ("out", out, True)])
+    params = pack_params([("u64", bufs[0].sim_base), ("u64", bufs[1].sim_base)])
+    return Workload(f"smem_reduce_b{block}", smem_reduce_ptx(block), "smem_reduce", n // block, block, params,
+                    bufs, max_ts=max_ts, meta={"n": n, "block": block})
+
+
 # --------------------------------------------------------------- divergent --
 
 DIVERGENT_BODY_OPS = 16
