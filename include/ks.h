@@ -14,14 +14,24 @@
  *      analyze_global_memory_access);
  *   4. per-warp trace slots in the IKET layout (CuTeDSL IKET 浅析, §2:
  *      16-byte header u32+u8+u8+u16+u64 then maxTsCntPerWarp 4-byte records,
- *      slot size rounded up to 8 bytes, one slot per warp, no atomics).
+ *      slot size rounded up to 8 bytes, one slot per warp, no atomics);
+ *   5. per-warp shared-memory requests and their bank-conflict degrees
+ *      (KernelScope backend doc, simulator/engine.py —
+ *      analyze_shared_memory_access: 32 banks of 4 bytes, bank =
+ *      (address / 4) % 32, a bank whose lanes all use one address is a
+ *      broadcast, any other bank's degree is its number of lanes, the
+ *      request's degree is the largest).
  *
  * Supported PTX subset: add/sub (.u32 .s32 .u64 .s64 .f32), mul.lo/mad.lo
  * (integers), mul.f32, fma.rn.f32, div.rn.f32, sqrt.rn.f32, and/or/xor
  * (.b32 .b64 .pred), shl (.b32 .b64), shr (.b32 .b64 .u32 .u64 .s32 .s64),
  * cvt (int<->int, .rn f32<-int, .rni/.rzi/.rmi/.rpi int<-f32), mov, setp
  * (eq ne lt le gt ge, lo ls hi hs), selp, bra, ld.param, ld.global,
- * st.global (4- and 8-byte), ret/exit; registers .b32 .u32 .s32 .f32 .b64
+ * st.global (4- and 8-byte), ld.shared and st.shared (4- and 8-byte; address
+ * [reg(+off)] with a 32- or 64-bit register, or [array(+off)]), .shared
+ * arrays in the kernel body (at most 48 KiB per CTA; `mov` of an array name
+ * gives its shared address), bar.sync 0 / barrier.sync 0 (unguarded, no
+ * thread count), ret/exit; registers .b32 .u32 .s32 .f32 .b64
  * .u64 .s64 .pred; special registers %tid %ntid %ctaid %nctaid (.x; .y/.z
  * read 0 or 1) and %laneid; trace pseudo-ops written as comments
  * `//@iket mark NAME`, `//@iket range_start NAME`, `//@iket range_end NAME`.
@@ -46,6 +56,19 @@
  *     value lands. Stores from different warps to the same address, or a load
  *     of a word another warp stores, are undefined (warps run concurrently).
  *   - Registers start at zero, predicates false.
+ *   - Shared memory and barriers (KernelScope backend doc, simulator/models.py
+ *     Block: a shared array and a barrier per block; Warp.at_barrier): a
+ *     kernel that declares .shared arrays or uses bar.sync runs CTA by CTA
+ *     with every warp of the CTA resident; its block may hold at most
+ *     KS_MAX_CTA_MODE_BLOCK threads (else KS_ERR_LIMIT). Shared memory starts
+ *     zeroed in every CTA. A warp that issues bar.sync (any active mask)
+ *     stops; when every warp of the CTA has stopped at a barrier or finished,
+ *     the stopped warps resume with t_next = latest bar.sync issue cycle +
+ *     lat[KS_LAT_BAR]; a finished warp never holds a barrier. Shared accesses
+ *     are checked like global ones (misaligned first, then outside the
+ *     declared arrays). Bank conflicts are counted, not timed. Between two
+ *     barriers, a shared word written by one warp and touched by another is
+ *     undefined, as for global memory.
  */
 #ifndef KS_H
 #define KS_H
@@ -75,7 +98,7 @@ extern "C" {
 #define KS_ST_INJECTED 6     /* the debug injection point was reached */
 
 /* ---- latency classes (index of ks_config.lat) --------------------------- */
-#define KS_NUM_LAT_CLASSES 8
+#define KS_NUM_LAT_CLASSES 12
 #define KS_LAT_ALU 0 /* int & f32 add/sub/mul/mad, logic, shifts, cvt, mov, setp, selp, ld.param */
 #define KS_LAT_FMA 1 /* fma.rn.f32 */
 #define KS_LAT_LDG 2 /* ld.global */
@@ -83,11 +106,16 @@ extern "C" {
 #define KS_LAT_BRA 4 /* bra */
 #define KS_LAT_SFU 5 /* div.rn.f32, sqrt.rn.f32 */
 #define KS_LAT_RET 6 /* ret, exit */
-/* class 7 is reserved */
+#define KS_LAT_LDS 7 /* ld.shared */
+#define KS_LAT_STS 8 /* st.shared */
+#define KS_LAT_BAR 9 /* bar.sync: last arrival to release */
+/* classes 10 and 11 are reserved */
 
 #define KS_MAX_BUFFERS 8
 #define KS_MAX_PARAM_BYTES 256
 #define KS_MAX_STACK 32
+#define KS_MAX_SHARED_BYTES 49152   /* simulated shared memory per CTA */
+#define KS_MAX_CTA_MODE_BLOCK 256   /* block limit of kernels with shared memory or bar.sync */
 
 typedef struct ks_module ks_module; /* opaque; owned by the library */
 
@@ -127,7 +155,8 @@ typedef struct {
   uint64_t st_lines;
   int32_t status;           /* 0 or a KS_ST_* code */
   uint32_t max_stack_depth; /* deepest reconvergence stack reached */
-  uint64_t reserved[2];     /* written as 0 */
+  uint64_t sh_req;          /* ld/st.shared requests with at least one executing lane */
+  uint64_t sh_wavefronts;   /* sum over those requests of the bank-conflict degree */
 } ks_warp_stats;
 
 /* Launch totals reduced over every warp record. */
@@ -147,9 +176,11 @@ typedef struct {
   int64_t first_failed_warp;  /* lowest failing warp id, -1 if none */
   int32_t status;             /* status of first_failed_warp, 0 if none */
   uint32_t max_stack_depth;
+  uint64_t sh_req;
+  uint64_t sh_wavefronts;
 } ks_totals;
 
-/* Fills the defaults: lat = {4, 4, 400, 20, 8, 36, 1, 0}, max_ts 0,
+/* Fills the defaults: lat = {4, 4, 400, 20, 8, 36, 1, 23, 23, 20, 0, 0}, max_ts 0,
  * stack depth 32, step limit 2^26, injection off. */
 void ks_config_default(ks_config* cfg);
 
@@ -203,7 +234,9 @@ size_t ks_stats_bytes(uint32_t grid, uint32_t block);
  * Simulated faults do not fail the call: they are reported per warp in the
  * stats records (read them with ks_read_stats). Host-side errors: KS_ERR_ARG
  * (shapes, sizes, buffer table, undersized outputs), KS_ERR_NOT_FOUND,
- * KS_ERR_LIMIT (shared memory), KS_ERR_CUDA. The first call on a device
+ * KS_ERR_LIMIT (the real launch's shared memory does not fit, or a kernel
+ * with shared memory or bar.sync has a block above KS_MAX_CTA_MODE_BLOCK),
+ * KS_ERR_CUDA. The first call on a device
  * uploads the module's program there (one allocation per module per device).
  * Simulations that share output or store-target buffers must not overlap in
  * time. */

@@ -15,7 +15,7 @@ class KsBuffer(ctypes.Structure):
 
 class KsConfig(ctypes.Structure):
     _fields_ = [
-        ("lat", ctypes.c_uint32 * 8),
+        ("lat", ctypes.c_uint32 * 12),
         ("max_ts_per_warp", ctypes.c_uint32),
         ("simt_stack_depth", ctypes.c_uint32),
         ("step_limit", ctypes.c_uint64),
@@ -30,7 +30,8 @@ class KsTotals(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "cycles_max", "cycles_sum", "warp_insts", "thread_insts", "ld_req", "ld_sectors", "st_req",
         "st_sectors", "ld_lines", "st_lines", "n_warps", "n_failed")] + [
-        ("first_failed_warp", ctypes.c_int64), ("status", ctypes.c_int32), ("max_stack_depth", ctypes.c_uint32)]
+        ("first_failed_warp", ctypes.c_int64), ("status", ctypes.c_int32), ("max_stack_depth", ctypes.c_uint32),
+        ("sh_req", ctypes.c_uint64), ("sh_wavefronts", ctypes.c_uint64)]
 
 
 EXPORTS = {

@@ -16,8 +16,11 @@ from . import _native
 STATS_DTYPE = np.dtype(
     [("cycles", "<u8"), ("warp_insts", "<u8"), ("thread_insts", "<u8"), ("ld_req", "<u8"),
      ("ld_sectors", "<u8"), ("st_req", "<u8"), ("st_sectors", "<u8"), ("ld_lines", "<u8"),
-     ("st_lines", "<u8"), ("status", "<i4"), ("max_stack_depth", "<u4"), ("reserved", "<u8", (2,))])
-DEFAULT_LAT = (4, 4, 400, 20, 8, 36, 1, 0)
+     ("st_lines", "<u8"), ("status", "<i4"), ("max_stack_depth", "<u4"), ("sh_req", "<u8"),
+     ("sh_wavefronts", "<u8")])
+# ALU, FMA, ld.global, st.global, bra, div/sqrt, ret, ld.shared, st.shared,
+# bar.sync, two reserved classes
+DEFAULT_LAT = (4, 4, 400, 20, 8, 36, 1, 23, 23, 20, 0, 0)
 
 ST_OOB, ST_MISALIGNED, ST_STEP_LIMIT, ST_SIMT_STACK, ST_TIMEOUT, ST_INJECTED = 1, 2, 3, 4, 5, 6
 
@@ -46,7 +49,7 @@ class Config:
     def to_c(self) -> _native.KsConfig:
         c = _native.KsConfig()
         _native.lib().ks_config_default(ctypes.byref(c))
-        for i in range(8):
+        for i in range(12):
             c.lat[i] = self.lat[i] if i < len(self.lat) else 0
         c.max_ts_per_warp = self.max_ts
         c.simt_stack_depth = self.stack_depth
@@ -73,6 +76,8 @@ class Totals:
     first_failed_warp: int
     status: int
     max_stack_depth: int
+    sh_req: int = 0
+    sh_wavefronts: int = 0
 
 
 class Module:

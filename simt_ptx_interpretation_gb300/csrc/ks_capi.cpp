@@ -68,7 +68,7 @@ int device_info(DevInfo* out, int* dev_out) {
 // Device accumulator for ks_read_stats, one per device, allocated once.
 std::mutex g_acc_mu;
 std::map<int, void*> g_acc;
-constexpr size_t ACC_WORDS = 13;
+constexpr size_t ACC_WORDS = 15;
 
 uint64_t warps_of(uint32_t grid, uint32_t block) { return (uint64_t)grid * ((block + 31u) / 32u); }
 
@@ -83,7 +83,7 @@ extern "C" {
 void ks_config_default(ks_config* cfg) {
   if (!cfg) return;
   std::memset(cfg, 0, sizeof *cfg);
-  const uint32_t lat[KS_NUM_LAT_CLASSES] = {4, 4, 400, 20, 8, 36, 1, 0};
+  const uint32_t lat[KS_NUM_LAT_CLASSES] = {4, 4, 400, 20, 8, 36, 1, 23, 23, 20, 0, 0};
   std::memcpy(cfg->lat, lat, sizeof lat);
   cfg->max_ts_per_warp = 0;
   cfg->simt_stack_depth = 32;
@@ -208,6 +208,8 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
     if (cfg.lat[i] > ks::KS_MAX_LATENCY) return KS_ERR_ARG;
   const uint64_t slot = (16ull + 4ull * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
   if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
+  // shared memory / bar.sync: every warp of a CTA resident on one real CTA
+  if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
 
   DevInfo di;
   int dev = 0;
@@ -245,6 +247,8 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   L.block = block;
   L.wpc = (block + 31u) / 32u;
   L.n_warps = (uint32_t)W;
+  L.shared_bytes = k->shared_bytes;
+  L.cta_mode = k->cta_mode() ? 1u : 0u;
   std::memcpy(L.lat, cfg.lat, sizeof L.lat);
   L.max_ts = cfg.max_ts_per_warp;
   L.stack_depth = cfg.simt_stack_depth;
@@ -265,7 +269,7 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
 
   // ---- real launch shape (persistent real warps, see ks::choose_launch) ----
   uint32_t wpc_real = 0, ctas = 0;
-  const int shape = ks::choose_launch(W, L.image_bytes, k->layout.region_bytes, di.sms, di.max_smem, &wpc_real, &ctas);
+  const int shape = ks::choose_launch(L, di.sms, di.max_smem, &wpc_real, &ctas);
   if (shape != KS_OK) return shape;
   if (ks::launch_interp(L, wpc_real, ctas, stream) != 0) return KS_ERR_CUDA;
   return KS_OK;
@@ -301,6 +305,8 @@ int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_tota
   out->n_warps = n_warps;
   out->n_failed = h[10];
   out->max_stack_depth = (uint32_t)h[12];
+  out->sh_req = h[13];
+  out->sh_wavefronts = h[14];
   out->first_failed_warp = -1;
   out->status = 0;
   if (h[10]) {

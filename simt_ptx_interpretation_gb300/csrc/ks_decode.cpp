@@ -211,6 +211,8 @@ struct KernelText {
   std::map<std::string, RegDecl> regs;
   std::vector<Stmt> body;
   std::map<std::string, size_t> labels;  // label -> index into body
+  std::map<std::string, uint32_t> shared;  // .shared array -> shared address
+  uint32_t shared_bytes = 0;
 };
 
 // --------------------------------------------------------------- parser ----
@@ -317,6 +319,7 @@ class Parser {
       }
       if (t.kind == TK_NAME && (t.text == ".loc" || t.text == ".file")) { skip_line(); continue; }
       if (t.kind == TK_NAME && t.text == ".reg") { reg_decl(k); continue; }
+      if (t.kind == TK_NAME && t.text == ".shared") { shared_decl(k); continue; }
       if (t.kind == TK_NAME && t.text[0] == '.') fail(KS_ERR_UNSUPPORTED, t.line, "unsupported directive in kernel body: " + t.text);
       if (t.kind == TK_NAME && peek().kind == TK_PUNCT && peek().text == ":" && is_ident(t.text)) {
         if (k.labels.count(t.text) || std::count(pending.begin(), pending.end(), t.text))
@@ -366,6 +369,50 @@ class Parser {
       break;
     }
     expect(";");
+  }
+
+  // .shared [.align A] .TYPE name[[N]];  arrays laid out in declaration order
+  // from shared address 0, each at its alignment (the type's size by default)
+  void shared_decl(KernelText& k) {
+    const int ln = cur().line;
+    pos_++;
+    uint64_t align = 0;
+    if (cur().kind == TK_NAME && cur().text == ".align") {
+      pos_++;
+      Lit a;
+      if (cur().kind != TK_NUM || !parse_number(cur().text, &a) || a.is_f32 || a.mag == 0 || (a.mag & (a.mag - 1)) ||
+          a.mag > 4096)
+        fail(KS_ERR_PARSE, ln, "bad .align");
+      align = a.mag;
+      pos_++;
+    }
+    const std::string ty = name();
+    static const std::map<std::string, uint32_t> esz = {
+        {".b8", 1}, {".u8", 1}, {".s8", 1}, {".b16", 2}, {".u16", 2}, {".s16", 2},
+        {".b32", 4}, {".u32", 4}, {".s32", 4}, {".f32", 4},
+        {".b64", 8}, {".u64", 8}, {".s64", 8}, {".f64", 8}};
+    auto et = esz.find(ty);
+    if (et == esz.end()) fail(KS_ERR_UNSUPPORTED, ln, "unsupported .shared type " + ty);
+    const std::string nm = name();
+    if (!is_ident(nm)) fail(KS_ERR_PARSE, ln, "bad .shared name");
+    uint64_t count = 1;
+    if (is("[")) {
+      pos_++;
+      Lit c;
+      if (cur().kind != TK_NUM || !parse_number(cur().text, &c) || c.is_f32 || c.mag == 0 || c.mag > (1u << 20))
+        fail(KS_ERR_PARSE, ln, "bad .shared array size");
+      count = c.mag;
+      pos_++;
+      expect("]");
+    }
+    expect(";");
+    if (k.shared.count(nm)) fail(KS_ERR_PARSE, ln, "shared array declared twice: " + nm);
+    if (!align) align = et->second;
+    const uint64_t off = (k.shared_bytes + align - 1) / align * align;
+    const uint64_t end = off + count * et->second;
+    if (end > KS_MAX_SHARED_BYTES) fail(KS_ERR_UNSUPPORTED, ln, "more than 48 KiB of shared memory");
+    k.shared[nm] = (uint32_t)off;
+    k.shared_bytes = (uint32_t)end;
   }
 
   Stmt instruction() {
@@ -467,6 +514,7 @@ class Decoder {
       off += sz;
     }
     K.param_bytes = off;
+    K.shared_bytes = T.shared_bytes;
     if (T.body.empty()) fail(KS_ERR_PARSE, T.line, "empty kernel");
     if (T.body.size() > KS_MAX_INSNS) fail(KS_ERR_LIMIT, T.line, "kernel longer than 2048 entries");
     for (Stmt& s : T.body) K.code.push_back(s.pseudo ? event(s) : insn(s));
@@ -771,7 +819,15 @@ class Decoder {
       arity(2);
       unsigned w = bits(t);
       in.d = dest(o[0], w, ln, &in.hd);
-      in.a = source(o[1], w, t, 'm', ln, &in.ha, &sp);
+      Operand src = o[1];
+      if (src.kind == Operand::LABEL) {  // the shared address of an array
+        auto it = T.shared.find(src.name);
+        if (it == T.shared.end() || t == PT_F32) fail(KS_ERR_PARSE, ln, "bad mov operand " + src.name);
+        src.kind = Operand::LIT;
+        src.lit = Lit{};
+        src.lit.mag = it->second;
+      }
+      in.a = source(src, w, t, 'm', ln, &in.ha, &sp);
       if (sp >= 0) {
         in.op = OP_MOVSP;
         in.imm = (uint64_t)sp;
@@ -870,9 +926,57 @@ class Decoder {
         in.b = source(o[1], w, t, 'r', ln, &in.hb, &sp);
         return in;
       }
+      if (op == "ld" && m[0] == "shared") {
+        in.op = w == 32 ? OP_LDS32 : OP_LDS64;
+        in.lat = KS_LAT_LDS;
+        in.d = dest(o[0], w, ln, &in.hd);
+        shared_address(o[1], ln, &in);
+        return in;
+      }
+      if (op == "st" && m[0] == "shared") {
+        in.op = w == 32 ? OP_STS32 : OP_STS64;
+        in.lat = KS_LAT_STS;
+        shared_address(o[0], ln, &in);
+        in.b = source(o[1], w, t, 'r', ln, &in.hb, &sp);
+        return in;
+      }
       unsupported();
     }
+    if (op == "bar" || op == "barrier") {
+      // bar.sync 0 / barrier.sync[.aligned] 0: CTA barrier 0 over every thread
+      const bool form = (op == "bar" && m.size() == 1 && m[0] == "sync") ||
+                        (op == "barrier" && (m.size() == 1 || m.size() == 2) && m[0] == "sync" &&
+                         (m.size() == 1 || m[1] == "aligned"));
+      if (!form) unsupported();
+      arity(1);
+      if (o[0].kind != Operand::LIT || o[0].lit.neg || o[0].lit.is_f32 || o[0].lit.mag != 0)
+        fail(KS_ERR_UNSUPPORTED, ln, "only barrier 0 without a thread count is supported");
+      if (in.guard != KS_NO_GUARD) fail(KS_ERR_UNSUPPORTED, ln, "guarded bar.sync is not supported");
+      in.op = OP_BAR;
+      in.lat = KS_LAT_BAR;
+      K.has_bar = true;
+      return in;
+    }
     fail(KS_ERR_UNSUPPORTED, ln, "unsupported opcode " + op);
+  }
+
+  // [%r(+off)] with a 32- or 64-bit register, or [array(+off)]
+  void shared_address(const Operand& o, int ln, KsInsn* in) {
+    if (o.kind == Operand::PARAM) {
+      auto it = T.shared.find(o.name);
+      if (it == T.shared.end()) fail(KS_ERR_PARSE, ln, "unknown shared array " + o.name);
+      in->flags = 0;
+      in->imm = (uint64_t)((int64_t)it->second + o.offset);
+      return;
+    }
+    if (o.kind != Operand::MEM) fail(KS_ERR_PARSE, ln, "shared address must be [register(+offset)] or [array(+offset)]");
+    RegDecl& r = reg(o.name, ln);
+    if (r.width != 32 && r.width != 64)
+      fail(KS_ERR_PARSE, ln, "shared address must be [register(+offset)] or [array(+offset)]");
+    in->a = (uint8_t)r.index;
+    in->ha = (uint8_t)r.index;
+    in->flags = (uint8_t)(KS_SHA_REG | (r.width == 64 ? KS_SHA_WIDE : 0));
+    in->imm = (uint64_t)o.offset;  // sign-extended
   }
 
   void address(const Operand& o, int ln, KsInsn* in) {
@@ -986,7 +1090,12 @@ class Decoder {
       case OP_CVT_ZX: case OP_CVT_SX: return w(32, 0, 0, 64);
       case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_F32: return w(32, 32, 0, 0);
       case OP_SETP_U64: case OP_SETP_S64: return w(64, 64, 0, 0);
-      default: return 0;  // events, control, predicate logic
+      case OP_LDS32: case OP_LDS64: case OP_STS32: case OP_STS64: {
+        const unsigned aw = (in.flags & KS_SHA_REG) ? ((in.flags & KS_SHA_WIDE) ? 64u : 32u) : 0u;
+        const unsigned dw = op == OP_LDS32 || op == OP_STS32 ? 32u : 64u;
+        return op == OP_LDS32 || op == OP_LDS64 ? w(aw, 0, 0, dw) : w(aw, dw, 0, 0);
+      }
+      default: return 0;  // events, control, predicate logic, bar.sync
     }
   }
 
@@ -1120,7 +1229,7 @@ class Decoder {
         }
         o.wlat = (uint32_t)in.lat;
         if (in.hd != KS_HZ_NONE) o.wlat |= DEV_HAS_DEST;
-        if (in.op == OP_STG32 || in.op == OP_STG64) o.wlat |= DEV_IS_STORE;
+        if (in.op == OP_STG32 || in.op == OP_STG64 || in.op == OP_STS32 || in.op == OP_STS64) o.wlat |= DEV_IS_STORE;
         if (in.op == OP_BRA || in.op == OP_RET) o.wlat |= DEV_IS_CTRL;
       }
       switch (in.op) {
@@ -1128,6 +1237,10 @@ class Decoder {
         case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64:
         case OP_LDP32: case OP_LDP64: case OP_MOVSP:
           o.aux = (uint32_t)in.imm;
+          break;
+        case OP_LDS32: case OP_LDS64: case OP_STS32: case OP_STS64:
+          o.aux = (uint32_t)in.imm;
+          if (in.flags & KS_SHA_WIDE) o.inc |= INC_ADDR64;
           break;
         case OP_CVT_F2I: o.aux = in.flags; break;
         case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32:

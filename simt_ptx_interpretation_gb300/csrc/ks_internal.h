@@ -32,9 +32,15 @@ enum Op : uint8_t {
   OP_CVT_F32_U32, OP_CVT_F32_S32, OP_CVT_F32_U64, OP_CVT_F32_S64,
   OP_CVT_F2I,          // flags: KS_CVT_* destination | rounding << 4
   OP_CVT_ZX, OP_CVT_SX,  // 32 -> 64 zero / sign extension
+  OP_LDS32, OP_LDS64,  // ld.shared (flags: KS_SHA_*)
+  OP_STS32, OP_STS64,  // st.shared
+  OP_BAR,              // bar.sync 0
   OP_COUNT
 };
 
+// shared address form in KsInsn::flags of OP_LDS* / OP_STS*: a register base
+// (KS_SHA_REG, 64-bit with KS_SHA_WIDE) plus KsInsn::imm, or imm alone
+constexpr uint8_t KS_SHA_REG = 1, KS_SHA_WIDE = 2;
 // setp comparison in KsInsn::flags
 enum Cmp : uint8_t { CMP_EQ = 0, CMP_NE, CMP_LT, CMP_LE, CMP_GT, CMP_GE };
 // cvt float->int destination (low nibble) and rounding (high nibble)
@@ -118,6 +124,8 @@ constexpr uint32_t DEV_IS_STORE = 1u << 9;
 constexpr uint32_t DEV_IS_CTRL = 1u << 10;
 // bits of DevInsn::inc
 constexpr uint32_t INC_ISSUE = 1u, INC_RDEST = 2u, INC_PDEST = 4u;
+// INC_ADDR64: the address operand `a` is a 64-bit register (shared accesses)
+constexpr uint32_t INC_ADDR64 = 32u;
 // INC_MID: unguarded register-to-register op with no predicate operand, no
 //          memory access and no control transfer (runs in the mid loop)
 // INC_PHAZ: has a predicate source or destination (its ready entries matter)
@@ -159,6 +167,10 @@ struct KsKernel {
   uint32_t n_slots = 0;
   uint32_t n_preds = 0;
   std::vector<int32_t> ipdom;
+  uint32_t shared_bytes = 0;  // simulated shared memory per CTA (.shared arrays)
+  bool has_bar = false;       // uses bar.sync
+  // a CTA's warps share state: they run together, one real CTA per simulated CTA
+  bool cta_mode() const { return shared_bytes > 0 || has_bar; }
   // [DevInsn x (n_insn + 1) | constant row values (u32 each), padded to 16]
   std::vector<uint8_t> image;
   DevLayout layout{};
@@ -186,7 +198,8 @@ struct KsLaunch {
   uint32_t n_crows;
   DevLayout layout;
   uint32_t grid, block, wpc;  // simulated grid, block, warps per simulated CTA
-  uint32_t gw_step_cta, gw_step_wic;  // the real-warp stride split into (CTAs, warps) of the simulated grid
+  uint32_t shared_bytes;      // simulated shared memory per CTA
+  uint32_t cta_mode;          // 1: one real CTA per simulated CTA, one real warp per simulated warp
   uint32_t n_warps;           // grid * wpc
   uint32_t lat[KS_NUM_LAT_CLASSES];
   uint32_t max_ts;
@@ -203,8 +216,9 @@ struct KsLaunch {
   alignas(16) uint8_t params[KS_MAX_PARAM_BYTES];
 };
 
-// Shared-memory footprint of one real CTA of `warps` warps.
-size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t warps);
+// Shared-memory footprint of one real CTA of `warps` warps (plus the
+// simulated shared memory of a CTA-mode launch).
+size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t warps, uint32_t shared_bytes);
 // Offset of the first warp region in shared memory.
 uint32_t interp_region0(uint32_t image_bytes);
 
@@ -212,13 +226,13 @@ uint32_t interp_region0(uint32_t image_bytes);
 const KsKernel* module_kernel(const ks_module* mod, const char* name);
 
 // Launchers (ks_interp.cu). Return a cudaError_t value.
-// Real launch shape for `n_warps` simulated warps: real warps per CTA (1..8)
-// and real CTAs (persistent). KS_OK, KS_ERR_LIMIT (no shape fits the shared
-// memory) or KS_ERR_CUDA.
-int choose_launch(uint64_t n_warps, uint32_t image_bytes, uint32_t region_bytes, int sms, int max_smem,
-                  uint32_t* real_warps_per_cta, uint32_t* real_ctas);
+// Real launch shape: real warps per CTA and real CTAs (persistent). A
+// CTA-mode launch (L.cta_mode) takes one real warp per simulated warp of a
+// CTA; otherwise 1..8 real warps per CTA over all simulated warps. KS_OK,
+// KS_ERR_LIMIT (no shape fits the shared memory) or KS_ERR_CUDA.
+int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps_per_cta, uint32_t* real_ctas);
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);
-int interp_occupancy(uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
+int interp_occupancy(bool cta_mode, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
 int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream);
 
 }  // namespace ks

@@ -170,8 +170,17 @@ __device__ __forceinline__ void st_pair(bool on, uint32_t addr, uint32_t v, uint
 constexpr uint32_t REBASE_AT = 1u << 30;
 constexpr uint64_t BUDGET_CHUNK = 1ull << 30;
 
+// Barrier rounds of a CTA-mode launch: the latest bar.sync issue cycle of the
+// round (absolute, two rounds in flight) and the count of finished warps.
+struct CtaCtl {
+  unsigned long long latest[2];
+  unsigned int done;
+  unsigned int pad;
+};
+constexpr uint32_t CTL_BYTES = 32;
+
 __host__ __device__ __forceinline__ uint32_t region0(uint32_t image_bytes) {
-  return (image_bytes + KS_MAX_PARAM_BYTES + 16u + 127u) / 128u * 128u;
+  return (image_bytes + KS_MAX_PARAM_BYTES + 16u + CTL_BYTES + 127u) / 128u * 128u;
 }
 
 __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32_t mask) {
@@ -180,6 +189,10 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 
 }  // namespace
 
+// CTA: the launch runs kernels with shared memory or bar.sync (one real CTA
+// per simulated CTA, barrier rounds, shared-memory handlers); compiled apart
+// so that the other kernels keep the register budget of the plain loop.
+template <bool CTA>
 __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant__ KsLaunch L) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
@@ -189,6 +202,9 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
 
   uint8_t* s_params = smem + L.image_bytes;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.image_bytes + KS_MAX_PARAM_BYTES);
+  CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + L.image_bytes + KS_MAX_PARAM_BYTES + 16u);
+  constexpr bool cta_mode = CTA;
+  const uint32_t sh_base = region0(L.image_bytes) + nwarps * Y.region_bytes;  // simulated shared memory
   const uint32_t wb = region0(L.image_bytes) + wid * Y.region_bytes;  // this warp's region
   const uint32_t lb = wb + lane * 8u;                                  // this lane's pair in row 0
   const uint32_t pg = wb + Y.pred_off;                                 // predicate ready table
@@ -239,6 +255,18 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
   for (uint32_t gw = blockIdx.x * nwarps + wid; gw < L.n_warps;
        gw += gw_stride, cta += step_cta, wic += step_wic, cta += (wic >= L.wpc), wic -= (wic >= L.wpc) ? L.wpc : 0u) {
     const uint32_t tid_sim = wic * 32u + lane;
+    if (cta_mode) {
+      // A new simulated CTA on this real CTA (one real warp per simulated
+      // warp, so every warp of the CTA is here): zeroed shared memory, fresh
+      // barrier rounds. The previous CTA's warps have all left its last round.
+      for (uint32_t i = threadIdx.x; i < (L.shared_bytes + 3u) / 4u; i += blockDim.x) SM32(sh_base + 4u * i) = 0u;
+      if (threadIdx.x == 0) {
+        ctl->latest[0] = 0ull;
+        ctl->latest[1] = 0ull;
+        ctl->done = 0u;
+      }
+      __syncthreads();
+    }
 
     // ---- warp set-up (a1): registers zero, predicates false, clock 0 ----
     for (uint32_t s = 0; s < Y.n_slots; s++) SM64(lb + s * ROW_BYTES) = 0ull;
@@ -248,6 +276,9 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
     uint32_t pc = 0, rpc = exit_pc;
     uint32_t mask = __ballot_sync(FULL, tid_sim < L.block);
     uint32_t depth = 1, max_depth = 1;
+    uint64_t sh_req = 0, sh_wf = 0;  // shared requests, their bank-conflict degrees
+    bool at_bar = false, finished = false;
+    uint64_t cyc_floor = 0;           // cycles owed to before a barrier's epoch move
     uint64_t epoch = 0;
     uint32_t t_next = 0, t_last = 0, max_ready = 0, drain = 0;
     uint64_t thread_insts = 0;
@@ -271,7 +302,8 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
     mark = budget;                                                      \
   } while (0)
 
-    if (status == 0) for (;;) {
+    for (uint32_t round = 0;; round++) {  // barrier rounds (one pass outside CTA mode)
+    if (status == 0 && !finished) for (;;) {
       // pop finished entries (a6); every control condition below is warp-uniform
       // in value
       if (pc == rpc || mask == 0) {
@@ -653,6 +685,58 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           pc++;
           break;
         }
+        // ---- shared memory: bank rule of analyze_shared_memory_access ----
+        case OP_LDS32: case OP_LDS64: case OP_STS32: case OP_STS64: if constexpr (CTA) {
+          const bool wide = (op == OP_LDS64 || op == OP_STS64);
+          const bool is_ld = (op == OP_LDS32 || op == OP_LDS64);
+          const uint32_t size = wide ? 8u : 4u;
+          const uint64_t va = ((inc & INC_ADDR64) ? A64() : (uint64_t)a0) + (uint64_t)(int64_t)(int32_t)aux;
+          int err = 0;
+          if (on)
+            err = (va & (uint64_t)(size - 1)) ? KS_ST_MISALIGNED
+                  : (L.shared_bytes < size || va > (uint64_t)(L.shared_bytes - size)) ? KS_ST_OOB : 0;
+          const uint32_t emask = __ballot_sync(FULL, err != 0);
+          if (emask) {
+            status = __shfl_sync(FULL, err, __ffs(emask) - 1);
+            break;
+          }
+          const uint32_t sva = (uint32_t)va;
+          // lanes on my address (the non-executing lanes get keys of their own)
+          const uint32_t same_addr = __match_any_sync(FULL, on ? sva : (0x80000000u | lane));
+          if (exec) {
+            // lanes in my bank: a bank that is all one address counts 1, any
+            // other bank its lanes; the request's degree is the largest
+            const uint32_t same_bank = __match_any_sync(FULL, on ? ((sva >> 2) & 31u) : (32u + lane));
+            const uint32_t deg = (on && same_addr != same_bank) ? (uint32_t)__popc(same_bank) : 1u;
+            sh_req++;
+            sh_wf += __reduce_max_sync(FULL, deg);
+          }
+          uint8_t* sp = smem + sh_base + sva;  // dereferenced by executing lanes only
+          if (is_ld) {
+            if (on) {
+              if (wide) {
+                const uint2 v = *reinterpret_cast<const uint2*>(sp);
+                SM32(lb + D) = v.x;
+                SM32(lb + D + ROW_BYTES) = v.y;
+              } else {
+                SM32(lb + D) = *reinterpret_cast<const uint32_t*>(sp);
+              }
+            }
+          } else if (on && (31u - __clz(same_addr)) == lane) {  // the highest lane on an address wins
+            if (wide) {
+              const uint64_t v = B64();
+              *reinterpret_cast<uint2*>(sp) = make_uint2((uint32_t)v, (uint32_t)(v >> 32));
+            } else {
+              *reinterpret_cast<uint32_t*>(sp) = b0;
+            }
+          }
+          pc++;
+          break;
+        }
+        case OP_BAR:  // stop until the CTA's barrier releases
+          if constexpr (CTA) at_bar = true;
+          pc++;
+          break;
         // ---- moves and integer ALU (a4) ----
         case OP_MOV32: W32(a0); pc++; break;
         case OP_MOV64: W64(A64()); pc++; break;
@@ -779,12 +863,58 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
         FLUSH_THREADS();
         break;
       }
+      if (at_bar) break;
     }
+    if constexpr (!cta_mode) break;
+    // ---- barrier round (CTA mode): each warp has stopped at bar.sync or
+    // finished; the stopped ones resume at the latest arrival + latency ----
+    if (!at_bar && !finished) {
+      finished = true;
+      if (lane == 0) atomicAdd(&ctl->done, 1u);
+    }
+    // the bar.sync is the last instruction issued: it arrived at epoch + t_last
+    if (at_bar && lane == 0) atomicMax(&ctl->latest[round & 1u], (unsigned long long)(epoch + t_last));
+    __syncthreads();
+    const unsigned long long latest = ctl->latest[round & 1u];
+    const bool all_done = ctl->done == nwarps;
+    if (threadIdx.x == 0) ctl->latest[(round + 1u) & 1u] = 0ull;  // last read two rounds ago
+    __syncthreads();
+    if (all_done) break;
+    if (at_bar) {
+      at_bar = false;
+      const uint64_t rel = (uint64_t)latest + L.lat[KS_LAT_BAR] - epoch;
+      if (rel < REBASE_AT) {
+        t_next = (uint32_t)rel;
+      } else {
+        // Far ahead of this warp's clock: move the epoch to just before the
+        // release. What the warp owes so far goes to cyc_floor; ready times
+        // before the release no longer matter (saturate to 0); t_last stays
+        // "none" (t_last + 1 == 0) until the next issue.
+        cyc_floor = max(cyc_floor, epoch + (uint64_t)max(max(t_last + 1u, max_ready), drain));
+        const uint64_t delta = rel - 1u;
+        for (uint32_t r = 0; r < Y.n_slots; r++) {
+          const uint32_t e = SM32(lb + r * ROW_BYTES + 4u);
+          SM32(lb + r * ROW_BYTES + 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
+        }
+        {
+          const uint32_t e = SM32(pg + lane * 4u);
+          SM32(pg + lane * 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
+        }
+        __syncwarp();
+        epoch += delta;
+        t_last = 0xFFFFFFFFu;
+        t_next = 1u;
+        max_ready = (uint64_t)max_ready > delta ? (uint32_t)(max_ready - delta) : 0u;
+        drain = (uint64_t)drain > delta ? (uint32_t)(drain - delta) : 0u;
+      }
+    }
+    }  // barrier rounds
 #undef FLUSH_THREADS
     const uint64_t warp_insts = stop_at - left - budget;
 
     // ---- write-back (a9) ----
-    const uint64_t cycles = warp_insts ? epoch + (uint64_t)max(max(t_last + 1u, max_ready), drain) : 0ull;
+    const uint64_t cycles =
+        warp_insts ? max(cyc_floor, epoch + (uint64_t)max(max(t_last + 1u, max_ready), drain)) : 0ull;
     if (lane == 0) {
       ulonglong2* r = reinterpret_cast<ulonglong2*>(L.stats + (uint64_t)gw * sizeof(ks_warp_stats));
       r[0] = make_ulonglong2(cycles, warp_insts);
@@ -792,7 +922,7 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       r[2] = make_ulonglong2(ld_sec, st_req);
       r[3] = make_ulonglong2(st_sec, ld_lin);
       r[4] = make_ulonglong2(st_lin, (uint64_t)(uint32_t)status | ((uint64_t)max_depth << 32));
-      r[5] = make_ulonglong2(0ull, 0ull);
+      r[5] = make_ulonglong2(sh_req, sh_wf);
     }
     if (slot) {
       uint32_t* sw = reinterpret_cast<uint32_t*>(slot);
@@ -813,10 +943,11 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
 
 // ---- launch-totals reduction -------------------------------------------------
 // acc: [0] cycles max, [1] cycles sum, [2..9] counter sums, [10] failed warps,
-// [11] max over failing warps of (2^64-1 - warp id), [12] max stack depth.
+// [11] max over failing warps of (2^64-1 - warp id), [12] max stack depth,
+// [13] shared requests, [14] shared wavefronts.
 __global__ void ks_reduce_kernel(const ks_warp_stats* __restrict__ s, uint64_t n,
                                  unsigned long long* __restrict__ acc) {
-  unsigned long long v[13] = {0};
+  unsigned long long v[15] = {0};
   for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
     const ks_warp_stats r = s[i];
     v[0] = v[0] > r.cycles ? v[0] : r.cycles;
@@ -835,9 +966,11 @@ __global__ void ks_reduce_kernel(const ks_warp_stats* __restrict__ s, uint64_t n
       v[11] = v[11] > inv ? v[11] : inv;
     }
     v[12] = v[12] > r.max_stack_depth ? v[12] : r.max_stack_depth;
+    v[13] += r.sh_req;
+    v[14] += r.sh_wavefronts;
   }
 #pragma unroll
-  for (int k = 0; k < 13; k++) {
+  for (int k = 0; k < 15; k++) {
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long u = __shfl_down_sync(FULL, v[k], o);
       if (k == 0 || k == 11 || k == 12) v[k] = v[k] > u ? v[k] : u;
@@ -846,7 +979,7 @@ __global__ void ks_reduce_kernel(const ks_warp_stats* __restrict__ s, uint64_t n
   }
   if ((threadIdx.x & 31) == 0) {
 #pragma unroll
-    for (int k = 0; k < 13; k++) {
+    for (int k = 0; k < 15; k++) {
       if (k == 0 || k == 11 || k == 12) atomicMax(&acc[k], v[k]);
       else if (v[k]) atomicAdd(&acc[k], v[k]);
     }
@@ -855,8 +988,8 @@ __global__ void ks_reduce_kernel(const ks_warp_stats* __restrict__ s, uint64_t n
 
 uint32_t interp_region0(uint32_t image_bytes) { return region0(image_bytes); }
 
-size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t warps) {
-  return (size_t)region0(image_bytes) + (size_t)region_bytes * warps;
+size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t warps, uint32_t shared_bytes) {
+  return (size_t)region0(image_bytes) + (size_t)region_bytes * warps + (size_t)(shared_bytes + 15u) / 16u * 16u;
 }
 
 static int g_attr_done[64];
@@ -869,21 +1002,34 @@ static int ensure_attr() {
   int mx = 0;
   e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return (int)e;
-  e = cudaFuncSetAttribute(ks_interp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  e = cudaFuncSetAttribute(ks_interp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e != cudaSuccess) return (int)e;
+  e = cudaFuncSetAttribute(ks_interp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   if (e != cudaSuccess) return (int)e;
   if (dev < 64) g_attr_done[dev] = 1;
   return 0;
 }
 
-int interp_occupancy(uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm) {
+int interp_occupancy(bool cta_mode, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm) {
   int e = ensure_attr();
   if (e) return e;
-  return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, ks_interp_kernel,
-                                                            (int)(real_warps_per_cta * 32), smem);
+  return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      ctas_per_sm, cta_mode ? ks_interp_kernel<true> : ks_interp_kernel<false>, (int)(real_warps_per_cta * 32), smem);
 }
 
-int choose_launch(uint64_t n_warps, uint32_t image_bytes, uint32_t region_bytes, int sms, int max_smem,
-                  uint32_t* real_warps_per_cta, uint32_t* real_ctas) {
+int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps_per_cta, uint32_t* real_ctas) {
+  const uint64_t n_warps = L.n_warps;
+  if (L.cta_mode) {
+    // one real CTA per simulated CTA at a time, one real warp per simulated warp
+    const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, L.wpc, L.shared_bytes);
+    if (smem > (size_t)max_smem) return KS_ERR_LIMIT;
+    int per_sm = 0;
+    if (interp_occupancy(true, L.wpc, smem, &per_sm)) return KS_ERR_CUDA;
+    if (per_sm < 1) return KS_ERR_LIMIT;
+    *real_warps_per_cta = L.wpc;
+    *real_ctas = (uint32_t)std::min<uint64_t>(L.grid, (uint64_t)sms * (uint64_t)per_sm);
+    return KS_OK;
+  }
   // Candidates: 1..8 real warps per CTA. While the simulated grid is small,
   // keep at least two CTAs per SM so that every SM gets work; among the rest
   // take the shape with the most resident real warps (shared memory,
@@ -893,13 +1039,13 @@ int choose_launch(uint64_t n_warps, uint32_t image_bytes, uint32_t region_bytes,
   uint64_t best_res = 0;
   bool any_fit = false;
   for (uint32_t w = 1; w <= 8; w++) {
-    const size_t smem = interp_smem_bytes(image_bytes, region_bytes, w);
+    const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, w, 0);
     if (smem > (size_t)max_smem) break;
     any_fit = true;
     const uint64_t want = (n_warps + w - 1) / w;
     if (w > 1 && want < 2ull * (uint64_t)sms) break;
     int per_sm = 0;
-    const int e = interp_occupancy(w, smem, &per_sm);
+    const int e = interp_occupancy(false, w, smem, &per_sm);
     if (e) return KS_ERR_CUDA;
     if (per_sm < 1) continue;
     const uint64_t cap = (uint64_t)sms * (uint64_t)per_sm;
@@ -919,8 +1065,12 @@ int choose_launch(uint64_t n_warps, uint32_t image_bytes, uint32_t region_bytes,
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream) {
   int e = ensure_attr();
   if (e) return e;
-  const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, real_warps_per_cta);
-  ks_interp_kernel<<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
+  const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, real_warps_per_cta,
+                                       L.cta_mode ? L.shared_bytes : 0u);
+  if (L.cta_mode)
+    ks_interp_kernel<true><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
+  else
+    ks_interp_kernel<false><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
   return (int)cudaGetLastError();
 }
 

@@ -78,6 +78,8 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
     if (cfg.lat[i] > ks::KS_MAX_LATENCY) return KS_ERR_ARG;
   const uint64_t slot = (16ull + 4ull * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
   if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
+  // shared memory / bar.sync: every warp of a CTA resident on one real CTA
+  if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
   // ---- the program image must fit the static array ----
   if (k->image.size() > KS_STATIC_IMAGE_BYTES) return KS_ERR_LIMIT;
 
@@ -102,6 +104,8 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   L.block = block;
   L.wpc = (block + 31u) / 32u;
   L.n_warps = (uint32_t)W;
+  L.shared_bytes = k->shared_bytes;
+  L.cta_mode = k->cta_mode() ? 1u : 0u;
   std::memcpy(L.lat, cfg.lat, sizeof L.lat);
   L.max_ts = cfg.max_ts_per_warp;
   L.stack_depth = cfg.simt_stack_depth;
@@ -121,8 +125,7 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   if (param_bytes) std::memcpy(L.params, params, param_bytes);
 
   uint32_t wpc_real = 0, ctas = 0;
-  const int shape = ks::choose_launch(W, L.image_bytes, k->layout.region_bytes, g_static_sms[dev],
-                                      g_static_smem[dev], &wpc_real, &ctas);
+  const int shape = ks::choose_launch(L, g_static_sms[dev], g_static_smem[dev], &wpc_real, &ctas);
   if (shape != KS_OK) return shape;
   if (ks::launch_interp(L, wpc_real, ctas, stream) != 0) return KS_ERR_CUDA;
   return KS_OK;

@@ -14,6 +14,7 @@ from simt_ptx_interpretation_gb300 import _build, _native
 from simt_ptx_interpretation_gb300 import api as ks
 from simt_ptx_interpretation_gb300 import workloads as wl
 from tests import test_oracle_control as toc
+from tests import test_oracle_shared as tsh
 from tests._kernels import op_kernel
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -57,6 +58,11 @@ def corpus():
     for name, body in toc.BAD_PROGRAMS:
         progs.append(("k", wl.HEADER + (".visible .entry k()\n{\n    .reg .pred %p<2>;\n    .reg .b32 %r<4>;\n"
                                         "    .reg .f32 %f<4>;\n    .reg .b64 %rd<4>;\n    " + body + "\n}\n")))
+    for block in (32, 64, 256):
+        progs.append(("smem_reduce", wl.smem_reduce_ptx(block)))
+    progs += [("probe", tsh.bank_probe_ptx(4)), ("probe", tsh.bank_probe_ptx(8)), ("bar2", tsh.barrier_ptx(3))]
+    for body, _ in tsh.SHARED_BAD:
+        progs.append(("bad", tsh.bad_shared_kernel(body)))
     for op, srcs, dst in [("add.u32", "uu", "u"), ("fma.rn.f32", "fff", "f"), ("setp.lt.f32", "ff", "p"),
                           ("selp.b64", "wwp", "w"), ("cvt.rzi.s64.f32", "f", "w"), ("shr.s64", "wu", "w")]:
         progs.append(("k_op", op_kernel("k_op", op, srcs, dst)))

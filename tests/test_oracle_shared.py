@@ -270,7 +270,7 @@ def test_shared_layout_alignment_and_bounds():
     assert oracle.run(kernel(16, "a"), "lay", 1, 32, b"", []).status == 1
 
 
-@pytest.mark.parametrize("body,code", [
+SHARED_BAD = [
     (".shared .align 4 .b8 s[49156];\n    ret;", -2),                                  # over 48 KiB
     ("bar.sync 1;\n    ret;", -2),                                                     # barrier 1
     ("bar.sync 0, 64;\n    ret;", -1),                                                 # thread count
@@ -278,9 +278,11 @@ def test_shared_layout_alignment_and_bounds():
     ("ld.shared.u32 %r1, [nowhere];\n    ret;", -1),                                   # unknown array
     (".shared .align 4 .b8 s[64];\n    mov.f32 %f1, s;\n    ret;", -1),                # float symbol
     (".shared .align 4 .b8 s[64];\n    ld.shared.u32 %r1, [%p1];\n    ret;", -1),      # predicate address
-])
-def test_rejected_forms(body, code):
-    ptx = wl.HEADER + f""".visible .entry bad()
+]
+
+
+def bad_shared_kernel(body: str) -> str:
+    return wl.HEADER + f""".visible .entry bad()
 {{
     .reg .pred %p<2>;
     .reg .b32 %r<3>;
@@ -288,4 +290,8 @@ def test_rejected_forms(body, code):
     {body}
 }}
 """
-    assert oracle.parse_check(ptx, "bad")[0] == code
+
+
+@pytest.mark.parametrize("body,code", SHARED_BAD)
+def test_rejected_forms(body, code):
+    assert oracle.parse_check(bad_shared_kernel(body), "bad")[0] == code
