@@ -8,7 +8,7 @@ block 128, 4096 outer iterations of 32 fma.rn.f32, one dependent-chain
 kernel and one with 8 rotating accumulators), i.e. two interpreter launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload ffma_pair|vector_add|gather_sS|divergent_kK|fuzz]
+                  [--workload ffma_pair|vector_add|gather_sS|divergent_kK|fuzz|smem_reduce]
 
 Prints one JSON line (rank 0). N > 1 runs N independent replicas, one per
 GPU (weak scaling; the path has no exchange step).
@@ -73,6 +73,9 @@ def workloads(name: str, iters: int = 4096, scale: int = 1):
         k = int(name[len("divergent_k"):])
         n = max(128, (1 << 20) // scale)
         return [wl.divergent(k, n=n)], {"workload": name, "threads": n, "block": 128, "k": k, "seed": 3}
+    if name == "smem_reduce":
+        n = max(256, (1 << 22) // scale)
+        return [wl.smem_reduce(n=n, block=256)], {"workload": "smem_reduce", "n": n, "block": 256, "seed": 5}
     if name == "fuzz":
         nk = max(1, 64 // scale)
         return [wl.fuzz(i) for i in range(nk)], {"workload": "fuzz64" if nk == 64 else f"fuzz{nk}", "grid": 1024,
@@ -333,7 +336,8 @@ def run_e2e(args, jobs, insts, dev, stream):
 
 def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None):
     """The oracle, as it stands, on the host cores over a bounded sample of the
-    workload: the first `n` warps of every kernel."""
+    workload: the first `n` warps of every kernel (whole CTAs for kernels with
+    shared memory or barriers, every one of which is counted)."""
     import oracle
     cores = os.cpu_count() or 1
     n = max_warps_per_kernel or 40 * cores
@@ -345,8 +349,9 @@ def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None):
         r = oracle.run(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in bufs],
                        max_ts=w.max_ts, trace=bool(w.max_ts), warps=warps, threads=cores)
         total_s += time.perf_counter() - t0
-        total_i += int(r.stats["thread_insts"][warps].sum())
-        desc.append(f"{w.name}: warps 0..{len(warps) - 1} of {w.warps}")
+        ran = r.stats["warp_insts"] > 0
+        total_i += int(r.stats["thread_insts"][ran].sum())
+        desc.append(f"{w.name}: warps 0..{int(np.nonzero(ran)[0].max())} of {w.warps}")
     return {"value": round(total_i / total_s, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "; ".join(desc), "thread_insts": total_i, "seconds": round(total_s, 3)}
 
