@@ -9,19 +9,25 @@
 //
 // Per real CTA, shared memory holds
 //   [program: 64-byte DevInsn records | constant row values]
-//   [parameter block | mbarrier]
+//   [parameter block | mbarrier | barrier-round control block]
 //   [one region per warp: register rows | constant rows | zero row |
-//    ready-time table | reconvergence stack]   (layout in ks_internal.h)
+//    predicate ready table | reconvergence stack]   (layout in ks_internal.h)
+//   [simulated shared memory of the CTA]             (CTA mode only)
 // The program image is staged once per CTA with one cp.async.bulk
 // global->shared copy completing on an mbarrier; the wait is bounded and
 // reports KS_ST_TIMEOUT instead of hanging. The launch's latency table is then
 // patched into the staged instructions.
 //
-// Every operand field of an instruction is the offset of a 128-byte row of the
-// warp's region, so lane l reads an operand with one shared load at
-// (region + offset + 4l): registers, constants (replicated across the row) and
-// "no operand" (the zero row) look the same. All operand and ready-time loads
-// of an instruction are issued together right after the fetch.
+// Every operand field of an instruction is the offset of a 256-byte row of the
+// warp's region holding one (value, ready) pair per lane, so lane l reads an
+// operand and its scoreboard entry with one 8-byte shared load at
+// (region + offset + 8l): registers, constants (replicated across the row) and
+// "no operand" (the zero row) look the same.
+//
+// Kernels with shared memory or bar.sync run in CTA mode (the CTA template
+// instantiation): one real CTA per simulated CTA, one real warp per simulated
+// warp, and barrier rounds between them (KernelScope backend doc,
+// simulator/models.py Block and Warp.at_barrier).
 //
 // Warp-uniform state (pc, active mask, scoreboard clock, counters) lives in
 // registers, identical in every lane; values every lane must agree on (ready
