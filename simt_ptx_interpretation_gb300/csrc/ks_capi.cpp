@@ -249,6 +249,10 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   L.n_warps = (uint32_t)W;
   L.shared_bytes = k->shared_bytes;
   L.cta_mode = k->cta_mode() ? 1u : 0u;
+  {
+    const uint32_t lmax = std::max(std::max(cfg.lat[KS_LAT_ALU], cfg.lat[KS_LAT_FMA]), 1u);
+    L.fast_shift = 32u - (uint32_t)__builtin_clz(lmax);  // 2^shift > lmax
+  }
   std::memcpy(L.lat, cfg.lat, sizeof L.lat);
   L.max_ts = cfg.max_ts_per_warp;
   L.stack_depth = cfg.simt_stack_depth;

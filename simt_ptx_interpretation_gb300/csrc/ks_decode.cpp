@@ -1254,6 +1254,14 @@ class Decoder {
         default: break;
       }
     }
+    // run lengths of the fast path (unguarded routed FPU / IMAD ops)
+    for (size_t i = n; i-- > 0;) {
+      DevInsn& o = dev[i];
+      if (o.op == DOP_FPU || o.op == DOP_IMAD) {
+        const uint32_t next = (dev[i + 1].op == DOP_FPU || dev[i + 1].op == DOP_IMAD) ? (dev[i + 1].inc >> INC_RUN_SHIFT) : 0u;
+        o.inc |= (next + 1u) << INC_RUN_SHIFT;
+      }
+    }
     K.prog_bytes = (uint32_t)((n + 1) * sizeof(DevInsn));
     const size_t cb = rowval.size() * 4;
     K.image.assign((K.prog_bytes + cb + 15) / 16 * 16, 0);

@@ -126,6 +126,9 @@ constexpr uint32_t DEV_IS_CTRL = 1u << 10;
 constexpr uint32_t INC_ISSUE = 1u, INC_RDEST = 2u, INC_PDEST = 4u;
 // INC_ADDR64: the address operand `a` is a 64-bit register (shared accesses)
 constexpr uint32_t INC_ADDR64 = 32u;
+// bits 16..31 of DevInsn::inc of a fast-path op: the number of consecutive
+// fast-path ops starting at it (a run's length, at most KS_MAX_INSNS)
+constexpr uint32_t INC_RUN_SHIFT = 16u;
 // INC_MID: unguarded register-to-register op with no predicate operand, no
 //          memory access and no control transfer (runs in the mid loop)
 // INC_PHAZ: has a predicate source or destination (its ready entries matter)
@@ -200,6 +203,7 @@ struct KsLaunch {
   uint32_t grid, block, wpc;  // simulated grid, block, warps per simulated CTA
   uint32_t shared_bytes;      // simulated shared memory per CTA
   uint32_t cta_mode;          // 1: one real CTA per simulated CTA, one real warp per simulated warp
+  uint32_t fast_shift;        // 2^fast_shift > the largest fast-path (ALU, FMA) latency
   uint32_t n_warps;           // grid * wpc
   uint32_t lat[KS_NUM_LAT_CLASSES];
   uint32_t max_ts;

@@ -337,8 +337,15 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       // the record of k+2 fetched; k+1's rows may predate k's store, so k's
       // result and ready time are forwarded into any of them that is k's
       // destination.
-      if (runnable && (q0.x | 1u) == DOP_IMAD) {
-        uint32_t fuel = fuel_in;
+      // The run is counted up front: at most the consecutive fast ops from pc
+      // (inc >> 16), the fuel, and as many steps as keep every clock below
+      // REBASE_AT (each step moves the clock by at most the largest fast-op
+      // latency, which 2^fast_shift bounds).
+      const uint32_t run_cap = max(t_next, max_ready) < REBASE_AT
+                                   ? (REBASE_AT - max(t_next, max_ready)) >> L.fast_shift : 0u;
+      const uint32_t run_n = min(min(fuel_in, q1.w >> INC_RUN_SHIFT), run_cap);
+      if (t_next < REBASE_AT && run_n != 0u && (q0.x | 1u) == DOP_IMAD) {
+        uint32_t n = run_n;
         const bool on_all = (mask >> lane) & 1u;
         // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
         uint4 ka = q0, kb = q1;
@@ -348,8 +355,6 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
         // k+2 stay within the program and its exit sentinel)
         uint4 na = ip[4], nb = ip[5];
         for (;;) {
-          // uniform in value; a plain branch is cheaper here than a vote
-          if (!(fuel != 0u && (ka.x | 1u) == DOP_IMAD && t_next < REBASE_AT)) break;
           uint2 a1 = SM2(lb + nb.x), b1 = SM2(lb + nb.y), c1 = SM2(lb + nb.z);
           uint32_t rd1 = SM32(lb + na.w + 4u);
           const uint4 ma = ip[8], mb = ip[9];
@@ -380,12 +385,11 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           b = b1;
           c = c1;
           rd = rd1;
-          fuel--;
           ip += 4;
+          if (--n == 0u) break;  // uniform in value
         }
-        const uint32_t steps = fuel_in - fuel;  // at least 1
-        pc += steps;
-        budget -= steps;
+        pc += run_n;
+        budget -= run_n;
         t_last = t_next - 1u;
         continue;
       }

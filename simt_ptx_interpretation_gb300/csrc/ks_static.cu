@@ -10,6 +10,7 @@
 // which every GPU that loads the library holds until the process exits.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -106,6 +107,10 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   L.n_warps = (uint32_t)W;
   L.shared_bytes = k->shared_bytes;
   L.cta_mode = k->cta_mode() ? 1u : 0u;
+  {
+    const uint32_t lmax = std::max(std::max(cfg.lat[KS_LAT_ALU], cfg.lat[KS_LAT_FMA]), 1u);
+    L.fast_shift = 32u - (uint32_t)__builtin_clz(lmax);  // 2^shift > lmax
+  }
   std::memcpy(L.lat, cfg.lat, sizeof L.lat);
   L.max_ts = cfg.max_ts_per_warp;
   L.stack_depth = cfg.simt_stack_depth;
