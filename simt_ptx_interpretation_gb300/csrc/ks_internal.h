@@ -38,6 +38,13 @@ enum Op : uint8_t {
   OP_COUNT
 };
 
+// the interpreter tests these opcode ranges with two compares
+static_assert(OP_LDG64 == OP_LDG32 + 1 && OP_STG32 == OP_LDG32 + 2 && OP_STG64 == OP_LDG32 + 3,
+              "ld/st.global opcodes must be consecutive");
+static_assert(OP_SETP_S32 == OP_SETP_U32 + 1 && OP_SETP_U64 == OP_SETP_U32 + 2 && OP_SETP_S64 == OP_SETP_U32 + 3 &&
+                  OP_SETP_F32 == OP_SETP_U32 + 4,
+              "setp opcodes must be consecutive");
+
 // shared address form in KsInsn::flags of OP_LDS* / OP_STS*: a register base
 // (KS_SHA_REG, 64-bit with KS_SHA_WIDE) plus KsInsn::imm, or imm alone
 constexpr uint8_t KS_SHA_REG = 1, KS_SHA_WIDE = 2;

@@ -565,18 +565,10 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
     st_shared_if(on, s_lane + D + ROW_BYTES, (uint32_t)(v_ >> 32)); \
   } while (0)
 
-      switch (op) {
-        // ---- the routed datapaths (guarded, or outside a fast run) ----
-        case DOP_FPU: case DOP_FPU | DOP_GUARDED:
-          W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))));
-          pc++;
-          break;
-        case DOP_IMAD: case DOP_IMAD | DOP_GUARDED:
-          W32(a0 * b0 + ((c0 ^ aux) - aux));
-          pc++;
-          break;
-        // ---- control (a6) ----
-        case OP_BRA: {
+      // The most frequent general-path ops take plain branches ahead of the
+      // switch (its indirect jump costs a lone warp more than the case itself);
+      // each body sits in do { } while (0) so that `break` ends the instruction.
+      if (op == OP_BRA) do {  // ---- control (a6)
           const uint32_t target = aux & 0xFFFFu, R = aux >> 16;
           const uint32_t taken = exec, fall = mask & ~exec;
           if (fall == 0) {
@@ -611,21 +603,31 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
             mask = (uint32_t)(e >> 32);
           }
           break;
-        }
-        case OP_RET: {
-          FLUSH_THREADS();
-          for (uint32_t i = 0; i + 1 < depth; i++) {
-            const uint32_t at = wb + Y.stack_off + i * 8u;
-            SM64(at) = SM64(at) & ~((uint64_t)exec << 32);
+        } while (0);
+      else if (op >= OP_SETP_U32 && op <= OP_SETP_F32) do {  // ---- predicates
+          const uint32_t cmp = aux & 0xFFu, pd = (aux >> 8) & 0xFFu;
+          bool lt, eq, gt;
+          if (op == OP_SETP_F32) {
+            const float x = __uint_as_float(a0), y = __uint_as_float(b0);
+            lt = x < y; eq = x == y; gt = x > y;
+          } else {
+            // signed order = unsigned order with the sign bits flipped
+            const bool sgn = op == OP_SETP_S32 || op == OP_SETP_S64;
+            uint64_t x, y;
+            if (op == OP_SETP_U64 || op == OP_SETP_S64) { x = A64(); y = B64(); }
+            else if (sgn) { x = (uint64_t)(int64_t)(int32_t)a0; y = (uint64_t)(int64_t)(int32_t)b0; }
+            else { x = a0; y = b0; }
+            const uint64_t flip = sgn ? (1ull << 63) : 0ull;
+            x ^= flip; y ^= flip;
+            lt = x < y; eq = x == y; gt = x > y;
           }
-          mask &= ~exec;
+          const uint32_t bal = __ballot_sync(FULL, rel_result(lt, eq, gt, cmp));
+          // lane pd holds predicate pd
+          if (lane == pd) my_pred = (my_pred & ~exec) | (bal & exec);
           pc++;
           break;
-        }
-        // ---- memory (a5) ----
-        case OP_LDP32: W32(*reinterpret_cast<const uint32_t*>(s_params + aux)); pc++; break;
-        case OP_LDP64: W64(*reinterpret_cast<const uint64_t*>(s_params + aux)); pc++; break;
-        case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64: {
+        } while (0);
+      else if (op >= OP_LDG32 && op <= OP_STG64) do {  // ---- global memory (a5)
           const bool wide = (op == OP_LDG64 || op == OP_STG64);
           const bool is_ld = (op == OP_LDG32 || op == OP_LDG64);
           const uint32_t size = wide ? 8u : 4u;
@@ -694,7 +696,33 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           }
           pc++;
           break;
+        } while (0);
+      else switch (op) {
+        // ---- the routed datapaths (guarded, or outside a fast run) ----
+        case DOP_FPU: case DOP_FPU | DOP_GUARDED:
+          W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))));
+          pc++;
+          break;
+        case DOP_IMAD: case DOP_IMAD | DOP_GUARDED:
+          W32(a0 * b0 + ((c0 ^ aux) - aux));
+          pc++;
+          break;
+        // ---- control (a6) ----
+
+        case OP_RET: {
+          FLUSH_THREADS();
+          for (uint32_t i = 0; i + 1 < depth; i++) {
+            const uint32_t at = wb + Y.stack_off + i * 8u;
+            SM64(at) = SM64(at) & ~((uint64_t)exec << 32);
+          }
+          mask &= ~exec;
+          pc++;
+          break;
         }
+        // ---- memory (a5) ----
+        case OP_LDP32: W32(*reinterpret_cast<const uint32_t*>(s_params + aux)); pc++; break;
+        case OP_LDP64: W64(*reinterpret_cast<const uint64_t*>(s_params + aux)); pc++; break;
+
         // ---- shared memory: bank rule of analyze_shared_memory_access ----
         case OP_LDS32: case OP_LDS64: case OP_STS32: case OP_STS64: if constexpr (CTA) {
           const bool wide = (op == OP_LDS64 || op == OP_STS64);
@@ -801,29 +829,7 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
         case OP_FDIV: W32(fbits(__fdiv_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
         case OP_FSQRT: W32(fbits(__fsqrt_rn(__uint_as_float(a0)))); pc++; break;
         // ---- predicates ----
-        case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32: {
-          const uint32_t cmp = aux & 0xFFu, pd = (aux >> 8) & 0xFFu;
-          bool lt, eq, gt;
-          if (op == OP_SETP_F32) {
-            const float x = __uint_as_float(a0), y = __uint_as_float(b0);
-            lt = x < y; eq = x == y; gt = x > y;
-          } else {
-            // signed order = unsigned order with the sign bits flipped
-            const bool sgn = op == OP_SETP_S32 || op == OP_SETP_S64;
-            uint64_t x, y;
-            if (op == OP_SETP_U64 || op == OP_SETP_S64) { x = A64(); y = B64(); }
-            else if (sgn) { x = (uint64_t)(int64_t)(int32_t)a0; y = (uint64_t)(int64_t)(int32_t)b0; }
-            else { x = a0; y = b0; }
-            const uint64_t flip = sgn ? (1ull << 63) : 0ull;
-            x ^= flip; y ^= flip;
-            lt = x < y; eq = x == y; gt = x > y;
-          }
-          const uint32_t bal = __ballot_sync(FULL, rel_result(lt, eq, gt, cmp));
-          // lane pd holds predicate pd
-          if (lane == pd) my_pred = (my_pred & ~exec) | (bal & exec);
-          pc++;
-          break;
-        }
+
         case OP_ANDP: case OP_ORP: case OP_XORP: {
           const uint32_t pa = __shfl_sync(FULL, my_pred, aux & 0xFFu);
           const uint32_t pb = __shfl_sync(FULL, my_pred, (aux >> 8) & 0xFFu);
