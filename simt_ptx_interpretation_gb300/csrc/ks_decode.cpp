@@ -1105,6 +1105,12 @@ class Decoder {
     return op == OP_ADD32 || op == OP_SUB32 || op == OP_MUL32 || op == OP_MAD32 || op == OP_MOV32;
   }
 
+  // ops whose second operand is read as b | aux (aux = an immediate b, or 0)
+  static bool imm_b_op(uint8_t op) {
+    return op == OP_AND32 || op == OP_OR32 || op == OP_XOR32 || op == OP_SHL32 || op == OP_SHR32U ||
+           op == OP_SHR32S || op == OP_SHL64 || op == OP_SHR64U || op == OP_SHR64S;
+  }
+
   static unsigned routed_width(const KsInsn& in, int pos) {
     if (fpu_family(in.op) || imad_family(in.op)) return 32;
     return row_width(in, pos);
@@ -1115,46 +1121,86 @@ class Decoder {
   // Lays out the warp region and emits the device image.
   void build_image() {
     const size_t n = K.code.size();
-    // rewrite the unified-datapath families onto (a, b, c) of fma / mad
+    // Rewrite the unified-datapath families onto (a, b, c) of fma / mad.
+    // The addend reads c ^ aux: an immediate addend goes into aux with c on
+    // the zero row (no constant row), a register addend has aux 0 (integer)
+    // or the sign flip of a subtraction (f32). Integer subtraction needs no
+    // negation: a - b = b * (-1) + a, a - imm = a * 1 + (-imm).
     struct Route { uint8_t a, b, c; uint32_t aux; };
     std::vector<Route> route(n);
+    auto is_const = [](uint8_t o) { return (o & KS_CONST_BIT) != 0; };
+    auto cval = [&](uint8_t o) { return (uint32_t)K.cpool[o & 0x7F]; };
     for (size_t i = 0; i < n; i++) {
       const KsInsn& in = K.code[i];
       Route r{in.a, in.b, in.c, 0};
       if (fpu_family(in.op)) {
         if (in.op == OP_FADD || in.op == OP_FSUB) {
+          uint8_t x = in.a, y = in.b;
+          const uint32_t flip = in.op == OP_FSUB ? 0x80000000u : 0u;
+          if (in.op == OP_FADD && is_const(x) && !is_const(y)) std::swap(x, y);  // add is commutative
+          r.a = x;
           r.b = constant(0x3F800000ull, in_line(i));
-          r.c = in.b;
-          r.aux = in.op == OP_FSUB ? 0x80000000u : 0u;
+          if (is_const(y)) { r.c = OPND_ZERO; r.aux = cval(y) ^ flip; }
+          else { r.c = y; r.aux = flip; }
         } else if (in.op == OP_FMUL) {
-          r.c = constant(0x80000000ull, in_line(i));
+          r.c = OPND_ZERO;
+          r.aux = 0x80000000u;  // + (-0.0): x * y exactly rounded, signs of zero kept
+        } else if (is_const(in.c)) {  // fma with an immediate addend
+          r.c = OPND_ZERO;
+          r.aux = cval(in.c);
         }
       } else if (imad_family(in.op)) {
-        if (in.op == OP_ADD32 || in.op == OP_SUB32) {
+        if (in.op == OP_ADD32) {
+          uint8_t x = in.a, y = in.b;
+          if (is_const(x) && !is_const(y)) std::swap(x, y);
+          r.a = x;
           r.b = constant(1ull, in_line(i));
-          r.c = in.b;
-          r.aux = in.op == OP_SUB32 ? 0xFFFFFFFFu : 0u;
+          if (is_const(y)) { r.c = OPND_ZERO; r.aux = cval(y); }
+          else { r.c = y; r.aux = 0; }
+        } else if (in.op == OP_SUB32) {
+          if (is_const(in.b)) {
+            r.a = in.a;
+            r.b = constant(1ull, in_line(i));
+            r.c = OPND_ZERO;
+            r.aux = 0u - cval(in.b);
+          } else {
+            r.a = in.b;
+            r.b = constant(0xFFFFFFFFull, in_line(i));
+            if (is_const(in.a)) { r.c = OPND_ZERO; r.aux = cval(in.a); }
+            else { r.c = in.a; r.aux = 0; }
+          }
         } else if (in.op == OP_MUL32) {
-          r.c = constant(0ull, in_line(i));
+          r.c = OPND_ZERO;
+        } else if (in.op == OP_MAD32) {
+          if (is_const(in.c)) { r.c = OPND_ZERO; r.aux = cval(in.c); }
         } else if (in.op == OP_MOV32) {
-          r.b = constant(1ull, in_line(i));
-          r.c = constant(0ull, in_line(i));
+          if (is_const(in.a)) { r.a = r.b = r.c = OPND_ZERO; r.aux = cval(in.a); }
+          else { r.b = constant(1ull, in_line(i)); r.c = OPND_ZERO; }
         }
+      } else if (imm_b_op(in.op)) {
+        // 32-bit logic and shifts (of either width) read b | aux
+        uint8_t x = in.a, y = in.b;
+        const bool commutes = in.op == OP_AND32 || in.op == OP_OR32 || in.op == OP_XOR32;
+        if (commutes && is_const(x) && !is_const(y)) std::swap(x, y);
+        if (is_const(y)) { r.a = x; r.b = OPND_ZERO; r.aux = cval(y); }
       }
       route[i] = r;
     }
-    // constant rows: one per constant, two if any use is 64-bit
-    std::vector<unsigned> cwidth(K.cpool.size(), 32);
+    // constant rows: one per constant still read from a row, two if any such
+    // use is 64-bit
+    std::vector<unsigned> cwidth(K.cpool.size(), 0);
     for (size_t i = 0; i < n; i++) {
       const KsInsn& in = K.code[i];
       const uint8_t ops[4] = {route[i].a, route[i].b, route[i].c, in.d};
       for (int p = 0; p < 4; p++) {
         const unsigned w = routed_width(in, p);
-        if (w && (ops[p] & KS_CONST_BIT)) cwidth[ops[p] & 0x7F] = std::max(cwidth[ops[p] & 0x7F], w);
+        if (w && ops[p] != OPND_ZERO && (ops[p] & KS_CONST_BIT))
+          cwidth[ops[p] & 0x7F] = std::max(cwidth[ops[p] & 0x7F], w);
       }
     }
-    std::vector<uint32_t> crow(K.cpool.size()), rowval;
+    std::vector<uint32_t> crow(K.cpool.size(), 0), rowval;
     for (size_t k = 0; k < K.cpool.size(); k++) {
+      if (!cwidth[k]) continue;
       crow[k] = (uint32_t)rowval.size();
       rowval.push_back((uint32_t)K.cpool[k]);
       if (cwidth[k] == 64) rowval.push_back((uint32_t)(K.cpool[k] >> 32));
@@ -1169,6 +1215,7 @@ class Decoder {
     Y.region_bytes = Y.stack_off + KS_MAX_STACK * 8u;
 
     auto row_of = [&](uint8_t o) -> uint32_t {
+      if (o == OPND_ZERO) return Y.zero_off;
       return (o & KS_CONST_BIT) ? Y.const_off + crow[o & 0x7F] * ROW_BYTES : (uint32_t)o * ROW_BYTES;
     };
     // predicate hazards live in the predicate table; register hazards travel
@@ -1200,7 +1247,7 @@ class Decoder {
       uint32_t* rows[4] = {&o.a, &o.b, &o.c, &o.d};
       for (int p = 0; p < 4; p++)
         if (routed_width(in, p)) *rows[p] = row_of(ops[p]);
-      if ((o.op & ~DOP_GUARDED) == DOP_FPU || (o.op & ~DOP_GUARDED) == DOP_IMAD) o.aux = route[i].aux;
+      if ((o.op & ~DOP_GUARDED) == DOP_FPU || (o.op & ~DOP_GUARDED) == DOP_IMAD || imm_b_op(in.op)) o.aux = route[i].aux;
       if (in.op != OP_EVENT) {
         o.ha = phz(in.ha);
         o.hb = phz(in.hb);

@@ -63,6 +63,8 @@ constexpr uint32_t KS_MAX_SLOTS = 96;
 constexpr uint32_t KS_MAX_PREDS = 31;
 constexpr uint32_t KS_MAX_CONSTS = 128;
 constexpr uint8_t KS_CONST_BIT = 0x80;
+// a routed operand position that reads the zero row (its value travels in aux)
+constexpr uint8_t OPND_ZERO = 0x7F;
 // Scoreboard (ready-time table) indices: slots 0..95, predicates 96..126,
 // 127 never written (always ready).
 constexpr uint32_t KS_HZ_PRED0 = 96;

@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           t_next = t + 1u;
           const uint32_t cx = c.x ^ ka.z;
           const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
-          const uint32_t ri = a.x * b.x + (cx - ka.z);
+          const uint32_t ri = a.x * b.x + cx;
           const uint32_t res = ka.x == DOP_FPU ? rf : ri;
           st_pair(on_all, s_lane + ka.w, res, wr);
           // forward k into k+1
@@ -429,20 +429,20 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
             case OP_SUB64: R64(MA64() - MB64()); break;
             case OP_MUL64: R64(MA64() * MB64()); break;
             case OP_MAD64: R64(MA64() * MB64() + ((uint64_t)pcc.x | ((uint64_t)SM32(lb + kb.z + ROW_BYTES) << 32))); break;
-            case OP_AND32: lo = a0 & b0; break;
-            case OP_OR32: lo = a0 | b0; break;
-            case OP_XOR32: lo = a0 ^ b0; break;
+            case OP_AND32: lo = a0 & (b0 | aux); break;
+            case OP_OR32: lo = a0 | (b0 | aux); break;
+            case OP_XOR32: lo = a0 ^ (b0 | aux); break;
             case OP_AND64: R64(MA64() & MB64()); break;
             case OP_OR64: R64(MA64() | MB64()); break;
             case OP_XOR64: R64(MA64() ^ MB64()); break;
-            case OP_SHL32: lo = b0 >= 32u ? 0u : a0 << b0; break;
-            case OP_SHR32U: lo = b0 >= 32u ? 0u : a0 >> b0; break;
-            case OP_SHR32S: lo = (uint32_t)(b0 >= 32u ? ((int32_t)a0 >> 31) : ((int32_t)a0 >> b0)); break;
-            case OP_SHL64: R64(b0 >= 64u ? 0ull : MA64() << b0); break;
-            case OP_SHR64U: R64(b0 >= 64u ? 0ull : MA64() >> b0); break;
+            case OP_SHL32: lo = (b0 | aux) >= 32u ? 0u : a0 << (b0 | aux); break;
+            case OP_SHR32U: lo = (b0 | aux) >= 32u ? 0u : a0 >> (b0 | aux); break;
+            case OP_SHR32S: lo = (uint32_t)((b0 | aux) >= 32u ? ((int32_t)a0 >> 31) : ((int32_t)a0 >> (b0 | aux))); break;
+            case OP_SHL64: R64((b0 | aux) >= 64u ? 0ull : MA64() << (b0 | aux)); break;
+            case OP_SHR64U: R64((b0 | aux) >= 64u ? 0ull : MA64() >> (b0 | aux)); break;
             case OP_SHR64S: {
               const int64_t x = (int64_t)MA64();
-              R64((uint64_t)(b0 >= 64u ? (x >> 63) : (x >> b0)));
+              R64((uint64_t)((b0 | aux) >= 64u ? (x >> 63) : (x >> (b0 | aux))));
               break;
             }
             case OP_FDIV: lo = fbits(__fdiv_rn(__uint_as_float(a0), __uint_as_float(b0))); break;
@@ -704,7 +704,7 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           pc++;
           break;
         case DOP_IMAD: case DOP_IMAD | DOP_GUARDED:
-          W32(a0 * b0 + ((c0 ^ aux) - aux));
+          W32(a0 * b0 + (c0 ^ aux));
           pc++;
           break;
         // ---- control (a6) ----
@@ -801,20 +801,20 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
         case OP_SUB64: W64(A64() - B64()); pc++; break;
         case OP_MUL64: W64(A64() * B64()); pc++; break;
         case OP_MAD64: W64(A64() * B64() + C64()); pc++; break;
-        case OP_AND32: W32(a0 & b0); pc++; break;
-        case OP_OR32: W32(a0 | b0); pc++; break;
-        case OP_XOR32: W32(a0 ^ b0); pc++; break;
+        case OP_AND32: W32(a0 & (b0 | aux)); pc++; break;
+        case OP_OR32: W32(a0 | (b0 | aux)); pc++; break;
+        case OP_XOR32: W32(a0 ^ (b0 | aux)); pc++; break;
         case OP_AND64: W64(A64() & B64()); pc++; break;
         case OP_OR64: W64(A64() | B64()); pc++; break;
         case OP_XOR64: W64(A64() ^ B64()); pc++; break;
-        case OP_SHL32: W32(b0 >= 32u ? 0u : a0 << b0); pc++; break;
-        case OP_SHR32U: W32(b0 >= 32u ? 0u : a0 >> b0); pc++; break;
-        case OP_SHR32S: W32((uint32_t)(b0 >= 32u ? ((int32_t)a0 >> 31) : ((int32_t)a0 >> b0))); pc++; break;
-        case OP_SHL64: W64(b0 >= 64u ? 0ull : A64() << b0); pc++; break;
-        case OP_SHR64U: W64(b0 >= 64u ? 0ull : A64() >> b0); pc++; break;
+        case OP_SHL32: W32((b0 | aux) >= 32u ? 0u : a0 << (b0 | aux)); pc++; break;
+        case OP_SHR32U: W32((b0 | aux) >= 32u ? 0u : a0 >> (b0 | aux)); pc++; break;
+        case OP_SHR32S: W32((uint32_t)((b0 | aux) >= 32u ? ((int32_t)a0 >> 31) : ((int32_t)a0 >> (b0 | aux)))); pc++; break;
+        case OP_SHL64: W64((b0 | aux) >= 64u ? 0ull : A64() << (b0 | aux)); pc++; break;
+        case OP_SHR64U: W64((b0 | aux) >= 64u ? 0ull : A64() >> (b0 | aux)); pc++; break;
         case OP_SHR64S: {
           const int64_t x = (int64_t)A64();
-          W64((uint64_t)(b0 >= 64u ? (x >> 63) : (x >> b0)));
+          W64((uint64_t)((b0 | aux) >= 64u ? (x >> 63) : (x >> (b0 | aux))));
           pc++;
           break;
         }
