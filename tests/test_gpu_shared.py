@@ -52,7 +52,8 @@ def shared_access_workload(pattern: str, guard: str, size: int) -> wl.Workload:
     """Each warp stores its thread ids to its own slice of shared memory (1024
     elements) through a pattern, passes a barrier, loads back through the same
     pattern (duplicate addresses give the highest lane's value) and writes
-    what it read to global memory."""
+    what it read to global memory (lanes that skip the load write the 0 they
+    were given, so the program is defined natively too)."""
     gset, g = {"all": ("", ""), "lt20": ("setp.lt.u32 %p1, %r7, 20;", "@%p1 "),
                "odd": ("and.b32 %r5, %r7, 1;\n    setp.ne.u32 %p1, %r5, 0;", "@%p1 ")}[guard]
     sh = 2 if size == 4 else 3
@@ -78,6 +79,8 @@ def shared_access_workload(pattern: str, guard: str, size: int) -> wl.Workload:
     add.u32 %r2, %r2, %r6;
     mov.u32 %r3, smem;
     add.u32 %r3, %r3, %r2;
+    mov.u32 %r4, 0;
+    mov.u64 %rd5, 0;
     {gset}
     {st}
     bar.sync 0;
@@ -215,3 +218,29 @@ def test_cta_mode_rejects_large_blocks():
         ks.run(m, w.kernel, 1, 288, w.params, [(b.sim_base, torch.zeros(b.data.nbytes, dtype=torch.uint8).cuda())
                                                for b in w.buffers])
     assert e.value.code == -6
+
+
+# -------------------------------------------- the driver JIT as a third party ----
+
+@pytest.mark.parametrize("block", [32, 64, 256])
+def test_jit_crosscheck_smem_reduce(block):
+    """The same PTX run natively through the driver JIT gives the same memory."""
+    from tests.test_gpu_parity import jit_memory
+    w = wl.smem_reduce(n=block * 64, block=block)
+    sim = _parity.gpu_run(w).buffers
+    nat = jit_memory(w)
+    for b, x, y in zip(w.buffers, sim, nat):
+        assert np.array_equal(x, y), b.name
+
+
+@pytest.mark.parametrize("size", [4, 8])
+@pytest.mark.parametrize("guard", ["all", "odd"])
+@pytest.mark.parametrize("pattern", ["seq", "stride2", "stride32", "stride33", "reverse"])
+def test_jit_crosscheck_shared_patterns(pattern, guard, size):
+    # patterns whose stores never share an address (PTX leaves the winner of
+    # same-address stores unspecified)
+    from tests.test_gpu_parity import jit_memory
+    w = shared_access_workload(pattern, guard, size)
+    sim = _parity.gpu_run(w).buffers
+    nat = jit_memory(w)
+    assert np.array_equal(sim[0], nat[0])
