@@ -1290,9 +1290,15 @@ class Decoder {
           if (in.flags & KS_SHA_WIDE) o.inc |= INC_ADDR64;
           break;
         case OP_CVT_F2I: o.aux = in.flags; break;
-        case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32:
+        case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32: {
           o.aux = (uint32_t)in.flags | ((uint32_t)in.d << 8);
+          const KsInsn* nx = i + 1 < n ? &K.code[i + 1] : nullptr;
+          if (in.guard == KS_NO_GUARD && nx && nx->op == OP_BRA && nx->guard == in.d && nx->target < (1u << 15)) {
+            o.inc |= INC_FUSE;
+            o.aux |= ((uint32_t)(nx->gneg ? 1u : 0u) << 16) | (nx->target << 17);
+          }
           break;
+        }
         case OP_ANDP: case OP_ORP: case OP_XORP:
           o.aux = (uint32_t)in.a | ((uint32_t)in.b << 8) | ((uint32_t)in.d << 16);
           break;

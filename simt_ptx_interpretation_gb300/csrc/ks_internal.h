@@ -135,6 +135,10 @@ constexpr uint32_t DEV_IS_CTRL = 1u << 10;
 constexpr uint32_t INC_ISSUE = 1u, INC_RDEST = 2u, INC_PDEST = 4u;
 // INC_ADDR64: the address operand `a` is a 64-bit register (shared accesses)
 constexpr uint32_t INC_ADDR64 = 32u;
+// INC_FUSE: an unguarded setp whose next entry is a bra guarded by the setp's
+// predicate; aux bit 16 = that guard's negation, aux bits 17..31 = the bra's
+// target, so a uniform outcome issues the bra in the same step
+constexpr uint32_t INC_FUSE = 64u;
 // bits 16..31 of DevInsn::inc of a fast-path op: the number of consecutive
 // fast-path ops starting at it (a run's length, at most KS_MAX_INSNS)
 constexpr uint32_t INC_RUN_SHIFT = 16u;

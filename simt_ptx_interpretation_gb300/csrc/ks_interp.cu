@@ -624,6 +624,22 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
           const uint32_t bal = __ballot_sync(FULL, rel_result(lt, eq, gt, cmp));
           // lane pd holds predicate pd
           if (lane == pd) my_pred = (my_pred & ~exec) | (bal & exec);
+          if ((inc & INC_FUSE) && exec == mask && budget != 0u && pc + 1u != rpc && t_next < REBASE_AT) {
+            // the next entry is `@[!]p bra` on this predicate: when every active
+            // lane goes the same way it issues here, exactly as the general
+            // path would (no register operands; its guard ready at wr)
+            const uint32_t taken = mask & (bal ^ (((aux >> 16) & 1u) ? 0xFFFFFFFFu : 0u));
+            if (taken == mask || taken == 0u) {
+              const uint32_t t2 = max(t_next, wr);
+              max_ready = max(max_ready, t2);
+              drain = max(drain, t2);
+              t_last = t2;
+              t_next = t2 + L.lat[KS_LAT_BRA];
+              budget--;
+              pc = taken ? (aux >> 17) : pc + 2u;
+              break;
+            }
+          }
           pc++;
           break;
         } while (0);

@@ -224,6 +224,19 @@ def test_access_patterns_match_the_oracle(pattern, guard, size):
 
 # ------------------------------------------------------------- statuses ----
 
+def test_step_limits_around_compare_and_branch_pairs():
+    """A step budget that ends on, between or after a setp and the bra it
+    guards (issued together when every lane agrees) stops the warp where the
+    oracle stops it: uniform loop back-edges (FFMA probe) and divergent loop
+    exits (divergent workload)."""
+    w = wl.ffma(acc=1, iters=3, per_iter=2, grid=1, block=64)
+    for limit in range(1, 48):
+        _parity.assert_parity(w, cfg=ks.Config(max_ts=w.max_ts, step_limit=limit))
+    d = wl.divergent(4, n=256)
+    for limit in (20, 21, 22, 23, 40, 41, 42, 43, 44, 45, 46, 300, 301, 302):
+        _parity.assert_parity(d, cfg=ks.Config(max_ts=d.max_ts, step_limit=limit))
+
+
 def test_error_statuses_match_the_oracle():
     base = 0x60000000
     buf = np.zeros(1024, dtype=np.uint8)
