@@ -126,6 +126,9 @@ def _load():
                                    ctypes.POINTER(ctypes.c_uint32), ctypes.c_uint32,
                                    ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32),
                                    ctypes.c_char_p, ctypes.c_uint64]
+        lib.orc_record_bytes.restype = ctypes.c_int
+        lib.orc_record_bytes.argtypes = [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_uint32),
+                                         ctypes.c_char_p, ctypes.c_uint64]
         lib.orc_events.restype = ctypes.c_int
         lib.orc_events.argtypes = [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_uint32),
                                    ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32), ctypes.c_char_p,
@@ -134,14 +137,14 @@ def _load():
     return _lib
 
 
-def slot_bytes(max_ts: int) -> int:
-    return (16 + 4 * max_ts + 7) // 8 * 8
+def slot_bytes(max_ts: int, record_bytes: int = 4) -> int:
+    return (16 + record_bytes * max_ts + 7) // 8 * 8
 
 
 @dataclass
 class Result:
     stats: np.ndarray      # STATS_DTYPE, one record per warp of the grid
-    trace: np.ndarray | None  # uint8, W * slot_bytes(max_ts)
+    trace: np.ndarray | None  # uint8, W * slot_bytes(max_ts, record_bytes)
     status: int
     race_flags: int
 
@@ -185,7 +188,7 @@ def run(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffers, *,
         cfg.n_warp_list = len(wl)
         cfg.warp_list = wl.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32))
     stats = np.zeros(W, dtype=STATS_DTYPE)
-    tr = np.zeros(W * slot_bytes(max_ts), dtype=np.uint8) if trace else None
+    tr = np.zeros(W * slot_bytes(max_ts, record_bytes(ptx, kernel)), dtype=np.uint8) if trace else None
     pbuf = ctypes.create_string_buffer(bytes(params), max(1, len(params)))
     status = ctypes.c_int32(0)
     race = ctypes.c_uint32(0)
@@ -222,6 +225,17 @@ def params_layout(ptx: str, kernel: str):
     if rc != 0:
         raise OracleError(rc, err.value.decode(errors="replace"))
     return [(offs[i], sizes[i]) for i in range(n.value)], total.value
+
+
+def record_bytes(ptx: str, kernel: str) -> int:
+    """Bytes per trace record of the kernel's slots: 4, 8 or 16."""
+    lib = _load()
+    b = ctypes.c_uint32(0)
+    err = ctypes.create_string_buffer(512)
+    rc = lib.orc_record_bytes(ptx.encode(), kernel.encode(), ctypes.byref(b), err, len(err))
+    if rc != 0:
+        raise OracleError(rc, err.value.decode(errors="replace"))
+    return b.value
 
 
 def events(ptx: str, kernel: str) -> list[int]:

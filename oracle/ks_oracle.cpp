@@ -166,6 +166,10 @@ struct Kernel {
   std::vector<Inst> code;
   std::vector<uint32_t> event_kind;   // 0 mark, 1 range_start, 2 range_end
   std::vector<std::string> event_name;
+  std::vector<uint32_t> event_payload;  // payload bytes of each event: 0, 4 or 8
+  // IKET NativeDump record size of the kernel's slots: 4 without payloads,
+  // 4 + 4 with 4-byte payloads, 16 with 8-byte ones (the largest event's)
+  uint32_t record_bytes = 4;
   std::vector<int> ipdom;             // per entry, n = virtual exit
   std::map<std::string, uint32_t> shared_sym;  // .shared array -> its shared address
   uint32_t shared_bytes = 0;
@@ -743,10 +747,21 @@ struct Parser {
     add_entry(in);
   }
 
+  // `@iket KIND NAME [%reg]`: an optional payload register (its value in the
+  // warp's lowest active lane goes into the record)
   void event(const std::string& stmt, int line) {
     std::vector<std::string> w;
     for (const std::string& t : split(stmt, ' ')) if (!trim(t).empty()) w.push_back(trim(t));
-    if (w.size() != 3) fail(ORC_ERR_PARSE, line, "bad //@iket pseudo-op");
+    if (w.size() != 3 && w.size() != 4) fail(ORC_ERR_PARSE, line, "bad //@iket pseudo-op");
+    int preg = -1;
+    uint32_t pbytes = 0;
+    if (w.size() == 4) {
+      if (w[3].empty() || w[3][0] != '%') fail(ORC_ERR_PARSE, line, "an //@iket payload must be a register");
+      preg = reg_of(w[3], line);
+      const int pw = K.regs[(size_t)preg].width;
+      if (pw != 32 && pw != 64) fail(ORC_ERR_PARSE, line, "an //@iket payload must be a 32- or 64-bit register");
+      pbytes = (uint32_t)pw / 8;
+    }
     uint32_t kind;
     if (w[1] == "mark") kind = 0;
     else if (w[1] == "range_start") kind = 1;
@@ -762,13 +777,18 @@ struct Parser {
       event_ids[key] = id;
       K.event_kind.push_back(kind);
       K.event_name.push_back(w[2]);
+      K.event_payload.push_back(pbytes);
     } else {
       id = it->second;
+      if (K.event_payload[(size_t)id] != pbytes)
+        fail(ORC_ERR_PARSE, line, "event " + w[2] + " used with two payload sizes");
     }
+    K.record_bytes = std::max(K.record_bytes, pbytes == 0 ? 4u : pbytes == 4 ? 8u : 16u);
     Inst in;
     in.line = line;
     in.k = K_EVENT;
     in.event = id;
+    if (preg >= 0) { in.a.k = Opnd::REG; in.a.reg = preg; }
     add_entry(in);
   }
 
@@ -1307,7 +1327,7 @@ struct WarpRun {
   uint64_t t_next = 0, t_last = 0, max_ready = 0, drain = 0;
   orc_warp_stats st;
   uint32_t n_events = 0, n_dropped = 0;
-  std::vector<uint32_t> records;
+  std::vector<std::pair<uint32_t, uint64_t>> records;  // (id << 24 | ts, payload)
 
   WarpRun(const Launch& L, uint32_t gw) : X(&L), gwarp(gw) {
     const Kernel& K = *X->K;
@@ -1342,8 +1362,13 @@ struct WarpRun {
 
       if (in.k == K_EVENT) {  // zero-cost pseudo-op
         if (n_events != 0xFFFFFFFFu) n_events++;
-        if (records.size() < cfg.max_ts_per_warp)
-          records.push_back(((uint32_t)(in.event & 0xFF) << 24) | (uint32_t)(t_next & 0xFFFFFF));
+        if (records.size() < cfg.max_ts_per_warp) {
+          uint64_t payload = 0;  // the lowest active lane's register
+          if (in.a.k == Opnd::REG)
+            for (int i = 0; i < 32; i++)
+              if ((top.mask >> i) & 1) { payload = lanes[(size_t)i].v[(size_t)in.a.reg]; break; }
+          records.push_back({((uint32_t)(in.event & 0xFF) << 24) | (uint32_t)(t_next & 0xFFFFFF), payload});
+        }
         else if (n_dropped < 0xFFFF)
           n_dropped++;
         top.pc = pc + 1;
@@ -1497,11 +1522,18 @@ struct WarpRun {
       uint8_t* slot = X->trace + (uint64_t)gwarp * X->slot_bytes;
       std::memset(slot, 0, X->slot_bytes);
       store_le(slot + 0, n_events, 4);
+      const uint32_t rb = X->K->record_bytes;
       slot[4] = 1;
-      slot[5] = 4;
+      slot[5] = (uint8_t)rb;
       store_le(slot + 6, n_dropped, 2);
       store_le(slot + 8, out.cycles, 8);
-      for (size_t i = 0; i < records.size(); i++) store_le(slot + 16 + 4 * i, records[i], 4);
+      // record layouts: [word] / [word | u32 payload] / [word | 0 | u64 payload]
+      for (size_t i = 0; i < records.size(); i++) {
+        uint8_t* r = slot + 16 + rb * i;
+        store_le(r, records[i].first, 4);
+        if (rb == 8) store_le(r + 4, records[i].second, 4);
+        if (rb == 16) store_le(r + 8, records[i].second, 8);
+      }
     }
   }
 };
@@ -1709,7 +1741,7 @@ int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
     X.cfg = cfg;
     X.stats = (uint8_t*)stats;
     X.trace = (uint8_t*)trace;
-    X.slot_bytes = ((16ull + 4ull * cfg->max_ts_per_warp) + 7) / 8 * 8;
+    X.slot_bytes = ((16ull + (uint64_t)K.record_bytes * cfg->max_ts_per_warp) + 7) / 8 * 8;
     const uint64_t W = (uint64_t)grid * X.warps_per_cta;
 
     std::vector<uint32_t> warps;
@@ -1826,6 +1858,17 @@ int orc_params(const char* ptx, const char* kernel, uint32_t* offsets, uint32_t*
       offsets[i] = K.params[i].off;
       sizes[i] = K.params[i].size;
     }
+    return ORC_OK;
+  } catch (const OracleError& e) {
+    copy_err(e.msg, err, errlen);
+    return e.code;
+  }
+}
+
+int orc_record_bytes(const char* ptx, const char* kernel, uint32_t* bytes, char* err, uint64_t errlen) {
+  try {
+    Kernel K = load(std::string(ptx), std::string(kernel));
+    *bytes = K.record_bytes;
     return ORC_OK;
   } catch (const OracleError& e) {
     copy_err(e.msg, err, errlen);

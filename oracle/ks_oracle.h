@@ -21,8 +21,9 @@
  * independently on each side):
  *   - per-warp statistics record, 96 bytes (orc_warp_stats below);
  *   - per-warp trace slot: 16-byte header {u32 n_events, u8 format=1,
- *     u8 bytes_per_event=4, u16 n_dropped, u64 warp_cycles} followed by
- *     max_ts 4-byte records, slot size rounded up to 8 bytes
+ *     u8 bytes_per_event, u16 n_dropped, u64 warp_cycles} followed by max_ts
+ *     records of bytes_per_event (4, 8 or 16: no payload, a 4-byte payload,
+ *     an 8-byte payload), slot size rounded up to 8 bytes
  *     (CuTeDSL IKET 浅析, §2 "buffer 是怎么定形的": warp_slot =
  *     align8(16B header + maxTsCntPerWarp × bytes_per_event)).
  */
@@ -133,6 +134,11 @@ int orc_ipdom(const char* ptx, const char* kernel, int32_t* out, uint32_t cap,
 int orc_params(const char* ptx, const char* kernel, uint32_t* offsets,
                uint32_t* sizes, uint32_t cap, uint32_t* n_params,
                uint32_t* param_bytes, char* err, uint64_t errlen);
+
+/* IKET record size of the kernel's trace slots (CuTeDSL IKET 浅析 §2, NativeDump:
+ * 4 bytes without payload, 4 + payload for payloads under 8 bytes, else 16):
+ * the largest record among its events. Slots are align8(16 + max_ts * bytes). */
+int orc_record_bytes(const char* ptx, const char* kernel, uint32_t* bytes, char* err, uint64_t errlen);
 
 /* Event table: kinds (0 mark, 1 range_start, 2 range_end) in id order. */
 int orc_events(const char* ptx, const char* kernel, uint32_t* kinds,
