@@ -214,7 +214,8 @@ def run_ours(args, world, rank, local):
         bufs = [(b.sim_base, torch.from_numpy(h.view(np.uint8)).to(dev)) for b, h in zip(w.buffers, host)]
         cfg = ks.Config(max_ts=w.max_ts)
         st = torch.empty(ks.stats_bytes(w.grid, w.block), dtype=torch.uint8, device=dev)
-        tr = torch.empty(ks.trace_bytes(w.grid, w.block, w.max_ts), dtype=torch.uint8, device=dev) if w.max_ts else None
+        tr = (torch.empty(ks.trace_bytes(w.grid, w.block, w.max_ts, mod.record_bytes(w.kernel)), dtype=torch.uint8,
+                          device=dev) if w.max_ts else None)
         jobs.append(dict(w=w, mod=mod, bufs=bufs, cfg=cfg, st=st, tr=tr))
 
     def step():

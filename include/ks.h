@@ -13,8 +13,10 @@
  *      ld/st request (KernelScope backend doc, simulator/engine.py —
  *      analyze_global_memory_access);
  *   4. per-warp trace slots in the IKET layout (CuTeDSL IKET 浅析, §2:
- *      16-byte header u32+u8+u8+u16+u64 then maxTsCntPerWarp 4-byte records,
- *      slot size rounded up to 8 bytes, one slot per warp, no atomics);
+ *      16-byte header u32+u8+u8+u16+u64 then maxTsCntPerWarp records of the
+ *      NativeDump size — 4 bytes, 4 + 4 with a 4-byte payload, 16 with an
+ *      8-byte payload — slot size rounded up to 8 bytes, one slot per warp,
+ *      no atomics);
  *   5. per-warp shared-memory requests and their bank-conflict degrees
  *      (KernelScope backend doc, simulator/engine.py —
  *      analyze_shared_memory_access: 32 banks of 4 bytes, bank =
@@ -34,7 +36,8 @@
  * thread count), ret/exit; registers .b32 .u32 .s32 .f32 .b64
  * .u64 .s64 .pred; special registers %tid %ntid %ctaid %nctaid (.x; .y/.z
  * read 0 or 1) and %laneid; trace pseudo-ops written as comments
- * `//@iket mark NAME`, `//@iket range_start NAME`, `//@iket range_end NAME`.
+ * `//@iket mark NAME`, `//@iket range_start NAME`, `//@iket range_end NAME`,
+ * each optionally followed by a 32- or 64-bit payload register.
  *
  * Semantics fixed where the pages are silent:
  *   - %tid.x is the thread's index in its CTA; lanes whose %tid.x >= block
@@ -56,6 +59,11 @@
  *     value lands. Stores from different warps to the same address, or a load
  *     of a word another warp stores, are undefined (warps run concurrently).
  *   - Registers start at zero, predicates false.
+ *   - Trace records: u32 (event_id << 24 | issue clock & 0xFFFFFF); with
+ *     payloads the kernel's records are 8 bytes (+ u32 payload) or 16 bytes
+ *     (+ u32 0 + u64 payload) for every event of the kernel (events without a
+ *     payload store 0); the payload is the register in the warp's lowest
+ *     active lane. The header's bytes_per_event holds the record size.
  *   - Shared memory and barriers (KernelScope backend doc, simulator/models.py
  *     Block: a shared array and a barrier per block; Warp.at_barrier): a
  *     kernel that declares .shared arrays or uses bar.sync runs CTA by CTA
@@ -216,6 +224,14 @@ int ks_kernel_ipdom(const ks_module* mod, const char* kernel, int32_t* out, uint
  * trace = W * align8(16 + 4 * max_ts_per_warp), stats = W * 96, where
  * W = grid * ceil(block / 32). */
 size_t ks_trace_bytes(uint32_t grid, uint32_t block, uint32_t max_ts_per_warp);
+/* The same for records of `record_bytes` (ks_kernel_record_bytes):
+ * W * align8(16 + record_bytes * max_ts_per_warp). ks_simulate requires
+ * trace_bytes >= this for the kernel's record size. */
+size_t ks_trace_bytes_records(uint32_t grid, uint32_t block, uint32_t max_ts_per_warp, uint32_t record_bytes);
+/* Trace record size of a kernel's slots: 4 (no payload events), 8 or 16. */
+int ks_kernel_record_bytes(const ks_module* mod, const char* kernel, uint32_t* bytes);
+/* Payload size of event `id`: 0, 4 or 8 bytes. */
+int ks_kernel_event_payload(const ks_module* mod, const char* kernel, uint32_t id, uint32_t* bytes);
 size_t ks_stats_bytes(uint32_t grid, uint32_t block);
 
 /* Enqueues the interpretation of `kernel` over grid x block simulated

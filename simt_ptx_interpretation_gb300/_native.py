@@ -49,6 +49,10 @@ EXPORTS = {
                                        ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
     "ks_trace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]),
     "ks_stats_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32]),
+    "ks_trace_bytes_records": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]),
+    "ks_kernel_record_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "ks_kernel_event_payload": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32,
+                                               ctypes.POINTER(ctypes.c_uint32)]),
     "ks_simulate": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
                                    ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(KsBuffer), ctypes.c_uint32,
                                    ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,

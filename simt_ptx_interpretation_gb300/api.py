@@ -120,6 +120,18 @@ class Module:
             out.append((name.value.decode(), off.value, size.value))
         return out
 
+    def record_bytes(self, kernel: str) -> int:
+        """Trace record size of the kernel's slots: 4, 8 or 16 bytes."""
+        b = ctypes.c_uint32()
+        _check(_native.lib().ks_kernel_record_bytes(self._h, kernel.encode(), ctypes.byref(b)))
+        return b.value
+
+    def event_payload(self, kernel: str, event_id: int) -> int:
+        """Payload bytes of an event: 0, 4 or 8."""
+        b = ctypes.c_uint32()
+        _check(_native.lib().ks_kernel_event_payload(self._h, kernel.encode(), event_id, ctypes.byref(b)))
+        return b.value
+
     def events(self, kernel: str) -> list[tuple[int, str]]:
         out = []
         for i in range(self.info(kernel)["n_events"]):
@@ -140,8 +152,10 @@ def stats_bytes(grid: int, block: int) -> int:
     return int(_native.lib().ks_stats_bytes(grid, block))
 
 
-def trace_bytes(grid: int, block: int, max_ts: int) -> int:
-    return int(_native.lib().ks_trace_bytes(grid, block, max_ts))
+def trace_bytes(grid: int, block: int, max_ts: int, record_bytes: int = 4) -> int:
+    if record_bytes == 4:
+        return int(_native.lib().ks_trace_bytes(grid, block, max_ts))
+    return int(_native.lib().ks_trace_bytes_records(grid, block, max_ts, record_bytes))
 
 
 def _stream_handle(stream) -> int | None:
@@ -219,7 +233,8 @@ def run(module: Module, kernel: str, grid: int, block: int, params: bytes, buffe
     config = config or Config()
     dev = buffers[0][1].device if buffers else torch.device("cuda")
     st = torch.empty(stats_bytes(grid, block), dtype=torch.uint8, device=dev)
-    tr = torch.empty(trace_bytes(grid, block, config.max_ts), dtype=torch.uint8, device=dev) if trace else None
+    tr = (torch.empty(trace_bytes(grid, block, config.max_ts, module.record_bytes(kernel)), dtype=torch.uint8, device=dev)
+          if trace else None)
     simulate(module, kernel, grid, block, params, buffers, st, tr, config, stream)
     n = grid * ((block + 31) // 32)
     return Run(st, tr, read_stats(st, n, stream), list(buffers))

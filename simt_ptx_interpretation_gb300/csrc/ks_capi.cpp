@@ -170,6 +170,28 @@ size_t ks_trace_bytes(uint32_t grid, uint32_t block, uint32_t max_ts_per_warp) {
   return (size_t)(warps_of(grid, block) * slot);
 }
 
+size_t ks_trace_bytes_records(uint32_t grid, uint32_t block, uint32_t max_ts_per_warp, uint32_t record_bytes) {
+  const uint64_t slot = (16ull + (uint64_t)record_bytes * max_ts_per_warp + 7ull) / 8ull * 8ull;
+  return (size_t)(warps_of(grid, block) * slot);
+}
+
+int ks_kernel_record_bytes(const ks_module* mod, const char* kernel, uint32_t* bytes) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  if (!bytes) return KS_ERR_ARG;
+  *bytes = k->record_bytes;
+  return KS_OK;
+}
+
+int ks_kernel_event_payload(const ks_module* mod, const char* kernel, uint32_t id, uint32_t* bytes) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  if (id >= k->events.size()) return KS_ERR_NOT_FOUND;
+  if (!bytes) return KS_ERR_ARG;
+  *bytes = k->events[id].payload_bytes;
+  return KS_OK;
+}
+
 size_t ks_stats_bytes(uint32_t grid, uint32_t block) {
   return (size_t)(warps_of(grid, block) * sizeof(ks_warp_stats));
 }
@@ -206,7 +228,7 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   if (cfg.max_ts_per_warp > (1u << 24)) return KS_ERR_ARG;
   for (uint32_t i = 0; i < KS_NUM_LAT_CLASSES; i++)
     if (cfg.lat[i] > ks::KS_MAX_LATENCY) return KS_ERR_ARG;
-  const uint64_t slot = (16ull + 4ull * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
+  const uint64_t slot = (16ull + (uint64_t)k->record_bytes * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
   if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
   // shared memory / bar.sync: every warp of a CTA resident on one real CTA
   if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
@@ -255,6 +277,7 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   }
   std::memcpy(L.lat, cfg.lat, sizeof L.lat);
   L.max_ts = cfg.max_ts_per_warp;
+  L.rec_bytes = k->record_bytes;
   L.stack_depth = cfg.simt_stack_depth;
   L.step_limit = cfg.step_limit;
   L.inject_warp = cfg.inject_warp;

@@ -196,7 +196,7 @@ struct RegDecl {
 struct Stmt {
   int line;
   bool pseudo = false;
-  std::string pseudo_kind, pseudo_name;
+  std::string pseudo_kind, pseudo_name, pseudo_payload;  // payload: a register, or empty
   std::string guard;  // predicate register name, empty if none
   bool guard_neg = false;
   std::string opcode;                 // base opcode
@@ -310,9 +310,10 @@ class Parser {
           if (std::isspace((unsigned char)ch)) { if (!word.empty()) w.push_back(word); word.clear(); }
           else word += ch;
         }
-        if (w.size() != 2) fail(KS_ERR_PARSE, t.line, "bad //@iket pseudo-op");
+        if (w.size() != 2 && w.size() != 3) fail(KS_ERR_PARSE, t.line, "bad //@iket pseudo-op");
         s.pseudo_kind = w[0];
         s.pseudo_name = w[1];
+        if (w.size() == 3) s.pseudo_payload = w[2];
         attach(k, pending, std::move(s));
         pos_++;
         continue;
@@ -560,6 +561,17 @@ class Decoder {
     else if (s.pseudo_kind == "range_end") kind = 2;
     else fail(KS_ERR_PARSE, s.line, "unknown //@iket kind " + s.pseudo_kind);
     if (!is_ident(s.pseudo_name)) fail(KS_ERR_PARSE, s.line, "bad event name");
+    // optional payload register (IKET payload events): its value in the
+    // warp's lowest active lane goes into the record
+    uint32_t pbytes = 0;
+    uint8_t preg = 0;
+    if (!s.pseudo_payload.empty()) {
+      if (s.pseudo_payload[0] != '%') fail(KS_ERR_PARSE, s.line, "an //@iket payload must be a register");
+      RegDecl& r = reg(s.pseudo_payload, s.line);
+      if (r.width != 32 && r.width != 64) fail(KS_ERR_PARSE, s.line, "an //@iket payload must be a 32- or 64-bit register");
+      pbytes = r.width / 8;
+      preg = (uint8_t)r.index;
+    }
     auto key = std::make_pair(kind, s.pseudo_name);
     auto it = event_ids_.find(key);
     uint32_t id;
@@ -567,13 +579,19 @@ class Decoder {
       id = (uint32_t)K.events.size();
       if (id >= 256) fail(KS_ERR_UNSUPPORTED, s.line, "more than 256 events");
       event_ids_[key] = id;
-      K.events.push_back({s.pseudo_name, kind});
+      K.events.push_back({s.pseudo_name, kind, pbytes});
     } else {
       id = it->second;
+      if (K.events[id].payload_bytes != pbytes)
+        fail(KS_ERR_PARSE, s.line, "event " + s.pseudo_name + " used with two payload sizes");
     }
+    // NativeDump record sizes: 4 without a payload, 4 + 4, or 16
+    K.record_bytes = std::max(K.record_bytes, pbytes == 0 ? 4u : pbytes == 4 ? 8u : 16u);
     KsInsn in = blank();
     in.op = OP_EVENT;
     in.event = (uint16_t)id;
+    in.a = preg;
+    in.flags = (uint8_t)pbytes;
     return in;
   }
 
@@ -1095,7 +1113,8 @@ class Decoder {
         const unsigned dw = op == OP_LDS32 || op == OP_STS32 ? 32u : 64u;
         return op == OP_LDS32 || op == OP_LDS64 ? w(aw, 0, 0, dw) : w(aw, dw, 0, 0);
       }
-      default: return 0;  // events, control, predicate logic, bar.sync
+      case OP_EVENT: return w(in.flags * 8u, 0, 0, 0);  // the payload register, if any
+      default: return 0;  // control, predicate logic, bar.sync
     }
   }
 
@@ -1280,7 +1299,7 @@ class Decoder {
         if (in.op == OP_BRA || in.op == OP_RET) o.wlat |= DEV_IS_CTRL;
       }
       switch (in.op) {
-        case OP_EVENT: o.aux = in.event; break;
+        case OP_EVENT: o.aux = in.event | ((uint32_t)in.flags << 8); break;
         case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64:
         case OP_LDP32: case OP_LDP64: case OP_MOVSP:
           o.aux = (uint32_t)in.imm;

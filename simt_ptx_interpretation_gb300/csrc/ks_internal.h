@@ -170,7 +170,8 @@ struct KsParam {
 
 struct KsEvent {
   std::string name;
-  uint32_t kind;  // 0 mark, 1 range_start, 2 range_end
+  uint32_t kind;           // 0 mark, 1 range_start, 2 range_end
+  uint32_t payload_bytes;  // 0, 4 or 8
 };
 
 struct KsKernel {
@@ -184,6 +185,7 @@ struct KsKernel {
   uint32_t n_preds = 0;
   std::vector<int32_t> ipdom;
   uint32_t shared_bytes = 0;  // simulated shared memory per CTA (.shared arrays)
+  uint32_t record_bytes = 4;  // trace record size: 4, 8 (4-byte payloads) or 16 (8-byte payloads)
   bool has_bar = false;       // uses bar.sync
   // a CTA's warps share state: they run together, one real CTA per simulated CTA
   bool cta_mode() const { return shared_bytes > 0 || has_bar; }
@@ -220,6 +222,7 @@ struct KsLaunch {
   uint32_t n_warps;           // grid * wpc
   uint32_t lat[KS_NUM_LAT_CLASSES];
   uint32_t max_ts;
+  uint32_t rec_bytes;  // trace record size (4, 8 or 16)
   uint32_t stack_depth;
   uint64_t step_limit;
   int64_t inject_warp;

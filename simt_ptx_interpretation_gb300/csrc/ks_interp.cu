@@ -494,9 +494,21 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
         if (op == OP_EVENT) {  // trace record (a7), zero cost
           if (n_events != 0xFFFFFFFFu) n_events++;
           if (n_rec < L.max_ts) {
-            if (slot && lane == 0)
-              *reinterpret_cast<uint32_t*>(slot + 16 + 4 * n_rec) =
-                  ((aux & 0xFFu) << 24) | (((uint32_t)epoch + t_next) & 0xFFFFFFu);
+            // record: [id << 24 | ts] (4 B), + u32 payload (8 B), or + 0 + u64
+            // payload (16 B); the payload is the lowest active lane's register
+            const uint32_t src = (uint32_t)__ffs(mask) - 1u;
+            const uint32_t plo = __shfl_sync(FULL, a0, src);
+            const uint32_t phi = __shfl_sync(FULL, ((aux >> 8) & 0xFFu) == 8u ? SM32(lb + A + ROW_BYTES) : 0u, src);
+            if (slot && lane == 0) {
+              uint8_t* r = slot + 16u + L.rec_bytes * n_rec;
+              *reinterpret_cast<uint32_t*>(r) = ((aux & 0xFFu) << 24) | (((uint32_t)epoch + t_next) & 0xFFFFFFu);
+              if (L.rec_bytes == 8u) {
+                *reinterpret_cast<uint32_t*>(r + 4) = plo;
+              } else if (L.rec_bytes == 16u) {
+                *reinterpret_cast<uint32_t*>(r + 4) = 0u;
+                *reinterpret_cast<uint64_t*>(r + 8) = (uint64_t)plo | ((uint64_t)phi << 32);
+              }
+            }
             n_rec++;
           } else if (n_dropped < 0xFFFFu) {
             n_dropped++;
@@ -961,11 +973,11 @@ __global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant
       const uint32_t words = (uint32_t)(L.slot_bytes / 4);
       if (lane == 0) {
         sw[0] = n_events;
-        sw[1] = 1u | (4u << 8) | (n_dropped << 16);
+        sw[1] = 1u | (L.rec_bytes << 8) | (n_dropped << 16);
         sw[2] = (uint32_t)cycles;
         sw[3] = (uint32_t)(cycles >> 32);
       }
-      for (uint32_t i = 4 + n_rec + lane; i < words; i += 32) sw[i] = 0u;
+      for (uint32_t i = 4 + n_rec * (L.rec_bytes / 4u) + lane; i < words; i += 32) sw[i] = 0u;
     }
     __syncwarp();
   }

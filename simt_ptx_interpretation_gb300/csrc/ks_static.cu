@@ -77,7 +77,7 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   if (cfg.max_ts_per_warp > (1u << 24)) return KS_ERR_ARG;
   for (uint32_t i = 0; i < KS_NUM_LAT_CLASSES; i++)
     if (cfg.lat[i] > ks::KS_MAX_LATENCY) return KS_ERR_ARG;
-  const uint64_t slot = (16ull + 4ull * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
+  const uint64_t slot = (16ull + (uint64_t)k->record_bytes * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
   if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
   // shared memory / bar.sync: every warp of a CTA resident on one real CTA
   if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
@@ -113,6 +113,7 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   }
   std::memcpy(L.lat, cfg.lat, sizeof L.lat);
   L.max_ts = cfg.max_ts_per_warp;
+  L.rec_bytes = k->record_bytes;
   L.stack_depth = cfg.simt_stack_depth;
   L.step_limit = cfg.step_limit;
   L.inject_warp = cfg.inject_warp;

@@ -37,8 +37,8 @@ def oracle_run(w: wl.Workload, warps=None, config: ks.Config | None = None, trac
     return r, [b.data.view(np.uint8) for b in bufs]
 
 
-def slot_bytes(max_ts: int) -> int:
-    return (16 + 4 * max_ts + 7) // 8 * 8
+def slot_bytes(max_ts: int, record_bytes: int = 4) -> int:
+    return (16 + record_bytes * max_ts + 7) // 8 * 8
 
 
 def assert_parity(w: wl.Workload, cfg: ks.Config | None = None, warps=None, out_words=None):
@@ -52,7 +52,7 @@ def assert_parity(w: wl.Workload, cfg: ks.Config | None = None, warps=None, out_
     os_ = o.stats[sel].view(np.uint8).reshape(len(sel), 96)
     bad = np.nonzero((gs != os_).any(axis=1))[0]
     assert len(bad) == 0, f"stats differ at warps {sel[bad[:5]]}: gpu {g.stats[sel[bad[0]]]} oracle {o.stats[sel[bad[0]]]}"
-    sb = slot_bytes(cfg.max_ts)
+    sb = slot_bytes(cfg.max_ts, oracle.record_bytes(w.ptx, w.kernel))
     gt = g.trace.reshape(w.warps, sb)[sel]
     ot = o.trace.reshape(w.warps, sb)[sel]
     badt = np.nonzero((gt != ot).any(axis=1))[0]

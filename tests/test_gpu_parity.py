@@ -222,6 +222,31 @@ def test_access_patterns_match_the_oracle(pattern, guard, size):
     _parity.assert_parity(access_workload(pattern, guard, size))
 
 
+# --------------------------------------------------------- payload events ----
+
+def test_payload_events_match_the_oracle():
+    from tests import test_oracle_events as tev
+    cases = [(tev.PAYLOADS, 64, 4), (tev.PAYLOADS, 40, 1), (tev.PAYLOADS, 96, 0),
+             ("    mov.u32 %r1, %tid.x;\n    setp.lt.u32 %p1, %r1, 8;\n    @%p1 ret;\n    //@iket mark m %r1\n    ret;", 64, 2),
+             ("    mov.u32 %r1, 7;\n    mov.f32 %f1, 0f3FC00000;\n    //@iket mark a\n    //@iket mark b %r1\n"
+              "    //@iket range_end c %f1\n    ret;", 96, 3)]
+    for body, block, max_ts in cases:
+        w = wl.Workload("ev", tev.kernel(body), "ev", 3, block, b"", [], max_ts=max_ts)
+        _parity.assert_parity(w)
+
+
+@pytest.mark.parametrize("k", [2, 32])
+def test_payload_marks_in_a_divergent_loop(k):
+    """A payload mark on the loop counter inside the divergent workload's loop
+    body: records of changing masks and values, over every warp."""
+    w = wl.divergent(k, n=1 << 12, max_ts=16)
+    ptx = w.ptx.replace("DV_HEAD:\n", "DV_HEAD:\n    //@iket mark it %r10\n", 1)
+    assert ptx != w.ptx
+    w2 = wl.Workload(w.name + "_payload", ptx, w.kernel, w.grid, w.block, w.params, w.buffers, max_ts=16)
+    assert ks.Module(ptx).record_bytes(w.kernel) == 8
+    _parity.assert_parity(w2)
+
+
 # ------------------------------------------------------------- statuses ----
 
 def test_step_limits_around_compare_and_branch_pairs():

@@ -14,6 +14,7 @@ from simt_ptx_interpretation_gb300 import _build, _native
 from simt_ptx_interpretation_gb300 import api as ks
 from simt_ptx_interpretation_gb300 import workloads as wl
 from tests import test_oracle_control as toc
+from tests import test_oracle_events as tev
 from tests import test_oracle_shared as tsh
 from tests._kernels import op_kernel
 
@@ -63,6 +64,11 @@ def corpus():
     progs += [("probe", tsh.bank_probe_ptx(4)), ("probe", tsh.bank_probe_ptx(8)), ("bar2", tsh.barrier_ptx(3))]
     for body, _ in tsh.SHARED_BAD:
         progs.append(("bad", tsh.bad_shared_kernel(body)))
+    progs.append(("ev", tev.kernel(tev.PAYLOADS)))
+    for body in ("    //@iket mark a %r1\n    ret;", "    //@iket mark a %rd1\n    ret;", "    //@iket mark a %f1\n    ret;",
+                 "    //@iket mark a\n    //@iket mark b %r1\n    ret;", "    //@iket mark a %r1\n    //@iket mark a %rd1\n    ret;",
+                 "    //@iket mark a %p1\n    ret;", "    //@iket mark a 5\n    ret;", "    //@iket mark a %r1 %r2\n    ret;"):
+        progs.append(("ev", tev.kernel(body)))
     for op, srcs, dst in [("add.u32", "uu", "u"), ("fma.rn.f32", "fff", "f"), ("setp.lt.f32", "ff", "p"),
                           ("selp.b64", "wwp", "w"), ("cvt.rzi.s64.f32", "f", "w"), ("shr.s64", "wu", "w")]:
         progs.append(("k_op", op_kernel("k_op", op, srcs, dst)))
@@ -85,6 +91,7 @@ def test_decoder_accepts_what_the_oracle_accepts(idx):
     assert [(o, s) for _, o, s in m.params(kernel)] == layout
     assert m.info(kernel)["param_bytes"] == total
     assert [k for k, _ in m.events(kernel)] == oracle.events(ptx, kernel)
+    assert m.record_bytes(kernel) == oracle.record_bytes(ptx, kernel)
     assert m.ipdom(kernel) == oracle.ipdom(ptx, kernel)
 
 
