@@ -290,6 +290,46 @@ int ks_simulate_static(const ks_module* mod, const char* kernel, uint32_t grid, 
  * serialised inside the library. */
 int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_totals* out);
 
+/* ---- host post-pass: occupancy (KernelScope backend doc,
+ * occupancy/calculator.py — calculate_occupancy) ----------------------------
+ * Resident warps per SM from three limits, as the page computes them:
+ * registers (threads' registers per warp rounded up to 256, the SM's file
+ * divided by that), shared memory (per-block bytes rounded up to 256, blocks
+ * that fit times warps per block) and block size (min(max threads / block,
+ * max blocks) times warps per block), capped at the SM's warp limit. A limit
+ * whose input is 0 does not bind. The limiter is the first of registers,
+ * shared memory, block size whose warps equal the result. */
+typedef struct {
+  uint32_t max_threads_per_sm;
+  uint32_t max_warps_per_sm;
+  uint32_t max_blocks_per_sm;
+  uint32_t registers_per_sm;
+  uint32_t shared_memory_per_sm;
+} ks_gpu_limits;
+
+#define KS_LIMITER_REGISTERS 0
+#define KS_LIMITER_SHARED_MEMORY 1
+#define KS_LIMITER_BLOCK_SIZE 2
+
+typedef struct {
+  uint32_t active_warps_per_sm;
+  uint32_t max_warps_per_sm;
+  uint32_t warps_by_registers;
+  uint32_t warps_by_shared_memory;
+  uint32_t warps_by_block_size;
+  int32_t limiter;           /* KS_LIMITER_* */
+  double occupancy_percent;  /* 100 * active / max warps */
+} ks_occupancy_result;
+
+/* Limits of an architecture by name: "sm_75", "sm_80", "sm_86", "sm_89",
+ * "sm_90" (the page's table; fields the page elides take the public CUDA
+ * values), "sm_100", "sm_103". KS_ERR_NOT_FOUND for other names. */
+int ks_gpu_limits_of(const char* arch, ks_gpu_limits* out);
+/* KS_ERR_ARG for a null pointer, threads_per_block of 0 or above the SM's
+ * threads, or a limits record with zero warps. */
+int ks_occupancy(const ks_gpu_limits* limits, uint32_t threads_per_block, uint32_t registers_per_thread,
+                 uint32_t shared_memory_per_block, ks_occupancy_result* out);
+
 /* Text for any KS_* return code or status. */
 const char* ks_status_string(int code);
 

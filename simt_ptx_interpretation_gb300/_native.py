@@ -34,6 +34,19 @@ class KsTotals(ctypes.Structure):
         ("sh_req", ctypes.c_uint64), ("sh_wavefronts", ctypes.c_uint64)]
 
 
+class KsGpuLimits(ctypes.Structure):
+    _fields_ = [("max_threads_per_sm", ctypes.c_uint32), ("max_warps_per_sm", ctypes.c_uint32),
+                ("max_blocks_per_sm", ctypes.c_uint32), ("registers_per_sm", ctypes.c_uint32),
+                ("shared_memory_per_sm", ctypes.c_uint32)]
+
+
+class KsOccupancy(ctypes.Structure):
+    _fields_ = [("active_warps_per_sm", ctypes.c_uint32), ("max_warps_per_sm", ctypes.c_uint32),
+                ("warps_by_registers", ctypes.c_uint32), ("warps_by_shared_memory", ctypes.c_uint32),
+                ("warps_by_block_size", ctypes.c_uint32), ("limiter", ctypes.c_int32),
+                ("occupancy_percent", ctypes.c_double)]
+
+
 EXPORTS = {
     "ks_config_default": (None, [ctypes.POINTER(KsConfig)]),
     "ks_load_module": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p),
@@ -49,6 +62,9 @@ EXPORTS = {
                                        ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
     "ks_trace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]),
     "ks_stats_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32]),
+    "ks_gpu_limits_of": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(KsGpuLimits)]),
+    "ks_occupancy": (ctypes.c_int, [ctypes.POINTER(KsGpuLimits), ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                    ctypes.POINTER(KsOccupancy)]),
     "ks_trace_bytes_records": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]),
     "ks_kernel_record_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_uint32)]),
     "ks_kernel_event_payload": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32,

@@ -152,6 +152,27 @@ def stats_bytes(grid: int, block: int) -> int:
     return int(_native.lib().ks_stats_bytes(grid, block))
 
 
+LIMITERS = ("registers", "shared_memory", "block_size")
+
+
+def gpu_limits(arch: str) -> dict:
+    """Per-SM limits of an architecture (ks_gpu_limits_of)."""
+    g = _native.KsGpuLimits()
+    _check(_native.lib().ks_gpu_limits_of(arch.encode(), ctypes.byref(g)))
+    return {f: getattr(g, f) for f, _ in _native.KsGpuLimits._fields_}
+
+
+def occupancy(limits: dict, threads_per_block: int, registers_per_thread: int, shared_memory_per_block: int = 0) -> dict:
+    """Resident warps per SM and the limiting resource (ks_occupancy)."""
+    g = _native.KsGpuLimits(**limits)
+    r = _native.KsOccupancy()
+    _check(_native.lib().ks_occupancy(ctypes.byref(g), threads_per_block, registers_per_thread,
+                                      shared_memory_per_block, ctypes.byref(r)))
+    out = {f: getattr(r, f) for f, _ in _native.KsOccupancy._fields_}
+    out["limiter"] = LIMITERS[out["limiter"]]
+    return out
+
+
 def trace_bytes(grid: int, block: int, max_ts: int, record_bytes: int = 4) -> int:
     if record_bytes == 4:
         return int(_native.lib().ks_trace_bytes(grid, block, max_ts))
