@@ -330,6 +330,25 @@ int ks_gpu_limits_of(const char* arch, ks_gpu_limits* out);
 int ks_occupancy(const ks_gpu_limits* limits, uint32_t threads_per_block, uint32_t registers_per_thread,
                  uint32_t shared_memory_per_block, ks_occupancy_result* out);
 
+/* ---- host post-pass: trace export (CuTeDSL IKET 浅析 §3, "postprocess →
+ * Perfetto trace") --------------------------------------------------------
+ * Converts a host copy of a launch's trace slots into Chrome trace-event JSON,
+ * which Perfetto opens: one process per CTA ("CTA c"), one thread per warp
+ * ("warp w", w counted in its CTA), a complete event "warp" from 0 to the
+ * slot's cycle count, and per record a "B" (range_start), "E" (range_end) or
+ * thread-scoped instant "i" (mark) named after the event, with args {"id"}
+ * and, for payload events, {"payload": raw bits as an unsigned integer}.
+ * Record stamps hold the low 24 bits of the cycle; they are unwrapped in
+ * record order (a warp's stamps never decrease, and consecutive stamps are
+ * taken to be less than 2^24 cycles apart). ts and dur are cycles /
+ * cycles_per_us (microseconds). grid, block and max_ts are the launch's.
+ * *needed gets the length without the NUL; KS_ERR_ARG when out is NULL or
+ * cap < *needed + 1 (call again with a larger buffer), when trace_bytes is
+ * smaller than the launch's slots, or when a record names an unknown event. */
+int ks_trace_to_json(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block, uint32_t max_ts,
+                     const void* trace_host, size_t trace_bytes, double cycles_per_us, char* out, size_t cap,
+                     size_t* needed);
+
 /* Text for any KS_* return code or status. */
 const char* ks_status_string(int code);
 

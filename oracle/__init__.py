@@ -126,6 +126,10 @@ def _load():
                                    ctypes.POINTER(ctypes.c_uint32), ctypes.c_uint32,
                                    ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32),
                                    ctypes.c_char_p, ctypes.c_uint64]
+        lib.orc_event_info.restype = ctypes.c_int
+        lib.orc_event_info.argtypes = [ctypes.c_char_p, ctypes.c_char_p, ctypes.c_uint32,
+                                       ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32),
+                                       ctypes.c_char_p, ctypes.c_uint64, ctypes.c_char_p, ctypes.c_uint64]
         lib.orc_record_bytes.restype = ctypes.c_int
         lib.orc_record_bytes.argtypes = [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_uint32),
                                          ctypes.c_char_p, ctypes.c_uint64]
@@ -225,6 +229,22 @@ def params_layout(ptx: str, kernel: str):
     if rc != 0:
         raise OracleError(rc, err.value.decode(errors="replace"))
     return [(offs[i], sizes[i]) for i in range(n.value)], total.value
+
+
+def event_info(ptx: str, kernel: str) -> list[tuple[int, int, str]]:
+    """(kind, payload bytes, name) of every event in id order."""
+    lib = _load()
+    out = []
+    for i in range(len(events(ptx, kernel))):
+        kind, pb = ctypes.c_uint32(0), ctypes.c_uint32(0)
+        name = ctypes.create_string_buffer(256)
+        err = ctypes.create_string_buffer(512)
+        rc = lib.orc_event_info(ptx.encode(), kernel.encode(), i, ctypes.byref(kind), ctypes.byref(pb), name,
+                                len(name), err, len(err))
+        if rc != 0:
+            raise OracleError(rc, err.value.decode(errors="replace"))
+        out.append((kind.value, pb.value, name.value.decode()))
+    return out
 
 
 def record_bytes(ptx: str, kernel: str) -> int:

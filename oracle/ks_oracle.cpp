@@ -1865,6 +1865,21 @@ int orc_params(const char* ptx, const char* kernel, uint32_t* offsets, uint32_t*
   }
 }
 
+int orc_event_info(const char* ptx, const char* kernel, uint32_t id, uint32_t* kind, uint32_t* payload_bytes,
+                   char* name, uint64_t cap, char* err, uint64_t errlen) {
+  try {
+    Kernel K = load(std::string(ptx), std::string(kernel));
+    if (id >= K.event_kind.size()) throw OracleError{ORC_ERR_NOT_FOUND, "no such event"};
+    *kind = K.event_kind[id];
+    *payload_bytes = K.event_payload[id];
+    copy_err(K.event_name[id], name, cap);
+    return ORC_OK;
+  } catch (const OracleError& e) {
+    copy_err(e.msg, err, errlen);
+    return e.code;
+  }
+}
+
 int orc_record_bytes(const char* ptx, const char* kernel, uint32_t* bytes, char* err, uint64_t errlen) {
   try {
     Kernel K = load(std::string(ptx), std::string(kernel));

@@ -140,6 +140,11 @@ int orc_params(const char* ptx, const char* kernel, uint32_t* offsets,
  * the largest record among its events. Slots are align8(16 + max_ts * bytes). */
 int orc_record_bytes(const char* ptx, const char* kernel, uint32_t* bytes, char* err, uint64_t errlen);
 
+/* Event `id`: kind (0 mark, 1 range_start, 2 range_end), payload bytes (0, 4
+ * or 8) and name (NUL-terminated, truncated to cap). */
+int orc_event_info(const char* ptx, const char* kernel, uint32_t id, uint32_t* kind, uint32_t* payload_bytes,
+                   char* name, uint64_t cap, char* err, uint64_t errlen);
+
 /* Event table: kinds (0 mark, 1 range_start, 2 range_end) in id order. */
 int orc_events(const char* ptx, const char* kernel, uint32_t* kinds,
                uint32_t cap, uint32_t* n_events, char* err, uint64_t errlen);

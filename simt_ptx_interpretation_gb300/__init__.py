@@ -9,7 +9,8 @@ export traces. The C ABI
 is include/ks.h (libks.so); this package marshals arguments to it.
 """
 from .api import (DEFAULT_LAT, STATS_DTYPE, Config, KsError, Module, Run, Totals, gpu_limits, occupancy, read_stats,
-                  run, simulate, simulate_static, stats_array, stats_bytes, trace_bytes)
+                  run, simulate, simulate_static, stats_array, stats_bytes, trace_bytes, trace_to_json)
 
 __all__ = ["DEFAULT_LAT", "STATS_DTYPE", "Config", "KsError", "Module", "Run", "Totals", "gpu_limits", "occupancy",
-           "read_stats", "run", "simulate", "simulate_static", "stats_array", "stats_bytes", "trace_bytes"]
+           "read_stats", "run", "simulate", "simulate_static", "stats_array", "stats_bytes", "trace_bytes",
+           "trace_to_json"]

@@ -62,6 +62,9 @@ EXPORTS = {
                                        ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
     "ks_trace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]),
     "ks_stats_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32]),
+    "ks_trace_to_json": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
+                                        ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_double,
+                                        ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_size_t)]),
     "ks_gpu_limits_of": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(KsGpuLimits)]),
     "ks_occupancy": (ctypes.c_int, [ctypes.POINTER(KsGpuLimits), ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                     ctypes.POINTER(KsOccupancy)]),

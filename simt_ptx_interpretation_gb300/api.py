@@ -152,6 +152,22 @@ def stats_bytes(grid: int, block: int) -> int:
     return int(_native.lib().ks_stats_bytes(grid, block))
 
 
+def trace_to_json(module: "Module", kernel: str, grid: int, block: int, max_ts: int, trace, cycles_per_us: float) -> str:
+    """Chrome trace-event JSON (Perfetto) of a launch's trace slots
+    (ks_trace_to_json); `trace` is a host numpy uint8 array or a tensor."""
+    data = trace.cpu().numpy() if isinstance(trace, torch.Tensor) else np.ascontiguousarray(trace)
+    need = ctypes.c_size_t(0)
+    L = _native.lib()
+    rc = L.ks_trace_to_json(module._h, kernel.encode(), grid, block, max_ts, data.ctypes.data, data.nbytes,
+                            cycles_per_us, None, 0, ctypes.byref(need))
+    if rc not in (0, -3) or need.value == 0:
+        _check(rc)
+    buf = ctypes.create_string_buffer(need.value + 1)
+    _check(L.ks_trace_to_json(module._h, kernel.encode(), grid, block, max_ts, data.ctypes.data, data.nbytes,
+                              cycles_per_us, buf, len(buf), ctypes.byref(need)))
+    return buf.value.decode()
+
+
 LIMITERS = ("registers", "shared_memory", "block_size")
 
 

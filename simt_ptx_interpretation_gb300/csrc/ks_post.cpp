@@ -1,6 +1,7 @@
 // ks_post.cpp — host post-passes of the C ABI: the occupancy calculator
 // (KernelScope backend doc, occupancy/calculator.py) and the trace export.
 #include <algorithm>
+#include <cstdio>
 #include <cstring>
 #include <string>
 
@@ -69,6 +70,76 @@ int ks_occupancy(const ks_gpu_limits* g, uint32_t threads_per_block, uint32_t re
                  : active == by_smem ? KS_LIMITER_SHARED_MEMORY
                                      : KS_LIMITER_BLOCK_SIZE;
   out->occupancy_percent = (double)active / (double)g->max_warps_per_sm * 100.0;  // the page's order
+  return KS_OK;
+}
+
+int ks_trace_to_json(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block, uint32_t max_ts,
+                     const void* trace_host, size_t trace_bytes, double cycles_per_us, char* out, size_t cap,
+                     size_t* needed) {
+  if (!mod || !kernel) return KS_ERR_ARG;
+  const ks::KsKernel* k = ks::module_kernel(mod, kernel);
+  if (!k) return KS_ERR_NOT_FOUND;
+  if (!trace_host || !needed || grid == 0 || block == 0 || !(cycles_per_us > 0.0)) return KS_ERR_ARG;
+  const uint64_t rb = k->record_bytes;
+  const uint64_t slot = (16ull + rb * max_ts + 7ull) / 8ull * 8ull;
+  const uint64_t wpc = (block + 31u) / 32u;
+  if ((uint64_t)trace_bytes < (uint64_t)grid * wpc * slot) return KS_ERR_ARG;
+  const uint8_t* t = static_cast<const uint8_t*>(trace_host);
+  auto u32 = [&](uint64_t off) { uint32_t v; std::memcpy(&v, t + off, 4); return v; };
+  auto u64 = [&](uint64_t off) { uint64_t v; std::memcpy(&v, t + off, 8); return v; };
+  std::string js;
+  js.reserve(256 + (size_t)grid * wpc * (64 + 96 * std::min<uint64_t>(max_ts, 64)));
+  char num[64];
+  auto dbl = [&](double v) {
+    std::snprintf(num, sizeof num, "%.17g", v);
+    return std::string(num);
+  };
+  auto ids = [&](uint32_t cta, uint32_t w) {
+    return "\"pid\":" + std::to_string(cta) + ",\"tid\":" + std::to_string(w);
+  };
+  bool first = true;
+  auto emit = [&](const std::string& ev) {
+    if (!first) js += ',';
+    first = false;
+    js += ev;
+  };
+  js += "{\"traceEvents\":[";
+  for (uint32_t cta = 0; cta < grid; cta++) {
+    emit("{\"name\":\"process_name\",\"ph\":\"M\"," + ids(cta, 0) + ",\"args\":{\"name\":\"CTA " +
+         std::to_string(cta) + "\"}}");
+    for (uint32_t w = 0; w < wpc; w++) {
+      const uint64_t base = ((uint64_t)cta * wpc + w) * slot;
+      const uint32_t n_events = u32(base);
+      const uint64_t cycles = u64(base + 8);
+      emit("{\"name\":\"thread_name\",\"ph\":\"M\"," + ids(cta, w) + ",\"args\":{\"name\":\"warp " +
+           std::to_string(w) + "\"}}");
+      emit("{\"name\":\"warp\",\"ph\":\"X\"," + ids(cta, w) + ",\"ts\":" + dbl(0.0 / cycles_per_us) +
+           ",\"dur\":" + dbl((double)cycles / cycles_per_us) + "}");
+      // record stamps hold the cycle's low 24 bits: unwrap in record order
+      uint64_t full = 0;
+      const uint32_t n = std::min<uint32_t>(n_events, max_ts);
+      for (uint32_t i = 0; i < n; i++) {
+        const uint64_t r = base + 16u + rb * i;
+        const uint32_t word = u32(r), eid = word >> 24, ts24 = word & 0xFFFFFFu;
+        full += (uint64_t)((ts24 - (uint32_t)(full & 0xFFFFFFu)) & 0xFFFFFFu);
+        if (eid >= k->events.size()) return KS_ERR_ARG;
+        const ks::KsEvent& e = k->events[eid];
+        const char* ph = e.kind == 1 ? "B" : e.kind == 2 ? "E" : "i";
+        std::string ev = "{\"name\":\"" + e.name + "\",\"ph\":\"" + ph + "\"," + ids(cta, w) +
+                         ",\"ts\":" + dbl((double)full / cycles_per_us);
+        if (e.kind == 0) ev += ",\"s\":\"t\"";
+        ev += ",\"args\":{\"id\":" + std::to_string(eid);
+        if (e.payload_bytes) ev += ",\"payload\":" + std::to_string(rb == 8 ? (uint64_t)u32(r + 4) : u64(r + 8));
+        ev += "}}";
+        emit(ev);
+      }
+    }
+  }
+  js += "],\"displayTimeUnit\":\"ns\"}";
+  *needed = js.size();
+  if (!out || cap < js.size() + 1) return KS_ERR_ARG;
+  std::memcpy(out, js.data(), js.size());
+  out[js.size()] = 0;
   return KS_OK;
 }
 
