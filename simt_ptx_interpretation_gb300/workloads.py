@@ -361,6 +361,155 @@ def smem_reduce(n: int = 1 << 22, block: int = 256, seed: int = 5, max_ts: int =
                     bufs, max_ts=max_ts, meta={"n": n, "block": block})
 
 
+# ---------------------------------------------------------- fuzz_shared --
+
+def fuzz_shared_ptx(seed: int, block: int) -> str:
+    """A random program over shared memory and bar.sync, race-free by
+    construction and defined natively (no word is read before it is
+    written). A .shared array holds two halves of 2*block u32 words and a
+    u64 area. Thread x starts from in[gtid] and stores it and a second word to
+    half 0 at tid and tid + block; then each phase (separated by bar.sync 0)
+    reads the half written last at a random index map (tid*A + B) &
+    (2*block - 1) — so lanes of a warp hit the same bank on different words,
+    or share a word — combines it with x, may run a divergent then-block, and
+    stores x and a second word to the other half; the half offset toggles in
+    a register, so phases can sit in uniform loops. Some phases write the u64
+    area with 8-byte stores and read a neighbour's entry after the barrier.
+    Every barrier is in convergent code. The result goes to out[gtid]."""
+    assert block & (block - 1) == 0 and 32 <= block <= 256
+    rng = random.Random(seed)
+    words = 2 * block
+    half = 4 * words
+    lines = [
+        f".visible .entry fuzz_sh(",
+        "    .param .u64 fs_in,",
+        "    .param .u64 fs_out",
+        ")",
+        "{",
+        "    .reg .pred  %p<4>;",
+        "    .reg .b32   %r<24>;",
+        "    .reg .b64   %rd<10>;",
+        f"    .shared .align 8 .b8 sw[{2 * half}];",
+        f"    .shared .align 8 .b8 sd[{8 * words}];",
+        "    ld.param.u64    %rd1, [fs_in];",
+        "    ld.param.u64    %rd2, [fs_out];",
+        "    mov.u32         %r1, %tid.x;",
+        "    mov.u32         %r2, %ctaid.x;",
+        "    mov.u32         %r3, %ntid.x;",
+        "    mad.lo.s32      %r4, %r2, %r3, %r1;",
+        "    cvt.u64.u32     %rd3, %r4;",
+        "    shl.b64         %rd3, %rd3, 2;",
+        "    add.s64         %rd4, %rd1, %rd3;",
+        "    ld.global.u32   %r5, [%rd4];",
+        "    mov.u32         %r6, sw;",
+        "    mov.u32         %r7, sd;",
+        "    shl.b32         %r8, %r1, 2;",
+        "    add.u32         %r9, %r6, %r8;",
+        "    st.shared.u32   [%r9], %r5;",
+        "    xor.b32         %r19, %r5, 1431655765;",
+        f"    st.shared.u32   [%r9+{4 * block}], %r19;",
+        "    mov.u32         %r10, 0;",   # byte offset of the half written last
+        "    bar.sync 0;",
+    ]
+    label = [0]
+
+    def phase(out):
+        a, b = rng.randrange(0, 2 * words), rng.randrange(0, words)
+        out += [
+            f"    mul.lo.u32      %r11, %r1, {a};",
+            f"    add.u32         %r11, %r11, {b};",
+            f"    and.b32         %r11, %r11, {words - 1};",
+            "    shl.b32         %r11, %r11, 2;",
+            "    add.u32         %r11, %r11, %r10;",
+            "    add.u32         %r11, %r11, %r6;",
+            "    ld.shared.u32   %r12, [%r11];",
+        ]
+        op = rng.choice(["xor", "add", "mad"])
+        if op == "xor":
+            out.append("    xor.b32         %r5, %r5, %r12;")
+        elif op == "add":
+            out.append("    add.u32         %r5, %r5, %r12;")
+        else:
+            out.append(f"    mad.lo.u32      %r5, %r12, {rng.randrange(1, 1 << 31) | 1}, %r5;")
+        if rng.random() < 0.4:  # a divergent then-block
+            label[0] += 1
+            m = rng.choice([1, 3, 7, 15, 31])
+            out += [
+                f"    and.b32         %r13, %r1, {m};",
+                "    setp.ne.u32     %p1, %r13, 0;",
+                f"    @%p1 bra        FS_SKIP{label[0]};",
+                f"    mul.lo.u32      %r5, %r5, {rng.randrange(3, 1 << 20) | 1};",
+                f"    add.u32         %r5, %r5, {rng.randrange(0, 1 << 30)};",
+                f"FS_SKIP{label[0]}:",
+            ]
+        wrote64 = rng.random() < 0.3
+        if wrote64:  # the u64 area: written here, read back through a map after the barrier
+            out += [
+                "    cvt.u64.u32     %rd5, %r5;",
+                "    shl.b64         %rd5, %rd5, 7;",
+                "    cvt.u64.u32     %rd6, %r12;",
+                "    xor.b64         %rd5, %rd5, %rd6;",
+                "    shl.b32         %r14, %r1, 3;",
+                "    add.u32         %r14, %r14, %r7;",
+                "    st.shared.u64   [%r14], %rd5;",
+            ]
+        # write x and a second word to the other half (every word of a half is
+        # written before it is read), then the barrier
+        out += [
+            f"    xor.b32         %r10, %r10, {half};",
+            "    add.u32         %r15, %r8, %r10;",
+            "    add.u32         %r15, %r15, %r6;",
+            "    st.shared.u32   [%r15], %r5;",
+            f"    add.u32         %r19, %r5, {rng.randrange(1, 1 << 31)};",
+            f"    st.shared.u32   [%r15+{4 * block}], %r19;",
+            "    bar.sync 0;",
+        ]
+        if wrote64 and rng.random() < 0.7:  # read the u64 area of a neighbour
+            c = rng.choice([1, 3, 5, 33])
+            out += [
+                f"    mul.lo.u32      %r16, %r1, {c};",
+                f"    and.b32         %r16, %r16, {block - 1};",
+                "    shl.b32         %r16, %r16, 3;",
+                "    add.u32         %r16, %r16, %r7;",
+                "    ld.shared.u64   %rd7, [%r16];",
+                "    cvt.u32.u64     %r17, %rd7;",
+                "    add.u32         %r5, %r5, %r17;",
+                "    bar.sync 0;",  # the u64 area may be written again next phase
+            ]
+
+    for _ in range(rng.randint(3, 6)):
+        if rng.random() < 0.3:  # a uniform loop of phases
+            label[0] += 1
+            loop = label[0]
+            trips = rng.randint(2, 4)
+            lines += ["    mov.u32         %r18, 0;", "    //@iket range_start loop", f"FS_LOOP{loop}:"]
+            phase(lines)
+            lines += ["    add.u32         %r18, %r18, 1;", f"    setp.lt.u32     %p2, %r18, {trips};",
+                      f"    @%p2 bra        FS_LOOP{loop};", "    //@iket range_end loop"]
+        else:
+            phase(lines)
+    lines += [
+        "    add.s64         %rd8, %rd2, %rd3;",
+        "    st.global.u32   [%rd8], %r5;",
+        "    ret;",
+        "}",
+        "",
+    ]
+    return HEADER + "\n".join(lines)
+
+
+def fuzz_shared(i: int, grid: int = 64, block: int = 128, seed_base: int = 2000, data_seed: int = 6,
+                max_ts: int = 16) -> Workload:
+    """Random shared-memory / barrier program i (seed seed_base + i)."""
+    n = grid * block
+    x = randint_u32(n, 0, 1 << 31, data_seed)
+    out = np.zeros(n, dtype=np.uint32)
+    bufs = place([("in", x, False), ("out", out, True)])
+    params = pack_params([("u64", bufs[0].sim_base), ("u64", bufs[1].sim_base)])
+    return Workload(f"fuzz_shared_{seed_base + i}", fuzz_shared_ptx(seed_base + i, block), "fuzz_sh", grid, block,
+                    params, bufs, max_ts=max_ts, meta={"seed": seed_base + i})
+
+
 # --------------------------------------------------------------- divergent --
 
 DIVERGENT_BODY_OPS = 16

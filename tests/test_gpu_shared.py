@@ -244,3 +244,18 @@ def test_jit_crosscheck_shared_patterns(pattern, guard, size):
     sim = _parity.gpu_run(w).buffers
     nat = jit_memory(w)
     assert np.array_equal(sim[0], nat[0])
+
+
+@pytest.mark.parametrize("block", [32, 128, 256])
+@pytest.mark.parametrize("i", range(24))
+def test_random_shared_programs_match_the_oracle(i, block):
+    _parity.assert_parity(wl.fuzz_shared(i, grid=16, block=block))
+
+
+@pytest.mark.parametrize("i", range(0, 24, 3))
+def test_jit_crosscheck_random_shared_programs(i):
+    from tests.test_gpu_parity import jit_memory
+    w = wl.fuzz_shared(i, grid=16, block=128)
+    sim = _parity.gpu_run(w).buffers
+    nat = jit_memory(w)
+    assert np.array_equal(sim[1], nat[1])

@@ -64,6 +64,8 @@ def corpus():
     progs += [("probe", tsh.bank_probe_ptx(4)), ("probe", tsh.bank_probe_ptx(8)), ("bar2", tsh.barrier_ptx(3))]
     for body, _ in tsh.SHARED_BAD:
         progs.append(("bad", tsh.bad_shared_kernel(body)))
+    for i in range(0, 24, 5):
+        progs.append(("fuzz_sh", wl.fuzz_shared_ptx(2000 + i, 128)))
     progs.append(("ev", tev.kernel(tev.PAYLOADS)))
     for body in ("    //@iket mark a %r1\n    ret;", "    //@iket mark a %rd1\n    ret;", "    //@iket mark a %f1\n    ret;",
                  "    //@iket mark a\n    //@iket mark b %r1\n    ret;", "    //@iket mark a %r1\n    //@iket mark a %rd1\n    ret;",

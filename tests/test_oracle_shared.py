@@ -295,3 +295,19 @@ def bad_shared_kernel(body: str) -> str:
 @pytest.mark.parametrize("body,code", SHARED_BAD)
 def test_rejected_forms(body, code):
     assert oracle.parse_check(bad_shared_kernel(body), "bad")[0] == code
+
+
+@pytest.mark.parametrize("i", range(0, 12, 3))
+@pytest.mark.parametrize("block", [32, 256])
+def test_random_shared_programs_are_race_free_and_mode_independent(i, block):
+    """The shared-memory program generator's contract, checked on the oracle:
+    no two threads of a CTA touch one word in one barrier interval with a
+    write among them, and warp mode and per-thread mode store the same."""
+    w = wl.fuzz_shared(i, grid=4, block=block)
+    b1, b2 = w.fresh_buffers(), w.fresh_buffers()
+    r1 = oracle.run(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in b1], race_check=True)
+    r2 = oracle.run(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in b2],
+                    mode=oracle.MODE_PER_THREAD)
+    assert r1.status == r2.status == 0 and r1.race_flags == 0
+    assert np.array_equal(b1[1].data, b2[1].data)
+    assert r1.stats["sh_wavefronts"].sum() >= r1.stats["sh_req"].sum() > 0
