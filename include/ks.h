@@ -67,8 +67,10 @@
  *   - Shared memory and barriers (KernelScope backend doc, simulator/models.py
  *     Block: a shared array and a barrier per block; Warp.at_barrier): a
  *     kernel that declares .shared arrays or uses bar.sync runs CTA by CTA
- *     with every warp of the CTA resident; its block may hold at most
- *     KS_MAX_CTA_MODE_BLOCK threads (else KS_ERR_LIMIT). Shared memory starts
+ *     with every warp of the CTA resident (KS_ERR_LIMIT when the warps'
+ *     interpreter state and the shared arrays exceed one SM's shared memory;
+ *     blocks above 256 threads run a slower 1024-thread configuration).
+ *     Shared memory starts
  *     zeroed in every CTA. A warp that issues bar.sync (any active mask)
  *     stops; when every warp of the CTA has stopped at a barrier or finished,
  *     the stopped warps resume with t_next = latest bar.sync issue cycle +
@@ -123,7 +125,7 @@ extern "C" {
 #define KS_MAX_PARAM_BYTES 256
 #define KS_MAX_STACK 32
 #define KS_MAX_SHARED_BYTES 49152   /* simulated shared memory per CTA */
-#define KS_MAX_CTA_MODE_BLOCK 256   /* block limit of kernels with shared memory or bar.sync */
+#define KS_MAX_CTA_MODE_BLOCK 1024  /* block limit of kernels with shared memory or bar.sync */
 
 typedef struct ks_module ks_module; /* opaque; owned by the library */
 
@@ -250,8 +252,8 @@ size_t ks_stats_bytes(uint32_t grid, uint32_t block);
  * Simulated faults do not fail the call: they are reported per warp in the
  * stats records (read them with ks_read_stats). Host-side errors: KS_ERR_ARG
  * (shapes, sizes, buffer table, undersized outputs), KS_ERR_NOT_FOUND,
- * KS_ERR_LIMIT (the real launch's shared memory does not fit, or a kernel
- * with shared memory or bar.sync has a block above KS_MAX_CTA_MODE_BLOCK),
+ * KS_ERR_LIMIT (the real launch's shared memory does not fit — for a kernel
+ * with shared memory or bar.sync, every warp of a CTA at once),
  * KS_ERR_CUDA. The first call on a device
  * uploads the module's program there (one allocation per module per device).
  * Simulations that share output or store-target buffers must not overlap in

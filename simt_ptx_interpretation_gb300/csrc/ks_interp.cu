@@ -197,9 +197,11 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 
 // CTA: the launch runs kernels with shared memory or bar.sync (one real CTA
 // per simulated CTA, barrier rounds, shared-memory handlers); compiled apart
-// so that the other kernels keep the register budget of the plain loop.
-template <bool CTA>
-__global__ void __launch_bounds__(256, 1) ks_interp_kernel(const __grid_constant__ KsLaunch L) {
+// so that the other kernels keep the register budget of the plain loop. BIG:
+// CTA mode for blocks of 9..32 warps (a 1024-thread real CTA, at most 64
+// registers a thread, so it spills: slower, used only for such blocks).
+template <bool CTA, bool BIG>
+__global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __grid_constant__ KsLaunch L) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t wid = threadIdx.x >> 5;
@@ -1046,9 +1048,11 @@ static int ensure_attr() {
   int mx = 0;
   e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return (int)e;
-  e = cudaFuncSetAttribute(ks_interp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  e = cudaFuncSetAttribute(ks_interp_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   if (e != cudaSuccess) return (int)e;
-  e = cudaFuncSetAttribute(ks_interp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  e = cudaFuncSetAttribute(ks_interp_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e != cudaSuccess) return (int)e;
+  e = cudaFuncSetAttribute(ks_interp_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   if (e != cudaSuccess) return (int)e;
   if (dev < 64) g_attr_done[dev] = 1;
   return 0;
@@ -1057,8 +1061,10 @@ static int ensure_attr() {
 int interp_occupancy(bool cta_mode, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm) {
   int e = ensure_attr();
   if (e) return e;
-  return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, cta_mode ? ks_interp_kernel<true> : ks_interp_kernel<false>, (int)(real_warps_per_cta * 32), smem);
+  const void* fn = !cta_mode ? (const void*)ks_interp_kernel<false, false>
+                   : real_warps_per_cta > 8 ? (const void*)ks_interp_kernel<true, true>
+                                            : (const void*)ks_interp_kernel<true, false>;
+  return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, (int)(real_warps_per_cta * 32), smem);
 }
 
 int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps_per_cta, uint32_t* real_ctas) {
@@ -1111,10 +1117,12 @@ int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_
   if (e) return e;
   const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, real_warps_per_cta,
                                        L.cta_mode ? L.shared_bytes : 0u);
-  if (L.cta_mode)
-    ks_interp_kernel<true><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
+  if (!L.cta_mode)
+    ks_interp_kernel<false, false><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
+  else if (real_warps_per_cta > 8)
+    ks_interp_kernel<true, true><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
   else
-    ks_interp_kernel<false><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
+    ks_interp_kernel<true, false><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
   return (int)cudaGetLastError();
 }
 

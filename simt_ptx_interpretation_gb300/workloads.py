@@ -351,8 +351,8 @@ RD_EXIT:
 
 def smem_reduce(n: int = 1 << 22, block: int = 256, seed: int = 5, max_ts: int = 4) -> Workload:
     """Shared-memory tree reduction: one u32 sum per CTA of `block` threads
-    (block a power of two, at most 256)."""
-    assert block & (block - 1) == 0 and 2 <= block <= 256 and n % block == 0
+    (block a power of two, at most 1024)."""
+    assert block & (block - 1) == 0 and 2 <= block <= 1024 and n % block == 0
     x = randint_u32(n, 0, 1 << 31, seed)
     out = np.zeros(n // block, dtype=np.uint32)
     bufs = place([("in", x, False), ("out", out, True)])
@@ -376,7 +376,7 @@ def fuzz_shared_ptx(seed: int, block: int) -> str:
     a register, so phases can sit in uniform loops. Some phases write the u64
     area with 8-byte stores and read a neighbour's entry after the barrier.
     Every barrier is in convergent code. The result goes to out[gtid]."""
-    assert block & (block - 1) == 0 and 32 <= block <= 256
+    assert block & (block - 1) == 0 and 32 <= block <= 1024
     rng = random.Random(seed)
     words = 2 * block
     half = 4 * words

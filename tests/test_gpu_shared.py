@@ -126,12 +126,11 @@ def test_barrier_closed_form_matches_the_oracle(n):
     assert list(g.stats["cycles"]) == [release + 1] * 2
 
 
-def test_zeroed_shared_memory_and_partial_warps():
-    ptx = wl.HEADER + """.visible .entry z(.param .u64 out)
+ZEROED_PTX = wl.HEADER + """.visible .entry z(.param .u64 out)
 {
     .reg .b32 %r<6>;
     .reg .b64 %rd<4>;
-    .shared .align 4 .b8 s[1024];
+    .shared .align 4 .b8 s[4096];
     ld.param.u64 %rd1, [out];
     mov.u32 %r1, %tid.x;
     mov.u32 %r2, %ctaid.x;
@@ -151,6 +150,10 @@ def test_zeroed_shared_memory_and_partial_warps():
     ret;
 }
 """
+
+
+def test_zeroed_shared_memory_and_partial_warps():
+    ptx = ZEROED_PTX
     for grid, block in [(700, 48), (5, 256), (1, 1)]:
         out = np.zeros(grid * block, dtype=np.uint32)
         bufs = wl.place([("out", out, True)])
@@ -211,12 +214,34 @@ SKIP:
     assert int(g.stats["cycles"][1]) > 1 << 30
 
 
-def test_cta_mode_rejects_large_blocks():
-    w = wl.smem_reduce(n=512, block=256)
+def test_blocks_above_256_threads():
+    """CTA mode for 9..32 warps per CTA (the 1024-thread configuration)."""
+    from tests.test_gpu_parity import jit_memory
+    for block in (512, 1024):
+        w = wl.smem_reduce(n=block * 8, block=block)
+        _parity.assert_parity(w)
+        assert np.array_equal(_parity.gpu_run(w).buffers[1], jit_memory(w)[1])
+
+
+@pytest.mark.parametrize("block", [640, 1000, 1024])
+def test_lean_kernel_at_large_blocks(block):
+    ptx = ZEROED_PTX
+    grid = 5
+    out = np.zeros(grid * block, dtype=np.uint32)
+    bufs = wl.place([("out", out, True)])
+    w = wl.Workload("z", ptx, "z", grid, block, wl.pack_params([("u64", bufs[0].sim_base)]), bufs)
+    g, _ = _parity.assert_parity(w)
+    assert np.array_equal(g.buffers[0].view(np.uint32), np.repeat(2 * np.arange(grid, dtype=np.uint32), block))
+
+
+def test_cta_mode_reports_state_that_does_not_fit():
+    # 16 warps of a random shared program's interpreter state (about 14 KB a
+    # warp) plus its shared arrays exceed an SM's shared memory
+    w = wl.fuzz_shared(0, grid=2, block=512)
     m = ks.Module(w.ptx)
     with pytest.raises(ks.KsError) as e:
-        ks.run(m, w.kernel, 1, 288, w.params, [(b.sim_base, torch.zeros(b.data.nbytes, dtype=torch.uint8).cuda())
-                                               for b in w.buffers])
+        ks.run(m, w.kernel, w.grid, w.block, w.params,
+               [(b.sim_base, torch.zeros(b.data.nbytes, dtype=torch.uint8).cuda()) for b in w.buffers])
     assert e.value.code == -6
 
 
