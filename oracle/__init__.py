@@ -19,6 +19,11 @@ Parity status per function (pins live in ``tests/test_oracle_*.py``):
     page and the strided closed form min(32, 4s).
   * trace slots — pinned by hand-derived vector_add records and the IKET slot
     size formula.
+  * L1/L2 hit model (run_cached) — pinned by hand-derived hit sequences and
+    cycle counts (reuse, L1-only and L1+L2 set conflicts, step order between
+    warps, the lowest executing lane, stores installing lines, barrier
+    release steps) and by a per-access replay of the pages' direct-mapped
+    cache over the access stream in (step, warp) order.
   * cycles, sectors and traces of random (fuzz) programs beyond these rules:
     parity unpinned (oracle-vs-GPU agreement only).
 """
@@ -85,6 +90,24 @@ class _Config(ctypes.Structure):
     ]
 
 
+class _Cache(ctypes.Structure):
+    _fields_ = [
+        ("l1_lines", ctypes.c_uint32),
+        ("l2_lines", ctypes.c_uint32),
+        ("lat_l1", ctypes.c_uint32),
+        ("lat_l2", ctypes.c_uint32),
+        ("log_cap", ctypes.c_uint32),
+        ("warps", ctypes.c_void_p),
+        ("log", ctypes.c_void_p),
+    ]
+
+
+# L1/L2 hit model outputs: per-warp counts and the access log (line, step, level)
+CACHE_L1_HIT, CACHE_L2_HIT, CACHE_DRAM = 0, 1, 2
+CACHE_WARP_DTYPE = np.dtype([("n_access", "<u4"), ("l1_hits", "<u4"), ("l2_hits", "<u4"), ("dram", "<u4")])
+CACHE_ACCESS_DTYPE = np.dtype([("line", "<u8"), ("step", "<u4"), ("level", "<u4")])
+
+
 class OracleError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"oracle error {code}: {msg}")
@@ -116,6 +139,13 @@ def _load():
             ctypes.POINTER(_Config), ctypes.c_void_p, ctypes.c_void_p,
             ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_uint32),
             ctypes.c_char_p, ctypes.c_uint64,
+        ]
+        lib.orc_run_cached.restype = ctypes.c_int
+        lib.orc_run_cached.argtypes = [
+            ctypes.c_char_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
+            ctypes.c_void_p, ctypes.c_uint64, ctypes.POINTER(_Buffer), ctypes.c_uint32,
+            ctypes.POINTER(_Config), ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.POINTER(ctypes.c_int32), ctypes.c_char_p, ctypes.c_uint64,
         ]
         lib.orc_ipdom.restype = ctypes.c_int
         lib.orc_ipdom.argtypes = [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
@@ -204,6 +234,57 @@ def run(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffers, *,
     if rc != 0:
         raise OracleError(rc, err.value.decode(errors="replace"))
     return Result(stats=stats, trace=tr, status=status.value, race_flags=race.value)
+
+
+@dataclass
+class CachedResult:
+    stats: np.ndarray
+    trace: np.ndarray | None
+    status: int
+    warps: np.ndarray  # CACHE_WARP_DTYPE, one record per warp
+    log: np.ndarray    # CACHE_ACCESS_DTYPE, shape (W, log_cap)
+
+
+def run_cached(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffers, *,
+               lat=DEFAULT_LAT, max_ts: int = 0, trace: bool = False, stack_depth: int = 32,
+               step_limit: int = 1 << 26, l1_lines: int = 1024, l2_lines: int = 49152, lat_l1: int = 28,
+               lat_l2: int = 150, log_cap: int = 256) -> CachedResult:
+    """Interprets `kernel` with the L1/L2 hit model: the whole grid, stepped
+    one instruction per warp per step on one host thread."""
+    lib = _load()
+    W = grid * ((block + 31) // 32)
+    bufs = (_Buffer * max(1, len(buffers)))()
+    keep = []
+    for i, (base, arr) in enumerate(buffers):
+        if not arr.flags["C_CONTIGUOUS"]:
+            raise ValueError("buffer arrays must be C-contiguous")
+        keep.append(arr)
+        bufs[i].sim_base = base
+        bufs[i].host = arr.ctypes.data
+        bufs[i].bytes = arr.nbytes
+    cfg = _Config()
+    for i in range(12):
+        cfg.lat[i] = lat[i] if i < len(lat) else 0
+    cfg.max_ts_per_warp = max_ts
+    cfg.stack_depth = stack_depth
+    cfg.step_limit = step_limit
+    cfg.inject_warp = -1
+    cfg.mode = MODE_WARP
+    warps = np.zeros(W, dtype=CACHE_WARP_DTYPE)
+    log = np.zeros((W, log_cap), dtype=CACHE_ACCESS_DTYPE)
+    cc = _Cache(l1_lines, l2_lines, lat_l1, lat_l2, log_cap, warps.ctypes.data, log.ctypes.data)
+    stats = np.zeros(W, dtype=STATS_DTYPE)
+    tr = np.zeros(W * slot_bytes(max_ts, record_bytes(ptx, kernel)), dtype=np.uint8) if trace else None
+    pbuf = ctypes.create_string_buffer(bytes(params), max(1, len(params)))
+    status = ctypes.c_int32(0)
+    err = ctypes.create_string_buffer(512)
+    rc = lib.orc_run_cached(ptx.encode(), kernel.encode(), grid, block, ctypes.cast(pbuf, ctypes.c_void_p),
+                            len(params), bufs, len(buffers), ctypes.byref(cfg), ctypes.byref(cc),
+                            stats.ctypes.data, tr.ctypes.data if tr is not None else None, ctypes.byref(status),
+                            err, len(err))
+    if rc != 0:
+        raise OracleError(rc, err.value.decode(errors="replace"))
+    return CachedResult(stats=stats, trace=tr, status=status.value, warps=warps, log=log)
 
 
 def ipdom(ptx: str, kernel: str) -> list[int]:

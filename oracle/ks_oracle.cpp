@@ -69,6 +69,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <set>
 #include <stdexcept>
 #include <string>
@@ -1235,6 +1236,8 @@ int popcount32(uint32_t m) {
   return n;
 }
 
+struct CacheModel;
+
 struct Launch {
   const Kernel* K;
   uint32_t grid, block, warps_per_cta;
@@ -1243,7 +1246,44 @@ struct Launch {
   uint8_t* stats;
   uint8_t* trace;
   uint64_t slot_bytes;
+  CacheModel* cache = nullptr;  // L1/L2 hit model, or none
+  uint8_t* cache_warps = nullptr;  // W x {u32 n_access, l1_hits, l2_hits, dram}
+  uint8_t* cache_log = nullptr;    // W x cache_cap x {u64 line, u32 step, u32 level}
+  uint32_t cache_cap = 0;
 };
+
+// ------------------------------------------------------- L1/L2 hit model ----
+// KernelScope backend doc, simulator/engine.py: "Cache parameters" (128-byte
+// lines; L1 1024 lines, hit 28 cycles; L2 49152 lines, hit 150 cycles; DRAM
+// 400) and SimpleCache, a direct-mapped cache: the set of a line is
+// line % num_lines, an access hits when the set's tag is that line, and a
+// miss installs it. (The page's LRU list never picks a victim in a
+// direct-mapped cache, so it is left out.) One L1 and one L2 serve the whole
+// grid, as the page's simulator holds one of each.
+struct SimpleCache {
+  std::vector<int64_t> tags;  // per set: the cached line, -1 = empty
+  explicit SimpleCache(uint32_t lines) : tags(lines, -1) {}
+  bool access(uint64_t line) {
+    int64_t& t = tags[(size_t)(line % tags.size())];
+    if (t == (int64_t)line) return true;
+    t = (int64_t)line;
+    return false;
+  }
+};
+
+struct CacheModel {
+  SimpleCache l1, l2;
+  uint32_t lat_l1, lat_l2;
+  CacheModel(uint32_t n1, uint32_t n2, uint32_t a1, uint32_t a2) : l1(n1), l2(n2), lat_l1(a1), lat_l2(a2) {}
+  // the page's _execute_instruction: L1 first, L2 on an L1 miss
+  uint32_t access(uint64_t line) {
+    if (l1.access(line)) return ORC_CACHE_L1_HIT;
+    if (l2.access(line)) return ORC_CACHE_L2_HIT;
+    return ORC_CACHE_DRAM;
+  }
+};
+
+struct CacheAccess { uint64_t line; uint64_t step; uint32_t level; };
 
 // ------------------------------------------------- shared memory (per CTA) ----
 
@@ -1316,7 +1356,11 @@ uint32_t bank_degree(const uint64_t* addr, uint32_t exec) {
 
 struct Entry { int pc, rpc; uint32_t mask; };
 
-// One simulated warp, resumable at barriers.
+// What WarpRun::run stopped on.
+enum { RUN_DONE = 0, RUN_BAR = 1, RUN_STEP = 2 };
+
+// One simulated warp, resumable at barriers (and, for the cache model, after
+// every instruction).
 struct WarpRun {
   const Launch* X;
   uint32_t gwarp, cta, wic;
@@ -1328,6 +1372,8 @@ struct WarpRun {
   orc_warp_stats st;
   uint32_t n_events = 0, n_dropped = 0;
   std::vector<std::pair<uint32_t, uint64_t>> records;  // (id << 24 | ts, payload)
+  uint64_t step = 0;                  // cache model: the step of the next instruction
+  std::vector<CacheAccess> accesses;  // cache model: this warp's accesses in order
 
   WarpRun(const Launch& L, uint32_t gw) : X(&L), gwarp(gw) {
     const Kernel& K = *X->K;
@@ -1347,12 +1393,16 @@ struct WarpRun {
     st.max_stack_depth = 1;
   }
 
-  // Interprets until the warp finishes (returns false) or issues bar.sync
-  // (returns true with the issue cycle in *arrival).
-  bool run(Memory& M, CtaMem* S, uint64_t* arrival) {
+  // Interprets until the warp finishes (RUN_DONE) or issues bar.sync (RUN_BAR,
+  // with the issue cycle in *arrival). With one_step it also stops before a
+  // second instruction would issue (RUN_STEP); a call that issues the
+  // warp's last instruction returns RUN_DONE, so a warp is done in the step of
+  // its last instruction.
+  int run(Memory& M, CtaMem* S, uint64_t* arrival, bool one_step = false) {
     const Kernel& K = *X->K;
     const orc_config& cfg = *X->cfg;
     const int n = (int)K.code.size();
+    bool issued = false;
     while (!stack.empty()) {
       Entry& top = stack.back();
       if (top.pc == top.rpc || top.mask == 0) { stack.pop_back(); continue; }
@@ -1374,11 +1424,35 @@ struct WarpRun {
         top.pc = pc + 1;
         continue;
       }
+      if (one_step && issued) return RUN_STEP;
       if (cfg.inject_warp >= 0 && (uint64_t)cfg.inject_warp == gwarp && st.warp_insts == cfg.inject_step) {
         st.status = ORC_ST_INJECTED;
-        return false;
+        return RUN_DONE;
       }
-      if (st.warp_insts == cfg.step_limit) { st.status = ORC_ST_STEP_LIMIT; return false; }
+      if (st.warp_insts == cfg.step_limit) { st.status = ORC_ST_STEP_LIMIT; return RUN_DONE; }
+      issued = true;
+
+      // ---- guard ----
+      uint32_t exec = 0;
+      for (int i = 0; i < 32; i++) {
+        if (!((top.mask >> i) & 1)) continue;
+        bool g = true;
+        if (in.guard >= 0) g = (lanes[(size_t)i].v[(size_t)in.guard] != 0) != in.guard_neg;
+        if (g) exec |= 1u << i;
+      }
+      uint64_t lat = cfg.lat[in.cls];
+
+      // ---- cache model: one access at the lowest executing lane's line ----
+      if (X->cache && (in.k == K_LDG || in.k == K_STG) && exec != 0) {
+        int rep = 0;
+        while (!((exec >> rep) & 1)) rep++;
+        const uint64_t addr = lanes[(size_t)rep].v[(size_t)in.a.reg] + (uint64_t)in.a.off;
+        const uint64_t line = addr / 128;
+        const uint32_t level = X->cache->access(line);
+        accesses.push_back(CacheAccess{line, step, level});
+        if (in.k == K_LDG)
+          lat = level == ORC_CACHE_L1_HIT ? X->cache->lat_l1 : level == ORC_CACHE_L2_HIT ? X->cache->lat_l2 : lat;
+      }
 
       // ---- issue: in-order scoreboard ----
       std::vector<int> srcs, dsts;
@@ -1392,7 +1466,6 @@ struct WarpRun {
       uint64_t t = t_next;
       for (int r : srcs) t = std::max(t, ready[(size_t)r]);
       for (int r : dsts) t = std::max(t, ready[(size_t)r]);
-      uint64_t lat = cfg.lat[in.cls];
       for (int r : dsts) { ready[(size_t)r] = t + lat; max_ready = std::max(max_ready, t + lat); }
       if (in.k == K_STG || in.k == K_STS) drain = std::max(drain, t + lat);
       t_last = t;
@@ -1400,20 +1473,11 @@ struct WarpRun {
       st.warp_insts++;
       st.thread_insts += (uint64_t)popcount32(top.mask);
 
-      // ---- guard ----
-      uint32_t exec = 0;
-      for (int i = 0; i < 32; i++) {
-        if (!((top.mask >> i) & 1)) continue;
-        bool g = true;
-        if (in.guard >= 0) g = (lanes[(size_t)i].v[(size_t)in.guard] != 0) != in.guard_neg;
-        if (g) exec |= 1u << i;
-      }
-
       // ---- execute ----
       if (in.k == K_BAR) {  // stop here until the CTA's barrier releases
         top.pc = pc + 1;
         *arrival = t;
-        return true;
+        return RUN_BAR;
       }
       if (in.k == K_BRA) {
         uint32_t taken = exec, fall = top.mask & ~exec;
@@ -1431,7 +1495,7 @@ struct WarpRun {
             if (stack.size() >= cfg.stack_depth) overflow = true;
             else stack.push_back(Entry{pc + 1, R, fall});
           }
-          if (overflow) { st.status = ORC_ST_SIMT_STACK; return false; }
+          if (overflow) { st.status = ORC_ST_SIMT_STACK; return RUN_DONE; }
           st.max_stack_depth = std::max(st.max_stack_depth, (uint32_t)stack.size());
         }
         continue;
@@ -1453,7 +1517,7 @@ struct WarpRun {
           addr[i] = lanes[(size_t)i].v[(size_t)in.a.reg] + (uint64_t)in.a.off;
           err = M.translate(addr[i], size, &host[i], &bi[i], &off[i]);
         }
-        if (err) { st.status = err; return false; }
+        if (err) { st.status = err; return RUN_DONE; }
         if (exec) {
           std::set<uint64_t> sectors, lines;
           for (int i = 0; i < 32; i++) {
@@ -1487,7 +1551,7 @@ struct WarpRun {
           addr[i] = shared_addr(in, lanes[(size_t)i]);
           err = shared_check(addr[i], size, K.shared_bytes);
         }
-        if (err) { st.status = err; return false; }
+        if (err) { st.status = err; return RUN_DONE; }
         if (exec) {
           st.sh_req++;
           st.sh_wavefronts += bank_degree(addr, exec);
@@ -1511,7 +1575,7 @@ struct WarpRun {
         if ((exec >> i) & 1) alu(in, lanes[(size_t)i], ctx[(size_t)i], X->params);
       top.pc = pc + 1;
     }
-    return false;
+    return RUN_DONE;
   }
 
   void write_back() const {
@@ -1533,6 +1597,25 @@ struct WarpRun {
         store_le(r, records[i].first, 4);
         if (rb == 8) store_le(r + 4, records[i].second, 4);
         if (rb == 16) store_le(r + 8, records[i].second, 8);
+      }
+    }
+    if (X->cache && X->cache_warps) {
+      uint32_t l1 = 0, l2 = 0;
+      for (const CacheAccess& a : accesses) {
+        l1 += a.level == ORC_CACHE_L1_HIT;
+        l2 += a.level == ORC_CACHE_L2_HIT;
+      }
+      const uint32_t n = (uint32_t)accesses.size();
+      uint8_t* c = X->cache_warps + (uint64_t)gwarp * 16;
+      store_le(c + 0, n, 4);
+      store_le(c + 4, l1, 4);
+      store_le(c + 8, l2, 4);
+      store_le(c + 12, n - l1 - l2, 4);
+      for (uint32_t k = 0; X->cache_log && k < n && k < X->cache_cap; k++) {
+        uint8_t* r = X->cache_log + ((uint64_t)gwarp * X->cache_cap + k) * 16;
+        store_le(r + 0, accesses[k].line, 8);
+        store_le(r + 8, accesses[k].step, 4);
+        store_le(r + 12, accesses[k].level, 4);
       }
     }
   }
@@ -1560,7 +1643,7 @@ void run_cta(const Launch& X, Memory& M, uint32_t cta) {
     for (size_t w = 0; w < ws.size(); w++) {
       if (done[w]) continue;
       uint64_t arrival = 0;
-      if (ws[w].run(M, &S, &arrival)) {
+      if (ws[w].run(M, &S, &arrival) == RUN_BAR) {
         waiting[w] = 1;
         any_waiting = true;
         latest = std::max(latest, arrival);
@@ -1576,6 +1659,54 @@ void run_cta(const Launch& X, Memory& M, uint32_t cta) {
   }
   for (const WarpRun& w : ws) w.write_back();
   M.race_flags |= S.race_flags;
+}
+
+// ------------------------------------------------ stepper (cache model) ----
+// The page's step()/run() taken literally: in every step each warp of the
+// grid that is neither done nor waiting at a barrier executes one
+// instruction, blocks in order and warps in order within a block; so global
+// accesses reach the caches in (step, block, warp) order. A CTA whose warps
+// are all waiting or done at the end of a step releases its barrier: the
+// waiting warps resume (t_next = latest bar.sync issue + lat[bar]) and issue
+// again in the next step. A warp is done in the step of its last
+// instruction.
+void run_stepped(const Launch& X, Memory& M) {
+  const Kernel& K = *X.K;
+  const uint32_t W = X.grid * X.warps_per_cta;
+  std::vector<WarpRun> ws;
+  ws.reserve(W);
+  for (uint32_t w = 0; w < W; w++) ws.emplace_back(X, w);
+  std::vector<CtaMem> shared;
+  if (K.cta_mode()) for (uint32_t c = 0; c < X.grid; c++) shared.emplace_back(K.shared_bytes, M.race_on);
+  enum { RUNNING, WAITING, DONE };
+  std::vector<int> state(W, RUNNING);
+  std::vector<uint64_t> arrival(W, 0);
+  uint32_t n_done = 0;
+  for (uint64_t step = 0; n_done < W; step++) {
+    for (uint32_t w = 0; w < W; w++) {
+      if (state[w] != RUNNING) continue;
+      ws[w].step = step;
+      CtaMem* S = K.cta_mode() ? &shared[w / X.warps_per_cta] : nullptr;
+      const int r = ws[w].run(M, S, &arrival[w], true);
+      if (r == RUN_BAR) state[w] = WAITING;
+      else if (r == RUN_DONE) { state[w] = DONE; n_done++; }
+    }
+    for (uint32_t c = 0; c < X.grid && K.cta_mode(); c++) {
+      const uint32_t w0 = c * X.warps_per_cta, w1 = w0 + X.warps_per_cta;
+      bool running = false, waiting = false;
+      uint64_t latest = 0;
+      for (uint32_t w = w0; w < w1; w++) {
+        running |= state[w] == RUNNING;
+        if (state[w] == WAITING) { waiting = true; latest = std::max(latest, arrival[w]); }
+      }
+      if (running || !waiting) continue;
+      for (uint32_t w = w0; w < w1; w++)
+        if (state[w] == WAITING) { ws[w].t_next = latest + X.cfg->lat[ORC_LAT_BAR]; state[w] = RUNNING; }
+      shared[c].new_interval();
+    }
+  }
+  for (const WarpRun& w : ws) w.write_back();
+  for (const CtaMem& S : shared) M.race_flags |= S.race_flags;
 }
 
 // ---------------------------------------------------- per-thread mode ----
@@ -1710,10 +1841,14 @@ void orc_config_default(orc_config* cfg) {
   cfg->mode = ORC_MODE_WARP;
 }
 
-int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
-            const void* params, uint64_t param_bytes, const orc_buffer* bufs,
-            uint32_t n_bufs, const orc_config* cfg, void* stats, void* trace,
-            int32_t* status, uint32_t* race_flags, char* err, uint64_t errlen) {
+}  // extern "C"
+
+namespace {
+
+int run_impl(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+             const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+             uint32_t n_bufs, const orc_config* cfg, void* stats, void* trace,
+             int32_t* status, uint32_t* race_flags, const orc_cache* cache, char* err, uint64_t errlen) {
   try {
     if (!ptx || !kernel || !cfg || !stats || !status) throw OracleError{ORC_ERR_ARG, "null argument"};
     if (grid == 0 || block == 0 || block > 1024) throw OracleError{ORC_ERR_ARG, "bad launch shape"};
@@ -1743,6 +1878,17 @@ int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
     X.trace = (uint8_t*)trace;
     X.slot_bytes = ((16ull + (uint64_t)K.record_bytes * cfg->max_ts_per_warp) + 7) / 8 * 8;
     const uint64_t W = (uint64_t)grid * X.warps_per_cta;
+    std::unique_ptr<CacheModel> cm;
+    if (cache) {
+      if (cache->l1_lines == 0 || cache->l2_lines == 0) throw OracleError{ORC_ERR_ARG, "cache with no lines"};
+      if (cfg->mode != ORC_MODE_WARP || cfg->n_warp_list)
+        throw OracleError{ORC_ERR_ARG, "the cache model runs the whole grid in warp mode"};
+      cm.reset(new CacheModel(cache->l1_lines, cache->l2_lines, cache->lat_l1, cache->lat_l2));
+      X.cache = cm.get();
+      X.cache_warps = (uint8_t*)cache->warps;
+      X.cache_log = (uint8_t*)cache->log;
+      X.cache_cap = cache->log_cap;
+    }
 
     std::vector<uint32_t> warps;
     if (cfg->n_warp_list) {
@@ -1804,7 +1950,9 @@ int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
         }
       }
     };
-    if (nthreads <= 1) {
+    if (cm) {
+      run_stepped(X, M);
+    } else if (nthreads <= 1) {
       work(0, units.size());
     } else {
       std::vector<std::thread> pool;
@@ -1832,6 +1980,30 @@ int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
     copy_err(e.what(), err, errlen);
     return ORC_ERR_ARG;
   }
+}
+
+}  // namespace
+
+extern "C" {
+
+int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+            const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+            uint32_t n_bufs, const orc_config* cfg, void* stats, void* trace,
+            int32_t* status, uint32_t* race_flags, char* err, uint64_t errlen) {
+  return run_impl(ptx, kernel, grid, block, params, param_bytes, bufs, n_bufs, cfg, stats, trace, status,
+                  race_flags, nullptr, err, errlen);
+}
+
+int orc_run_cached(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+                   const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+                   uint32_t n_bufs, const orc_config* cfg, const orc_cache* cache, void* stats,
+                   void* trace, int32_t* status, char* err, uint64_t errlen) {
+  if (!cache) {
+    copy_err("null cache", err, errlen);
+    return ORC_ERR_ARG;
+  }
+  return run_impl(ptx, kernel, grid, block, params, param_bytes, bufs, n_bufs, cfg, stats, trace, status,
+                  nullptr, cache, err, errlen);
 }
 
 int orc_ipdom(const char* ptx, const char* kernel, int32_t* out, uint32_t cap,

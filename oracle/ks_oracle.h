@@ -125,6 +125,34 @@ int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
             uint32_t n_bufs, const orc_config* cfg, void* stats, void* trace,
             int32_t* status, uint32_t* race_flags, char* err, uint64_t errlen);
 
+/* L1/L2 hit model (KernelScope backend doc, simulator/engine.py — "Cache
+ * parameters", SimpleCache, _execute_instruction): one direct-mapped L1 and
+ * one direct-mapped L2 of 128-byte lines for the whole grid (set = line %
+ * lines; a miss installs the line). Every ld/st.global with an executing lane
+ * accesses L1 at its lowest executing lane's address, then L2 on a miss; a
+ * load's destination is ready after lat_l1, lat_l2 or lat[ORC_LAT_LDG]. The
+ * grid runs as the page's step() does: each step, every warp that is not done
+ * or waiting at a barrier executes one instruction, blocks then warps in
+ * order; a barrier releases at the end of the step in which its CTA's last
+ * warp arrived or finished. */
+#define ORC_CACHE_L1_HIT 0
+#define ORC_CACHE_L2_HIT 1
+#define ORC_CACHE_DRAM 2
+
+typedef struct {
+  uint32_t l1_lines, l2_lines;
+  uint32_t lat_l1, lat_l2;
+  uint32_t log_cap;  /* records per warp kept in `log` */
+  void* warps;       /* W x {u32 n_access, u32 l1_hits, u32 l2_hits, u32 dram}, or NULL */
+  void* log;         /* W x log_cap x {u64 line, u32 step, u32 level}, or NULL */
+} orc_cache;
+
+/* orc_run (warp mode, whole grid, one host thread) with the hit model. */
+int orc_run_cached(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+                   const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+                   uint32_t n_bufs, const orc_config* cfg, const orc_cache* cache, void* stats,
+                   void* trace, int32_t* status, char* err, uint64_t errlen);
+
 /* Immediate post-dominator of every program entry (instructions and trace
  * pseudo-ops, in program order); the virtual exit is n (= *n_out). */
 int orc_ipdom(const char* ptx, const char* kernel, int32_t* out, uint32_t cap,
