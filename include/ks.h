@@ -106,6 +106,10 @@ extern "C" {
 #define KS_ST_SIMT_STACK 4   /* reconvergence stack deeper than allowed */
 #define KS_ST_TIMEOUT 5      /* a bounded wait inside the interpreter ran out */
 #define KS_ST_INJECTED 6     /* the debug injection point was reached */
+#define KS_ST_CACHE_LOG 7    /* cache model: a warp made more global accesses than the
+                                log holds, or an access step reached 2^32 - 1 */
+#define KS_ST_CACHE_STREAM 8 /* cache model: the second pass's global accesses differ
+                                from the first pass's (see ks_simulate_cached) */
 
 /* ---- latency classes (index of ks_config.lat) --------------------------- */
 #define KS_NUM_LAT_CLASSES 12
@@ -291,6 +295,94 @@ int ks_simulate_static(const ks_module* mod, const char* kernel, uint32_t grid, 
  * accumulator that the library allocates once per device; calls are
  * serialised inside the library. */
 int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_totals* out);
+
+/* ---- L1/L2 hit model (KernelScope backend doc, simulator/engine.py —
+ * "Cache parameters", SimpleCache, _execute_instruction) ----------------------
+ * Two direct-mapped caches of 128-byte lines, one L1 of l1_lines lines and one
+ * L2 of l2_lines lines, each a single instance shared by the whole simulated
+ * grid (as the page's simulator holds one of each). A line of address a is
+ * a / 128; its set is line % lines; an access hits when the set holds that
+ * line, and a miss installs it. Every ld.global / st.global with at least one
+ * executing lane makes one access with the address of its lowest executing
+ * lane (the page's "representative" address): L1 first, L2 on an L1 miss. A
+ * load's destination is then ready lat_l1 (L1 hit), lat_l2 (L2 hit) or
+ * lat[KS_LAT_LDG] (both miss: the DRAM latency) cycles after issue instead of
+ * lat[KS_LAT_LDG]; stores keep lat[KS_LAT_STG]. Nothing else changes.
+ *
+ * Access order (the page's step(): one instruction of every warp per step,
+ * blocks then warps in order): accesses are ordered by (step, global warp id),
+ * where an instruction's step is the number of instructions its warp issued
+ * before it, plus, after each bar.sync, the steps the warp spent waiting: a
+ * barrier releases at the end of the step in which the last warp of the CTA
+ * arrived or finished, and its warps issue again at the next step. Trace
+ * pseudo-ops take no step.
+ *
+ * How it runs: the library interprets the launch twice on `stream`. The first
+ * pass suppresses the simulated stores and logs every access (line, step) per
+ * warp; two stable radix sorts of the log — by (L1 set, step, warp), then the
+ * L1 misses by their L2 set — put each set's accesses in order, and an access
+ * hits when the one before it in its set had the same line. The second pass
+ * is the real run: stores land, loads take the logged level's latency, and
+ * every access is checked against the log. If the addresses or the control
+ * flow depend on a value that the launch itself stored, the first pass may
+ * log other accesses than the second makes; such warps end with
+ * KS_ST_CACHE_STREAM rather than a wrong result.
+ */
+typedef struct {
+  uint32_t l1_lines;              /* default 1024 (128 KB); 1..65536 */
+  uint32_t l2_lines;              /* default 49152 (6 MB); a multiple of l1_lines, l2/l1 <= 65535 */
+  uint32_t lat_l1;                /* default 28 cycles, <= 2^24 */
+  uint32_t lat_l2;                /* default 150 cycles, <= 2^24 */
+  uint32_t max_accesses_per_warp; /* log capacity per warp (default 1024) */
+  uint32_t reserved[3];
+} ks_cache_config;
+
+#define KS_CACHE_LINE_BYTES 128
+#define KS_CACHE_L1_HIT 0
+#define KS_CACHE_L2_HIT 1
+#define KS_CACHE_DRAM 2
+
+/* Per-warp cache counts, the first W records of the workspace. */
+typedef struct {
+  uint32_t n_access; /* global accesses made */
+  uint32_t l1_hits;
+  uint32_t l2_hits;
+  uint32_t dram;     /* missed both */
+} ks_cache_warp;
+
+/* One logged access; warp w's k-th access is record w * max_accesses_per_warp
+ * + k of the log, which starts at byte ceil(16 W / 256) * 256 of the workspace
+ * (after the W ks_cache_warp records). */
+typedef struct {
+  uint64_t line;  /* representative address / 128 */
+  uint32_t step;  /* position in the access order (see above) */
+  uint32_t level; /* KS_CACHE_L1_HIT, KS_CACHE_L2_HIT or KS_CACHE_DRAM */
+} ks_cache_access;
+
+/* Defaults: 1024 and 49152 lines, 28 and 150 cycles, 1024 accesses per warp. */
+void ks_cache_config_default(ks_cache_config* cc);
+
+/* Bytes of the caller-owned device workspace of ks_simulate_cached: W
+ * ks_cache_warp records, W * max_accesses_per_warp ks_cache_access records,
+ * then the sort's scratch (its size is asked of the current CUDA device).
+ * 0 when the configuration is invalid, when the log would hold 2^31 records
+ * or more, or when no CUDA device can be queried. */
+size_t ks_cache_workspace_bytes(uint32_t grid, uint32_t block, const ks_cache_config* cc);
+
+/* ks_simulate with the L1/L2 hit model. Arguments and errors as ks_simulate,
+ * plus cc (host; NULL = defaults) and `workspace`, device memory of at least
+ * ks_cache_workspace_bytes(grid, block, cc) bytes (KS_ERR_ARG otherwise, and
+ * for an invalid cc; KS_ERR_LIMIT when ceil(log2(l1_lines)) + 32 +
+ * ceil(log2(W)) > 64, the sort key's width). Enqueues the two passes and the
+ * sorts on `stream` and returns. Afterwards the workspace holds the per-warp
+ * counts and the access log with each access's level; per-warp statuses
+ * KS_ST_CACHE_LOG and KS_ST_CACHE_STREAM report a log that was too small or
+ * an access stream that the first pass could not predict. */
+int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block,
+                       const void* params, size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs,
+                       void* trace_buf, size_t trace_bytes, void* stats_buf, size_t stats_bytes,
+                       const ks_config* cfg, const ks_cache_config* cc, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /* ---- host post-pass: occupancy (KernelScope backend doc,
  * occupancy/calculator.py — calculate_occupancy) ----------------------------

@@ -47,6 +47,12 @@ class KsOccupancy(ctypes.Structure):
                 ("occupancy_percent", ctypes.c_double)]
 
 
+class KsCacheConfig(ctypes.Structure):
+    _fields_ = [("l1_lines", ctypes.c_uint32), ("l2_lines", ctypes.c_uint32), ("lat_l1", ctypes.c_uint32),
+                ("lat_l2", ctypes.c_uint32), ("max_accesses_per_warp", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32 * 3)]
+
+
 EXPORTS = {
     "ks_config_default": (None, [ctypes.POINTER(KsConfig)]),
     "ks_load_module": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p),
@@ -80,6 +86,13 @@ EXPORTS = {
                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(KsBuffer),
                                           ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                           ctypes.c_size_t, ctypes.POINTER(KsConfig), ctypes.c_void_p]),
+    "ks_cache_config_default": (None, [ctypes.POINTER(KsCacheConfig)]),
+    "ks_cache_workspace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.POINTER(KsCacheConfig)]),
+    "ks_simulate_cached": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(KsBuffer),
+                                          ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.POINTER(KsConfig), ctypes.POINTER(KsCacheConfig),
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "ks_read_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.POINTER(KsTotals)]),
     "ks_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }

@@ -23,6 +23,12 @@ STATS_DTYPE = np.dtype(
 DEFAULT_LAT = (4, 4, 400, 20, 8, 36, 1, 23, 23, 20, 0, 0)
 
 ST_OOB, ST_MISALIGNED, ST_STEP_LIMIT, ST_SIMT_STACK, ST_TIMEOUT, ST_INJECTED = 1, 2, 3, 4, 5, 6
+ST_CACHE_LOG, ST_CACHE_STREAM = 7, 8
+
+# L1/L2 hit model: per-warp counts and logged accesses (include/ks.h)
+CACHE_L1_HIT, CACHE_L2_HIT, CACHE_DRAM = 0, 1, 2
+CACHE_WARP_DTYPE = np.dtype([("n_access", "<u4"), ("l1_hits", "<u4"), ("l2_hits", "<u4"), ("dram", "<u4")])
+CACHE_ACCESS_DTYPE = np.dtype([("line", "<u8"), ("step", "<u4"), ("level", "<u4")])
 
 
 class KsError(RuntimeError):
@@ -244,6 +250,64 @@ def simulate_static(module: Module, kernel: str, grid: int, block: int, params: 
     _check(rc)
 
 
+@dataclass
+class CacheConfig:
+    """The L1/L2 hit model's parameters (ks_cache_config)."""
+    l1_lines: int = 1024
+    l2_lines: int = 49152
+    lat_l1: int = 28
+    lat_l2: int = 150
+    max_accesses_per_warp: int = 1024
+
+    def to_c(self) -> _native.KsCacheConfig:
+        c = _native.KsCacheConfig()
+        _native.lib().ks_cache_config_default(ctypes.byref(c))
+        c.l1_lines, c.l2_lines = self.l1_lines, self.l2_lines
+        c.lat_l1, c.lat_l2 = self.lat_l1, self.lat_l2
+        c.max_accesses_per_warp = self.max_accesses_per_warp
+        return c
+
+
+def cache_workspace_bytes(grid: int, block: int, cache: CacheConfig | None = None) -> int:
+    """Device workspace of simulate_cached (0 when the configuration is invalid)."""
+    cc = (cache or CacheConfig()).to_c()
+    return int(_native.lib().ks_cache_workspace_bytes(grid, block, ctypes.byref(cc)))
+
+
+def simulate_cached(module: Module, kernel: str, grid: int, block: int, params: bytes, buffers, stats: torch.Tensor,
+                    workspace: torch.Tensor, trace: torch.Tensor | None = None, config: Config | None = None,
+                    cache: CacheConfig | None = None, stream=None) -> None:
+    """ks_simulate_cached: simulate() with the L1/L2 hit model; `workspace` is
+    a uint8 cuda tensor of cache_workspace_bytes(grid, block, cache)."""
+    bufs = (_native.KsBuffer * max(1, len(buffers)))()
+    for i, (base, t) in enumerate(buffers):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("buffers must be contiguous CUDA tensors")
+        bufs[i].sim_base = base
+        bufs[i].dev_ptr = t.data_ptr()
+        bufs[i].bytes = t.numel() * t.element_size()
+    cfg = (config or Config()).to_c()
+    cc = (cache or CacheConfig()).to_c()
+    pbuf = ctypes.create_string_buffer(bytes(params), max(1, len(params)))
+    rc = _native.lib().ks_simulate_cached(
+        module.handle, kernel.encode(), grid, block, ctypes.cast(pbuf, ctypes.c_void_p), len(params), bufs,
+        len(buffers), trace.data_ptr() if trace is not None else None,
+        trace.numel() if trace is not None else 0, stats.data_ptr(), stats.numel(), ctypes.byref(cfg),
+        ctypes.byref(cc), workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(rc)
+
+
+def cache_results(workspace: torch.Tensor, n_warps: int, cache: CacheConfig | None = None):
+    """(per-warp counts, access log of shape (W, max_accesses_per_warp)) as numpy
+    arrays, copied from a simulate_cached workspace."""
+    cache = cache or CacheConfig()
+    cap = cache.max_accesses_per_warp
+    log_off = (n_warps * 16 + 255) // 256 * 256
+    warps = workspace[:n_warps * 16].cpu().numpy().view(CACHE_WARP_DTYPE)
+    log = workspace[log_off:log_off + n_warps * cap * 16].cpu().numpy().view(CACHE_ACCESS_DTYPE)
+    return warps, log.reshape(n_warps, cap)
+
+
 def read_stats(stats: torch.Tensor, n_warps: int, stream=None) -> Totals:
     """Launch totals (ks_read_stats); waits for the stream."""
     t = _native.KsTotals()
@@ -262,16 +326,28 @@ class Run:
     trace: torch.Tensor | None
     totals: Totals
     buffers: list = field(default_factory=list)
+    cache_warps: np.ndarray | None = None  # CACHE_WARP_DTYPE per warp (cache model only)
+    cache_log: np.ndarray | None = None    # CACHE_ACCESS_DTYPE, (W, max_accesses_per_warp)
 
 
 def run(module: Module, kernel: str, grid: int, block: int, params: bytes, buffers, config: Config | None = None,
-        trace: bool = False, stream=None) -> Run:
-    """Allocates the outputs, simulates, and reduces the totals."""
+        trace: bool = False, stream=None, cache: CacheConfig | None = None) -> Run:
+    """Allocates the outputs, simulates (with the L1/L2 hit model when `cache`
+    is given), and reduces the totals."""
     config = config or Config()
     dev = buffers[0][1].device if buffers else torch.device("cuda")
     st = torch.empty(stats_bytes(grid, block), dtype=torch.uint8, device=dev)
     tr = (torch.empty(trace_bytes(grid, block, config.max_ts, module.record_bytes(kernel)), dtype=torch.uint8, device=dev)
           if trace else None)
-    simulate(module, kernel, grid, block, params, buffers, st, tr, config, stream)
     n = grid * ((block + 31) // 32)
-    return Run(st, tr, read_stats(st, n, stream), list(buffers))
+    if cache is None:
+        simulate(module, kernel, grid, block, params, buffers, st, tr, config, stream)
+        return Run(st, tr, read_stats(st, n, stream), list(buffers))
+    nbytes = cache_workspace_bytes(grid, block, cache)
+    if nbytes == 0:
+        raise KsError(-3, "invalid cache configuration")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    simulate_cached(module, kernel, grid, block, params, buffers, st, ws, tr, config, cache, stream)
+    totals = read_stats(st, n, stream)
+    warps, log = cache_results(ws, n, cache)
+    return Run(st, tr, totals, list(buffers), warps, log)

@@ -196,9 +196,15 @@ size_t ks_stats_bytes(uint32_t grid, uint32_t block) {
   return (size_t)(warps_of(grid, block) * sizeof(ks_warp_stats));
 }
 
-int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t block, const void* params,
-                size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf, size_t trace_bytes,
-                void* stats_buf, size_t stats_bytes, const ks_config* cfg_in, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks, the lazy program upload and the launch block shared by
+// ks_simulate and ks_simulate_cached.
+int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t block, const void* params,
+            size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf, size_t trace_bytes,
+            void* stats_buf, size_t stats_bytes, const ks_config* cfg_in, ks::KsLaunch* Lp, DevInfo* dip) {
   ks_module* mod = const_cast<ks_module*>(mod_c);
   size_t kidx = 0;
   const ks::KsKernel* k = find_kernel(mod, kernel, &kidx);
@@ -233,7 +239,7 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   // shared memory / bar.sync: every warp of a CTA resident on one real CTA
   if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
 
-  DevInfo di;
+  DevInfo& di = *dip;
   int dev = 0;
   if (device_info(&di, &dev) != KS_OK) return KS_ERR_CUDA;
 
@@ -256,7 +262,7 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   }
 
   // ---- launch block ----
-  ks::KsLaunch L;
+  ks::KsLaunch& L = *Lp;
   std::memset(&L, 0, sizeof L);
   L.image = static_cast<const uint8_t*>(image);
   L.image_bytes = (uint32_t)k->image.size();
@@ -294,12 +300,95 @@ int ks_simulate(const ks_module* mod_c, const char* kernel, uint32_t grid, uint3
   L.param_bytes = (uint32_t)param_bytes;
   if (param_bytes) std::memcpy(L.params, params, param_bytes);
 
-  // ---- real launch shape (persistent real warps, see ks::choose_launch) ----
+  return KS_OK;
+}
+
+// Real launch shape (persistent real warps, see ks::choose_launch) and launch.
+int shape_and_launch(const ks::KsLaunch& L, const DevInfo& di, void* stream) {
   uint32_t wpc_real = 0, ctas = 0;
   const int shape = ks::choose_launch(L, di.sms, di.max_smem, &wpc_real, &ctas);
   if (shape != KS_OK) return shape;
   if (ks::launch_interp(L, wpc_real, ctas, stream) != 0) return KS_ERR_CUDA;
   return KS_OK;
+}
+
+bool cache_config_ok(const ks_cache_config& c) {
+  return c.l1_lines >= 1 && c.l1_lines <= 65536 && c.l2_lines >= c.l1_lines && c.l2_lines % c.l1_lines == 0 &&
+         c.l2_lines / c.l1_lines <= 65535 && c.lat_l1 <= ks::KS_MAX_LATENCY && c.lat_l2 <= ks::KS_MAX_LATENCY &&
+         c.max_accesses_per_warp >= 1;
+}
+
+uint32_t bits_for(uint64_t max_value) {
+  uint32_t b = 0;
+  while (b < 64 && (max_value >> b) != 0) b++;
+  return b;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ks_simulate(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block, const void* params,
+                size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf, size_t trace_bytes,
+                void* stats_buf, size_t stats_bytes, const ks_config* cfg, void* stream) {
+  ks::KsLaunch L;
+  DevInfo di;
+  const int rc = prepare(mod, kernel, grid, block, params, param_bytes, bufs, n_bufs, trace_buf, trace_bytes,
+                         stats_buf, stats_bytes, cfg, &L, &di);
+  if (rc != KS_OK) return rc;
+  return shape_and_launch(L, di, stream);
+}
+
+void ks_cache_config_default(ks_cache_config* cc) {
+  if (!cc) return;
+  std::memset(cc, 0, sizeof *cc);
+  cc->l1_lines = 1024;
+  cc->l2_lines = 49152;
+  cc->lat_l1 = 28;
+  cc->lat_l2 = 150;
+  cc->max_accesses_per_warp = 1024;
+}
+
+size_t ks_cache_workspace_bytes(uint32_t grid, uint32_t block, const ks_cache_config* cc_in) {
+  ks_cache_config cc;
+  if (cc_in) cc = *cc_in; else ks_cache_config_default(&cc);
+  if (grid == 0 || block == 0 || block > 1024 || !cache_config_ok(cc)) return 0;
+  ks::CacheLayout C;
+  if (ks::cache_layout(warps_of(grid, block), cc.max_accesses_per_warp, &C) != KS_OK) return 0;
+  return (size_t)C.total;
+}
+
+int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block, const void* params,
+                       size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf,
+                       size_t trace_bytes, void* stats_buf, size_t stats_bytes, const ks_config* cfg,
+                       const ks_cache_config* cc_in, void* workspace, size_t workspace_bytes, void* stream) {
+  ks_cache_config cc;
+  if (cc_in) cc = *cc_in; else ks_cache_config_default(&cc);
+  if (!cache_config_ok(cc) || !workspace) return KS_ERR_ARG;
+  if (grid == 0 || block == 0 || block > 1024) return KS_ERR_ARG;
+  const uint64_t W = warps_of(grid, block);
+  if (bits_for(cc.l1_lines - 1u) + 32u + bits_for(W - 1u) > 64u) return KS_ERR_LIMIT;
+  ks::CacheLayout C;
+  const int lc = ks::cache_layout(W, cc.max_accesses_per_warp, &C);
+  if (lc != KS_OK) return lc;
+  if (workspace_bytes < C.total) return KS_ERR_ARG;
+  ks::KsLaunch L;
+  DevInfo di;
+  int rc = prepare(mod, kernel, grid, block, params, param_bytes, bufs, n_bufs, trace_buf, trace_bytes, stats_buf,
+                   stats_bytes, cfg, &L, &di);
+  if (rc != KS_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  L.cache_cap = cc.max_accesses_per_warp;
+  L.lat_l1 = cc.lat_l1;
+  L.lat_l2 = cc.lat_l2;
+  L.cache_warps = reinterpret_cast<ks_cache_warp*>(ws + C.warps_off);
+  L.cache_log = reinterpret_cast<ks_cache_access*>(ws + C.log_off);
+  L.cache_pass = 1;  // log the accesses, stores suppressed
+  rc = shape_and_launch(L, di, stream);
+  if (rc != KS_OK) return rc;
+  if (ks::launch_cache_levels(L, ws, C, cc.l1_lines, cc.l2_lines, stream) != 0) return KS_ERR_CUDA;
+  L.cache_pass = 2;  // the real run, latencies from the levels
+  return shape_and_launch(L, di, stream);
 }
 
 int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_totals* out) {
@@ -363,6 +452,8 @@ const char* ks_status_string(int code) {
     case KS_ST_SIMT_STACK: return "reconvergence stack overflow";
     case KS_ST_TIMEOUT: return "bounded wait ran out";
     case KS_ST_INJECTED: return "injected fault";
+    case KS_ST_CACHE_LOG: return "cache model: access log full or access step too large";
+    case KS_ST_CACHE_STREAM: return "cache model: accesses differ between the two passes";
     default: return "unknown status";
   }
 }

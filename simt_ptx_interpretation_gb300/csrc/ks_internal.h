@@ -233,6 +233,13 @@ struct KsLaunch {
   uint8_t* trace;  // may be null
   uint64_t slot_bytes;
   uint8_t* stats;
+  // L1/L2 hit model (ks_simulate_cached): 0 off; 1 first pass (stores
+  // suppressed, accesses logged); 2 second pass (levels from the log)
+  uint32_t cache_pass;
+  uint32_t cache_cap;             // log records per warp
+  uint32_t lat_l1, lat_l2;        // load latency on an L1 / L2 hit
+  ks_cache_warp* cache_warps;     // [n_warps]
+  ks_cache_access* cache_log;     // [n_warps * cache_cap]
   alignas(16) uint8_t params[KS_MAX_PARAM_BYTES];
 };
 
@@ -252,7 +259,21 @@ const KsKernel* module_kernel(const ks_module* mod, const char* name);
 // KS_ERR_LIMIT (no shape fits the shared memory) or KS_ERR_CUDA.
 int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps_per_cta, uint32_t* real_ctas);
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);
-int interp_occupancy(bool cta_mode, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
+int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
+
+// Workspace of the L1/L2 hit model (ks_cache.cu): per-warp counts, the log,
+// and the sort's buffers, each at a 256-byte boundary.
+struct CacheLayout {
+  uint64_t warps_off, log_off, keys_a, keys_b, vals_a, vals_b, temp_off, temp_bytes, total;
+};
+// KS_OK, KS_ERR_ARG (log of 2^31 records or more) or KS_ERR_CUDA (the sort's
+// scratch size could not be queried: it needs a current CUDA device).
+int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out);
+// Enqueues the hit computation between the two passes: keys from the log,
+// sort by (L1 set, step, warp), L1 hits, stable sort of the misses by their
+// L2 set, L2 hits. Returns a cudaError_t value.
+int launch_cache_levels(const KsLaunch& L, uint8_t* workspace, const CacheLayout& C, uint32_t l1_lines,
+                        uint32_t l2_lines, void* stream);
 int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream);
 
 }  // namespace ks

@@ -177,13 +177,16 @@ constexpr uint32_t REBASE_AT = 1u << 30;
 constexpr uint64_t BUDGET_CHUNK = 1ull << 30;
 
 // Barrier rounds of a CTA-mode launch: the latest bar.sync issue cycle of the
-// round (absolute, two rounds in flight) and the count of finished warps.
+// round (absolute, two rounds in flight), the count of finished warps, and
+// (cache model) 1 + the last step issued in the round by a warp that arrived
+// or finished.
 struct CtaCtl {
   unsigned long long latest[2];
   unsigned int done;
   unsigned int pad;
+  unsigned long long step_end[2];
 };
-constexpr uint32_t CTL_BYTES = 32;
+constexpr uint32_t CTL_BYTES = 48;
 
 __host__ __device__ __forceinline__ uint32_t region0(uint32_t image_bytes) {
   return (image_bytes + KS_MAX_PARAM_BYTES + 16u + CTL_BYTES + 127u) / 128u * 128u;
@@ -200,7 +203,7 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 // so that the other kernels keep the register budget of the plain loop. BIG:
 // CTA mode for blocks of 9..32 warps (a 1024-thread real CTA, at most 64
 // registers a thread, so it spills: slower, used only for such blocks).
-template <bool CTA, bool BIG>
+template <bool CTA, bool BIG, bool CACHE>
 __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __grid_constant__ KsLaunch L) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
@@ -272,6 +275,8 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
         ctl->latest[0] = 0ull;
         ctl->latest[1] = 0ull;
         ctl->done = 0u;
+        ctl->step_end[0] = 0ull;
+        ctl->step_end[1] = 0ull;
       }
       __syncthreads();
     }
@@ -293,6 +298,17 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     uint64_t ld_req = 0, ld_sec = 0, st_req = 0, st_sec = 0, ld_lin = 0, st_lin = 0;
     uint32_t n_events = 0, n_rec = 0, n_dropped = 0;
     int status = staged ? 0 : KS_ST_TIMEOUT;
+    // cache model: accesses made (c_k), hits, the first pass's count (c_n),
+    // and the steps spent waiting at barriers (an access's step is c_off +
+    // the instructions its warp issued before it)
+    uint32_t c_k = 0, c_l1 = 0, c_l2 = 0, c_n = 0;
+    uint64_t c_off = 0;
+    if constexpr (CACHE) {
+      if (L.cache_pass == 2) {
+        c_n = L.cache_warps[gw].n_access;
+        if (c_n > L.cache_cap && status == 0) status = KS_ST_CACHE_LOG;
+      }
+    }
     uint8_t* slot = L.trace ? L.trace + (uint64_t)gw * L.slot_bytes : nullptr;
     const bool injected = L.inject_warp >= 0 && (uint64_t)L.inject_warp == gw;
     const uint64_t stop_at = (injected && L.inject_step < L.step_limit) ? L.inject_step : L.step_limit;
@@ -553,9 +569,53 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
         continue;
       }
 
+      // cache model: one access per ld/st.global that a lane executes, at the
+      // lowest executing lane's line; a load's latency follows the level
+      uint32_t wlat = q0.y;
+      if constexpr (CACHE) {
+        const uint32_t ex = mask & (pm ^ gneg);
+        if (op >= OP_LDG32 && op <= OP_STG64 && ex != 0u) {
+          const uint64_t va_c =
+              ((uint64_t)a0 | ((uint64_t)SM32(lb + A + ROW_BYTES) << 32)) + (uint64_t)(int64_t)(int32_t)aux;
+          const uint64_t line = __shfl_sync(FULL, va_c, __ffs(ex) - 1) >> 7;
+          const uint64_t step = c_off + (stop_at - left - budget);
+          ks_cache_access* rec = L.cache_log + (uint64_t)gw * L.cache_cap + c_k;
+          int cst = 0;
+          if (step >= 0xFFFFFFFFull) {
+            cst = KS_ST_CACHE_LOG;
+          } else if (L.cache_pass == 1) {
+            if (c_k < L.cache_cap && lane == 0) {
+              rec->line = line;
+              rec->step = (uint32_t)step;
+              rec->level = KS_CACHE_DRAM;
+            }
+            c_k++;
+          } else if (c_k >= c_n) {
+            cst = KS_ST_CACHE_STREAM;
+          } else {
+            const ulonglong2 r = *reinterpret_cast<const ulonglong2*>(rec);
+            const uint32_t level = (uint32_t)(r.y >> 32);
+            if (r.x != line || (uint32_t)r.y != (uint32_t)step) {
+              cst = KS_ST_CACHE_STREAM;
+            } else {
+              c_l1 += level == KS_CACHE_L1_HIT;
+              c_l2 += level == KS_CACHE_L2_HIT;
+              if (op == OP_LDG32 || op == OP_LDG64)
+                wlat = level == KS_CACHE_L1_HIT ? L.lat_l1 : level == KS_CACHE_L2_HIT ? L.lat_l2 : q0.y;
+              c_k++;
+            }
+          }
+          if (cst != 0) {  // stop before issuing
+            status = cst;
+            FLUSH_THREADS();
+            break;
+          }
+        }
+      }
+
       // issue: in-order scoreboard (a3), epoch-relative 32-bit clock
       const uint32_t t = max(max(max(t_next, pa.y), max(pb.y, pcc.y)), max(max(rd, rg), hmax));
-      const uint32_t wr = t + q0.y;
+      const uint32_t wr = t + wlat;
       if (inc & INC_RDEST) SM32(lb + D + 4u) = wr;  // register destination
       if (inc & INC_PDEST) SM32(wb + q3.y) = wr;    // predicate destination
       max_ready = max(max_ready, wr);
@@ -719,7 +779,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
             const uint64_t va_dn = __shfl_down_sync(FULL, va, 1);
             const bool wins = sorted ? (lane == 31 || va_dn != va)
                                      : (31u - __clz(__match_any_sync(FULL, on ? va : ~0ull))) == lane;
-            if (on && wins) {
+            if (on && wins && !(CACHE && L.cache_pass == 1)) {  // the cache model's first pass stores nothing
               if (wide) *reinterpret_cast<uint64_t*>(ptr) = B64();
               else *reinterpret_cast<uint32_t*>(ptr) = b0;
             }
@@ -914,6 +974,13 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     if constexpr (!cta_mode) break;
     // ---- barrier round (CTA mode): each warp has stopped at bar.sync or
     // finished; the stopped ones resume at the latest arrival + latency ----
+    if constexpr (CACHE) {
+      // the release comes at the end of the step in which the last warp
+      // arrived or finished: 1 + the last step issued by those warps
+      const uint64_t issued = stop_at - left - budget;
+      if ((at_bar || !finished) && issued != 0 && lane == 0)
+        atomicMax(&ctl->step_end[round & 1u], (unsigned long long)(c_off + issued));
+    }
     if (!at_bar && !finished) {
       finished = true;
       if (lane == 0) atomicAdd(&ctl->done, 1u);
@@ -922,12 +989,17 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     if (at_bar && lane == 0) atomicMax(&ctl->latest[round & 1u], (unsigned long long)(epoch + t_last));
     __syncthreads();
     const unsigned long long latest = ctl->latest[round & 1u];
+    const unsigned long long step_end = CACHE ? ctl->step_end[round & 1u] : 0ull;
     const bool all_done = ctl->done == nwarps;
-    if (threadIdx.x == 0) ctl->latest[(round + 1u) & 1u] = 0ull;  // last read two rounds ago
+    if (threadIdx.x == 0) {  // last read two rounds ago
+      ctl->latest[(round + 1u) & 1u] = 0ull;
+      if (CACHE) ctl->step_end[(round + 1u) & 1u] = 0ull;
+    }
     __syncthreads();
     if (all_done) break;
     if (at_bar) {
       at_bar = false;
+      if constexpr (CACHE) c_off = step_end - (stop_at - left - budget);
       const uint64_t rel = (uint64_t)latest + L.lat[KS_LAT_BAR] - epoch;
       if (rel < REBASE_AT) {
         t_next = (uint32_t)rel;
@@ -957,6 +1029,17 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     }  // barrier rounds
 #undef FLUSH_THREADS
     const uint64_t warp_insts = stop_at - left - budget;
+    if constexpr (CACHE) {
+      if (L.cache_pass == 2 && status == 0 && c_k != c_n) status = KS_ST_CACHE_STREAM;
+      if (lane == 0) {
+        ks_cache_warp cw;
+        cw.n_access = c_k;
+        cw.l1_hits = c_l1;
+        cw.l2_hits = c_l2;
+        cw.dram = c_k - c_l1 - c_l2;
+        L.cache_warps[gw] = cw;
+      }
+    }
 
     // ---- write-back (a9) ----
     const uint64_t cycles =
@@ -1040,6 +1123,15 @@ size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t w
 
 static int g_attr_done[64];
 
+// The instantiation that runs a launch: CTA mode (9..32 warps: the 1024-thread
+// form), and the cache model's two passes.
+static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, bool cache) {
+  if (!cta) return cache ? (const void*)ks_interp_kernel<false, false, true> : (const void*)ks_interp_kernel<false, false, false>;
+  if (real_warps_per_cta > 8)
+    return cache ? (const void*)ks_interp_kernel<true, true, true> : (const void*)ks_interp_kernel<true, true, false>;
+  return cache ? (const void*)ks_interp_kernel<true, false, true> : (const void*)ks_interp_kernel<true, false, false>;
+}
+
 static int ensure_attr() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1048,22 +1140,21 @@ static int ensure_attr() {
   int mx = 0;
   e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return (int)e;
-  e = cudaFuncSetAttribute(ks_interp_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-  if (e != cudaSuccess) return (int)e;
-  e = cudaFuncSetAttribute(ks_interp_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-  if (e != cudaSuccess) return (int)e;
-  e = cudaFuncSetAttribute(ks_interp_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-  if (e != cudaSuccess) return (int)e;
+  for (int cta = 0; cta < 2; cta++)
+    for (int big = 0; big < 2; big++)
+      for (int cache = 0; cache < 2; cache++) {
+        if (!cta && big) continue;
+        e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, cache), cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        if (e != cudaSuccess) return (int)e;
+      }
   if (dev < 64) g_attr_done[dev] = 1;
   return 0;
 }
 
-int interp_occupancy(bool cta_mode, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm) {
+int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm) {
   int e = ensure_attr();
   if (e) return e;
-  const void* fn = !cta_mode ? (const void*)ks_interp_kernel<false, false>
-                   : real_warps_per_cta > 8 ? (const void*)ks_interp_kernel<true, true>
-                                            : (const void*)ks_interp_kernel<true, false>;
+  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, L.cache_pass != 0);
   return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, (int)(real_warps_per_cta * 32), smem);
 }
 
@@ -1074,7 +1165,7 @@ int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps
     const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, L.wpc, L.shared_bytes);
     if (smem > (size_t)max_smem) return KS_ERR_LIMIT;
     int per_sm = 0;
-    if (interp_occupancy(true, L.wpc, smem, &per_sm)) return KS_ERR_CUDA;
+    if (interp_occupancy(L, L.wpc, smem, &per_sm)) return KS_ERR_CUDA;
     if (per_sm < 1) return KS_ERR_LIMIT;
     *real_warps_per_cta = L.wpc;
     *real_ctas = (uint32_t)std::min<uint64_t>(L.grid, (uint64_t)sms * (uint64_t)per_sm);
@@ -1095,7 +1186,7 @@ int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps
     const uint64_t want = (n_warps + w - 1) / w;
     if (w > 1 && want < 2ull * (uint64_t)sms) break;
     int per_sm = 0;
-    const int e = interp_occupancy(false, w, smem, &per_sm);
+    const int e = interp_occupancy(L, w, smem, &per_sm);
     if (e) return KS_ERR_CUDA;
     if (per_sm < 1) continue;
     const uint64_t cap = (uint64_t)sms * (uint64_t)per_sm;
@@ -1117,13 +1208,9 @@ int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_
   if (e) return e;
   const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, real_warps_per_cta,
                                        L.cta_mode ? L.shared_bytes : 0u);
-  if (!L.cta_mode)
-    ks_interp_kernel<false, false><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
-  else if (real_warps_per_cta > 8)
-    ks_interp_kernel<true, true><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
-  else
-    ks_interp_kernel<true, false><<<real_ctas, real_warps_per_cta * 32, smem, (cudaStream_t)stream>>>(L);
-  return (int)cudaGetLastError();
+  void* args[] = {const_cast<KsLaunch*>(&L)};
+  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, real_warps_per_cta, L.cache_pass != 0), dim3(real_ctas),
+                               dim3(real_warps_per_cta * 32), args, smem, (cudaStream_t)stream);
 }
 
 int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream) {
