@@ -9,6 +9,10 @@ kernel and one with 8 rotating accumulators), i.e. two interpreter launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload ffma_pair|vector_add|gather_sS|divergent_kK|fuzz|smem_reduce]
+                  [--cache [--cache-cap C]]
+
+--cache runs every launch with the L1/L2 hit model (ks_simulate_cached: a
+logging pass, the sorted levels, the checked second pass).
 
 Prints one JSON line (rank 0). N > 1 runs N independent replicas, one per
 GPU (weak scaling; the path has no exchange step).
@@ -50,6 +54,10 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--iters", type=int, default=4096, help="FFMA outer iterations (smaller cases for profiling)")
+    p.add_argument("--cache", action="store_true", help="simulate with the L1/L2 hit model")
+    p.add_argument("--cache-cap", type=int, default=0,
+                   help="logged global accesses per warp (--cache); 0: the largest count of a plain run, "
+                        "rounded up to a power of two")
     p.add_argument("--scale", type=int, default=1,
                    help="divide the gather outputs, divergent threads or fuzz kernels (smaller cases for profiling)")
     return p.parse_args()
@@ -217,11 +225,37 @@ def run_ours(args, world, rank, local):
         tr = (torch.empty(ks.trace_bytes(w.grid, w.block, w.max_ts, mod.record_bytes(w.kernel)), dtype=torch.uint8,
                           device=dev) if w.max_ts else None)
         jobs.append(dict(w=w, mod=mod, bufs=bufs, cfg=cfg, st=st, tr=tr))
-
-    def step():
+    cap = args.cache_cap
+    if args.cache and cap <= 0:  # size the log from an untimed plain run
+        most = 1
         for j in jobs:
             w = j["w"]
             ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"], stream)
+            a = ks.stats_array(j["st"])
+            most = max(most, int((a["ld_req"] + a["st_req"]).max()))
+        cap = 1 << (most - 1).bit_length()
+    cache = ks.CacheConfig(max_accesses_per_warp=cap) if args.cache else None
+    if cache:  # one workspace, sized for the largest grid
+        wmax = max(jobs, key=lambda j: j["w"].warps)["w"]
+        nbytes = ks.cache_workspace_bytes(wmax.grid, wmax.block, cache)
+        if nbytes == 0:
+            raise SystemExit("invalid cache configuration")
+        cache_ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        config = dict(config, cache_model={"l1_lines": cache.l1_lines, "l2_lines": cache.l2_lines,
+                                           "lat_l1": cache.lat_l1, "lat_l2": cache.lat_l2,
+                                           "max_accesses_per_warp": cache.max_accesses_per_warp})
+
+    def launch(j):
+        w = j["w"]
+        if cache:
+            ks.simulate_cached(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], cache_ws, j["tr"],
+                               j["cfg"], cache, stream)
+        else:
+            ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"], stream)
+
+    def step():
+        for j in jobs:
+            launch(j)
 
     # work per step (deterministic): one run, reduce totals, check statuses
     step()
@@ -249,9 +283,7 @@ def run_ours(args, world, rank, local):
             flush.zero_()
             evs[k][0].record(stream)
             for i, j in enumerate(jobs):
-                w = j["w"]
-                ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"],
-                            stream)
+                launch(j)
                 evs[k][i + 1].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
@@ -268,32 +300,42 @@ def run_ours(args, world, rank, local):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     peak = sms * 4 * 32 * mhz * 1e6 / 1e9  # G thread-inst/s: 4 warp-issues per SM per clock, 32 lanes
     mean_launch_s = sum(sum(x) for x in launch_ms) / (args.steps * n_launch) / 1e3
-    achieved = (insts / n_launch) / mean_launch_s / 1e9
+    # with the cache model a call interprets the launch twice (and sorts in
+    # between): charge the whole call to the two interpreter passes
+    passes = 2 if cache else 1
+    achieved = passes * (insts / n_launch) / mean_launch_s / 1e9
     traffic = traffic_for(config["workload"])
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "Gthread-inst/s",
                 "frac": round(achieved / peak, 5), "traffic": traffic,
                 "peak_source": f"{sms} SMs x 4 issue/clk x 32 lanes x {mhz:.0f} MHz ({peak_src})",
                 "algorithmic_units_per_launch": [int(x) for x in launch_insts],
                 "launch_ms_mean": [round(sum(x) / len(x), 4) for x in launch_ms]}
+    if cache:
+        roofline["note"] = ("each call runs ks_interp_kernel twice plus the level kernels and radix sorts; "
+                            "achieved counts both passes over the whole call's time")
 
     # end to end through the public API with pinned host buffers
-    e2e = None if args.no_e2e else run_e2e(args, jobs, insts, dev, stream)
+    e2e = None if args.no_e2e else run_e2e(args, jobs, insts, dev, stream, launch)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(sum(step_ms) / len(step_ms), 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)", "data": "synthetic (seeded)",
         "config": dict(config, l2="flushed between steps (256 MiB write)", parallelism=f"replicas{world}"),
-        "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * n_launch, "clocks": clocks,
+        # our kernels per call: the interpreter, or (cache model) two interpreter
+        # passes and the four level kernels (the radix sorts and the scan are
+        # library code)
+        "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * n_launch * (6 if cache else 1),
+        "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3), "kernel_sha": kernel_sha(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(ws, sample_warps=None)
+        line["cpu_baseline"] = cpu_baseline_cached(ws, cache) if cache else cpu_baseline(ws, sample_warps=None)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, jobs, insts, dev, stream):
+def run_e2e(args, jobs, insts, dev, stream, launch):
     import torch
     import simt_ptx_interpretation_gb300 as ks
     pinned_in, pinned_out = [], []
@@ -323,9 +365,7 @@ def run_e2e(args, jobs, insts, dev, stream):
             for j, ins, outs in zip(jobs, pinned_in, pinned_out):
                 for h, t in ins:
                     t.copy_(h, non_blocking=True)
-                w = j["w"]
-                ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"],
-                            stream)
+                launch(j)
                 for t, h in outs:
                     h.copy_(t, non_blocking=True)
         stream.synchronize()
@@ -357,6 +397,27 @@ def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None):
             "sample": "; ".join(desc), "thread_insts": total_i, "seconds": round(total_s, 3)}
 
 
+def cpu_baseline_cached(ws, cache, warps_per_kernel=16):
+    """The oracle's cache-model stepper (one host thread: the caches are
+    global state) on a bounded sample: each kernel on a grid cut down to about
+    `warps_per_kernel` warps."""
+    import oracle
+    total_i, total_s, desc = 0, 0.0, []
+    for w in ws:
+        wpc = (w.block + 31) // 32
+        grid = max(1, min(w.grid, warps_per_kernel // wpc))
+        bufs = w.fresh_buffers()
+        t0 = time.perf_counter()
+        r = oracle.run_cached(w.ptx, w.kernel, grid, w.block, w.params, [(b.sim_base, b.data) for b in bufs],
+                              max_ts=w.max_ts, trace=bool(w.max_ts), l1_lines=cache.l1_lines,
+                              l2_lines=cache.l2_lines, lat_l1=cache.lat_l1, lat_l2=cache.lat_l2, log_cap=1)
+        total_s += time.perf_counter() - t0
+        total_i += int(r.stats["thread_insts"].sum())
+        desc.append(f"{w.name}: grid {grid} of {w.grid}")
+    return {"value": round(total_i / total_s, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "; ".join(desc), "thread_insts": total_i, "seconds": round(total_s, 3)}
+
+
 # ----------------------------------------------------------- reference ----
 
 def run_reference(args, world, rank):
@@ -365,12 +426,25 @@ def run_reference(args, world, rank):
     ws, config = workloads(args.workload, args.iters, args.scale)
     cores = os.cpu_count() or 1
     per = max(4, min(64, 2 * cores))
+    if args.cache:
+        from simt_ptx_interpretation_gb300.api import CacheConfig
+        cache = CacheConfig(max_accesses_per_warp=args.cache_cap)
+        per = 8
+        config = dict(config, cache_model={"l1_lines": cache.l1_lines, "l2_lines": cache.l2_lines,
+                                           "lat_l1": cache.lat_l1, "lat_l2": cache.lat_l2})
+        cores = 1
+
+        def sample(n):
+            return cpu_baseline_cached(ws, cache, warps_per_kernel=n)
+    else:
+        def sample(n):
+            return cpu_baseline(ws, max_warps_per_kernel=n)
     for _ in range(args.warmup):
-        cpu_baseline(ws, max_warps_per_kernel=4)
+        sample(4)
     times, insts = [], 0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        b = cpu_baseline(ws, max_warps_per_kernel=per)
+        b = sample(per)
         times.append(time.perf_counter() - t0)
         insts = b["thread_insts"]
     value = insts * len(times) / sum(times)
@@ -380,7 +454,8 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)",
         "data": "synthetic (seeded)", "config": dict(config, sample_warps_per_kernel=per),
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"first {per} warps of each kernel per step"},
+                         "sample": (f"each kernel on a grid of about {per} warps per step" if args.cache
+                                    else f"first {per} warps of each kernel per step")},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

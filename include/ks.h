@@ -373,8 +373,11 @@ size_t ks_cache_workspace_bytes(uint32_t grid, uint32_t block, const ks_cache_co
  * plus cc (host; NULL = defaults) and `workspace`, device memory of at least
  * ks_cache_workspace_bytes(grid, block, cc) bytes (KS_ERR_ARG otherwise, and
  * for an invalid cc; KS_ERR_LIMIT when ceil(log2(l1_lines)) + 32 +
- * ceil(log2(W)) > 64, the sort key's width). Enqueues the two passes and the
- * sorts on `stream` and returns. Afterwards the workspace holds the per-warp
+ * ceil(log2(W)) > 64, the sort key's width). Enqueues the first pass, waits
+ * for `stream` once (to read the number of logged accesses, which sizes the
+ * sorts: they cost in proportion to the accesses made, not to the log's
+ * capacity), then enqueues the sorts and the second pass and returns; so the
+ * call cannot be captured into a CUDA graph. Afterwards the workspace holds the per-warp
  * counts and the access log with each access's level; per-warp statuses
  * KS_ST_CACHE_LOG and KS_ST_CACHE_STREAM report a log that was too small or
  * an access stream that the first pass could not predict. */

@@ -14,7 +14,10 @@
 // contiguous and still in (step, warp) order, and the same neighbour test
 // gives the L2 hits.
 #include <cub/device/device_radix_sort.cuh>
+#include <cub/device/device_scan.cuh>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "ks_internal.h"
 
@@ -31,28 +34,36 @@ __host__ __device__ inline uint32_t bits_for(uint64_t max_value) {  // bits to h
 
 inline uint64_t align256(uint64_t x) { return (x + 255u) / 256u * 256u; }
 
-// One key per log slot: (L1 set, step, warp) packed from the top, or NO_KEY
-// for a slot past the warp's logged accesses.
-__global__ void cache_keys_kernel(const ks_cache_warp* __restrict__ warps, const ks_cache_access* __restrict__ log,
-                                  uint64_t n_warps, uint32_t cap, uint32_t l1_lines, uint32_t warp_bits,
-                                  uint64_t* __restrict__ keys, uint32_t* __restrict__ vals) {
-  const uint64_t n = n_warps * cap;
-  for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
-    const uint64_t w = i / cap;
-    const uint32_t k = (uint32_t)(i - w * cap);
-    const uint32_t logged = min(warps[w].n_access, cap);
-    uint64_t key = NO_KEY;
-    if (k < logged) {
+// Records each warp logged (its count, at most the log's capacity).
+__global__ void cache_logged_kernel(const ks_cache_warp* __restrict__ warps, uint64_t n_warps, uint32_t cap,
+                                    uint32_t* __restrict__ logged) {
+  for (uint64_t w = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; w < n_warps;
+       w += (uint64_t)gridDim.x * blockDim.x)
+    logged[w] = min(warps[w].n_access, cap);
+}
+
+// The logged records packed densely (warp w's at offsets[w]): key (L1 set,
+// step, warp) packed from the top, value the record's log index. One real
+// warp per simulated warp's records.
+__global__ void cache_keys_kernel(const uint32_t* __restrict__ logged, const uint32_t* __restrict__ offsets,
+                                  const ks_cache_access* __restrict__ log, uint64_t n_warps, uint32_t cap,
+                                  uint32_t l1_lines, uint32_t warp_bits, uint64_t* __restrict__ keys,
+                                  uint32_t* __restrict__ vals) {
+  const uint64_t lane = threadIdx.x & 31u;
+  for (uint64_t w = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n_warps;
+       w += ((uint64_t)gridDim.x * blockDim.x) >> 5) {
+    const uint32_t n = logged[w], off = offsets[w];
+    for (uint32_t k = (uint32_t)lane; k < n; k += 32) {
+      const uint64_t i = w * cap + k;
       const ks_cache_access a = log[i];
-      key = ((a.line % l1_lines) << (32 + warp_bits)) | ((uint64_t)a.step << warp_bits) | w;
+      keys[off + k] = ((a.line % l1_lines) << (32 + warp_bits)) | ((uint64_t)a.step << warp_bits) | w;
+      vals[off + k] = (uint32_t)i;
     }
-    keys[i] = key;
-    vals[i] = (uint32_t)i;
   }
 }
 
 // L1: hit when the previous access of the set had the same line. Misses get
-// the sort key of their L2 set's high part; hits and empty slots go last.
+// the sort key of their L2 set's high part; hits go last.
 __global__ void cache_l1_kernel(const uint64_t* __restrict__ keys, const uint32_t* __restrict__ vals, uint64_t n,
                                 ks_cache_access* __restrict__ log, uint32_t l1_lines, uint32_t n_l2_parts,
                                 uint32_t* __restrict__ keys2) {
@@ -98,22 +109,27 @@ unsigned grid_for(uint64_t n) {
 int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out) {
   const uint64_t n = n_warps * (uint64_t)cap;
   if (n == 0 || n >= (1ull << 31)) return KS_ERR_ARG;
-  size_t t1 = 0, t2 = 0;
+  size_t t1 = 0, t2 = 0, t3 = 0;
   if (cub::DeviceRadixSort::SortPairs(nullptr, t1, (const uint64_t*)nullptr, (uint64_t*)nullptr,
                                       (const uint32_t*)nullptr, (uint32_t*)nullptr, (int)n) != cudaSuccess)
     return KS_ERR_CUDA;
   if (cub::DeviceRadixSort::SortPairs(nullptr, t2, (const uint32_t*)nullptr, (uint32_t*)nullptr,
                                       (const uint32_t*)nullptr, (uint32_t*)nullptr, (int)n) != cudaSuccess)
     return KS_ERR_CUDA;
+  if (cub::DeviceScan::ExclusiveSum(nullptr, t3, (const uint32_t*)nullptr, (uint32_t*)nullptr, (int)n_warps + 1) !=
+      cudaSuccess)
+    return KS_ERR_CUDA;
   CacheLayout C;
   C.warps_off = 0;
   C.log_off = align256(n_warps * sizeof(ks_cache_warp));
-  C.keys_a = C.log_off + align256(n * sizeof(ks_cache_access));
+  C.logged_off = C.log_off + align256(n * sizeof(ks_cache_access));
+  C.offsets_off = C.logged_off + align256((n_warps + 1) * 4);
+  C.keys_a = C.offsets_off + align256((n_warps + 1) * 4);
   C.keys_b = C.keys_a + align256(n * 8);
   C.vals_a = C.keys_b + align256(n * 8);
   C.vals_b = C.vals_a + align256(n * 4);
   C.temp_off = C.vals_b + align256(n * 4);
-  C.temp_bytes = align256(t1 > t2 ? t1 : t2);
+  C.temp_bytes = align256(std::max(std::max(t1, t2), t3));
   C.total = C.temp_off + C.temp_bytes;
   *out = C;
   return KS_OK;
@@ -122,10 +138,12 @@ int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out) {
 int launch_cache_levels(const KsLaunch& L, uint8_t* ws, const CacheLayout& C, uint32_t l1_lines, uint32_t l2_lines,
                         void* stream_v) {
   cudaStream_t stream = (cudaStream_t)stream_v;
-  const uint64_t n = (uint64_t)L.n_warps * L.cache_cap;
-  const uint32_t warp_bits = bits_for(L.n_warps - 1u);
+  const uint64_t W = L.n_warps;
+  const uint32_t warp_bits = bits_for(W - 1u);
   const uint32_t key_bits = bits_for(l1_lines - 1u) + 32u + warp_bits;
   const uint32_t n_parts = l2_lines / l1_lines;
+  uint32_t* logged = reinterpret_cast<uint32_t*>(ws + C.logged_off);
+  uint32_t* offsets = reinterpret_cast<uint32_t*>(ws + C.offsets_off);
   uint64_t* keys_a = reinterpret_cast<uint64_t*>(ws + C.keys_a);
   uint64_t* keys_b = reinterpret_cast<uint64_t*>(ws + C.keys_b);
   uint32_t* vals_a = reinterpret_cast<uint32_t*>(ws + C.vals_a);
@@ -135,15 +153,27 @@ int launch_cache_levels(const KsLaunch& L, uint8_t* ws, const CacheLayout& C, ui
   uint32_t* keys2_b = reinterpret_cast<uint32_t*>(ws + C.keys_b);
   void* temp = ws + C.temp_off;
   size_t temp_bytes = C.temp_bytes;
+
+  // per-warp record counts, their exclusive prefix (offsets[W] = the total),
+  // and the total on the host: the sorts run over the logged records only
+  cache_logged_kernel<<<grid_for(W), 256, 0, stream>>>(L.cache_warps, W, L.cache_cap, logged);
+  cudaError_t e = cudaMemsetAsync(logged + W, 0, 4, stream);
+  if (e != cudaSuccess) return (int)e;
+  e = cub::DeviceScan::ExclusiveSum(temp, temp_bytes, logged, offsets, (int)W + 1, stream);
+  if (e != cudaSuccess) return (int)e;
+  uint32_t total = 0;
+  e = cudaMemcpyAsync(&total, offsets + W, 4, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return (int)e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return (int)e;
+  if (total == 0) return 0;
+  const uint64_t n = total;
   const unsigned g = grid_for(n);
 
-  cache_keys_kernel<<<g, 256, 0, stream>>>(L.cache_warps, L.cache_log, L.n_warps, L.cache_cap, l1_lines, warp_bits,
-                                           keys_a, vals_a);
-  cudaError_t e = cudaGetLastError();
+  cache_keys_kernel<<<grid_for(W * 32), 256, 0, stream>>>(logged, offsets, L.cache_log, W, L.cache_cap, l1_lines,
+                                                          warp_bits, keys_a, vals_a);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
-  // Only the key's bits take part. Empty slots (all ones) still sort last: a
-  // real key's step field is below 2^32 - 1 (the interpreter stops a warp
-  // before that step), so no real key reaches all ones in its low key_bits.
   e = cub::DeviceRadixSort::SortPairs(temp, temp_bytes, keys_a, keys_b, vals_a, vals_b, (int)n, 0, (int)key_bits,
                                       stream);
   if (e != cudaSuccess) return (int)e;

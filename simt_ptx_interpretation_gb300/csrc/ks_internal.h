@@ -264,14 +264,15 @@ int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem
 // Workspace of the L1/L2 hit model (ks_cache.cu): per-warp counts, the log,
 // and the sort's buffers, each at a 256-byte boundary.
 struct CacheLayout {
-  uint64_t warps_off, log_off, keys_a, keys_b, vals_a, vals_b, temp_off, temp_bytes, total;
+  uint64_t warps_off, log_off, logged_off, offsets_off, keys_a, keys_b, vals_a, vals_b, temp_off, temp_bytes, total;
 };
 // KS_OK, KS_ERR_ARG (log of 2^31 records or more) or KS_ERR_CUDA (the sort's
 // scratch size could not be queried: it needs a current CUDA device).
 int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out);
-// Enqueues the hit computation between the two passes: keys from the log,
-// sort by (L1 set, step, warp), L1 hits, stable sort of the misses by their
-// L2 set, L2 hits. Returns a cudaError_t value.
+// The hit computation between the two passes: the logged records packed,
+// sorted by (L1 set, step, warp), L1 hits, a stable sort of the misses by
+// their L2 set, L2 hits. Waits for the stream once (the sorts' length is the
+// number of logged records). Returns a cudaError_t value.
 int launch_cache_levels(const KsLaunch& L, uint8_t* workspace, const CacheLayout& C, uint32_t l1_lines,
                         uint32_t l2_lines, void* stream);
 int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream);
