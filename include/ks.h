@@ -153,7 +153,37 @@ typedef struct {
   uint64_t inject_step;             /* ...when its issued-instruction count reaches this */
   uint32_t flags;                   /* reserved, 0 */
   uint32_t reserved;
+  /* Optional per-instruction profile (device, NULL = none): one
+   * ks_pc_profile per program entry, profile_bytes >= ks_profile_bytes();
+   * the call zeroes it first. */
+  void* profile_buf;
+  uint64_t profile_bytes;
 } ks_config;
+
+/* Per-instruction profile record (72 bytes), indexed by program entry (the
+ * order of ks_kernel_ipdom). It keeps what the page's hints analyzer reads
+ * from each trace event (KernelScope backend doc, hints/analyzer.py —
+ * analyze_trace_hints), counted per static instruction:
+ *   global ld/st: efficiency = min(1, ideal / lines), ideal = ceil(executing
+ *     lanes * access size / 128), lines = distinct 128-byte lines (the page's
+ *     analyze_global_memory_access); "poor" below 0.25, "uncoalesced" in
+ *     [0.25, 0.5); percentages are floor(100 * ideal / lines), exactly;
+ *   shared ld/st: the bank-conflict degree (1 = none);
+ *   bra: "divergent" when the guard splits the active lanes; the divergence
+ *     ratio is the smaller side's lanes / the active lanes, "high" above 0.4,
+ *     its percentage floor(100 * smaller / active). */
+typedef struct {
+  uint64_t requests;        /* ld/st (global or shared) with an executing lane */
+  uint64_t poor;            /* global requests with efficiency < 0.25 */
+  uint64_t uncoalesced;     /* global requests with 0.25 <= efficiency < 0.5 */
+  uint64_t conflicted;      /* shared requests of degree > 1 */
+  uint64_t severe;          /* shared requests of degree >= 8 */
+  uint64_t divergent;       /* bra executions that split the active lanes */
+  uint64_t high_divergence; /* ... with a divergence ratio above 0.4 */
+  uint32_t degrees;         /* bit d - 1: a shared request of degree d */
+  uint32_t poor_pcts;       /* bit p: a poor global request of efficiency p % */
+  uint64_t high_div_pcts;   /* bit p: a high-divergence branch of ratio p % */
+} ks_pc_profile;
 
 /* Per-warp statistics record (96 bytes), indexed by global warp id
  * (ctaid * ceil(block/32) + warp index in the CTA). */
@@ -239,6 +269,8 @@ int ks_kernel_record_bytes(const ks_module* mod, const char* kernel, uint32_t* b
 /* Payload size of event `id`: 0, 4 or 8 bytes. */
 int ks_kernel_event_payload(const ks_module* mod, const char* kernel, uint32_t id, uint32_t* bytes);
 size_t ks_stats_bytes(uint32_t grid, uint32_t block);
+/* Bytes of a kernel's per-instruction profile: 72 per program entry. */
+int ks_profile_bytes(const ks_module* mod, const char* kernel, size_t* bytes);
 
 /* Enqueues the interpretation of `kernel` over grid x block simulated
  * threads on `stream` (a cudaStream_t; NULL = the legacy default stream) of
@@ -445,6 +477,58 @@ int ks_occupancy(const ks_gpu_limits* limits, uint32_t threads_per_block, uint32
 int ks_trace_to_json(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block, uint32_t max_ts,
                      const void* trace_host, size_t trace_bytes, double cycles_per_us, char* out, size_t cap,
                      size_t* needed);
+
+/* ---- host post-pass: hints (KernelScope backend doc, hints/analyzer.py —
+ * analyze_trace_hints) ---------------------------------------------------------
+ * The page's rules, read from a per-instruction profile (a host copy of
+ * ks_config.profile_buf) instead of from every trace event: the page emits
+ * one hint per event, here one hint per (instruction, rule) stands for all of
+ * that instruction's events, with their number in `count` and the worst
+ * event's value in the message. In order, per program entry:
+ *   shared degree >= 8:  CRITICAL MEMORY "<d>-way bank conflict" (largest d),
+ *                        "Severe bank conflict causing serialized access";
+ *   shared degree 2..7:  WARNING MEMORY "<d>-way bank conflict" (largest d),
+ *                        "Bank conflict reducing throughput";
+ *   global efficiency < 0.25: CRITICAL MEMORY "Poor memory efficiency (<p>%)"
+ *                        (lowest p), "Scattered access causing many transactions";
+ *   divergence ratio > 0.4: WARNING DIVERGENCE "High divergence (<p>%)" (largest
+ *                        p), "Significant warp divergence at this branch";
+ * then, with pc = -1: more than 5 shared requests of degree > 1 in the launch:
+ * WARNING MEMORY "Shared memory bank conflicts (<n> events)", "Consider padding
+ * arrays or restructuring access patterns"; more than 3 divergent branch
+ * executions: WARNING DIVERGENCE "Branch divergence detected (<n> events)",
+ * "Consider restructuring conditionals or using predication"; and with an
+ * occupancy result: below 25 %: CRITICAL OCCUPANCY "Very low occupancy (<x>%)",
+ * "Limited by <limiter>. Consider reducing resource usage."; below 50 %:
+ * WARNING OCCUPANCY "Low occupancy (<x>%)", "Limited by <limiter>." (x printed
+ * as the shortest decimal that reads back as the same double, with ".0" when
+ * it is whole; limiter "registers", "shared_memory" or "block_size"). The
+ * page also counts uncoalesced requests and register pressure but bases no
+ * hint on them. */
+#define KS_HINT_INFO 0
+#define KS_HINT_WARNING 1
+#define KS_HINT_CRITICAL 2
+#define KS_HINT_MEMORY 0
+#define KS_HINT_DIVERGENCE 1
+#define KS_HINT_OCCUPANCY 2
+#define KS_HINT_REGISTERS 3
+
+typedef struct {
+  int32_t category; /* KS_HINT_MEMORY ... */
+  int32_t severity; /* KS_HINT_INFO ... */
+  int32_t pc;       /* program entry, -1 for launch-wide hints */
+  uint32_t reserved;
+  uint64_t count;   /* events the hint stands for (1 for occupancy) */
+  char message[64];
+  char detail[96];
+} ks_hint;
+
+/* Hints of one launch. profile: host array of n_entries records (may be NULL
+ * with n_entries 0); occupancy: NULL or a ks_occupancy result. Writes at most
+ * cap hints to out and their number to *n_hints; KS_ERR_ARG when out is too
+ * small (call again with *n_hints) or an argument is null. */
+int ks_hints(const ks_pc_profile* profile, uint32_t n_entries, const ks_occupancy_result* occupancy,
+             ks_hint* out, uint32_t cap, uint32_t* n_hints);
 
 /* Text for any KS_* return code or status. */
 const char* ks_status_string(int code);

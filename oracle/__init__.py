@@ -147,6 +147,13 @@ def _load():
             ctypes.POINTER(_Config), ctypes.POINTER(_Cache), ctypes.c_void_p, ctypes.c_void_p,
             ctypes.POINTER(ctypes.c_int32), ctypes.c_char_p, ctypes.c_uint64,
         ]
+        lib.orc_run_events.restype = ctypes.c_int
+        lib.orc_run_events.argtypes = [
+            ctypes.c_char_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
+            ctypes.c_void_p, ctypes.c_uint64, ctypes.POINTER(_Buffer), ctypes.c_uint32,
+            ctypes.POINTER(_Config), ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32),
+            ctypes.c_void_p, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64), ctypes.c_char_p, ctypes.c_uint64,
+        ]
         lib.orc_ipdom.restype = ctypes.c_int
         lib.orc_ipdom.argtypes = [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                   ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32), ctypes.c_char_p,
@@ -234,6 +241,54 @@ def run(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffers, *,
     if rc != 0:
         raise OracleError(rc, err.value.decode(errors="replace"))
     return Result(stats=stats, trace=tr, status=status.value, race_flags=race.value)
+
+
+# events the page's hints analyzer reads (orc_run_events)
+EV_GLOBAL, EV_SHARED, EV_DIVERGE = 0, 1, 2
+HINT_EVENT_DTYPE = np.dtype([("pc", "<u4"), ("kind", "<u4"), ("a", "<u4"), ("b", "<u4"), ("c", "<u4"),
+                             ("pad", "<u4")])
+
+
+def run_events(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffers, *, lat=DEFAULT_LAT,
+               step_limit: int = 1 << 26):
+    """orc_run on one host thread that also returns the hint events in run
+    order (HINT_EVENT_DTYPE): global requests (a lanes, b lines, c bytes),
+    shared requests (a degree), divergent branches (a taken, b fall-through)."""
+    lib = _load()
+    W = grid * ((block + 31) // 32)
+    bufs = (_Buffer * max(1, len(buffers)))()
+    keep = []
+    for i, (base, arr) in enumerate(buffers):
+        keep.append(arr)
+        bufs[i].sim_base = base
+        bufs[i].host = arr.ctypes.data
+        bufs[i].bytes = arr.nbytes
+    cfg = _Config()
+    for i in range(12):
+        cfg.lat[i] = lat[i] if i < len(lat) else 0
+    cfg.stack_depth = 32
+    cfg.step_limit = step_limit
+    cfg.inject_warp = -1
+    cfg.mode = MODE_WARP
+    stats = np.zeros(W, dtype=STATS_DTYPE)
+    pbuf = ctypes.create_string_buffer(bytes(params), max(1, len(params)))
+    status = ctypes.c_int32(0)
+    n = ctypes.c_uint64(0)
+    err = ctypes.create_string_buffer(512)
+    args = (ptx.encode(), kernel.encode(), grid, block, ctypes.cast(pbuf, ctypes.c_void_p), len(params), bufs,
+            len(buffers), ctypes.byref(cfg), stats.ctypes.data, None, ctypes.byref(status))
+    fresh = [(base, arr.copy()) for base, arr in buffers]
+    rc = lib.orc_run_events(*args, None, 0, ctypes.byref(n), err, len(err))
+    if rc != 0:
+        raise OracleError(rc, err.value.decode(errors="replace"))
+    # run again into a buffer of the right size, from the original memory
+    for (_, arr), (_, orig) in zip(buffers, fresh):
+        arr[...] = orig
+    ev = np.zeros(n.value, dtype=HINT_EVENT_DTYPE)
+    rc = lib.orc_run_events(*args, ev.ctypes.data if n.value else None, n.value, ctypes.byref(n), err, len(err))
+    if rc != 0:
+        raise OracleError(rc, err.value.decode(errors="replace"))
+    return Result(stats=stats, trace=None, status=status.value, race_flags=0), ev
 
 
 @dataclass

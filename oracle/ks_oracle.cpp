@@ -1238,6 +1238,13 @@ int popcount32(uint32_t m) {
 
 struct CacheModel;
 
+// One event of the kind the page's hints analyzer reads: a global request
+// (a = executing lanes, b = distinct lines, c = access bytes), a shared
+// request (a = bank-conflict degree), a divergent branch (a = taken lanes,
+// b = fall-through lanes).
+struct HintEvent { uint32_t pc, kind, a, b, c, pad; };
+enum { EV_GLOBAL = 0, EV_SHARED = 1, EV_DIVERGE = 2 };
+
 struct Launch {
   const Kernel* K;
   uint32_t grid, block, warps_per_cta;
@@ -1250,6 +1257,7 @@ struct Launch {
   uint8_t* cache_warps = nullptr;  // W x {u32 n_access, l1_hits, l2_hits, dram}
   uint8_t* cache_log = nullptr;    // W x cache_cap x {u64 line, u32 step, u32 level}
   uint32_t cache_cap = 0;
+  std::vector<HintEvent>* events = nullptr;  // hint events, in run order (one host thread)
 };
 
 // ------------------------------------------------------- L1/L2 hit model ----
@@ -1484,6 +1492,9 @@ struct WarpRun {
         if (fall == 0) { top.pc = in.target; }
         else if (taken == 0) { top.pc = pc + 1; }
         else {
+          if (X->events)
+            X->events->push_back(HintEvent{(uint32_t)pc, EV_DIVERGE, (uint32_t)popcount32(taken),
+                                           (uint32_t)popcount32(fall), 0, 0});
           int R = K.ipdom[(size_t)pc];
           if (top.rpc == R) stack.pop_back(); else top.pc = R;
           bool overflow = false;
@@ -1527,6 +1538,9 @@ struct WarpRun {
           }
           if (in.k == K_LDG) { st.ld_req++; st.ld_sectors += sectors.size(); st.ld_lines += lines.size(); }
           else { st.st_req++; st.st_sectors += sectors.size(); st.st_lines += lines.size(); }
+          if (X->events)
+            X->events->push_back(HintEvent{(uint32_t)pc, EV_GLOBAL, (uint32_t)popcount32(exec),
+                                           (uint32_t)lines.size(), size, 0});
         }
         for (int i = 0; i < 32; i++) {  // ascending lanes: the highest lane's store lands last
           if (!((exec >> i) & 1)) continue;
@@ -1553,8 +1567,10 @@ struct WarpRun {
         }
         if (err) { st.status = err; return RUN_DONE; }
         if (exec) {
+          const uint32_t degree = bank_degree(addr, exec);
           st.sh_req++;
-          st.sh_wavefronts += bank_degree(addr, exec);
+          st.sh_wavefronts += degree;
+          if (X->events) X->events->push_back(HintEvent{(uint32_t)pc, EV_SHARED, degree, 0, 0, 0});
         }
         for (int i = 0; i < 32; i++) {  // ascending lanes: the highest lane's store lands last
           if (!((exec >> i) & 1)) continue;
@@ -1848,7 +1864,8 @@ namespace {
 int run_impl(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
              const void* params, uint64_t param_bytes, const orc_buffer* bufs,
              uint32_t n_bufs, const orc_config* cfg, void* stats, void* trace,
-             int32_t* status, uint32_t* race_flags, const orc_cache* cache, char* err, uint64_t errlen) {
+             int32_t* status, uint32_t* race_flags, const orc_cache* cache, char* err, uint64_t errlen,
+             std::vector<HintEvent>* events = nullptr) {
   try {
     if (!ptx || !kernel || !cfg || !stats || !status) throw OracleError{ORC_ERR_ARG, "null argument"};
     if (grid == 0 || block == 0 || block > 1024) throw OracleError{ORC_ERR_ARG, "bad launch shape"};
@@ -1927,6 +1944,8 @@ int run_impl(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
 
     unsigned nthreads = cfg->threads ? cfg->threads : std::max(1u, std::thread::hardware_concurrency());
     if (cfg->race_check) nthreads = 1;
+    X.events = events;
+    if (events) nthreads = 1;
     nthreads = (unsigned)std::min<size_t>(nthreads, std::max<size_t>(1, units.size()));
 
     auto work = [&](size_t lo, size_t hi) {
@@ -1992,6 +2011,24 @@ int orc_run(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
             int32_t* status, uint32_t* race_flags, char* err, uint64_t errlen) {
   return run_impl(ptx, kernel, grid, block, params, param_bytes, bufs, n_bufs, cfg, stats, trace, status,
                   race_flags, nullptr, err, errlen);
+}
+
+int orc_run_events(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+                   const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+                   uint32_t n_bufs, const orc_config* cfg, void* stats, void* trace,
+                   int32_t* status, void* events, uint64_t events_cap, uint64_t* n_events,
+                   char* err, uint64_t errlen) {
+  if (!n_events) {
+    copy_err("null n_events", err, errlen);
+    return ORC_ERR_ARG;
+  }
+  std::vector<HintEvent> ev;
+  const int rc = run_impl(ptx, kernel, grid, block, params, param_bytes, bufs, n_bufs, cfg, stats, trace, status,
+                          nullptr, nullptr, err, errlen, &ev);
+  *n_events = ev.size();
+  if (rc == ORC_OK && events)
+    std::memcpy(events, ev.data(), std::min<uint64_t>(ev.size(), events_cap) * sizeof(HintEvent));
+  return rc;
 }
 
 int orc_run_cached(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,

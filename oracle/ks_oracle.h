@@ -153,6 +153,20 @@ int orc_run_cached(const char* ptx, const char* kernel, uint32_t grid, uint32_t 
                    uint32_t n_bufs, const orc_config* cfg, const orc_cache* cache, void* stats,
                    void* trace, int32_t* status, char* err, uint64_t errlen);
 
+/* orc_run (warp mode, one host thread) that also lists, in run order, the
+ * events the page's hints analyzer reads (KernelScope backend doc,
+ * hints/analyzer.py): 24-byte records {u32 pc, u32 kind, u32 a, u32 b, u32 c,
+ * u32 0} — kind 0 a global ld/st request (a executing lanes, b distinct
+ * 128-byte lines, c access bytes), kind 1 a shared request (a its
+ * bank-conflict degree), kind 2 a branch that splits the active lanes (a
+ * taken lanes, b fall-through lanes). At most events_cap records are copied;
+ * *n_events gets the total. */
+int orc_run_events(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+                   const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+                   uint32_t n_bufs, const orc_config* cfg, void* stats, void* trace,
+                   int32_t* status, void* events, uint64_t events_cap, uint64_t* n_events,
+                   char* err, uint64_t errlen);
+
 /* Immediate post-dominator of every program entry (instructions and trace
  * pseudo-ops, in program order); the virtual exit is n (= *n_out). */
 int orc_ipdom(const char* ptx, const char* kernel, int32_t* out, uint32_t cap,

@@ -8,11 +8,13 @@ IKET-style per-warp trace slots and, optionally, an L1/L2 hit model on load
 latency; host post-passes compute occupancy and export traces. The C ABI
 is include/ks.h (libks.so); this package marshals arguments to it.
 """
-from .api import (CACHE_ACCESS_DTYPE, CACHE_WARP_DTYPE, DEFAULT_LAT, STATS_DTYPE, CacheConfig, Config, KsError,
-                  Module, Run, Totals, cache_results, cache_workspace_bytes, gpu_limits, occupancy, read_stats, run,
-                  simulate, simulate_cached, simulate_static, stats_array, stats_bytes, trace_bytes, trace_to_json)
+from .api import (CACHE_ACCESS_DTYPE, CACHE_WARP_DTYPE, DEFAULT_LAT, PROFILE_DTYPE, STATS_DTYPE, CacheConfig, Config,
+                  KsError, Module, Run, Totals, cache_results, cache_workspace_bytes, gpu_limits, hints, occupancy,
+                  profile_array, read_stats, run, simulate, simulate_cached, simulate_static, stats_array,
+                  stats_bytes, trace_bytes, trace_to_json)
 
-__all__ = ["CACHE_ACCESS_DTYPE", "CACHE_WARP_DTYPE", "DEFAULT_LAT", "STATS_DTYPE", "CacheConfig", "Config", "KsError",
-           "Module", "Run", "Totals", "cache_results", "cache_workspace_bytes", "gpu_limits", "occupancy",
+__all__ = ["CACHE_ACCESS_DTYPE", "CACHE_WARP_DTYPE", "DEFAULT_LAT", "PROFILE_DTYPE", "STATS_DTYPE", "CacheConfig",
+           "Config", "KsError", "Module", "Run", "Totals", "cache_results", "cache_workspace_bytes", "gpu_limits",
+           "hints", "occupancy", "profile_array",
            "read_stats", "run", "simulate", "simulate_cached", "simulate_static", "stats_array", "stats_bytes",
            "trace_bytes", "trace_to_json"]

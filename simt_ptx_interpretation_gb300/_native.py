@@ -23,6 +23,8 @@ class KsConfig(ctypes.Structure):
         ("inject_step", ctypes.c_uint64),
         ("flags", ctypes.c_uint32),
         ("reserved", ctypes.c_uint32),
+        ("profile_buf", ctypes.c_void_p),
+        ("profile_bytes", ctypes.c_uint64),
     ]
 
 
@@ -51,6 +53,12 @@ class KsCacheConfig(ctypes.Structure):
     _fields_ = [("l1_lines", ctypes.c_uint32), ("l2_lines", ctypes.c_uint32), ("lat_l1", ctypes.c_uint32),
                 ("lat_l2", ctypes.c_uint32), ("max_accesses_per_warp", ctypes.c_uint32),
                 ("reserved", ctypes.c_uint32 * 3)]
+
+
+class KsHint(ctypes.Structure):
+    _fields_ = [("category", ctypes.c_int32), ("severity", ctypes.c_int32), ("pc", ctypes.c_int32),
+                ("reserved", ctypes.c_uint32), ("count", ctypes.c_uint64), ("message", ctypes.c_char * 64),
+                ("detail", ctypes.c_char * 96)]
 
 
 EXPORTS = {
@@ -93,6 +101,9 @@ EXPORTS = {
                                           ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                           ctypes.c_size_t, ctypes.POINTER(KsConfig), ctypes.POINTER(KsCacheConfig),
                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "ks_profile_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_size_t)]),
+    "ks_hints": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.POINTER(KsOccupancy), ctypes.POINTER(KsHint),
+                                ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
     "ks_read_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.POINTER(KsTotals)]),
     "ks_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }

@@ -51,6 +51,7 @@ class Config:
     step_limit: int = 1 << 26
     inject_warp: int = -1
     inject_step: int = 0
+    profile: torch.Tensor | None = None  # uint8 cuda tensor of Module.profile_bytes(kernel), or None
 
     def to_c(self) -> _native.KsConfig:
         c = _native.KsConfig()
@@ -62,6 +63,9 @@ class Config:
         c.step_limit = self.step_limit
         c.inject_warp = self.inject_warp
         c.inject_step = self.inject_step
+        if self.profile is not None:
+            c.profile_buf = self.profile.data_ptr()
+            c.profile_bytes = self.profile.numel() * self.profile.element_size()
         return c
 
 
@@ -132,6 +136,12 @@ class Module:
         _check(_native.lib().ks_kernel_record_bytes(self._h, kernel.encode(), ctypes.byref(b)))
         return b.value
 
+    def profile_bytes(self, kernel: str) -> int:
+        """Bytes of the kernel's per-instruction profile (ks_profile_bytes)."""
+        n = ctypes.c_size_t()
+        _check(_native.lib().ks_profile_bytes(self._h, kernel.encode(), ctypes.byref(n)))
+        return n.value
+
     def event_payload(self, kernel: str, event_id: int) -> int:
         """Payload bytes of an event: 0, 4 or 8."""
         b = ctypes.c_uint32()
@@ -175,6 +185,43 @@ def trace_to_json(module: "Module", kernel: str, grid: int, block: int, max_ts: 
 
 
 LIMITERS = ("registers", "shared_memory", "block_size")
+
+# per-instruction profile record (ks_pc_profile)
+PROFILE_DTYPE = np.dtype([
+    ("requests", "<u8"), ("poor", "<u8"), ("uncoalesced", "<u8"), ("conflicted", "<u8"), ("severe", "<u8"),
+    ("divergent", "<u8"), ("high_divergence", "<u8"), ("degrees", "<u4"), ("poor_pcts", "<u4"),
+    ("high_div_pcts", "<u8")])
+HINT_SEVERITIES = ("info", "warning", "critical")
+HINT_CATEGORIES = ("memory", "divergence", "occupancy", "registers")
+
+
+def profile_array(profile) -> np.ndarray:
+    """A profile buffer (tensor or uint8 array) as PROFILE_DTYPE records."""
+    data = profile.cpu().numpy() if isinstance(profile, torch.Tensor) else np.ascontiguousarray(profile)
+    return data.view(np.uint8).view(PROFILE_DTYPE)
+
+
+def hints(profile, occupancy_result: dict | None = None) -> list[dict]:
+    """The page's performance hints from a launch's per-instruction profile
+    (ks_hints); occupancy_result as returned by occupancy()."""
+    prof = np.ascontiguousarray(profile_array(profile))
+    occ = None
+    if occupancy_result is not None:
+        occ = _native.KsOccupancy()
+        for f, _ in _native.KsOccupancy._fields_:
+            v = occupancy_result[f] if f != "limiter" else LIMITERS.index(occupancy_result["limiter"])
+            setattr(occ, f, v)
+    L = _native.lib()
+    n = ctypes.c_uint32(0)
+    rc = L.ks_hints(prof.ctypes.data if len(prof) else None, len(prof), ctypes.byref(occ) if occ else None, None, 0,
+                    ctypes.byref(n))
+    if rc not in (0, -3):
+        _check(rc)
+    out = (_native.KsHint * max(1, n.value))()
+    _check(L.ks_hints(prof.ctypes.data if len(prof) else None, len(prof), ctypes.byref(occ) if occ else None, out,
+                      n.value, ctypes.byref(n)))
+    return [dict(category=HINT_CATEGORIES[h.category], severity=HINT_SEVERITIES[h.severity], pc=h.pc,
+                 count=h.count, message=h.message.decode(), detail=h.detail.decode()) for h in out[:n.value]]
 
 
 def gpu_limits(arch: str) -> dict:

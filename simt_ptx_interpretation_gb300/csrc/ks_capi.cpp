@@ -238,6 +238,7 @@ int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t 
   if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
   // shared memory / bar.sync: every warp of a CTA resident on one real CTA
   if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
+  if (cfg.profile_buf && cfg.profile_bytes < k->code.size() * sizeof(ks_pc_profile)) return KS_ERR_ARG;
 
   DevInfo& di = *dip;
   int dev = 0;
@@ -299,8 +300,17 @@ int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t 
   L.stats = static_cast<uint8_t*>(stats_buf);
   L.param_bytes = (uint32_t)param_bytes;
   if (param_bytes) std::memcpy(L.params, params, param_bytes);
-
+  L.profile = static_cast<ks_pc_profile*>(cfg.profile_buf);
   return KS_OK;
+}
+
+// Zeroes the profile (if any) on the stream before the launch that fills it.
+int clear_profile(const ks::KsLaunch& L, void* stream) {
+  if (!L.profile) return KS_OK;
+  return cudaMemsetAsync(L.profile, 0, (size_t)L.n_insn * sizeof(ks_pc_profile), static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? KS_OK
+             : KS_ERR_CUDA;
 }
 
 // Real launch shape (persistent real warps, see ks::choose_launch) and launch.
@@ -336,7 +346,16 @@ int ks_simulate(const ks_module* mod, const char* kernel, uint32_t grid, uint32_
   const int rc = prepare(mod, kernel, grid, block, params, param_bytes, bufs, n_bufs, trace_buf, trace_bytes,
                          stats_buf, stats_bytes, cfg, &L, &di);
   if (rc != KS_OK) return rc;
+  if (clear_profile(L, stream) != KS_OK) return KS_ERR_CUDA;
   return shape_and_launch(L, di, stream);
+}
+
+int ks_profile_bytes(const ks_module* mod, const char* kernel, size_t* bytes) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  if (!bytes) return KS_ERR_ARG;
+  *bytes = k->code.size() * sizeof(ks_pc_profile);
+  return KS_OK;
 }
 
 void ks_cache_config_default(ks_cache_config* cc) {
@@ -383,11 +402,15 @@ int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, 
   L.lat_l2 = cc.lat_l2;
   L.cache_warps = reinterpret_cast<ks_cache_warp*>(ws + C.warps_off);
   L.cache_log = reinterpret_cast<ks_cache_access*>(ws + C.log_off);
-  L.cache_pass = 1;  // log the accesses, stores suppressed
+  ks_pc_profile* profile = L.profile;
+  L.profile = nullptr;  // the first pass counts nothing
+  L.cache_pass = 1;     // log the accesses, stores suppressed
   rc = shape_and_launch(L, di, stream);
   if (rc != KS_OK) return rc;
   if (ks::launch_cache_levels(L, ws, C, cc.l1_lines, cc.l2_lines, stream) != 0) return KS_ERR_CUDA;
   L.cache_pass = 2;  // the real run, latencies from the levels
+  L.profile = profile;
+  if (clear_profile(L, stream) != KS_OK) return KS_ERR_CUDA;
   return shape_and_launch(L, di, stream);
 }
 

@@ -240,6 +240,7 @@ struct KsLaunch {
   uint32_t lat_l1, lat_l2;        // load latency on an L1 / L2 hit
   ks_cache_warp* cache_warps;     // [n_warps]
   ks_cache_access* cache_log;     // [n_warps * cache_cap]
+  ks_pc_profile* profile;         // per-instruction profile, or null
   alignas(16) uint8_t params[KS_MAX_PARAM_BYTES];
 };
 

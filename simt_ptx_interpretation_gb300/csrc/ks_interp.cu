@@ -203,7 +203,7 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 // so that the other kernels keep the register budget of the plain loop. BIG:
 // CTA mode for blocks of 9..32 warps (a 1024-thread real CTA, at most 64
 // registers a thread, so it spills: slower, used only for such blocks).
-template <bool CTA, bool BIG, bool CACHE>
+template <bool CTA, bool BIG, bool INSTR>
 __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __grid_constant__ KsLaunch L) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     // the instructions its warp issued before it)
     uint32_t c_k = 0, c_l1 = 0, c_l2 = 0, c_n = 0;
     uint64_t c_off = 0;
-    if constexpr (CACHE) {
+    if constexpr (INSTR) {
       if (L.cache_pass == 2) {
         c_n = L.cache_warps[gw].n_access;
         if (c_n > L.cache_cap && status == 0) status = KS_ST_CACHE_LOG;
@@ -497,6 +497,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
       }
       // ---- general path: one instruction; every operand / ready-time load at once
       const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q2.x, gneg = q2.y, inc = q1.w;
+      [[maybe_unused]] const uint32_t pc_here = pc;  // the instrumented handlers' program entry
       const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q0.w;
       const uint32_t aux = q0.z;
       const uint2 pa = SM2(lb + A), pb = SM2(lb + B), pcc = SM2(lb + C);
@@ -572,9 +573,9 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
       // cache model: one access per ld/st.global that a lane executes, at the
       // lowest executing lane's line; a load's latency follows the level
       uint32_t wlat = q0.y;
-      if constexpr (CACHE) {
+      if constexpr (INSTR) {
         const uint32_t ex = mask & (pm ^ gneg);
-        if (op >= OP_LDG32 && op <= OP_STG64 && ex != 0u) {
+        if (L.cache_pass != 0u && op >= OP_LDG32 && op <= OP_STG64 && ex != 0u) {
           const uint64_t va_c =
               ((uint64_t)a0 | ((uint64_t)SM32(lb + A + ROW_BYTES) << 32)) + (uint64_t)(int64_t)(int32_t)aux;
           const uint64_t line = __shfl_sync(FULL, va_c, __ffs(ex) - 1) >> 7;
@@ -651,6 +652,15 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
             pc = pc + 1;
           } else {
             FLUSH_THREADS();
+            if (INSTR && L.profile && lane == 0) {  // a divergent branch (hints: divergence ratio)
+              ks_pc_profile* pp = L.profile + pc_here;
+              const uint32_t small = min(__popc(taken), __popc(fall)), act = __popc(mask);
+              atomicAdd(reinterpret_cast<unsigned long long*>(&pp->divergent), 1ull);
+              if (5u * small > 2u * act) {
+                atomicAdd(reinterpret_cast<unsigned long long*>(&pp->high_divergence), 1ull);
+                atomicOr(reinterpret_cast<unsigned long long*>(&pp->high_div_pcts), 1ull << (100u * small / act));
+              }
+            }
             const uint32_t sbase = wb + Y.stack_off;
             uint32_t n = depth;  // entries held in shared memory once the top is resolved
             if (rpc == R) {
@@ -750,18 +760,30 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
           // the lane below starts a new one; otherwise lanes are grouped by value.
           const uint64_t va_up = __shfl_up_sync(FULL, va, 1);
           const bool sorted = exec == FULL && __all_sync(FULL, lane == 0 || va >= va_up);
+          uint32_t lines = 0;
           if (sorted) {
             const uint32_t sectors = 1u + __popc(__ballot_sync(FULL, lane != 0 && (va >> 5) != (va_up >> 5)));
-            const uint32_t lines = 1u + __popc(__ballot_sync(FULL, lane != 0 && (va >> 7) != (va_up >> 7)));
+            lines = 1u + __popc(__ballot_sync(FULL, lane != 0 && (va >> 7) != (va_up >> 7)));
             if (is_ld) { ld_req++; ld_sec += sectors; ld_lin += lines; }
             else { st_req++; st_sec += sectors; st_lin += lines; }
           } else if (exec) {
             const uint32_t ms = __match_any_sync(FULL, on ? (va >> 5) : ~0ull);
             const uint32_t sectors = __popc(__ballot_sync(FULL, on && (uint32_t)(__ffs(ms) - 1) == lane));
             const uint32_t ml = __match_any_sync(FULL, on ? (va >> 7) : ~0ull);
-            const uint32_t lines = __popc(__ballot_sync(FULL, on && (uint32_t)(__ffs(ml) - 1) == lane));
+            lines = __popc(__ballot_sync(FULL, on && (uint32_t)(__ffs(ml) - 1) == lane));
             if (is_ld) { ld_req++; ld_sec += sectors; ld_lin += lines; }
             else { st_req++; st_sec += sectors; st_lin += lines; }
+          }
+          if (INSTR && L.profile && exec && lane == 0) {  // hints: coalescing efficiency min(1, ideal / lines)
+            ks_pc_profile* pp = L.profile + pc_here;
+            const uint32_t ideal = (__popc(exec) * size + 127u) / 128u;
+            atomicAdd(reinterpret_cast<unsigned long long*>(&pp->requests), 1ull);
+            if (4u * ideal < lines) {
+              atomicAdd(reinterpret_cast<unsigned long long*>(&pp->poor), 1ull);
+              atomicOr(&pp->poor_pcts, 1u << (100u * ideal / lines));
+            } else if (2u * ideal < lines) {
+              atomicAdd(reinterpret_cast<unsigned long long*>(&pp->uncoalesced), 1ull);
+            }
           }
           if (is_ld) {
             if (on) {
@@ -779,7 +801,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
             const uint64_t va_dn = __shfl_down_sync(FULL, va, 1);
             const bool wins = sorted ? (lane == 31 || va_dn != va)
                                      : (31u - __clz(__match_any_sync(FULL, on ? va : ~0ull))) == lane;
-            if (on && wins && !(CACHE && L.cache_pass == 1)) {  // the cache model's first pass stores nothing
+            if (on && wins && !(INSTR && L.cache_pass == 1)) {  // the cache model's first pass stores nothing
               if (wide) *reinterpret_cast<uint64_t*>(ptr) = B64();
               else *reinterpret_cast<uint32_t*>(ptr) = b0;
             }
@@ -836,8 +858,16 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
             // other bank its lanes; the request's degree is the largest
             const uint32_t same_bank = __match_any_sync(FULL, on ? ((sva >> 2) & 31u) : (32u + lane));
             const uint32_t deg = (on && same_addr != same_bank) ? (uint32_t)__popc(same_bank) : 1u;
+            const uint32_t degree = __reduce_max_sync(FULL, deg);
             sh_req++;
-            sh_wf += __reduce_max_sync(FULL, deg);
+            sh_wf += degree;
+            if (INSTR && L.profile && lane == 0) {  // hints: bank-conflict degree
+              ks_pc_profile* pp = L.profile + pc_here;
+              atomicAdd(reinterpret_cast<unsigned long long*>(&pp->requests), 1ull);
+              if (degree > 1u) atomicAdd(reinterpret_cast<unsigned long long*>(&pp->conflicted), 1ull);
+              if (degree >= 8u) atomicAdd(reinterpret_cast<unsigned long long*>(&pp->severe), 1ull);
+              atomicOr(&pp->degrees, 1u << (degree - 1u));
+            }
           }
           uint8_t* sp = smem + sh_base + sva;  // dereferenced by executing lanes only
           if (is_ld) {
@@ -974,11 +1004,11 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     if constexpr (!cta_mode) break;
     // ---- barrier round (CTA mode): each warp has stopped at bar.sync or
     // finished; the stopped ones resume at the latest arrival + latency ----
-    if constexpr (CACHE) {
+    if constexpr (INSTR) {
       // the release comes at the end of the step in which the last warp
       // arrived or finished: 1 + the last step issued by those warps
       const uint64_t issued = stop_at - left - budget;
-      if ((at_bar || !finished) && issued != 0 && lane == 0)
+      if (L.cache_pass != 0u && (at_bar || !finished) && issued != 0 && lane == 0)
         atomicMax(&ctl->step_end[round & 1u], (unsigned long long)(c_off + issued));
     }
     if (!at_bar && !finished) {
@@ -989,17 +1019,17 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     if (at_bar && lane == 0) atomicMax(&ctl->latest[round & 1u], (unsigned long long)(epoch + t_last));
     __syncthreads();
     const unsigned long long latest = ctl->latest[round & 1u];
-    const unsigned long long step_end = CACHE ? ctl->step_end[round & 1u] : 0ull;
+    const unsigned long long step_end = INSTR ? ctl->step_end[round & 1u] : 0ull;
     const bool all_done = ctl->done == nwarps;
     if (threadIdx.x == 0) {  // last read two rounds ago
       ctl->latest[(round + 1u) & 1u] = 0ull;
-      if (CACHE) ctl->step_end[(round + 1u) & 1u] = 0ull;
+      if (INSTR) ctl->step_end[(round + 1u) & 1u] = 0ull;
     }
     __syncthreads();
     if (all_done) break;
     if (at_bar) {
       at_bar = false;
-      if constexpr (CACHE) c_off = step_end - (stop_at - left - budget);
+      if constexpr (INSTR) c_off = step_end - (stop_at - left - budget);
       const uint64_t rel = (uint64_t)latest + L.lat[KS_LAT_BAR] - epoch;
       if (rel < REBASE_AT) {
         t_next = (uint32_t)rel;
@@ -1029,9 +1059,9 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     }  // barrier rounds
 #undef FLUSH_THREADS
     const uint64_t warp_insts = stop_at - left - budget;
-    if constexpr (CACHE) {
+    if constexpr (INSTR) {
       if (L.cache_pass == 2 && status == 0 && c_k != c_n) status = KS_ST_CACHE_STREAM;
-      if (lane == 0) {
+      if (L.cache_pass != 0u && lane == 0) {
         ks_cache_warp cw;
         cw.n_access = c_k;
         cw.l1_hits = c_l1;
@@ -1124,13 +1154,16 @@ size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t w
 static int g_attr_done[64];
 
 // The instantiation that runs a launch: CTA mode (9..32 warps: the 1024-thread
-// form), and the cache model's two passes.
-static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, bool cache) {
-  if (!cta) return cache ? (const void*)ks_interp_kernel<false, false, true> : (const void*)ks_interp_kernel<false, false, false>;
+// form), and the instrumented form for the cache model's passes and the
+// per-instruction profile (the lean forms carry neither).
+static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, bool instr) {
+  if (!cta) return instr ? (const void*)ks_interp_kernel<false, false, true> : (const void*)ks_interp_kernel<false, false, false>;
   if (real_warps_per_cta > 8)
-    return cache ? (const void*)ks_interp_kernel<true, true, true> : (const void*)ks_interp_kernel<true, true, false>;
-  return cache ? (const void*)ks_interp_kernel<true, false, true> : (const void*)ks_interp_kernel<true, false, false>;
+    return instr ? (const void*)ks_interp_kernel<true, true, true> : (const void*)ks_interp_kernel<true, true, false>;
+  return instr ? (const void*)ks_interp_kernel<true, false, true> : (const void*)ks_interp_kernel<true, false, false>;
 }
+
+static bool instrumented(const KsLaunch& L) { return L.cache_pass != 0 || L.profile != nullptr; }
 
 static int ensure_attr() {
   int dev = 0;
@@ -1142,9 +1175,9 @@ static int ensure_attr() {
   if (e != cudaSuccess) return (int)e;
   for (int cta = 0; cta < 2; cta++)
     for (int big = 0; big < 2; big++)
-      for (int cache = 0; cache < 2; cache++) {
+      for (int instr = 0; instr < 2; instr++) {
         if (!cta && big) continue;
-        e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, cache), cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, instr), cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         if (e != cudaSuccess) return (int)e;
       }
   if (dev < 64) g_attr_done[dev] = 1;
@@ -1154,7 +1187,7 @@ static int ensure_attr() {
 int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm) {
   int e = ensure_attr();
   if (e) return e;
-  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, L.cache_pass != 0);
+  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, instrumented(L));
   return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, (int)(real_warps_per_cta * 32), smem);
 }
 
@@ -1209,7 +1242,7 @@ int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_
   const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, real_warps_per_cta,
                                        L.cta_mode ? L.shared_bytes : 0u);
   void* args[] = {const_cast<KsLaunch*>(&L)};
-  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, real_warps_per_cta, L.cache_pass != 0), dim3(real_ctas),
+  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, real_warps_per_cta, instrumented(L)), dim3(real_ctas),
                                dim3(real_warps_per_cta * 32), args, smem, (cudaStream_t)stream);
 }
 

@@ -1,9 +1,12 @@
 // ks_post.cpp — host post-passes of the C ABI: the occupancy calculator
-// (KernelScope backend doc, occupancy/calculator.py) and the trace export.
+// (KernelScope backend doc, occupancy/calculator.py), the trace export and the
+// hints (hints/analyzer.py).
 #include <algorithm>
+#include <charconv>
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "ks_internal.h"
 
@@ -28,9 +31,90 @@ const NamedLimits kLimits[] = {
     {"sm_103", {2048, 64, 32, 65536, 233472}},
 };
 
+void put_text(char* dst, size_t cap, const std::string& text) {
+  const size_t n = std::min(text.size(), cap - 1);
+  std::memcpy(dst, text.data(), n);
+  dst[n] = 0;
+}
+
+// A double as Python prints it here: the shortest decimal that reads back as
+// the same value, with ".0" when that has no fraction part (values 0..100).
+std::string shortest(double v) {
+  char buf[64];
+  const auto r = std::to_chars(buf, buf + sizeof buf, v);
+  std::string t(buf, r.ptr);
+  if (t.find_first_of(".e") == std::string::npos) t += ".0";
+  return t;
+}
+
+uint32_t highest_bit(uint64_t m) { return 63u - (uint32_t)__builtin_clzll(m); }
+uint32_t lowest_bit(uint64_t m) { return (uint32_t)__builtin_ctzll(m); }
+
 }  // namespace
 
 extern "C" {
+
+int ks_hints(const ks_pc_profile* profile, uint32_t n_entries, const ks_occupancy_result* occupancy,
+             ks_hint* out, uint32_t cap, uint32_t* n_hints) {
+  if (!n_hints || (n_entries && !profile)) return KS_ERR_ARG;
+  std::vector<ks_hint> h;
+  auto add = [&](int cat, int sev, int pc, uint64_t count, const std::string& msg, const std::string& detail) {
+    ks_hint x;
+    std::memset(&x, 0, sizeof x);
+    x.category = cat;
+    x.severity = sev;
+    x.pc = pc;
+    x.count = count;
+    put_text(x.message, sizeof x.message, msg);
+    put_text(x.detail, sizeof x.detail, detail);
+    h.push_back(x);
+  };
+  uint64_t bank_events = 0, divergent_events = 0;
+  for (uint32_t pc = 0; pc < n_entries; pc++) {
+    const ks_pc_profile& p = profile[pc];
+    bank_events += p.conflicted;
+    divergent_events += p.divergent;
+    if (p.severe)
+      add(KS_HINT_MEMORY, KS_HINT_CRITICAL, (int)pc, p.severe, std::to_string(highest_bit(p.degrees) + 1) +
+          "-way bank conflict", "Severe bank conflict causing serialized access");
+    const uint32_t mild = p.degrees & 0x7Eu;  // degrees 2..7
+    if (p.conflicted > p.severe && mild)
+      add(KS_HINT_MEMORY, KS_HINT_WARNING, (int)pc, p.conflicted - p.severe,
+          std::to_string(highest_bit(mild) + 1) + "-way bank conflict", "Bank conflict reducing throughput");
+    if (p.poor && p.poor_pcts)
+      add(KS_HINT_MEMORY, KS_HINT_CRITICAL, (int)pc, p.poor,
+          "Poor memory efficiency (" + std::to_string(lowest_bit(p.poor_pcts)) + "%)",
+          "Scattered access causing many transactions");
+    if (p.high_divergence && p.high_div_pcts)
+      add(KS_HINT_DIVERGENCE, KS_HINT_WARNING, (int)pc, p.high_divergence,
+          "High divergence (" + std::to_string(highest_bit(p.high_div_pcts)) + "%)",
+          "Significant warp divergence at this branch");
+  }
+  if (bank_events > 5)
+    add(KS_HINT_MEMORY, KS_HINT_WARNING, -1, bank_events,
+        "Shared memory bank conflicts (" + std::to_string(bank_events) + " events)",
+        "Consider padding arrays or restructuring access patterns");
+  if (divergent_events > 3)
+    add(KS_HINT_DIVERGENCE, KS_HINT_WARNING, -1, divergent_events,
+        "Branch divergence detected (" + std::to_string(divergent_events) + " events)",
+        "Consider restructuring conditionals or using predication");
+  if (occupancy) {
+    static const char* const kNames[] = {"registers", "shared_memory", "block_size"};
+    const int li = occupancy->limiter;
+    const std::string lim = (li >= 0 && li < 3) ? kNames[li] : "";
+    const double pct = occupancy->occupancy_percent;
+    if (pct < 25)
+      add(KS_HINT_OCCUPANCY, KS_HINT_CRITICAL, -1, 1, "Very low occupancy (" + shortest(pct) + "%)",
+          "Limited by " + lim + ". Consider reducing resource usage.");
+    else if (pct < 50)
+      add(KS_HINT_OCCUPANCY, KS_HINT_WARNING, -1, 1, "Low occupancy (" + shortest(pct) + "%)",
+          "Limited by " + lim + ".");
+  }
+  *n_hints = (uint32_t)h.size();
+  if (!out || cap < h.size()) return h.empty() ? KS_OK : KS_ERR_ARG;
+  std::copy(h.begin(), h.end(), out);
+  return KS_OK;
+}
 
 int ks_gpu_limits_of(const char* arch, ks_gpu_limits* out) {
   if (!arch || !out) return KS_ERR_ARG;

@@ -81,6 +81,7 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
   // shared memory / bar.sync: every warp of a CTA resident on one real CTA
   if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
+  if (cfg.profile_buf && cfg.profile_bytes < k->code.size() * sizeof(ks_pc_profile)) return KS_ERR_ARG;
   // ---- the program image must fit the static array ----
   if (k->image.size() > KS_STATIC_IMAGE_BYTES) return KS_ERR_LIMIT;
 
@@ -129,6 +130,10 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   L.stats = static_cast<uint8_t*>(stats_buf);
   L.param_bytes = (uint32_t)param_bytes;
   if (param_bytes) std::memcpy(L.params, params, param_bytes);
+  L.profile = static_cast<ks_pc_profile*>(cfg.profile_buf);
+  if (L.profile && cudaMemsetAsync(L.profile, 0, k->code.size() * sizeof(ks_pc_profile),
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KS_ERR_CUDA;
 
   uint32_t wpc_real = 0, ctas = 0;
   const int shape = ks::choose_launch(L, g_static_sms[dev], g_static_smem[dev], &wpc_real, &ctas);
