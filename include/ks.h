@@ -110,6 +110,8 @@ extern "C" {
                                 log holds, or an access step reached 2^32 - 1 */
 #define KS_ST_CACHE_STREAM 8 /* cache model: the second pass's global accesses differ
                                 from the first pass's (see ks_simulate_cached) */
+#define KS_ST_SCHED_LIMIT 9  /* SM issue model: a warp's issue log is full, or an SM's
+                                clock reached 2^31 (see ks_simulate_sched) */
 
 /* ---- latency classes (index of ks_config.lat) --------------------------- */
 #define KS_NUM_LAT_CLASSES 12
@@ -418,6 +420,79 @@ int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, 
                        void* trace_buf, size_t trace_bytes, void* stats_buf, size_t stats_bytes,
                        const ks_config* cfg, const ks_cache_config* cc, void* workspace,
                        size_t workspace_bytes, void* stream);
+
+/* ---- SM-level issue model (KernelScope backend doc, simulator/engine.py and
+ * simulator/models.py — WarpStallReason, _determine_stall_reason,
+ * WarpScheduleInfo) ------------------------------------------------------------
+ * The launch's warps share simulated SMs: CTA c runs on SM c % n_sm; an SM
+ * holds ctas_per_sm CTAs at once (at most 32 warps) and starts its next CTA in
+ * a slot when the slot's CTA has finished (the latest end of its warps). Warp
+ * slot i of an SM issues on scheduler i % schedulers_per_sm; a scheduler issues
+ * at most one instruction per cycle, to the ready warp with the lowest global
+ * warp id (the order of the page's step()). A warp is ready when the in-order
+ * scoreboard of the per-warp model lets it issue; the per-warp rules stay as
+ * they are (latencies, barriers, the store drain), with absolute cycles from
+ * the SM's cycle 0. Cycles a warp waits are counted by what it waits for: the
+ * scheduler picked another ready warp ("not selected"); a result of a load
+ * (ld.global / ld.shared: "memory dependency"), of div/sqrt ("math pipe"), of
+ * anything else or a branch's latency ("execution dependency"; when results of
+ * several kinds arrive in the same cycle the load counts first, then div/sqrt);
+ * a barrier's release ("barrier"). Per warp: start + issued + the waits + the
+ * drain after its last issue = end. Not modelled: the page's memory throttle
+ * (a bound on memory requests in flight across the whole simulator) and its
+ * divergence stall (serialised paths already issue one after the other). */
+typedef struct {
+  uint32_t n_sm;              /* simulated SMs (default 152) */
+  uint32_t ctas_per_sm;       /* resident CTAs per SM, ctas_per_sm * ceil(block / 32) <= 32;
+                                 0 = as many as fit in 32 warps (default 0) */
+  uint32_t schedulers_per_sm; /* 1, 2 or 4 (default 4) */
+  uint32_t max_runs_per_warp; /* issue-log capacity: runs of consecutive program entries
+                                 a warp consumes between control transfers (default 4096) */
+  uint32_t reserved[4];
+} ks_sched_config;
+
+/* Per-warp schedule record (64 bytes), indexed by global warp id. */
+typedef struct {
+  uint64_t start, end;     /* the SM cycles at which the warp's CTA started, and its last
+                              result or store completed */
+  uint64_t issued;         /* instructions issued (= ks_warp_stats.warp_insts) */
+  uint64_t not_selected;   /* ready, another warp of the scheduler issued */
+  uint64_t stall_exec;     /* waiting on an ALU / FMA result or a branch's latency */
+  uint64_t stall_mem;      /* waiting on a load's result */
+  uint64_t stall_math;     /* waiting on a div / sqrt result */
+  uint64_t stall_barrier;  /* waiting at bar.sync for the release */
+} ks_sched_warp;
+
+/* Per-SM record (32 bytes). */
+typedef struct {
+  uint64_t cycles;  /* the SM's last warp end (0 without CTAs) */
+  uint64_t issued;  /* instructions its warps issued: IPC = issued / cycles */
+  uint64_t ctas;    /* CTAs it ran */
+  int32_t status;   /* 0 or KS_ST_SCHED_LIMIT */
+  uint32_t reserved;
+} ks_sched_sm;
+
+void ks_sched_config_default(ks_sched_config* sc);
+
+/* Device workspace of ks_simulate_sched (the issue log): W * (4 *
+ * max_runs_per_warp + 4) bytes rounded up; 0 for an invalid configuration. */
+size_t ks_sched_workspace_bytes(uint32_t grid, uint32_t block, const ks_sched_config* sc);
+
+/* ks_simulate plus the SM-level issue model. The interpreter runs once (its
+ * outputs are those of ks_simulate) and logs each warp's issued program
+ * entries; a replay kernel then schedules the SMs. sched_warps: device, W
+ * ks_sched_warp records; sched_sms: device, n_sm ks_sched_sm records;
+ * workspace: device, ks_sched_workspace_bytes. KS_ERR_ARG for an invalid sc
+ * or undersized buffers, KS_ERR_LIMIT when a replay's shared memory (the
+ * program plus a ready table per warp slot) does not fit. Enqueues on `stream`
+ * and returns. A warp whose issue log overflows ends with KS_ST_SCHED_LIMIT in
+ * its stats, and its SM's record carries the same status. */
+int ks_simulate_sched(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block,
+                      const void* params, size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs,
+                      void* trace_buf, size_t trace_bytes, void* stats_buf, size_t stats_bytes,
+                      const ks_config* cfg, const ks_sched_config* sc, void* sched_warps,
+                      size_t sched_warps_bytes, void* sched_sms, size_t sched_sms_bytes, void* workspace,
+                      size_t workspace_bytes, void* stream);
 
 /* ---- host post-pass: occupancy (KernelScope backend doc,
  * occupancy/calculator.py — calculate_occupancy) ----------------------------

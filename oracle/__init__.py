@@ -154,6 +154,13 @@ def _load():
             ctypes.POINTER(_Config), ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32),
             ctypes.c_void_p, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64), ctypes.c_char_p, ctypes.c_uint64,
         ]
+        lib.orc_run_sched.restype = ctypes.c_int
+        lib.orc_run_sched.argtypes = [
+            ctypes.c_char_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
+            ctypes.c_void_p, ctypes.c_uint64, ctypes.POINTER(_Buffer), ctypes.c_uint32,
+            ctypes.POINTER(_Config), ctypes.POINTER(ctypes.c_uint32 * 3), ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_char_p, ctypes.c_uint64,
+        ]
         lib.orc_ipdom.restype = ctypes.c_int
         lib.orc_ipdom.argtypes = [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                   ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32), ctypes.c_char_p,
@@ -289,6 +296,48 @@ def run_events(ptx: str, kernel: str, grid: int, block: int, params: bytes, buff
     if rc != 0:
         raise OracleError(rc, err.value.decode(errors="replace"))
     return Result(stats=stats, trace=None, status=status.value, race_flags=0), ev
+
+
+# SM issue model outputs (orc_run_sched)
+SCHED_WARP_DTYPE = np.dtype([("start", "<u8"), ("end", "<u8"), ("issued", "<u8"), ("not_selected", "<u8"),
+                             ("stall_exec", "<u8"), ("stall_mem", "<u8"), ("stall_math", "<u8"),
+                             ("stall_barrier", "<u8")])
+SCHED_SM_DTYPE = np.dtype([("cycles", "<u8"), ("issued", "<u8"), ("ctas", "<u8"), ("status", "<i4"),
+                           ("reserved", "<u4")])
+
+
+def run_sched(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffers, *, lat=DEFAULT_LAT,
+              n_sm: int = 152, ctas_per_sm: int = 0, schedulers: int = 4, step_limit: int = 1 << 26):
+    """The SM issue model, cycle by cycle on one host thread: (per-warp
+    SCHED_WARP_DTYPE records, per-SM SCHED_SM_DTYPE records). Buffers are
+    updated in place."""
+    lib = _load()
+    W = grid * ((block + 31) // 32)
+    bufs = (_Buffer * max(1, len(buffers)))()
+    keep = []
+    for i, (base, arr) in enumerate(buffers):
+        keep.append(arr)
+        bufs[i].sim_base = base
+        bufs[i].host = arr.ctypes.data
+        bufs[i].bytes = arr.nbytes
+    cfg = _Config()
+    for i in range(12):
+        cfg.lat[i] = lat[i] if i < len(lat) else 0
+    cfg.stack_depth = 32
+    cfg.step_limit = step_limit
+    cfg.inject_warp = -1
+    cfg.mode = MODE_WARP
+    sc = (ctypes.c_uint32 * 3)(n_sm, ctas_per_sm, schedulers)
+    warps = np.zeros(W, dtype=SCHED_WARP_DTYPE)
+    sms = np.zeros(n_sm, dtype=SCHED_SM_DTYPE)
+    pbuf = ctypes.create_string_buffer(bytes(params), max(1, len(params)))
+    err = ctypes.create_string_buffer(512)
+    rc = lib.orc_run_sched(ptx.encode(), kernel.encode(), grid, block, ctypes.cast(pbuf, ctypes.c_void_p),
+                           len(params), bufs, len(buffers), ctypes.byref(cfg), ctypes.byref(sc), warps.ctypes.data,
+                           sms.ctypes.data, err, len(err))
+    if rc != 0:
+        raise OracleError(rc, err.value.decode(errors="replace"))
+    return warps, sms
 
 
 @dataclass

@@ -1365,7 +1365,12 @@ uint32_t bank_degree(const uint64_t* addr, uint32_t exec) {
 struct Entry { int pc, rpc; uint32_t mask; };
 
 // What WarpRun::run stopped on.
-enum { RUN_DONE = 0, RUN_BAR = 1, RUN_STEP = 2 };
+enum { RUN_DONE = 0, RUN_BAR = 1, RUN_STEP = 2, RUN_PEEK = 3 };
+
+// What a warp's next instruction waits for, by the kind of result that
+// arrives last (SM issue model): a load's, a div/sqrt's, or any other
+// (including a branch's latency); loads count first, then div/sqrt.
+enum { WAIT_EXEC = 0, WAIT_MATH = 1, WAIT_MEM = 2 };
 
 // One simulated warp, resumable at barriers (and, for the cache model, after
 // every instruction).
@@ -1382,6 +1387,10 @@ struct WarpRun {
   std::vector<std::pair<uint32_t, uint64_t>> records;  // (id << 24 | ts, payload)
   uint64_t step = 0;                  // cache model: the step of the next instruction
   std::vector<CacheAccess> accesses;  // cache model: this warp's accesses in order
+  uint64_t floor = 0;                 // SM issue model: the cycle its scheduler issues it at
+  std::vector<int> rkind;             // SM issue model: WAIT_* kind of each register's producer
+  uint64_t peek_e = 0;                // SM issue model: scoreboard time of the next instruction
+  int peek_kind = WAIT_EXEC;          //                 and what binds it
 
   WarpRun(const Launch& L, uint32_t gw) : X(&L), gwarp(gw) {
     const Kernel& K = *X->K;
@@ -1397,6 +1406,7 @@ struct WarpRun {
     }
     stack.push_back(Entry{0, (int)K.code.size(), mask0});
     ready.assign(K.regs.size(), 0);
+    rkind.assign(K.regs.size(), WAIT_EXEC);
     std::memset(&st, 0, sizeof st);
     st.max_stack_depth = 1;
   }
@@ -1406,7 +1416,7 @@ struct WarpRun {
   // second instruction would issue (RUN_STEP); a call that issues the
   // warp's last instruction returns RUN_DONE, so a warp is done in the step of
   // its last instruction.
-  int run(Memory& M, CtaMem* S, uint64_t* arrival, bool one_step = false) {
+  int run(Memory& M, CtaMem* S, uint64_t* arrival, bool one_step = false, bool peek = false) {
     const Kernel& K = *X->K;
     const orc_config& cfg = *X->cfg;
     const int n = (int)K.code.size();
@@ -1438,6 +1448,23 @@ struct WarpRun {
         return RUN_DONE;
       }
       if (st.warp_insts == cfg.step_limit) { st.status = ORC_ST_STEP_LIMIT; return RUN_DONE; }
+      if (peek) {  // the next instruction's scoreboard time, without issuing it
+        std::vector<int> regs;
+        auto use = [&](const Opnd& o) { if ((o.k == Opnd::REG || o.k == Opnd::MEM) && o.reg >= 0) regs.push_back(o.reg); };
+        if (in.k == K_STG || in.k == K_STS) { use(in.a); use(in.b); }
+        else if (in.k != K_BRA && in.k != K_RET && in.k != K_BAR) {
+          use(in.a); use(in.b); use(in.c);
+          regs.push_back(in.d.reg);
+        }
+        if (in.guard >= 0) regs.push_back(in.guard);
+        uint64_t e = t_next;
+        for (int r : regs) e = std::max(e, ready[(size_t)r]);
+        int kind = WAIT_EXEC;
+        for (int r : regs) if (ready[(size_t)r] == e) kind = std::max(kind, rkind[(size_t)r]);
+        peek_e = e;
+        peek_kind = kind;
+        return RUN_PEEK;
+      }
       issued = true;
 
       // ---- guard ----
@@ -1474,7 +1501,13 @@ struct WarpRun {
       uint64_t t = t_next;
       for (int r : srcs) t = std::max(t, ready[(size_t)r]);
       for (int r : dsts) t = std::max(t, ready[(size_t)r]);
-      for (int r : dsts) { ready[(size_t)r] = t + lat; max_ready = std::max(max_ready, t + lat); }
+      t = std::max(t, floor);
+      const int produced = (in.k == K_LDG || in.k == K_LDS) ? WAIT_MEM : in.cls == ORC_LAT_SFU ? WAIT_MATH : WAIT_EXEC;
+      for (int r : dsts) {
+        ready[(size_t)r] = t + lat;
+        rkind[(size_t)r] = produced;
+        max_ready = std::max(max_ready, t + lat);
+      }
       if (in.k == K_STG || in.k == K_STS) drain = std::max(drain, t + lat);
       t_last = t;
       t_next = (in.k == K_BRA || in.k == K_RET) ? t + lat : t + 1;
@@ -1723,6 +1756,147 @@ void run_stepped(const Launch& X, Memory& M) {
   }
   for (const WarpRun& w : ws) w.write_back();
   for (const CtaMem& S : shared) M.race_flags |= S.race_flags;
+}
+
+// ------------------------------------------------- SM issue model ----
+// Each SM cycle by cycle: CTA c runs on SM c % n_sm, ctas_per_sm of them at
+// once, the next one starting in a slot when the slot's CTA has finished (the
+// latest end of its warps); warp slot i issues on scheduler i % schedulers;
+// every cycle each scheduler issues one instruction of its ready warp with
+// the lowest global warp id, if any (the page's step() order). A warp is ready
+// when its in-order scoreboard lets it issue (peek); it then issues at this
+// cycle (floor). Waits are counted by what the warp waited for.
+struct SchedWarp {
+  std::unique_ptr<WarpRun> w;
+  int state = 0;  // 0 empty, 1 running, 2 waiting, 3 done
+  uint64_t start = 0, end = 0, base = 0, arrival = 0;
+  uint64_t not_selected = 0, stall[3] = {0, 0, 0}, stall_bar = 0;
+};
+
+void run_sm_model(const Launch& X, Memory& M, uint32_t n_sm, uint32_t ctas_per_sm, uint32_t schedulers,
+                  uint8_t* warps_out, uint8_t* sms_out) {
+  const Kernel& K = *X.K;
+  const uint32_t wpc = X.warps_per_cta;
+  enum { EMPTY, RUNNING, WAITING, DONE };
+  for (uint32_t sm = 0; sm < n_sm; sm++) {
+    std::vector<SchedWarp> slot(ctas_per_sm * wpc);
+    std::vector<std::unique_ptr<CtaMem>> smem(ctas_per_sm);
+    uint32_t next_k = 0;
+    uint64_t sm_end = 0, sm_issued = 0, ctas = 0;
+    auto finish = [&](SchedWarp& q) {
+      q.state = DONE;
+      q.end = q.w->st.warp_insts ? std::max(std::max(q.w->t_last + 1, q.w->max_ready), q.w->drain) : q.start;
+      uint8_t* r = warps_out + (uint64_t)q.w->gwarp * 64;
+      const uint64_t v[8] = {q.start, q.end, q.w->st.warp_insts, q.not_selected, q.stall[WAIT_EXEC],
+                             q.stall[WAIT_MEM], q.stall[WAIT_MATH], q.stall_bar};
+      for (int i = 0; i < 8; i++) store_le(r + 8 * i, v[i], 8);
+      sm_end = std::max(sm_end, q.end);
+      sm_issued += q.w->st.warp_insts;
+    };
+    auto peek = [&](SchedWarp& q) {  // no memory access before the issue
+      uint64_t arr = 0;
+      if (q.w->run(M, nullptr, &arr, true, true) == RUN_PEEK) q.state = RUNNING;
+      else finish(q);
+    };
+    auto start_cta = [&](uint32_t c, uint64_t t0) {
+      const uint64_t cta = sm + (uint64_t)(next_k++) * n_sm;
+      for (uint32_t i = 0; i < wpc; i++) slot[c * wpc + i] = SchedWarp();
+      if (cta >= X.grid) return;
+      smem[c].reset(K.cta_mode() ? new CtaMem(K.shared_bytes, M.race_on) : nullptr);
+      for (uint32_t i = 0; i < wpc; i++) {
+        SchedWarp& q = slot[c * wpc + i];
+        q.w.reset(new WarpRun(X, (uint32_t)cta * wpc + i));
+        q.w->t_next = t0;
+        q.start = q.base = t0;
+        q.state = RUNNING;
+        peek(q);
+      }
+    };
+    // release a barrier nobody runs towards; start the next CTA in a finished slot
+    auto settle = [&](uint32_t c) {
+      for (;;) {
+        bool running = false, waiting = false, any = false;
+        uint64_t latest = 0, fin = 0;
+        for (uint32_t i = 0; i < wpc; i++) {
+          const SchedWarp& q = slot[c * wpc + i];
+          if (q.state == EMPTY) continue;
+          any = true;
+          running |= q.state == RUNNING;
+          if (q.state == WAITING) { waiting = true; latest = std::max(latest, q.arrival); }
+          if (q.state == DONE) fin = std::max(fin, q.end);
+        }
+        if (!any || running) return;
+        if (waiting) {
+          const uint64_t rel = latest + X.cfg->lat[ORC_LAT_BAR];
+          for (uint32_t i = 0; i < wpc; i++) {
+            SchedWarp& q = slot[c * wpc + i];
+            if (q.state != WAITING) continue;
+            q.stall_bar += rel - (q.arrival + 1);
+            q.w->t_next = rel;
+            q.base = rel;
+            peek(q);
+          }
+          if (smem[c]) smem[c]->new_interval();
+          continue;
+        }
+        if (smem[c]) M.race_flags |= smem[c]->race_flags;
+        ctas++;
+        start_cta(c, fin);
+      }
+    };
+    for (uint32_t c = 0; c < ctas_per_sm; c++) {
+      start_cta(c, 0);
+      settle(c);
+    }
+    for (uint64_t cycle = 0;;) {
+      bool live = false;
+      for (uint32_t sch = 0; sch < schedulers; sch++) {
+        SchedWarp* pick = nullptr;
+        for (uint32_t i = sch; i < slot.size(); i += schedulers) {
+          SchedWarp& q = slot[i];
+          if (q.state == RUNNING || q.state == WAITING) live = true;
+          if (q.state != RUNNING) continue;
+          if (q.w->peek_e > cycle) continue;
+          if (!pick || q.w->gwarp < pick->w->gwarp) pick = &q;
+        }
+        if (!pick) continue;
+        SchedWarp& q = *pick;
+        const uint32_t c = (uint32_t)((&q - slot.data()) / wpc);
+        q.not_selected += cycle - q.w->peek_e;
+        if (q.w->peek_e > q.base) q.stall[q.w->peek_kind] += q.w->peek_e - q.base;
+        q.w->floor = cycle;
+        uint64_t arr = 0;
+        const int r = q.w->run(M, smem[c].get(), &arr, true);
+        q.base = cycle + 1;
+        if (r == RUN_BAR) {
+          q.state = WAITING;
+          q.arrival = arr;
+          settle(c);
+        } else if (r == RUN_STEP) {
+          peek(q);
+          if (q.state == DONE) settle(c);
+        } else {
+          finish(q);
+          settle(c);
+        }
+      }
+      if (!live) break;
+      // the next cycle at which some warp can issue
+      uint64_t soonest = UINT64_MAX;
+      for (const SchedWarp& q : slot)
+        if (q.state == RUNNING) soonest = std::min(soonest, std::max(q.w->peek_e, cycle + 1));
+      if (soonest == UINT64_MAX) {
+        bool any = false;
+        for (const SchedWarp& q : slot) any |= q.state == RUNNING || q.state == WAITING;
+        if (!any) break;
+        soonest = cycle + 1;
+      }
+      cycle = soonest;
+    }
+    const uint64_t v[3] = {sm_end, sm_issued, ctas};
+    for (int i = 0; i < 3; i++) store_le(sms_out + (uint64_t)sm * 32 + 8 * i, v[i], 8);
+    store_le(sms_out + (uint64_t)sm * 32 + 24, 0, 8);
+  }
 }
 
 // ---------------------------------------------------- per-thread mode ----
@@ -2029,6 +2203,47 @@ int orc_run_events(const char* ptx, const char* kernel, uint32_t grid, uint32_t 
   if (rc == ORC_OK && events)
     std::memcpy(events, ev.data(), std::min<uint64_t>(ev.size(), events_cap) * sizeof(HintEvent));
   return rc;
+}
+
+int orc_run_sched(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+                  const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+                  uint32_t n_bufs, const orc_config* cfg, const orc_sched* sched, void* sched_warps,
+                  void* sched_sms, char* err, uint64_t errlen) {
+  if (!sched || !sched_warps || !sched_sms) {
+    copy_err("null argument", err, errlen);
+    return ORC_ERR_ARG;
+  }
+  try {
+    if (!ptx || !kernel || !cfg) throw OracleError{ORC_ERR_ARG, "null argument"};
+    if (grid == 0 || block == 0 || block > 1024) throw OracleError{ORC_ERR_ARG, "bad launch shape"};
+    const uint32_t wpc = (block + 31) / 32;
+    const uint32_t ctas = sched->ctas_per_sm ? sched->ctas_per_sm : 32 / wpc;
+    if (sched->n_sm == 0 || ctas == 0 || ctas * wpc > 32 ||
+        !(sched->schedulers == 1 || sched->schedulers == 2 || sched->schedulers == 4))
+      throw OracleError{ORC_ERR_ARG, "bad schedule configuration"};
+    Kernel K = load(std::string(ptx), std::string(kernel));
+    if (param_bytes < K.param_bytes || (K.param_bytes && !params)) throw OracleError{ORC_ERR_ARG, "parameter block too small"};
+    Launch X;
+    X.K = &K;
+    X.grid = grid;
+    X.block = block;
+    X.warps_per_cta = wpc;
+    X.params = (const uint8_t*)params;
+    X.cfg = cfg;
+    std::vector<uint8_t> stats((size_t)grid * wpc * sizeof(orc_warp_stats));
+    X.stats = stats.data();
+    X.trace = nullptr;
+    X.slot_bytes = 0;
+    Memory M;
+    M.bufs = bufs;
+    M.n = n_bufs;
+    run_sm_model(X, M, sched->n_sm, ctas, sched->schedulers, (uint8_t*)sched_warps, (uint8_t*)sched_sms);
+    copy_err("", err, errlen);
+    return ORC_OK;
+  } catch (const OracleError& e) {
+    copy_err(e.msg, err, errlen);
+    return e.code;
+  }
 }
 
 int orc_run_cached(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,

@@ -167,6 +167,25 @@ int orc_run_events(const char* ptx, const char* kernel, uint32_t grid, uint32_t 
                    int32_t* status, void* events, uint64_t events_cap, uint64_t* n_events,
                    char* err, uint64_t errlen);
 
+/* SM-level issue model (KernelScope backend doc, simulator/engine.py and
+ * simulator/models.py — WarpStallReason, WarpScheduleInfo), simulated cycle
+ * by cycle: CTA c on SM c % n_sm, ctas_per_sm resident CTAs per SM (0 = as
+ * many as fit in 32 warps) with the next CTA starting in a slot when the
+ * slot's CTA has finished; warp slot i on scheduler i % schedulers; each cycle
+ * each scheduler issues for its ready warp with the lowest global warp id.
+ * Writes one 64-byte record per warp {start, end, issued, not_selected,
+ * stall_exec, stall_mem, stall_math, stall_barrier} (u64 each) and one 32-byte
+ * record per SM {cycles, issued, ctas, 0}. Memory is updated; per-warp
+ * statistics and traces are not written. */
+typedef struct {
+  uint32_t n_sm, ctas_per_sm, schedulers;
+} orc_sched;
+
+int orc_run_sched(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
+                  const void* params, uint64_t param_bytes, const orc_buffer* bufs,
+                  uint32_t n_bufs, const orc_config* cfg, const orc_sched* sched, void* sched_warps,
+                  void* sched_sms, char* err, uint64_t errlen);
+
 /* Immediate post-dominator of every program entry (instructions and trace
  * pseudo-ops, in program order); the virtual exit is n (= *n_out). */
 int orc_ipdom(const char* ptx, const char* kernel, int32_t* out, uint32_t cap,

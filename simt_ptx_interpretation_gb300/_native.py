@@ -55,6 +55,11 @@ class KsCacheConfig(ctypes.Structure):
                 ("reserved", ctypes.c_uint32 * 3)]
 
 
+class KsSchedConfig(ctypes.Structure):
+    _fields_ = [("n_sm", ctypes.c_uint32), ("ctas_per_sm", ctypes.c_uint32), ("schedulers_per_sm", ctypes.c_uint32),
+                ("max_runs_per_warp", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 4)]
+
+
 class KsHint(ctypes.Structure):
     _fields_ = [("category", ctypes.c_int32), ("severity", ctypes.c_int32), ("pc", ctypes.c_int32),
                 ("reserved", ctypes.c_uint32), ("count", ctypes.c_uint64), ("message", ctypes.c_char * 64),
@@ -104,6 +109,14 @@ EXPORTS = {
     "ks_profile_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_size_t)]),
     "ks_hints": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.POINTER(KsOccupancy), ctypes.POINTER(KsHint),
                                 ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
+    "ks_sched_config_default": (None, [ctypes.POINTER(KsSchedConfig)]),
+    "ks_sched_workspace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.POINTER(KsSchedConfig)]),
+    "ks_simulate_sched": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
+                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(KsBuffer), ctypes.c_uint32,
+                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t,
+                                         ctypes.POINTER(KsConfig), ctypes.POINTER(KsSchedConfig), ctypes.c_void_p,
+                                         ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                         ctypes.c_size_t, ctypes.c_void_p]),
     "ks_read_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.POINTER(KsTotals)]),
     "ks_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }

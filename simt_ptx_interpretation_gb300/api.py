@@ -23,7 +23,14 @@ STATS_DTYPE = np.dtype(
 DEFAULT_LAT = (4, 4, 400, 20, 8, 36, 1, 23, 23, 20, 0, 0)
 
 ST_OOB, ST_MISALIGNED, ST_STEP_LIMIT, ST_SIMT_STACK, ST_TIMEOUT, ST_INJECTED = 1, 2, 3, 4, 5, 6
-ST_CACHE_LOG, ST_CACHE_STREAM = 7, 8
+ST_CACHE_LOG, ST_CACHE_STREAM, ST_SCHED_LIMIT = 7, 8, 9
+
+# SM issue model records (include/ks.h)
+SCHED_WARP_DTYPE = np.dtype([("start", "<u8"), ("end", "<u8"), ("issued", "<u8"), ("not_selected", "<u8"),
+                             ("stall_exec", "<u8"), ("stall_mem", "<u8"), ("stall_math", "<u8"),
+                             ("stall_barrier", "<u8")])
+SCHED_SM_DTYPE = np.dtype([("cycles", "<u8"), ("issued", "<u8"), ("ctas", "<u8"), ("status", "<i4"),
+                           ("reserved", "<u4")])
 
 # L1/L2 hit model: per-warp counts and logged accesses (include/ks.h)
 CACHE_L1_HIT, CACHE_L2_HIT, CACHE_DRAM = 0, 1, 2
@@ -315,6 +322,53 @@ class CacheConfig:
         return c
 
 
+@dataclass
+class SchedConfig:
+    """The SM issue model's parameters (ks_sched_config)."""
+    n_sm: int = 152
+    ctas_per_sm: int = 0
+    schedulers_per_sm: int = 4
+    max_runs_per_warp: int = 4096
+
+    def to_c(self) -> _native.KsSchedConfig:
+        c = _native.KsSchedConfig()
+        _native.lib().ks_sched_config_default(ctypes.byref(c))
+        c.n_sm, c.ctas_per_sm = self.n_sm, self.ctas_per_sm
+        c.schedulers_per_sm, c.max_runs_per_warp = self.schedulers_per_sm, self.max_runs_per_warp
+        return c
+
+
+def sched_workspace_bytes(grid: int, block: int, sched: SchedConfig | None = None) -> int:
+    sc = (sched or SchedConfig()).to_c()
+    return int(_native.lib().ks_sched_workspace_bytes(grid, block, ctypes.byref(sc)))
+
+
+def simulate_sched(module: Module, kernel: str, grid: int, block: int, params: bytes, buffers, stats: torch.Tensor,
+                   sched_warps: torch.Tensor, sched_sms: torch.Tensor, workspace: torch.Tensor,
+                   trace: torch.Tensor | None = None, config: Config | None = None,
+                   sched: SchedConfig | None = None, stream=None) -> None:
+    """ks_simulate_sched: simulate() plus the SM issue model; sched_warps /
+    sched_sms / workspace are uint8 cuda tensors (64 B per warp, 32 B per SM,
+    sched_workspace_bytes)."""
+    bufs = (_native.KsBuffer * max(1, len(buffers)))()
+    for i, (base, t) in enumerate(buffers):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("buffers must be contiguous CUDA tensors")
+        bufs[i].sim_base = base
+        bufs[i].dev_ptr = t.data_ptr()
+        bufs[i].bytes = t.numel() * t.element_size()
+    cfg = (config or Config()).to_c()
+    sc = (sched or SchedConfig()).to_c()
+    pbuf = ctypes.create_string_buffer(bytes(params), max(1, len(params)))
+    rc = _native.lib().ks_simulate_sched(
+        module.handle, kernel.encode(), grid, block, ctypes.cast(pbuf, ctypes.c_void_p), len(params), bufs,
+        len(buffers), trace.data_ptr() if trace is not None else None,
+        trace.numel() if trace is not None else 0, stats.data_ptr(), stats.numel(), ctypes.byref(cfg),
+        ctypes.byref(sc), sched_warps.data_ptr(), sched_warps.numel(), sched_sms.data_ptr(), sched_sms.numel(),
+        workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    _check(rc)
+
+
 def cache_workspace_bytes(grid: int, block: int, cache: CacheConfig | None = None) -> int:
     """Device workspace of simulate_cached (0 when the configuration is invalid)."""
     cc = (cache or CacheConfig()).to_c()
@@ -375,18 +429,30 @@ class Run:
     buffers: list = field(default_factory=list)
     cache_warps: np.ndarray | None = None  # CACHE_WARP_DTYPE per warp (cache model only)
     cache_log: np.ndarray | None = None    # CACHE_ACCESS_DTYPE, (W, max_accesses_per_warp)
+    sched_warps: np.ndarray | None = None  # SCHED_WARP_DTYPE per warp (SM issue model only)
+    sched_sms: np.ndarray | None = None    # SCHED_SM_DTYPE per SM
 
 
 def run(module: Module, kernel: str, grid: int, block: int, params: bytes, buffers, config: Config | None = None,
-        trace: bool = False, stream=None, cache: CacheConfig | None = None) -> Run:
+        trace: bool = False, stream=None, cache: CacheConfig | None = None, sched: SchedConfig | None = None) -> Run:
     """Allocates the outputs, simulates (with the L1/L2 hit model when `cache`
-    is given), and reduces the totals."""
+    is given, with the SM issue model when `sched` is), and reduces the totals."""
     config = config or Config()
     dev = buffers[0][1].device if buffers else torch.device("cuda")
     st = torch.empty(stats_bytes(grid, block), dtype=torch.uint8, device=dev)
     tr = (torch.empty(trace_bytes(grid, block, config.max_ts, module.record_bytes(kernel)), dtype=torch.uint8, device=dev)
           if trace else None)
     n = grid * ((block + 31) // 32)
+    if cache is not None and sched is not None:
+        raise ValueError("the cache model and the SM issue model run separately")
+    if sched is not None:
+        sw = torch.empty(n * 64, dtype=torch.uint8, device=dev)
+        ss = torch.empty(sched.n_sm * 32, dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(1, sched_workspace_bytes(grid, block, sched)), dtype=torch.uint8, device=dev)
+        simulate_sched(module, kernel, grid, block, params, buffers, st, sw, ss, ws, tr, config, sched, stream)
+        totals = read_stats(st, n, stream)
+        return Run(st, tr, totals, list(buffers), sched_warps=sw.cpu().numpy().view(SCHED_WARP_DTYPE),
+                   sched_sms=ss.cpu().numpy().view(SCHED_SM_DTYPE))
     if cache is None:
         simulate(module, kernel, grid, block, params, buffers, st, tr, config, stream)
         return Run(st, tr, read_stats(st, n, stream), list(buffers))

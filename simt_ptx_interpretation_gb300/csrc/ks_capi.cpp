@@ -358,6 +358,63 @@ int ks_profile_bytes(const ks_module* mod, const char* kernel, size_t* bytes) {
   return KS_OK;
 }
 
+void ks_sched_config_default(ks_sched_config* sc) {
+  if (!sc) return;
+  std::memset(sc, 0, sizeof *sc);
+  sc->n_sm = 152;
+  sc->ctas_per_sm = 0;
+  sc->schedulers_per_sm = 4;
+  sc->max_runs_per_warp = 4096;
+}
+
+size_t ks_sched_workspace_bytes(uint32_t grid, uint32_t block, const ks_sched_config* sc_in) {
+  ks_sched_config sc;
+  if (sc_in) sc = *sc_in; else ks_sched_config_default(&sc);
+  if (grid == 0 || block == 0 || block > 1024 || sc.max_runs_per_warp == 0) return 0;
+  const uint64_t W = warps_of(grid, block);
+  return (size_t)((W * 4 + 255) / 256 * 256 + W * (uint64_t)sc.max_runs_per_warp * 4);
+}
+
+int ks_simulate_sched(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block, const void* params,
+                      size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf,
+                      size_t trace_bytes, void* stats_buf, size_t stats_bytes, const ks_config* cfg,
+                      const ks_sched_config* sc_in, void* sched_warps, size_t sched_warps_bytes, void* sched_sms,
+                      size_t sched_sms_bytes, void* workspace, size_t workspace_bytes, void* stream) {
+  ks_sched_config sc;
+  if (sc_in) sc = *sc_in; else ks_sched_config_default(&sc);
+  if (grid == 0 || block == 0 || block > 1024) return KS_ERR_ARG;
+  const uint32_t wpc = (block + 31u) / 32u;
+  if (sc.n_sm == 0 || sc.max_runs_per_warp == 0 ||
+      !(sc.schedulers_per_sm == 1 || sc.schedulers_per_sm == 2 || sc.schedulers_per_sm == 4))
+    return KS_ERR_ARG;
+  const uint32_t ctas = sc.ctas_per_sm ? sc.ctas_per_sm : 32u / wpc;
+  if (ctas == 0 || ctas * wpc > 32u) return KS_ERR_ARG;
+  const uint64_t W = warps_of(grid, block);
+  if (!sched_warps || sched_warps_bytes < W * sizeof(ks_sched_warp)) return KS_ERR_ARG;
+  if (!sched_sms || sched_sms_bytes < (uint64_t)sc.n_sm * sizeof(ks_sched_sm)) return KS_ERR_ARG;
+  const size_t need = ks_sched_workspace_bytes(grid, block, &sc);
+  if (!workspace || need == 0 || workspace_bytes < need) return KS_ERR_ARG;
+  if (W * (uint64_t)sc.max_runs_per_warp >= (1ull << 40)) return KS_ERR_ARG;
+  ks::KsLaunch L;
+  DevInfo di;
+  int rc = prepare(mod, kernel, grid, block, params, param_bytes, bufs, n_bufs, trace_buf, trace_bytes, stats_buf,
+                   stats_bytes, cfg, &L, &di);
+  if (rc != KS_OK) return rc;
+  const uint32_t n_rows = L.layout.zero_off / ks::ROW_BYTES + 1u;
+  if (ks::sched_smem_bytes(L.n_insn, n_rows) > (size_t)di.max_smem) return KS_ERR_LIMIT;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  L.sched_runs = reinterpret_cast<uint32_t*>(ws);
+  L.sched_log = reinterpret_cast<uint32_t*>(ws + (W * 4 + 255) / 256 * 256);
+  L.sched_cap = sc.max_runs_per_warp;
+  if (clear_profile(L, stream) != KS_OK) return KS_ERR_CUDA;
+  rc = shape_and_launch(L, di, stream);
+  if (rc != KS_OK) return rc;
+  if (ks::launch_sched(L, n_rows, sc.n_sm, ctas, sc.schedulers_per_sm, static_cast<ks_sched_warp*>(sched_warps),
+                       static_cast<ks_sched_sm*>(sched_sms), stream) != 0)
+    return KS_ERR_CUDA;
+  return KS_OK;
+}
+
 void ks_cache_config_default(ks_cache_config* cc) {
   if (!cc) return;
   std::memset(cc, 0, sizeof *cc);
@@ -477,6 +534,7 @@ const char* ks_status_string(int code) {
     case KS_ST_INJECTED: return "injected fault";
     case KS_ST_CACHE_LOG: return "cache model: access log full or access step too large";
     case KS_ST_CACHE_STREAM: return "cache model: accesses differ between the two passes";
+    case KS_ST_SCHED_LIMIT: return "SM issue model: issue log full or SM clock too large";
     default: return "unknown status";
   }
 }

@@ -241,6 +241,11 @@ struct KsLaunch {
   ks_cache_warp* cache_warps;     // [n_warps]
   ks_cache_access* cache_log;     // [n_warps * cache_cap]
   ks_pc_profile* profile;         // per-instruction profile, or null
+  // SM issue model: each warp's issued program-entry runs, u32 (first entry
+  // << 16 | length - 1), sched_cap per warp; their number per warp
+  uint32_t* sched_log;
+  uint32_t* sched_runs;
+  uint32_t sched_cap;
   alignas(16) uint8_t params[KS_MAX_PARAM_BYTES];
 };
 
@@ -276,6 +281,13 @@ int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out);
 // number of logged records). Returns a cudaError_t value.
 int launch_cache_levels(const KsLaunch& L, uint8_t* workspace, const CacheLayout& C, uint32_t l1_lines,
                         uint32_t l2_lines, void* stream);
+
+// SM issue model replay (ks_sched.cu): shared memory of one simulated SM's
+// replay, and the launch (one 32-thread block per simulated SM). Returns a
+// cudaError_t value.
+size_t sched_smem_bytes(uint32_t n_insn, uint32_t n_rows);
+int launch_sched(const KsLaunch& L, uint32_t n_rows, uint32_t n_sm, uint32_t ctas_per_sm, uint32_t schedulers,
+                 ks_sched_warp* warps_out, ks_sched_sm* sms_out, void* stream);
 int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream);
 
 }  // namespace ks

@@ -303,6 +303,9 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
     // the instructions its warp issued before it)
     uint32_t c_k = 0, c_l1 = 0, c_l2 = 0, c_n = 0;
     uint64_t c_off = 0;
+    // SM issue model: the run of consecutive program entries being consumed
+    // [run_start, run_next) and the runs logged so far
+    uint32_t run_start = 0, run_next = 0, n_runs = 0;
     if constexpr (INSTR) {
       if (L.cache_pass == 2) {
         c_n = L.cache_warps[gw].n_access;
@@ -344,6 +347,16 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
       // mask is not empty and pc is not the reconvergence pc here; `fuel_in` =
       // instructions that may run before the reconvergence pc or the end of the
       // step budget.
+      if constexpr (INSTR) {
+        if (L.sched_log && pc != run_next) {  // a new run: log the one that ended
+          if (run_next != run_start) {
+            if (lane == 0 && n_runs < L.sched_cap)
+              L.sched_log[(uint64_t)gw * L.sched_cap + n_runs] = (run_start << 16) | (run_next - run_start - 1u);
+            n_runs++;
+          }
+          run_start = run_next = pc;
+        }
+      }
       const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
       const uint4 q0 = ip[0], q1 = ip[1], q2 = ip[2], q3 = ip[3];
       const uint32_t fuel_in = min(budget, rpc > pc ? rpc - pc : 0xFFFFFFFFu);
@@ -409,6 +422,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
         pc += run_n;
         budget -= run_n;
         t_last = t_next - 1u;
+        if constexpr (INSTR) run_next = pc;
         continue;
       }
       // ---- mid path: runs of the other unguarded register-to-register ops
@@ -493,11 +507,13 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
         pc += steps;
         budget -= steps;
         t_last = t_next - 1u;
+        if constexpr (INSTR) run_next = pc;
         continue;
       }
       // ---- general path: one instruction; every operand / ready-time load at once
       const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q2.x, gneg = q2.y, inc = q1.w;
       [[maybe_unused]] const uint32_t pc_here = pc;  // the instrumented handlers' program entry
+      [[maybe_unused]] uint32_t consumed = 1;        // program entries this step issues (2: setp + bra)
       const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q0.w;
       const uint32_t aux = q0.z;
       const uint2 pa = SM2(lb + A), pb = SM2(lb + B), pcc = SM2(lb + C);
@@ -533,6 +549,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
             n_dropped++;
           }
           pc++;
+          if constexpr (INSTR) run_next = pc;
           continue;
         }
         if (op == OP_EXIT) {  // reached the virtual exit: the remaining lanes finish
@@ -721,6 +738,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
               t_next = t2 + L.lat[KS_LAT_BRA];
               budget--;
               pc = taken ? (aux >> 17) : pc + 2u;
+              consumed = 2;
               break;
             }
           }
@@ -995,6 +1013,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
 #undef A64
 #undef B64
 #undef C64
+      if constexpr (INSTR) run_next = pc_here + consumed;
       if (status != 0) {
         FLUSH_THREADS();
         break;
@@ -1060,6 +1079,15 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
 #undef FLUSH_THREADS
     const uint64_t warp_insts = stop_at - left - budget;
     if constexpr (INSTR) {
+      if (L.sched_log) {  // the last run, and the count
+        if (run_next != run_start) {
+          if (lane == 0 && n_runs < L.sched_cap)
+            L.sched_log[(uint64_t)gw * L.sched_cap + n_runs] = (run_start << 16) | (run_next - run_start - 1u);
+          n_runs++;
+        }
+        if (lane == 0) L.sched_runs[gw] = n_runs;
+        if (n_runs > L.sched_cap && status == 0) status = KS_ST_SCHED_LIMIT;
+      }
       if (L.cache_pass == 2 && status == 0 && c_k != c_n) status = KS_ST_CACHE_STREAM;
       if (L.cache_pass != 0u && lane == 0) {
         ks_cache_warp cw;
@@ -1163,7 +1191,9 @@ static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, bool instr) 
   return instr ? (const void*)ks_interp_kernel<true, false, true> : (const void*)ks_interp_kernel<true, false, false>;
 }
 
-static bool instrumented(const KsLaunch& L) { return L.cache_pass != 0 || L.profile != nullptr; }
+static bool instrumented(const KsLaunch& L) {
+  return L.cache_pass != 0 || L.profile != nullptr || L.sched_log != nullptr;
+}
 
 static int ensure_attr() {
   int dev = 0;

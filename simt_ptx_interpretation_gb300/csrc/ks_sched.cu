@@ -1,0 +1,316 @@
+// ks_sched.cu — the SM-level issue model (KernelScope backend doc,
+// simulator/engine.py and simulator/models.py — WarpStallReason,
+// _determine_stall_reason, WarpScheduleInfo: warps that are ready but not
+// picked, waiting on a load, on a result, on the math pipe, at a barrier).
+//
+// The interpreter's instrumented pass logs, per warp, the runs of program
+// entries it consumed; values and control flow do not depend on timing, so
+// the schedule can be replayed from those runs and the decoded program alone.
+// One real warp replays one simulated SM: lane l holds the warp in resident
+// slot l (CTA slot l / warps-per-CTA), its scoreboard (a ready time and the
+// producer's kind per register row and predicate) in shared memory, and its
+// position in its runs. Every step the lanes offer their next issue time
+// max(own scoreboard time, their scheduler's free cycle); the earliest, and
+// among equal times the lowest global warp id (the page's step() order),
+// issues. Barriers release as in the interpreter (latest arrival + bar
+// latency, finished warps do not hold them); a CTA whose warps are all done
+// frees its slot, and the SM's next CTA (s, s + n_sm, s + 2 n_sm, ...) starts
+// there at that cycle.
+#include <cuda_runtime.h>
+
+#include "ks_internal.h"
+
+namespace ks {
+namespace {
+
+constexpr unsigned FULL = 0xFFFFFFFFu;
+constexpr uint32_t NEVER = 0xFFFFFFFFu;
+constexpr uint32_t CLOCK_LIMIT = 1u << 31;
+enum : uint32_t { ST_EMPTY = 0, ST_RUNNING = 1, ST_WAITING = 2, ST_DONE = 3 };
+enum : uint32_t { K_EXEC = 0, K_MATH = 1, K_MEM = 2 };  // what a stall waits on (priority order)
+
+struct SchedLaunch {
+  const uint8_t* image;  // DevInsn program (unpatched latencies)
+  uint32_t n_insn;       // entries, the exit sentinel not included
+  uint32_t n_rows;       // register, constant and zero rows of a warp region
+  uint32_t pred_off;     // region offset of the predicate ready table
+  uint32_t lat[KS_NUM_LAT_CLASSES];
+  uint32_t grid, wpc, n_sm, ctas_per_sm, schedulers;
+  const uint32_t* log;
+  const uint32_t* runs;
+  uint32_t cap;
+  ks_sched_warp* warps_out;
+  ks_sched_sm* sms_out;
+};
+
+__device__ __forceinline__ uint64_t warp_min_u64(uint64_t v) {
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t w = __shfl_xor_sync(FULL, v, o);
+    v = w < v ? w : v;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) { return __reduce_max_sync(FULL, v); }
+
+struct Lane {
+  uint32_t state, gw, cta_slot;
+  uint32_t pc, run_left, k, n_runs;  // next entry to issue; entries left in its run; next run index
+  uint32_t t_next, t_last, max_ready, drain, base, start, e, bind, arrival, end;
+  uint64_t issued, not_selected, stall[3], stall_bar;
+};
+
+__global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ SchedLaunch S) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  const uint32_t lane = threadIdx.x;
+  const uint32_t s_id = blockIdx.x;
+  DevInsn* prog = reinterpret_cast<DevInsn*>(sm);
+  uint8_t* kind = sm + (S.n_insn + 1) * sizeof(DevInsn);  // stall kind of each entry's result
+  const uint32_t NR = S.n_rows + 32u;                      // rows, then the 32 predicates
+  uint32_t* ready_all = reinterpret_cast<uint32_t*>(sm + ((S.n_insn + 1) * (sizeof(DevInsn) + 1) + 15u) / 16u * 16u);
+  uint8_t* rkind_all = reinterpret_cast<uint8_t*>(ready_all + 32u * NR);
+  uint32_t* ready = ready_all + lane * NR;
+  uint8_t* rkind = rkind_all + lane * NR;
+
+  // the program with this launch's latencies (as the interpreter patches it)
+  for (uint32_t i = lane; i <= S.n_insn; i += 32) {
+    DevInsn d = reinterpret_cast<const DevInsn*>(S.image)[i];
+    const uint32_t f = d.wlat, cls = f & 0xFFu, lat = S.lat[cls];
+    d.wlat = (f & DEV_HAS_DEST) ? lat : 0u;
+    d.dlat = (f & DEV_IS_STORE) ? lat : 0u;
+    d.nlat = d.inc ? ((f & DEV_IS_CTRL) ? lat : 1u) : 0u;
+    prog[i] = d;
+    kind[i] = (cls == KS_LAT_LDG || cls == KS_LAT_LDS) ? K_MEM : cls == KS_LAT_SFU ? K_MATH : K_EXEC;
+  }
+  __syncwarp();
+
+  const uint32_t slots = S.ctas_per_sm * S.wpc;  // resident warp slots (<= 32)
+  const uint32_t my_sched = lane % S.schedulers;
+  Lane L;
+  L.state = ST_EMPTY;
+  L.cta_slot = lane / S.wpc;
+  uint32_t port = 0;  // next free cycle of my scheduler
+  uint32_t next_cta_k = 0;
+  uint32_t status = 0;
+  uint64_t sm_issued = 0;
+  uint32_t sm_end = 0, ctas = 0;
+
+  // position at the next issued entry of the runs; false when none is left
+  auto advance = [&](bool consume) -> bool {
+    if (consume) {
+      L.pc++;
+      L.run_left--;
+    }
+    for (;;) {
+      while (L.run_left == 0) {
+        if (L.k >= L.n_runs) return false;
+        const uint32_t r = S.log[(uint64_t)L.gw * S.cap + L.k++];
+        L.pc = r >> 16;
+        L.run_left = (r & 0xFFFFu) + 1u;
+      }
+      if (prog[L.pc].inc & INC_ISSUE) return true;
+      L.pc++;
+      L.run_left--;
+    }
+  };
+  auto ready_of_row = [&](uint32_t off) -> uint32_t { return off / ROW_BYTES; };
+  auto ready_of_pred = [&](uint32_t off) -> uint32_t { return S.n_rows + (off - S.pred_off) / 4u; };
+  // scoreboard time of the next entry and what binds it
+  auto compute_e = [&]() {
+    const DevInsn& d = prog[L.pc];
+    uint32_t idx[9];
+    uint32_t n = 0;
+    idx[n++] = ready_of_row(d.a);
+    idx[n++] = ready_of_row(d.b);
+    idx[n++] = ready_of_row(d.c);
+    idx[n++] = ready_of_row(d.d);
+    idx[n++] = S.n_rows + d.guard;
+    if (d.inc & INC_PHAZ) {
+      idx[n++] = ready_of_pred(d.ha);
+      idx[n++] = ready_of_pred(d.hb);
+      idx[n++] = ready_of_pred(d.hc);
+      idx[n++] = ready_of_pred(d.hd);
+    }
+    uint32_t e = L.t_next;
+    for (uint32_t i = 0; i < n; i++) e = max(e, ready[idx[i]]);
+    uint32_t b = K_EXEC;  // t_next itself (a branch's latency) counts as a result wait
+    for (uint32_t i = 0; i < n; i++)
+      if (ready[idx[i]] == e) b = max(b, (uint32_t)rkind[idx[i]]);
+    L.e = e;
+    L.bind = b;
+  };
+  auto finish = [&]() {
+    L.state = ST_DONE;
+    L.end = L.issued ? max(max(L.t_last + 1u, L.max_ready), L.drain) : L.start;
+    ks_sched_warp r;
+    r.start = L.start;
+    r.end = L.end;
+    r.issued = L.issued;
+    r.not_selected = L.not_selected;
+    r.stall_exec = L.stall[K_EXEC];
+    r.stall_mem = L.stall[K_MEM];
+    r.stall_math = L.stall[K_MATH];
+    r.stall_barrier = L.stall_bar;
+    S.warps_out[L.gw] = r;
+    sm_end = max(sm_end, L.end);
+    sm_issued += L.issued;
+  };
+  // lanes of slot c (mine) load their warps of the slot's next CTA at cycle t0
+  auto load_cta = [&](bool mine, uint32_t t0) {
+    const uint32_t k = next_cta_k++;
+    const uint64_t cta = (uint64_t)s_id + (uint64_t)k * S.n_sm;
+    if (!mine) return;
+    if (cta >= S.grid) {
+      L.state = ST_EMPTY;
+      return;
+    }
+    L.gw = (uint32_t)cta * S.wpc + (lane - L.cta_slot * S.wpc);
+    for (uint32_t i = 0; i < NR; i++) {
+      ready[i] = 0u;
+      rkind[i] = K_EXEC;
+    }
+    L.state = ST_RUNNING;
+    L.k = 0;
+    L.run_left = 0;
+    L.n_runs = S.runs[L.gw];
+    L.t_next = L.base = L.start = t0;
+    L.t_last = t0;
+    L.max_ready = L.drain = 0u;
+    L.issued = L.not_selected = L.stall_bar = 0;
+    L.stall[0] = L.stall[1] = L.stall[2] = 0;
+    if (L.n_runs > S.cap) {
+      status = KS_ST_SCHED_LIMIT;
+      L.n_runs = 0;
+    }
+    if (advance(false)) compute_e();
+    else finish();
+  };
+  // Settles CTA slot c after one of its warps arrived or finished: releases
+  // its barrier when no warp runs, and when every warp is done starts the
+  // SM's next CTA there (at once again if that CTA has nothing to issue).
+  auto settle = [&](uint32_t c) {
+    for (;;) {
+      const bool mine = lane < slots && L.cta_slot == c;
+      if (__any_sync(FULL, mine && L.state == ST_RUNNING)) return;
+      const uint32_t waiting = __ballot_sync(FULL, mine && L.state == ST_WAITING);
+      if (waiting) {
+        const uint32_t latest = warp_max_u32(mine && L.state == ST_WAITING ? L.arrival : 0u);
+        if (mine && L.state == ST_WAITING) {
+          const uint32_t rel = latest + S.lat[KS_LAT_BAR];
+          L.stall_bar += rel - (L.arrival + 1u);
+          L.t_next = L.base = rel;
+          L.state = ST_RUNNING;
+          if (L.run_left != 0 || L.k < L.n_runs) compute_e();
+          else finish();
+        }
+        continue;
+      }
+      if (!__any_sync(FULL, mine && L.state == ST_DONE)) return;  // an empty slot
+      const uint32_t fin = warp_max_u32(mine ? L.end : 0u);
+      ctas++;
+      load_cta(mine, fin);
+      if (!__any_sync(FULL, mine && L.state != ST_EMPTY)) return;
+    }
+  };
+
+  for (uint32_t c = 0; c < S.ctas_per_sm; c++) {
+    const bool mine = lane < slots && L.cta_slot == c;
+    load_cta(mine, 0u);
+    if (__any_sync(FULL, mine && L.state != ST_EMPTY)) settle(c);
+  }
+
+  for (;;) {
+    const uint32_t cand = L.state == ST_RUNNING ? max(L.e, port) : NEVER;
+    const uint64_t best = warp_min_u64(((uint64_t)cand << 32) | (L.state == ST_RUNNING ? L.gw : NEVER));
+    const uint32_t T = (uint32_t)(best >> 32);
+    if (T == NEVER) break;
+    if (T >= CLOCK_LIMIT) {
+      status = KS_ST_SCHED_LIMIT;
+      break;
+    }
+    const uint32_t w = __ffs(__ballot_sync(FULL, L.state == ST_RUNNING && L.gw == (uint32_t)best)) - 1u;
+    uint32_t ev = 0;  // 1: arrived at a barrier or finished
+    if (lane == w) {
+      L.not_selected += T - L.e;
+      if (L.e > L.base) L.stall[L.bind] += L.e - L.base;
+      const DevInsn& d = prog[L.pc];
+      const uint32_t wr = T + d.wlat;
+      if (d.inc & INC_RDEST) {
+        ready[ready_of_row(d.d)] = wr;
+        rkind[ready_of_row(d.d)] = kind[L.pc];
+      }
+      if (d.inc & INC_PDEST) {
+        ready[ready_of_pred(d.hd)] = wr;
+        rkind[ready_of_pred(d.hd)] = kind[L.pc];
+      }
+      L.max_ready = max(L.max_ready, wr);
+      L.drain = max(L.drain, T + d.dlat);
+      L.t_last = T;
+      L.t_next = T + d.nlat;
+      L.base = T + 1u;
+      L.issued++;
+      const bool bar = d.op == OP_BAR;
+      const bool more = advance(true);
+      if (bar) {
+        L.state = ST_WAITING;
+        L.arrival = T;
+        ev = 1;
+      } else if (more) {
+        compute_e();
+      } else {
+        finish();
+        ev = 1;
+      }
+    }
+    if (my_sched == w % S.schedulers) port = T + 1u;
+    if (__shfl_sync(FULL, ev, w)) settle(w / S.wpc);
+  }
+
+  // SM totals (each lane added its own warps)
+  for (int o = 16; o > 0; o >>= 1) sm_issued += __shfl_xor_sync(FULL, sm_issued, o);
+  sm_end = warp_max_u32(sm_end);
+  status = warp_max_u32(status);
+  if (lane == 0) {
+    ks_sched_sm r;
+    r.cycles = sm_end;
+    r.issued = sm_issued;
+    r.ctas = ctas;
+    r.status = (int32_t)status;
+    r.reserved = 0;
+    S.sms_out[s_id] = r;
+  }
+}
+
+}  // namespace
+
+size_t sched_smem_bytes(uint32_t n_insn, uint32_t n_rows) {
+  const size_t prog = ((size_t)(n_insn + 1) * (sizeof(DevInsn) + 1) + 15u) / 16u * 16u;
+  return prog + 32u * (size_t)(n_rows + 32u) * 5u;
+}
+
+int launch_sched(const KsLaunch& L, uint32_t n_rows, uint32_t n_sm, uint32_t ctas_per_sm, uint32_t schedulers,
+                 ks_sched_warp* warps_out, ks_sched_sm* sms_out, void* stream) {
+  SchedLaunch S;
+  S.image = L.image;
+  S.n_insn = L.n_insn;
+  S.n_rows = n_rows;
+  S.pred_off = L.layout.pred_off;
+  for (int i = 0; i < KS_NUM_LAT_CLASSES; i++) S.lat[i] = L.lat[i];
+  S.grid = L.grid;
+  S.wpc = L.wpc;
+  S.n_sm = n_sm;
+  S.ctas_per_sm = ctas_per_sm;
+  S.schedulers = schedulers;
+  S.log = L.sched_log;
+  S.runs = L.sched_runs;
+  S.cap = L.sched_cap;
+  S.warps_out = warps_out;
+  S.sms_out = sms_out;
+  const size_t smem = sched_smem_bytes(L.n_insn, n_rows);
+  cudaError_t e = cudaFuncSetAttribute(ks_sched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  ks_sched_kernel<<<n_sm, 32, smem, (cudaStream_t)stream>>>(S);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace ks
