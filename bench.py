@@ -9,10 +9,12 @@ kernel and one with 8 rotating accumulators), i.e. two interpreter launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload ffma_pair|vector_add|gather_sS|divergent_kK|fuzz|smem_reduce]
-                  [--cache [--cache-cap C]]
+                  [--cache [--cache-cap C]] [--sched [--sched-sms S]]
 
 --cache runs every launch with the L1/L2 hit model (ks_simulate_cached: a
-logging pass, the sorted levels, the checked second pass).
+logging pass, the sorted levels, the checked second pass); --sched with the
+SM-level issue model (ks_simulate_sched: the interpreter logging each warp's
+issued runs, then one replay warp per simulated SM).
 
 Prints one JSON line (rank 0). N > 1 runs N independent replicas, one per
 GPU (weak scaling; the path has no exchange step).
@@ -58,6 +60,8 @@ def parse_args():
     p.add_argument("--cache-cap", type=int, default=0,
                    help="logged global accesses per warp (--cache); 0: the largest count of a plain run, "
                         "rounded up to a power of two")
+    p.add_argument("--sched", action="store_true", help="simulate with the SM-level issue model")
+    p.add_argument("--sched-sms", type=int, default=152, help="simulated SMs (--sched)")
     p.add_argument("--scale", type=int, default=1,
                    help="divide the gather outputs, divergent threads or fuzz kernels (smaller cases for profiling)")
     return p.parse_args()
@@ -245,9 +249,37 @@ def run_ours(args, world, rank, local):
                                            "lat_l1": cache.lat_l1, "lat_l2": cache.lat_l2,
                                            "max_accesses_per_warp": cache.max_accesses_per_warp})
 
+    sched = ks.SchedConfig(n_sm=args.sched_sms) if args.sched else None
+    if sched:
+        if cache:
+            raise SystemExit("--cache and --sched run separately")
+        wmax = max(jobs, key=lambda j: j["w"].warps)["w"]
+        runs = 1
+        for j in jobs:  # size the issue log from an untimed logging run
+            w = j["w"]
+            probe = ks.SchedConfig(n_sm=args.sched_sms, max_runs_per_warp=1 << 16)
+            nb = ks.sched_workspace_bytes(w.grid, w.block, probe)
+            tmp = torch.empty(nb, dtype=torch.uint8, device=dev)
+            sw = torch.empty(w.warps * 64, dtype=torch.uint8, device=dev)
+            ss = torch.empty(args.sched_sms * 32, dtype=torch.uint8, device=dev)
+            ks.simulate_sched(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], sw, ss, tmp, j["tr"],
+                              j["cfg"], probe, stream)
+            torch.cuda.synchronize(dev)
+            runs = max(runs, int(tmp[:w.warps * 4].view(torch.int32).max().item()))
+            del tmp
+        sched = ks.SchedConfig(n_sm=args.sched_sms, max_runs_per_warp=1 << (runs - 1).bit_length())
+        sched_ws = torch.empty(ks.sched_workspace_bytes(wmax.grid, wmax.block, sched), dtype=torch.uint8, device=dev)
+        sched_w = torch.empty(wmax.warps * 64, dtype=torch.uint8, device=dev)
+        sched_s = torch.empty(args.sched_sms * 32, dtype=torch.uint8, device=dev)
+        config = dict(config, sm_model={"n_sm": sched.n_sm, "schedulers_per_sm": sched.schedulers_per_sm,
+                                        "ctas_per_sm": "fill 32 warps", "max_runs_per_warp": sched.max_runs_per_warp})
+
     def launch(j):
         w = j["w"]
-        if cache:
+        if sched:
+            ks.simulate_sched(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], sched_w, sched_s,
+                              sched_ws, j["tr"], j["cfg"], sched, stream)
+        elif cache:
             ks.simulate_cached(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], cache_ws, j["tr"],
                                j["cfg"], cache, stream)
         else:
@@ -302,7 +334,7 @@ def run_ours(args, world, rank, local):
     mean_launch_s = sum(sum(x) for x in launch_ms) / (args.steps * n_launch) / 1e3
     # with the cache model a call interprets the launch twice (and sorts in
     # between): charge the whole call to the two interpreter passes
-    passes = 2 if cache else 1
+    passes = 2 if cache else 1  # (the SM model's replay runs once per call)
     achieved = passes * (insts / n_launch) / mean_launch_s / 1e9
     traffic = traffic_for(config["workload"])
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "Gthread-inst/s",
@@ -313,6 +345,9 @@ def run_ours(args, world, rank, local):
     if cache:
         roofline["note"] = ("each call runs ks_interp_kernel twice plus the level kernels and radix sorts; "
                             "achieved counts both passes over the whole call's time")
+    if sched:
+        roofline["note"] = ("each call runs ks_interp_kernel once and ks_sched_kernel once; achieved counts the "
+                            "simulated thread-instructions over the whole call's time")
 
     # end to end through the public API with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(args, jobs, insts, dev, stream, launch)
@@ -325,12 +360,14 @@ def run_ours(args, world, rank, local):
         # our kernels per call: the interpreter, or (cache model) two interpreter
         # passes and the four level kernels (the radix sorts and the scan are
         # library code)
-        "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps * n_launch * (6 if cache else 1),
+        "roofline": roofline, "e2e": e2e,
+        "gpu_launches": args.steps * n_launch * (6 if cache else 2 if sched else 1),
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3), "kernel_sha": kernel_sha(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_cached(ws, cache) if cache else cpu_baseline(ws, sample_warps=None)
+        line["cpu_baseline"] = (cpu_baseline_cached(ws, cache) if cache else cpu_baseline_sched(ws, sched) if sched
+                                else cpu_baseline(ws, sample_warps=None))
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -418,6 +455,27 @@ def cpu_baseline_cached(ws, cache, warps_per_kernel=16):
             "sample": "; ".join(desc), "thread_insts": total_i, "seconds": round(total_s, 3)}
 
 
+def cpu_baseline_sched(ws, sched, warps_per_kernel=16):
+    """The oracle's cycle-by-cycle SM model (one host thread) on a bounded
+    sample: each kernel on a grid cut down to about `warps_per_kernel` warps,
+    on as many SMs as it has CTAs."""
+    import oracle
+    total_i, total_s, desc = 0, 0.0, []
+    for w in ws:
+        wpc = (w.block + 31) // 32
+        grid = max(1, min(w.grid, warps_per_kernel // wpc))
+        bufs = w.fresh_buffers()
+        t0 = time.perf_counter()
+        st = np.zeros(grid * wpc, dtype=oracle.STATS_DTYPE)
+        oracle.run_sched(w.ptx, w.kernel, grid, w.block, w.params, [(b.sim_base, b.data) for b in bufs],
+                         n_sm=min(grid, sched.n_sm), schedulers=sched.schedulers_per_sm, stats=st)
+        total_s += time.perf_counter() - t0
+        total_i += int(st["thread_insts"].sum())
+        desc.append(f"{w.name}: grid {grid} of {w.grid}")
+    return {"value": round(total_i / total_s, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "; ".join(desc), "thread_insts": total_i, "seconds": round(total_s, 3)}
+
+
 # ----------------------------------------------------------- reference ----
 
 def run_reference(args, world, rank):
@@ -436,6 +494,15 @@ def run_reference(args, world, rank):
 
         def sample(n):
             return cpu_baseline_cached(ws, cache, warps_per_kernel=n)
+    elif args.sched:
+        from simt_ptx_interpretation_gb300.api import SchedConfig
+        sc = SchedConfig(n_sm=args.sched_sms)
+        per = 8
+        config = dict(config, sm_model={"n_sm": sc.n_sm, "schedulers_per_sm": sc.schedulers_per_sm})
+        cores = 1
+
+        def sample(n):
+            return cpu_baseline_sched(ws, sc, warps_per_kernel=n)
     else:
         def sample(n):
             return cpu_baseline(ws, max_warps_per_kernel=n)
@@ -454,8 +521,8 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)",
         "data": "synthetic (seeded)", "config": dict(config, sample_warps_per_kernel=per),
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": (f"each kernel on a grid of about {per} warps per step" if args.cache
-                                    else f"first {per} warps of each kernel per step")},
+                         "sample": (f"each kernel on a grid of about {per} warps per step"
+                                    if args.cache or args.sched else f"first {per} warps of each kernel per step")},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

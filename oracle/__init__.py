@@ -159,7 +159,7 @@ def _load():
             ctypes.c_char_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,
             ctypes.c_void_p, ctypes.c_uint64, ctypes.POINTER(_Buffer), ctypes.c_uint32,
             ctypes.POINTER(_Config), ctypes.POINTER(ctypes.c_uint32 * 3), ctypes.c_void_p, ctypes.c_void_p,
-            ctypes.c_char_p, ctypes.c_uint64,
+            ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint64,
         ]
         lib.orc_ipdom.restype = ctypes.c_int
         lib.orc_ipdom.argtypes = [ctypes.c_char_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
@@ -307,10 +307,12 @@ SCHED_SM_DTYPE = np.dtype([("cycles", "<u8"), ("issued", "<u8"), ("ctas", "<u8")
 
 
 def run_sched(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffers, *, lat=DEFAULT_LAT,
-              n_sm: int = 152, ctas_per_sm: int = 0, schedulers: int = 4, step_limit: int = 1 << 26):
+              n_sm: int = 152, ctas_per_sm: int = 0, schedulers: int = 4, step_limit: int = 1 << 26,
+              stats: np.ndarray | None = None):
     """The SM issue model, cycle by cycle on one host thread: (per-warp
     SCHED_WARP_DTYPE records, per-SM SCHED_SM_DTYPE records). Buffers are
-    updated in place."""
+    updated in place; `stats` (STATS_DTYPE, one per warp) gets the per-warp
+    statistics, with this model's absolute ends as cycles."""
     lib = _load()
     W = grid * ((block + 31) // 32)
     bufs = (_Buffer * max(1, len(buffers)))()
@@ -334,7 +336,7 @@ def run_sched(ptx: str, kernel: str, grid: int, block: int, params: bytes, buffe
     err = ctypes.create_string_buffer(512)
     rc = lib.orc_run_sched(ptx.encode(), kernel.encode(), grid, block, ctypes.cast(pbuf, ctypes.c_void_p),
                            len(params), bufs, len(buffers), ctypes.byref(cfg), ctypes.byref(sc), warps.ctypes.data,
-                           sms.ctypes.data, err, len(err))
+                           sms.ctypes.data, stats.ctypes.data if stats is not None else None, err, len(err))
     if rc != 0:
         raise OracleError(rc, err.value.decode(errors="replace"))
     return warps, sms

@@ -1790,6 +1790,7 @@ void run_sm_model(const Launch& X, Memory& M, uint32_t n_sm, uint32_t ctas_per_s
       const uint64_t v[8] = {q.start, q.end, q.w->st.warp_insts, q.not_selected, q.stall[WAIT_EXEC],
                              q.stall[WAIT_MEM], q.stall[WAIT_MATH], q.stall_bar};
       for (int i = 0; i < 8; i++) store_le(r + 8 * i, v[i], 8);
+      q.w->write_back();  // statistics (cycles there are this model's absolute end)
       sm_end = std::max(sm_end, q.end);
       sm_issued += q.w->st.warp_insts;
     };
@@ -2208,7 +2209,7 @@ int orc_run_events(const char* ptx, const char* kernel, uint32_t grid, uint32_t 
 int orc_run_sched(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
                   const void* params, uint64_t param_bytes, const orc_buffer* bufs,
                   uint32_t n_bufs, const orc_config* cfg, const orc_sched* sched, void* sched_warps,
-                  void* sched_sms, char* err, uint64_t errlen) {
+                  void* sched_sms, void* stats_out, char* err, uint64_t errlen) {
   if (!sched || !sched_warps || !sched_sms) {
     copy_err("null argument", err, errlen);
     return ORC_ERR_ARG;
@@ -2238,6 +2239,7 @@ int orc_run_sched(const char* ptx, const char* kernel, uint32_t grid, uint32_t b
     M.bufs = bufs;
     M.n = n_bufs;
     run_sm_model(X, M, sched->n_sm, ctas, sched->schedulers, (uint8_t*)sched_warps, (uint8_t*)sched_sms);
+    if (stats_out) std::memcpy(stats_out, stats.data(), stats.size());
     copy_err("", err, errlen);
     return ORC_OK;
   } catch (const OracleError& e) {

@@ -175,8 +175,9 @@ int orc_run_events(const char* ptx, const char* kernel, uint32_t grid, uint32_t 
  * each scheduler issues for its ready warp with the lowest global warp id.
  * Writes one 64-byte record per warp {start, end, issued, not_selected,
  * stall_exec, stall_mem, stall_math, stall_barrier} (u64 each) and one 32-byte
- * record per SM {cycles, issued, ctas, 0}. Memory is updated; per-warp
- * statistics and traces are not written. */
+ * record per SM {cycles, issued, ctas, 0}. Memory is updated; `stats` (NULL
+ * or W records) gets the per-warp statistics, whose cycles are this model's
+ * absolute ends; no trace is written. */
 typedef struct {
   uint32_t n_sm, ctas_per_sm, schedulers;
 } orc_sched;
@@ -184,7 +185,7 @@ typedef struct {
 int orc_run_sched(const char* ptx, const char* kernel, uint32_t grid, uint32_t block,
                   const void* params, uint64_t param_bytes, const orc_buffer* bufs,
                   uint32_t n_bufs, const orc_config* cfg, const orc_sched* sched, void* sched_warps,
-                  void* sched_sms, char* err, uint64_t errlen);
+                  void* sched_sms, void* stats, char* err, uint64_t errlen);
 
 /* Immediate post-dominator of every program entry (instructions and trace
  * pseudo-ops, in program order); the virtual exit is n (= *n_out). */

@@ -130,3 +130,18 @@ def test_ffma_headline_properties(acc):
     # so no warp waits for another
     assert (ws["not_selected"] == 0).all()
     assert np.array_equal(ws["end"] - ws["start"], st["cycles"])
+
+
+def test_warp_sweep_matches_oracle():
+    from simt_ptx_interpretation_gb300 import sweep
+    rows = sweep.warp_sweep(iters=4, n_sm=4, schedulers=4, configs=sweep.default_configs(4))
+    want = []
+    for grid, block in sweep.default_configs(4):
+        w = wl.ffma(acc=1, iters=4, grid=grid, block=block)
+        ws, sms = oracle.run_sched(w.ptx, w.kernel, w.grid, w.block, w.params,
+                                   [(b.sim_base, b.data) for b in w.fresh_buffers()], n_sm=4, schedulers=4)
+        want.append((int(ws["issued"].sum()), int(sms["cycles"].max())))
+    assert [(r["total_instructions"], r["cycles"]) for r in rows] == want
+    assert [r["active_warps"] for r in rows] == [1, 1, 2, 4, 16]
+    ipc = [r["instructions_per_cycle"] for r in rows]
+    assert ipc[0] == ipc[1] and abs(ipc[3] - 4 * ipc[1]) < 1e-9 and abs(ipc[4] - 4 * ipc[3]) < 1e-9

@@ -178,3 +178,28 @@ def test_waits_add_up(name):
     assert ((ws["end"] - ws["start"]) >= p.stats["cycles"]).all()
     assert int(sms["issued"].sum()) == int(p.stats["warp_insts"].sum())
     assert int(sms["ctas"].sum()) == w.grid
+
+
+def _sweep_row(grid, block, n_sm, schedulers, acc=1, iters=4):
+    w = wl.ffma(acc=acc, iters=iters, grid=grid, block=block)
+    ws, sms = oracle.run_sched(w.ptx, w.kernel, w.grid, w.block, w.params,
+                               [(b.sim_base, b.data) for b in w.fresh_buffers()], n_sm=n_sm, schedulers=schedulers)
+    return int(ws["issued"].sum()), int(sms["cycles"].max())
+
+
+def test_warp_sweep_shape():
+    """The probe methodology's warp sweep on the model: lanes do not change
+    a warp's timing; with 4 schedulers up to 4 warps of a CTA each run alone;
+    more SMs run more CTAs in the same time; with one scheduler, 4 dependent
+    chains share the port and hide part of the latency."""
+    i1, c1 = _sweep_row(1, 1, 4, 4)
+    i32, c32 = _sweep_row(1, 32, 4, 4)
+    i128, c128 = _sweep_row(1, 128, 4, 4)
+    isms, csms = _sweep_row(4, 128, 4, 4)
+    assert (i1, c1) == (i32, c32)
+    assert c128 == c32 and i128 == 4 * i32
+    assert csms == c128 and isms == 4 * i128
+    i1s, c1s = _sweep_row(1, 128, 1, 1)
+    assert i1s == i128
+    ipc_one, ipc_four = i32 / c32, i1s / c1s
+    assert ipc_one < ipc_four <= 1.0
