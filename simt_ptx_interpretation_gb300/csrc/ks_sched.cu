@@ -53,34 +53,63 @@ __device__ __forceinline__ uint64_t warp_min_u64(uint64_t v) {
 
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) { return __reduce_max_sync(FULL, v); }
 
+// What the replay needs of a program entry, 32 bytes:
+//   x: row a | row b << 16        y: row c | row d << 16
+//   z: guard | pred a << 8 | pred b << 16 | pred c << 24
+//   w: pred d | flags << 8 | kind of its result << 16
+//   then dest latency, store latency, issue-clock advance
+struct alignas(16) Rec {
+  uint4 q;
+  uint4 lat;
+};
+constexpr uint32_t F_ISSUE = 1, F_RDEST = 2, F_PDEST = 4, F_PHAZ = 8, F_BAR = 16;
+
 struct Lane {
   uint32_t state, gw, cta_slot;
   uint32_t pc, run_left, k, n_runs;  // next entry to issue; entries left in its run; next run index
   uint32_t t_next, t_last, max_ready, drain, base, start, e, bind, arrival, end;
-  uint64_t issued, not_selected, stall[3], stall_bar;
+  Rec r;                             // the record of the next entry
+  uint64_t issued, not_selected, st_exec, st_mem, st_math, stall_bar;
 };
+
+// ready table entry: ready time | kind of the producer << 32
+__device__ __forceinline__ void take(uint64_t v, uint32_t& e, uint32_t& kind) {
+  const uint32_t t = (uint32_t)v, k = (uint32_t)(v >> 32);
+  if (t > e) { e = t; kind = k; }
+  else if (t == e && k > kind) kind = k;
+}
 
 __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ SchedLaunch S) {
   extern __shared__ __align__(16) uint8_t sm[];
   const uint32_t lane = threadIdx.x;
   const uint32_t s_id = blockIdx.x;
-  DevInsn* prog = reinterpret_cast<DevInsn*>(sm);
-  uint8_t* kind = sm + (S.n_insn + 1) * sizeof(DevInsn);  // stall kind of each entry's result
-  const uint32_t NR = S.n_rows + 32u;                      // rows, then the 32 predicates
-  uint32_t* ready_all = reinterpret_cast<uint32_t*>(sm + ((S.n_insn + 1) * (sizeof(DevInsn) + 1) + 15u) / 16u * 16u);
-  uint8_t* rkind_all = reinterpret_cast<uint8_t*>(ready_all + 32u * NR);
-  uint32_t* ready = ready_all + lane * NR;
-  uint8_t* rkind = rkind_all + lane * NR;
+  Rec* prog = reinterpret_cast<Rec*>(sm);
+  const uint32_t NR = S.n_rows + 32u;  // rows, then the 32 predicates
+  uint64_t* ready = reinterpret_cast<uint64_t*>(sm + (size_t)(S.n_insn + 1) * sizeof(Rec)) + (size_t)lane * NR;
 
-  // the program with this launch's latencies (as the interpreter patches it)
+  // the program's records with this launch's latencies (patched as the
+  // interpreter patches its copy)
   for (uint32_t i = lane; i <= S.n_insn; i += 32) {
-    DevInsn d = reinterpret_cast<const DevInsn*>(S.image)[i];
+    const DevInsn d = reinterpret_cast<const DevInsn*>(S.image)[i];
     const uint32_t f = d.wlat, cls = f & 0xFFu, lat = S.lat[cls];
-    d.wlat = (f & DEV_HAS_DEST) ? lat : 0u;
-    d.dlat = (f & DEV_IS_STORE) ? lat : 0u;
-    d.nlat = d.inc ? ((f & DEV_IS_CTRL) ? lat : 1u) : 0u;
-    prog[i] = d;
-    kind[i] = (cls == KS_LAT_LDG || cls == KS_LAT_LDS) ? K_MEM : cls == KS_LAT_SFU ? K_MATH : K_EXEC;
+    const uint32_t kind = (cls == KS_LAT_LDG || cls == KS_LAT_LDS) ? K_MEM : cls == KS_LAT_SFU ? K_MATH : K_EXEC;
+    uint32_t flags = 0;
+    if (d.inc & INC_ISSUE) flags |= F_ISSUE;
+    if (d.inc & INC_RDEST) flags |= F_RDEST;
+    if (d.inc & INC_PDEST) flags |= F_PDEST;
+    if (d.inc & INC_PHAZ) flags |= F_PHAZ;
+    if (d.op == OP_BAR) flags |= F_BAR;
+    auto pred = [&](uint32_t off) { return (off - S.pred_off) / 4u; };
+    Rec r;
+    r.q.x = (d.a / ROW_BYTES) | ((d.b / ROW_BYTES) << 16);
+    r.q.y = (d.c / ROW_BYTES) | ((d.d / ROW_BYTES) << 16);
+    r.q.z = d.guard | (pred(d.ha) << 8) | (pred(d.hb) << 16) | (pred(d.hc) << 24);
+    r.q.w = pred(d.hd) | (flags << 8) | (kind << 16);
+    r.lat.x = (f & DEV_HAS_DEST) ? lat : 0u;
+    r.lat.y = (f & DEV_IS_STORE) ? lat : 0u;
+    r.lat.z = d.inc ? ((f & DEV_IS_CTRL) ? lat : 1u) : 0u;
+    r.lat.w = 0u;
+    prog[i] = r;
   }
   __syncwarp();
 
@@ -95,7 +124,8 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
   uint64_t sm_issued = 0;
   uint32_t sm_end = 0, ctas = 0;
 
-  // position at the next issued entry of the runs; false when none is left
+  // position at the next issued entry of the runs (its record in L.r);
+  // false when none is left
   auto advance = [&](bool consume) -> bool {
     if (consume) {
       L.pc++;
@@ -108,36 +138,32 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
         L.pc = r >> 16;
         L.run_left = (r & 0xFFFFu) + 1u;
       }
-      if (prog[L.pc].inc & INC_ISSUE) return true;
+      L.r = prog[L.pc];
+      if ((L.r.q.w >> 8) & F_ISSUE) return true;
       L.pc++;
       L.run_left--;
     }
   };
-  auto ready_of_row = [&](uint32_t off) -> uint32_t { return off / ROW_BYTES; };
-  auto ready_of_pred = [&](uint32_t off) -> uint32_t { return S.n_rows + (off - S.pred_off) / 4u; };
   // scoreboard time of the next entry and what binds it
   auto compute_e = [&]() {
-    const DevInsn& d = prog[L.pc];
-    uint32_t idx[9];
-    uint32_t n = 0;
-    idx[n++] = ready_of_row(d.a);
-    idx[n++] = ready_of_row(d.b);
-    idx[n++] = ready_of_row(d.c);
-    idx[n++] = ready_of_row(d.d);
-    idx[n++] = S.n_rows + d.guard;
-    if (d.inc & INC_PHAZ) {
-      idx[n++] = ready_of_pred(d.ha);
-      idx[n++] = ready_of_pred(d.hb);
-      idx[n++] = ready_of_pred(d.hc);
-      idx[n++] = ready_of_pred(d.hd);
+    const uint4 q = L.r.q;
+    const uint32_t P = S.n_rows;
+    const uint64_t va = ready[q.x & 0xFFFFu], vb = ready[q.x >> 16], vc = ready[q.y & 0xFFFFu],
+                   vd = ready[q.y >> 16], vg = ready[P + (q.z & 0xFFu)];
+    uint32_t e = L.t_next, kind = K_EXEC;
+    take(va, e, kind);
+    take(vb, e, kind);
+    take(vc, e, kind);
+    take(vd, e, kind);
+    take(vg, e, kind);
+    if ((q.w >> 8) & F_PHAZ) {
+      take(ready[P + ((q.z >> 8) & 0xFFu)], e, kind);
+      take(ready[P + ((q.z >> 16) & 0xFFu)], e, kind);
+      take(ready[P + (q.z >> 24)], e, kind);
+      take(ready[P + (q.w & 0xFFu)], e, kind);
     }
-    uint32_t e = L.t_next;
-    for (uint32_t i = 0; i < n; i++) e = max(e, ready[idx[i]]);
-    uint32_t b = K_EXEC;  // t_next itself (a branch's latency) counts as a result wait
-    for (uint32_t i = 0; i < n; i++)
-      if (ready[idx[i]] == e) b = max(b, (uint32_t)rkind[idx[i]]);
     L.e = e;
-    L.bind = b;
+    L.bind = kind;
   };
   auto finish = [&]() {
     L.state = ST_DONE;
@@ -147,15 +173,15 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     r.end = L.end;
     r.issued = L.issued;
     r.not_selected = L.not_selected;
-    r.stall_exec = L.stall[K_EXEC];
-    r.stall_mem = L.stall[K_MEM];
-    r.stall_math = L.stall[K_MATH];
+    r.stall_exec = L.st_exec;
+    r.stall_mem = L.st_mem;
+    r.stall_math = L.st_math;
     r.stall_barrier = L.stall_bar;
     S.warps_out[L.gw] = r;
     sm_end = max(sm_end, L.end);
     sm_issued += L.issued;
   };
-  // lanes of slot c (mine) load their warps of the slot's next CTA at cycle t0
+  // lanes of slot c (mine) load their warps of the SM's next CTA at cycle t0
   auto load_cta = [&](bool mine, uint32_t t0) {
     const uint32_t k = next_cta_k++;
     const uint64_t cta = (uint64_t)s_id + (uint64_t)k * S.n_sm;
@@ -165,10 +191,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
       return;
     }
     L.gw = (uint32_t)cta * S.wpc + (lane - L.cta_slot * S.wpc);
-    for (uint32_t i = 0; i < NR; i++) {
-      ready[i] = 0u;
-      rkind[i] = K_EXEC;
-    }
+    for (uint32_t i = 0; i < NR; i++) ready[i] = 0ull;
     L.state = ST_RUNNING;
     L.k = 0;
     L.run_left = 0;
@@ -177,7 +200,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     L.t_last = t0;
     L.max_ready = L.drain = 0u;
     L.issued = L.not_selected = L.stall_bar = 0;
-    L.stall[0] = L.stall[1] = L.stall[2] = 0;
+    L.st_exec = L.st_mem = L.st_math = 0;
     if (L.n_runs > S.cap) {
       status = KS_ST_SCHED_LIMIT;
       L.n_runs = 0;
@@ -219,39 +242,58 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     if (__any_sync(FULL, mine && L.state != ST_EMPTY)) settle(c);
   }
 
+  // Every step, each scheduler's best offer (earliest cycle, then lowest
+  // global warp id) is found with shuffles over the lanes of that scheduler;
+  // the schedulers whose offer is at the earliest cycle of all issue at once.
+  // That is the order of one issue at a time: what an issue changes for other
+  // warps (a barrier release, a new CTA) takes effect a cycle later at the
+  // soonest, so issues of the same cycle on different schedulers do not see
+  // each other. With a zero barrier latency a release takes effect in the
+  // same cycle, and the schedulers take turns one issue at a time.
+  const bool one_at_a_time = S.lat[KS_LAT_BAR] == 0u;
   for (;;) {
     const uint32_t cand = L.state == ST_RUNNING ? max(L.e, port) : NEVER;
-    const uint64_t best = warp_min_u64(((uint64_t)cand << 32) | (L.state == ST_RUNNING ? L.gw : NEVER));
-    const uint32_t T = (uint32_t)(best >> 32);
+    const uint64_t key = ((uint64_t)cand << 32) | (L.state == ST_RUNNING ? L.gw : NEVER);
+    uint64_t best = key;  // my scheduler's best offer
+    for (uint32_t o = S.schedulers; o < 32u; o <<= 1) {
+      const uint64_t v = __shfl_xor_sync(FULL, best, o);
+      best = v < best ? v : best;
+    }
+    const uint32_t Ts = (uint32_t)(best >> 32);
+    const uint32_t T = __reduce_min_sync(FULL, Ts);
     if (T == NEVER) break;
     if (T >= CLOCK_LIMIT) {
       status = KS_ST_SCHED_LIMIT;
       break;
     }
-    const uint32_t w = __ffs(__ballot_sync(FULL, L.state == ST_RUNNING && L.gw == (uint32_t)best)) - 1u;
-    uint32_t ev = 0;  // 1: arrived at a barrier or finished
-    if (lane == w) {
+    bool win = L.state == ST_RUNNING && key == best && Ts == T;
+    if (one_at_a_time) {  // only the lowest warp id among this cycle's offers
+      const uint32_t gmin = __reduce_min_sync(FULL, win ? L.gw : NEVER);
+      win = win && L.gw == gmin;
+    }
+    uint32_t ev = 0;  // arrived at a barrier or finished
+    if (win) {
       L.not_selected += T - L.e;
-      if (L.e > L.base) L.stall[L.bind] += L.e - L.base;
-      const DevInsn& d = prog[L.pc];
-      const uint32_t wr = T + d.wlat;
-      if (d.inc & INC_RDEST) {
-        ready[ready_of_row(d.d)] = wr;
-        rkind[ready_of_row(d.d)] = kind[L.pc];
+      if (L.e > L.base) {
+        const uint64_t d = L.e - L.base;
+        if (L.bind == K_MEM) L.st_mem += d;
+        else if (L.bind == K_MATH) L.st_math += d;
+        else L.st_exec += d;
       }
-      if (d.inc & INC_PDEST) {
-        ready[ready_of_pred(d.hd)] = wr;
-        rkind[ready_of_pred(d.hd)] = kind[L.pc];
-      }
-      L.max_ready = max(L.max_ready, wr);
-      L.drain = max(L.drain, T + d.dlat);
+      const uint4 q = L.r.q, lt = L.r.lat;
+      const uint32_t flags = (q.w >> 8) & 0xFFu;
+      const uint64_t wr = T + lt.x;
+      const uint64_t entry = wr | ((uint64_t)(q.w >> 16) << 32);
+      if (flags & F_RDEST) ready[q.y >> 16] = entry;
+      if (flags & F_PDEST) ready[S.n_rows + (q.w & 0xFFu)] = entry;
+      L.max_ready = max(L.max_ready, (uint32_t)wr);
+      L.drain = max(L.drain, T + lt.y);
       L.t_last = T;
-      L.t_next = T + d.nlat;
+      L.t_next = T + lt.z;
       L.base = T + 1u;
       L.issued++;
-      const bool bar = d.op == OP_BAR;
       const bool more = advance(true);
-      if (bar) {
+      if (flags & F_BAR) {
         L.state = ST_WAITING;
         L.arrival = T;
         ev = 1;
@@ -262,8 +304,18 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
         ev = 1;
       }
     }
-    if (my_sched == w % S.schedulers) port = T + 1u;
-    if (__shfl_sync(FULL, ev, w)) settle(w / S.wpc);
+    // the winning schedulers' ports move on
+    const uint32_t won = __ballot_sync(FULL, win);
+    for (uint32_t m = won; m; m &= m - 1u)
+      if (my_sched == (uint32_t)(__ffs(m) - 1) % S.schedulers) port = T + 1u;
+    // settle every CTA slot in which a warp arrived or finished
+    for (uint32_t m = __ballot_sync(FULL, ev != 0u); m;) {
+      const uint32_t c = (uint32_t)(__ffs(m) - 1) / S.wpc;
+      settle(c);
+      const uint32_t lo = c * S.wpc;
+      const uint32_t slot_mask = (S.wpc >= 32u ? FULL : ((1u << S.wpc) - 1u)) << lo;
+      m &= ~slot_mask;
+    }
   }
 
   // SM totals (each lane added its own warps)
@@ -284,8 +336,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
 }  // namespace
 
 size_t sched_smem_bytes(uint32_t n_insn, uint32_t n_rows) {
-  const size_t prog = ((size_t)(n_insn + 1) * (sizeof(DevInsn) + 1) + 15u) / 16u * 16u;
-  return prog + 32u * (size_t)(n_rows + 32u) * 5u;
+  return (size_t)(n_insn + 1) * 32u + 32u * (size_t)(n_rows + 32u) * 8u;
 }
 
 int launch_sched(const KsLaunch& L, uint32_t n_rows, uint32_t n_sm, uint32_t ctas_per_sm, uint32_t schedulers,
