@@ -203,7 +203,7 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 // so that the other kernels keep the register budget of the plain loop. BIG:
 // CTA mode for blocks of 9..32 warps (a 1024-thread real CTA, at most 64
 // registers a thread, so it spills: slower, used only for such blocks).
-template <bool CTA, bool BIG, bool INSTR>
+template <bool CTA, bool BIG, bool INSTR, bool RUNLOG>
 __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __grid_constant__ KsLaunch L) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t lane = threadIdx.x & 31u;
@@ -347,8 +347,8 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
       // mask is not empty and pc is not the reconvergence pc here; `fuel_in` =
       // instructions that may run before the reconvergence pc or the end of the
       // step budget.
-      if constexpr (INSTR) {
-        if (L.sched_log && pc != run_next) {  // a new run: log the one that ended
+      if constexpr (RUNLOG) {
+        if (pc != run_next) {  // a new run: log the one that ended
           if (run_next != run_start) {
             if (lane == 0 && n_runs < L.sched_cap)
               L.sched_log[(uint64_t)gw * L.sched_cap + n_runs] = (run_start << 16) | (run_next - run_start - 1u);
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
         pc += run_n;
         budget -= run_n;
         t_last = t_next - 1u;
-        if constexpr (INSTR) run_next = pc;
+        if constexpr (RUNLOG) run_next = pc;
         continue;
       }
       // ---- mid path: runs of the other unguarded register-to-register ops
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
         pc += steps;
         budget -= steps;
         t_last = t_next - 1u;
-        if constexpr (INSTR) run_next = pc;
+        if constexpr (RUNLOG) run_next = pc;
         continue;
       }
       // ---- general path: one instruction; every operand / ready-time load at once
@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
             n_dropped++;
           }
           pc++;
-          if constexpr (INSTR) run_next = pc;
+          if constexpr (RUNLOG) run_next = pc;
           continue;
         }
         if (op == OP_EXIT) {  // reached the virtual exit: the remaining lanes finish
@@ -1013,7 +1013,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
 #undef A64
 #undef B64
 #undef C64
-      if constexpr (INSTR) run_next = pc_here + consumed;
+      if constexpr (RUNLOG) run_next = pc_here + consumed;
       if (status != 0) {
         FLUSH_THREADS();
         break;
@@ -1079,7 +1079,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
 #undef FLUSH_THREADS
     const uint64_t warp_insts = stop_at - left - budget;
     if constexpr (INSTR) {
-      if (L.sched_log) {  // the last run, and the count
+      if constexpr (RUNLOG) {  // the last run, and the count
         if (run_next != run_start) {
           if (lane == 0 && n_runs < L.sched_cap)
             L.sched_log[(uint64_t)gw * L.sched_cap + n_runs] = (run_start << 16) | (run_next - run_start - 1u);
@@ -1182,17 +1182,25 @@ size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t w
 static int g_attr_done[64];
 
 // The instantiation that runs a launch: CTA mode (9..32 warps: the 1024-thread
-// form), and the instrumented form for the cache model's passes and the
-// per-instruction profile (the lean forms carry neither).
-static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, bool instr) {
-  if (!cta) return instr ? (const void*)ks_interp_kernel<false, false, true> : (const void*)ks_interp_kernel<false, false, false>;
-  if (real_warps_per_cta > 8)
-    return instr ? (const void*)ks_interp_kernel<true, true, true> : (const void*)ks_interp_kernel<true, true, false>;
-  return instr ? (const void*)ks_interp_kernel<true, false, true> : (const void*)ks_interp_kernel<true, false, false>;
+// form); the instrumented form for the cache model's passes and the
+// per-instruction profile, and that form with the issue-run log for the SM
+// issue model (the lean forms carry none of it).
+template <bool CTA, bool BIG>
+static const void* interp_fn_of(int form) {
+  return form == 0   ? (const void*)ks_interp_kernel<CTA, BIG, false, false>
+         : form == 1 ? (const void*)ks_interp_kernel<CTA, BIG, true, false>
+                     : (const void*)ks_interp_kernel<CTA, BIG, true, true>;
 }
 
-static bool instrumented(const KsLaunch& L) {
-  return L.cache_pass != 0 || L.profile != nullptr || L.sched_log != nullptr;
+static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, int form) {
+  if (!cta) return interp_fn_of<false, false>(form);
+  if (real_warps_per_cta > 8) return interp_fn_of<true, true>(form);
+  return interp_fn_of<true, false>(form);
+}
+
+static int form_of(const KsLaunch& L) {
+  if (L.sched_log != nullptr) return 2;
+  return (L.cache_pass != 0 || L.profile != nullptr) ? 1 : 0;
 }
 
 static int ensure_attr() {
@@ -1205,9 +1213,9 @@ static int ensure_attr() {
   if (e != cudaSuccess) return (int)e;
   for (int cta = 0; cta < 2; cta++)
     for (int big = 0; big < 2; big++)
-      for (int instr = 0; instr < 2; instr++) {
+      for (int form = 0; form < 3; form++) {
         if (!cta && big) continue;
-        e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, instr), cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+        e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, form), cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
         if (e != cudaSuccess) return (int)e;
       }
   if (dev < 64) g_attr_done[dev] = 1;
@@ -1217,7 +1225,7 @@ static int ensure_attr() {
 int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm) {
   int e = ensure_attr();
   if (e) return e;
-  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, instrumented(L));
+  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L));
   return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, (int)(real_warps_per_cta * 32), smem);
 }
 
@@ -1272,7 +1280,7 @@ int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_
   const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, real_warps_per_cta,
                                        L.cta_mode ? L.shared_bytes : 0u);
   void* args[] = {const_cast<KsLaunch*>(&L)};
-  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, real_warps_per_cta, instrumented(L)), dim3(real_ctas),
+  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L)), dim3(real_ctas),
                                dim3(real_warps_per_cta * 32), args, smem, (cudaStream_t)stream);
 }
 

@@ -209,3 +209,9 @@ def test_fuzz_full_size_properties(i):
     assert np.array_equal(r.cache_warps["n_access"].astype(np.uint64), rs["ld_req"] + rs["st_req"])
     levels, valid = _replay_levels(r.cache_warps, r.cache_log, cache.l1_lines, cache.l2_lines)
     assert np.array_equal(r.cache_log["level"][valid], levels[valid])
+
+
+@pytest.mark.parametrize("block", [512, 1024])
+def test_large_blocks(block):
+    # CTA mode with 16 and 32 warps (the 1024-thread instantiation)
+    wl_check(wl.smem_reduce(n=block * 4, block=block))

@@ -100,3 +100,10 @@ def test_profile_too_small_is_refused():
     dev = [(b.sim_base, torch.from_numpy(b.data.view(np.uint8)).cuda()) for b in w.fresh_buffers()]
     with pytest.raises(ks.KsError):
         ks.run(mod, w.kernel, w.grid, w.block, w.params, dev, config=ks.Config(profile=prof))
+
+
+@pytest.mark.parametrize("block", [512, 1024])
+def test_profile_large_blocks(block):
+    w = wl.smem_reduce(n=block * 3, block=block)
+    o, _ = oracle_profile(w)
+    assert np.array_equal(gpu_profile(w).view(np.uint8), o.view(np.uint8))

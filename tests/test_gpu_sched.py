@@ -145,3 +145,10 @@ def test_warp_sweep_matches_oracle():
     assert [r["active_warps"] for r in rows] == [1, 1, 2, 4, 16]
     ipc = [r["instructions_per_cycle"] for r in rows]
     assert ipc[0] == ipc[1] and abs(ipc[3] - 4 * ipc[1]) < 1e-9 and abs(ipc[4] - 4 * ipc[3]) < 1e-9
+
+
+@pytest.mark.parametrize("block", [512, 1024])
+def test_large_blocks(block):
+    w = wl.smem_reduce(n=block * 5, block=block)
+    check(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in w.fresh_buffers()],
+          n_sm=2, schedulers=4, max_ts=w.max_ts)
