@@ -43,14 +43,6 @@ struct SchedLaunch {
   ks_sched_sm* sms_out;
 };
 
-__device__ __forceinline__ uint64_t warp_min_u64(uint64_t v) {
-  for (int o = 16; o > 0; o >>= 1) {
-    const uint64_t w = __shfl_xor_sync(FULL, v, o);
-    v = w < v ? w : v;
-  }
-  return v;
-}
-
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) { return __reduce_max_sync(FULL, v); }
 
 // What the replay needs of a program entry, 32 bytes:
@@ -69,14 +61,13 @@ struct Lane {
   uint32_t pc, run_left, k, n_runs;  // next entry to issue; entries left in its run; next run index
   uint32_t t_next, t_last, max_ready, drain, base, start, e, bind, arrival, end;
   Rec r;                             // the record of the next entry
-  uint64_t issued, not_selected, st_exec, st_mem, st_math, stall_bar;
+  uint32_t issued, not_selected, st_exec, st_mem, st_math, stall_bar;  // each below the 2^31 clock limit
 };
 
-// ready table entry: ready time | kind of the producer << 32
-__device__ __forceinline__ void take(uint64_t v, uint32_t& e, uint32_t& kind) {
-  const uint32_t t = (uint32_t)v, k = (uint32_t)(v >> 32);
-  if (t > e) { e = t; kind = k; }
-  else if (t == e && k > kind) kind = k;
+// ready table entry: ready time | kind of the producer << 32; the kind of a
+// term counts when its time is the latest
+__device__ __forceinline__ uint32_t kind_at(uint64_t v, uint32_t e) {
+  return (uint32_t)v == e ? (uint32_t)(v >> 32) : K_EXEC;
 }
 
 __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ SchedLaunch S) {
@@ -114,7 +105,10 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
   __syncwarp();
 
   const uint32_t slots = S.ctas_per_sm * S.wpc;  // resident warp slots (<= 32)
-  const uint32_t my_sched = lane % S.schedulers;
+  const uint32_t my_sched = lane & (S.schedulers - 1u);  // schedulers: 1, 2 or 4
+  // the lanes of my scheduler
+  const uint32_t sched_lanes = (S.schedulers == 1u ? 0xFFFFFFFFu : S.schedulers == 2u ? 0x55555555u : 0x11111111u)
+                               << my_sched;
   Lane L;
   L.state = ST_EMPTY;
   L.cta_slot = lane / S.wpc;
@@ -150,18 +144,20 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     const uint32_t P = S.n_rows;
     const uint64_t va = ready[q.x & 0xFFFFu], vb = ready[q.x >> 16], vc = ready[q.y & 0xFFFFu],
                    vd = ready[q.y >> 16], vg = ready[P + (q.z & 0xFFu)];
-    uint32_t e = L.t_next, kind = K_EXEC;
-    take(va, e, kind);
-    take(vb, e, kind);
-    take(vc, e, kind);
-    take(vd, e, kind);
-    take(vg, e, kind);
+    uint32_t e = max(max(L.t_next, max((uint32_t)va, (uint32_t)vb)),
+                     max(max((uint32_t)vc, (uint32_t)vd), (uint32_t)vg));
+    uint64_t p0 = 0, p1 = 0, p2 = 0, p3 = 0;
     if ((q.w >> 8) & F_PHAZ) {
-      take(ready[P + ((q.z >> 8) & 0xFFu)], e, kind);
-      take(ready[P + ((q.z >> 16) & 0xFFu)], e, kind);
-      take(ready[P + (q.z >> 24)], e, kind);
-      take(ready[P + (q.w & 0xFFu)], e, kind);
+      p0 = ready[P + ((q.z >> 8) & 0xFFu)];
+      p1 = ready[P + ((q.z >> 16) & 0xFFu)];
+      p2 = ready[P + (q.z >> 24)];
+      p3 = ready[P + (q.w & 0xFFu)];
+      e = max(e, max(max((uint32_t)p0, (uint32_t)p1), max((uint32_t)p2, (uint32_t)p3)));
     }
+    // the t_next term (a branch's latency) is an execution wait: kind 0
+    const uint32_t kind = max(max(max(kind_at(va, e), kind_at(vb, e)), max(kind_at(vc, e), kind_at(vd, e))),
+                              max(max(kind_at(vg, e), kind_at(p0, e)),
+                                  max(max(kind_at(p1, e), kind_at(p2, e)), kind_at(p3, e))));
     L.e = e;
     L.bind = kind;
   };
@@ -242,9 +238,8 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     if (__any_sync(FULL, mine && L.state != ST_EMPTY)) settle(c);
   }
 
-  // Every step, each scheduler's best offer (earliest cycle, then lowest
-  // global warp id) is found with shuffles over the lanes of that scheduler;
-  // the schedulers whose offer is at the earliest cycle of all issue at once.
+  // Every step the earliest offer of all is found, and for each scheduler the
+  // lowest global warp id offering it; those schedulers issue at once.
   // That is the order of one issue at a time: what an issue changes for other
   // warps (a barrier release, a new CTA) takes effect a cycle later at the
   // soonest, so issues of the same cycle on different schedulers do not see
@@ -252,30 +247,35 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
   // same cycle, and the schedulers take turns one issue at a time.
   const bool one_at_a_time = S.lat[KS_LAT_BAR] == 0u;
   for (;;) {
+    // the earliest offer, then per scheduler the lowest warp id offering it
     const uint32_t cand = L.state == ST_RUNNING ? max(L.e, port) : NEVER;
-    const uint64_t key = ((uint64_t)cand << 32) | (L.state == ST_RUNNING ? L.gw : NEVER);
-    uint64_t best = key;  // my scheduler's best offer
-    for (uint32_t o = S.schedulers; o < 32u; o <<= 1) {
-      const uint64_t v = __shfl_xor_sync(FULL, best, o);
-      best = v < best ? v : best;
-    }
-    const uint32_t Ts = (uint32_t)(best >> 32);
-    const uint32_t T = __reduce_min_sync(FULL, Ts);
+    const uint32_t T = __reduce_min_sync(FULL, cand);
     if (T == NEVER) break;
     if (T >= CLOCK_LIMIT) {
       status = KS_ST_SCHED_LIMIT;
       break;
     }
-    bool win = L.state == ST_RUNNING && key == best && Ts == T;
-    if (one_at_a_time) {  // only the lowest warp id among this cycle's offers
-      const uint32_t gmin = __reduce_min_sync(FULL, win ? L.gw : NEVER);
-      win = win && L.gw == gmin;
+    const bool at_T = cand == T;
+    uint32_t gmin;
+    if (one_at_a_time || S.schedulers == 1u) {
+      gmin = __reduce_min_sync(FULL, at_T ? L.gw : NEVER);
+    } else {
+      const uint32_t g = at_T ? L.gw : NEVER;
+      const uint32_t m0 = __reduce_min_sync(FULL, my_sched == 0u ? g : NEVER);
+      const uint32_t m1 = __reduce_min_sync(FULL, my_sched == 1u ? g : NEVER);
+      uint32_t m2 = NEVER, m3 = NEVER;
+      if (S.schedulers == 4u) {
+        m2 = __reduce_min_sync(FULL, my_sched == 2u ? g : NEVER);
+        m3 = __reduce_min_sync(FULL, my_sched == 3u ? g : NEVER);
+      }
+      gmin = my_sched == 0u ? m0 : my_sched == 1u ? m1 : my_sched == 2u ? m2 : m3;
     }
+    const bool win = at_T && L.gw == gmin;
     uint32_t ev = 0;  // arrived at a barrier or finished
     if (win) {
       L.not_selected += T - L.e;
       if (L.e > L.base) {
-        const uint64_t d = L.e - L.base;
+        const uint32_t d = L.e - L.base;
         if (L.bind == K_MEM) L.st_mem += d;
         else if (L.bind == K_MATH) L.st_math += d;
         else L.st_exec += d;
@@ -305,9 +305,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
       }
     }
     // the winning schedulers' ports move on
-    const uint32_t won = __ballot_sync(FULL, win);
-    for (uint32_t m = won; m; m &= m - 1u)
-      if (my_sched == (uint32_t)(__ffs(m) - 1) % S.schedulers) port = T + 1u;
+    if (__ballot_sync(FULL, win) & sched_lanes) port = T + 1u;
     // settle every CTA slot in which a warp arrived or finished
     for (uint32_t m = __ballot_sync(FULL, ev != 0u); m;) {
       const uint32_t c = (uint32_t)(__ffs(m) - 1) / S.wpc;
