@@ -362,6 +362,54 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
       const uint32_t fuel_in = min(budget, rpc > pc ? rpc - pc : 0xFFFFFFFFu);
       const bool runnable = fuel_in != 0u && t_next < REBASE_AT;
 
+      // ---- a setp fused with the bra after it (32-bit or f32 compare): the
+      // setp issues here as the general path issues it, and the bra with it
+      // when every active lane goes the same way (else the bra takes the
+      // general path next), without the general path's operand loads and
+      // dispatch. The setp is unguarded, so every active lane executes it.
+      if (runnable && (q1.w & INC_FUSE) && (q0.x == OP_SETP_U32 || q0.x == OP_SETP_S32 || q0.x == OP_SETP_F32)) {
+        const uint2 sa = SM2(lb + q1.x), sb = SM2(lb + q1.y);
+        const uint32_t sop = q0.x, saux = q0.z, cmp = saux & 0xFFu, pd = (saux >> 8) & 0xFFu;
+        bool lt, eq, gt;
+        if (sop == OP_SETP_F32) {
+          const float x = __uint_as_float(sa.x), y = __uint_as_float(sb.x);
+          lt = x < y; eq = x == y; gt = x > y;
+        } else {
+          const uint32_t flip = sop == OP_SETP_S32 ? 0x80000000u : 0u;  // signed order
+          const uint32_t x = sa.x ^ flip, y = sb.x ^ flip;
+          lt = x < y; eq = x == y; gt = x > y;
+        }
+        const uint32_t bal = __ballot_sync(FULL, rel_result(lt, eq, gt, cmp));
+        // its scoreboard: the sources, and the predicate it writes (the
+        // other hazard entries of an unguarded setp are the always-true
+        // predicate and the zero row, ready at 0)
+        const uint32_t t = max(max(t_next, sa.y), max(sb.y, SM32(wb + q3.y)));
+        const uint32_t wr = t + q0.y;
+        SM32(wb + q3.y) = wr;
+        if (lane == pd) my_pred = (my_pred & ~mask) | (bal & mask);
+        max_ready = max(max_ready, wr);
+        drain = max(drain, t + q3.z);
+        t_last = t;
+        t_next = t + q3.w;
+        budget--;
+        const uint32_t pc_setp = pc;
+        pc++;
+        const uint32_t taken = mask & (bal ^ (((saux >> 16) & 1u) ? 0xFFFFFFFFu : 0u));
+        if ((taken == mask || taken == 0u) && budget != 0u && pc != rpc && t_next < REBASE_AT) {
+          const uint32_t t2 = max(t_next, wr);  // the bra waits for its guard
+          max_ready = max(max_ready, t2);
+          drain = max(drain, t2);
+          t_last = t2;
+          t_next = t2 + L.lat[KS_LAT_BRA];
+          budget--;
+          pc = taken ? (saux >> 17) : pc + 1u;
+          if constexpr (RUNLOG) run_next = pc_setp + 2u;
+        } else {
+          if constexpr (RUNLOG) run_next = pc_setp + 1u;
+        }
+        continue;
+      }
+
       // ---- fast path: runs of unguarded routed FPU / IMAD instructions.
       // pc, budget and t_last are rebuilt when the run ends. Software-pipelined:
       // while instruction k executes, the rows of instruction k+1 are loaded and
