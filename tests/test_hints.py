@@ -176,3 +176,64 @@ def test_library_matches_restatement_on_workloads(name):
     p = oh.profile(e, n)
     assert int(p["requests"].sum()) == int(((e["kind"] == oh.EV_GLOBAL) | (e["kind"] == oh.EV_SHARED)).sum())
     assert int(p["divergent"].sum()) == int((e["kind"] == oh.EV_DIVERGE).sum())
+
+
+SPLIT = wl.HEADER + """.visible .entry sp(.param .u32 p_k)
+{
+    .reg .pred %p<2>;
+    .reg .b32 %r<5>;
+    ld.param.u32    %r1, [p_k];
+    mov.u32         %r2, %tid.x;
+    setp.lt.u32     %p1, %r2, %r1;
+    @%p1 bra        TAKEN;
+    add.u32         %r3, %r2, 1;
+TAKEN:
+    ret;
+}
+"""
+
+
+@pytest.mark.parametrize("k, message", [(16, "High divergence (50%)"), (13, "High divergence (40%)"),
+                                        (19, "High divergence (40%)"), (12, None), (1, None)])
+def test_divergence_ratio_of_a_split(k, message):
+    """k lanes take the branch and 32 - k fall through: the ratio is the
+    smaller side over the 32 active lanes (13/32 = 0.406, 12/32 = 0.375)."""
+    r, e = oracle.run_events(SPLIT, "sp", 1, 32, wl.pack_params([("u32", k)]), [])
+    assert r.status == 0
+    d = e[e["kind"] == oh.EV_DIVERGE]
+    assert len(d) == 1 and (int(d[0]["a"]), int(d[0]["b"])) == (k, 32 - k)
+    got = [h["message"] for h in oh.aggregate(e) if h["category"] == oh.DIVERGENCE]
+    assert got == ([message] if message else [])
+
+
+WIDE = wl.HEADER + """.visible .entry wd(.param .u64 p_in, .param .u32 p_lanes)
+{
+    .reg .pred %p<2>;
+    .reg .b32 %r<5>;
+    .reg .b64 %rd<6>;
+    ld.param.u64    %rd1, [p_in];
+    ld.param.u32    %r1, [p_lanes];
+    mov.u32         %r2, %tid.x;
+    cvt.u64.u32     %rd2, %r2;
+    shl.b64         %rd2, %rd2, 7;
+    add.s64         %rd3, %rd1, %rd2;
+    setp.lt.u32     %p1, %r2, %r1;
+    @%p1 ld.global.u64 %rd4, [%rd3];
+    ret;
+}
+"""
+
+
+@pytest.mark.parametrize("lanes, message", [(32, "Poor memory efficiency (6%)"), (16, "Poor memory efficiency (6%)"),
+                                            (8, "Poor memory efficiency (12%)"), (2, None)])
+def test_efficiency_counts_the_executing_lanes(lanes, message):
+    """8-byte loads, one line per lane: ideal = ceil(lanes * 8 / 128) lines
+    (2 for 32 lanes, 1 for 16 or fewer), efficiency ideal / lanes."""
+    src = np.zeros(32 * 32 + 64, dtype=np.uint32)
+    params = wl.pack_params([("u64", 0x1000_0000), ("u32", lanes)])
+    r, e = oracle.run_events(WIDE, "wd", 1, 32, params, [(0x1000_0000, src)])
+    assert r.status == 0
+    g = e[e["kind"] == oh.EV_GLOBAL]
+    assert len(g) == 1 and (int(g[0]["a"]), int(g[0]["b"]), int(g[0]["c"])) == (lanes, lanes, 8)
+    got = [h["message"] for h in oh.aggregate(e)]
+    assert got == ([message] if message else [])
