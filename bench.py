@@ -39,7 +39,8 @@ import numpy as np  # noqa: E402
 
 METRIC = "simulated thread-instructions/sec"
 UNIT = "thread-inst/s"
-KERNEL_SRC = os.path.join(ROOT, "simt_ptx_interpretation_gb300", "csrc", "ks_interp.cu")
+KERNEL_SRC = [os.path.join(ROOT, "simt_ptx_interpretation_gb300", "csrc", f)
+              for f in ("ks_interp_kernel.cuh", "ks_interp.cu", "ks_batch.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_SM_MHZ = 2070.0
@@ -62,6 +63,11 @@ def parse_args():
                         "rounded up to a power of two")
     p.add_argument("--sched", action="store_true", help="simulate with the SM-level issue model")
     p.add_argument("--sched-sms", type=int, default=152, help="simulated SMs (--sched)")
+    p.add_argument("--streams", type=int, default=0,
+                   help="CUDA streams the step's independent calls are spread over (0: one per launch, at most 8, "
+                        "with --sched; else 1)")
+    p.add_argument("--no-batch", action="store_true",
+                   help="one ks_simulate per launch instead of one ks_simulate_batch per step")
     p.add_argument("--scale", type=int, default=1,
                    help="divide the gather outputs, divergent threads or fuzz kernels (smaller cases for profiling)")
     return p.parse_args()
@@ -182,7 +188,11 @@ class ClockSampler:
 
 
 def kernel_sha() -> str:
-    return hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    """Hash of the interpreter kernel's sources (the kernel and its launchers)."""
+    h = hashlib.sha256()
+    for f in KERNEL_SRC:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(workload: str):
@@ -229,6 +239,15 @@ def run_ours(args, world, rank, local):
         tr = (torch.empty(ks.trace_bytes(w.grid, w.block, w.max_ts, mod.record_bytes(w.kernel)), dtype=torch.uint8,
                           device=dev) if w.max_ts else None)
         jobs.append(dict(w=w, mod=mod, bufs=bufs, cfg=cfg, st=st, tr=tr))
+    # The step's launches are independent simulations (own buffers, stats and
+    # trace). Plain runs go to the GPU as one batch (ks_simulate_batch: their
+    # warps share one real grid). With the SM model, whose calls hold the
+    # GPU with a small replay grid, they may be spread over streams forked
+    # from and joined to `stream`.
+    batch = not (args.cache or args.sched or args.no_batch) and len(jobs) > 1
+    n_streams = args.streams if args.streams > 0 else (min(len(jobs), 8) if args.sched else 1)
+    n_streams = max(1, min(n_streams, len(jobs)))
+    streams = [stream] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
     cap = args.cache_cap
     if args.cache and cap <= 0:  # size the log from an untimed plain run
         most = 1
@@ -244,7 +263,7 @@ def run_ours(args, world, rank, local):
         nbytes = ks.cache_workspace_bytes(wmax.grid, wmax.block, cache)
         if nbytes == 0:
             raise SystemExit("invalid cache configuration")
-        cache_ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        cache_ws = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
         config = dict(config, cache_model={"l1_lines": cache.l1_lines, "l2_lines": cache.l2_lines,
                                            "lat_l1": cache.lat_l1, "lat_l2": cache.lat_l2,
                                            "max_accesses_per_warp": cache.max_accesses_per_warp})
@@ -268,26 +287,61 @@ def run_ours(args, world, rank, local):
             runs = max(runs, int(tmp[:w.warps * 4].view(torch.int32).max().item()))
             del tmp
         sched = ks.SchedConfig(n_sm=args.sched_sms, max_runs_per_warp=1 << (runs - 1).bit_length())
-        sched_ws = torch.empty(ks.sched_workspace_bytes(wmax.grid, wmax.block, sched), dtype=torch.uint8, device=dev)
-        sched_w = torch.empty(wmax.warps * 64, dtype=torch.uint8, device=dev)
-        sched_s = torch.empty(args.sched_sms * 32, dtype=torch.uint8, device=dev)
+        nbytes = ks.sched_workspace_bytes(wmax.grid, wmax.block, sched)
+        sched_ws = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
+        sched_w = [torch.empty(wmax.warps * 64, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
+        sched_s = [torch.empty(args.sched_sms * 32, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
         config = dict(config, sm_model={"n_sm": sched.n_sm, "schedulers_per_sm": sched.schedulers_per_sm,
                                         "ctas_per_sm": "fill 32 warps", "max_runs_per_warp": sched.max_runs_per_warp})
 
-    def launch(j):
-        w = j["w"]
+    def launch(i):
+        j, q = jobs[i], i % n_streams
+        w, s = j["w"], streams[q]
         if sched:
-            ks.simulate_sched(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], sched_w, sched_s,
-                              sched_ws, j["tr"], j["cfg"], sched, stream)
+            ks.simulate_sched(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], sched_w[q],
+                              sched_s[q], sched_ws[q], j["tr"], j["cfg"], sched, s)
         elif cache:
-            ks.simulate_cached(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], cache_ws, j["tr"],
-                               j["cfg"], cache, stream)
+            ks.simulate_cached(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], cache_ws[q], j["tr"],
+                               j["cfg"], cache, s)
         else:
-            ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"], stream)
+            ks.simulate(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], j["tr"], j["cfg"], s)
 
-    def step():
-        for j in jobs:
-            launch(j)
+    def fork():
+        if n_streams > 1:
+            e = torch.cuda.Event()
+            e.record(stream)
+            for s in streams[1:]:
+                s.wait_event(e)
+
+    def join():
+        for s in streams[1:]:
+            e = torch.cuda.Event()
+            e.record(s)
+            stream.wait_event(e)
+
+    batch_launches = [0]  # real kernel launches of the last batch call
+
+    def launch_batch():
+        batch_launches[0] = ks.simulate_batch(
+            [ks.BatchItem(j["mod"], j["w"].kernel, j["w"].grid, j["w"].block, j["w"].params, j["bufs"], j["st"],
+                          j["tr"], j["cfg"]) for j in jobs], stream)
+
+    def step(lev=None):
+        if batch:
+            if lev:
+                lev[0][0].record(stream)
+            launch_batch()
+            if lev:
+                lev[0][1].record(stream)
+            return
+        fork()
+        for i in range(len(jobs)):
+            if lev:
+                lev[i][0].record(streams[i % n_streams])
+            launch(i)
+            if lev:
+                lev[i][1].record(streams[i % n_streams])
+        join()
 
     # work per step (deterministic): one run, reduce totals, check statuses
     step()
@@ -305,8 +359,10 @@ def run_ours(args, world, rank, local):
         step()
     torch.cuda.synchronize(dev)
 
-    n_launch = len(jobs)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_launch + 1)] for _ in range(args.steps)]
+    n_launch = 1 if batch else len(jobs)  # timed calls per step
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    lev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_launch)]
+           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
@@ -314,14 +370,13 @@ def run_ours(args, world, rank, local):
         for k in range(args.steps):
             flush.zero_()
             evs[k][0].record(stream)
-            for i, j in enumerate(jobs):
-                launch(j)
-                evs[k][i + 1].record(stream)
+            step(lev[k])
+            evs[k][1].record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
     barrier(world)
-    step_ms = [evs[k][0].elapsed_time(evs[k][n_launch]) for k in range(args.steps)]
-    launch_ms = [[evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)] for i in range(n_launch)]
+    step_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
+    launch_ms = [[lev[k][i][0].elapsed_time(lev[k][i][1]) for k in range(args.steps)] for i in range(n_launch)]
     dev_s = sum(step_ms) / 1e3
     dev_s = max_over_ranks(dev_s, world)
     value = insts * args.steps * world / dev_s
@@ -331,17 +386,24 @@ def run_ours(args, world, rank, local):
     mhz, peak_src = sm_peak_mhz()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     peak = sms * 4 * 32 * mhz * 1e6 / 1e9  # G thread-inst/s: 4 warp-issues per SM per clock, 32 lanes
-    mean_launch_s = sum(sum(x) for x in launch_ms) / (args.steps * n_launch) / 1e3
+    # Every kernel of a step is a ks_interp_kernel launch (plus, with the
+    # models, their own kernels): the launches of one step may run
+    # concurrently, so the roofline takes the step's algorithmic units over
+    # the span from the first launch's start to the last one's end (the
+    # step's events; nothing else runs inside them).
+    span_s = sum(step_ms) / args.steps / 1e3
     # with the cache model a call interprets the launch twice (and sorts in
     # between): charge the whole call to the two interpreter passes
     passes = 2 if cache else 1  # (the SM model's replay runs once per call)
-    achieved = passes * (insts / n_launch) / mean_launch_s / 1e9
+    achieved = passes * insts / span_s / 1e9
     traffic = traffic_for(config["workload"])
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "Gthread-inst/s",
                 "frac": round(achieved / peak, 5), "traffic": traffic,
                 "peak_source": f"{sms} SMs x 4 issue/clk x 32 lanes x {mhz:.0f} MHz ({peak_src})",
                 "algorithmic_units_per_launch": [int(x) for x in launch_insts],
-                "launch_ms_mean": [round(sum(x) / len(x), 4) for x in launch_ms]}
+                "launch_ms_mean": [round(sum(x) / len(x), 4) for x in launch_ms],
+                "streams": n_streams, "batched": batch,
+                "timed_over": "each step's span (its launches may overlap)"}
     if cache:
         roofline["note"] = ("each call runs ks_interp_kernel twice plus the level kernels and radix sorts; "
                             "achieved counts both passes over the whole call's time")
@@ -350,18 +412,22 @@ def run_ours(args, world, rank, local):
                             "simulated thread-instructions over the whole call's time")
 
     # end to end through the public API with pinned host buffers
-    e2e = None if args.no_e2e else run_e2e(args, jobs, insts, dev, stream, launch)
+    e2e = None if args.no_e2e else run_e2e(args, jobs, insts, dev, streams, launch, fork, join,
+                                           launch_batch if batch else None)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(sum(step_ms) / len(step_ms), 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)", "data": "synthetic (seeded)",
-        "config": dict(config, l2="flushed between steps (256 MiB write)", parallelism=f"replicas{world}"),
+        "config": dict(config, l2="flushed between steps (256 MiB write)", parallelism=f"replicas{world}",
+                       streams=n_streams, batched=batch),
         # our kernels per call: the interpreter, or (cache model) two interpreter
         # passes and the four level kernels (the radix sorts and the scan are
         # library code)
         "roofline": roofline, "e2e": e2e,
-        "gpu_launches": args.steps * n_launch * (6 if cache else 2 if sched else 1),
+        # (a batch call reports its real launches)
+        "gpu_launches": args.steps * (batch_launches[0] if batch else n_launch * (6 if cache else 2 if sched
+                                                                                  else 1)),
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3), "kernel_sha": kernel_sha(),
     }
@@ -372,9 +438,12 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, jobs, insts, dev, stream, launch):
+def run_e2e(args, jobs, insts, dev, streams, launch, fork, join, launch_batch=None):
+    """The same step through the public API from pinned host memory: each
+    launch's inputs are copied in, it runs, and its outputs, stats and trace
+    are copied out, all on the launch's own stream (a batch: every input in,
+    the batch, every output out)."""
     import torch
-    import simt_ptx_interpretation_gb300 as ks
     pinned_in, pinned_out = [], []
     h2d = d2h = 0
     for j in jobs:
@@ -398,14 +467,28 @@ def run_e2e(args, jobs, insts, dev, stream, launch):
     for k in range(args.e2e_steps):
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for j, ins, outs in zip(jobs, pinned_in, pinned_out):
+        if launch_batch is not None:
+            with torch.cuda.stream(streams[0]):
+                for ins in pinned_in:
+                    for h, t in ins:
+                        t.copy_(h, non_blocking=True)
+                launch_batch()
+                for outs in pinned_out:
+                    for t, h in outs:
+                        h.copy_(t, non_blocking=True)
+            streams[0].synchronize()
+            times.append(time.perf_counter() - t0)
+            continue
+        fork()
+        for i, (ins, outs) in enumerate(zip(pinned_in, pinned_out)):
+            with torch.cuda.stream(streams[i % len(streams)]):
                 for h, t in ins:
                     t.copy_(h, non_blocking=True)
-                launch(j)
+                launch(i)
                 for t, h in outs:
                     h.copy_(t, non_blocking=True)
-        stream.synchronize()
+        join()
+        streams[0].synchronize()
         times.append(time.perf_counter() - t0)
     mean = sum(times) / len(times)
     return {"value": round(insts / mean, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),

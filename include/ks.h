@@ -295,7 +295,9 @@ int ks_profile_bytes(const ks_module* mod, const char* kernel, size_t* bytes);
  * KS_ERR_CUDA. The first call on a device
  * uploads the module's program there (one allocation per module per device).
  * Simulations that share output or store-target buffers must not overlap in
- * time. */
+ * time; others may be enqueued on different streams and run concurrently
+ * (they share only the read-only program copy), which is how small grids
+ * fill the GPU. */
 int ks_simulate(const ks_module* mod, const char* kernel, uint32_t grid, uint32_t block,
                 const void* params, size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs,
                 void* trace_buf, size_t trace_bytes, void* stats_buf, size_t stats_bytes,
@@ -323,6 +325,49 @@ int ks_simulate_static(const ks_module* mod, const char* kernel, uint32_t grid, 
                        const void* params, size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs,
                        void* trace_buf, size_t trace_bytes, void* stats_buf, size_t stats_bytes,
                        const ks_config* cfg, void* stream);
+
+/* ---- Batches (no counterpart on the pages) ----------------------------------
+ * Several simulated launches in one call, each with ks_simulate's arguments
+ * and each giving exactly ks_simulate's outputs (memory, stats, trace slots,
+ * profile), but with the items' warps spread over one real grid: a simulated
+ * grid of a few hundred warps leaves most of the GPU idle on its own, and one
+ * of many warps ends in a tail where its slowest warps run alone. */
+typedef struct ks_batch_item {
+  const ks_module* mod;
+  const char* kernel;
+  uint32_t grid, block;
+  const void* params;
+  size_t param_bytes;
+  const ks_buffer* bufs;
+  uint32_t n_bufs;
+  uint32_t reserved;      /* 0 */
+  void* trace_buf;        /* device, may be NULL */
+  size_t trace_bytes;
+  void* stats_buf;        /* device, W x 96 bytes */
+  size_t stats_bytes;
+  const ks_config* cfg;   /* NULL: ks_config_default */
+} ks_batch_item;
+
+/* Enqueues n_items simulations on `stream`. Every item is checked first as
+ * ks_simulate checks it; if one fails, its error is returned, *failed_item
+ * (if not NULL) is set to its index and nothing is launched (modules may
+ * still have been uploaded). Otherwise *failed_item = n_items and the items
+ * run in real grids of one kernel form each (the same mode, lean or
+ * profiled, and in CTA mode the same block), in the order of each grid's
+ * first item: at most 32 items and at most 16 simulated warps per SM of the
+ * GPU in a grid, so that a grid runs as one wave (an item larger than that
+ * fills the GPU alone and is launched as ks_simulate launches it). Within a
+ * grid the real CTAs are shared out in proportion to the items' simulated
+ * warps (CTAs in CTA mode); when every simulated warp fits on the GPU at
+ * once, the grid is a multiple of the SM count with the same number of real
+ * warps on every SM. Items must not share
+ * output, trace, stats, profile or store-target buffers (they run at the same
+ * time). *n_launched (if not NULL) receives the number of real kernel
+ * launches enqueued. KS_ERR_ARG for items == NULL or n_items == 0, else the
+ * errors of ks_simulate (a launch error after earlier grids were enqueued
+ * leaves those enqueued). */
+int ks_simulate_batch(const ks_batch_item* items, uint32_t n_items, void* stream, uint32_t* failed_item,
+                      uint32_t* n_launched);
 
 /* Reduces n_warps stats records (device pointer) on `stream`, waits for the
  * stream, and writes the totals to *out (host). Uses a small device

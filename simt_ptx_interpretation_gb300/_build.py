@@ -25,7 +25,7 @@ def _cuda_home() -> str:
 
 
 def _sources():
-    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cpp", ".h"))] + [
+    return [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cuh", ".cpp", ".h"))] + [
         os.path.join(os.path.dirname(PKG), "include", "ks.h")]
 
 

@@ -66,6 +66,14 @@ class KsHint(ctypes.Structure):
                 ("detail", ctypes.c_char * 96)]
 
 
+class KsBatchItem(ctypes.Structure):
+    _fields_ = [("mod", ctypes.c_void_p), ("kernel", ctypes.c_char_p), ("grid", ctypes.c_uint32),
+                ("block", ctypes.c_uint32), ("params", ctypes.c_void_p), ("param_bytes", ctypes.c_size_t),
+                ("bufs", ctypes.POINTER(KsBuffer)), ("n_bufs", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+                ("trace_buf", ctypes.c_void_p), ("trace_bytes", ctypes.c_size_t), ("stats_buf", ctypes.c_void_p),
+                ("stats_bytes", ctypes.c_size_t), ("cfg", ctypes.POINTER(KsConfig))]
+
+
 EXPORTS = {
     "ks_config_default": (None, [ctypes.POINTER(KsConfig)]),
     "ks_load_module": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p),
@@ -99,6 +107,8 @@ EXPORTS = {
                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(KsBuffer),
                                           ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                           ctypes.c_size_t, ctypes.POINTER(KsConfig), ctypes.c_void_p]),
+    "ks_simulate_batch": (ctypes.c_int, [ctypes.POINTER(KsBatchItem), ctypes.c_uint32, ctypes.c_void_p,
+                                         ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)]),
     "ks_cache_config_default": (None, [ctypes.POINTER(KsCacheConfig)]),
     "ks_cache_workspace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.POINTER(KsCacheConfig)]),
     "ks_simulate_cached": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,

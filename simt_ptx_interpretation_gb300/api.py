@@ -282,6 +282,60 @@ def simulate(module: Module, kernel: str, grid: int, block: int, params: bytes, 
     _check(rc)
 
 
+@dataclass
+class BatchItem:
+    """One launch of simulate_batch: simulate()'s arguments."""
+    module: Module
+    kernel: str
+    grid: int
+    block: int
+    params: bytes
+    buffers: list
+    stats: torch.Tensor
+    trace: torch.Tensor | None = None
+    config: Config | None = None
+
+
+def simulate_batch(items, stream=None) -> int:
+    """Enqueues several simulations as ks_simulate_batch (real grids of items
+    of one kernel form); returns the number of real kernel launches. items:
+    BatchItem list. On a refused item, KsError names it; nothing was
+    launched."""
+    items = list(items)
+    arr = (_native.KsBatchItem * max(1, len(items)))()
+    keep = []  # ctypes objects the C call reads
+    for k, it in enumerate(items):
+        bufs = (_native.KsBuffer * max(1, len(it.buffers)))()
+        for i, (base, t) in enumerate(it.buffers):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("buffers must be contiguous CUDA tensors")
+            bufs[i].sim_base = base
+            bufs[i].dev_ptr = t.data_ptr()
+            bufs[i].bytes = t.numel() * t.element_size()
+        cfg = (it.config or Config()).to_c()
+        name = it.kernel.encode()
+        pbuf = ctypes.create_string_buffer(bytes(it.params), max(1, len(it.params)))
+        keep += [bufs, cfg, name, pbuf]
+        a = arr[k]
+        a.mod = it.module.handle
+        a.kernel = name
+        a.grid, a.block = it.grid, it.block
+        a.params = ctypes.cast(pbuf, ctypes.c_void_p)
+        a.param_bytes = len(it.params)
+        a.bufs = bufs
+        a.n_bufs = len(it.buffers)
+        a.trace_buf = it.trace.data_ptr() if it.trace is not None else None
+        a.trace_bytes = it.trace.numel() if it.trace is not None else 0
+        a.stats_buf = it.stats.data_ptr()
+        a.stats_bytes = it.stats.numel()
+        a.cfg = ctypes.pointer(cfg)
+    failed, launched = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    rc = _native.lib().ks_simulate_batch(arr, len(items), _stream_handle(stream), ctypes.byref(failed),
+                                         ctypes.byref(launched))
+    _check(rc, f"batch item {failed.value}" if failed.value < len(items) else "")
+    return launched.value
+
+
 def simulate_static(module: Module, kernel: str, grid: int, block: int, params: bytes, buffers, stats: torch.Tensor,
                     trace: torch.Tensor | None = None, config: Config | None = None, stream=None) -> None:
     """ks_simulate_static: like simulate(), but the library allocates no device

@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -204,7 +205,8 @@ namespace {
 // ks_simulate and ks_simulate_cached.
 int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t block, const void* params,
             size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf, size_t trace_bytes,
-            void* stats_buf, size_t stats_bytes, const ks_config* cfg_in, ks::KsLaunch* Lp, DevInfo* dip) {
+            void* stats_buf, size_t stats_bytes, const ks_config* cfg_in, ks::KsLaunch* Lp, DevInfo* dip,
+            bool host_checks_only = false) {
   ks_module* mod = const_cast<ks_module*>(mod_c);
   size_t kidx = 0;
   const ks::KsKernel* k = find_kernel(mod, kernel, &kidx);
@@ -240,6 +242,7 @@ int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t 
   if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
   if (cfg.profile_buf && cfg.profile_bytes < k->code.size() * sizeof(ks_pc_profile)) return KS_ERR_ARG;
 
+  if (host_checks_only) return KS_OK;
   DevInfo& di = *dip;
   int dev = 0;
   if (device_info(&di, &dev) != KS_OK) return KS_ERR_CUDA;
@@ -348,6 +351,62 @@ int ks_simulate(const ks_module* mod, const char* kernel, uint32_t grid, uint32_
   if (rc != KS_OK) return rc;
   if (clear_profile(L, stream) != KS_OK) return KS_ERR_CUDA;
   return shape_and_launch(L, di, stream);
+}
+
+int ks_simulate_batch(const ks_batch_item* items, uint32_t n_items, void* stream, uint32_t* failed_item,
+                      uint32_t* n_launched) {
+  if (failed_item) *failed_item = n_items;
+  if (n_launched) *n_launched = 0;
+  if (!items || n_items == 0) return KS_ERR_ARG;
+  std::vector<ks::KsLaunch> Ls(n_items);
+  DevInfo di;
+  // every item's host-side checks first, then the device work of each
+  for (int pass = 0; pass < 2; pass++) {
+    for (uint32_t i = 0; i < n_items; i++) {
+      const ks_batch_item& it = items[i];
+      const int rc = it.reserved ? KS_ERR_ARG
+                                 : prepare(it.mod, it.kernel, it.grid, it.block, it.params, it.param_bytes, it.bufs,
+                                           it.n_bufs, it.trace_buf, it.trace_bytes, it.stats_buf, it.stats_bytes,
+                                           it.cfg, &Ls[i], &di, pass == 0);
+      if (rc != KS_OK) {
+        if (failed_item) *failed_item = i;
+        return rc;
+      }
+    }
+  }
+  for (uint32_t i = 0; i < n_items; i++)
+    if (clear_profile(Ls[i], stream) != KS_OK) return KS_ERR_CUDA;
+  // Real grids: items of one instantiation (mode, form, and in CTA mode the
+  // block), in the order of their first items, at most KS_BATCH_ITEMS and
+  // at most BATCH_WARPS_PER_SM simulated warps per SM of them, so that a
+  // grid runs as one wave and ends with its slowest warp (items are not
+  // weighted by their unknown cost per warp). An item larger than that
+  // fills the GPU alone and is launched as ks_simulate launches it.
+  constexpr uint64_t BATCH_WARPS_PER_SM = 16;
+  const uint64_t budget = BATCH_WARPS_PER_SM * (uint64_t)std::max(di.sms, 1);
+  auto key = [](const ks::KsLaunch& L) {
+    return ((uint64_t)L.cta_mode << 40) | ((uint64_t)ks::interp_form(L) << 32) | (L.cta_mode ? L.wpc : 0u);
+  };
+  std::vector<char> done(n_items, 0);
+  auto G = std::make_unique<ks::KsGrid<ks::KS_BATCH_ITEMS>>();
+  for (uint32_t i = 0; i < n_items; i++) {
+    if (done[i]) continue;
+    G->n = 0;
+    uint64_t warps = 0;
+    for (uint32_t j = i; j < n_items && G->n < ks::KS_BATCH_ITEMS; j++) {
+      if (done[j] || key(Ls[j]) != key(Ls[i])) continue;
+      if (G->n > 0 && (Ls[j].n_warps > budget || warps + Ls[j].n_warps > budget)) continue;
+      G->item[G->n++] = Ls[j];
+      warps += Ls[j].n_warps;
+      done[j] = 1;
+      if (warps > budget) break;  // a large first item goes alone
+    }
+    const int rc = G->n == 1 ? shape_and_launch(G->item[0], di, stream)
+                             : ks::launch_batch(G.get(), di.sms, di.max_smem, stream);
+    if (rc != KS_OK) return rc;
+    if (n_launched) ++*n_launched;
+  }
+  return KS_OK;
 }
 
 int ks_profile_bytes(const ks_module* mod, const char* kernel, size_t* bytes) {

@@ -205,8 +205,8 @@ struct KsBufDev {
   uint8_t* ptr;
 };
 
-// Everything one interpreter launch needs, passed by value as the kernel
-// argument (about 0.6 KB).
+// Everything one interpreter launch needs (720 bytes), passed by value in the
+// kernel argument (KsGrid).
 struct KsLaunch {
   const uint8_t* image;  // device: DevInsn program then constant row values
   uint32_t image_bytes;  // multiple of 16
@@ -249,6 +249,19 @@ struct KsLaunch {
   alignas(16) uint8_t params[KS_MAX_PARAM_BYTES];
 };
 
+// The kernel argument: up to NB launches interpreted by one real grid, real
+// CTAs [cta_begin[i], cta_begin[i + 1]) running item[i] (ks_simulate_batch).
+// Single launches use NB = 1 (one item, every CTA), batches NB =
+// KS_BATCH_ITEMS (about 23 KB, under the 32 KB kernel-argument limit).
+constexpr uint32_t KS_BATCH_ITEMS = 32;
+template <uint32_t NB>
+struct KsGrid {
+  uint32_t n;
+  uint32_t cta_begin[NB + 1];
+  KsLaunch item[NB];
+};
+static_assert(sizeof(KsGrid<KS_BATCH_ITEMS>) <= 32764, "kernel argument too large");
+
 // Shared-memory footprint of one real CTA of `warps` warps (plus the
 // simulated shared memory of a CTA-mode launch).
 size_t interp_smem_bytes(uint32_t image_bytes, uint32_t region_bytes, uint32_t warps, uint32_t shared_bytes);
@@ -266,6 +279,14 @@ const KsKernel* module_kernel(const ks_module* mod, const char* name);
 int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps_per_cta, uint32_t* real_ctas);
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);
 int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
+// Instantiation form of a launch: 0 lean, 1 instrumented (cache model or
+// profile), 2 instrumented with the issue-run log (SM model).
+int interp_form(const KsLaunch& L);
+// One real grid over G->n launches of one instantiation (the same mode and
+// form; in CTA mode the same simulated block): picks the shape, shares the
+// real CTAs out (G->cta_begin) and launches (ks_batch.cu). KS_OK, KS_ERR_ARG
+// (mixed items), KS_ERR_LIMIT (shared memory), KS_ERR_CUDA.
+int launch_batch(KsGrid<KS_BATCH_ITEMS>* G, int sms, int max_smem, void* stream);
 
 // Workspace of the L1/L2 hit model (ks_cache.cu): per-warp counts, the log,
 // and the sort's buffers, each at a 256-byte boundary.

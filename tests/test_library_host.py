@@ -152,3 +152,29 @@ def test_unknown_kernel_and_bad_arguments():
     assert L.ks_simulate(m.handle, b"vector_add", 1, 32, p, 28, bufs, 2, None, 0, stats, 96, None, None) == -3
     for code in (0, -1, -2, -3, -4, -5, -6, 1, 2, 3, 4, 5, 6):
         assert L.ks_status_string(code)
+
+
+def test_batch_arguments_are_checked_before_any_gpu_work():
+    """ks_simulate_batch refuses an empty or NULL list, and names the first
+    item that ks_simulate would refuse (launching nothing)."""
+    m = ks.Module(wl.vector_add_ptx())
+    L = _native.lib()
+    failed = ctypes.c_uint32(7)
+    assert L.ks_simulate_batch(None, 3, None, ctypes.byref(failed), None) == -3
+    items = (_native.KsBatchItem * 3)()
+    assert L.ks_simulate_batch(items, 0, None, ctypes.byref(failed), None) == -3 and failed.value == 0
+    stats = ctypes.create_string_buffer(96 * 16 * 8)
+    p = ctypes.create_string_buffer(28)
+    for it in items:
+        it.mod, it.kernel, it.grid, it.block = m.handle, b"vector_add", 16, 256
+        it.params, it.param_bytes = ctypes.cast(p, ctypes.c_void_p), 28
+        it.stats_buf, it.stats_bytes = ctypes.cast(stats, ctypes.c_void_p), 96 * 16 * 8
+    items[1].stats_bytes = 96  # too small
+    assert L.ks_simulate_batch(items, 3, None, ctypes.byref(failed), None) == -3 and failed.value == 1
+    items[1].stats_bytes = 96 * 16 * 8
+    items[2].kernel = b"nope"
+    assert L.ks_simulate_batch(items, 3, None, ctypes.byref(failed), None) == -5 and failed.value == 2
+    items[2].kernel = b"vector_add"
+    items[0].reserved = 1
+    assert L.ks_simulate_batch(items, 3, None, ctypes.byref(failed), None) == -3 and failed.value == 0
+    assert ctypes.sizeof(_native.KsBatchItem) == 96
