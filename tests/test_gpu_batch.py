@@ -186,3 +186,12 @@ def test_refused_item_launches_nothing():
     torch.cuda.synchronize()
     assert bool((jobs[0].stats == 0xA5).all())
     assert bool((jobs[1].stats == 0xA5).all())
+
+
+@pytest.mark.parametrize("block", [512, 1024])
+def test_cta_mode_large_blocks(block):
+    """CTA-mode items of 16 and 32 warps (the 1024-thread form) in one grid."""
+    jobs = [Job(wl.smem_reduce(n=block * 3, block=block)), Job(wl.smem_reduce(n=block * 2, block=block, seed=9))]
+    assert run_batch(jobs) == 1
+    for j in jobs:
+        j.check_oracle()
