@@ -245,6 +245,7 @@ def run_ours(args, world, rank, local):
     # GPU with a small replay grid, they may be spread over streams forked
     # from and joined to `stream`.
     batch = not (args.cache or args.sched or args.no_batch) and len(jobs) > 1
+    cache_batch = None  # the cached batch's items (--cache, small grids)
     n_streams = args.streams if args.streams > 0 else (min(len(jobs), 8) if args.sched else 1)
     n_streams = max(1, min(n_streams, len(jobs)))
     streams = [stream] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
@@ -264,6 +265,15 @@ def run_ours(args, world, rank, local):
         if nbytes == 0:
             raise SystemExit("invalid cache configuration")
         cache_ws = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
+        # launches that fit one wave together go as one cached batch (their
+        # passes share real grids), each with a workspace of its own
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        if not args.no_batch and len(jobs) > 1 and sum(j["w"].warps for j in jobs) <= 16 * sms:
+            cache_batch = [ks.CachedBatchItem(
+                ks.BatchItem(j["mod"], j["w"].kernel, j["w"].grid, j["w"].block, j["w"].params, j["bufs"], j["st"],
+                             j["tr"], j["cfg"]), cache,
+                torch.empty(ks.cache_workspace_bytes(j["w"].grid, j["w"].block, cache), dtype=torch.uint8,
+                            device=dev)) for j in jobs]
         config = dict(config, cache_model={"l1_lines": cache.l1_lines, "l2_lines": cache.l2_lines,
                                            "lat_l1": cache.lat_l1, "lat_l2": cache.lat_l2,
                                            "max_accesses_per_warp": cache.max_accesses_per_warp})
@@ -327,6 +337,13 @@ def run_ours(args, world, rank, local):
                           j["tr"], j["cfg"]) for j in jobs], stream)
 
     def step(lev=None):
+        if cache_batch:
+            if lev:
+                lev[0][0].record(stream)
+            batch_launches[0] = ks.simulate_cached_batch(cache_batch, stream)
+            if lev:
+                lev[0][1].record(stream)
+            return
         if batch:
             if lev:
                 lev[0][0].record(stream)
@@ -359,7 +376,7 @@ def run_ours(args, world, rank, local):
         step()
     torch.cuda.synchronize(dev)
 
-    n_launch = 1 if batch else len(jobs)  # timed calls per step
+    n_launch = 1 if (batch or cache_batch) else len(jobs)  # timed calls per step
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     lev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_launch)]
            for _ in range(args.steps)]
@@ -402,7 +419,7 @@ def run_ours(args, world, rank, local):
                 "peak_source": f"{sms} SMs x 4 issue/clk x 32 lanes x {mhz:.0f} MHz ({peak_src})",
                 "algorithmic_units_per_launch": [int(x) for x in launch_insts],
                 "launch_ms_mean": [round(sum(x) / len(x), 4) for x in launch_ms],
-                "streams": n_streams, "batched": batch,
+                "streams": n_streams, "batched": bool(batch or cache_batch),
                 "timed_over": "each step's span (its launches may overlap)"}
     if cache:
         roofline["note"] = ("each call runs ks_interp_kernel twice plus the level kernels and radix sorts; "
@@ -413,21 +430,23 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public API with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(args, jobs, insts, dev, streams, launch, fork, join,
-                                           launch_batch if batch else None)
+                                           launch_batch if batch else
+                                           (lambda: ks.simulate_cached_batch(cache_batch, stream)) if cache_batch
+                                           else None)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(sum(step_ms) / len(step_ms), 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)", "data": "synthetic (seeded)",
         "config": dict(config, l2="flushed between steps (256 MiB write)", parallelism=f"replicas{world}",
-                       streams=n_streams, batched=batch),
+                       streams=n_streams, batched=bool(batch or cache_batch)),
         # our kernels per call: the interpreter, or (cache model) two interpreter
         # passes and the four level kernels (the radix sorts and the scan are
         # library code)
         "roofline": roofline, "e2e": e2e,
         # (a batch call reports its real launches)
-        "gpu_launches": args.steps * (batch_launches[0] if batch else n_launch * (6 if cache else 2 if sched
-                                                                                  else 1)),
+        "gpu_launches": args.steps * (batch_launches[0] if (batch or cache_batch)
+                                      else n_launch * (6 if cache else 2 if sched else 1)),
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3), "kernel_sha": kernel_sha(),
     }

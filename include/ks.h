@@ -466,6 +466,26 @@ int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, 
                        const ks_config* cfg, const ks_cache_config* cc, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/* Several cached simulations in one call (no counterpart on the pages), each
+ * giving exactly ks_simulate_cached's outputs: the items' first passes run
+ * as ks_simulate_batch runs its items (shared real grids), then each item's
+ * levels (one stream wait each), then the second passes, again batched.
+ * Each item has its own hit model: cache NULL means ks_cache_config_default,
+ * and its workspace is sized by ks_cache_workspace_bytes. Checks, failed_item
+ * and the no-launch guarantee are those of ks_simulate_batch, plus the
+ * cache arguments' checks of ks_simulate_cached. *n_launched (if not NULL)
+ * receives the kernel launches of this library's own kernels (interpreter
+ * grids and the level kernels; the sorts and the scan are CUB's). Items must
+ * not share buffers or workspaces. */
+typedef struct ks_cached_item {
+  ks_batch_item sim;
+  const ks_cache_config* cache;
+  void* workspace;
+  size_t workspace_bytes;
+} ks_cached_item;
+int ks_simulate_cached_batch(const ks_cached_item* items, uint32_t n_items, void* stream, uint32_t* failed_item,
+                             uint32_t* n_launched);
+
 /* ---- SM-level issue model (KernelScope backend doc, simulator/engine.py and
  * simulator/models.py — WarpStallReason, _determine_stall_reason,
  * WarpScheduleInfo) ------------------------------------------------------------

@@ -9,14 +9,14 @@ latency; host post-passes compute occupancy and export traces. The C ABI
 is include/ks.h (libks.so); this package marshals arguments to it.
 """
 from .api import (CACHE_ACCESS_DTYPE, CACHE_WARP_DTYPE, DEFAULT_LAT, PROFILE_DTYPE, SCHED_SM_DTYPE, SCHED_WARP_DTYPE,
-                  STATS_DTYPE, BatchItem, CacheConfig, Config, KsError, Module, Run, SchedConfig, Totals, cache_results,
+                  STATS_DTYPE, BatchItem, CacheConfig, CachedBatchItem, Config, KsError, Module, Run, SchedConfig, Totals, cache_results,
                   cache_workspace_bytes, gpu_limits, hints, occupancy, profile_array, read_stats, run,
-                  sched_workspace_bytes, simulate, simulate_batch, simulate_cached, simulate_sched, simulate_static, stats_array,
+                  sched_workspace_bytes, simulate, simulate_batch, simulate_cached, simulate_cached_batch, simulate_sched, simulate_static, stats_array,
                   stats_bytes, trace_bytes, trace_to_json)
 
 __all__ = ["CACHE_ACCESS_DTYPE", "CACHE_WARP_DTYPE", "DEFAULT_LAT", "PROFILE_DTYPE", "SCHED_SM_DTYPE",
-           "SCHED_WARP_DTYPE", "STATS_DTYPE", "BatchItem", "CacheConfig", "Config", "KsError", "Module", "Run", "SchedConfig",
+           "SCHED_WARP_DTYPE", "STATS_DTYPE", "BatchItem", "CacheConfig", "CachedBatchItem", "Config", "KsError", "Module", "Run", "SchedConfig",
            "Totals", "cache_results", "cache_workspace_bytes", "gpu_limits", "hints", "occupancy", "profile_array",
            "sched_workspace_bytes", "simulate_sched",
-           "read_stats", "run", "simulate", "simulate_batch", "simulate_cached", "simulate_static", "stats_array", "stats_bytes",
+           "read_stats", "run", "simulate", "simulate_batch", "simulate_cached", "simulate_cached_batch", "simulate_static", "stats_array", "stats_bytes",
            "trace_bytes", "trace_to_json"]

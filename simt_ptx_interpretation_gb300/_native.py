@@ -74,6 +74,11 @@ class KsBatchItem(ctypes.Structure):
                 ("stats_bytes", ctypes.c_size_t), ("cfg", ctypes.POINTER(KsConfig))]
 
 
+class KsCachedItem(ctypes.Structure):
+    _fields_ = [("sim", KsBatchItem), ("cache", ctypes.POINTER(KsCacheConfig)), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
 EXPORTS = {
     "ks_config_default": (None, [ctypes.POINTER(KsConfig)]),
     "ks_load_module": (ctypes.c_int, [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p),
@@ -109,6 +114,8 @@ EXPORTS = {
                                           ctypes.c_size_t, ctypes.POINTER(KsConfig), ctypes.c_void_p]),
     "ks_simulate_batch": (ctypes.c_int, [ctypes.POINTER(KsBatchItem), ctypes.c_uint32, ctypes.c_void_p,
                                          ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)]),
+    "ks_simulate_cached_batch": (ctypes.c_int, [ctypes.POINTER(KsCachedItem), ctypes.c_uint32, ctypes.c_void_p,
+                                                ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)]),
     "ks_cache_config_default": (None, [ctypes.POINTER(KsCacheConfig)]),
     "ks_cache_workspace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.POINTER(KsCacheConfig)]),
     "ks_simulate_cached": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32, ctypes.c_uint32,

@@ -296,6 +296,34 @@ class BatchItem:
     config: Config | None = None
 
 
+def _fill_batch_item(a, it: BatchItem, keep: list) -> None:
+    """Marshals one BatchItem into a ks_batch_item (the ctypes objects it
+    points to go to `keep`)."""
+    bufs = (_native.KsBuffer * max(1, len(it.buffers)))()
+    for i, (base, t) in enumerate(it.buffers):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("buffers must be contiguous CUDA tensors")
+        bufs[i].sim_base = base
+        bufs[i].dev_ptr = t.data_ptr()
+        bufs[i].bytes = t.numel() * t.element_size()
+    cfg = (it.config or Config()).to_c()
+    name = it.kernel.encode()
+    pbuf = ctypes.create_string_buffer(bytes(it.params), max(1, len(it.params)))
+    keep += [bufs, cfg, name, pbuf]
+    a.mod = it.module.handle
+    a.kernel = name
+    a.grid, a.block = it.grid, it.block
+    a.params = ctypes.cast(pbuf, ctypes.c_void_p)
+    a.param_bytes = len(it.params)
+    a.bufs = bufs
+    a.n_bufs = len(it.buffers)
+    a.trace_buf = it.trace.data_ptr() if it.trace is not None else None
+    a.trace_bytes = it.trace.numel() if it.trace is not None else 0
+    a.stats_buf = it.stats.data_ptr()
+    a.stats_bytes = it.stats.numel()
+    a.cfg = ctypes.pointer(cfg)
+
+
 def simulate_batch(items, stream=None) -> int:
     """Enqueues several simulations as ks_simulate_batch (real grids of items
     of one kernel form); returns the number of real kernel launches. items:
@@ -305,30 +333,7 @@ def simulate_batch(items, stream=None) -> int:
     arr = (_native.KsBatchItem * max(1, len(items)))()
     keep = []  # ctypes objects the C call reads
     for k, it in enumerate(items):
-        bufs = (_native.KsBuffer * max(1, len(it.buffers)))()
-        for i, (base, t) in enumerate(it.buffers):
-            if not t.is_cuda or not t.is_contiguous():
-                raise ValueError("buffers must be contiguous CUDA tensors")
-            bufs[i].sim_base = base
-            bufs[i].dev_ptr = t.data_ptr()
-            bufs[i].bytes = t.numel() * t.element_size()
-        cfg = (it.config or Config()).to_c()
-        name = it.kernel.encode()
-        pbuf = ctypes.create_string_buffer(bytes(it.params), max(1, len(it.params)))
-        keep += [bufs, cfg, name, pbuf]
-        a = arr[k]
-        a.mod = it.module.handle
-        a.kernel = name
-        a.grid, a.block = it.grid, it.block
-        a.params = ctypes.cast(pbuf, ctypes.c_void_p)
-        a.param_bytes = len(it.params)
-        a.bufs = bufs
-        a.n_bufs = len(it.buffers)
-        a.trace_buf = it.trace.data_ptr() if it.trace is not None else None
-        a.trace_bytes = it.trace.numel() if it.trace is not None else 0
-        a.stats_buf = it.stats.data_ptr()
-        a.stats_bytes = it.stats.numel()
-        a.cfg = ctypes.pointer(cfg)
+        _fill_batch_item(arr[k], it, keep)
     failed, launched = ctypes.c_uint32(0), ctypes.c_uint32(0)
     rc = _native.lib().ks_simulate_batch(arr, len(items), _stream_handle(stream), ctypes.byref(failed),
                                          ctypes.byref(launched))
@@ -451,6 +456,38 @@ def simulate_cached(module: Module, kernel: str, grid: int, block: int, params: 
         ctypes.byref(cc), workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
     _check(rc)
 
+
+
+@dataclass
+class CachedBatchItem:
+    """One launch of simulate_cached_batch: a BatchItem, its hit model (None:
+    the defaults) and its workspace (uint8 cuda tensor of
+    cache_workspace_bytes)."""
+    item: BatchItem
+    cache: "CacheConfig | None"
+    workspace: torch.Tensor
+
+
+def simulate_cached_batch(items, stream=None) -> int:
+    """ks_simulate_cached_batch: several cached simulations, their passes
+    batched; returns the launches of the library's own kernels. items:
+    CachedBatchItem list. On a refused item, KsError names it; nothing was
+    launched."""
+    items = list(items)
+    arr = (_native.KsCachedItem * max(1, len(items)))()
+    keep = []
+    for k, it in enumerate(items):
+        _fill_batch_item(arr[k].sim, it.item, keep)
+        cc = (it.cache or CacheConfig()).to_c()
+        keep.append(cc)
+        arr[k].cache = ctypes.pointer(cc)
+        arr[k].workspace = it.workspace.data_ptr()
+        arr[k].workspace_bytes = it.workspace.numel()
+    failed, launched = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    rc = _native.lib().ks_simulate_cached_batch(arr, len(items), _stream_handle(stream), ctypes.byref(failed),
+                                                ctypes.byref(launched))
+    _check(rc, f"batch item {failed.value}" if failed.value < len(items) else "")
+    return launched.value
 
 def cache_results(workspace: torch.Tensor, n_warps: int, cache: CacheConfig | None = None):
     """(per-warp counts, access log of shape (W, max_accesses_per_warp)) as numpy

@@ -136,7 +136,7 @@ int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out) {
 }
 
 int launch_cache_levels(const KsLaunch& L, uint8_t* ws, const CacheLayout& C, uint32_t l1_lines, uint32_t l2_lines,
-                        void* stream_v) {
+                        void* stream_v, uint32_t* own_kernels) {
   cudaStream_t stream = (cudaStream_t)stream_v;
   const uint64_t W = L.n_warps;
   const uint32_t warp_bits = bits_for(W - 1u);
@@ -157,6 +157,7 @@ int launch_cache_levels(const KsLaunch& L, uint8_t* ws, const CacheLayout& C, ui
   // per-warp record counts, their exclusive prefix (offsets[W] = the total),
   // and the total on the host: the sorts run over the logged records only
   cache_logged_kernel<<<grid_for(W), 256, 0, stream>>>(L.cache_warps, W, L.cache_cap, logged);
+  if (own_kernels) *own_kernels += 1;
   cudaError_t e = cudaMemsetAsync(logged + W, 0, 4, stream);
   if (e != cudaSuccess) return (int)e;
   e = cub::DeviceScan::ExclusiveSum(temp, temp_bytes, logged, offsets, (int)W + 1, stream);
@@ -167,6 +168,7 @@ int launch_cache_levels(const KsLaunch& L, uint8_t* ws, const CacheLayout& C, ui
   e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return (int)e;
   if (total == 0) return 0;
+  if (own_kernels) *own_kernels += 3;
   const uint64_t n = total;
   const unsigned g = grid_for(n);
 

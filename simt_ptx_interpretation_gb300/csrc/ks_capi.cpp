@@ -337,6 +337,72 @@ uint32_t bits_for(uint64_t max_value) {
   return b;
 }
 
+// The cache model's own argument checks (ks_simulate_cached): the
+// configuration (defaults for NULL), the key width, then (not with
+// host_checks_only: the sorts' scratch size asks the device) the workspace
+// layout and size.
+int cache_checks(const ks_cache_config* cc_in, const void* workspace, size_t workspace_bytes, uint32_t grid,
+                 uint32_t block, ks_cache_config* cc, ks::CacheLayout* C, bool host_checks_only = false) {
+  if (cc_in) *cc = *cc_in; else ks_cache_config_default(cc);
+  if (!cache_config_ok(*cc) || !workspace) return KS_ERR_ARG;
+  if (grid == 0 || block == 0 || block > 1024) return KS_ERR_ARG;
+  const uint64_t W = warps_of(grid, block);
+  if (bits_for(cc->l1_lines - 1u) + 32u + bits_for(W - 1u) > 64u) return KS_ERR_LIMIT;
+  if (host_checks_only) return KS_OK;
+  const int lc = ks::cache_layout(W, cc->max_accesses_per_warp, C);
+  if (lc != KS_OK) return lc;
+  if (workspace_bytes < C->total) return KS_ERR_ARG;
+  return KS_OK;
+}
+
+// Points a prepared launch at its cache-model workspace (first pass: the
+// accesses logged, stores suppressed, no profile).
+void cache_first_pass(ks::KsLaunch* L, const ks_cache_config& cc, uint8_t* ws, const ks::CacheLayout& C) {
+  L->cache_cap = cc.max_accesses_per_warp;
+  L->lat_l1 = cc.lat_l1;
+  L->lat_l2 = cc.lat_l2;
+  L->cache_warps = reinterpret_cast<ks_cache_warp*>(ws + C.warps_off);
+  L->cache_log = reinterpret_cast<ks_cache_access*>(ws + C.log_off);
+  L->profile = nullptr;
+  L->cache_pass = 1;
+}
+
+// Launches prepared simulations as real grids of one instantiation each (mode,
+// form, and in CTA mode the block), in the order of their first items, at
+// most KS_BATCH_ITEMS and at most BATCH_WARPS_PER_SM simulated warps per SM
+// of them, so that a grid runs as one wave and ends with its slowest warp
+// (items are not weighted by their unknown cost per warp). An item larger
+// than that fills the GPU alone and is launched as ks_simulate launches it.
+// Adds the real launches to *n_launched (if not null).
+int launch_items(const std::vector<ks::KsLaunch>& Ls, const DevInfo& di, void* stream, uint32_t* n_launched) {
+  constexpr uint64_t BATCH_WARPS_PER_SM = 16;
+  const uint64_t budget = BATCH_WARPS_PER_SM * (uint64_t)std::max(di.sms, 1);
+  auto key = [](const ks::KsLaunch& L) {
+    return ((uint64_t)L.cta_mode << 40) | ((uint64_t)ks::interp_form(L) << 32) | (L.cta_mode ? L.wpc : 0u);
+  };
+  const size_t n_items = Ls.size();
+  std::vector<char> done(n_items, 0);
+  auto G = std::make_unique<ks::KsGrid<ks::KS_BATCH_ITEMS>>();
+  for (size_t i = 0; i < n_items; i++) {
+    if (done[i]) continue;
+    G->n = 0;
+    uint64_t warps = 0;
+    for (size_t j = i; j < n_items && G->n < ks::KS_BATCH_ITEMS; j++) {
+      if (done[j] || key(Ls[j]) != key(Ls[i])) continue;
+      if (G->n > 0 && (Ls[j].n_warps > budget || warps + Ls[j].n_warps > budget)) continue;
+      G->item[G->n++] = Ls[j];
+      warps += Ls[j].n_warps;
+      done[j] = 1;
+      if (warps > budget) break;  // a large first item goes alone
+    }
+    const int rc = G->n == 1 ? shape_and_launch(G->item[0], di, stream)
+                             : ks::launch_batch(G.get(), di.sms, di.max_smem, stream);
+    if (rc != KS_OK) return rc;
+    if (n_launched) ++*n_launched;
+  }
+  return KS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -376,37 +442,7 @@ int ks_simulate_batch(const ks_batch_item* items, uint32_t n_items, void* stream
   }
   for (uint32_t i = 0; i < n_items; i++)
     if (clear_profile(Ls[i], stream) != KS_OK) return KS_ERR_CUDA;
-  // Real grids: items of one instantiation (mode, form, and in CTA mode the
-  // block), in the order of their first items, at most KS_BATCH_ITEMS and
-  // at most BATCH_WARPS_PER_SM simulated warps per SM of them, so that a
-  // grid runs as one wave and ends with its slowest warp (items are not
-  // weighted by their unknown cost per warp). An item larger than that
-  // fills the GPU alone and is launched as ks_simulate launches it.
-  constexpr uint64_t BATCH_WARPS_PER_SM = 16;
-  const uint64_t budget = BATCH_WARPS_PER_SM * (uint64_t)std::max(di.sms, 1);
-  auto key = [](const ks::KsLaunch& L) {
-    return ((uint64_t)L.cta_mode << 40) | ((uint64_t)ks::interp_form(L) << 32) | (L.cta_mode ? L.wpc : 0u);
-  };
-  std::vector<char> done(n_items, 0);
-  auto G = std::make_unique<ks::KsGrid<ks::KS_BATCH_ITEMS>>();
-  for (uint32_t i = 0; i < n_items; i++) {
-    if (done[i]) continue;
-    G->n = 0;
-    uint64_t warps = 0;
-    for (uint32_t j = i; j < n_items && G->n < ks::KS_BATCH_ITEMS; j++) {
-      if (done[j] || key(Ls[j]) != key(Ls[i])) continue;
-      if (G->n > 0 && (Ls[j].n_warps > budget || warps + Ls[j].n_warps > budget)) continue;
-      G->item[G->n++] = Ls[j];
-      warps += Ls[j].n_warps;
-      done[j] = 1;
-      if (warps > budget) break;  // a large first item goes alone
-    }
-    const int rc = G->n == 1 ? shape_and_launch(G->item[0], di, stream)
-                             : ks::launch_batch(G.get(), di.sms, di.max_smem, stream);
-    if (rc != KS_OK) return rc;
-    if (n_launched) ++*n_launched;
-  }
-  return KS_OK;
+  return launch_items(Ls, di, stream, n_launched);
 }
 
 int ks_profile_bytes(const ks_module* mod, const char* kernel, size_t* bytes) {
@@ -498,29 +534,17 @@ int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, 
                        size_t trace_bytes, void* stats_buf, size_t stats_bytes, const ks_config* cfg,
                        const ks_cache_config* cc_in, void* workspace, size_t workspace_bytes, void* stream) {
   ks_cache_config cc;
-  if (cc_in) cc = *cc_in; else ks_cache_config_default(&cc);
-  if (!cache_config_ok(cc) || !workspace) return KS_ERR_ARG;
-  if (grid == 0 || block == 0 || block > 1024) return KS_ERR_ARG;
-  const uint64_t W = warps_of(grid, block);
-  if (bits_for(cc.l1_lines - 1u) + 32u + bits_for(W - 1u) > 64u) return KS_ERR_LIMIT;
   ks::CacheLayout C;
-  const int lc = ks::cache_layout(W, cc.max_accesses_per_warp, &C);
+  const int lc = cache_checks(cc_in, workspace, workspace_bytes, grid, block, &cc, &C);
   if (lc != KS_OK) return lc;
-  if (workspace_bytes < C.total) return KS_ERR_ARG;
   ks::KsLaunch L;
   DevInfo di;
   int rc = prepare(mod, kernel, grid, block, params, param_bytes, bufs, n_bufs, trace_buf, trace_bytes, stats_buf,
                    stats_bytes, cfg, &L, &di);
   if (rc != KS_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  L.cache_cap = cc.max_accesses_per_warp;
-  L.lat_l1 = cc.lat_l1;
-  L.lat_l2 = cc.lat_l2;
-  L.cache_warps = reinterpret_cast<ks_cache_warp*>(ws + C.warps_off);
-  L.cache_log = reinterpret_cast<ks_cache_access*>(ws + C.log_off);
   ks_pc_profile* profile = L.profile;
-  L.profile = nullptr;  // the first pass counts nothing
-  L.cache_pass = 1;     // log the accesses, stores suppressed
+  cache_first_pass(&L, cc, ws, C);
   rc = shape_and_launch(L, di, stream);
   if (rc != KS_OK) return rc;
   if (ks::launch_cache_levels(L, ws, C, cc.l1_lines, cc.l2_lines, stream) != 0) return KS_ERR_CUDA;
@@ -528,6 +552,51 @@ int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, 
   L.profile = profile;
   if (clear_profile(L, stream) != KS_OK) return KS_ERR_CUDA;
   return shape_and_launch(L, di, stream);
+}
+
+int ks_simulate_cached_batch(const ks_cached_item* items, uint32_t n_items, void* stream, uint32_t* failed_item,
+                             uint32_t* n_launched) {
+  if (failed_item) *failed_item = n_items;
+  if (n_launched) *n_launched = 0;
+  if (!items || n_items == 0) return KS_ERR_ARG;
+  std::vector<ks::KsLaunch> Ls(n_items);
+  std::vector<ks_cache_config> ccs(n_items);
+  std::vector<ks::CacheLayout> Cs(n_items);
+  std::vector<ks_pc_profile*> profiles(n_items);
+  DevInfo di;
+  // every item's host-side checks first, then the device work of each
+  for (int pass = 0; pass < 2; pass++) {
+    for (uint32_t i = 0; i < n_items; i++) {
+      const ks_batch_item& it = items[i].sim;
+      int rc = it.reserved ? KS_ERR_ARG
+                           : cache_checks(items[i].cache, items[i].workspace, items[i].workspace_bytes, it.grid,
+                                          it.block, &ccs[i], &Cs[i], pass == 0);
+      if (rc == KS_OK)
+        rc = prepare(it.mod, it.kernel, it.grid, it.block, it.params, it.param_bytes, it.bufs, it.n_bufs,
+                     it.trace_buf, it.trace_bytes, it.stats_buf, it.stats_bytes, it.cfg, &Ls[i], &di, pass == 0);
+      if (rc != KS_OK) {
+        if (failed_item) *failed_item = i;
+        return rc;
+      }
+    }
+  }
+  // first pass of every item, then every item's levels, then the second
+  for (uint32_t i = 0; i < n_items; i++) {
+    profiles[i] = Ls[i].profile;
+    cache_first_pass(&Ls[i], ccs[i], static_cast<uint8_t*>(items[i].workspace), Cs[i]);
+  }
+  int rc = launch_items(Ls, di, stream, n_launched);
+  if (rc != KS_OK) return rc;
+  for (uint32_t i = 0; i < n_items; i++)
+    if (ks::launch_cache_levels(Ls[i], static_cast<uint8_t*>(items[i].workspace), Cs[i], ccs[i].l1_lines,
+                                ccs[i].l2_lines, stream, n_launched) != 0)
+      return KS_ERR_CUDA;
+  for (uint32_t i = 0; i < n_items; i++) {
+    Ls[i].cache_pass = 2;
+    Ls[i].profile = profiles[i];
+    if (clear_profile(Ls[i], stream) != KS_OK) return KS_ERR_CUDA;
+  }
+  return launch_items(Ls, di, stream, n_launched);
 }
 
 int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_totals* out) {

@@ -299,9 +299,10 @@ int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out);
 // The hit computation between the two passes: the logged records packed,
 // sorted by (L1 set, step, warp), L1 hits, a stable sort of the misses by
 // their L2 set, L2 hits. Waits for the stream once (the sorts' length is the
-// number of logged records). Returns a cudaError_t value.
+// number of logged records). Returns a cudaError_t value; adds the kernels of
+// its own that it launched to *own_kernels (if not null).
 int launch_cache_levels(const KsLaunch& L, uint8_t* workspace, const CacheLayout& C, uint32_t l1_lines,
-                        uint32_t l2_lines, void* stream);
+                        uint32_t l2_lines, void* stream, uint32_t* own_kernels = nullptr);
 
 // SM issue model replay (ks_sched.cu): shared memory of one simulated SM's
 // replay, and the launch (one 32-thread block per simulated SM). Returns a

@@ -215,3 +215,77 @@ def test_fuzz_full_size_properties(i):
 def test_large_blocks(block):
     # CTA mode with 16 and 32 warps (the 1024-thread instantiation)
     wl_check(wl.smem_reduce(n=block * 4, block=block))
+
+
+def _cached_job(w: wl.Workload, cache: ks.CacheConfig):
+    mod = ks.Module(w.ptx)
+    dev = [(b.sim_base, torch.from_numpy(b.data.view(np.uint8)).cuda()) for b in w.fresh_buffers()]
+    st = torch.empty(ks.stats_bytes(w.grid, w.block), dtype=torch.uint8, device="cuda")
+    tr = torch.empty(ks.trace_bytes(w.grid, w.block, w.max_ts, mod.record_bytes(w.kernel)), dtype=torch.uint8,
+                     device="cuda")
+    ws = torch.zeros(ks.cache_workspace_bytes(w.grid, w.block, cache), dtype=torch.uint8, device="cuda")
+    item = ks.BatchItem(mod, w.kernel, w.grid, w.block, w.params, dev, st, tr, ks.Config(max_ts=w.max_ts))
+    return ks.CachedBatchItem(item, cache, ws)
+
+
+def test_cached_batch_matches_the_oracle():
+    """ks_simulate_cached_batch: items of two modes with their own hit models
+    (two small, one default), first and second passes batched; each equals
+    the oracle's literal stepper byte for byte."""
+    small = ks.CacheConfig(l1_lines=4, l2_lines=12, max_accesses_per_warp=4096)
+    ws = [(wl.vector_add(), ks.CacheConfig(max_accesses_per_warp=8)),
+          (wl.gather(4, n_out=1 << 12), ks.CacheConfig(max_accesses_per_warp=8)),
+          (wl.divergent(4, n=1 << 11), ks.CacheConfig(max_accesses_per_warp=64)),
+          (wl.fuzz(0, grid=4, block=64), small), (wl.fuzz(5, grid=4, block=64), ks.CacheConfig(max_accesses_per_warp=4096)),
+          (wl.smem_reduce(n=256 * 4, block=256), ks.CacheConfig(max_accesses_per_warp=64)),
+          (wl.fuzz_shared(3, grid=4, block=128), small)]
+    jobs = [_cached_job(w, c) for w, c in ws]
+    n = ks.simulate_cached_batch(jobs)
+    torch.cuda.synchronize()
+    assert n >= 4  # two passes of two groups, plus the level kernels
+    for (w, c), j in zip(ws, jobs):
+        o = oracle.run_cached(w.ptx, w.kernel, w.grid, w.block, w.params,
+                              [(b.sim_base, b.data) for b in w.fresh_buffers()], max_ts=w.max_ts, trace=True,
+                              l1_lines=c.l1_lines, l2_lines=c.l2_lines, lat_l1=c.lat_l1, lat_l2=c.lat_l2,
+                              log_cap=c.max_accesses_per_warp)
+        assert o.status == 0
+        assert np.array_equal(j.item.stats.cpu().numpy(), o.stats.view(np.uint8)), w.name
+        assert np.array_equal(j.item.trace.cpu().numpy(), o.trace), w.name
+        cw, log = ks.cache_results(j.workspace, w.warps, c)
+        assert np.array_equal(cw, o.warps), w.name
+        for k in range(w.warps):
+            m = int(o.warps[k]["n_access"])
+            assert np.array_equal(log[k][:m], o.log[k][:m]), (w.name, k)
+        obufs = w.fresh_buffers()
+        oracle.run_cached(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in obufs],
+                          l1_lines=c.l1_lines, l2_lines=c.l2_lines, lat_l1=c.lat_l1, lat_l2=c.lat_l2,
+                          log_cap=c.max_accesses_per_warp)
+        for (_, t), b in zip(j.item.buffers, obufs):
+            assert np.array_equal(t.cpu().numpy(), b.data.view(np.uint8)), w.name
+
+
+def test_cached_batch_pair_equals_single_calls():
+    """The FFMA pair (grid 132 x block 128, 64 iterations) through one cached
+    batch and through two ks_simulate_cached calls."""
+    cache = ks.CacheConfig(max_accesses_per_warp=4)
+    ws = [wl.ffma(acc=1, iters=64), wl.ffma(acc=8, iters=64)]
+    jobs = [_cached_job(w, cache) for w in ws]
+    ks.simulate_cached_batch(jobs)
+    for w, j in zip(ws, jobs):
+        r = ks.run(ks.Module(w.ptx), w.kernel, w.grid, w.block, w.params,
+                   [(b.sim_base, torch.from_numpy(b.data.view(np.uint8)).cuda()) for b in w.fresh_buffers()],
+                   config=ks.Config(max_ts=w.max_ts), trace=True, cache=cache)
+        torch.cuda.synchronize()
+        assert r.totals.status == 0
+        assert torch.equal(j.item.stats, r.stats) and torch.equal(j.item.trace, r.trace)
+        cw, _ = ks.cache_results(j.workspace, w.warps, cache)
+        assert np.array_equal(cw, r.cache_warps)
+
+
+def test_cached_batch_workspace_too_small():
+    w = wl.vector_add()
+    jobs = [_cached_job(w, ks.CacheConfig(max_accesses_per_warp=8)) for _ in range(2)]
+    jobs[1].workspace = jobs[1].workspace[:-256]
+    with pytest.raises(ks.KsError) as e:
+        ks.simulate_cached_batch(jobs)
+    assert "batch item 1" in str(e.value)

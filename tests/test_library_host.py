@@ -178,3 +178,31 @@ def test_batch_arguments_are_checked_before_any_gpu_work():
     items[0].reserved = 1
     assert L.ks_simulate_batch(items, 3, None, ctypes.byref(failed), None) == -3 and failed.value == 0
     assert ctypes.sizeof(_native.KsBatchItem) == 96
+
+
+def test_cached_batch_arguments_are_checked_before_any_gpu_work():
+    """ks_simulate_cached_batch checks every item (its simulation and its
+    cache arguments) before any GPU work and names the first refused one."""
+    m = ks.Module(wl.vector_add_ptx())
+    L = _native.lib()
+    failed = ctypes.c_uint32(7)
+    assert L.ks_simulate_cached_batch(None, 2, None, ctypes.byref(failed), None) == -3
+    items = (_native.KsCachedItem * 2)()
+    stats = ctypes.create_string_buffer(96 * 16 * 8)
+    p = ctypes.create_string_buffer(28)
+    need = 1 << 20
+    ws = ctypes.create_string_buffer(need)
+    for it in items:
+        s = it.sim
+        s.mod, s.kernel, s.grid, s.block = m.handle, b"vector_add", 16, 256
+        s.params, s.param_bytes = ctypes.cast(p, ctypes.c_void_p), 28
+        s.stats_buf, s.stats_bytes = ctypes.cast(stats, ctypes.c_void_p), 96 * 16 * 8
+        it.workspace, it.workspace_bytes = ctypes.cast(ws, ctypes.c_void_p), need
+    items[1].workspace = None  # (a workspace's size is checked against a layout that needs the GPU)
+    assert L.ks_simulate_cached_batch(items, 2, None, ctypes.byref(failed), None) == -3 and failed.value == 1
+    bad = _native.KsCacheConfig()
+    L.ks_cache_config_default(ctypes.byref(bad))
+    bad.l2_lines = bad.l1_lines + 1  # not a multiple of the L1
+    items[0].cache = ctypes.pointer(bad)
+    assert L.ks_simulate_cached_batch(items, 2, None, ctypes.byref(failed), None) == -3 and failed.value == 0
+    assert ctypes.sizeof(_native.KsCachedItem) == 120
