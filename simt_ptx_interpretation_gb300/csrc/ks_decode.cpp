@@ -1205,6 +1205,47 @@ class Decoder {
       }
       route[i] = r;
     }
+    // Immediate multipliers. A constant row costs a warp 256 bytes of shared
+    // memory, and kernels whose address arithmetic multiplies by many
+    // distinct immediates fill their regions with them: when the rows would
+    // pass MANY_CONST_ROWS, every unguarded mul.lo / mad.lo of a register by
+    // an immediate leaves the fast path for the mid loop as DOP_MADI
+    // (d = a * aux + c row) or DOP_MADII (d = a * aux + hc, an immediate
+    // addend in the record's hc field, which ops without predicate operands
+    // do not use), and its immediates leave the rows.
+    constexpr size_t MANY_CONST_ROWS = 16;
+    std::vector<uint8_t> madi(n, 0);
+    std::vector<uint32_t> madi_c(n, 0);
+    {
+      std::vector<char> used(K.cpool.size(), 0);
+      size_t rows = 0;
+      for (size_t i = 0; i < n; i++) {
+        const uint8_t ops[4] = {route[i].a, route[i].b, route[i].c, K.code[i].d};
+        for (int p = 0; p < 4; p++)
+          if (routed_width(K.code[i], p) && ops[p] != OPND_ZERO && is_const(ops[p]) && !used[ops[p] & 0x7F]) {
+            used[ops[p] & 0x7F] = 1;
+            rows++;
+          }
+      }
+      if (rows > MANY_CONST_ROWS) {
+        for (size_t i = 0; i < n; i++) {
+          const KsInsn& in = K.code[i];
+          if (in.guard != KS_NO_GUARD || (in.op != OP_MUL32 && in.op != OP_MAD32)) continue;
+          uint8_t x = in.a, y = in.b;
+          if (is_const(x) && !is_const(y)) std::swap(x, y);  // the product commutes
+          if (is_const(x) || !is_const(y)) continue;
+          Route r{x, OPND_ZERO, OPND_ZERO, cval(y)};
+          if (in.op == OP_MAD32 && is_const(in.c)) {
+            madi[i] = 2;
+            madi_c[i] = cval(in.c);
+          } else {
+            madi[i] = 1;
+            if (in.op == OP_MAD32) r.c = in.c;
+          }
+          route[i] = r;
+        }
+      }
+    }
     // constant rows: one per constant still read from a row, two if any such
     // use is 64-bit
     std::vector<unsigned> cwidth(K.cpool.size(), 0);
@@ -1255,7 +1296,8 @@ class Decoder {
         continue;
       }
       const KsInsn& in = K.code[i];
-      o.op = fpu_family(in.op) ? DOP_FPU : imad_family(in.op) ? DOP_IMAD : in.op;
+      o.op = madi[i] ? (madi[i] == 1 ? DOP_MADI : DOP_MADII)
+             : fpu_family(in.op) ? DOP_FPU : imad_family(in.op) ? DOP_IMAD : in.op;
       if ((o.op == DOP_FPU || o.op == DOP_IMAD) && in.guard != KS_NO_GUARD) o.op |= DOP_GUARDED;
       o.inc = in.op == OP_EVENT ? 0u : INC_ISSUE;
       if (in.guard != KS_NO_GUARD) {
@@ -1266,7 +1308,8 @@ class Decoder {
       uint32_t* rows[4] = {&o.a, &o.b, &o.c, &o.d};
       for (int p = 0; p < 4; p++)
         if (routed_width(in, p)) *rows[p] = row_of(ops[p]);
-      if ((o.op & ~DOP_GUARDED) == DOP_FPU || (o.op & ~DOP_GUARDED) == DOP_IMAD || imm_b_op(in.op)) o.aux = route[i].aux;
+      if ((o.op & ~DOP_GUARDED) == DOP_FPU || (o.op & ~DOP_GUARDED) == DOP_IMAD || imm_b_op(in.op) || madi[i])
+        o.aux = route[i].aux;
       if (in.op != OP_EVENT) {
         o.ha = phz(in.ha);
         o.hb = phz(in.hb);
@@ -1280,6 +1323,10 @@ class Decoder {
                                   (in.hb >= KS_HZ_PRED0 && in.hb != KS_HZ_NONE) ||
                                   (in.hc >= KS_HZ_PRED0 && in.hc != KS_HZ_NONE) || (o.inc & INC_PDEST);
         if (pred_operand) o.inc |= INC_PHAZ;
+        if (madi[i]) {
+          o.inc |= INC_MID;  // unguarded, no predicate operand
+          if (madi[i] == 2) o.hc = madi_c[i];
+        }
         switch (in.op) {
           case OP_LDP32: case OP_LDP64: case OP_MOV64: case OP_MOVSP:
           case OP_ADD64: case OP_SUB64: case OP_MUL64: case OP_MAD64:

@@ -156,6 +156,11 @@ constexpr uint32_t OP_EXIT = 0xFE;  // sentinel at index n_insn: the remaining l
 constexpr uint32_t DOP_FPU = 0x40;
 constexpr uint32_t DOP_IMAD = 0x41;
 constexpr uint32_t DOP_GUARDED = 0x02;
+// Unguarded mul.lo / mad.lo of a register by an immediate, in kernels with
+// many constants (the immediates stay out of the constant rows; mid loop):
+//   DOP_MADI:  d = a * aux + c             DOP_MADII: d = a * aux + hc
+constexpr uint32_t DOP_MADI = 0x44;
+constexpr uint32_t DOP_MADII = 0x45;
 
 struct DevLayout {
   uint32_t n_slots, n_crows;

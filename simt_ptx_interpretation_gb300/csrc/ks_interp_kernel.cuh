@@ -510,6 +510,8 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
 #define MB64() ((uint64_t)b0 | ((uint64_t)SM32(lb + B + ROW_BYTES) << 32))
 #define R64(v) do { const uint64_t v_ = (v); lo = (uint32_t)v_; hi = (uint32_t)(v_ >> 32); wide = true; } while (0)
           switch (__shfl_sync(FULL, ka.x, 0)) {
+            case DOP_MADI: lo = a0 * aux + pcc.x; break;
+            case DOP_MADII: lo = a0 * aux + mp[3].x; break;
             case OP_LDP32: lo = *reinterpret_cast<const uint32_t*>(s_params + aux); break;
             case OP_LDP64: R64(*reinterpret_cast<const uint64_t*>(s_params + aux)); break;
             case OP_MOV64: R64(MA64()); break;
@@ -897,6 +899,8 @@ __global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __
           W32(a0 * b0 + (c0 ^ aux));
           pc++;
           break;
+        case DOP_MADI: W32(a0 * aux + c0); pc++; break;
+        case DOP_MADII: W32(a0 * aux + q3.x); pc++; break;
         // ---- control (a6) ----
 
         case OP_RET: {

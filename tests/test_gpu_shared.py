@@ -235,9 +235,9 @@ def test_lean_kernel_at_large_blocks(block):
 
 
 def test_cta_mode_reports_state_that_does_not_fit():
-    # 16 warps of a random shared program's interpreter state (about 14 KB a
+    # 32 warps of a random shared program's interpreter state (about 11 KB a
     # warp) plus its shared arrays exceed an SM's shared memory
-    w = wl.fuzz_shared(0, grid=2, block=512)
+    w = wl.fuzz_shared(0, grid=2, block=1024)
     m = ks.Module(w.ptx)
     with pytest.raises(ks.KsError) as e:
         ks.run(m, w.kernel, w.grid, w.block, w.params,
