@@ -424,3 +424,37 @@ def test_jit_crosscheck_single_instructions(op, srcs, dst, kind):
         assert np.array_equal(s64[~isnan], n64[~isnan])
         return
     assert np.array_equal(sim, nat)
+
+
+def many_multipliers(grid: int = 4, block: int = 96) -> wl.Workload:
+    """A kernel with more than 16 distinct immediates, most of them
+    multipliers (so the decoder keeps them out of the constant rows): mul.lo
+    and mad.lo by an immediate in either operand position, immediate and
+    register addends, signed and unsigned, one guarded (its immediate stays a
+    row), each result folded into the value stored at out[gtid]."""
+    lines = ["mov.u32 %r0, %tid.x;", "mov.u32 %r1, %ctaid.x;", "mov.u32 %r2, %ntid.x;",
+             "mad.lo.s32 %r3, %r1, %r2, %r0;", "mov.u32 %r4, %r3;"]
+    rng = np.random.default_rng(11)
+    for k in range(24):
+        m, c = int(rng.integers(1, 1 << 31)), int(rng.integers(0, 1 << 32))
+        form = k % 4
+        if form == 0:
+            lines.append(f"mul.lo.u32 %r5, %r4, {m};")
+        elif form == 1:
+            lines.append(f"mad.lo.u32 %r5, {m}, %r4, {c};")
+        elif form == 2:
+            lines.append(f"mad.lo.s32 %r5, %r4, {m - (1 << 30)}, %r3;")
+        else:
+            lines.append(f"mul.lo.s32 %r5, {m}, %r4;")
+        lines.append("xor.b32 %r4, %r4, %r5;")
+    lines += ["and.b32 %r6, %r0, 1;", "setp.eq.u32 %p1, %r6, 0;", "@%p1 mad.lo.u32 %r4, %r4, 77777, 5;",
+              "ld.param.u64 %rd0, [out];", "cvt.u64.u32 %rd1, %r3;", "shl.b64 %rd1, %rd1, 2;",
+              "add.u64 %rd0, %rd0, %rd1;", "st.global.u32 [%rd0], %r4;"]
+    ptx = (wl.HEADER + ".visible .entry mm(.param .u64 out)\n{\n    .reg .pred %p<2>;\n    .reg .b32 %r<7>;\n"
+           "    .reg .b64 %rd<2>;\n" + "\n".join("    " + x for x in lines) + "\n    ret;\n}\n")
+    bufs = wl.place([("out", np.zeros(grid * block, dtype=np.uint32), True)])
+    return wl.Workload("many_multipliers", ptx, "mm", grid, block, wl.pack_params([("u64", bufs[0].sim_base)]), bufs)
+
+
+def test_immediate_multipliers_out_of_rows():
+    _parity.assert_parity(many_multipliers())
