@@ -279,7 +279,7 @@ const KsKernel* module_kernel(const ks_module* mod, const char* name);
 // Launchers (ks_interp.cu). Return a cudaError_t value.
 // Real launch shape: real warps per CTA and real CTAs (persistent). A
 // CTA-mode launch (L.cta_mode) takes one real warp per simulated warp of a
-// CTA; otherwise 1..8 real warps per CTA over all simulated warps. KS_OK,
+// CTA; otherwise 1..12 real warps per CTA over all simulated warps. KS_OK,
 // KS_ERR_LIMIT (no shape fits the shared memory) or KS_ERR_CUDA.
 int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps_per_cta, uint32_t* real_ctas);
 int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);

@@ -121,15 +121,17 @@ int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps
     *real_ctas = (uint32_t)std::min<uint64_t>(L.grid, (uint64_t)sms * (uint64_t)per_sm);
     return KS_OK;
   }
-  // Candidates: 1..8 real warps per CTA. While the simulated grid is small,
-  // keep at least two CTAs per SM so that every SM gets work; among the rest
+  // Candidates: 1..12 real warps per CTA (one CTA of many warps holds one
+  // program copy where large warp regions leave room for few CTAs). While
+  // the simulated grid is small, keep at least two CTAs per SM so that every
+  // SM gets work; among the rest
   // take the shape with the most resident real warps (shared memory,
   // registers and the CTA limit all count), then the larger CTA (fewer
   // program copies).
   uint32_t best_w = 0, best_ctas = 0;
   uint64_t best_res = 0;
   bool any_fit = false;
-  for (uint32_t w = 1; w <= 8; w++) {
+  for (uint32_t w = 1; w <= 12; w++) {
     const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, w, 0);
     if (smem > (size_t)max_smem) break;
     any_fit = true;

@@ -204,12 +204,14 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 // per simulated CTA, barrier rounds, shared-memory handlers); compiled apart
 // so that the other kernels keep the register budget of the plain loop. BIG:
 // CTA mode for blocks of 9..32 warps (a 1024-thread real CTA, at most 64
-// registers a thread, so it spills: slower, used only for such blocks).
+// registers a thread, so it spills: slower, used only for such blocks). The
+// plain forms take CTAs of up to 12 warps.
 // NB: launches per real grid (1, or KS_BATCH_ITEMS for ks_simulate_batch);
 // each real CTA runs the item whose CTA range holds it, as if that item's
 // CTAs were a grid of their own.
 template <bool CTA, bool BIG, bool INSTR, bool RUNLOG, uint32_t NB>
-__global__ void __launch_bounds__(BIG ? 1024 : 256, 1) ks_interp_kernel(const __grid_constant__ KsGrid<NB> G) {
+__global__ void __launch_bounds__(BIG ? 1024 : (CTA ? 256 : 384), 1)
+    ks_interp_kernel(const __grid_constant__ KsGrid<NB> G) {
   uint32_t item = 0;
   if constexpr (NB > 1) {
     while (item + 1u < G.n && blockIdx.x >= G.cta_begin[item + 1u]) item++;  // uniform in the CTA
