@@ -318,10 +318,10 @@ int clear_profile(const ks::KsLaunch& L, void* stream) {
 
 // Real launch shape (persistent real warps, see ks::choose_launch) and launch.
 int shape_and_launch(const ks::KsLaunch& L, const DevInfo& di, void* stream) {
-  uint32_t wpc_real = 0, ctas = 0;
-  const int shape = ks::choose_launch(L, di.sms, di.max_smem, &wpc_real, &ctas);
-  if (shape != KS_OK) return shape;
-  if (ks::launch_interp(L, wpc_real, ctas, stream) != 0) return KS_ERR_CUDA;
+  ks::LaunchShape shape;
+  const int rc = ks::choose_launch(L, di.sms, di.max_smem, &shape);
+  if (rc != KS_OK) return rc;
+  if (ks::launch_interp(L, shape, stream) != 0) return KS_ERR_CUDA;
   return KS_OK;
 }
 

@@ -281,9 +281,17 @@ const KsKernel* module_kernel(const ks_module* mod, const char* name);
 // CTA-mode launch (L.cta_mode) takes one real warp per simulated warp of a
 // CTA; otherwise 1..12 real warps per CTA over all simulated warps. KS_OK,
 // KS_ERR_LIMIT (no shape fits the shared memory) or KS_ERR_CUDA.
-int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps_per_cta, uint32_t* real_ctas);
-int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream);
-int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm);
+// The real launch of one simulation: CTAs of warps_per_cta real warps, and
+// (plain mode) whether the register-capped form runs it.
+struct LaunchShape {
+  uint32_t warps_per_cta;
+  uint32_t ctas;
+  bool reg_capped;
+};
+int choose_launch(const KsLaunch& L, int sms, int max_smem, LaunchShape* shape);
+int launch_interp(const KsLaunch& L, const LaunchShape& shape, void* stream);
+int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm,
+                     bool reg_capped = false);
 // Instantiation form of a launch: 0 lean, 1 instrumented (cache model or
 // profile), 2 instrumented with the issue-run log (SM model).
 int interp_form(const KsLaunch& L);

@@ -1,6 +1,10 @@
 // ks_interp.cu — launchers of the interpreter kernel (ks_interp_kernel.cuh)
 // for single launches, and the launch-totals reduction.
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "ks_interp_kernel.cuh"
 
 namespace ks {
@@ -62,17 +66,17 @@ static int g_attr_done[64];
 // form); the instrumented form for the cache model's passes and the
 // per-instruction profile, and that form with the issue-run log for the SM
 // issue model (the lean forms carry none of it).
-template <bool CTA, bool BIG>
+template <bool CTA, bool BIG, bool CAP>
 static const void* interp_fn_of(int form) {
-  return form == 0   ? (const void*)ks_interp_kernel<CTA, BIG, false, false, 1u>
-         : form == 1 ? (const void*)ks_interp_kernel<CTA, BIG, true, false, 1u>
-                     : (const void*)ks_interp_kernel<CTA, BIG, true, true, 1u>;
+  return form == 0   ? (const void*)ks_interp_kernel<CTA, BIG, false, false, 1u, CAP>
+         : form == 1 ? (const void*)ks_interp_kernel<CTA, BIG, true, false, 1u, CAP>
+                     : (const void*)ks_interp_kernel<CTA, BIG, true, true, 1u, CAP>;
 }
 
-static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, int form) {
-  if (!cta) return interp_fn_of<false, false>(form);
-  if (real_warps_per_cta > 8) return interp_fn_of<true, true>(form);
-  return interp_fn_of<true, false>(form);
+static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, int form, bool reg_capped) {
+  if (!cta) return reg_capped ? interp_fn_of<false, false, true>(form) : interp_fn_of<false, false, false>(form);
+  if (real_warps_per_cta > 8) return interp_fn_of<true, true, false>(form);
+  return interp_fn_of<true, false, false>(form);
 }
 
 int interp_form(const KsLaunch& L) {
@@ -92,23 +96,47 @@ static int ensure_attr() {
   if (e != cudaSuccess) return (int)e;
   for (int cta = 0; cta < 2; cta++)
     for (int big = 0; big < 2; big++)
-      for (int form = 0; form < 3; form++) {
-        if (!cta && big) continue;
-        e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, form), cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-        if (e != cudaSuccess) return (int)e;
-      }
+      for (int capped = 0; capped < 2; capped++)
+        for (int form = 0; form < 3; form++) {
+          if (!cta && big) continue;
+          if (cta && capped) continue;
+          e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, form, capped), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   mx);
+          if (e != cudaSuccess) return (int)e;
+        }
   if (dev < 64) g_attr_done[dev] = 1;
   return 0;
 }
 
-int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm) {
+// Resident CTAs per SM of one instantiation at one CTA size and shared-memory
+// size, asked of the runtime once per device and remembered (the shape
+// choice asks for several candidates at every launch).
+int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm,
+                     bool reg_capped) {
   int e = ensure_attr();
   if (e) return e;
-  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L));
-  return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, (int)(real_warps_per_cta * 32), smem);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
+  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L), reg_capped);
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, uint32_t, size_t>, int> known;
+  const auto key = std::make_tuple(dev, fn, real_warps_per_cta, smem);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    const auto it = known.find(key);
+    if (it != known.end()) {
+      *ctas_per_sm = it->second;
+      return 0;
+    }
+  }
+  e = (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, (int)(real_warps_per_cta * 32), smem);
+  if (e) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  known[key] = *ctas_per_sm;
+  return 0;
 }
 
-int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps_per_cta, uint32_t* real_ctas) {
+int choose_launch(const KsLaunch& L, int sms, int max_smem, LaunchShape* shape) {
   const uint64_t n_warps = L.n_warps;
   if (L.cta_mode) {
     // one real CTA per simulated CTA at a time, one real warp per simulated warp
@@ -117,8 +145,9 @@ int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps
     int per_sm = 0;
     if (interp_occupancy(L, L.wpc, smem, &per_sm)) return KS_ERR_CUDA;
     if (per_sm < 1) return KS_ERR_LIMIT;
-    *real_warps_per_cta = L.wpc;
-    *real_ctas = (uint32_t)std::min<uint64_t>(L.grid, (uint64_t)sms * (uint64_t)per_sm);
+    shape->warps_per_cta = L.wpc;
+    shape->ctas = (uint32_t)std::min<uint64_t>(L.grid, (uint64_t)sms * (uint64_t)per_sm);
+    shape->reg_capped = false;
     return KS_OK;
   }
   // Candidates: 1..12 real warps per CTA (one CTA of many warps holds one
@@ -127,47 +156,53 @@ int choose_launch(const KsLaunch& L, int sms, int max_smem, uint32_t* real_warps
   // SM gets work; among the rest
   // take the shape with the most resident real warps (shared memory,
   // registers and the CTA limit all count), then the larger CTA (fewer
-  // program copies).
+  // program copies). The register-capped form (CTAs of up to 10 warps) is
+  // taken only where it holds strictly more warps.
   uint32_t best_w = 0, best_ctas = 0;
+  bool best_capped = false;
   uint64_t best_res = 0;
   bool any_fit = false;
-  for (uint32_t w = 1; w <= 12; w++) {
-    const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, w, 0);
-    if (smem > (size_t)max_smem) break;
-    any_fit = true;
-    const uint64_t want = (n_warps + w - 1) / w;
-    if (w > 1 && want < 2ull * (uint64_t)sms) break;
-    int per_sm = 0;
-    const int e = interp_occupancy(L, w, smem, &per_sm);
-    if (e) return KS_ERR_CUDA;
-    if (per_sm < 1) continue;
-    const uint64_t cap = (uint64_t)sms * (uint64_t)per_sm;
-    const uint64_t res = std::min<uint64_t>(n_warps, cap * w);
-    if (res >= best_res) {
-      best_res = res;
-      best_w = w;
-      best_ctas = (uint32_t)std::min<uint64_t>(want, cap);
+  for (int capped = 0; capped < 2; capped++) {
+    for (uint32_t w = 1; w <= (capped ? 10u : 12u); w++) {
+      const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, w, 0);
+      if (smem > (size_t)max_smem) break;
+      any_fit = true;
+      const uint64_t want = (n_warps + w - 1) / w;
+      if (w > 1 && want < 2ull * (uint64_t)sms) break;
+      int per_sm = 0;
+      const int e = interp_occupancy(L, w, smem, &per_sm, capped != 0);
+      if (e) return KS_ERR_CUDA;
+      if (per_sm < 1) continue;
+      const uint64_t cap = (uint64_t)sms * (uint64_t)per_sm;
+      const uint64_t res = std::min<uint64_t>(n_warps, cap * w);
+      if (capped ? res > best_res : res >= best_res) {
+        best_res = res;
+        best_w = w;
+        best_ctas = (uint32_t)std::min<uint64_t>(want, cap);
+        best_capped = capped != 0;
+      }
     }
   }
   if (!any_fit || best_w == 0) return KS_ERR_LIMIT;
-  *real_warps_per_cta = best_w;
-  *real_ctas = best_ctas;
+  shape->warps_per_cta = best_w;
+  shape->ctas = best_ctas;
+  shape->reg_capped = best_capped;
   return KS_OK;
 }
 
-int launch_interp(const KsLaunch& L, uint32_t real_warps_per_cta, uint32_t real_ctas, void* stream) {
+int launch_interp(const KsLaunch& L, const LaunchShape& shape, void* stream) {
   int e = ensure_attr();
   if (e) return e;
-  const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, real_warps_per_cta,
+  const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, shape.warps_per_cta,
                                        L.cta_mode ? L.shared_bytes : 0u);
   KsGrid<1> G;
   G.n = 1;
   G.cta_begin[0] = 0;
-  G.cta_begin[1] = real_ctas;
+  G.cta_begin[1] = shape.ctas;
   G.item[0] = L;
   void* args[] = {&G};
-  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L)), dim3(real_ctas),
-                               dim3(real_warps_per_cta * 32), args, smem, (cudaStream_t)stream);
+  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, shape.warps_per_cta, form_of(L), shape.reg_capped),
+                               dim3(shape.ctas), dim3(shape.warps_per_cta * 32), args, smem, (cudaStream_t)stream);
 }
 
 int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream) {

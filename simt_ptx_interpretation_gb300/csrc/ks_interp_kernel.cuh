@@ -209,8 +209,11 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 // NB: launches per real grid (1, or KS_BATCH_ITEMS for ks_simulate_batch);
 // each real CTA runs the item whose CTA range holds it, as if that item's
 // CTAs were a grid of their own.
-template <bool CTA, bool BIG, bool INSTR, bool RUNLOG, uint32_t NB>
-__global__ void __launch_bounds__(BIG ? 1024 : (CTA ? 256 : 384), 1)
+// CAP (plain forms): compiled for two CTAs of up to 10 warps per SM, which
+// holds the kernel to 96 registers (no spills) so that 21 warps fit an SM
+// where registers, not shared memory, bound the resident warps.
+template <bool CTA, bool BIG, bool INSTR, bool RUNLOG, uint32_t NB, bool CAP = false>
+__global__ void __launch_bounds__(CAP ? 320 : (BIG ? 1024 : (CTA ? 256 : 384)), CAP ? 2 : 1)
     ks_interp_kernel(const __grid_constant__ KsGrid<NB> G) {
   uint32_t item = 0;
   if constexpr (NB > 1) {

@@ -135,9 +135,9 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KS_ERR_CUDA;
 
-  uint32_t wpc_real = 0, ctas = 0;
-  const int shape = ks::choose_launch(L, g_static_sms[dev], g_static_smem[dev], &wpc_real, &ctas);
-  if (shape != KS_OK) return shape;
-  if (ks::launch_interp(L, wpc_real, ctas, stream) != 0) return KS_ERR_CUDA;
+  ks::LaunchShape shape;
+  const int rc = ks::choose_launch(L, g_static_sms[dev], g_static_smem[dev], &shape);
+  if (rc != KS_OK) return rc;
+  if (ks::launch_interp(L, shape, stream) != 0) return KS_ERR_CUDA;
   return KS_OK;
 }
