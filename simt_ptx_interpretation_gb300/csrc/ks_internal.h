@@ -282,7 +282,7 @@ const KsKernel* module_kernel(const ks_module* mod, const char* name);
 // CTA; otherwise 1..12 real warps per CTA over all simulated warps. KS_OK,
 // KS_ERR_LIMIT (no shape fits the shared memory) or KS_ERR_CUDA.
 // The real launch of one simulation: CTAs of warps_per_cta real warps, and
-// (plain mode) whether the register-capped form runs it.
+// whether the register-capped form runs it.
 struct LaunchShape {
   uint32_t warps_per_cta;
   uint32_t ctas;

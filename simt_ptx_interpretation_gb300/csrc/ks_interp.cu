@@ -76,7 +76,7 @@ static const void* interp_fn_of(int form) {
 static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, int form, bool reg_capped) {
   if (!cta) return reg_capped ? interp_fn_of<false, false, true>(form) : interp_fn_of<false, false, false>(form);
   if (real_warps_per_cta > 8) return interp_fn_of<true, true, false>(form);
-  return interp_fn_of<true, false, false>(form);
+  return reg_capped ? interp_fn_of<true, false, true>(form) : interp_fn_of<true, false, false>(form);
 }
 
 int interp_form(const KsLaunch& L) {
@@ -99,7 +99,7 @@ static int ensure_attr() {
       for (int capped = 0; capped < 2; capped++)
         for (int form = 0; form < 3; form++) {
           if (!cta && big) continue;
-          if (cta && capped) continue;
+          if (big && capped) continue;
           e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, form, capped), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    mx);
           if (e != cudaSuccess) return (int)e;
@@ -142,12 +142,17 @@ int choose_launch(const KsLaunch& L, int sms, int max_smem, LaunchShape* shape) 
     // one real CTA per simulated CTA at a time, one real warp per simulated warp
     const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, L.wpc, L.shared_bytes);
     if (smem > (size_t)max_smem) return KS_ERR_LIMIT;
-    int per_sm = 0;
+    int per_sm = 0, per_sm_capped = 0;
     if (interp_occupancy(L, L.wpc, smem, &per_sm)) return KS_ERR_CUDA;
+    // the register-capped form (blocks of up to 8 warps) where it holds
+    // more CTAs
+    if (L.wpc <= 8 && interp_occupancy(L, L.wpc, smem, &per_sm_capped, true)) return KS_ERR_CUDA;
+    const bool capped = per_sm_capped > per_sm;
+    if (capped) per_sm = per_sm_capped;
     if (per_sm < 1) return KS_ERR_LIMIT;
     shape->warps_per_cta = L.wpc;
     shape->ctas = (uint32_t)std::min<uint64_t>(L.grid, (uint64_t)sms * (uint64_t)per_sm);
-    shape->reg_capped = false;
+    shape->reg_capped = capped;
     return KS_OK;
   }
   // Candidates: 1..12 real warps per CTA (one CTA of many warps holds one

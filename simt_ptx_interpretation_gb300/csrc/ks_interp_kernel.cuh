@@ -209,11 +209,12 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 // NB: launches per real grid (1, or KS_BATCH_ITEMS for ks_simulate_batch);
 // each real CTA runs the item whose CTA range holds it, as if that item's
 // CTAs were a grid of their own.
-// CAP (plain forms): compiled for two CTAs of up to 10 warps per SM, which
-// holds the kernel to 96 registers (no spills) so that 21 warps fit an SM
-// where registers, not shared memory, bound the resident warps.
+// CAP: compiled for more CTAs per SM where registers, not shared memory,
+// bound the resident warps: plain, two CTAs of up to 10 warps (96
+// registers, no spills, 21 warps an SM); CTA mode, three CTAs of up to 8
+// warps (80 registers, a few spills, 24 warps an SM).
 template <bool CTA, bool BIG, bool INSTR, bool RUNLOG, uint32_t NB, bool CAP = false>
-__global__ void __launch_bounds__(CAP ? 320 : (BIG ? 1024 : (CTA ? 256 : 384)), CAP ? 2 : 1)
+__global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ? 256 : 384)), CAP ? (CTA ? 3 : 2) : 1)
     ks_interp_kernel(const __grid_constant__ KsGrid<NB> G) {
   uint32_t item = 0;
   if constexpr (NB > 1) {
