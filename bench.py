@@ -413,7 +413,8 @@ def run_ours(args, world, rank, local):
     # between): charge the whole call to the two interpreter passes
     passes = 2 if cache else 1  # (the SM model's replay runs once per call)
     achieved = passes * insts / span_s / 1e9
-    traffic = traffic_for(config["workload"])
+    # the stored counters are for the full-size workloads only
+    traffic = traffic_for(config["workload"]) if args.scale == 1 and args.iters == 4096 else None
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "Gthread-inst/s",
                 "frac": round(achieved / peak, 5), "traffic": traffic,
                 "peak_source": f"{sms} SMs x 4 issue/clk x 32 lanes x {mhz:.0f} MHz ({peak_src})",
