@@ -230,11 +230,18 @@ typedef struct {
  * stack depth 32, step limit 2^26, injection off. */
 void ks_config_default(ks_config* cfg);
 
-/* Parses and decodes a PTX module (host only; no GPU work). `len` bytes of
- * `ptx` (need not be NUL-terminated). On success *out owns the module; free
- * it with ks_free_module. On failure returns KS_ERR_PARSE /
- * KS_ERR_UNSUPPORTED / KS_ERR_LIMIT / KS_ERR_ARG with a message in err
- * (NUL-terminated, truncated to errlen). */
+/* Parses and decodes a PTX module (host only; no GPU work): the C form of the
+ * page's two loading steps (KernelScope backend doc, "PTX Parser" —
+ * ptx/parser.py parse_ptx, which turns the module text into kernels,
+ * parameters and instructions with their optional predicates; and
+ * simulator/engine.py PtxSimulator.load_kernel, which keeps the executable
+ * instructions and builds the pc lookup table). Here the kernels are decoded
+ * once into packed instruction records with their reconvergence points, and
+ * any kernel of the module can be simulated by name (the page's load_kernel
+ * takes the first). `len` bytes of `ptx` (need not be NUL-terminated). On
+ * success *out owns the module; free it with ks_free_module. On failure
+ * returns KS_ERR_PARSE / KS_ERR_UNSUPPORTED / KS_ERR_LIMIT / KS_ERR_ARG with
+ * a message in err (NUL-terminated, truncated to errlen). */
 int ks_load_module(const char* ptx, size_t len, ks_module** out, char* err, size_t errlen);
 
 /* Frees the module and the device copies of its programs (which are created
@@ -258,9 +265,13 @@ int ks_kernel_event(const ks_module* mod, const char* kernel, uint32_t id, uint3
 int ks_kernel_ipdom(const ks_module* mod, const char* kernel, int32_t* out, uint32_t cap,
                     uint32_t* n_out);
 
-/* Sizes of the caller-owned output buffers:
- * trace = W * align8(16 + 4 * max_ts_per_warp), stats = W * 96, where
- * W = grid * ceil(block / 32). */
+/* Size of the caller-owned trace buffer (CuTeDSL IKET 浅析, §2 "buffer
+ * 是怎么定形的" — compute_warp_buffer_size_bytes: one slot per warp of
+ * align8(16-byte header + maxTsCntPerWarp x bytes_per_event), warps per CTA
+ * = ceil(block / 32)): W * align8(16 + 4 * max_ts_per_warp), W = grid *
+ * ceil(block / 32). The page multiplies its total by 1.15 for launches whose
+ * grid is not known in advance; the grid is an argument here, so the size is
+ * exact and ks_simulate rejects anything smaller. */
 size_t ks_trace_bytes(uint32_t grid, uint32_t block, uint32_t max_ts_per_warp);
 /* The same for records of `record_bytes` (ks_kernel_record_bytes):
  * W * align8(16 + record_bytes * max_ts_per_warp). ks_simulate requires
@@ -270,13 +281,28 @@ size_t ks_trace_bytes_records(uint32_t grid, uint32_t block, uint32_t max_ts_per
 int ks_kernel_record_bytes(const ks_module* mod, const char* kernel, uint32_t* bytes);
 /* Payload size of event `id`: 0, 4 or 8 bytes. */
 int ks_kernel_event_payload(const ks_module* mod, const char* kernel, uint32_t id, uint32_t* bytes);
+/* Size of the caller-owned stats buffer: W * 96 bytes, one ks_warp_stats
+ * record per simulated warp. The record holds, per warp, what the page's
+ * trace carries per executed instruction and its analyses count
+ * (KernelScope backend doc, simulator/models.py — TraceEvent.active_threads,
+ * the popcount of the active mask, summed into thread_insts; and
+ * simulator/engine.py — analyze_global_memory_access sectors and lines,
+ * analyze_shared_memory_access degrees), plus the cycle count and status. */
 size_t ks_stats_bytes(uint32_t grid, uint32_t block);
 /* Bytes of a kernel's per-instruction profile: 72 per program entry. */
 int ks_profile_bytes(const ks_module* mod, const char* kernel, size_t* bytes);
 
 /* Enqueues the interpretation of `kernel` over grid x block simulated
  * threads on `stream` (a cudaStream_t; NULL = the legacy default stream) of
- * the current device, and returns without waiting.
+ * the current device, and returns without waiting. This is the page's
+ * simulation call (KernelScope backend doc: api/routes.py calls
+ * simulate_kernel(parsed, sim_config), sim_config holding {grid_dim,
+ * block_dim}; the simulation is simulator/engine.py PtxSimulator.run(), whose
+ * step() executes one instruction of every unfinished warp until all have
+ * finished), run to
+ * completion for every warp of the grid: the page's max_steps bound becomes
+ * the per-warp cfg->step_limit, and its trace list becomes the per-warp
+ * statistics records and IKET trace slots.
  *   params      host pointer to the kernel's parameter block (layout from
  *               ks_kernel_param), param_bytes >= the kernel's block size,
  *               at most KS_MAX_PARAM_BYTES; copied at launch.
@@ -304,9 +330,14 @@ int ks_simulate(const ks_module* mod, const char* kernel, uint32_t grid, uint32_
                 const ks_config* cfg, void* stream);
 
 /* Allocation-free variant of ks_simulate. The pages have no counterpart: it
- * exists for callers that cannot let a library allocate device memory —
- * code running during CUDA graph capture, programs that give all device
- * memory to their own allocator, embedders with a fixed budget. Instead of the
+ * exists for callers that cannot let a library call cudaMalloc. Some
+ * processes hand all of the GPU's memory to their own pool when they start
+ * (a serving process that reserves its HBM up front), so a library
+ * allocation would fail or fragment it; some run under a fixed device-memory
+ * budget that is checked once at start-up and may not grow afterwards (a
+ * tenant under an MPS memory limit, an embedded or certified deployment); and
+ * some cannot afford the implicit device-wide synchronisation that
+ * cudaMalloc / cudaFree may cause while other streams are busy. Instead of the
  * per-module device copy that ks_simulate allocates, the kernel's program
  * image (its decoded instructions and constant rows: 64 bytes per program
  * entry plus 4 per constant row) is copied with cudaMemcpyAsync on `stream`
@@ -370,9 +401,18 @@ int ks_simulate_batch(const ks_batch_item* items, uint32_t n_items, void* stream
                       uint32_t* n_launched);
 
 /* Reduces n_warps stats records (device pointer) on `stream`, waits for the
- * stream, and writes the totals to *out (host). Uses a small device
- * accumulator that the library allocates once per device; calls are
- * serialised inside the library. */
+ * stream, and writes the totals to *out (host): the launch-wide sums of the
+ * per-warp records (KernelScope backend doc, simulator/models.py —
+ * TraceEvent.active_threads summed over the trace, here thread_insts), the
+ * largest cycle count, and the first failing warp with its status. Uses a
+ * small device accumulator that the library allocates once per device; calls
+ * are serialised inside the library.
+ * Shape: the call takes the stats buffer and its warp count rather than only
+ * (stream, host totals, device status), because the library keeps no state
+ * per simulation: the records live in the caller's buffer, any earlier
+ * simulation's records can be reduced again, and the device status of the
+ * launch is the `status` / first_failed_warp fields of *out (the status of the
+ * lowest-indexed failing warp), so no separate status word is needed. */
 int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_totals* out);
 
 /* ---- L1/L2 hit model (KernelScope backend doc, simulator/engine.py —
@@ -452,11 +492,13 @@ size_t ks_cache_workspace_bytes(uint32_t grid, uint32_t block, const ks_cache_co
  * plus cc (host; NULL = defaults) and `workspace`, device memory of at least
  * ks_cache_workspace_bytes(grid, block, cc) bytes (KS_ERR_ARG otherwise, and
  * for an invalid cc; KS_ERR_LIMIT when ceil(log2(l1_lines)) + 32 +
- * ceil(log2(W)) > 64, the sort key's width). Enqueues the first pass, waits
- * for `stream` once (to read the number of logged accesses, which sizes the
- * sorts: they cost in proportion to the accesses made, not to the log's
- * capacity), then enqueues the sorts and the second pass and returns; so the
- * call cannot be captured into a CUDA graph. Afterwards the workspace holds the per-warp
+ * ceil(log2(W)) > 64, the sort key's width). Unlike ks_simulate, this call
+ * does not only enqueue: it enqueues the first pass, then BLOCKS the calling
+ * host thread until `stream` has finished everything enqueued on it so far
+ * (one cudaStreamSynchronize, to read the number of logged accesses, which
+ * sizes the sorts: they cost in proportion to the accesses made, not to the
+ * log's capacity), then enqueues the sorts and the second pass and returns;
+ * so the call cannot be captured into a CUDA graph. Afterwards the workspace holds the per-warp
  * counts and the access log with each access's level; per-warp statuses
  * KS_ST_CACHE_LOG and KS_ST_CACHE_STREAM report a log that was too small or
  * an access stream that the first pass could not predict. */

@@ -3,11 +3,16 @@
 //
 // ks_simulate keeps each kernel's program image (decoded instructions and
 // constant rows) in device memory that the library allocates on first use
-// per device. Some callers cannot let a library allocate device memory: code
-// running while a CUDA graph is being captured, programs that hand all device
-// memory to their own pool, or embedders with a fixed memory budget. For them
-// this entry point stages the image into the file-scope array below instead,
-// which every GPU that loads the library holds until the process exits.
+// per device. Some callers cannot let a library call cudaMalloc: processes
+// that give all of the GPU's memory to their own pool at start-up (the
+// library's allocation would fail or fragment it), deployments with a fixed
+// device-memory budget that may not grow after start-up, and callers that
+// cannot afford the implicit device-wide synchronisation cudaMalloc /
+// cudaFree may cause. For them this entry point stages the image into the
+// file-scope array below instead, which every GPU that loads the library
+// holds until the process exits. It calls no allocating routine: the array's
+// address comes from cudaGetSymbolAddress, the launch shape from device
+// attributes and the occupancy calculator.
 #include <cuda_runtime.h>
 
 #include <algorithm>

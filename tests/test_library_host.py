@@ -206,3 +206,75 @@ def test_cached_batch_arguments_are_checked_before_any_gpu_work():
     items[0].cache = ctypes.pointer(bad)
     assert L.ks_simulate_cached_batch(items, 2, None, ctypes.byref(failed), None) == -3 and failed.value == 0
     assert ctypes.sizeof(_native.KsCachedItem) == 120
+
+
+def test_static_entry_point_rejects_what_ks_simulate_rejects():
+    """ks_simulate_static repeats ks_simulate's argument checks; both must
+    return the same code for every invalid call. Each case fails on the host
+    before any CUDA call (device pointers here are never dereferenced)."""
+    L = _native.lib()
+    w = wl.vector_add(n=4000)
+    mod = ks.Module(w.ptx)
+    FAKE = 0x10000  # a non-null device pointer that no case reaches
+    W = w.grid * ((w.block + 31) // 32)
+
+    def base():
+        bufs = (_native.KsBuffer * 8)()
+        for i, b in enumerate(w.buffers):
+            bufs[i].sim_base, bufs[i].dev_ptr, bufs[i].bytes = b.sim_base, FAKE, b.data.nbytes
+        cfg = _native.KsConfig()
+        L.ks_config_default(ctypes.byref(cfg))
+        cfg.max_ts_per_warp = 8
+        return dict(mod=mod.handle, kernel=w.kernel.encode(), grid=w.grid, block=w.block, params=bytes(w.params),
+                    param_bytes=len(w.params), bufs=bufs, n_bufs=len(w.buffers), trace=FAKE,
+                    trace_bytes=W * 48, stats=FAKE, stats_bytes=W * 96, cfg=cfg)
+
+    def overlap(a):
+        a["bufs"][1].sim_base = a["bufs"][0].sim_base
+
+    def cfgset(field, value):
+        return lambda a: setattr(a["cfg"], field, value)
+
+    def lat(a):
+        a["cfg"].lat[3] = (1 << 24) + 1
+
+    def profile(a):
+        a["cfg"].profile_buf, a["cfg"].profile_bytes = FAKE, 72
+
+    cases = {
+        "null module": lambda a: a.update(mod=None),
+        "unknown kernel": lambda a: a.update(kernel=b"nope"),
+        "grid 0": lambda a: a.update(grid=0),
+        "block 0": lambda a: a.update(block=0),
+        "block 1025": lambda a: a.update(block=1025),
+        "2^31 warps": lambda a: a.update(grid=1 << 28, block=256),
+        "short params": lambda a: a.update(param_bytes=len(w.params) - 4),
+        "params over 256 B": lambda a: a.update(params=bytes(260), param_bytes=260),
+        "null params": lambda a: a.update(params=None),
+        "9 buffers": lambda a: a.update(n_bufs=9),
+        "null buffer table": lambda a: a.update(bufs=None),
+        "unaligned sim_base": lambda a: setattr(a["bufs"][0], "sim_base", a["bufs"][0].sim_base + 16),
+        "empty buffer": lambda a: setattr(a["bufs"][1], "bytes", 0),
+        "null buffer pointer": lambda a: setattr(a["bufs"][2], "dev_ptr", None),
+        "overlapping buffers": overlap,
+        "null stats": lambda a: a.update(stats=None),
+        "short stats": lambda a: a.update(stats_bytes=W * 96 - 1),
+        "stack depth 0": cfgset("simt_stack_depth", 0),
+        "stack depth 33": cfgset("simt_stack_depth", 33),
+        "max_ts over 2^24": cfgset("max_ts_per_warp", (1 << 24) + 1),
+        "latency over 2^24": lat,
+        "short trace": lambda a: a.update(trace_bytes=W * 48 - 8),
+        "short profile": profile,
+    }
+    for name, mutate in cases.items():
+        a = base()
+        mutate(a)
+        codes = []
+        for fn in (L.ks_simulate, L.ks_simulate_static):
+            pb = ctypes.create_string_buffer(a["params"], max(1, len(a["params"]))) if a["params"] is not None else None
+            codes.append(fn(a["mod"], a["kernel"], a["grid"], a["block"],
+                            ctypes.cast(pb, ctypes.c_void_p) if pb is not None else None, a["param_bytes"], a["bufs"],
+                            a["n_bufs"], a["trace"], a["trace_bytes"], a["stats"], a["stats_bytes"],
+                            ctypes.byref(a["cfg"]), None))
+        assert codes[0] == codes[1], f"{name}: ks_simulate {codes[0]}, ks_simulate_static {codes[1]}"
+        assert codes[0] < 0, f"{name}: accepted ({codes[0]})"
