@@ -16,6 +16,14 @@ logging pass, the sorted levels, the checked second pass); --sched with the
 SM-level issue model (ks_simulate_sched: the interpreter logging each warp's
 issued runs, then one replay warp per simulated SM).
 
+The default run (headline workload, one GPU) also measures every benchmark
+configuration at its stated size on its own and adds them to the line as
+"per_config": vector_add, the FFMA pair, the strided gather at s = 1, 8, 32
+(roofline against HBM), the divergent workload at k = 2, 4, 32, the 64 fuzz
+kernels and the shared-memory reduction, each with the median, minimum and
+mean over --config-reps timed repetitions (L2 flushed before each) and the
+oracle's rate on all host cores and on one core.
+
 Prints one JSON line (rank 0). N > 1 runs N independent replicas, one per
 GPU (weak scaling; the path has no exchange step).
 """
@@ -46,6 +54,14 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_SM_MHZ = 2070.0
 
 
+# The configurations measured by the per-configuration suite: every benchmark
+# configuration at its stated size (vector_add; the FFMA probe pair; the
+# strided gather at s = 1, 8, 32; the divergent workload at k = 2, 4, 32; the
+# 64 fuzz kernels) and the shared-memory reduction.
+SUITE = ("vector_add", "ffma_pair", "gather_s1", "gather_s8", "gather_s32", "divergent_k2", "divergent_k4",
+         "divergent_k32", "fuzz", "smem_reduce")
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -70,6 +86,12 @@ def parse_args():
                    help="one ks_simulate per launch instead of one ks_simulate_batch per step")
     p.add_argument("--scale", type=int, default=1,
                    help="divide the gather outputs, divergent threads or fuzz kernels (smaller cases for profiling)")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the per-configuration suite that the default run adds to its line")
+    p.add_argument("--config-reps", type=int, default=50, help="timed repetitions per configuration (suite)")
+    p.add_argument("--config-warmup", type=int, default=3, help="warm-up repetitions per configuration (suite)")
+    p.add_argument("--configs", default=",".join(SUITE),
+                   help="comma-separated configurations of the suite (default: all)")
     return p.parse_args()
 
 
@@ -417,6 +439,8 @@ def run_ours(args, world, rank, local):
     traffic = traffic_for(config["workload"]) if args.scale == 1 and args.iters == 4096 else None
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1), "unit": "Gthread-inst/s",
                 "frac": round(achieved / peak, 5), "traffic": traffic,
+                "measure": "simulated thread-instructions per second against the GPU's issue peak in "
+                           "thread-instructions (1.0 would be one simulated instruction per real issue slot)",
                 "peak_source": f"{sms} SMs x 4 issue/clk x 32 lanes x {mhz:.0f} MHz ({peak_src})",
                 "algorithmic_units_per_launch": [int(x) for x in launch_insts],
                 "launch_ms_mean": [round(sum(x) / len(x), 4) for x in launch_ms],
@@ -437,7 +461,9 @@ def run_ours(args, world, rank, local):
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(sum(step_ms) / len(step_ms), 4), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(sum(step_ms) / len(step_ms), 4),
+        "ms_per_step_median": round(statistics.median(step_ms), 4), "ms_per_step_min": round(min(step_ms), 4),
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)", "data": "synthetic (seeded)",
         "config": dict(config, l2="flushed between steps (256 MiB write)", parallelism=f"replicas{world}",
                        streams=n_streams, batched=bool(batch or cache_batch)),
@@ -454,6 +480,12 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = (cpu_baseline_cached(ws, cache) if cache else cpu_baseline_sched(ws, sched) if sched
                                 else cpu_baseline(ws, sample_warps=None))
+    # the default run (headline workload, plain model, one GPU) adds every
+    # configuration measured on its own
+    if (world == 1 and not args.no_per_config and args.workload == "ffma_pair" and not (cache or sched)
+            and args.scale == 1 and args.iters == 4096):
+        torch.cuda.empty_cache()
+        line["per_config"] = run_suite(args, dev, stream)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -515,17 +547,19 @@ def run_e2e(args, jobs, insts, dev, streams, launch, fork, join, launch_batch=No
             "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
 
 
-def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None):
+def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None, threads=None, buffers=None):
     """The oracle, as it stands, on the host cores over a bounded sample of the
     workload: the first `n` warps of every kernel (whole CTAs for kernels with
-    shared memory or barriers, every one of which is counted)."""
+    shared memory or barriers, every one of which is counted), on `threads`
+    host threads (default: every core). `buffers`: per kernel, buffers to run
+    on (default: a fresh copy of the kernel's inputs)."""
     import oracle
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     n = max_warps_per_kernel or 40 * cores
     total_i, total_s, desc = 0, 0.0, []
-    for w in ws:
+    for i, w in enumerate(ws):
         warps = list(range(min(n, w.warps)))
-        bufs = w.fresh_buffers()
+        bufs = buffers[i] if buffers is not None else w.fresh_buffers()
         t0 = time.perf_counter()
         r = oracle.run(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in bufs],
                        max_ts=w.max_ts, trace=bool(w.max_ts), warps=warps, threads=cores)
@@ -535,6 +569,151 @@ def cpu_baseline(ws, sample_warps=None, max_warps_per_kernel=None):
         desc.append(f"{w.name}: warps 0..{int(np.nonzero(ran)[0].max())} of {w.warps}")
     return {"value": round(total_i / total_s, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "; ".join(desc), "thread_insts": total_i, "seconds": round(total_s, 3)}
+
+
+def cpu_baseline_suite(ws, target_s: float = 2.0):
+    """The oracle on a bounded sample of one configuration, on every host core
+    and on one core: the first n warps of every kernel (of every eighth kernel
+    when there are more than eight, so that each call's set-up stays small
+    against its warps), n grown from a small probe until a leg takes about
+    target_s (or covers every warp). The oracle's stores are idempotent for
+    these workloads (no kernel reads what it stores), so the probes share one
+    copy of the inputs."""
+    cores = os.cpu_count() or 1
+    if len(ws) > 8:
+        ws = ws[::8]
+    bufs = [w.fresh_buffers() for w in ws]
+    most = max(w.warps for w in ws)
+    legs = {}
+    for label, threads in (("all_cores", cores), ("one_core", 1)):
+        n = min(most, 2 * threads)
+        r = cpu_baseline(ws, max_warps_per_kernel=n, threads=threads, buffers=bufs)
+        while r["seconds"] < target_s / 3 and n < most:
+            n = min(most, max(n + 1, int(n * min(64.0, target_s / max(r["seconds"], 1e-4)))))
+            r = cpu_baseline(ws, max_warps_per_kernel=n, threads=threads, buffers=bufs)
+        legs[label] = r
+    a, o = legs["all_cores"], legs["one_core"]
+    return {"value": a["value"], "unit": UNIT, "cores": cores, "kind": "oracle", "sample": a["sample"],
+            "thread_insts": a["thread_insts"], "seconds": a["seconds"],
+            "one_core": {"value": o["value"], "cores": 1, "sample": o["sample"], "thread_insts": o["thread_insts"],
+                         "seconds": o["seconds"]}}
+
+
+def hbm_peak():
+    try:
+        return float(json.load(open(PEAKS_FILE))["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+def gather_bytes(w, s: int) -> int:
+    """Algorithmic DRAM bytes of one strided-gather launch: per warp, min(32,
+    4s) sectors of 32 bytes read (sector-granular), one 128-byte store and its
+    96-byte statistics record."""
+    return w.warps * (min(32, 4 * s) * 32 + 128 + 96)
+
+
+def issue_peak(dev):
+    """G thread-inst/s the GPU issues at most: SMs x 4 warp-instructions per
+    clock x 32 lanes x the measured maximum SM clock."""
+    import torch
+    mhz, src = sm_peak_mhz()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return sms * 4 * 32 * mhz * 1e6 / 1e9, f"{sms} SMs x 4 issue/clk x 32 lanes x {mhz:.0f} MHz ({src})"
+
+
+def measure_config(name: str, reps: int, warmup: int, dev, stream, flush, cpu: bool = True):
+    """One configuration at its stated size: plain simulations (one
+    ks_simulate_batch call when it has several launches), `warmup` untimed
+    repetitions, then `reps` timed ones with the L2 flushed before each,
+    CUDA events on the launching stream around each; median, minimum and
+    mean, the roofline of the interpreter launch and the oracle's rate."""
+    import torch
+    import simt_ptx_interpretation_gb300 as ks
+    ws, config = workloads(name)
+    jobs = []
+    for w in ws:
+        mod = ks.Module(w.ptx)
+        bufs = [(b.sim_base, torch.from_numpy(b.data.view(np.uint8)).to(dev)) for b in w.buffers]
+        cfg = ks.Config(max_ts=w.max_ts)
+        st = torch.empty(ks.stats_bytes(w.grid, w.block), dtype=torch.uint8, device=dev)
+        tr = (torch.empty(ks.trace_bytes(w.grid, w.block, w.max_ts, mod.record_bytes(w.kernel)), dtype=torch.uint8,
+                          device=dev) if w.max_ts else None)
+        jobs.append((w, mod, bufs, cfg, st, tr))
+    items = [ks.BatchItem(mod, w.kernel, w.grid, w.block, w.params, bufs, st, tr, cfg)
+             for (w, mod, bufs, cfg, st, tr) in jobs]
+    launched = [0]
+
+    def step():
+        if len(items) > 1:
+            launched[0] = ks.simulate_batch(items, stream)
+        else:
+            w, mod, bufs, cfg, st, tr = jobs[0]
+            ks.simulate(mod, w.kernel, w.grid, w.block, w.params, bufs, st, tr, cfg, stream)
+            launched[0] = 1
+
+    step()
+    insts = 0
+    for (w, mod, bufs, cfg, st, tr) in jobs:
+        t = ks.read_stats(st, w.warps, stream)
+        if t.status != 0:
+            raise SystemExit(f"simulation status {t.status} on {w.name}")
+        insts += t.thread_insts
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with ClockSampler(dev.index or 0) as clk:
+        for k in range(reps):
+            flush.zero_()
+            evs[k][0].record(stream)
+            step()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in evs]
+    med, mn, mean = statistics.median(ms), min(ms), sum(ms) / len(ms)
+    entry = {"config": config, "reps": reps, "warmup": warmup, "ms_median": round(med, 5), "ms_min": round(mn, 5),
+             "ms_mean": round(mean, 5), "value": round(insts / (med / 1e3), 1),
+             "value_at_min": round(insts / (mn / 1e3), 1), "unit": UNIT, "thread_insts_per_step": int(insts),
+             "gpu_launches_per_step": launched[0], "l2": "flushed before each repetition (256 MiB write)",
+             "clocks": clk.summary()}
+    traffic = traffic_for(config["workload"])
+    if name.startswith("gather_s"):
+        s_ = int(name[len("gather_s"):])
+        nbytes = gather_bytes(ws[0], s_)
+        hbm, src = hbm_peak()
+        achieved = nbytes / (med / 1e3) / 1e9
+        entry["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                             "frac": round(achieved / hbm, 5), "traffic": traffic,
+                             "algorithmic_bytes_per_launch": int(nbytes),
+                             "peak_source": f"copy bandwidth, MEASURED_PEAKS.json ({src})",
+                             "timed_over": "the median launch"}
+    else:
+        peak, src = issue_peak(dev)
+        achieved = insts / (med / 1e3) / 1e9
+        entry["roofline"] = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1),
+                             "unit": "Gthread-inst/s", "frac": round(achieved / peak, 5), "traffic": traffic,
+                             "measure": "simulated thread-instructions per second against the GPU's issue peak "
+                                        "in thread-instructions (1.0 would be one simulated instruction per real "
+                                        "issue slot)",
+                             "peak_source": src, "timed_over": "the median step"}
+    if cpu:
+        entry["cpu_baseline"] = cpu_baseline_suite(ws)
+    del jobs, items
+    return entry
+
+
+def run_suite(args, dev, stream):
+    """Every configuration of SUITE (or --configs) measured in turn."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    out = {}
+    for name in [c for c in args.configs.split(",") if c]:
+        out[name] = measure_config(name, args.config_reps, args.config_warmup, dev, stream, flush,
+                                   cpu=not args.no_cpu_baseline)
+        torch.cuda.empty_cache()
+    return out
 
 
 def cpu_baseline_cached(ws, cache, warps_per_kernel=16):
