@@ -50,6 +50,7 @@ UNIT = "thread-inst/s"
 KERNEL_SRC = [os.path.join(ROOT, "simt_ptx_interpretation_gb300", "csrc", f)
               for f in ("ks_interp_kernel.cuh", "ks_interp.cu", "ks_batch.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+NCU_FILE = os.path.join(ROOT, "profiles", "ncu_full_size.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_SM_MHZ = 2070.0
 
@@ -229,6 +230,19 @@ def traffic_for(workload: str):
     return t.get("workloads", {}).get(workload)
 
 
+def ncu_figures(workload: str):
+    """Per-launch ncu figures of a full-size workload (DRAM bytes, issue and
+    warp activity) from the committed capture, if it was taken on the current
+    kernel source; else None."""
+    try:
+        t = json.load(open(NCU_FILE))
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_sha") != kernel_sha():
+        return None
+    return t.get("workloads", {}).get(workload)
+
+
 def sm_peak_mhz():
     try:
         return float(json.load(open(PEAKS_FILE)).get("sm_max_mhz", FALLBACK_SM_MHZ)), "measured"
@@ -311,7 +325,7 @@ def run_ours(args, world, rank, local):
             probe = ks.SchedConfig(n_sm=args.sched_sms, max_runs_per_warp=1 << 16)
             nb = ks.sched_workspace_bytes(w.grid, w.block, probe)
             tmp = torch.empty(nb, dtype=torch.uint8, device=dev)
-            sw = torch.empty(w.warps * 64, dtype=torch.uint8, device=dev)
+            sw = torch.empty(w.warps * ks.SCHED_WARP_DTYPE.itemsize, dtype=torch.uint8, device=dev)
             ss = torch.empty(args.sched_sms * 32, dtype=torch.uint8, device=dev)
             ks.simulate_sched(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], sw, ss, tmp, j["tr"],
                               j["cfg"], probe, stream)
@@ -321,7 +335,8 @@ def run_ours(args, world, rank, local):
         sched = ks.SchedConfig(n_sm=args.sched_sms, max_runs_per_warp=1 << (runs - 1).bit_length())
         nbytes = ks.sched_workspace_bytes(wmax.grid, wmax.block, sched)
         sched_ws = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
-        sched_w = [torch.empty(wmax.warps * 64, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
+        sched_w = [torch.empty(wmax.warps * ks.SCHED_WARP_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+                   for _ in range(n_streams)]
         sched_s = [torch.empty(args.sched_sms * 32, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
         config = dict(config, sm_model={"n_sm": sched.n_sm, "schedulers_per_sm": sched.schedulers_per_sm,
                                         "ctas_per_sm": "fill 32 warps", "max_runs_per_warp": sched.max_runs_per_warp})
@@ -678,7 +693,8 @@ def measure_config(name: str, reps: int, warmup: int, dev, stream, flush, cpu: b
              "value_at_min": round(insts / (mn / 1e3), 1), "unit": UNIT, "thread_insts_per_step": int(insts),
              "gpu_launches_per_step": launched[0], "l2": "flushed before each repetition (256 MiB write)",
              "clocks": clk.summary()}
-    traffic = traffic_for(config["workload"])
+    ncu = ncu_figures(config["workload"])
+    traffic = ncu["dram_bytes"] if ncu else traffic_for(config["workload"])
     if name.startswith("gather_s"):
         s_ = int(name[len("gather_s"):])
         nbytes = gather_bytes(ws[0], s_)
@@ -689,6 +705,9 @@ def measure_config(name: str, reps: int, warmup: int, dev, stream, flush, cpu: b
                              "algorithmic_bytes_per_launch": int(nbytes),
                              "peak_source": f"copy bandwidth, MEASURED_PEAKS.json ({src})",
                              "timed_over": "the median launch"}
+        if traffic:  # what the GPU actually moved (whole lines when the stride leaves sectors unused)
+            dram = traffic / (med / 1e3) / 1e9
+            entry["roofline"].update(dram_gbs=round(dram, 2), dram_frac=round(dram / hbm, 5))
     else:
         peak, src = issue_peak(dev)
         achieved = insts / (med / 1e3) / 1e9
@@ -698,6 +717,8 @@ def measure_config(name: str, reps: int, warmup: int, dev, stream, flush, cpu: b
                                         "in thread-instructions (1.0 would be one simulated instruction per real "
                                         "issue slot)",
                              "peak_source": src, "timed_over": "the median step"}
+    if ncu:  # the interpreter's own instruction stream, per ncu on this kernel source
+        entry["roofline"]["ncu"] = {k: v for k, v in ncu.items() if k != "dram_bytes"}
     if cpu:
         entry["cpu_baseline"] = cpu_baseline_suite(ws)
     del jobs, items

@@ -545,9 +545,18 @@ int ks_simulate_cached_batch(const ks_cached_item* items, uint32_t n_items, void
  * anything else or a branch's latency ("execution dependency"; when results of
  * several kinds arrive in the same cycle the load counts first, then div/sqrt);
  * a barrier's release ("barrier"). Per warp: start + issued + the waits + the
- * drain after its last issue = end. Not modelled: the page's memory throttle
- * (a bound on memory requests in flight across the whole simulator) and its
- * divergence stall (serialised paths already issue one after the other). */
+ * drain after its last issue = end.
+ * Two more of the page's reasons are labels on issued instructions, as the
+ * page's own step() attaches them (it never holds a warp back for them), so
+ * they are counts of instructions, not cycles, and change no timing:
+ * "memory throttle" (the page: an instruction of its memory class — ld, st,
+ * mov — issued while 4 or more memory operations are pending), read per SM:
+ * an ld.*, st.* or mov issued at a cycle when at least 4 other warps of its
+ * SM have their latest global or shared load or store issued at an earlier
+ * cycle and not yet complete (the load's result not yet ready, the store not
+ * yet drained); and "divergence" (declared by the page, returned nowhere),
+ * read as: an instruction issued while some of the warp's live lanes (lanes
+ * that have not executed ret) wait on the reconvergence stack. */
 typedef struct {
   uint32_t n_sm;              /* simulated SMs (default 152) */
   uint32_t ctas_per_sm;       /* resident CTAs per SM, ctas_per_sm * ceil(block / 32) <= 32;
@@ -558,7 +567,7 @@ typedef struct {
   uint32_t reserved[4];
 } ks_sched_config;
 
-/* Per-warp schedule record (64 bytes), indexed by global warp id. */
+/* Per-warp schedule record (80 bytes), indexed by global warp id. */
 typedef struct {
   uint64_t start, end;     /* the SM cycles at which the warp's CTA started, and its last
                               result or store completed */
@@ -568,6 +577,10 @@ typedef struct {
   uint64_t stall_mem;      /* waiting on a load's result */
   uint64_t stall_math;     /* waiting on a div / sqrt result */
   uint64_t stall_barrier;  /* waiting at bar.sync for the release */
+  uint64_t throttled;      /* label: ld / st / mov issued with >= 4 other warps' memory
+                              operations pending on the SM (instructions, not cycles) */
+  uint64_t diverged;       /* label: instructions issued while live lanes of the warp
+                              waited on the reconvergence stack */
 } ks_sched_warp;
 
 /* Per-SM record (32 bytes). */

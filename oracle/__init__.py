@@ -301,7 +301,7 @@ def run_events(ptx: str, kernel: str, grid: int, block: int, params: bytes, buff
 # SM issue model outputs (orc_run_sched)
 SCHED_WARP_DTYPE = np.dtype([("start", "<u8"), ("end", "<u8"), ("issued", "<u8"), ("not_selected", "<u8"),
                              ("stall_exec", "<u8"), ("stall_mem", "<u8"), ("stall_math", "<u8"),
-                             ("stall_barrier", "<u8")])
+                             ("stall_barrier", "<u8"), ("throttled", "<u8"), ("diverged", "<u8")])
 SCHED_SM_DTYPE = np.dtype([("cycles", "<u8"), ("issued", "<u8"), ("ctas", "<u8"), ("status", "<i4"),
                            ("reserved", "<u4")])
 

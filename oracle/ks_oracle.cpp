@@ -1391,6 +1391,8 @@ struct WarpRun {
   std::vector<int> rkind;             // SM issue model: WAIT_* kind of each register's producer
   uint64_t peek_e = 0;                // SM issue model: scoreboard time of the next instruction
   int peek_kind = WAIT_EXEC;          //                 and what binds it
+  bool labels = false;                // SM issue model: count the divergence label
+  uint64_t diverged = 0;              // instructions issued while some live lane waited on the stack
 
   WarpRun(const Launch& L, uint32_t gw) : X(&L), gwarp(gw) {
     const Kernel& K = *X->K;
@@ -1466,6 +1468,11 @@ struct WarpRun {
         return RUN_PEEK;
       }
       issued = true;
+      if (labels) {  // DIVERGENCE: live lanes (in any stack entry) outside the active mask
+        uint32_t live = 0;
+        for (const Entry& e : stack) live |= e.mask;
+        if (live != top.mask) diverged++;
+      }
 
       // ---- guard ----
       uint32_t exec = 0;
@@ -1766,12 +1773,34 @@ void run_stepped(const Launch& X, Memory& M) {
 // the lowest global warp id, if any (the page's step() order). A warp is ready
 // when its in-order scoreboard lets it issue (peek); it then issues at this
 // cycle (floor). Waits are counted by what the warp waited for.
+//
+// Two labels on issued instructions (they change no timing): MEMORY_THROTTLE,
+// an instruction of the page's memory class (its MEMORY_OPS: ld, st, mov)
+// issued while at least 4 other warps of its SM have a memory operation
+// pending — a warp's pending operation is its latest global or shared load
+// or store, issued at an earlier cycle and not yet complete (a load's result
+// not yet ready, a store not yet drained); and DIVERGENCE, an instruction
+// issued while some of the warp's live lanes wait on the reconvergence stack.
 struct SchedWarp {
   std::unique_ptr<WarpRun> w;
   int state = 0;  // 0 empty, 1 running, 2 waiting, 3 done
   uint64_t start = 0, end = 0, base = 0, arrival = 0;
   uint64_t not_selected = 0, stall[3] = {0, 0, 0}, stall_bar = 0;
+  bool has_mem = false;                  // a global/shared access issued so far
+  uint64_t mem_issue = 0, mem_done = 0;  // the latest one's issue cycle and completion
+  bool has_prev = false;                 // the one before it (a warp issues once a cycle, so
+  uint64_t prev_done = 0;                // the latest access before a cycle is one of the two)
+  uint64_t throttled = 0;
+  bool pending_at(uint64_t cycle) const {  // its latest access issued before `cycle` is incomplete
+    if (!has_mem) return false;
+    if (mem_issue < cycle) return mem_done > cycle;
+    return has_prev && prev_done > cycle;
+  }
 };
+
+bool page_memory_class(const Inst& in) {  // the page's MEMORY_OPS within the subset
+  return in.k == K_LDP || in.k == K_LDG || in.k == K_LDS || in.k == K_STG || in.k == K_STS || in.k == K_MOV;
+}
 
 void run_sm_model(const Launch& X, Memory& M, uint32_t n_sm, uint32_t ctas_per_sm, uint32_t schedulers,
                   uint8_t* warps_out, uint8_t* sms_out) {
@@ -1786,10 +1815,10 @@ void run_sm_model(const Launch& X, Memory& M, uint32_t n_sm, uint32_t ctas_per_s
     auto finish = [&](SchedWarp& q) {
       q.state = DONE;
       q.end = q.w->st.warp_insts ? std::max(std::max(q.w->t_last + 1, q.w->max_ready), q.w->drain) : q.start;
-      uint8_t* r = warps_out + (uint64_t)q.w->gwarp * 64;
-      const uint64_t v[8] = {q.start, q.end, q.w->st.warp_insts, q.not_selected, q.stall[WAIT_EXEC],
-                             q.stall[WAIT_MEM], q.stall[WAIT_MATH], q.stall_bar};
-      for (int i = 0; i < 8; i++) store_le(r + 8 * i, v[i], 8);
+      uint8_t* r = warps_out + (uint64_t)q.w->gwarp * 80;
+      const uint64_t v[10] = {q.start, q.end, q.w->st.warp_insts, q.not_selected, q.stall[WAIT_EXEC],
+                              q.stall[WAIT_MEM], q.stall[WAIT_MATH], q.stall_bar, q.throttled, q.w->diverged};
+      for (int i = 0; i < 10; i++) store_le(r + 8 * i, v[i], 8);
       q.w->write_back();  // statistics (cycles there are this model's absolute end)
       sm_end = std::max(sm_end, q.end);
       sm_issued += q.w->st.warp_insts;
@@ -1807,6 +1836,7 @@ void run_sm_model(const Launch& X, Memory& M, uint32_t n_sm, uint32_t ctas_per_s
       for (uint32_t i = 0; i < wpc; i++) {
         SchedWarp& q = slot[c * wpc + i];
         q.w.reset(new WarpRun(X, (uint32_t)cta * wpc + i));
+        q.w->labels = true;
         q.w->t_next = t0;
         q.start = q.base = t0;
         q.state = RUNNING;
@@ -1865,6 +1895,21 @@ void run_sm_model(const Launch& X, Memory& M, uint32_t n_sm, uint32_t ctas_per_s
         const uint32_t c = (uint32_t)((&q - slot.data()) / wpc);
         q.not_selected += cycle - q.w->peek_e;
         if (q.w->peek_e > q.base) q.stall[q.w->peek_kind] += q.w->peek_e - q.base;
+        // the instruction about to issue (the peek stopped at it)
+        const Inst& nx = K.code[(size_t)q.w->stack.back().pc];
+        if (page_memory_class(nx)) {  // MEMORY_THROTTLE label
+          uint32_t pending = 0;
+          for (const SchedWarp& o : slot)
+            if (&o != &q && o.state != EMPTY && o.pending_at(cycle)) pending++;
+          if (pending >= 4) q.throttled++;
+        }
+        if (nx.k == K_LDG || nx.k == K_STG || nx.k == K_LDS || nx.k == K_STS) {  // issues at `cycle`
+          q.has_prev = q.has_mem;
+          q.prev_done = q.mem_done;
+          q.has_mem = true;
+          q.mem_issue = cycle;
+          q.mem_done = cycle + X.cfg->lat[nx.cls];
+        }
         q.w->floor = cycle;
         uint64_t arr = 0;
         const int r = q.w->run(M, smem[c].get(), &arr, true);

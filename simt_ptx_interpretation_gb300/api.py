@@ -28,7 +28,7 @@ ST_CACHE_LOG, ST_CACHE_STREAM, ST_SCHED_LIMIT = 7, 8, 9
 # SM issue model records (include/ks.h)
 SCHED_WARP_DTYPE = np.dtype([("start", "<u8"), ("end", "<u8"), ("issued", "<u8"), ("not_selected", "<u8"),
                              ("stall_exec", "<u8"), ("stall_mem", "<u8"), ("stall_math", "<u8"),
-                             ("stall_barrier", "<u8")])
+                             ("stall_barrier", "<u8"), ("throttled", "<u8"), ("diverged", "<u8")])
 SCHED_SM_DTYPE = np.dtype([("cycles", "<u8"), ("issued", "<u8"), ("ctas", "<u8"), ("status", "<i4"),
                            ("reserved", "<u4")])
 
@@ -407,7 +407,7 @@ def simulate_sched(module: Module, kernel: str, grid: int, block: int, params: b
                    trace: torch.Tensor | None = None, config: Config | None = None,
                    sched: SchedConfig | None = None, stream=None) -> None:
     """ks_simulate_sched: simulate() plus the SM issue model; sched_warps /
-    sched_sms / workspace are uint8 cuda tensors (64 B per warp, 32 B per SM,
+    sched_sms / workspace are uint8 cuda tensors (80 B per warp, 32 B per SM,
     sched_workspace_bytes)."""
     bufs = (_native.KsBuffer * max(1, len(buffers)))()
     for i, (base, t) in enumerate(buffers):
@@ -537,7 +537,7 @@ def run(module: Module, kernel: str, grid: int, block: int, params: bytes, buffe
     if cache is not None and sched is not None:
         raise ValueError("the cache model and the SM issue model run separately")
     if sched is not None:
-        sw = torch.empty(n * 64, dtype=torch.uint8, device=dev)
+        sw = torch.empty(n * SCHED_WARP_DTYPE.itemsize, dtype=torch.uint8, device=dev)
         ss = torch.empty(sched.n_sm * 32, dtype=torch.uint8, device=dev)
         ws = torch.empty(max(1, sched_workspace_bytes(grid, block, sched)), dtype=torch.uint8, device=dev)
         simulate_sched(module, kernel, grid, block, params, buffers, st, sw, ss, ws, tr, config, sched, stream)

@@ -48,6 +48,9 @@ static_assert(OP_SETP_S32 == OP_SETP_U32 + 1 && OP_SETP_U64 == OP_SETP_U32 + 2 &
 // shared address form in KsInsn::flags of OP_LDS* / OP_STS*: a register base
 // (KS_SHA_REG, 64-bit with KS_SHA_WIDE) plus KsInsn::imm, or imm alone
 constexpr uint8_t KS_SHA_REG = 1, KS_SHA_WIDE = 2;
+// KsInsn::flags of OP_MOV32 / OP_MOV64 / OP_MOVSP: written with the `mov`
+// opcode (an integer cvt of one width decodes to a move as well)
+constexpr uint8_t KS_MOV_OPCODE = 0x80;
 // setp comparison in KsInsn::flags
 enum Cmp : uint8_t { CMP_EQ = 0, CMP_NE, CMP_LT, CMP_LE, CMP_GT, CMP_GE };
 // cvt float->int destination (low nibble) and rounding (high nibble)
@@ -139,6 +142,14 @@ constexpr uint32_t INC_ADDR64 = 32u;
 // predicate; aux bit 16 = that guard's negation, aux bits 17..31 = the bra's
 // target, so a uniform outcome issues the bra in the same step
 constexpr uint32_t INC_FUSE = 64u;
+// SM issue model labels: INC_MCLASS, an instruction of the page's memory
+// class (ld, st, mov); INC_MEMOP, a global or shared load or store (a memory
+// operation that stays pending until it completes)
+constexpr uint32_t INC_MCLASS = 128u, INC_MEMOP = 256u;
+// bit 15 of an issue-run log record: the run issued while some live lanes
+// waited on the reconvergence stack (the divergence label); bits 0..14 hold
+// its length - 1, bits 16..31 its first program entry
+constexpr uint32_t RUN_DIVERGED = 1u << 15;
 // bits 16..31 of DevInsn::inc of a fast-path op: the number of consecutive
 // fast-path ops starting at it (a run's length, at most KS_MAX_INSNS)
 constexpr uint32_t INC_RUN_SHIFT = 16u;

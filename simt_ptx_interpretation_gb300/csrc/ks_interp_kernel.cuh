@@ -322,8 +322,11 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
     uint32_t c_k = 0, c_l1 = 0, c_l2 = 0, c_n = 0;
     uint64_t c_off = 0;
     // SM issue model: the run of consecutive program entries being consumed
-    // [run_start, run_next) and the runs logged so far
+    // [run_start, run_next) and the runs logged so far; `live` = the lanes
+    // that have not executed ret, and run_div whether the run issues while
+    // some of them wait on the stack (mask != live, the divergence label)
     uint32_t run_start = 0, run_next = 0, n_runs = 0;
+    [[maybe_unused]] uint32_t live = mask, run_div = 0;
     if constexpr (INSTR) {
       if (L.cache_pass == 2) {
         c_n = L.cache_warps[gw].n_access;
@@ -366,13 +369,16 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       // instructions that may run before the reconvergence pc or the end of the
       // step budget.
       if constexpr (RUNLOG) {
-        if (pc != run_next) {  // a new run: log the one that ended
+        const uint32_t div = mask != live ? RUN_DIVERGED : 0u;
+        if (pc != run_next || div != run_div) {  // a new run: log the one that ended
           if (run_next != run_start) {
             if (lane == 0 && n_runs < L.sched_cap)
-              L.sched_log[(uint64_t)gw * L.sched_cap + n_runs] = (run_start << 16) | (run_next - run_start - 1u);
+              L.sched_log[(uint64_t)gw * L.sched_cap + n_runs] =
+                  (run_start << 16) | run_div | (run_next - run_start - 1u);
             n_runs++;
           }
           run_start = run_next = pc;
+          run_div = div;
         }
       }
       const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
@@ -916,6 +922,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             SM64(at) = SM64(at) & ~((uint64_t)exec << 32);
           }
           mask &= ~exec;
+          if constexpr (RUNLOG) live &= ~exec;
           pc++;
           break;
         }
@@ -1152,7 +1159,8 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       if constexpr (RUNLOG) {  // the last run, and the count
         if (run_next != run_start) {
           if (lane == 0 && n_runs < L.sched_cap)
-            L.sched_log[(uint64_t)gw * L.sched_cap + n_runs] = (run_start << 16) | (run_next - run_start - 1u);
+            L.sched_log[(uint64_t)gw * L.sched_cap + n_runs] =
+                (run_start << 16) | run_div | (run_next - run_start - 1u);
           n_runs++;
         }
         if (lane == 0) L.sched_runs[gw] = n_runs;

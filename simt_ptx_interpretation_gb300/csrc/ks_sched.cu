@@ -54,14 +54,23 @@ struct alignas(16) Rec {
   uint4 q;
   uint4 lat;
 };
-constexpr uint32_t F_ISSUE = 1, F_RDEST = 2, F_PDEST = 4, F_PHAZ = 8, F_BAR = 16;
+constexpr uint32_t F_ISSUE = 1, F_RDEST = 2, F_PDEST = 4, F_PHAZ = 8, F_BAR = 16, F_MCLASS = 32, F_MEMOP = 64;
 
 struct Lane {
   uint32_t state, gw, cta_slot;
   uint32_t pc, run_left, k, n_runs;  // next entry to issue; entries left in its run; next run index
   uint32_t t_next, t_last, max_ready, drain, base, start, e, bind, arrival, end;
   Rec r;                             // the record of the next entry
+  uint32_t div;                      // the run of the next entry issues diverged (RUN_DIVERGED)
   uint32_t issued, not_selected, st_exec, st_mem, st_math, stall_bar;  // each below the 2^31 clock limit
+  uint32_t throttled, diverged;      // the two labels (instructions)
+  // the latest global / shared access (issue cycle, completion) and the one
+  // before it: at cycle T the pending one is the latest issued before T
+  uint32_t mem_at, mem_done, prev_done;
+  bool has_mem, has_prev;
+  __device__ __forceinline__ bool mem_pending(uint32_t T) const {
+    return has_mem && (mem_at < T ? mem_done > T : (has_prev && prev_done > T));
+  }
 };
 
 // ready table entry: ready time | kind of the producer << 32; the kind of a
@@ -90,6 +99,8 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     if (d.inc & INC_PDEST) flags |= F_PDEST;
     if (d.inc & INC_PHAZ) flags |= F_PHAZ;
     if (d.op == OP_BAR) flags |= F_BAR;
+    if (d.inc & INC_MCLASS) flags |= F_MCLASS;
+    if (d.inc & INC_MEMOP) flags |= F_MEMOP;
     auto pred = [&](uint32_t off) { return (off - S.pred_off) / 4u; };
     Rec r;
     r.q.x = (d.a / ROW_BYTES) | ((d.b / ROW_BYTES) << 16);
@@ -112,6 +123,8 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
   Lane L;
   L.state = ST_EMPTY;
   L.cta_slot = lane / S.wpc;
+  L.has_mem = L.has_prev = false;
+  L.mem_at = L.mem_done = L.prev_done = 0;
   uint32_t port = 0;  // next free cycle of my scheduler
   uint32_t next_cta_k = 0;
   uint32_t status = 0;
@@ -130,7 +143,8 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
         if (L.k >= L.n_runs) return false;
         const uint32_t r = S.log[(uint64_t)L.gw * S.cap + L.k++];
         L.pc = r >> 16;
-        L.run_left = (r & 0xFFFFu) + 1u;
+        L.run_left = (r & (RUN_DIVERGED - 1u)) + 1u;
+        L.div = r & RUN_DIVERGED;
       }
       L.r = prog[L.pc];
       if ((L.r.q.w >> 8) & F_ISSUE) return true;
@@ -173,6 +187,8 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     r.stall_mem = L.st_mem;
     r.stall_math = L.st_math;
     r.stall_barrier = L.stall_bar;
+    r.throttled = L.throttled;
+    r.diverged = L.diverged;
     S.warps_out[L.gw] = r;
     sm_end = max(sm_end, L.end);
     sm_issued += L.issued;
@@ -197,6 +213,10 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     L.max_ready = L.drain = 0u;
     L.issued = L.not_selected = L.stall_bar = 0;
     L.st_exec = L.st_mem = L.st_math = 0;
+    L.throttled = L.diverged = 0;
+    L.has_mem = L.has_prev = false;
+    L.mem_at = L.mem_done = L.prev_done = 0;
+    L.div = 0;
     if (L.n_runs > S.cap) {
       status = KS_ST_SCHED_LIMIT;
       L.n_runs = 0;
@@ -271,6 +291,9 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
       gmin = my_sched == 0u ? m0 : my_sched == 1u ? m1 : my_sched == 2u ? m2 : m3;
     }
     const bool win = at_T && L.gw == gmin;
+    // warps of this SM with a memory operation pending at T (issued earlier,
+    // not yet complete), for the memory-throttle label
+    const uint32_t pending = __ballot_sync(FULL, lane < slots && L.state != ST_EMPTY && L.mem_pending(T));
     uint32_t ev = 0;  // arrived at a barrier or finished
     if (win) {
       L.not_selected += T - L.e;
@@ -292,6 +315,15 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
       L.t_next = T + lt.z;
       L.base = T + 1u;
       L.issued++;
+      if ((flags & F_MCLASS) && __popc(pending & ~(1u << lane)) >= 4) L.throttled++;
+      if (flags & F_MEMOP) {
+        L.has_prev = L.has_mem;
+        L.prev_done = L.mem_done;
+        L.has_mem = true;
+        L.mem_at = T;
+        L.mem_done = T + max(lt.x, lt.y);  // a load's result, a store's drain
+      }
+      if (L.div) L.diverged++;
       const bool more = advance(true);
       if (flags & F_BAR) {
         L.state = ST_WAITING;

@@ -33,7 +33,7 @@ def check(ptx, kernel, grid, block, params, buffers, n_sm, ctas_per_sm=0, schedu
     obufs = [(base, np.ascontiguousarray(a).copy()) for base, a in buffers]
     ow, osm = oracle.run_sched(ptx, kernel, grid, block, params, obufs, n_sm=n_sm, ctas_per_sm=ctas_per_sm,
                                schedulers=schedulers)
-    bad = np.nonzero(r.sched_warps.view(np.uint8).reshape(-1, 64) != ow.view(np.uint8).reshape(-1, 64))[0]
+    bad = np.nonzero(r.sched_warps.view(np.uint8).reshape(-1, 80) != ow.view(np.uint8).reshape(-1, 80))[0]
     assert len(bad) == 0, f"schedule differs at warps {np.unique(bad)[:5]}: gpu {r.sched_warps[bad[0]]} oracle {ow[bad[0]]}"
     assert np.array_equal(r.sched_sms.view(np.uint8), osm.view(np.uint8)), f"SM records differ: {r.sched_sms} {osm}"
     for (_, g), (_, o) in zip(dev, obufs):

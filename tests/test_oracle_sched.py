@@ -39,7 +39,14 @@ def sched(ptx, grid, block, **kw):
 
 
 def rows(ws):
-    return [tuple(int(x) for x in r) for r in ws]
+    """(start, end, issued, not_selected, exec, mem, math, barrier) per warp."""
+    return [tuple(int(r[k]) for k in ("start", "end", "issued", "not_selected", "stall_exec", "stall_mem",
+                                       "stall_math", "stall_barrier")) for r in ws]
+
+
+def labels(ws):
+    """(throttled, diverged) per warp: the two label counts."""
+    return [(int(r["throttled"]), int(r["diverged"])) for r in ws]
 
 
 @pytest.mark.parametrize("k", [1, 2, 3, 4])
@@ -203,3 +210,135 @@ def test_warp_sweep_shape():
     assert i1s == i128
     ipc_one, ipc_four = i32 / c32, i1s / c1s
     assert ipc_one < ipc_four <= 1.0
+
+
+# ---------------------------------------------------------------- labels ----
+# The page's _determine_stall_reason labels an instruction as it executes:
+# MEMORY_THROTTLE for an instruction of its memory class (MEMORY_OPS: ld, st,
+# mov) while 4 or more memory operations are pending; DIVERGENCE is declared
+# and returned nowhere. Readings: pending per SM, other warps' latest global
+# or shared access issued at an earlier cycle and not yet complete; diverged
+# while live lanes wait on the reconvergence stack. Labels change no timing.
+
+THROTTLE = wl.HEADER + """.visible .entry k(.param .u64 p_in)
+{
+    .reg .b32 %r<3>;
+    .reg .b64 %rd<3>;
+    ld.param.u64    %rd1, [p_in];
+    ld.global.u32   %r1, [%rd1];
+    ret;
+}
+"""
+
+
+@pytest.mark.parametrize("warps", [4, 5, 6])
+def test_memory_throttle_label(warps):
+    """One SM, one scheduler, warps 0..n-1 from cycle 0, lowest id first.
+    ld.param of w0..w3 at 0..3 (each load waits 4 on its ld.param); then
+    w0 ld.global 4, ret 5; w1 ld.global 6, ret 7; w2 8, 9; w3 10, 11 (a load
+    sees 0, 1, 2, 3 other pending loads: none throttled); w4 ld.param 12 and
+    w5 ld.param 13 see w0..w3 pending (4): throttled; w4 ld.global 16 sees 4
+    (w5 has no access yet): throttled, ret 17; w5 ld.global 18 sees 5:
+    throttled. ret (not memory class) is never labelled. A load's warp ends
+    when its result is ready, 400 cycles after it issued."""
+    src = np.arange(32 * warps, dtype=np.uint32)
+    ws, _ = oracle.run_sched(THROTTLE, "k", 1, 32 * warps, (0x1000_0000).to_bytes(8, "little"),
+                             [(0x1000_0000, src)], n_sm=1, schedulers=1)
+    ldg = [4, 6, 8, 10, 16, 18][:warps]
+    assert [r[1] for r in rows(ws)] == [t + 400 for t in ldg]
+    expect = [0, 0, 0, 0, 2, 2][:warps]
+    assert [t for t, _ in labels(ws)] == expect
+    assert all(d == 0 for _, d in labels(ws))
+
+
+IF_ELSE = wl.HEADER + """.visible .entry k()
+{
+    .reg .pred %p<2>;
+    .reg .b32 %r<4>;
+    mov.u32         %r1, %tid.x;
+    setp.lt.u32     %p1, %r1, 16;
+    @%p1 bra        THEN;
+    add.u32         %r2, %r1, 1;
+    add.u32         %r2, %r2, 1;
+    bra             JOIN;
+THEN:
+    add.u32         %r2, %r1, 2;
+JOIN:
+    add.u32         %r3, %r2, 1;
+    ret;
+}
+"""
+
+
+def test_divergence_label_if_else():
+    """Warp 0 splits at the branch: the fall-through path (lanes 16..31: two
+    adds and the bra to JOIN) and the taken path (lanes 0..15: one add) issue
+    while the other half waits at JOIN: 4 diverged instructions of 9. Warp 1
+    (tid 32..63) goes one way: none. mov and the adds are not memory class
+    except mov, which issues with nothing pending."""
+    ws, _ = sched(IF_ELSE, 1, 64, n_sm=1, schedulers=4)
+    assert [int(r["issued"]) for r in ws] == [9, 8]
+    assert labels(ws) == [(0, 4), (0, 0)]
+
+
+RET_IN_PATH = wl.HEADER + """.visible .entry k()
+{
+    .reg .pred %p<2>;
+    .reg .b32 %r<4>;
+    mov.u32         %r1, %tid.x;
+    setp.lt.u32     %p1, %r1, 8;
+    @%p1 bra        OUT;
+    add.u32         %r2, %r1, 1;
+    ret;
+OUT:
+    add.u32         %r3, %r1, 2;
+    ret;
+}
+"""
+
+
+def test_divergence_label_ends_when_the_other_path_exits():
+    """The paths end in different rets (reconvergence at the virtual exit).
+    Lanes 8..31 run first: add and ret issue while lanes 0..7 wait (2
+    diverged); after that ret those lanes have left, so lanes 0..7 are all the
+    live lanes and their add and ret are not diverged."""
+    ws, _ = sched(RET_IN_PATH, 1, 32, n_sm=1, schedulers=1)
+    assert int(ws[0]["issued"]) == 7
+    assert labels(ws) == [(0, 2)]
+
+
+THROTTLE2 = wl.HEADER + """.visible .entry k(.param .u64 p_in)
+{
+    .reg .b32 %r<3>;
+    .reg .b64 %rd<3>;
+    ld.param.u64    %rd1, [p_in];
+    ld.global.u32   %r1, [%rd1];
+    ld.global.u32   %r2, [%rd1+4];
+    ret;
+}
+"""
+
+
+def test_memory_throttle_counts_other_warps_only():
+    """Two loads per warp, four warps: ld.param 0..3; w0 loads at 4 and 5, ret
+    6; w1 at 7 and 8, ret 9; w2 at 10 and 11, ret 12; w3 at 13 and 14, ret 15.
+    w3's second load finds three other warps pending and its own first load:
+    the warp's own access does not count, so nothing is throttled."""
+    src = np.arange(256, dtype=np.uint32)
+    ws, _ = oracle.run_sched(THROTTLE2, "k", 1, 128, (0x1000_0000).to_bytes(8, "little"),
+                             [(0x1000_0000, src)], n_sm=1, schedulers=1)
+    assert [r[1] for r in rows(ws)] == [405, 408, 411, 414]
+    assert labels(ws) == [(0, 0)] * 4
+
+
+def test_divergence_label_on_the_divergent_workload():
+    """The divergent workload splits at its lane % k test on every iteration:
+    labels appear and never exceed the issued instructions."""
+    w = wl.divergent(4, n=1024)
+    bufs = w.fresh_buffers()
+    ws, _ = oracle.run_sched(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in bufs],
+                             n_sm=2, schedulers=4)
+    assert int(ws["diverged"].sum()) > 0
+    for r in ws:
+        assert int(r["diverged"]) <= int(r["issued"])
+        assert int(r["throttled"]) <= int(r["issued"])
