@@ -22,7 +22,9 @@
 // warp's region holding one (value, ready) pair per lane, so lane l reads an
 // operand and its scoreboard entry with one 8-byte shared load at
 // (region + offset + 8l): registers, constants (replicated across the row) and
-// "no operand" (the zero row) look the same.
+// "no operand" (the zero row) look the same. A destination's ready time
+// alone (the write-after-write wait) is read from lane 0's pair by every
+// lane: one broadcast word instead of a strided load of two wavefronts.
 //
 // Kernels with shared memory or bar.sync run in CTA mode (the CTA template
 // instantiation): one real CTA per simulated CTA, one real warp per simulated
@@ -31,8 +33,10 @@
 //
 // Warp-uniform state (pc, active mask, scoreboard clock, counters) lives in
 // registers, identical in every lane; values every lane must agree on (ready
-// times, stack entries) are written by all lanes with the same value, so each
-// lane only ever reads back its own store. Predicates are per-warp ballot
+// times, stack entries) are written by all lanes with the same value, and the
+// warp's shared-memory accesses complete in program order, so a lane may read
+// any lane's copy (the predicate ready table and a destination's ready time
+// are read as one broadcast word). Predicates are per-warp ballot
 // masks, predicate p held by lane p (lane 31 holds the always-true predicate)
 // and read with a shuffle. The scoreboard clock is 32-bit relative to a 64-bit
 // epoch that moves forward before any clock reaches 2^31.
@@ -453,13 +457,13 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
         uint4 ka = q0, kb = q1;
         uint2 a = SM2(lb + kb.x), b = SM2(lb + kb.y), c = SM2(lb + kb.z);
-        uint32_t rd = SM32(lb + ka.w + 4u);
+        uint32_t rd = SM32(wb + ka.w + 4u);
         // instruction k+1 (the last instruction is never a fast op, so k+1 and
         // k+2 stay within the program and its exit sentinel)
         uint4 na = ip[4], nb = ip[5];
         for (;;) {
           uint2 a1 = SM2(lb + nb.x), b1 = SM2(lb + nb.y), c1 = SM2(lb + nb.z);
-          uint32_t rd1 = SM32(lb + na.w + 4u);
+          uint32_t rd1 = SM32(wb + na.w + 4u);
           const uint4 ma = ip[8], mb = ip[9];
           const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));
           const uint32_t wr = t + ka.y;
@@ -509,7 +513,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         for (;;) {
           const uint4 na = mp[4], nb = mp[5];  // the next record, fetched early
           const uint2 pa = SM2(lb + kb.x), pb = SM2(lb + kb.y), pcc = SM2(lb + kb.z);
-          const uint32_t rd = SM32(lb + ka.w + 4u);
+          const uint32_t rd = SM32(wb + ka.w + 4u);
           const uint32_t t = max(max(t_next, pa.y), max(max(pb.y, pcc.y), rd));
           const uint32_t wr = t + ka.y;
           max_ready = max(max_ready, wr);
@@ -592,7 +596,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       const uint32_t aux = q0.z;
       const uint2 pa = SM2(lb + A), pb = SM2(lb + B), pcc = SM2(lb + C);
       const uint32_t a0 = pa.x, b0 = pb.x, c0 = pcc.x;
-      const uint32_t rd = SM32(lb + D + 4u);
+      const uint32_t rd = SM32(wb + D + 4u);
       uint32_t hmax = 0;
       if (inc & INC_PHAZ)
         hmax = max(max(SM32(wb + q2.z), SM32(wb + q2.w)), max(SM32(wb + q3.x), SM32(wb + q3.y)));
