@@ -133,6 +133,20 @@ extern "C" {
 #define KS_MAX_SHARED_BYTES 49152   /* simulated shared memory per CTA */
 #define KS_MAX_CTA_MODE_BLOCK 1024  /* block limit of kernels with shared memory or bar.sync */
 
+/* ks_config.flags: the layout of each simulated warp's state in the
+ * interpreter's shared memory. With neither flag the library picks: PAIR,
+ * where every register row holds (value, ready time) pairs and one 8-byte
+ * load per lane reads an operand with its scoreboard entry (fewest
+ * instructions per simulated instruction), unless the kernel runs outside
+ * CTA mode and its PAIR warp state exceeds 12 KiB, where SPLIT (value rows
+ * and a separate table of ready times, half the shared memory per warp, so
+ * more simulated warps resident) is taken. Results are identical in both
+ * layouts; only speed differs. Both flags, or SPLIT forced on a kernel with
+ * shared memory or bar.sync (CTA mode runs in PAIR only): KS_ERR_ARG /
+ * KS_ERR_UNSUPPORTED. */
+#define KS_FLAG_LAYOUT_PAIR 1u
+#define KS_FLAG_LAYOUT_SPLIT 2u
+
 typedef struct ks_module ks_module; /* opaque; owned by the library */
 
 /* A simulated global buffer: the caller picks sim_base (4 KiB aligned,
@@ -153,7 +167,7 @@ typedef struct {
   uint64_t step_limit;              /* max issued instructions per warp */
   int64_t inject_warp;              /* debug: global warp id that posts KS_ST_INJECTED; -1 off */
   uint64_t inject_step;             /* ...when its issued-instruction count reaches this */
-  uint32_t flags;                   /* reserved, 0 */
+  uint32_t flags;                   /* 0, or one KS_FLAG_LAYOUT_* (below) */
   uint32_t reserved;
   /* Optional per-instruction profile (device, NULL = none): one
    * ks_pc_profile per program entry, profile_bytes >= ks_profile_bytes();
@@ -264,6 +278,13 @@ int ks_kernel_event(const ks_module* mod, const char* kernel, uint32_t id, uint3
  * (instructions and pseudo-ops in order); the virtual exit is *n_out. */
 int ks_kernel_ipdom(const ks_module* mod, const char* kernel, int32_t* out, uint32_t cap,
                     uint32_t* n_out);
+/* The register-file layout a launch of `kernel` with these ks_config.flags
+ * runs in (*split: 0 PAIR, 1 SPLIT; see KS_FLAG_LAYOUT_*) and the shared
+ * memory each simulated warp's state takes in it (*region_bytes). Errors are
+ * those the launch would return for the flags: KS_ERR_ARG (both flags or
+ * unknown bits), KS_ERR_UNSUPPORTED (SPLIT forced on a CTA-mode kernel). */
+int ks_kernel_layout(const ks_module* mod, const char* kernel, uint32_t flags, uint32_t* split,
+                     uint32_t* region_bytes);
 
 /* Size of the caller-owned trace buffer (CuTeDSL IKET 浅析, §2 "buffer
  * 是怎么定形的" — compute_warp_buffer_size_bytes: one slot per warp of

@@ -50,6 +50,10 @@ def _check(rc: int, msg: str = ""):
         raise KsError(rc, msg)
 
 
+# ks_config.flags values of Config.layout (include/ks.h KS_FLAG_LAYOUT_*)
+LAYOUT_FLAGS = {"auto": 0, "pair": 1, "split": 2}
+
+
 @dataclass
 class Config:
     lat: tuple = DEFAULT_LAT
@@ -59,6 +63,9 @@ class Config:
     inject_warp: int = -1
     inject_step: int = 0
     profile: torch.Tensor | None = None  # uint8 cuda tensor of Module.profile_bytes(kernel), or None
+    # register-file layout of the interpreter: "auto" (the library picks),
+    # "pair" or "split" (KS_FLAG_LAYOUT_*); results are identical, speed differs
+    layout: str = "auto"
 
     def to_c(self) -> _native.KsConfig:
         c = _native.KsConfig()
@@ -70,6 +77,7 @@ class Config:
         c.step_limit = self.step_limit
         c.inject_warp = self.inject_warp
         c.inject_step = self.inject_step
+        c.flags = LAYOUT_FLAGS[self.layout]
         if self.profile is not None:
             c.profile_buf = self.profile.data_ptr()
             c.profile_bytes = self.profile.numel() * self.profile.element_size()
@@ -169,6 +177,14 @@ class Module:
         cnt = ctypes.c_uint32()
         _check(_native.lib().ks_kernel_ipdom(self._h, kernel.encode(), arr, n, ctypes.byref(cnt)))
         return [arr[i] for i in range(cnt.value)]
+
+    def layout(self, kernel: str, layout: str = "auto") -> tuple[str, int]:
+        """The register-file layout a launch with Config(layout=layout) runs
+        in ("pair" or "split") and the shared memory per simulated warp."""
+        split, region = ctypes.c_uint32(), ctypes.c_uint32()
+        _check(_native.lib().ks_kernel_layout(self._h, kernel.encode(), LAYOUT_FLAGS[layout], ctypes.byref(split),
+                                              ctypes.byref(region)))
+        return ("split" if split.value else "pair"), int(region.value)
 
 
 def stats_bytes(grid: int, block: int) -> int:

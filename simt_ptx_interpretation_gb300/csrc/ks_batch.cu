@@ -8,7 +8,8 @@
 // runs its item exactly as a single launch would run it on a grid of that
 // range's size (ks_interp_kernel.cuh, NB = KS_BATCH_ITEMS), so results do
 // not depend on the batching. The items of one real grid share the kernel
-// instantiation: the same mode and form, and in CTA mode the same block.
+// instantiation: the same mode, form and layout, and in CTA mode the same
+// block.
 
 #include "ks_interp_kernel.cuh"
 
@@ -25,7 +26,8 @@ const void* batch_fn_of(int form) {
                      : (const void*)ks_interp_kernel<CTA, BIG, true, true, NB>;
 }
 
-const void* batch_fn(bool cta, uint32_t real_warps_per_cta, int form) {
+const void* batch_fn(bool cta, uint32_t real_warps_per_cta, int form, bool split) {
+  if (split) return batch_fn_split(form);  // plain mode only
   if (!cta) return batch_fn_of<false, false>(form);
   if (real_warps_per_cta > 8) return batch_fn_of<true, true>(form);
   return batch_fn_of<true, false>(form);
@@ -41,20 +43,24 @@ int ensure_batch_attr() {
   int mx = 0;
   e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return (int)e;
-  for (int cta = 0; cta < 2; cta++)
-    for (int big = 0; big < 2; big++)
-      for (int form = 0; form < 3; form++) {
-        if (!cta && big) continue;
-        e = cudaFuncSetAttribute(batch_fn(cta, big ? 32u : 1u, form), cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-        if (e != cudaSuccess) return (int)e;
-      }
+  for (int split = 0; split < 2; split++)
+    for (int cta = 0; cta < 2; cta++)
+      for (int big = 0; big < 2; big++)
+        for (int form = 0; form < 3; form++) {
+          if (!cta && big) continue;
+          if (split && cta) continue;
+          e = cudaFuncSetAttribute(batch_fn(cta, big ? 32u : 1u, form, split),
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+          if (e != cudaSuccess) return (int)e;
+        }
   if (dev < 64) g_batch_attr_done[dev] = 1;
   return 0;
 }
 
-int occupancy(bool cta, uint32_t w, int form, size_t smem, int* per_sm) {
+int occupancy(bool cta, uint32_t w, int form, bool split, size_t smem, int* per_sm) {
   *per_sm = 0;
-  return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, batch_fn(cta, w, form), (int)(w * 32u), smem);
+  return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, batch_fn(cta, w, form, split), (int)(w * 32u),
+                                                            smem);
 }
 
 // Shared memory of a real CTA of w warps that may run any item.
@@ -75,9 +81,12 @@ int launch_batch(KsGrid<NB>* Gp, int sms, int max_smem, void* stream) {
   const KsLaunch& L0 = G.item[0];
   const bool cta = L0.cta_mode != 0;
   const int form = interp_form(L0);
+  const bool split = L0.layout.split != 0;
   for (uint32_t i = 1; i < G.n; i++) {
     const KsLaunch& L = G.item[i];
-    if ((L.cta_mode != 0) != cta || interp_form(L) != form || (cta && L.wpc != L0.wpc)) return KS_ERR_ARG;
+    if ((L.cta_mode != 0) != cta || interp_form(L) != form || (L.layout.split != 0) != split ||
+        (cta && L.wpc != L0.wpc))
+      return KS_ERR_ARG;
   }
   int e = ensure_batch_attr();
   if (e) return KS_ERR_CUDA;
@@ -93,7 +102,7 @@ int launch_batch(KsGrid<NB>* Gp, int sms, int max_smem, void* stream) {
     smem = batch_smem(G, w);
     if (smem > (size_t)max_smem) return KS_ERR_LIMIT;
     int per_sm = 0;
-    if (occupancy(true, w, form, smem, &per_sm)) return KS_ERR_CUDA;
+    if (occupancy(true, w, form, split, smem, &per_sm)) return KS_ERR_CUDA;
     if (per_sm < 1) return KS_ERR_LIMIT;
     for (uint32_t i = 0; i < G.n; i++) total += units[i] = useful[i] = G.item[i].grid;
     ctas = std::min<uint64_t>(total, (uint64_t)sms * (uint64_t)per_sm);
@@ -109,7 +118,7 @@ int launch_batch(KsGrid<NB>* Gp, int sms, int max_smem, void* stream) {
       const size_t s = batch_smem(G, wk);
       int per_sm = 0;
       if (s <= (size_t)max_smem) {
-        if (occupancy(false, wk, form, s, &per_sm)) return KS_ERR_CUDA;
+        if (occupancy(false, wk, form, split, s, &per_sm)) return KS_ERR_CUDA;
         if ((uint64_t)per_sm >= k) {
           w = wk;
           smem = s;
@@ -125,7 +134,7 @@ int launch_batch(KsGrid<NB>* Gp, int sms, int max_smem, void* stream) {
         const size_t s = batch_smem(G, c);
         if (s > (size_t)max_smem) break;
         int per_sm = 0;
-        if (occupancy(false, c, form, s, &per_sm)) return KS_ERR_CUDA;
+        if (occupancy(false, c, form, split, s, &per_sm)) return KS_ERR_CUDA;
         if (per_sm < 1) continue;
         const uint64_t cap = (uint64_t)sms * (uint64_t)per_sm;
         const uint64_t res = std::min<uint64_t>(total, cap * c);
@@ -163,7 +172,7 @@ int launch_batch(KsGrid<NB>* Gp, int sms, int max_smem, void* stream) {
   G.cta_begin[0] = 0;
   for (uint32_t i = 0; i < G.n; i++) G.cta_begin[i + 1] = G.cta_begin[i] + (uint32_t)alloc[i];
   void* args[] = {Gp};
-  return cudaLaunchKernel(batch_fn(cta, w, form), dim3(G.cta_begin[G.n]), dim3(w * 32u), args, smem,
+  return cudaLaunchKernel(batch_fn(cta, w, form, split), dim3(G.cta_begin[G.n]), dim3(w * 32u), args, smem,
                           (cudaStream_t)stream) == cudaSuccess
              ? KS_OK
              : KS_ERR_CUDA;

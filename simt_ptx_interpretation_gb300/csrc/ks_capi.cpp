@@ -12,6 +12,7 @@
 #include <memory>
 #include <mutex>
 #include <string>
+#include <tuple>
 #include <vector>
 
 #include "ks_internal.h"
@@ -19,7 +20,7 @@
 struct ks_module {
   std::vector<ks::KsKernel> kernels;
   std::mutex mu;
-  std::map<std::pair<size_t, int>, void*> images;  // (kernel index, device) -> device copy
+  std::map<std::tuple<size_t, int, int>, void*> images;  // (kernel index, device, layout) -> device copy
 };
 
 namespace {
@@ -77,6 +78,14 @@ uint64_t warps_of(uint32_t grid, uint32_t block) { return (uint64_t)grid * ((blo
 
 namespace ks {
 const KsKernel* module_kernel(const ks_module* mod, const char* name) { return find_kernel(mod, name, nullptr); }
+
+int pick_layout(const KsKernel& k, uint32_t flags) {
+  const bool pair = (flags & KS_FLAG_LAYOUT_PAIR) != 0, split = (flags & KS_FLAG_LAYOUT_SPLIT) != 0;
+  if ((flags & ~(KS_FLAG_LAYOUT_PAIR | KS_FLAG_LAYOUT_SPLIT)) != 0 || (pair && split)) return KS_ERR_ARG;
+  if (split) return k.cta_mode() ? KS_ERR_UNSUPPORTED : 1;
+  if (pair) return 0;
+  return (!k.cta_mode() && k.layout[0].region_bytes > SPLIT_REGION_MIN) ? 1 : 0;
+}
 }  // namespace ks
 
 extern "C" {
@@ -118,7 +127,7 @@ void ks_free_module(ks_module* mod) {
   int cur = -1;
   cudaGetDevice(&cur);
   for (auto& kv : mod->images) {
-    cudaSetDevice(kv.first.second);
+    cudaSetDevice(std::get<1>(kv.first));
     cudaFree(kv.second);
   }
   if (cur >= 0 && !mod->images.empty()) cudaSetDevice(cur);
@@ -163,6 +172,17 @@ int ks_kernel_ipdom(const ks_module* mod, const char* kernel, int32_t* out, uint
   if (n_out) *n_out = (uint32_t)k->ipdom.size();
   if (out)
     for (size_t i = 0; i < k->ipdom.size() && i < cap; i++) out[i] = k->ipdom[i];
+  return KS_OK;
+}
+
+int ks_kernel_layout(const ks_module* mod, const char* kernel, uint32_t flags, uint32_t* split,
+                     uint32_t* region_bytes) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  const int lay = ks::pick_layout(*k, flags);
+  if (lay < 0) return lay;
+  if (split) *split = (uint32_t)lay;
+  if (region_bytes) *region_bytes = k->layout[lay].region_bytes;
   return KS_OK;
 }
 
@@ -241,21 +261,24 @@ int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t 
   // shared memory / bar.sync: every warp of a CTA resident on one real CTA
   if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
   if (cfg.profile_buf && cfg.profile_bytes < k->code.size() * sizeof(ks_pc_profile)) return KS_ERR_ARG;
+  const int lay = ks::pick_layout(*k, cfg.flags);
+  if (lay < 0) return lay;
 
   if (host_checks_only) return KS_OK;
   DevInfo& di = *dip;
   int dev = 0;
   if (device_info(&di, &dev) != KS_OK) return KS_ERR_CUDA;
 
-  // ---- program image on this device (uploaded once) ----
+  // ---- program image of the chosen layout on this device (uploaded once) ----
+  const std::vector<uint8_t>& img = k->image[lay];
   void* image = nullptr;
   {
     std::lock_guard<std::mutex> lk(mod->mu);
-    auto key = std::make_pair(kidx, dev);
+    auto key = std::make_tuple(kidx, dev, lay);
     auto it = mod->images.find(key);
     if (it == mod->images.end()) {
-      if (cudaMalloc(&image, k->image.size()) != cudaSuccess) return KS_ERR_CUDA;
-      if (cudaMemcpy(image, k->image.data(), k->image.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+      if (cudaMalloc(&image, img.size()) != cudaSuccess) return KS_ERR_CUDA;
+      if (cudaMemcpy(image, img.data(), img.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
         cudaFree(image);
         return KS_ERR_CUDA;
       }
@@ -269,12 +292,12 @@ int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t 
   ks::KsLaunch& L = *Lp;
   std::memset(&L, 0, sizeof L);
   L.image = static_cast<const uint8_t*>(image);
-  L.image_bytes = (uint32_t)k->image.size();
+  L.image_bytes = (uint32_t)img.size();
   L.prog_bytes = k->prog_bytes;
   L.n_insn = (uint32_t)k->code.size();
   L.n_slots = k->n_slots;
-  L.n_crows = k->layout.n_crows;
-  L.layout = k->layout;
+  L.n_crows = k->layout[lay].n_crows;
+  L.layout = k->layout[lay];
   L.grid = grid;
   L.block = block;
   L.wpc = (block + 31u) / 32u;
@@ -368,7 +391,7 @@ void cache_first_pass(ks::KsLaunch* L, const ks_cache_config& cc, uint8_t* ws, c
 }
 
 // Launches prepared simulations as real grids of one instantiation each (mode,
-// form, and in CTA mode the block), in the order of their first items, at
+// form, layout, and in CTA mode the block), in the order of their first items, at
 // most KS_BATCH_ITEMS and at most BATCH_WARPS_PER_SM simulated warps per SM
 // of them, so that a grid runs as one wave and ends with its slowest warp
 // (items are not weighted by their unknown cost per warp). An item larger
@@ -378,7 +401,8 @@ int launch_items(const std::vector<ks::KsLaunch>& Ls, const DevInfo& di, void* s
   constexpr uint64_t BATCH_WARPS_PER_SM = 16;
   const uint64_t budget = BATCH_WARPS_PER_SM * (uint64_t)std::max(di.sms, 1);
   auto key = [](const ks::KsLaunch& L) {
-    return ((uint64_t)L.cta_mode << 40) | ((uint64_t)ks::interp_form(L) << 32) | (L.cta_mode ? L.wpc : 0u);
+    return ((uint64_t)L.cta_mode << 40) | ((uint64_t)L.layout.split << 36) | ((uint64_t)ks::interp_form(L) << 32) |
+           (L.cta_mode ? L.wpc : 0u);
   };
   const size_t n_items = Ls.size();
   std::vector<char> done(n_items, 0);
@@ -495,7 +519,7 @@ int ks_simulate_sched(const ks_module* mod, const char* kernel, uint32_t grid, u
   int rc = prepare(mod, kernel, grid, block, params, param_bytes, bufs, n_bufs, trace_buf, trace_bytes, stats_buf,
                    stats_bytes, cfg, &L, &di);
   if (rc != KS_OK) return rc;
-  const uint32_t n_rows = L.layout.zero_off / ks::ROW_BYTES + 1u;
+  const uint32_t n_rows = L.layout.n_rows();
   if (ks::sched_smem_bytes(L.n_insn, n_rows) > (size_t)di.max_smem) return KS_ERR_LIMIT;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   L.sched_runs = reinterpret_cast<uint32_t*>(ws);

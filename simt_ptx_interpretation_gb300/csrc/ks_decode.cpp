@@ -1139,6 +1139,207 @@ class Decoder {
   int in_line(size_t) const { return T.line; }
 
   // Lays out the warp region and emits the device image.
+  // Operand routing of one instruction onto the unified datapaths (a, b, c
+  // rows and the aux immediate).
+  struct Route { uint8_t a, b, c; uint32_t aux; };
+
+  // The program image of one layout (split = 0 PAIR, 1 SPLIT): the region
+  // layout, one DevInsn per program entry plus the exit sentinel, the fast
+  // runs' lengths and forwarding flags, and the constant row values.
+  void resolve_image(uint32_t split, const std::vector<Route>& route, const std::vector<uint8_t>& madi,
+                     const std::vector<uint32_t>& madi_c, const std::vector<uint32_t>& crow,
+                     const std::vector<uint32_t>& rowval) {
+    const size_t n = K.code.size();
+    DevLayout& Y = K.layout[split];
+    const uint32_t RB = split ? ROW_SPLIT : ROW_PAIR;
+    Y.split = split;
+    Y.row_bytes = RB;
+    Y.n_slots = K.n_slots;
+    Y.n_crows = (uint32_t)rowval.size();
+    Y.const_off = K.n_slots * RB;
+    Y.zero_off = Y.const_off + Y.n_crows * RB;
+    const uint32_t n_rows = K.n_slots + Y.n_crows + 1u;
+    if (split) {
+      Y.ready_off = Y.zero_off + RB;
+      Y.pred_off = Y.ready_off + n_rows * 4u;
+      Y.n_ready = n_rows + 32u;
+      Y.stack_off = (Y.pred_off + 32u * 4u + 7u) / 8u * 8u;
+      Y.region_bytes = (Y.stack_off + KS_MAX_STACK * 8u + 127u) / 128u * 128u;
+      // hazard offsets are 16-bit
+      if (Y.region_bytes > 0xFFFFu) fail(KS_ERR_UNSUPPORTED, 0, "warp state beyond 64 KiB");
+    } else {
+      Y.ready_off = 0;
+      Y.n_ready = 0;
+      Y.pred_off = Y.zero_off + RB;
+      Y.stack_off = Y.pred_off + 256u;
+      Y.region_bytes = Y.stack_off + KS_MAX_STACK * 8u;
+    }
+
+    auto row_of = [&](uint8_t o) -> uint32_t {
+      if (o == OPND_ZERO) return Y.zero_off;
+      return (o & KS_CONST_BIT) ? Y.const_off + crow[o & 0x7F] * RB : (uint32_t)o * RB;
+    };
+    // predicate-table entry of a scoreboard index (the always-true
+    // predicate's entry, which stays 0, when absent or not a predicate)
+    auto phz = [&](uint8_t h) -> uint32_t {
+      if (h != KS_HZ_NONE && h >= KS_HZ_PRED0) return Y.pred_entry(h - KS_HZ_PRED0);
+      return Y.pred_entry(31);
+    };
+    auto pack = [](uint32_t lo, uint32_t hi) { return lo | (hi << 16); };
+    // where the guard, its negation and DOP_MADII's immediate go
+    uint32_t* (*guard_of)(DevInsn&) = split ? +[](DevInsn& o) { return &o.x[4]; } : +[](DevInsn& o) { return &o.x[0]; };
+    uint32_t* (*gneg_of)(DevInsn&) = split ? +[](DevInsn& o) { return &o.x[5]; } : +[](DevInsn& o) { return &o.x[1]; };
+    std::vector<DevInsn> dev(n + 1);
+    for (size_t i = 0; i <= n; i++) {
+      DevInsn& o = dev[i];
+      std::memset(&o, 0, sizeof o);
+      *guard_of(o) = 31;
+      o.a = o.b = o.c = o.d = Y.zero_off;
+      if (split) {
+        const uint32_t z = Y.ready_of(Y.zero_off), p31 = Y.pred_entry(31);
+        o.x[0] = o.x[1] = pack(z, z);
+        o.x[2] = o.x[3] = pack(p31, p31);
+      } else {
+        o.x[2] = o.x[3] = o.x[4] = o.x[5] = Y.pred_entry(31);  // ha, hb, hc, hd
+      }
+      if (i == n) {  // exit sentinel
+        o.op = OP_EXIT;
+        continue;
+      }
+      const KsInsn& in = K.code[i];
+      o.op = madi[i] ? (madi[i] == 1 ? DOP_MADI : DOP_MADII)
+             : fpu_family(in.op) ? DOP_FPU : imad_family(in.op) ? DOP_IMAD : in.op;
+      if ((o.op == DOP_FPU || o.op == DOP_IMAD) && in.guard != KS_NO_GUARD) o.op |= DOP_GUARDED;
+      o.inc = in.op == OP_EVENT ? 0u : INC_ISSUE;
+      if (in.guard != KS_NO_GUARD) {
+        *guard_of(o) = in.guard;
+        *gneg_of(o) = in.gneg ? 0xFFFFFFFFu : 0u;
+      }
+      const uint8_t ops[4] = {route[i].a, route[i].b, route[i].c, in.d};
+      uint32_t* rows[4] = {&o.a, &o.b, &o.c, &o.d};
+      for (int p = 0; p < 4; p++)
+        if (routed_width(in, p)) *rows[p] = row_of(ops[p]);
+      if ((o.op & ~DOP_GUARDED) == DOP_FPU || (o.op & ~DOP_GUARDED) == DOP_IMAD || imm_b_op(in.op) || madi[i])
+        o.aux = route[i].aux;
+      if (in.op != OP_EVENT) {
+        const bool pdest = in.hd != KS_HZ_NONE && in.hd >= KS_HZ_PRED0;
+        if (pdest) o.inc |= INC_PDEST;
+        if (split) {
+          // scoreboard terms: the rows read and written, the guard, the
+          // predicate sources (the destination term is the predicate of
+          // setp / predicate logic, which have no register destination)
+          o.x[0] = pack(Y.ready_of(o.a), Y.ready_of(o.b));
+          o.x[1] = pack(Y.ready_of(o.c), pdest ? phz(in.hd) : Y.ready_of(o.d));
+          o.x[2] = pack(Y.pred_entry(*guard_of(o)), phz(in.ha));
+          o.x[3] = pack(phz(in.hb), phz(in.hc));
+        } else {
+          // predicate hazards live in the predicate table; register hazards
+          // travel with the register rows themselves
+          o.x[2] = phz(in.ha);
+          o.x[3] = phz(in.hb);
+          o.x[4] = phz(in.hc);
+          if (pdest) o.x[5] = phz(in.hd);
+        }
+        if (routed_width(in, 3)) o.inc |= INC_RDEST;
+        const bool pred_operand = (in.ha >= KS_HZ_PRED0 && in.ha != KS_HZ_NONE) ||
+                                  (in.hb >= KS_HZ_PRED0 && in.hb != KS_HZ_NONE) ||
+                                  (in.hc >= KS_HZ_PRED0 && in.hc != KS_HZ_NONE) || pdest;
+        if (pred_operand) o.inc |= INC_PHAZ;
+        if (madi[i]) {
+          o.inc |= INC_MID;  // unguarded, no predicate operand
+          // DOP_MADII's immediate addend: x[4] in both layouts (PAIR: the
+          // unused hc; SPLIT: the guard, whose term is already in hz)
+          if (madi[i] == 2) o.x[4] = madi_c[i];
+        }
+        switch (in.op) {
+          case OP_LDP32: case OP_LDP64: case OP_MOV64: case OP_MOVSP:
+          case OP_ADD64: case OP_SUB64: case OP_MUL64: case OP_MAD64:
+          case OP_AND32: case OP_OR32: case OP_XOR32: case OP_AND64: case OP_OR64: case OP_XOR64:
+          case OP_SHL32: case OP_SHR32U: case OP_SHR32S: case OP_SHL64: case OP_SHR64U: case OP_SHR64S:
+          case OP_FDIV: case OP_FSQRT:
+          case OP_CVT_F32_U32: case OP_CVT_F32_S32: case OP_CVT_F32_U64: case OP_CVT_F32_S64:
+          case OP_CVT_F2I: case OP_CVT_ZX: case OP_CVT_SX:
+            if (in.guard == KS_NO_GUARD && !pred_operand) o.inc |= INC_MID;
+            break;
+          default:
+            break;
+        }
+        switch (in.op) {  // the SM issue model's memory-throttle label
+          case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64:
+          case OP_LDS32: case OP_LDS64: case OP_STS32: case OP_STS64:
+            o.inc |= INC_MCLASS | INC_MEMOP;
+            break;
+          case OP_LDP32: case OP_LDP64:
+            o.inc |= INC_MCLASS;
+            break;
+          case OP_MOV32: case OP_MOV64: case OP_MOVSP:
+            if (in.flags & KS_MOV_OPCODE) o.inc |= INC_MCLASS;
+            break;
+          default:
+            break;
+        }
+        o.wlat = (uint32_t)in.lat;
+        if (in.hd != KS_HZ_NONE) o.wlat |= DEV_HAS_DEST;
+        if (in.op == OP_STG32 || in.op == OP_STG64 || in.op == OP_STS32 || in.op == OP_STS64) o.wlat |= DEV_IS_STORE;
+        if (in.op == OP_BRA || in.op == OP_RET) o.wlat |= DEV_IS_CTRL;
+      }
+      switch (in.op) {
+        case OP_EVENT: o.aux = in.event | ((uint32_t)in.flags << 8); break;
+        case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64:
+        case OP_LDP32: case OP_LDP64: case OP_MOVSP:
+          o.aux = (uint32_t)in.imm;
+          break;
+        case OP_LDS32: case OP_LDS64: case OP_STS32: case OP_STS64:
+          o.aux = (uint32_t)in.imm;
+          if (in.flags & KS_SHA_WIDE) o.inc |= INC_ADDR64;
+          break;
+        case OP_CVT_F2I: o.aux = in.flags; break;
+        case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32: {
+          o.aux = (uint32_t)in.flags | ((uint32_t)in.d << 8);
+          const KsInsn* nx = i + 1 < n ? &K.code[i + 1] : nullptr;
+          if (in.guard == KS_NO_GUARD && nx && nx->op == OP_BRA && nx->guard == in.d && nx->target < (1u << 15)) {
+            o.inc |= INC_FUSE;
+            o.aux |= ((uint32_t)(nx->gneg ? 1u : 0u) << 16) | (nx->target << 17);
+          }
+          break;
+        }
+        case OP_ANDP: case OP_ORP: case OP_XORP:
+          o.aux = (uint32_t)in.a | ((uint32_t)in.b << 8) | ((uint32_t)in.d << 16);
+          break;
+        case OP_SELP32: case OP_SELP64: o.aux = in.c; break;
+        case OP_BRA: o.aux = (in.target & 0xFFFFu) | ((in.rpc & 0xFFFFu) << 16); break;
+        default: break;
+      }
+    }
+    // run lengths of the fast path (unguarded routed FPU / IMAD ops)
+    auto fast = [&](size_t i) { return dev[i].op == DOP_FPU || dev[i].op == DOP_IMAD; };
+    for (size_t i = n; i-- > 0;) {
+      DevInsn& o = dev[i];
+      if (fast(i)) {
+        const uint32_t next = fast(i + 1) ? (dev[i + 1].inc >> INC_RUN_SHIFT) : 0u;
+        o.inc |= (next + 1u) << INC_RUN_SHIFT;
+      }
+    }
+    // forwarding flags between consecutive fast ops (read by the SPLIT fast
+    // loop): inside a run the next op's operands and scoreboard terms are
+    // loaded before this op's stores
+    for (size_t i = 1; i < n; i++) {
+      if (!fast(i) || !fast(i - 1)) continue;
+      DevInsn& o = dev[i];
+      const uint32_t pd = dev[i - 1].d;
+      if (o.a == pd) o.inc |= INC_FWD_A;
+      if (o.b == pd) o.inc |= INC_FWD_B;
+      if (o.c == pd) o.inc |= INC_FWD_C;
+      if (o.a == pd || o.b == pd || o.c == pd || o.d == pd) o.inc |= INC_FWD_T;
+    }
+    K.prog_bytes = (uint32_t)((n + 1) * sizeof(DevInsn));
+    const size_t cb = rowval.size() * 4;
+    std::vector<uint8_t>& img = K.image[split];
+    img.assign((K.prog_bytes + cb + 15) / 16 * 16, 0);
+    std::memcpy(img.data(), dev.data(), K.prog_bytes);
+    if (cb) std::memcpy(img.data() + K.prog_bytes, rowval.data(), cb);
+  }
+
   void build_image() {
     const size_t n = K.code.size();
     // Rewrite the unified-datapath families onto (a, b, c) of fma / mad.
@@ -1146,7 +1347,6 @@ class Decoder {
     // the zero row (no constant row), a register addend has aux 0 (integer)
     // or the sign flip of a subtraction (f32). Integer subtraction needs no
     // negation: a - b = b * (-1) + a, a - imm = a * 1 + (-imm).
-    struct Route { uint8_t a, b, c; uint32_t aux; };
     std::vector<Route> route(n);
     auto is_const = [](uint8_t o) { return (o & KS_CONST_BIT) != 0; };
     auto cval = [&](uint8_t o) { return (uint32_t)K.cpool[o & 0x7F]; };
@@ -1266,141 +1466,8 @@ class Decoder {
       rowval.push_back((uint32_t)K.cpool[k]);
       if (cwidth[k] == 64) rowval.push_back((uint32_t)(K.cpool[k] >> 32));
     }
-    DevLayout& Y = K.layout;
-    Y.n_slots = K.n_slots;
-    Y.n_crows = (uint32_t)rowval.size();
-    Y.const_off = K.n_slots * ROW_BYTES;
-    Y.zero_off = Y.const_off + Y.n_crows * ROW_BYTES;
-    Y.pred_off = Y.zero_off + ROW_BYTES;
-    Y.stack_off = Y.pred_off + 256u;
-    Y.region_bytes = Y.stack_off + KS_MAX_STACK * 8u;
-
-    auto row_of = [&](uint8_t o) -> uint32_t {
-      if (o == OPND_ZERO) return Y.zero_off;
-      return (o & KS_CONST_BIT) ? Y.const_off + crow[o & 0x7F] * ROW_BYTES : (uint32_t)o * ROW_BYTES;
-    };
-    // predicate hazards live in the predicate table; register hazards travel
-    // with the register rows themselves
-    auto phz = [&](uint8_t h) -> uint32_t {
-      if (h != KS_HZ_NONE && h >= KS_HZ_PRED0) return Y.pred_entry(h - KS_HZ_PRED0);
-      return Y.pred_entry(31);
-    };
-    std::vector<DevInsn> dev(n + 1);
-    for (size_t i = 0; i <= n; i++) {
-      DevInsn& o = dev[i];
-      std::memset(&o, 0, sizeof o);
-      o.guard = 31;
-      o.a = o.b = o.c = o.d = Y.zero_off;
-      o.ha = o.hb = o.hc = o.hd = Y.pred_entry(31);
-      if (i == n) {  // exit sentinel
-        o.op = OP_EXIT;
-        continue;
-      }
-      const KsInsn& in = K.code[i];
-      o.op = madi[i] ? (madi[i] == 1 ? DOP_MADI : DOP_MADII)
-             : fpu_family(in.op) ? DOP_FPU : imad_family(in.op) ? DOP_IMAD : in.op;
-      if ((o.op == DOP_FPU || o.op == DOP_IMAD) && in.guard != KS_NO_GUARD) o.op |= DOP_GUARDED;
-      o.inc = in.op == OP_EVENT ? 0u : INC_ISSUE;
-      if (in.guard != KS_NO_GUARD) {
-        o.guard = in.guard;
-        o.gneg = in.gneg ? 0xFFFFFFFFu : 0u;
-      }
-      const uint8_t ops[4] = {route[i].a, route[i].b, route[i].c, in.d};
-      uint32_t* rows[4] = {&o.a, &o.b, &o.c, &o.d};
-      for (int p = 0; p < 4; p++)
-        if (routed_width(in, p)) *rows[p] = row_of(ops[p]);
-      if ((o.op & ~DOP_GUARDED) == DOP_FPU || (o.op & ~DOP_GUARDED) == DOP_IMAD || imm_b_op(in.op) || madi[i])
-        o.aux = route[i].aux;
-      if (in.op != OP_EVENT) {
-        o.ha = phz(in.ha);
-        o.hb = phz(in.hb);
-        o.hc = phz(in.hc);
-        if (in.hd != KS_HZ_NONE && in.hd >= KS_HZ_PRED0) {
-          o.hd = Y.pred_entry(in.hd - KS_HZ_PRED0);
-          o.inc |= INC_PDEST;
-        }
-        if (routed_width(in, 3)) o.inc |= INC_RDEST;
-        const bool pred_operand = (in.ha >= KS_HZ_PRED0 && in.ha != KS_HZ_NONE) ||
-                                  (in.hb >= KS_HZ_PRED0 && in.hb != KS_HZ_NONE) ||
-                                  (in.hc >= KS_HZ_PRED0 && in.hc != KS_HZ_NONE) || (o.inc & INC_PDEST);
-        if (pred_operand) o.inc |= INC_PHAZ;
-        if (madi[i]) {
-          o.inc |= INC_MID;  // unguarded, no predicate operand
-          if (madi[i] == 2) o.hc = madi_c[i];
-        }
-        switch (in.op) {
-          case OP_LDP32: case OP_LDP64: case OP_MOV64: case OP_MOVSP:
-          case OP_ADD64: case OP_SUB64: case OP_MUL64: case OP_MAD64:
-          case OP_AND32: case OP_OR32: case OP_XOR32: case OP_AND64: case OP_OR64: case OP_XOR64:
-          case OP_SHL32: case OP_SHR32U: case OP_SHR32S: case OP_SHL64: case OP_SHR64U: case OP_SHR64S:
-          case OP_FDIV: case OP_FSQRT:
-          case OP_CVT_F32_U32: case OP_CVT_F32_S32: case OP_CVT_F32_U64: case OP_CVT_F32_S64:
-          case OP_CVT_F2I: case OP_CVT_ZX: case OP_CVT_SX:
-            if (in.guard == KS_NO_GUARD && !pred_operand) o.inc |= INC_MID;
-            break;
-          default:
-            break;
-        }
-        switch (in.op) {  // the SM issue model's memory-throttle label
-          case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64:
-          case OP_LDS32: case OP_LDS64: case OP_STS32: case OP_STS64:
-            o.inc |= INC_MCLASS | INC_MEMOP;
-            break;
-          case OP_LDP32: case OP_LDP64:
-            o.inc |= INC_MCLASS;
-            break;
-          case OP_MOV32: case OP_MOV64: case OP_MOVSP:
-            if (in.flags & KS_MOV_OPCODE) o.inc |= INC_MCLASS;
-            break;
-          default:
-            break;
-        }
-        o.wlat = (uint32_t)in.lat;
-        if (in.hd != KS_HZ_NONE) o.wlat |= DEV_HAS_DEST;
-        if (in.op == OP_STG32 || in.op == OP_STG64 || in.op == OP_STS32 || in.op == OP_STS64) o.wlat |= DEV_IS_STORE;
-        if (in.op == OP_BRA || in.op == OP_RET) o.wlat |= DEV_IS_CTRL;
-      }
-      switch (in.op) {
-        case OP_EVENT: o.aux = in.event | ((uint32_t)in.flags << 8); break;
-        case OP_LDG32: case OP_LDG64: case OP_STG32: case OP_STG64:
-        case OP_LDP32: case OP_LDP64: case OP_MOVSP:
-          o.aux = (uint32_t)in.imm;
-          break;
-        case OP_LDS32: case OP_LDS64: case OP_STS32: case OP_STS64:
-          o.aux = (uint32_t)in.imm;
-          if (in.flags & KS_SHA_WIDE) o.inc |= INC_ADDR64;
-          break;
-        case OP_CVT_F2I: o.aux = in.flags; break;
-        case OP_SETP_U32: case OP_SETP_S32: case OP_SETP_U64: case OP_SETP_S64: case OP_SETP_F32: {
-          o.aux = (uint32_t)in.flags | ((uint32_t)in.d << 8);
-          const KsInsn* nx = i + 1 < n ? &K.code[i + 1] : nullptr;
-          if (in.guard == KS_NO_GUARD && nx && nx->op == OP_BRA && nx->guard == in.d && nx->target < (1u << 15)) {
-            o.inc |= INC_FUSE;
-            o.aux |= ((uint32_t)(nx->gneg ? 1u : 0u) << 16) | (nx->target << 17);
-          }
-          break;
-        }
-        case OP_ANDP: case OP_ORP: case OP_XORP:
-          o.aux = (uint32_t)in.a | ((uint32_t)in.b << 8) | ((uint32_t)in.d << 16);
-          break;
-        case OP_SELP32: case OP_SELP64: o.aux = in.c; break;
-        case OP_BRA: o.aux = (in.target & 0xFFFFu) | ((in.rpc & 0xFFFFu) << 16); break;
-        default: break;
-      }
-    }
-    // run lengths of the fast path (unguarded routed FPU / IMAD ops)
-    for (size_t i = n; i-- > 0;) {
-      DevInsn& o = dev[i];
-      if (o.op == DOP_FPU || o.op == DOP_IMAD) {
-        const uint32_t next = (dev[i + 1].op == DOP_FPU || dev[i + 1].op == DOP_IMAD) ? (dev[i + 1].inc >> INC_RUN_SHIFT) : 0u;
-        o.inc |= (next + 1u) << INC_RUN_SHIFT;
-      }
-    }
-    K.prog_bytes = (uint32_t)((n + 1) * sizeof(DevInsn));
-    const size_t cb = rowval.size() * 4;
-    K.image.assign((K.prog_bytes + cb + 15) / 16 * 16, 0);
-    std::memcpy(K.image.data(), dev.data(), K.prog_bytes);
-    if (cb) std::memcpy(K.image.data() + K.prog_bytes, rowval.data(), cb);
+    // one program image per layout
+    for (uint32_t split = 0; split < 2; split++) resolve_image(split, route, madi, madi_c, crow, rowval);
   }
 };
 

@@ -98,9 +98,14 @@ static_assert(sizeof(KsInsn) == 32, "KsInsn must be 32 bytes");
 // ---- device program format ---------------------------------------------
 // The host resolves every KsInsn into a 64-byte DevInsn whose operand fields
 // are byte offsets of rows inside a warp's shared-memory region. A row holds
-// one 8-byte pair per lane: (value, ready), where `ready` is the simulated
-// cycle at which the register becomes available (the same in every lane), so
-// one 64-bit shared load returns both an operand and its scoreboard entry:
+// one simulated register (or constant) across the 32 lanes. Two layouts of
+// the region exist; the decoder writes one program image for each and the
+// launch takes one of them (ks::pick_layout):
+//
+// PAIR layout (rows of 256 B): a row holds one 8-byte pair per lane,
+// (value, ready), where `ready` is the simulated cycle at which the register
+// becomes available (the same in every lane), so one 64-bit shared load
+// returns both an operand and its scoreboard entry:
 //
 //   warp region: [register rows: n_slots x 256 B]   row s = slot s
 //                [constant rows: n_crows x 256 B]   (constant, 0) in every lane
@@ -109,12 +114,31 @@ static_assert(sizeof(KsInsn) == 32, "KsInsn must be 32 bytes");
 //                    entry p: predicate p (p = 31 is the always-true predicate and stays 0)
 //                [reconvergence stack: 32 x 8 B]
 //
-// A 64-bit register or constant uses two consecutive rows (low word first),
-// so its high word is at row offset + 256.
-constexpr uint32_t ROW_BYTES = 256;
+// SPLIT layout (rows of 128 B): a row holds the values only, and the ready
+// times live in a table of one word per row -- half the shared memory per
+// warp, for kernels whose warp regions would otherwise bound the resident
+// warps:
+//
+//   warp region: [register rows: n_slots x 128 B]
+//                [constant rows: n_crows x 128 B]
+//                [zero row: 128 B]
+//                [ready table: one u32 per row]     (constant rows and the zero row: 0)
+//                [predicate ready table: 32 u32]
+//                [reconvergence stack: 32 x 8 B]
+//
+//   An instruction's scoreboard terms are gathered one per lane: lane l
+//   loads the ready word named by halfword l mod 4 (fast and mid loops: rows
+//   a, b, c, destination) or l mod 8 (general path: then the guard and the
+//   predicate sources) of the record's hazard words, and one warp max
+//   reduction gives the latest term.
+//
+// In both layouts a 64-bit register or constant uses two consecutive rows
+// (low word first), so its high word is at row offset + row_bytes, and its
+// scoreboard entry is the low row's.
+constexpr uint32_t ROW_PAIR = 256, ROW_SPLIT = 128;
 
 struct alignas(16) DevInsn {
-  // first 16 bytes + next 16: everything the fast path reads
+  // q0, q1: everything the fast and mid loops read (both layouts)
   uint32_t op;
   uint32_t wlat;   // in the image: latency class | flags (below); patched to dest latency
   uint32_t aux;    // offset / param offset / special / event / cvt / cmp|pred / target|rpc<<16 / pred idx
@@ -122,13 +146,28 @@ struct alignas(16) DevInsn {
   uint32_t a, b, c;  // source row offsets (region-relative; the zero row if absent)
   uint32_t inc;    // bit 0: issued (0 for a trace pseudo-op or the exit sentinel);
                    // bit 1: has a register destination; bit 2: has a predicate destination
-  uint32_t guard;  // predicate lane 0..30, or 31 (always true)
-  uint32_t gneg;   // 0 or 0xFFFFFFFF
-  uint32_t ha, hb, hc, hd;   // predicate-table offsets of predicate sources / destination (entry 31 if absent)
-  uint32_t dlat;   // patched: store completion latency (0 if not a store)
-  uint32_t nlat;   // patched: issue-clock advance (latency for bra/ret, 1 otherwise, 0 if inc == 0)
+  // q2, q3 by layout (x[6] = dlat and x[7] = nlat in both):
+  //   PAIR:  guard, gneg, ha, hb, hc, hd, dlat, nlat
+  //          ha/hb/hc/hd: predicate-table offsets of predicate sources /
+  //          destination (entry 31 if absent); DOP_MADII: hc = its immediate
+  //   SPLIT: hz[0..3], guard, gneg, dlat, nlat
+  //          hz: ready-word offsets (16 bits each, region-relative) of the
+  //          scoreboard terms: halfwords 0..3 = rows a, b, c and the
+  //          destination (the register's row, or the predicate written by
+  //          setp / predicate logic), 4 = the guard predicate, 5..7 =
+  //          predicate sources; an absent term names a word that stays 0.
+  //          DOP_MADII: guard = its immediate (the mid loop runs every
+  //          DOP_MADII; its guard term is in hz)
+  //   guard: predicate lane 0..30, or 31 (always true); gneg: 0 or 0xFFFFFFFF
+  //   dlat (patched): store completion latency (0 if not a store)
+  //   nlat (patched): issue-clock advance (latency for bra/ret, 1 otherwise, 0 if inc == 0)
+  uint32_t x[8];
 };
 static_assert(sizeof(DevInsn) == 64, "DevInsn must be 64 bytes");
+// byte offset of the SPLIT layout's hazard halfwords inside a DevInsn
+constexpr uint32_t DEV_HZ_OFF = 32;
+// positions in DevInsn::x
+constexpr uint32_t DX_DLAT = 6, DX_NLAT = 7;
 
 // flags in DevInsn::wlat of the uploaded image
 constexpr uint32_t DEV_HAS_DEST = 1u << 8;
@@ -157,6 +196,11 @@ constexpr uint32_t INC_RUN_SHIFT = 16u;
 //          memory access and no control transfer (runs in the mid loop)
 // INC_PHAZ: has a predicate source or destination (its ready entries matter)
 constexpr uint32_t INC_MID = 8u, INC_PHAZ = 16u;
+// Forwarding flags of a fast-path op relative to the entry before it (used
+// only inside a fast run, where that entry is the previous instruction):
+// INC_FWD_A/B/C, operand a / b / c is the previous entry's destination;
+// INC_FWD_T, one of its scoreboard terms is that destination's ready word.
+constexpr uint32_t INC_FWD_A = 1u << 9, INC_FWD_B = 1u << 10, INC_FWD_C = 1u << 11, INC_FWD_T = 1u << 12;
 constexpr uint32_t OP_EXIT = 0xFE;  // sentinel at index n_insn: the remaining lanes finish
 // Unified datapaths selected at resolve time (DevInsn::op only):
 //   DOP_FPU:  d = fma.rn(a, b, c ^ aux)      add: b = 1.0, c = y;  sub: b = 1.0, c = y, aux = sign bit;
@@ -174,9 +218,18 @@ constexpr uint32_t DOP_MADI = 0x44;
 constexpr uint32_t DOP_MADII = 0x45;
 
 struct DevLayout {
+  uint32_t split;      // 0: PAIR layout, 1: SPLIT layout
+  uint32_t row_bytes;  // ROW_PAIR or ROW_SPLIT
   uint32_t n_slots, n_crows;
   uint32_t const_off, zero_off, pred_off, stack_off, region_bytes;
+  // SPLIT: the ready table (one word per row, then the 32 predicates, which
+  // start at pred_off), zeroed per warp
+  uint32_t ready_off, n_ready;
   uint32_t pred_entry(uint32_t p) const { return pred_off + p * 4u; }
+  // SPLIT: the ready word of the row at region offset `row`
+  uint32_t ready_of(uint32_t row) const { return ready_off + row / row_bytes * 4u; }
+  // rows: register, constant and zero rows of a region
+  uint32_t n_rows() const { return zero_off / row_bytes + 1u; }
 };
 
 struct KsParam {
@@ -205,11 +258,21 @@ struct KsKernel {
   bool has_bar = false;       // uses bar.sync
   // a CTA's warps share state: they run together, one real CTA per simulated CTA
   bool cta_mode() const { return shared_bytes > 0 || has_bar; }
+  // Program images, [0] PAIR layout, [1] SPLIT layout:
   // [DevInsn x (n_insn + 1) | constant row values (u32 each), padded to 16]
-  std::vector<uint8_t> image;
-  DevLayout layout{};
-  uint32_t prog_bytes = 0;  // DevInsn part of the image
+  std::vector<uint8_t> image[2];
+  DevLayout layout[2]{};
+  uint32_t prog_bytes = 0;  // DevInsn part of an image
 };
+
+// The layout a launch of `k` runs in: forced by KS_FLAG_LAYOUT_PAIR /
+// KS_FLAG_LAYOUT_SPLIT in ks_config.flags, else SPLIT for a kernel outside
+// CTA mode whose PAIR warp region exceeds SPLIT_REGION_MIN bytes (its regions
+// would bound the resident warps below what the registers allow), else PAIR.
+// Returns 0 / 1, or a negative KS_ERR_* (both flags; SPLIT forced on a CTA-mode
+// kernel, which runs in the PAIR layout only).
+constexpr uint32_t SPLIT_REGION_MIN = 12u * 1024u;
+int pick_layout(const KsKernel& k, uint32_t flags);
 
 // Decoder entry point (ks_decode.cpp). Returns KS_OK or a KS_ERR_* code and
 // fills `err` with a message.
@@ -303,6 +366,11 @@ int choose_launch(const KsLaunch& L, int sms, int max_smem, LaunchShape* shape);
 int launch_interp(const KsLaunch& L, const LaunchShape& shape, void* stream);
 int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm,
                      bool reg_capped = false);
+// SPLIT-layout instantiations (ks_interp_split.cu; plain mode only): the
+// single-launch kernel of a form (0 lean, 1 instrumented, 2 issue-logging),
+// register-capped or not, and the batch kernel of a form.
+const void* interp_fn_split(int form, bool reg_capped);
+const void* batch_fn_split(int form);
 // Instantiation form of a launch: 0 lean, 1 instrumented (cache model or
 // profile), 2 instrumented with the issue-run log (SM model).
 int interp_form(const KsLaunch& L);

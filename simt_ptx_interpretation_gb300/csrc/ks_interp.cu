@@ -73,7 +73,8 @@ static const void* interp_fn_of(int form) {
                      : (const void*)ks_interp_kernel<CTA, BIG, true, true, 1u, CAP>;
 }
 
-static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, int form, bool reg_capped) {
+static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, int form, bool reg_capped, bool split) {
+  if (split) return interp_fn_split(form, reg_capped);  // plain mode only
   if (!cta) return reg_capped ? interp_fn_of<false, false, true>(form) : interp_fn_of<false, false, false>(form);
   if (real_warps_per_cta > 8) return interp_fn_of<true, true, false>(form);
   return reg_capped ? interp_fn_of<true, false, true>(form) : interp_fn_of<true, false, false>(form);
@@ -94,16 +95,18 @@ static int ensure_attr() {
   int mx = 0;
   e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return (int)e;
-  for (int cta = 0; cta < 2; cta++)
-    for (int big = 0; big < 2; big++)
-      for (int capped = 0; capped < 2; capped++)
-        for (int form = 0; form < 3; form++) {
-          if (!cta && big) continue;
-          if (big && capped) continue;
-          e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, form, capped), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   mx);
-          if (e != cudaSuccess) return (int)e;
-        }
+  for (int split = 0; split < 2; split++)
+    for (int cta = 0; cta < 2; cta++)
+      for (int big = 0; big < 2; big++)
+        for (int capped = 0; capped < 2; capped++)
+          for (int form = 0; form < 3; form++) {
+            if (!cta && big) continue;
+            if (big && capped) continue;
+            if (split && cta) continue;
+            e = cudaFuncSetAttribute(interp_fn(cta, big ? 32u : 1u, form, capped, split),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+            if (e != cudaSuccess) return (int)e;
+          }
   if (dev < 64) g_attr_done[dev] = 1;
   return 0;
 }
@@ -117,7 +120,7 @@ int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem
   if (e) return e;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
-  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L), reg_capped);
+  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L), reg_capped, L.layout.split != 0);
   static std::mutex mu;
   static std::map<std::tuple<int, const void*, uint32_t, size_t>, int> known;
   const auto key = std::make_tuple(dev, fn, real_warps_per_cta, smem);
@@ -206,7 +209,8 @@ int launch_interp(const KsLaunch& L, const LaunchShape& shape, void* stream) {
   G.cta_begin[1] = shape.ctas;
   G.item[0] = L;
   void* args[] = {&G};
-  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, shape.warps_per_cta, form_of(L), shape.reg_capped),
+  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, shape.warps_per_cta, form_of(L), shape.reg_capped,
+                                         L.layout.split != 0),
                                dim3(shape.ctas), dim3(shape.warps_per_cta * 32), args, smem, (cudaStream_t)stream);
 }
 

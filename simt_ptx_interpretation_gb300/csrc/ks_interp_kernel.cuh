@@ -18,13 +18,24 @@
 // reports KS_ST_TIMEOUT instead of hanging. The launch's latency table is then
 // patched into the staged instructions.
 //
-// Every operand field of an instruction is the offset of a 256-byte row of the
-// warp's region holding one (value, ready) pair per lane, so lane l reads an
-// operand and its scoreboard entry with one 8-byte shared load at
-// (region + offset + 8l): registers, constants (replicated across the row) and
-// "no operand" (the zero row) look the same. A destination's ready time
-// alone (the write-after-write wait) is read from lane 0's pair by every
-// lane: one broadcast word instead of a strided load of two wavefronts.
+// Every operand field of an instruction is the offset of a row of the warp's
+// region, so registers, constants (replicated across the row) and "no
+// operand" (the zero row) look the same. Two layouts (ks_internal.h; the
+// SPLIT template parameter):
+//  - PAIR: a 256-byte row holds one (value, ready) pair per lane, so lane l
+//    reads an operand and its scoreboard entry with one 8-byte shared load at
+//    (region + offset + 8l). A destination's ready time alone (the
+//    write-after-write wait) is read from lane 0's pair by every lane: one
+//    broadcast word instead of a strided load of two wavefronts.
+//  - SPLIT: a 128-byte row holds the values (one 4-byte load per lane at
+//    region + offset + 4l), and the warp-uniform ready times live apart, one
+//    word per row and per predicate; an instruction's terms (its rows,
+//    destination, guard and predicate sources) are gathered one per lane --
+//    lane l loads the ready word named by halfword l mod 4 (fast and mid
+//    loops) or l mod 8 (general path) of the record -- and one redux.sync max
+//    gives the latest. Half the shared memory per warp, for kernels whose
+//    regions would bound the resident warps; a few more instructions per
+//    simulated instruction.
 //
 // Kernels with shared memory or bar.sync run in CTA mode (the CTA template
 // instantiation): one real CTA per simulated CTA, one real warp per simulated
@@ -164,8 +175,8 @@ __device__ __forceinline__ void st_shared_if(bool p, uint32_t addr, uint32_t v) 
       : "memory");
 }
 
-// Stores (value, ready) for a lane that executes and only `ready` for one
-// that does not (the scoreboard entry is written in every lane).
+// PAIR layout: stores (value, ready) for a lane that executes and only
+// `ready` for one that does not (the scoreboard entry is written in every lane).
 __device__ __forceinline__ void st_pair(bool on, uint32_t addr, uint32_t v, uint32_t ready) {
   asm volatile(
       "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t"
@@ -178,6 +189,10 @@ __device__ __forceinline__ void st_pair(bool on, uint32_t addr, uint32_t v, uint
 #define SM32(off) (*reinterpret_cast<uint32_t*>(smem + (off)))
 #define SM2(off) (*reinterpret_cast<const uint2*>(smem + (off)))
 #define SM64(off) (*reinterpret_cast<uint64_t*>(smem + (off)))
+// this lane's scoreboard-term offset in the record at `rec` (a const uint4*):
+// halfword `hsel` (bytes) of its hazard words
+#define HZ_AT(rec, hsel) \
+  ((uint32_t)*reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(rec) + (hsel)))
 
 constexpr uint32_t REBASE_AT = 1u << 30;
 constexpr uint64_t BUDGET_CHUNK = 1ull << 30;
@@ -217,9 +232,11 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 // bound the resident warps: plain, two CTAs of up to 10 warps (96
 // registers, no spills, 21 warps an SM); CTA mode, three CTAs of up to 8
 // warps (80 registers, a few spills, 24 warps an SM).
-template <bool CTA, bool BIG, bool INSTR, bool RUNLOG, uint32_t NB, bool CAP = false>
+// SPLIT: the SPLIT register-file layout (plain mode only).
+template <bool CTA, bool BIG, bool INSTR, bool RUNLOG, uint32_t NB, bool CAP = false, bool SPLIT = false>
 __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ? 256 : 384)), CAP ? (CTA ? 3 : 2) : 1)
     ks_interp_kernel(const __grid_constant__ KsGrid<NB> G) {
+  static_assert(!(SPLIT && CTA), "CTA mode runs in the PAIR layout");
   uint32_t item = 0;
   if constexpr (NB > 1) {
     while (item + 1u < G.n && blockIdx.x >= G.cta_begin[item + 1u]) item++;  // uniform in the CTA
@@ -239,9 +256,17 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
   constexpr bool cta_mode = CTA;
   const uint32_t sh_base = region0(L.image_bytes) + nwarps * Y.region_bytes;  // simulated shared memory
   const uint32_t wb = region0(L.image_bytes) + wid * Y.region_bytes;  // this warp's region
-  const uint32_t lb = wb + lane * 8u;                                  // this lane's pair in row 0
-  const uint32_t pg = wb + Y.pred_off;                                 // predicate ready table
-  const uint32_t s_lane = cvta_shared(smem) + lb;                      // shared-window address of lb
+  constexpr uint32_t RB = SPLIT ? ROW_SPLIT : ROW_PAIR;               // row bytes
+  const uint32_t lv = wb + lane * (SPLIT ? 4u : 8u);                   // this lane's value in row 0
+  const uint32_t s_lane = cvta_shared(smem) + lv;                      // shared-window address of lv
+  [[maybe_unused]] const uint32_t s_wb = cvta_shared(smem) + wb;       // ... of the region
+  [[maybe_unused]] const uint32_t pg = wb + Y.pred_off;                // predicate ready table
+  // SPLIT: the scoreboard-term halfword this lane gathers: of four (fast and
+  // mid loops: rows a, b, c, destination) or of eight (general path: then the
+  // guard and the predicate sources); the lanes that hold the destination's
+  // term write its ready time
+  [[maybe_unused]] const uint32_t hs4 = DEV_HZ_OFF + 2u * (lane & 3u), hs8 = DEV_HZ_OFF + 2u * (lane & 7u);
+  [[maybe_unused]] const bool is_d4 = (lane & 3u) == 3u, is_d8 = (lane & 7u) == 3u;
 
   // ---- stage the program once per CTA (a1) ----
   if (threadIdx.x == 0) {
@@ -263,15 +288,20 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       DevInsn* p = reinterpret_cast<DevInsn*>(smem) + i;
       const uint32_t f = p->wlat, lat = L.lat[f & 0xFFu];
       p->wlat = (f & DEV_HAS_DEST) ? lat : 0u;
-      p->dlat = (f & DEV_IS_STORE) ? lat : 0u;
-      p->nlat = p->inc ? ((f & DEV_IS_CTRL) ? lat : 1u) : 0u;
+      p->x[DX_DLAT] = (f & DEV_IS_STORE) ? lat : 0u;
+      p->x[DX_NLAT] = p->inc ? ((f & DEV_IS_CTRL) ? lat : 1u) : 0u;
     }
   }
   // constant rows and the zero row of this warp's region (read-only afterwards)
   {
     const uint32_t* vals = reinterpret_cast<const uint32_t*>(smem + L.prog_bytes);
-    for (uint32_t r = 0; r < Y.n_crows; r++) SM64(lb + Y.const_off + r * ROW_BYTES) = (uint64_t)vals[r];
-    SM64(lb + Y.zero_off) = 0ull;
+    if constexpr (SPLIT) {
+      for (uint32_t r = 0; r < Y.n_crows; r++) SM32(lv + Y.const_off + r * RB) = vals[r];
+      SM32(lv + Y.zero_off) = 0u;
+    } else {  // (value, ready = 0) pairs
+      for (uint32_t r = 0; r < Y.n_crows; r++) SM64(lv + Y.const_off + r * RB) = (uint64_t)vals[r];
+      SM64(lv + Y.zero_off) = 0ull;
+    }
   }
   __syncthreads();
 
@@ -304,8 +334,13 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
     }
 
     // ---- warp set-up (a1): registers zero, predicates false, clock 0 ----
-    for (uint32_t s = 0; s < Y.n_slots; s++) SM64(lb + s * ROW_BYTES) = 0ull;
-    SM32(pg + lane * 4u) = 0u;
+    if constexpr (SPLIT) {
+      for (uint32_t s = 0; s < Y.n_slots; s++) SM32(lv + s * RB) = 0u;
+      for (uint32_t i = lane; i < Y.n_ready; i += 32u) SM32(wb + Y.ready_off + 4u * i) = 0u;
+    } else {
+      for (uint32_t s = 0; s < Y.n_slots; s++) SM64(lv + s * RB) = 0ull;
+      SM32(pg + lane * 4u) = 0u;
+    }
     __syncwarp();
     uint32_t my_pred = (lane == 31u) ? 0xFFFFFFFFu : 0u;  // predicate 31 is always true
     uint32_t pc = 0, rpc = exit_pc;
@@ -386,7 +421,9 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         }
       }
       const uint4* ip = reinterpret_cast<const uint4*>(smem + pc * (uint32_t)sizeof(DevInsn));
-      const uint4 q0 = ip[0], q1 = ip[1], q2 = ip[2], q3 = ip[3];
+      const uint4 q0 = ip[0], q1 = ip[1], q3 = ip[3];
+      // PAIR: guard, gneg, ha, hb (SPLIT: the hazard halfwords, gathered per lane)
+      const uint4 q2 = SPLIT ? make_uint4(0u, 0u, 0u, 0u) : ip[2];
       const uint32_t fuel_in = min(budget, rpc > pc ? rpc - pc : 0xFFFFFFFFu);
       const bool runnable = fuel_in != 0u && t_next < REBASE_AT;
 
@@ -396,24 +433,37 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       // general path next), without the general path's operand loads and
       // dispatch. The setp is unguarded, so every active lane executes it.
       if (runnable && (q1.w & INC_FUSE) && (q0.x == OP_SETP_U32 || q0.x == OP_SETP_S32 || q0.x == OP_SETP_F32)) {
-        const uint2 sa = SM2(lb + q1.x), sb = SM2(lb + q1.y);
+        // operands (PAIR: with their ready times); SPLIT: this lane's term
+        // offset and term
+        const uint2 sa2 = SPLIT ? make_uint2(SM32(lv + q1.x), 0u) : SM2(lv + q1.x);
+        const uint2 sb2 = SPLIT ? make_uint2(SM32(lv + q1.y), 0u) : SM2(lv + q1.y);
+        const uint32_t sa = sa2.x, sb = sb2.x;
+        const uint32_t hk = SPLIT ? HZ_AT(ip, hs4) : 0u;
+        const uint32_t hr = SPLIT ? SM32(wb + hk) : 0u;
         const uint32_t sop = q0.x, saux = q0.z, cmp = saux & 0xFFu, pd = (saux >> 8) & 0xFFu;
         bool lt, eq, gt;
         if (sop == OP_SETP_F32) {
-          const float x = __uint_as_float(sa.x), y = __uint_as_float(sb.x);
+          const float x = __uint_as_float(sa), y = __uint_as_float(sb);
           lt = x < y; eq = x == y; gt = x > y;
         } else {
           const uint32_t flip = sop == OP_SETP_S32 ? 0x80000000u : 0u;  // signed order
-          const uint32_t x = sa.x ^ flip, y = sb.x ^ flip;
+          const uint32_t x = sa ^ flip, y = sb ^ flip;
           lt = x < y; eq = x == y; gt = x > y;
         }
         const uint32_t bal = __ballot_sync(FULL, rel_result(lt, eq, gt, cmp));
         // its scoreboard: the sources, and the predicate it writes (the
-        // other hazard entries of an unguarded setp are the always-true
-        // predicate and the zero row, ready at 0)
-        const uint32_t t = max(max(t_next, sa.y), max(sb.y, SM32(wb + q3.y)));
-        const uint32_t wr = t + q0.y;
-        SM32(wb + q3.y) = wr;
+        // other terms of an unguarded setp are the always-true predicate and
+        // the zero row, ready at 0)
+        uint32_t t, wr;
+        if constexpr (SPLIT) {
+          t = max(t_next, __reduce_max_sync(FULL, hr));
+          wr = t + q0.y;
+          st_shared_if(is_d4, s_wb + hk, wr);
+        } else {  // PAIR: ready times in the rows' pairs, the predicate's in q3.y (hd)
+          t = max(max(t_next, sa2.y), max(sb2.y, SM32(wb + q3.y)));
+          wr = t + q0.y;
+          SM32(wb + q3.y) = wr;
+        }
         if (lane == pd) my_pred = (my_pred & ~mask) | (bal & mask);
         max_ready = max(max_ready, wr);
         drain = max(drain, t + q3.z);
@@ -439,11 +489,13 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       }
 
       // ---- fast path: runs of unguarded routed FPU / IMAD instructions.
-      // pc, budget and t_last are rebuilt when the run ends. Software-pipelined:
-      // while instruction k executes, the rows of instruction k+1 are loaded and
-      // the record of k+2 fetched; k+1's rows may predate k's store, so k's
-      // result and ready time are forwarded into any of them that is k's
-      // destination.
+      // pc, budget and t_last are rebuilt when the run ends. Software-pipelined
+      // in three stages: while instruction k executes, the operand rows (and
+      // SPLIT: scoreboard terms) of k+1 are loaded and the record of k+2
+      // fetched; k+1's loads may predate k's stores, so k's result goes into
+      // any operand of k+1 that is k's destination and k's ready time into
+      // k+1's scoreboard (PAIR: by comparing row offsets; SPLIT: as the
+      // decoder's INC_FWD_* flags say).
       // The run is counted up front: at most the consecutive fast ops from pc
       // (inc >> 16), the fuel, and as many steps as keep every clock below
       // REBASE_AT (each step moves the clock by at most the largest fast-op
@@ -452,54 +504,109 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
                                    ? (REBASE_AT - max(t_next, max_ready)) >> L.fast_shift : 0u;
       const uint32_t run_n = min(min(fuel_in, q1.w >> INC_RUN_SHIFT), run_cap);
       if (t_next < REBASE_AT && run_n != 0u && (q0.x | 1u) == DOP_IMAD) {
-        uint32_t n = run_n;
-        const bool on_all = (mask >> lane) & 1u;
-        // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
-        uint4 ka = q0, kb = q1;
-        uint2 a = SM2(lb + kb.x), b = SM2(lb + kb.y), c = SM2(lb + kb.z);
-        uint32_t rd = SM32(wb + ka.w + 4u);
-        // instruction k+1 (the last instruction is never a fast op, so k+1 and
-        // k+2 stay within the program and its exit sentinel)
-        uint4 na = ip[4], nb = ip[5];
-        for (;;) {
-          uint2 a1 = SM2(lb + nb.x), b1 = SM2(lb + nb.y), c1 = SM2(lb + nb.z);
-          uint32_t rd1 = SM32(wb + na.w + 4u);
-          const uint4 ma = ip[8], mb = ip[9];
-          const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));
-          const uint32_t wr = t + ka.y;
-          max_ready = max(max_ready, wr);
-          t_next = t + 1u;
-          const uint32_t cx = c.x ^ ka.z;
-          const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
-          const uint32_t ri = a.x * b.x + cx;
-          const uint32_t res = ka.x == DOP_FPU ? rf : ri;
-          st_pair(on_all, s_lane + ka.w, res, wr);
-          // forward k into k+1
-          const uint32_t dk = ka.w;
-          const bool fa = nb.x == dk, fb = nb.y == dk, fc = nb.z == dk;
-          a1.x = (fa && on_all) ? res : a1.x;
-          a1.y = fa ? wr : a1.y;
-          b1.x = (fb && on_all) ? res : b1.x;
-          b1.y = fb ? wr : b1.y;
-          c1.x = (fc && on_all) ? res : c1.x;
-          c1.y = fc ? wr : c1.y;
-          rd1 = na.w == dk ? wr : rd1;
-          ka = na;
-          kb = nb;
-          na = ma;
-          nb = mb;
-          a = a1;
-          b = b1;
-          c = c1;
-          rd = rd1;
-          ip += 4;
-          if (--n == 0u) break;  // uniform in value
+        if constexpr (SPLIT) {
+          uint32_t n = run_n;
+          const bool on_all = (mask >> lane) & 1u;
+          // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its operand
+          // values, this lane's term offset and the latest term
+          uint4 ka = q0, kb = q1;
+          uint32_t a = SM32(lv + kb.x), b = SM32(lv + kb.y), c = SM32(lv + kb.z);
+          uint32_t hk = HZ_AT(ip, hs4);
+          uint32_t hm = __reduce_max_sync(FULL, SM32(wb + hk));
+          // instruction k+1's record and term offset (the last instruction is
+          // never a fast op, so k+1 and k+2 stay within the program and its
+          // exit sentinel)
+          uint4 na = ip[4], nb = ip[5];
+          uint32_t hk1 = HZ_AT(ip + 4, hs4);
+          for (;;) {
+            uint32_t a1 = SM32(lv + nb.x), b1 = SM32(lv + nb.y), c1 = SM32(lv + nb.z);
+            const uint32_t r1 = SM32(wb + hk1);
+            const uint4 ma = ip[8], mb = ip[9];
+            const uint32_t hk2 = HZ_AT(ip + 8, hs4);
+            const uint32_t t = max(t_next, hm);
+            const uint32_t wr = t + ka.y;
+            max_ready = max(max_ready, wr);
+            t_next = t + 1u;
+            const uint32_t cx = c ^ ka.z;
+            const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a), __uint_as_float(b), __uint_as_float(cx)));
+            const uint32_t ri = a * b + cx;
+            const uint32_t res = ka.x == DOP_FPU ? rf : ri;
+            st_shared_if(on_all, s_lane + ka.w, res);
+            st_shared_if(is_d4, s_wb + hk, wr);  // the destination's ready word
+            // forward k into k+1
+            const uint32_t f = nb.w;
+            a1 = ((f & INC_FWD_A) && on_all) ? res : a1;
+            b1 = ((f & INC_FWD_B) && on_all) ? res : b1;
+            c1 = ((f & INC_FWD_C) && on_all) ? res : c1;
+            const uint32_t hm1 = __reduce_max_sync(FULL, r1);
+            hm = (f & INC_FWD_T) ? max(hm1, wr) : hm1;
+            ka = na;
+            kb = nb;
+            na = ma;
+            nb = mb;
+            a = a1;
+            b = b1;
+            c = c1;
+            hk = hk1;
+            hk1 = hk2;
+            ip += 4;
+            if (--n == 0u) break;  // uniform in value
+          }
+          pc += run_n;
+          budget -= run_n;
+          t_last = t_next - 1u;
+          if constexpr (RUNLOG) run_next = pc;
+          continue;
+        } else {
+          uint32_t n = run_n;
+          const bool on_all = (mask >> lane) & 1u;
+          // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
+          uint4 ka = q0, kb = q1;
+          uint2 a = SM2(lv + kb.x), b = SM2(lv + kb.y), c = SM2(lv + kb.z);
+          uint32_t rd = SM32(wb + ka.w + 4u);
+          // instruction k+1 (the last instruction is never a fast op, so k+1 and
+          // k+2 stay within the program and its exit sentinel)
+          uint4 na = ip[4], nb = ip[5];
+          for (;;) {
+            uint2 a1 = SM2(lv + nb.x), b1 = SM2(lv + nb.y), c1 = SM2(lv + nb.z);
+            uint32_t rd1 = SM32(wb + na.w + 4u);
+            const uint4 ma = ip[8], mb = ip[9];
+            const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));
+            const uint32_t wr = t + ka.y;
+            max_ready = max(max_ready, wr);
+            t_next = t + 1u;
+            const uint32_t cx = c.x ^ ka.z;
+            const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
+            const uint32_t ri = a.x * b.x + cx;
+            const uint32_t res = ka.x == DOP_FPU ? rf : ri;
+            st_pair(on_all, s_lane + ka.w, res, wr);
+            // forward k into k+1
+            const uint32_t dk = ka.w;
+            const bool fa = nb.x == dk, fb = nb.y == dk, fc = nb.z == dk;
+            a1.x = (fa && on_all) ? res : a1.x;
+            a1.y = fa ? wr : a1.y;
+            b1.x = (fb && on_all) ? res : b1.x;
+            b1.y = fb ? wr : b1.y;
+            c1.x = (fc && on_all) ? res : c1.x;
+            c1.y = fc ? wr : c1.y;
+            rd1 = na.w == dk ? wr : rd1;
+            ka = na;
+            kb = nb;
+            na = ma;
+            nb = mb;
+            a = a1;
+            b = b1;
+            c = c1;
+            rd = rd1;
+            ip += 4;
+            if (--n == 0u) break;  // uniform in value
+          }
+          pc += run_n;
+          budget -= run_n;
+          t_last = t_next - 1u;
+          if constexpr (RUNLOG) run_next = pc;
+          continue;
         }
-        pc += run_n;
-        budget -= run_n;
-        t_last = t_next - 1u;
-        if constexpr (RUNLOG) run_next = pc;
-        continue;
       }
       // ---- mid path: runs of the other unguarded register-to-register ops
       // (64-bit arithmetic, logic, shifts, conversions, specials, ld.param,
@@ -510,23 +617,37 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         const bool on = (mask >> lane) & 1u;
         const uint4* mp = ip;
         uint4 ka = q0, kb = q1;
+        [[maybe_unused]] uint32_t hk = SPLIT ? HZ_AT(mp, hs4) : 0u;  // SPLIT: this lane's term offset
         for (;;) {
           const uint4 na = mp[4], nb = mp[5];  // the next record, fetched early
-          const uint2 pa = SM2(lb + kb.x), pb = SM2(lb + kb.y), pcc = SM2(lb + kb.z);
-          const uint32_t rd = SM32(wb + ka.w + 4u);
-          const uint32_t t = max(max(t_next, pa.y), max(max(pb.y, pcc.y), rd));
+          [[maybe_unused]] uint32_t hk1 = 0;
+          uint32_t a0, b0, c0, t;
+          if constexpr (SPLIT) {
+            hk1 = HZ_AT(mp + 4, hs4);
+            a0 = SM32(lv + kb.x);
+            b0 = SM32(lv + kb.y);
+            c0 = SM32(lv + kb.z);
+            t = max(t_next, __reduce_max_sync(FULL, SM32(wb + hk)));
+          } else {  // operands with their ready times, the destination's from lane 0's pair
+            const uint2 pa = SM2(lv + kb.x), pb = SM2(lv + kb.y), pcc = SM2(lv + kb.z);
+            const uint32_t rd = SM32(wb + ka.w + 4u);
+            t = max(max(t_next, pa.y), max(max(pb.y, pcc.y), rd));
+            a0 = pa.x;
+            b0 = pb.x;
+            c0 = pcc.x;
+          }
           const uint32_t wr = t + ka.y;
           max_ready = max(max_ready, wr);
           t_next = t + 1u;
-          const uint32_t a0 = pa.x, b0 = pb.x, D = ka.w, aux = ka.z;
+          const uint32_t D = ka.w, aux = ka.z;
           const uint32_t A = kb.x, B = kb.y;
           uint32_t lo = 0, hi = 0;
           bool wide = false;
-#define MA64() ((uint64_t)a0 | ((uint64_t)SM32(lb + A + ROW_BYTES) << 32))
-#define MB64() ((uint64_t)b0 | ((uint64_t)SM32(lb + B + ROW_BYTES) << 32))
+#define MA64() ((uint64_t)a0 | ((uint64_t)SM32(lv + A + RB) << 32))
+#define MB64() ((uint64_t)b0 | ((uint64_t)SM32(lv + B + RB) << 32))
 #define R64(v) do { const uint64_t v_ = (v); lo = (uint32_t)v_; hi = (uint32_t)(v_ >> 32); wide = true; } while (0)
           switch (__shfl_sync(FULL, ka.x, 0)) {
-            case DOP_MADI: lo = a0 * aux + pcc.x; break;
+            case DOP_MADI: lo = a0 * aux + c0; break;
             case DOP_MADII: lo = a0 * aux + mp[3].x; break;
             case OP_LDP32: lo = *reinterpret_cast<const uint32_t*>(s_params + aux); break;
             case OP_LDP64: R64(*reinterpret_cast<const uint64_t*>(s_params + aux)); break;
@@ -538,7 +659,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             case OP_ADD64: R64(MA64() + MB64()); break;
             case OP_SUB64: R64(MA64() - MB64()); break;
             case OP_MUL64: R64(MA64() * MB64()); break;
-            case OP_MAD64: R64(MA64() * MB64() + ((uint64_t)pcc.x | ((uint64_t)SM32(lb + kb.z + ROW_BYTES) << 32))); break;
+            case OP_MAD64: R64(MA64() * MB64() + ((uint64_t)c0 | ((uint64_t)SM32(lv + kb.z + RB) << 32))); break;
             case OP_AND32: lo = a0 & (b0 | aux); break;
             case OP_OR32: lo = a0 | (b0 | aux); break;
             case OP_XOR32: lo = a0 ^ (b0 | aux); break;
@@ -573,8 +694,14 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
 #undef MA64
 #undef MB64
 #undef R64
-          st_pair(on, s_lane + D, lo, wr);
-          st_shared_if(on && wide, s_lane + D + ROW_BYTES, hi);
+          if constexpr (SPLIT) {
+            st_shared_if(on, s_lane + D, lo);
+            st_shared_if(is_d4, s_wb + hk, wr);  // the destination's ready word
+            hk = hk1;
+          } else {
+            st_pair(on, s_lane + D, lo, wr);
+          }
+          st_shared_if(on && wide, s_lane + D + RB, hi);
           fuel--;
           mp += 4;
           ka = na;
@@ -589,18 +716,38 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         continue;
       }
       // ---- general path: one instruction; every operand / ready-time load at once
-      const uint32_t op = __shfl_sync(FULL, q0.x, 0), guard = q2.x, gneg = q2.y, inc = q1.w;
+      const uint32_t op = __shfl_sync(FULL, q0.x, 0), inc = q1.w;
+      const uint32_t guard = SPLIT ? q3.x : q2.x, gneg = SPLIT ? q3.y : q2.y;
       [[maybe_unused]] const uint32_t pc_here = pc;  // the instrumented handlers' program entry
       [[maybe_unused]] uint32_t consumed = 1;        // program entries this step issues (2: setp + bra)
       const uint32_t A = q1.x, B = q1.y, C = q1.z, D = q0.w;
       const uint32_t aux = q0.z;
-      const uint2 pa = SM2(lb + A), pb = SM2(lb + B), pcc = SM2(lb + C);
-      const uint32_t a0 = pa.x, b0 = pb.x, c0 = pcc.x;
-      const uint32_t rd = SM32(wb + D + 4u);
-      uint32_t hmax = 0;
-      if (inc & INC_PHAZ)
-        hmax = max(max(SM32(wb + q2.z), SM32(wb + q2.w)), max(SM32(wb + q3.x), SM32(wb + q3.y)));
-      const uint32_t rg = SM32(pg + guard * 4u);
+      uint32_t a0, b0, c0;
+      // the scoreboard: SPLIT, the latest of all eight terms (rows a, b, c,
+      // the destination, the guard, the predicate sources) gathered one per
+      // lane; PAIR, the rows' ready times from their pairs, the
+      // destination's from lane 0's pair, the guard's and (predicate
+      // operands) the predicates' from the predicate table
+      [[maybe_unused]] uint32_t hk = 0;
+      uint32_t hr;
+      if constexpr (SPLIT) {
+        hk = HZ_AT(ip, hs8);
+        a0 = SM32(lv + A);
+        b0 = SM32(lv + B);
+        c0 = SM32(lv + C);
+        hr = SM32(wb + hk);
+      } else {
+        const uint2 pa = SM2(lv + A), pb = SM2(lv + B), pcc = SM2(lv + C);
+        a0 = pa.x;
+        b0 = pb.x;
+        c0 = pcc.x;
+        const uint32_t rd = SM32(wb + D + 4u);
+        uint32_t hmax = 0;
+        if (inc & INC_PHAZ)
+          hmax = max(max(SM32(wb + q2.z), SM32(wb + q2.w)), max(SM32(wb + q3.x), SM32(wb + q3.y)));
+        const uint32_t rg = SM32(pg + guard * 4u);
+        hr = max(max(max(pa.y, pb.y), pcc.y), max(max(rd, rg), hmax));
+      }
       const uint32_t pm = __shfl_sync(FULL, my_pred, guard);
 
       if ((inc & INC_ISSUE) == 0u || budget == 0u || t_next >= REBASE_AT) {  // rare path
@@ -611,7 +758,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             // payload (16 B); the payload is the lowest active lane's register
             const uint32_t src = (uint32_t)__ffs(mask) - 1u;
             const uint32_t plo = __shfl_sync(FULL, a0, src);
-            const uint32_t phi = __shfl_sync(FULL, ((aux >> 8) & 0xFFu) == 8u ? SM32(lb + A + ROW_BYTES) : 0u, src);
+            const uint32_t phi = __shfl_sync(FULL, ((aux >> 8) & 0xFFu) == 8u ? SM32(lv + A + RB) : 0u, src);
             if (slot && lane == 0) {
               uint8_t* r = slot + 16u + L.rec_bytes * n_rec;
               *reinterpret_cast<uint32_t*>(r) = ((aux & 0xFFu) << 24) | (((uint32_t)epoch + t_next) & 0xFFFFFFu);
@@ -637,11 +784,16 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         }
         if (t_next >= REBASE_AT) {  // keep every clock below 2^31: move the epoch to t_last
           const uint32_t delta = t_last;
-          for (uint32_t r = 0; r < Y.n_slots; r++) {
-            const uint32_t e = SM32(lb + r * ROW_BYTES + 4u);
-            SM32(lb + r * ROW_BYTES + 4u) = e > delta ? e - delta : 0u;
-          }
-          {
+          if constexpr (SPLIT) {
+            for (uint32_t i = lane; i < Y.n_ready; i += 32u) {
+              const uint32_t e = SM32(wb + Y.ready_off + 4u * i);
+              SM32(wb + Y.ready_off + 4u * i) = e > delta ? e - delta : 0u;
+            }
+          } else {
+            for (uint32_t r = 0; r < Y.n_slots; r++) {
+              const uint32_t e = SM32(lv + r * RB + 4u);
+              SM32(lv + r * RB + 4u) = e > delta ? e - delta : 0u;
+            }
             const uint32_t e = SM32(pg + lane * 4u);
             SM32(pg + lane * 4u) = e > delta ? e - delta : 0u;
           }
@@ -672,7 +824,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         const uint32_t ex = mask & (pm ^ gneg);
         if (L.cache_pass != 0u && op >= OP_LDG32 && op <= OP_STG64 && ex != 0u) {
           const uint64_t va_c =
-              ((uint64_t)a0 | ((uint64_t)SM32(lb + A + ROW_BYTES) << 32)) + (uint64_t)(int64_t)(int32_t)aux;
+              ((uint64_t)a0 | ((uint64_t)SM32(lv + A + RB) << 32)) + (uint64_t)(int64_t)(int32_t)aux;
           const uint64_t line = __shfl_sync(FULL, va_c, __ffs(ex) - 1) >> 7;
           const uint64_t step = c_off + (stop_at - left - budget);
           ks_cache_access* rec = L.cache_log + (uint64_t)gw * L.cache_cap + c_k;
@@ -710,10 +862,15 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       }
 
       // issue: in-order scoreboard (a3), epoch-relative 32-bit clock
-      const uint32_t t = max(max(max(t_next, pa.y), max(pb.y, pcc.y)), max(max(rd, rg), hmax));
+      const uint32_t t = max(t_next, SPLIT ? __reduce_max_sync(FULL, hr) : hr);
       const uint32_t wr = t + wlat;
-      if (inc & INC_RDEST) SM32(lb + D + 4u) = wr;  // register destination
-      if (inc & INC_PDEST) SM32(wb + q3.y) = wr;    // predicate destination
+      if constexpr (SPLIT) {
+        // the destination's ready word (a register row's, or the predicate's)
+        if (inc & (INC_RDEST | INC_PDEST)) st_shared_if(is_d8, s_wb + hk, wr);
+      } else {
+        if (inc & INC_RDEST) SM32(lv + D + 4u) = wr;  // register destination (every lane's pair)
+        if (inc & INC_PDEST) SM32(wb + q3.y) = wr;    // predicate destination
+      }
       max_ready = max(max_ready, wr);
       drain = max(drain, t + q3.z);
       t_last = t;
@@ -724,15 +881,15 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       const uint32_t exec = mask & (pm ^ gneg);
       const bool on = (exec >> lane) & 1u;
       // high words of 64-bit operands, loaded by the handlers that need them
-#define A64() ((uint64_t)a0 | ((uint64_t)SM32(lb + A + ROW_BYTES) << 32))
-#define B64() ((uint64_t)b0 | ((uint64_t)SM32(lb + B + ROW_BYTES) << 32))
-#define C64() ((uint64_t)c0 | ((uint64_t)SM32(lb + C + ROW_BYTES) << 32))
+#define A64() ((uint64_t)a0 | ((uint64_t)SM32(lv + A + RB) << 32))
+#define B64() ((uint64_t)b0 | ((uint64_t)SM32(lv + B + RB) << 32))
+#define C64() ((uint64_t)c0 | ((uint64_t)SM32(lv + C + RB) << 32))
 #define W32(v) st_shared_if(on, s_lane + D, (v))
 #define W64(v)                                                  \
   do {                                                          \
     const uint64_t v_ = (v);                                    \
     st_shared_if(on, s_lane + D, (uint32_t)v_);                 \
-    st_shared_if(on, s_lane + D + ROW_BYTES, (uint32_t)(v_ >> 32)); \
+    st_shared_if(on, s_lane + D + RB, (uint32_t)(v_ >> 32)); \
   } while (0)
 
       // The most frequent general-path ops take plain branches ahead of the
@@ -885,10 +1042,10 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             if (on) {
               if (wide) {
                 const uint64_t v = *reinterpret_cast<const uint64_t*>(ptr);
-                SM32(lb + D) = (uint32_t)v;
-                SM32(lb + D + ROW_BYTES) = (uint32_t)(v >> 32);
+                SM32(lv + D) = (uint32_t)v;
+                SM32(lv + D + RB) = (uint32_t)(v >> 32);
               } else {
-                SM32(lb + D) = *reinterpret_cast<const uint32_t*>(ptr);
+                SM32(lv + D) = *reinterpret_cast<const uint32_t*>(ptr);
               }
             }
           } else {
@@ -973,10 +1130,10 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             if (on) {
               if (wide) {
                 const uint2 v = *reinterpret_cast<const uint2*>(sp);
-                SM32(lb + D) = v.x;
-                SM32(lb + D + ROW_BYTES) = v.y;
+                SM32(lv + D) = v.x;
+                SM32(lv + D + RB) = v.y;
               } else {
-                SM32(lb + D) = *reinterpret_cast<const uint32_t*>(sp);
+                SM32(lv + D) = *reinterpret_cast<const uint32_t*>(sp);
               }
             }
           } else if (on && (31u - __clz(same_addr)) == lane) {  // the highest lane on an address wins
@@ -1140,11 +1297,16 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         // "none" (t_last + 1 == 0) until the next issue.
         cyc_floor = max(cyc_floor, epoch + (uint64_t)max(max(t_last + 1u, max_ready), drain));
         const uint64_t delta = rel - 1u;
-        for (uint32_t r = 0; r < Y.n_slots; r++) {
-          const uint32_t e = SM32(lb + r * ROW_BYTES + 4u);
-          SM32(lb + r * ROW_BYTES + 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
-        }
-        {
+        if constexpr (SPLIT) {
+          for (uint32_t i = lane; i < Y.n_ready; i += 32u) {
+            const uint32_t e = SM32(wb + Y.ready_off + 4u * i);
+            SM32(wb + Y.ready_off + 4u * i) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
+          }
+        } else {
+          for (uint32_t r = 0; r < Y.n_slots; r++) {
+            const uint32_t e = SM32(lv + r * RB + 4u);
+            SM32(lv + r * RB + 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
+          }
           const uint32_t e = SM32(pg + lane * 4u);
           SM32(pg + lane * 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
         }

@@ -34,6 +34,8 @@ struct SchedLaunch {
   uint32_t n_insn;       // entries, the exit sentinel not included
   uint32_t n_rows;       // register, constant and zero rows of a warp region
   uint32_t pred_off;     // region offset of the predicate ready table
+  uint32_t row_bytes;    // row size of the image's layout
+  uint32_t split;        // the image's layout: 0 PAIR, 1 SPLIT (DevInsn::x differs)
   uint32_t lat[KS_NUM_LAT_CLASSES];
   uint32_t grid, wpc, n_sm, ctas_per_sm, schedulers;
   const uint32_t* log;
@@ -101,12 +103,30 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     if (d.op == OP_BAR) flags |= F_BAR;
     if (d.inc & INC_MCLASS) flags |= F_MCLASS;
     if (d.inc & INC_MEMOP) flags |= F_MEMOP;
+    // predicate index of a predicate-table offset
     auto pred = [&](uint32_t off) { return (off - S.pred_off) / 4u; };
+    // the guard, the predicate sources and the predicate destination (31:
+    // none), from either layout's record
+    uint32_t guard, pa, pb, pc, pd;
+    if (S.split) {  // hazard halfwords 4..7: guard, sources; 3: the destination's term
+      guard = pred(d.x[2] & 0xFFFFu);
+      pa = pred(d.x[2] >> 16);
+      pb = pred(d.x[3] & 0xFFFFu);
+      pc = pred(d.x[3] >> 16);
+      pd = (d.inc & INC_PDEST) ? pred(d.x[1] >> 16) : 31u;
+    } else {        // guard, gneg, ha, hb, hc, hd
+      guard = d.x[0];
+      pa = pred(d.x[2]);
+      pb = pred(d.x[3]);
+      pc = pred(d.x[4]);
+      pd = pred(d.x[5]);
+    }
+    const uint32_t RB = S.row_bytes;
     Rec r;
-    r.q.x = (d.a / ROW_BYTES) | ((d.b / ROW_BYTES) << 16);
-    r.q.y = (d.c / ROW_BYTES) | ((d.d / ROW_BYTES) << 16);
-    r.q.z = d.guard | (pred(d.ha) << 8) | (pred(d.hb) << 16) | (pred(d.hc) << 24);
-    r.q.w = pred(d.hd) | (flags << 8) | (kind << 16);
+    r.q.x = (d.a / RB) | ((d.b / RB) << 16);
+    r.q.y = (d.c / RB) | ((d.d / RB) << 16);
+    r.q.z = guard | (pa << 8) | (pb << 16) | (pc << 24);
+    r.q.w = pd | (flags << 8) | (kind << 16);
     r.lat.x = (f & DEV_HAS_DEST) ? lat : 0u;
     r.lat.y = (f & DEV_IS_STORE) ? lat : 0u;
     r.lat.z = d.inc ? ((f & DEV_IS_CTRL) ? lat : 1u) : 0u;
@@ -376,6 +396,8 @@ int launch_sched(const KsLaunch& L, uint32_t n_rows, uint32_t n_sm, uint32_t cta
   S.n_insn = L.n_insn;
   S.n_rows = n_rows;
   S.pred_off = L.layout.pred_off;
+  S.row_bytes = L.layout.row_bytes;
+  S.split = L.layout.split;
   for (int i = 0; i < KS_NUM_LAT_CLASSES; i++) S.lat[i] = L.lat[i];
   S.grid = L.grid;
   S.wpc = L.wpc;

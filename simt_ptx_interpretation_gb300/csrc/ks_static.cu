@@ -87,26 +87,29 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   // shared memory / bar.sync: every warp of a CTA resident on one real CTA
   if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
   if (cfg.profile_buf && cfg.profile_bytes < k->code.size() * sizeof(ks_pc_profile)) return KS_ERR_ARG;
-  // ---- the program image must fit the static array ----
-  if (k->image.size() > KS_STATIC_IMAGE_BYTES) return KS_ERR_LIMIT;
+  // ---- the program image of the layout ks_simulate would take must fit the static array ----
+  const int lay = ks::pick_layout(*k, cfg.flags);
+  if (lay < 0) return lay;
+  const std::vector<uint8_t>& img = k->image[lay];
+  if (img.size() > KS_STATIC_IMAGE_BYTES) return KS_ERR_LIMIT;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KS_ERR_CUDA;
   if (static_setup(dev) != KS_OK) return KS_ERR_CUDA;
   void* image = g_static_addr[dev];
-  if (cudaMemcpyAsync(image, k->image.data(), k->image.size(), cudaMemcpyHostToDevice,
+  if (cudaMemcpyAsync(image, img.data(), img.size(), cudaMemcpyHostToDevice,
                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KS_ERR_CUDA;
 
   ks::KsLaunch L;
   std::memset(&L, 0, sizeof L);
   L.image = static_cast<const uint8_t*>(image);
-  L.image_bytes = (uint32_t)k->image.size();
+  L.image_bytes = (uint32_t)img.size();
   L.prog_bytes = k->prog_bytes;
   L.n_insn = (uint32_t)k->code.size();
   L.n_slots = k->n_slots;
-  L.n_crows = k->layout.n_crows;
-  L.layout = k->layout;
+  L.n_crows = k->layout[lay].n_crows;
+  L.layout = k->layout[lay];
   L.grid = grid;
   L.block = block;
   L.wpc = (block + 31u) / 32u;

@@ -29,8 +29,9 @@ class Job:
     """One batch item with its device buffers and outputs (stats filled with
     a sentinel so that an untouched record shows)."""
 
-    def __init__(self, w: wl.Workload, module=None, profile: bool = False):
+    def __init__(self, w: wl.Workload, module=None, profile: bool = False, layout: str = "auto"):
         self.w = w
+        self.layout = layout
         self.mod = module or ks.Module(w.ptx)
         self.dev = [(b.sim_base, torch.from_numpy(b.data.view(np.uint8)).cuda()) for b in w.fresh_buffers()]
         self.stats = torch.full((ks.stats_bytes(w.grid, w.block),), 0xA5, dtype=torch.uint8, device="cuda")
@@ -40,7 +41,7 @@ class Job:
                      if profile else None)
 
     def item(self) -> ks.BatchItem:
-        cfg = ks.Config(max_ts=self.w.max_ts, profile=self.prof)
+        cfg = ks.Config(max_ts=self.w.max_ts, profile=self.prof, layout=self.layout)
         return ks.BatchItem(self.mod, self.w.kernel, self.w.grid, self.w.block, self.w.params, self.dev, self.stats,
                             self.trace, cfg)
 
@@ -76,11 +77,14 @@ def run_batch(jobs) -> int:
     return n
 
 
-def test_plain_items_in_one_grid():
+@pytest.mark.parametrize("fuzz_layout", ["pair", "auto"])
+def test_plain_items_in_one_grid(fuzz_layout):
+    """Plain items of one layout share one real grid; the fuzz kernels run in
+    the SPLIT layout unless forced to PAIR, and then take a grid of their own."""
     jobs = [Job(wl.ffma(acc=1, iters=40, grid=6, block=128)), Job(wl.ffma(acc=8, iters=40, grid=6, block=128)),
             Job(wl.divergent(2, n=2048)), Job(wl.vector_add()), Job(wl.gather(4, n_out=1 << 12))]
-    jobs += [Job(wl.fuzz(i, grid=4, block=64)) for i in range(6)]
-    assert run_batch(jobs) == 1
+    jobs += [Job(wl.fuzz(i, grid=4, block=64), layout=fuzz_layout) for i in range(6)]
+    assert run_batch(jobs) == (1 if fuzz_layout == "pair" else 2)
     for j in jobs:
         j.check_oracle()
 
@@ -152,9 +156,11 @@ def many_registers(seed: int, n_regs: int = 60, grid: int = 16, block: int = 128
 def test_persistent_shape_when_one_wave_does_not_fit():
     """20 items of 64 warps with 60 registers each: two 8-warp CTAs of such
     warps do not fit an SM's shared memory, so the grid falls back to
-    persistent real warps sharing each item's warps."""
+    persistent real warps sharing each item's warps (in the PAIR layout: the
+    SPLIT one, which the library would pick for them, halves that state)."""
     ws = [many_registers(i) for i in range(20)]
-    jobs = [Job(w) for w in ws]
+    assert ks.Module(ws[0].ptx).layout("chain")[0] == "split"
+    jobs = [Job(w, layout="pair") for w in ws]
     run_batch(jobs)
     for j in jobs[::4]:
         j.check_oracle()

@@ -45,10 +45,10 @@ class Launch:
     """One workload's device buffers and outputs (stats and trace filled with a
     sentinel, so that a record the GPU never wrote shows)."""
 
-    def __init__(self, w: wl.Workload):
+    def __init__(self, w: wl.Workload, layout: str = "auto"):
         self.w = w
         self.mod = ks.Module(w.ptx)
-        self.cfg = ks.Config(max_ts=w.max_ts)
+        self.cfg = ks.Config(max_ts=w.max_ts, layout=layout)
         self.dev = [(b.sim_base, torch.from_numpy(b.data.view(np.uint8)).cuda()) for b in w.fresh_buffers()]
         self.stats = torch.full((ks.stats_bytes(w.grid, w.block),), 0xA5, dtype=torch.uint8, device="cuda")
         self.trace = (torch.full((ks.trace_bytes(w.grid, w.block, w.max_ts, self.mod.record_bytes(w.kernel)),),
@@ -93,8 +93,8 @@ def assert_whole(g: Launch, o, obufs):
     return gs
 
 
-def run_single(w: wl.Workload):
-    g = Launch(w)
+def run_single(w: wl.Workload, layout: str = "auto"):
+    g = Launch(w, layout)
     g.simulate()
     torch.cuda.synchronize()
     o, obufs = oracle_whole(w)
@@ -167,3 +167,27 @@ def test_fuzz_whole(part):
 def test_smem_reduce_whole():
     w = wl.smem_reduce(n=1 << 22, block=256)
     run_single(w)
+
+
+# ------------------------------------------- the other register layout ----
+
+def test_headline_sizes_in_the_other_layout():
+    """The library picks the PAIR layout for the FFMA pair, the gather and the
+    divergent workload and SPLIT for the fuzz kernels; each also runs whole in
+    the layout it does not pick (the batched FFMA pair as the benchmark times
+    it, gather s = 8, divergent k = 4, four fuzz kernels)."""
+    ws = [wl.ffma(acc=1), wl.ffma(acc=8)]
+    assert all(ks.Module(w.ptx).layout(w.kernel)[0] == "pair" for w in ws)
+    oracles = [oracle_whole(w) for w in ws]
+    jobs = [Launch(w, "split") for w in ws]
+    assert ks.simulate_batch([j.item() for j in jobs]) == 1
+    torch.cuda.synchronize()
+    for j, (o, obufs) in zip(jobs, oracles):
+        assert_whole(j, o, obufs)
+    del jobs
+    run_single(wl.gather(8), "split")
+    run_single(wl.divergent(4), "split")
+    for i in (0, 21, 42, 63):
+        w = wl.fuzz(i)
+        assert ks.Module(w.ptx).layout(w.kernel)[0] == "split"
+        run_single(w, "pair")

@@ -278,3 +278,37 @@ def test_static_entry_point_rejects_what_ks_simulate_rejects():
                             ctypes.byref(a["cfg"]), None))
         assert codes[0] == codes[1], f"{name}: ks_simulate {codes[0]}, ks_simulate_static {codes[1]}"
         assert codes[0] < 0, f"{name}: accepted ({codes[0]})"
+
+
+def test_register_layout_choice():
+    """ks_kernel_layout: the library picks PAIR for kernels whose warp state is
+    small or that run in CTA mode, SPLIT for plain kernels whose PAIR warp
+    state exceeds 12 KiB (the fuzz kernels); a forced layout is honoured, and
+    SPLIT warp state is about half the PAIR one (128-byte value rows and a
+    ready table instead of 256-byte (value, ready) rows)."""
+    for w in (wl.vector_add(), wl.ffma(acc=8, iters=8, grid=2), wl.gather(8, n_out=1 << 10),
+              wl.divergent(4, n=1 << 10)):
+        m = ks.Module(w.ptx)
+        lay, pair_bytes = m.layout(w.kernel)
+        assert lay == "pair" and pair_bytes <= 12 * 1024, w.name
+        assert m.layout(w.kernel, "pair") == ("pair", pair_bytes)
+        s_lay, split_bytes = m.layout(w.kernel, "split")
+        assert s_lay == "split" and split_bytes < 0.6 * pair_bytes, w.name
+    for i in range(0, 64, 7):
+        w = wl.fuzz(i)
+        m = ks.Module(w.ptx)
+        _, pair_bytes = m.layout(w.kernel, "pair")
+        lay, split_bytes = m.layout(w.kernel)
+        assert lay == "split" and pair_bytes > 12 * 1024 and split_bytes < 0.6 * pair_bytes, w.name
+    r = wl.smem_reduce(n=1 << 12, block=256)
+    m = ks.Module(r.ptx)
+    assert m.layout(r.kernel)[0] == "pair"
+    with pytest.raises(ks.KsError) as e:
+        m.layout(r.kernel, "split")  # CTA mode runs in PAIR only
+    assert e.value.code == -2
+    lib = _native.lib()
+    sp, rb = ctypes.c_uint32(), ctypes.c_uint32()
+    v = ks.Module(wl.vector_add().ptx)
+    assert lib.ks_kernel_layout(v._h, b"vector_add", 3, ctypes.byref(sp), ctypes.byref(rb)) == -3  # both flags
+    assert lib.ks_kernel_layout(v._h, b"vector_add", 4, ctypes.byref(sp), ctypes.byref(rb)) == -3  # unknown bit
+    assert lib.ks_kernel_layout(v._h, b"nope", 0, ctypes.byref(sp), ctypes.byref(rb)) == -5
