@@ -67,9 +67,14 @@
  *   - Shared memory and barriers (KernelScope backend doc, simulator/models.py
  *     Block: a shared array and a barrier per block; Warp.at_barrier): a
  *     kernel that declares .shared arrays or uses bar.sync runs CTA by CTA
- *     with every warp of the CTA resident (KS_ERR_LIMIT when the warps'
- *     interpreter state and the shared arrays exceed one SM's shared memory;
- *     blocks above 256 threads run a slower 1024-thread configuration).
+ *     with every warp of the CTA resident (blocks above 256 threads run a
+ *     slower 1024-thread configuration). When the warps' interpreter state
+ *     and the shared arrays exceed one SM's shared memory, the warps' state
+ *     moves to global memory (cached in L1/L2; the simulated shared arrays
+ *     stay on chip): slower again, and the call then takes a stream-ordered
+ *     device allocation of (real CTAs) x (warps per CTA) x (state per warp)
+ *     for the launch (cudaMallocAsync / cudaFreeAsync on its stream).
+ *     KS_ERR_LIMIT only when the shared arrays alone do not fit.
  *     Shared memory starts
  *     zeroed in every CTA. A warp that issues bar.sync (any active mask)
  *     stops; when every warp of the CTA has stopped at a barrier or finished,
@@ -337,10 +342,12 @@ int ks_profile_bytes(const ks_module* mod, const char* kernel, size_t* bytes);
  * Simulated faults do not fail the call: they are reported per warp in the
  * stats records (read them with ks_read_stats). Host-side errors: KS_ERR_ARG
  * (shapes, sizes, buffer table, undersized outputs), KS_ERR_NOT_FOUND,
- * KS_ERR_LIMIT (the real launch's shared memory does not fit — for a kernel
- * with shared memory or bar.sync, every warp of a CTA at once),
- * KS_ERR_CUDA. The first call on a device
- * uploads the module's program there (one allocation per module per device).
+ * KS_ERR_LIMIT (the real launch's shared memory does not fit: the program
+ * and parameters, and for a kernel with shared memory or bar.sync its shared
+ * arrays), KS_ERR_CUDA. The first call on a device
+ * uploads the module's program there (one allocation per module per device);
+ * a kernel with shared memory or bar.sync whose CTA's warp state does not fit
+ * on chip also takes a stream-ordered scratch allocation per call (above).
  * Simulations that share output or store-target buffers must not overlap in
  * time; others may be enqueued on different streams and run concurrently
  * (they share only the read-only program copy), which is how small grids
@@ -365,7 +372,9 @@ int ks_simulate(const ks_module* mod, const char* kernel, uint32_t grid, uint32_
  * into one file-scope device array of KS_STATIC_IMAGE_BYTES bytes, which every
  * GPU that loads the library holds until the process exits. Arguments,
  * outputs and errors are those of ks_simulate, plus KS_ERR_LIMIT when the
- * image exceeds KS_STATIC_IMAGE_BYTES (checked before any GPU work). The first
+ * image exceeds KS_STATIC_IMAGE_BYTES (checked before any GPU work) and for
+ * a kernel with shared memory or bar.sync whose CTA's warp state would need
+ * ks_simulate's global scratch. The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress)
  * and the device limits; make that first call before any stream capture.
  * Nothing in the array has to start at zero: each call writes every byte the

@@ -404,6 +404,11 @@ int launch_items(const std::vector<ks::KsLaunch>& Ls, const DevInfo& di, void* s
     return ((uint64_t)L.cta_mode << 40) | ((uint64_t)L.layout.split << 36) | ((uint64_t)ks::interp_form(L) << 32) |
            (L.cta_mode ? L.wpc : 0u);
   };
+  // a CTA-mode item whose warps' state does not fit shared memory runs alone
+  // (its regions in global scratch, ks::LaunchShape::greg)
+  auto alone = [&](const ks::KsLaunch& L) {
+    return L.cta_mode && ks::cta_mode_smem(L) > (size_t)di.max_smem;
+  };
   const size_t n_items = Ls.size();
   std::vector<char> done(n_items, 0);
   auto G = std::make_unique<ks::KsGrid<ks::KS_BATCH_ITEMS>>();
@@ -412,7 +417,7 @@ int launch_items(const std::vector<ks::KsLaunch>& Ls, const DevInfo& di, void* s
     G->n = 0;
     uint64_t warps = 0;
     for (size_t j = i; j < n_items && G->n < ks::KS_BATCH_ITEMS; j++) {
-      if (done[j] || key(Ls[j]) != key(Ls[i])) continue;
+      if (done[j] || key(Ls[j]) != key(Ls[i]) || (G->n > 0 && (alone(Ls[i]) || alone(Ls[j])))) continue;
       if (G->n > 0 && (Ls[j].n_warps > budget || warps + Ls[j].n_warps > budget)) continue;
       G->item[G->n++] = Ls[j];
       warps += Ls[j].n_warps;

@@ -325,6 +325,9 @@ struct KsLaunch {
   uint32_t* sched_log;
   uint32_t* sched_runs;
   uint32_t sched_cap;
+  // CTA mode with the warps' state in global memory (LaunchShape::greg): the
+  // regions of real CTA c at greg + c * wpc * region_bytes (set by launch_interp)
+  uint8_t* greg;
   alignas(16) uint8_t params[KS_MAX_PARAM_BYTES];
 };
 
@@ -361,16 +364,27 @@ struct LaunchShape {
   uint32_t warps_per_cta;
   uint32_t ctas;
   bool reg_capped;
+  // CTA mode whose warp regions do not fit the SM's shared memory with the
+  // simulated shared memory: the regions go to global memory, a scratch of
+  // ctas * wpc * region_bytes that launch_interp takes from the stream-ordered
+  // allocator for the launch
+  bool greg;
 };
 int choose_launch(const KsLaunch& L, int sms, int max_smem, LaunchShape* shape);
 int launch_interp(const KsLaunch& L, const LaunchShape& shape, void* stream);
 int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm,
-                     bool reg_capped = false);
+                     bool reg_capped = false, bool greg = false);
+// Shared memory of a CTA-mode launch with every warp region in it; above the
+// device limit the launch runs with its regions in global memory.
+size_t cta_mode_smem(const KsLaunch& L);
 // SPLIT-layout instantiations (ks_interp_split.cu; plain mode only): the
 // single-launch kernel of a form (0 lean, 1 instrumented, 2 issue-logging),
 // register-capped or not, and the batch kernel of a form.
 const void* interp_fn_split(int form, bool reg_capped);
 const void* batch_fn_split(int form);
+// CTA mode with the warps' state in global memory (ks_interp_greg.cu): the
+// 1024-thread single-launch kernel of a form.
+const void* interp_fn_greg(int form);
 // Instantiation form of a launch: 0 lean, 1 instrumented (cache model or
 // profile), 2 instrumented with the issue-run log (SM model).
 int interp_form(const KsLaunch& L);

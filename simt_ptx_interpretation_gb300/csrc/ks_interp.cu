@@ -73,7 +73,9 @@ static const void* interp_fn_of(int form) {
                      : (const void*)ks_interp_kernel<CTA, BIG, true, true, 1u, CAP>;
 }
 
-static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, int form, bool reg_capped, bool split) {
+static const void* interp_fn(bool cta, uint32_t real_warps_per_cta, int form, bool reg_capped, bool split,
+                             bool greg = false) {
+  if (greg) return interp_fn_greg(form);                // CTA mode, warp regions in global memory
   if (split) return interp_fn_split(form, reg_capped);  // plain mode only
   if (!cta) return reg_capped ? interp_fn_of<false, false, true>(form) : interp_fn_of<false, false, false>(form);
   if (real_warps_per_cta > 8) return interp_fn_of<true, true, false>(form);
@@ -107,6 +109,10 @@ static int ensure_attr() {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
             if (e != cudaSuccess) return (int)e;
           }
+  for (int form = 0; form < 3; form++) {
+    e = cudaFuncSetAttribute(interp_fn_greg(form), cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e != cudaSuccess) return (int)e;
+  }
   if (dev < 64) g_attr_done[dev] = 1;
   return 0;
 }
@@ -115,12 +121,12 @@ static int ensure_attr() {
 // size, asked of the runtime once per device and remembered (the shape
 // choice asks for several candidates at every launch).
 int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem, int* ctas_per_sm,
-                     bool reg_capped) {
+                     bool reg_capped, bool greg) {
   int e = ensure_attr();
   if (e) return e;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
-  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L), reg_capped, L.layout.split != 0);
+  const void* fn = interp_fn(L.cta_mode != 0, real_warps_per_cta, form_of(L), reg_capped, L.layout.split != 0, greg);
   static std::mutex mu;
   static std::map<std::tuple<int, const void*, uint32_t, size_t>, int> known;
   const auto key = std::make_tuple(dev, fn, real_warps_per_cta, smem);
@@ -139,12 +145,30 @@ int interp_occupancy(const KsLaunch& L, uint32_t real_warps_per_cta, size_t smem
   return 0;
 }
 
+size_t cta_mode_smem(const KsLaunch& L) {
+  return interp_smem_bytes(L.image_bytes, L.layout.region_bytes, L.wpc, L.shared_bytes);
+}
+
 int choose_launch(const KsLaunch& L, int sms, int max_smem, LaunchShape* shape) {
   const uint64_t n_warps = L.n_warps;
+  shape->greg = false;
   if (L.cta_mode) {
     // one real CTA per simulated CTA at a time, one real warp per simulated warp
-    const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, L.wpc, L.shared_bytes);
-    if (smem > (size_t)max_smem) return KS_ERR_LIMIT;
+    const size_t smem = cta_mode_smem(L);
+    if (smem > (size_t)max_smem) {
+      // the warps' state does not fit next to the simulated shared memory:
+      // regions in global memory, the rest in shared memory
+      const size_t smem_g = interp_smem_bytes(L.image_bytes, 0u, L.wpc, L.shared_bytes);
+      if (smem_g > (size_t)max_smem) return KS_ERR_LIMIT;
+      int per_sm = 0;
+      if (interp_occupancy(L, L.wpc, smem_g, &per_sm, false, true)) return KS_ERR_CUDA;
+      if (per_sm < 1) return KS_ERR_LIMIT;
+      shape->warps_per_cta = L.wpc;
+      shape->ctas = (uint32_t)std::min<uint64_t>(L.grid, (uint64_t)sms * (uint64_t)per_sm);
+      shape->reg_capped = false;
+      shape->greg = true;
+      return KS_OK;
+    }
     int per_sm = 0, per_sm_capped = 0;
     if (interp_occupancy(L, L.wpc, smem, &per_sm)) return KS_ERR_CUDA;
     // the register-capped form (blocks of up to 8 warps) where it holds
@@ -201,17 +225,29 @@ int choose_launch(const KsLaunch& L, int sms, int max_smem, LaunchShape* shape) 
 int launch_interp(const KsLaunch& L, const LaunchShape& shape, void* stream) {
   int e = ensure_attr();
   if (e) return e;
-  const size_t smem = interp_smem_bytes(L.image_bytes, L.layout.region_bytes, shape.warps_per_cta,
+  const size_t smem = interp_smem_bytes(L.image_bytes, shape.greg ? 0u : L.layout.region_bytes, shape.warps_per_cta,
                                        L.cta_mode ? L.shared_bytes : 0u);
   KsGrid<1> G;
   G.n = 1;
   G.cta_begin[0] = 0;
   G.cta_begin[1] = shape.ctas;
   G.item[0] = L;
+  void* scratch = nullptr;
+  if (shape.greg) {  // the warp regions of every real CTA, for this launch only
+    const size_t bytes = (size_t)shape.ctas * shape.warps_per_cta * L.layout.region_bytes;
+    e = (int)cudaMallocAsync(&scratch, bytes, (cudaStream_t)stream);
+    if (e) return e;
+    G.item[0].greg = static_cast<uint8_t*>(scratch);
+  }
   void* args[] = {&G};
-  return (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, shape.warps_per_cta, form_of(L), shape.reg_capped,
-                                         L.layout.split != 0),
-                               dim3(shape.ctas), dim3(shape.warps_per_cta * 32), args, smem, (cudaStream_t)stream);
+  e = (int)cudaLaunchKernel(interp_fn(L.cta_mode != 0, shape.warps_per_cta, form_of(L), shape.reg_capped,
+                                      L.layout.split != 0, shape.greg),
+                            dim3(shape.ctas), dim3(shape.warps_per_cta * 32), args, smem, (cudaStream_t)stream);
+  if (scratch) {
+    const int f = (int)cudaFreeAsync(scratch, (cudaStream_t)stream);
+    if (!e) e = f;
+  }
+  return e;
 }
 
 int launch_reduce_stats(const void* stats, uint64_t n_warps, void* acc_dev, void* stream) {

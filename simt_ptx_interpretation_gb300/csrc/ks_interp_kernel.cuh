@@ -189,6 +189,30 @@ __device__ __forceinline__ void st_pair(bool on, uint32_t addr, uint32_t v, uint
 #define SM32(off) (*reinterpret_cast<uint32_t*>(smem + (off)))
 #define SM2(off) (*reinterpret_cast<const uint2*>(smem + (off)))
 #define SM64(off) (*reinterpret_cast<uint64_t*>(smem + (off)))
+// warp-region accesses (shared memory, or global memory under GREG)
+#define RG32(off) (*reinterpret_cast<uint32_t*>(rg + (off)))
+#define RG2(off) (*reinterpret_cast<const uint2*>(rg + (off)))
+#define RG64(off) (*reinterpret_cast<uint64_t*>(rg + (off)))
+// predicated region stores at lv + x / wb + x, and a (value, ready) pair at lv + x
+#define ST_LANE_IF(p, x, v)                                    \
+  do {                                                         \
+    if constexpr (GREG) { if (p) RG32(lv + (x)) = (v); }       \
+    else st_shared_if((p), s_lane + (x), (v));                 \
+  } while (0)
+#define ST_WB_IF(p, x, v)                                      \
+  do {                                                         \
+    if constexpr (GREG) { if (p) RG32(wb + (x)) = (v); }       \
+    else st_shared_if((p), s_wb + (x), (v));                   \
+  } while (0)
+#define ST_LANE_PAIR(p, x, v, r)                               \
+  do {                                                         \
+    if constexpr (GREG) {                                      \
+      if (p) RG32(lv + (x)) = (v);                             \
+      RG32(lv + (x) + 4u) = (r);                               \
+    } else {                                                   \
+      st_pair((p), s_lane + (x), (v), (r));                    \
+    }                                                          \
+  } while (0)
 // this lane's scoreboard-term offset in the record at `rec` (a const uint4*):
 // halfword `hsel` (bytes) of its hazard words
 #define HZ_AT(rec, hsel) \
@@ -233,10 +257,16 @@ __device__ __forceinline__ uint64_t pack_entry(uint32_t pc, uint32_t rpc, uint32
 // registers, no spills, 21 warps an SM); CTA mode, three CTAs of up to 8
 // warps (80 registers, a few spills, 24 warps an SM).
 // SPLIT: the SPLIT register-file layout (plain mode only).
-template <bool CTA, bool BIG, bool INSTR, bool RUNLOG, uint32_t NB, bool CAP = false, bool SPLIT = false>
+// GREG: CTA mode whose warps' state does not fit the SM's shared memory: the
+// warp regions live in global memory (L.greg, one slice per real CTA, cached
+// in L1/L2), the program, parameters, barrier control and simulated shared
+// memory stay in shared memory (1024-thread form, single launches, PAIR).
+template <bool CTA, bool BIG, bool INSTR, bool RUNLOG, uint32_t NB, bool CAP = false, bool SPLIT = false,
+          bool GREG = false>
 __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ? 256 : 384)), CAP ? (CTA ? 3 : 2) : 1)
     ks_interp_kernel(const __grid_constant__ KsGrid<NB> G) {
   static_assert(!(SPLIT && CTA), "CTA mode runs in the PAIR layout");
+  static_assert(!GREG || (CTA && BIG && !SPLIT && NB == 1 && !CAP), "global warp state: single CTA-mode launches");
   uint32_t item = 0;
   if constexpr (NB > 1) {
     while (item + 1u < G.n && blockIdx.x >= G.cta_begin[item + 1u]) item++;  // uniform in the CTA
@@ -254,12 +284,20 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L.image_bytes + KS_MAX_PARAM_BYTES);
   CtaCtl* ctl = reinterpret_cast<CtaCtl*>(smem + L.image_bytes + KS_MAX_PARAM_BYTES + 16u);
   constexpr bool cta_mode = CTA;
-  const uint32_t sh_base = region0(L.image_bytes) + nwarps * Y.region_bytes;  // simulated shared memory
-  const uint32_t wb = region0(L.image_bytes) + wid * Y.region_bytes;  // this warp's region
+  // simulated shared memory, after the warp regions (GREG: no regions here)
+  const uint32_t sh_base = region0(L.image_bytes) + (GREG ? 0u : nwarps * Y.region_bytes);
+  // the warp regions: shared memory from region0, or (GREG) this CTA's slice
+  // of L.greg from 0; region accesses go through rg
+  uint8_t* const rg = GREG ? L.greg + (uint64_t)cta_x * nwarps * Y.region_bytes : smem;
+  const uint32_t wb = (GREG ? 0u : region0(L.image_bytes)) + wid * Y.region_bytes;  // this warp's region
   constexpr uint32_t RB = SPLIT ? ROW_SPLIT : ROW_PAIR;               // row bytes
   const uint32_t lv = wb + lane * (SPLIT ? 4u : 8u);                   // this lane's value in row 0
-  const uint32_t s_lane = cvta_shared(smem) + lv;                      // shared-window address of lv
+  [[maybe_unused]] const uint32_t s_lane = cvta_shared(smem) + lv;     // shared-window address of lv
   [[maybe_unused]] const uint32_t s_wb = cvta_shared(smem) + wb;       // ... of the region
+  // where a lane reads a destination's ready time: lane 0's pair (one
+  // broadcast word), or under GREG its own pair (global memory gives no
+  // order between one lane's store and another lane's load)
+  [[maybe_unused]] const uint32_t rdb = GREG ? lv : wb;
   [[maybe_unused]] const uint32_t pg = wb + Y.pred_off;                // predicate ready table
   // SPLIT: the scoreboard-term halfword this lane gathers: of four (fast and
   // mid loops: rows a, b, c, destination) or of eight (general path: then the
@@ -296,11 +334,11 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
   {
     const uint32_t* vals = reinterpret_cast<const uint32_t*>(smem + L.prog_bytes);
     if constexpr (SPLIT) {
-      for (uint32_t r = 0; r < Y.n_crows; r++) SM32(lv + Y.const_off + r * RB) = vals[r];
-      SM32(lv + Y.zero_off) = 0u;
+      for (uint32_t r = 0; r < Y.n_crows; r++) RG32(lv + Y.const_off + r * RB) = vals[r];
+      RG32(lv + Y.zero_off) = 0u;
     } else {  // (value, ready = 0) pairs
-      for (uint32_t r = 0; r < Y.n_crows; r++) SM64(lv + Y.const_off + r * RB) = (uint64_t)vals[r];
-      SM64(lv + Y.zero_off) = 0ull;
+      for (uint32_t r = 0; r < Y.n_crows; r++) RG64(lv + Y.const_off + r * RB) = (uint64_t)vals[r];
+      RG64(lv + Y.zero_off) = 0ull;
     }
   }
   __syncthreads();
@@ -335,11 +373,11 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
 
     // ---- warp set-up (a1): registers zero, predicates false, clock 0 ----
     if constexpr (SPLIT) {
-      for (uint32_t s = 0; s < Y.n_slots; s++) SM32(lv + s * RB) = 0u;
-      for (uint32_t i = lane; i < Y.n_ready; i += 32u) SM32(wb + Y.ready_off + 4u * i) = 0u;
+      for (uint32_t s = 0; s < Y.n_slots; s++) RG32(lv + s * RB) = 0u;
+      for (uint32_t i = lane; i < Y.n_ready; i += 32u) RG32(wb + Y.ready_off + 4u * i) = 0u;
     } else {
-      for (uint32_t s = 0; s < Y.n_slots; s++) SM64(lv + s * RB) = 0ull;
-      SM32(pg + lane * 4u) = 0u;
+      for (uint32_t s = 0; s < Y.n_slots; s++) RG64(lv + s * RB) = 0ull;
+      RG32(pg + lane * 4u) = 0u;
     }
     __syncwarp();
     uint32_t my_pred = (lane == 31u) ? 0xFFFFFFFFu : 0u;  // predicate 31 is always true
@@ -397,7 +435,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         FLUSH_THREADS();
         if (depth == 1) break;
         depth--;
-        const uint64_t e = SM64(wb + Y.stack_off + (depth - 1) * 8u);
+        const uint64_t e = RG64(wb + Y.stack_off + (depth - 1) * 8u);
         pc = (uint32_t)(e & 0xFFFFu);
         rpc = (uint32_t)((e >> 16) & 0xFFFFu);
         mask = (uint32_t)(e >> 32);
@@ -435,11 +473,11 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       if (runnable && (q1.w & INC_FUSE) && (q0.x == OP_SETP_U32 || q0.x == OP_SETP_S32 || q0.x == OP_SETP_F32)) {
         // operands (PAIR: with their ready times); SPLIT: this lane's term
         // offset and term
-        const uint2 sa2 = SPLIT ? make_uint2(SM32(lv + q1.x), 0u) : SM2(lv + q1.x);
-        const uint2 sb2 = SPLIT ? make_uint2(SM32(lv + q1.y), 0u) : SM2(lv + q1.y);
+        const uint2 sa2 = SPLIT ? make_uint2(RG32(lv + q1.x), 0u) : RG2(lv + q1.x);
+        const uint2 sb2 = SPLIT ? make_uint2(RG32(lv + q1.y), 0u) : RG2(lv + q1.y);
         const uint32_t sa = sa2.x, sb = sb2.x;
         const uint32_t hk = SPLIT ? HZ_AT(ip, hs4) : 0u;
-        const uint32_t hr = SPLIT ? SM32(wb + hk) : 0u;
+        const uint32_t hr = SPLIT ? RG32(wb + hk) : 0u;
         const uint32_t sop = q0.x, saux = q0.z, cmp = saux & 0xFFu, pd = (saux >> 8) & 0xFFu;
         bool lt, eq, gt;
         if (sop == OP_SETP_F32) {
@@ -458,11 +496,11 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         if constexpr (SPLIT) {
           t = max(t_next, __reduce_max_sync(FULL, hr));
           wr = t + q0.y;
-          st_shared_if(is_d4, s_wb + hk, wr);
+          ST_WB_IF(is_d4, hk, wr);
         } else {  // PAIR: ready times in the rows' pairs, the predicate's in q3.y (hd)
-          t = max(max(t_next, sa2.y), max(sb2.y, SM32(wb + q3.y)));
+          t = max(max(t_next, sa2.y), max(sb2.y, RG32(wb + q3.y)));
           wr = t + q0.y;
-          SM32(wb + q3.y) = wr;
+          RG32(wb + q3.y) = wr;
         }
         if (lane == pd) my_pred = (my_pred & ~mask) | (bal & mask);
         max_ready = max(max_ready, wr);
@@ -510,17 +548,17 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its operand
           // values, this lane's term offset and the latest term
           uint4 ka = q0, kb = q1;
-          uint32_t a = SM32(lv + kb.x), b = SM32(lv + kb.y), c = SM32(lv + kb.z);
+          uint32_t a = RG32(lv + kb.x), b = RG32(lv + kb.y), c = RG32(lv + kb.z);
           uint32_t hk = HZ_AT(ip, hs4);
-          uint32_t hm = __reduce_max_sync(FULL, SM32(wb + hk));
+          uint32_t hm = __reduce_max_sync(FULL, RG32(wb + hk));
           // instruction k+1's record and term offset (the last instruction is
           // never a fast op, so k+1 and k+2 stay within the program and its
           // exit sentinel)
           uint4 na = ip[4], nb = ip[5];
           uint32_t hk1 = HZ_AT(ip + 4, hs4);
           for (;;) {
-            uint32_t a1 = SM32(lv + nb.x), b1 = SM32(lv + nb.y), c1 = SM32(lv + nb.z);
-            const uint32_t r1 = SM32(wb + hk1);
+            uint32_t a1 = RG32(lv + nb.x), b1 = RG32(lv + nb.y), c1 = RG32(lv + nb.z);
+            const uint32_t r1 = RG32(wb + hk1);
             const uint4 ma = ip[8], mb = ip[9];
             const uint32_t hk2 = HZ_AT(ip + 8, hs4);
             const uint32_t t = max(t_next, hm);
@@ -531,8 +569,8 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a), __uint_as_float(b), __uint_as_float(cx)));
             const uint32_t ri = a * b + cx;
             const uint32_t res = ka.x == DOP_FPU ? rf : ri;
-            st_shared_if(on_all, s_lane + ka.w, res);
-            st_shared_if(is_d4, s_wb + hk, wr);  // the destination's ready word
+            ST_LANE_IF(on_all, ka.w, res);
+            ST_WB_IF(is_d4, hk, wr);  // the destination's ready word
             // forward k into k+1
             const uint32_t f = nb.w;
             a1 = ((f & INC_FWD_A) && on_all) ? res : a1;
@@ -562,14 +600,14 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           const bool on_all = (mask >> lane) & 1u;
           // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
           uint4 ka = q0, kb = q1;
-          uint2 a = SM2(lv + kb.x), b = SM2(lv + kb.y), c = SM2(lv + kb.z);
-          uint32_t rd = SM32(wb + ka.w + 4u);
+          uint2 a = RG2(lv + kb.x), b = RG2(lv + kb.y), c = RG2(lv + kb.z);
+          uint32_t rd = RG32(rdb + ka.w + 4u);
           // instruction k+1 (the last instruction is never a fast op, so k+1 and
           // k+2 stay within the program and its exit sentinel)
           uint4 na = ip[4], nb = ip[5];
           for (;;) {
-            uint2 a1 = SM2(lv + nb.x), b1 = SM2(lv + nb.y), c1 = SM2(lv + nb.z);
-            uint32_t rd1 = SM32(wb + na.w + 4u);
+            uint2 a1 = RG2(lv + nb.x), b1 = RG2(lv + nb.y), c1 = RG2(lv + nb.z);
+            uint32_t rd1 = RG32(rdb + na.w + 4u);
             const uint4 ma = ip[8], mb = ip[9];
             const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));
             const uint32_t wr = t + ka.y;
@@ -579,7 +617,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
             const uint32_t ri = a.x * b.x + cx;
             const uint32_t res = ka.x == DOP_FPU ? rf : ri;
-            st_pair(on_all, s_lane + ka.w, res, wr);
+            ST_LANE_PAIR(on_all, ka.w, res, wr);
             // forward k into k+1
             const uint32_t dk = ka.w;
             const bool fa = nb.x == dk, fb = nb.y == dk, fc = nb.z == dk;
@@ -624,13 +662,13 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           uint32_t a0, b0, c0, t;
           if constexpr (SPLIT) {
             hk1 = HZ_AT(mp + 4, hs4);
-            a0 = SM32(lv + kb.x);
-            b0 = SM32(lv + kb.y);
-            c0 = SM32(lv + kb.z);
-            t = max(t_next, __reduce_max_sync(FULL, SM32(wb + hk)));
+            a0 = RG32(lv + kb.x);
+            b0 = RG32(lv + kb.y);
+            c0 = RG32(lv + kb.z);
+            t = max(t_next, __reduce_max_sync(FULL, RG32(wb + hk)));
           } else {  // operands with their ready times, the destination's from lane 0's pair
-            const uint2 pa = SM2(lv + kb.x), pb = SM2(lv + kb.y), pcc = SM2(lv + kb.z);
-            const uint32_t rd = SM32(wb + ka.w + 4u);
+            const uint2 pa = RG2(lv + kb.x), pb = RG2(lv + kb.y), pcc = RG2(lv + kb.z);
+            const uint32_t rd = RG32(rdb + ka.w + 4u);
             t = max(max(t_next, pa.y), max(max(pb.y, pcc.y), rd));
             a0 = pa.x;
             b0 = pb.x;
@@ -643,8 +681,8 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           const uint32_t A = kb.x, B = kb.y;
           uint32_t lo = 0, hi = 0;
           bool wide = false;
-#define MA64() ((uint64_t)a0 | ((uint64_t)SM32(lv + A + RB) << 32))
-#define MB64() ((uint64_t)b0 | ((uint64_t)SM32(lv + B + RB) << 32))
+#define MA64() ((uint64_t)a0 | ((uint64_t)RG32(lv + A + RB) << 32))
+#define MB64() ((uint64_t)b0 | ((uint64_t)RG32(lv + B + RB) << 32))
 #define R64(v) do { const uint64_t v_ = (v); lo = (uint32_t)v_; hi = (uint32_t)(v_ >> 32); wide = true; } while (0)
           switch (__shfl_sync(FULL, ka.x, 0)) {
             case DOP_MADI: lo = a0 * aux + c0; break;
@@ -659,7 +697,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             case OP_ADD64: R64(MA64() + MB64()); break;
             case OP_SUB64: R64(MA64() - MB64()); break;
             case OP_MUL64: R64(MA64() * MB64()); break;
-            case OP_MAD64: R64(MA64() * MB64() + ((uint64_t)c0 | ((uint64_t)SM32(lv + kb.z + RB) << 32))); break;
+            case OP_MAD64: R64(MA64() * MB64() + ((uint64_t)c0 | ((uint64_t)RG32(lv + kb.z + RB) << 32))); break;
             case OP_AND32: lo = a0 & (b0 | aux); break;
             case OP_OR32: lo = a0 | (b0 | aux); break;
             case OP_XOR32: lo = a0 ^ (b0 | aux); break;
@@ -695,13 +733,13 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
 #undef MB64
 #undef R64
           if constexpr (SPLIT) {
-            st_shared_if(on, s_lane + D, lo);
-            st_shared_if(is_d4, s_wb + hk, wr);  // the destination's ready word
+            ST_LANE_IF(on, D, lo);
+            ST_WB_IF(is_d4, hk, wr);  // the destination's ready word
             hk = hk1;
           } else {
-            st_pair(on, s_lane + D, lo, wr);
+            ST_LANE_PAIR(on, D, lo, wr);
           }
-          st_shared_if(on && wide, s_lane + D + RB, hi);
+          ST_LANE_IF(on && wide, D + RB, hi);
           fuel--;
           mp += 4;
           ka = na;
@@ -732,21 +770,21 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       uint32_t hr;
       if constexpr (SPLIT) {
         hk = HZ_AT(ip, hs8);
-        a0 = SM32(lv + A);
-        b0 = SM32(lv + B);
-        c0 = SM32(lv + C);
-        hr = SM32(wb + hk);
+        a0 = RG32(lv + A);
+        b0 = RG32(lv + B);
+        c0 = RG32(lv + C);
+        hr = RG32(wb + hk);
       } else {
-        const uint2 pa = SM2(lv + A), pb = SM2(lv + B), pcc = SM2(lv + C);
+        const uint2 pa = RG2(lv + A), pb = RG2(lv + B), pcc = RG2(lv + C);
         a0 = pa.x;
         b0 = pb.x;
         c0 = pcc.x;
-        const uint32_t rd = SM32(wb + D + 4u);
+        const uint32_t rd = RG32(rdb + D + 4u);
         uint32_t hmax = 0;
         if (inc & INC_PHAZ)
-          hmax = max(max(SM32(wb + q2.z), SM32(wb + q2.w)), max(SM32(wb + q3.x), SM32(wb + q3.y)));
-        const uint32_t rg = SM32(pg + guard * 4u);
-        hr = max(max(max(pa.y, pb.y), pcc.y), max(max(rd, rg), hmax));
+          hmax = max(max(RG32(wb + q2.z), RG32(wb + q2.w)), max(RG32(wb + q3.x), RG32(wb + q3.y)));
+        const uint32_t rgd = RG32(pg + guard * 4u);  // the guard's ready time
+        hr = max(max(max(pa.y, pb.y), pcc.y), max(max(rd, rgd), hmax));
       }
       const uint32_t pm = __shfl_sync(FULL, my_pred, guard);
 
@@ -758,7 +796,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             // payload (16 B); the payload is the lowest active lane's register
             const uint32_t src = (uint32_t)__ffs(mask) - 1u;
             const uint32_t plo = __shfl_sync(FULL, a0, src);
-            const uint32_t phi = __shfl_sync(FULL, ((aux >> 8) & 0xFFu) == 8u ? SM32(lv + A + RB) : 0u, src);
+            const uint32_t phi = __shfl_sync(FULL, ((aux >> 8) & 0xFFu) == 8u ? RG32(lv + A + RB) : 0u, src);
             if (slot && lane == 0) {
               uint8_t* r = slot + 16u + L.rec_bytes * n_rec;
               *reinterpret_cast<uint32_t*>(r) = ((aux & 0xFFu) << 24) | (((uint32_t)epoch + t_next) & 0xFFFFFFu);
@@ -786,16 +824,16 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           const uint32_t delta = t_last;
           if constexpr (SPLIT) {
             for (uint32_t i = lane; i < Y.n_ready; i += 32u) {
-              const uint32_t e = SM32(wb + Y.ready_off + 4u * i);
-              SM32(wb + Y.ready_off + 4u * i) = e > delta ? e - delta : 0u;
+              const uint32_t e = RG32(wb + Y.ready_off + 4u * i);
+              RG32(wb + Y.ready_off + 4u * i) = e > delta ? e - delta : 0u;
             }
           } else {
             for (uint32_t r = 0; r < Y.n_slots; r++) {
-              const uint32_t e = SM32(lv + r * RB + 4u);
-              SM32(lv + r * RB + 4u) = e > delta ? e - delta : 0u;
+              const uint32_t e = RG32(lv + r * RB + 4u);
+              RG32(lv + r * RB + 4u) = e > delta ? e - delta : 0u;
             }
-            const uint32_t e = SM32(pg + lane * 4u);
-            SM32(pg + lane * 4u) = e > delta ? e - delta : 0u;
+            const uint32_t e = RG32(pg + lane * 4u);
+            RG32(pg + lane * 4u) = e > delta ? e - delta : 0u;
           }
           __syncwarp();
           epoch += delta;
@@ -824,7 +862,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         const uint32_t ex = mask & (pm ^ gneg);
         if (L.cache_pass != 0u && op >= OP_LDG32 && op <= OP_STG64 && ex != 0u) {
           const uint64_t va_c =
-              ((uint64_t)a0 | ((uint64_t)SM32(lv + A + RB) << 32)) + (uint64_t)(int64_t)(int32_t)aux;
+              ((uint64_t)a0 | ((uint64_t)RG32(lv + A + RB) << 32)) + (uint64_t)(int64_t)(int32_t)aux;
           const uint64_t line = __shfl_sync(FULL, va_c, __ffs(ex) - 1) >> 7;
           const uint64_t step = c_off + (stop_at - left - budget);
           ks_cache_access* rec = L.cache_log + (uint64_t)gw * L.cache_cap + c_k;
@@ -866,10 +904,10 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       const uint32_t wr = t + wlat;
       if constexpr (SPLIT) {
         // the destination's ready word (a register row's, or the predicate's)
-        if (inc & (INC_RDEST | INC_PDEST)) st_shared_if(is_d8, s_wb + hk, wr);
+        if (inc & (INC_RDEST | INC_PDEST)) ST_WB_IF(is_d8, hk, wr);
       } else {
-        if (inc & INC_RDEST) SM32(lv + D + 4u) = wr;  // register destination (every lane's pair)
-        if (inc & INC_PDEST) SM32(wb + q3.y) = wr;    // predicate destination
+        if (inc & INC_RDEST) RG32(lv + D + 4u) = wr;  // register destination (every lane's pair)
+        if (inc & INC_PDEST) RG32(wb + q3.y) = wr;    // predicate destination
       }
       max_ready = max(max_ready, wr);
       drain = max(drain, t + q3.z);
@@ -881,15 +919,15 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       const uint32_t exec = mask & (pm ^ gneg);
       const bool on = (exec >> lane) & 1u;
       // high words of 64-bit operands, loaded by the handlers that need them
-#define A64() ((uint64_t)a0 | ((uint64_t)SM32(lv + A + RB) << 32))
-#define B64() ((uint64_t)b0 | ((uint64_t)SM32(lv + B + RB) << 32))
-#define C64() ((uint64_t)c0 | ((uint64_t)SM32(lv + C + RB) << 32))
-#define W32(v) st_shared_if(on, s_lane + D, (v))
+#define A64() ((uint64_t)a0 | ((uint64_t)RG32(lv + A + RB) << 32))
+#define B64() ((uint64_t)b0 | ((uint64_t)RG32(lv + B + RB) << 32))
+#define C64() ((uint64_t)c0 | ((uint64_t)RG32(lv + C + RB) << 32))
+#define W32(v) ST_LANE_IF(on, D, (v))
 #define W64(v)                                                  \
   do {                                                          \
     const uint64_t v_ = (v);                                    \
-    st_shared_if(on, s_lane + D, (uint32_t)v_);                 \
-    st_shared_if(on, s_lane + D + RB, (uint32_t)(v_ >> 32)); \
+    ST_LANE_IF(on, D, (uint32_t)v_);                            \
+    ST_LANE_IF(on, D + RB, (uint32_t)(v_ >> 32));            \
   } while (0)
 
       // The most frequent general-path ops take plain branches ahead of the
@@ -918,22 +956,22 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             if (rpc == R) {
               n = depth - 1;  // the top already waits at R below: replace it
             } else {
-              SM64(sbase + (depth - 1) * 8u) = pack_entry(R, rpc, mask);
+              RG64(sbase + (depth - 1) * 8u) = pack_entry(R, rpc, mask);
             }
             if (target != R) {
               if (n >= L.stack_depth) { status = KS_ST_SIMT_STACK; break; }
-              SM64(sbase + n * 8u) = pack_entry(target, R, taken);
+              RG64(sbase + n * 8u) = pack_entry(target, R, taken);
               n++;
             }
             if (pc + 1 != R) {
               if (n >= L.stack_depth) { status = KS_ST_SIMT_STACK; break; }
-              SM64(sbase + n * 8u) = pack_entry(pc + 1, R, fall);
+              RG64(sbase + n * 8u) = pack_entry(pc + 1, R, fall);
               n++;
             }
             if (n == 0) { depth = 1; pc = rpc = exit_pc; mask = 0; break; }
             depth = n;
             max_depth = max(max_depth, depth);
-            const uint64_t e = SM64(sbase + (depth - 1) * 8u);
+            const uint64_t e = RG64(sbase + (depth - 1) * 8u);
             pc = (uint32_t)(e & 0xFFFFu);
             rpc = (uint32_t)((e >> 16) & 0xFFFFu);
             mask = (uint32_t)(e >> 32);
@@ -1042,10 +1080,10 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             if (on) {
               if (wide) {
                 const uint64_t v = *reinterpret_cast<const uint64_t*>(ptr);
-                SM32(lv + D) = (uint32_t)v;
-                SM32(lv + D + RB) = (uint32_t)(v >> 32);
+                RG32(lv + D) = (uint32_t)v;
+                RG32(lv + D + RB) = (uint32_t)(v >> 32);
               } else {
-                SM32(lv + D) = *reinterpret_cast<const uint32_t*>(ptr);
+                RG32(lv + D) = *reinterpret_cast<const uint32_t*>(ptr);
               }
             }
           } else {
@@ -1080,7 +1118,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           FLUSH_THREADS();
           for (uint32_t i = 0; i + 1 < depth; i++) {
             const uint32_t at = wb + Y.stack_off + i * 8u;
-            SM64(at) = SM64(at) & ~((uint64_t)exec << 32);
+            RG64(at) = RG64(at) & ~((uint64_t)exec << 32);
           }
           mask &= ~exec;
           if constexpr (RUNLOG) live &= ~exec;
@@ -1130,10 +1168,10 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             if (on) {
               if (wide) {
                 const uint2 v = *reinterpret_cast<const uint2*>(sp);
-                SM32(lv + D) = v.x;
-                SM32(lv + D + RB) = v.y;
+                RG32(lv + D) = v.x;
+                RG32(lv + D + RB) = v.y;
               } else {
-                SM32(lv + D) = *reinterpret_cast<const uint32_t*>(sp);
+                RG32(lv + D) = *reinterpret_cast<const uint32_t*>(sp);
               }
             }
           } else if (on && (31u - __clz(same_addr)) == lane) {  // the highest lane on an address wins
@@ -1299,16 +1337,16 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
         const uint64_t delta = rel - 1u;
         if constexpr (SPLIT) {
           for (uint32_t i = lane; i < Y.n_ready; i += 32u) {
-            const uint32_t e = SM32(wb + Y.ready_off + 4u * i);
-            SM32(wb + Y.ready_off + 4u * i) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
+            const uint32_t e = RG32(wb + Y.ready_off + 4u * i);
+            RG32(wb + Y.ready_off + 4u * i) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
           }
         } else {
           for (uint32_t r = 0; r < Y.n_slots; r++) {
-            const uint32_t e = SM32(lv + r * RB + 4u);
-            SM32(lv + r * RB + 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
+            const uint32_t e = RG32(lv + r * RB + 4u);
+            RG32(lv + r * RB + 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
           }
-          const uint32_t e = SM32(pg + lane * 4u);
-          SM32(pg + lane * 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
+          const uint32_t e = RG32(pg + lane * 4u);
+          RG32(pg + lane * 4u) = (uint64_t)e > delta ? (uint32_t)(e - delta) : 0u;
         }
         __syncwarp();
         epoch += delta;

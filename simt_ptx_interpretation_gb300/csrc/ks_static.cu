@@ -96,6 +96,11 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KS_ERR_CUDA;
   if (static_setup(dev) != KS_OK) return KS_ERR_CUDA;
+  // a kernel with shared memory or bar.sync whose CTA's warp state does not
+  // fit on chip needs ks_simulate's global scratch: refused before any GPU work
+  if (k->cta_mode() && ks::interp_smem_bytes((uint32_t)img.size(), k->layout[lay].region_bytes, (block + 31u) / 32u,
+                                             k->shared_bytes) > (size_t)g_static_smem[dev])
+    return KS_ERR_LIMIT;
   void* image = g_static_addr[dev];
   if (cudaMemcpyAsync(image, img.data(), img.size(), cudaMemcpyHostToDevice,
                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -146,6 +151,8 @@ extern "C" int ks_simulate_static(const ks_module* mod, const char* kernel, uint
   ks::LaunchShape shape;
   const int rc = ks::choose_launch(L, g_static_sms[dev], g_static_smem[dev], &shape);
   if (rc != KS_OK) return rc;
+  // a CTA whose warps' state needs global scratch cannot run without an allocation
+  if (shape.greg) return KS_ERR_LIMIT;
   if (ks::launch_interp(L, shape, stream) != 0) return KS_ERR_CUDA;
   return KS_OK;
 }

@@ -217,6 +217,12 @@ def test_large_blocks(block):
     wl_check(wl.smem_reduce(n=block * 4, block=block))
 
 
+def test_cta_warp_state_in_global_memory():
+    """A random shared program at block 1024, whose warps' state lives in
+    global memory: both passes of the hit model equal the oracle's stepper."""
+    wl_check(wl.fuzz_shared(0, grid=3, block=1024), cache=ks.CacheConfig(max_accesses_per_warp=4096))
+
+
 def _cached_job(w: wl.Workload, cache: ks.CacheConfig):
     mod = ks.Module(w.ptx)
     dev = [(b.sim_base, torch.from_numpy(b.data.view(np.uint8)).cuda()) for b in w.fresh_buffers()]

@@ -152,3 +152,11 @@ def test_large_blocks(block):
     w = wl.smem_reduce(n=block * 5, block=block)
     check(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in w.fresh_buffers()],
           n_sm=2, schedulers=4, max_ts=w.max_ts)
+
+
+def test_cta_warp_state_in_global_memory():
+    """A random shared program at block 1024, whose warps' state lives in
+    global memory: the issue log and the replay equal the oracle's SM model."""
+    w = wl.fuzz_shared(1, grid=3, block=1024)
+    check(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in w.fresh_buffers()],
+          n_sm=2, schedulers=4, max_ts=w.max_ts)

@@ -234,14 +234,81 @@ def test_lean_kernel_at_large_blocks(block):
     assert np.array_equal(g.buffers[0].view(np.uint32), np.repeat(2 * np.arange(grid, dtype=np.uint32), block))
 
 
-def test_cta_mode_reports_state_that_does_not_fit():
-    # 32 warps of a random shared program's interpreter state (about 11 KB a
-    # warp) plus its shared arrays exceed an SM's shared memory
+def cta_state_exceeds_smem(w: wl.Workload) -> bool:
+    """The PAIR warp state of one CTA alone exceeds the SM's shared memory."""
+    region = ks.Module(w.ptx).layout(w.kernel)[1]
+    return region * ((w.block + 31) // 32) > torch.cuda.get_device_properties(0).shared_memory_per_block_optin
+
+
+@pytest.mark.parametrize("i", [0, 1, 2, 7])
+def test_cta_warp_state_in_global_memory(i):
+    """Random shared programs at block 1024: 32 warps of about 11 KB of
+    interpreter state each exceed an SM's shared memory, so the warps' state
+    moves to global memory (the simulated shared arrays stay on chip); every
+    warp's record, trace slot and byte of memory equals the oracle's."""
+    w = wl.fuzz_shared(i, grid=4, block=1024)
+    assert cta_state_exceeds_smem(w)
+    _parity.assert_parity(w)
+
+
+def test_cta_warp_state_in_global_memory_far_release():
+    """As test_barrier_release_far_ahead_of_a_warps_clock, at block 1024 with
+    40 more registers per thread: the barrier release moves the epochs of the
+    waiting warps' clocks in global memory."""
+    loads = "\n".join("    ld.global.u64 %rd2, [%rd2];" for _ in range(70))
+    pads = "\n".join(f"    add.u32 %x{i}, %r1, {i};" for i in range(40))
+    sums = "\n".join(f"    add.u32 %r2, %r2, %x{i};" for i in range(40))
+    ptx = wl.HEADER + f""".visible .entry farbig(.param .u64 buf, .param .u64 out)
+{{
+    .reg .pred %p<2>;
+    .reg .b32 %r<3>;
+    .reg .b32 %x<40>;
+    .reg .b64 %rd<6>;
+    ld.param.u64 %rd2, [buf];
+    mov.u32 %r1, %tid.x;
+{pads}
+    setp.lt.u32 %p1, %r1, 32;
+    @!%p1 bra SKIP;
+{loads}
+SKIP:
+    bar.sync 0;
+    mov.u32 %r2, 0;
+{sums}
+    ld.param.u64 %rd3, [out];
+    mov.u32 %r0, %ctaid.x;
+    mad.lo.s32 %r0, %r0, 1024, %r1;
+    cvt.u64.u32 %rd4, %r0;
+    shl.b64 %rd4, %rd4, 2;
+    add.s64 %rd5, %rd3, %rd4;
+    st.global.u32 [%rd5], %r2;
+    ret;
+}}
+"""
+    buf = np.zeros(2, dtype=np.uint64)
+    out = np.zeros(2 * 1024, dtype=np.uint32)
+    bufs = wl.place([("buf", buf, False), ("out", out, True)])
+    buf[0] = bufs[0].sim_base  # every load reads the buffer's own address
+    w = wl.Workload("farbig", ptx, "farbig", 2, 1024,
+                    wl.pack_params([("u64", bufs[0].sim_base), ("u64", bufs[1].sim_base)]), bufs)
+    assert cta_state_exceeds_smem(w)
+    lat = list(ks.DEFAULT_LAT)
+    lat[2] = 1 << 24
+    g, _ = _parity.assert_parity(w, cfg=ks.Config(lat=tuple(lat)))
+    assert int(g.stats["cycles"][1]) > 1 << 30
+    tid = np.arange(1024, dtype=np.uint64)
+    want = (40 * tid + sum(range(40))) & 0xFFFFFFFF
+    assert np.array_equal(g.buffers[1].view(np.uint32), np.tile(want.astype(np.uint32), 2))
+
+
+def test_static_entry_refuses_global_warp_state():
+    """The allocation-free entry point cannot take the global scratch such a
+    launch needs: KS_ERR_LIMIT before any GPU work."""
     w = wl.fuzz_shared(0, grid=2, block=1024)
     m = ks.Module(w.ptx)
+    dev = [(b.sim_base, torch.zeros(b.data.nbytes, dtype=torch.uint8).cuda()) for b in w.buffers]
+    stats = torch.zeros(ks.stats_bytes(w.grid, w.block), dtype=torch.uint8, device="cuda")
     with pytest.raises(ks.KsError) as e:
-        ks.run(m, w.kernel, w.grid, w.block, w.params,
-               [(b.sim_base, torch.zeros(b.data.nbytes, dtype=torch.uint8).cuda()) for b in w.buffers])
+        ks.simulate_static(m, w.kernel, w.grid, w.block, w.params, dev, stats)
     assert e.value.code == -6
 
 
