@@ -571,11 +571,12 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             const uint32_t res = ka.x == DOP_FPU ? rf : ri;
             ST_LANE_IF(on_all, ka.w, res);
             ST_WB_IF(is_d4, hk, wr);  // the destination's ready word
-            // forward k into k+1
+            // forward k into k+1 (in every lane: a lane outside the mask
+            // stores nothing during the run)
             const uint32_t f = nb.w;
-            a1 = ((f & INC_FWD_A) && on_all) ? res : a1;
-            b1 = ((f & INC_FWD_B) && on_all) ? res : b1;
-            c1 = ((f & INC_FWD_C) && on_all) ? res : c1;
+            a1 = (f & INC_FWD_A) ? res : a1;
+            b1 = (f & INC_FWD_B) ? res : b1;
+            c1 = (f & INC_FWD_C) ? res : c1;
             const uint32_t hm1 = __reduce_max_sync(FULL, r1);
             hm = (f & INC_FWD_T) ? max(hm1, wr) : hm1;
             ka = na;
@@ -618,16 +619,18 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             const uint32_t ri = a.x * b.x + cx;
             const uint32_t res = ka.x == DOP_FPU ? rf : ri;
             ST_LANE_PAIR(on_all, ka.w, res, wr);
-            // forward k into k+1
-            const uint32_t dk = ka.w;
-            const bool fa = nb.x == dk, fb = nb.y == dk, fc = nb.z == dk;
-            a1.x = (fa && on_all) ? res : a1.x;
-            a1.y = fa ? wr : a1.y;
-            b1.x = (fb && on_all) ? res : b1.x;
-            b1.y = fb ? wr : b1.y;
-            c1.x = (fc && on_all) ? res : c1.x;
-            c1.y = fc ? wr : c1.y;
-            rd1 = na.w == dk ? wr : rd1;
+            // forward k into k+1 (the decoder's INC_FWD_* flags of k+1): the
+            // value into each operand that is k's destination -- in every
+            // lane: a lane outside the mask stores nothing during the run, so
+            // what it computes from a forwarded value is never seen -- and
+            // k's ready time into k+1's scoreboard, through the destination
+            // term (every term of k+1 is maxed together, and a stale entry of
+            // k's destination is never later than k's own ready time)
+            const uint32_t f = nb.w;
+            a1.x = (f & INC_FWD_A) ? res : a1.x;
+            b1.x = (f & INC_FWD_B) ? res : b1.x;
+            c1.x = (f & INC_FWD_C) ? res : c1.x;
+            rd1 = (f & INC_FWD_T) ? max(rd1, wr) : rd1;
             ka = na;
             kb = nb;
             na = ma;
