@@ -36,6 +36,7 @@ struct SchedLaunch {
   uint32_t pred_off;     // region offset of the predicate ready table
   uint32_t row_bytes;    // row size of the image's layout
   uint32_t split;        // the image's layout: 0 PAIR, 1 SPLIT (DevInsn::x differs)
+  uint32_t cta_mode;     // the kernel has shared memory or bar.sync
   uint32_t lat[KS_NUM_LAT_CLASSES];
   uint32_t grid, wpc, n_sm, ctas_per_sm, schedulers;
   const uint32_t* log;
@@ -60,6 +61,7 @@ constexpr uint32_t F_ISSUE = 1, F_RDEST = 2, F_PDEST = 4, F_PHAZ = 8, F_BAR = 16
 
 struct Lane {
   uint32_t state, gw, cta_slot;
+  uint32_t rank;                     // order of gw among the occupied lanes of my scheduler
   uint32_t pc, run_left, k, n_runs;  // next entry to issue; entries left in its run; next run index
   uint32_t t_next, t_last, max_ready, drain, base, start, e, bind, arrival, end;
   Rec r;                             // the record of the next entry
@@ -81,6 +83,11 @@ __device__ __forceinline__ uint32_t kind_at(uint64_t v, uint32_t e) {
   return (uint32_t)v == e ? (uint32_t)(v >> 32) : K_EXEC;
 }
 
+// RUN_AHEAD: the form for kernels without barriers whose CTAs all reach
+// their SMs at the start (every CTA slot filled at once, none left), where a
+// warp alone on its scheduler runs ahead (below); the other form keeps the
+// step loop alone (its code shape costs the other workloads 13 %).
+template <bool RUN_AHEAD>
 __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ SchedLaunch S) {
   extern __shared__ __align__(16) uint8_t sm[];
   const uint32_t lane = threadIdx.x;
@@ -150,6 +157,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
   uint32_t status = 0;
   uint64_t sm_issued = 0;
   uint32_t sm_end = 0, ctas = 0;
+  bool ranks_dirty = true;  // a CTA was loaded since the ranks were taken
 
   // position at the next issued entry of the runs (its record in L.r);
   // false when none is left
@@ -215,6 +223,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
   };
   // lanes of slot c (mine) load their warps of the SM's next CTA at cycle t0
   auto load_cta = [&](bool mine, uint32_t t0) {
+    ranks_dirty = true;
     const uint32_t k = next_cta_k++;
     const uint64_t cta = (uint64_t)s_id + (uint64_t)k * S.n_sm;
     if (!mine) return;
@@ -272,6 +281,34 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     }
   };
 
+  // This lane's warp issues its next entry at cycle T: the waits it stood
+  // (not selected, or stalled on what bound its scoreboard time), its
+  // destination's ready entry, its clocks and counts. Returns the entry's
+  // flags; the memory-class label and memory bookkeeping are the caller's.
+  auto issue = [&](uint32_t T) -> uint32_t {
+    L.not_selected += T - L.e;
+    if (L.e > L.base) {
+      const uint32_t d = L.e - L.base;
+      if (L.bind == K_MEM) L.st_mem += d;
+      else if (L.bind == K_MATH) L.st_math += d;
+      else L.st_exec += d;
+    }
+    const uint4 q = L.r.q, lt = L.r.lat;
+    const uint32_t flags = (q.w >> 8) & 0xFFu;
+    const uint64_t wr = T + lt.x;
+    const uint64_t entry = wr | ((uint64_t)(q.w >> 16) << 32);
+    if (flags & F_RDEST) ready[q.y >> 16] = entry;
+    if (flags & F_PDEST) ready[S.n_rows + (q.w & 0xFFu)] = entry;
+    L.max_ready = max(L.max_ready, (uint32_t)wr);
+    L.drain = max(L.drain, T + lt.y);
+    L.t_last = T;
+    L.t_next = T + lt.z;
+    L.base = T + 1u;
+    L.issued++;
+    if (L.div) L.diverged++;
+    return flags;
+  };
+
   for (uint32_t c = 0; c < S.ctas_per_sm; c++) {
     const bool mine = lane < slots && L.cta_slot == c;
     load_cta(mine, 0u);
@@ -286,6 +323,8 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
   // each other. With a zero barrier latency a release takes effect in the
   // same cycle, and the schedulers take turns one issue at a time.
   const bool one_at_a_time = S.lat[KS_LAT_BAR] == 0u;
+  const uint32_t per = 32u / S.schedulers;  // lanes of one scheduler
+  const bool run_ahead = RUN_AHEAD && !one_at_a_time && S.cta_mode == 0u;
   for (;;) {
     // the earliest offer, then per scheduler the lowest warp id offering it
     const uint32_t cand = L.state == ST_RUNNING ? max(L.e, port) : NEVER;
@@ -296,45 +335,31 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
       break;
     }
     const bool at_T = cand == T;
-    uint32_t gmin;
-    if (one_at_a_time || S.schedulers == 1u) {
-      gmin = __reduce_min_sync(FULL, at_T ? L.gw : NEVER);
+    bool win;
+    if (one_at_a_time) {
+      win = at_T && L.gw == __reduce_min_sync(FULL, at_T ? L.gw : NEVER);
     } else {
-      const uint32_t g = at_T ? L.gw : NEVER;
-      const uint32_t m0 = __reduce_min_sync(FULL, my_sched == 0u ? g : NEVER);
-      const uint32_t m1 = __reduce_min_sync(FULL, my_sched == 1u ? g : NEVER);
-      uint32_t m2 = NEVER, m3 = NEVER;
-      if (S.schedulers == 4u) {
-        m2 = __reduce_min_sync(FULL, my_sched == 2u ? g : NEVER);
-        m3 = __reduce_min_sync(FULL, my_sched == 3u ? g : NEVER);
+      // every scheduler's lowest warp id at T in one reduction: lane l sets
+      // bit (scheduler * per + rank) where per = 32 / schedulers lanes share
+      // a scheduler and rank orders their warp ids
+      if (ranks_dirty) {
+        const uint32_t key = L.state != ST_EMPTY ? L.gw : NEVER;
+        uint32_t r = 0;
+        for (uint32_t j = 0; j < per; j++) r += __shfl_sync(FULL, key, my_sched + j * S.schedulers) < key ? 1u : 0u;
+        L.rank = r;
+        ranks_dirty = false;
       }
-      gmin = my_sched == 0u ? m0 : my_sched == 1u ? m1 : my_sched == 2u ? m2 : m3;
+      const uint32_t all = __reduce_or_sync(FULL, at_T ? 1u << (my_sched * per + L.rank) : 0u);
+      const uint32_t mine_bits = per == 32u ? all : (all >> (my_sched * per)) & ((1u << per) - 1u);
+      win = at_T && (uint32_t)(__ffs(mine_bits) - 1) == L.rank;
     }
-    const bool win = at_T && L.gw == gmin;
     // warps of this SM with a memory operation pending at T (issued earlier,
     // not yet complete), for the memory-throttle label
     const uint32_t pending = __ballot_sync(FULL, lane < slots && L.state != ST_EMPTY && L.mem_pending(T));
     uint32_t ev = 0;  // arrived at a barrier or finished
     if (win) {
-      L.not_selected += T - L.e;
-      if (L.e > L.base) {
-        const uint32_t d = L.e - L.base;
-        if (L.bind == K_MEM) L.st_mem += d;
-        else if (L.bind == K_MATH) L.st_math += d;
-        else L.st_exec += d;
-      }
-      const uint4 q = L.r.q, lt = L.r.lat;
-      const uint32_t flags = (q.w >> 8) & 0xFFu;
-      const uint64_t wr = T + lt.x;
-      const uint64_t entry = wr | ((uint64_t)(q.w >> 16) << 32);
-      if (flags & F_RDEST) ready[q.y >> 16] = entry;
-      if (flags & F_PDEST) ready[S.n_rows + (q.w & 0xFFu)] = entry;
-      L.max_ready = max(L.max_ready, (uint32_t)wr);
-      L.drain = max(L.drain, T + lt.y);
-      L.t_last = T;
-      L.t_next = T + lt.z;
-      L.base = T + 1u;
-      L.issued++;
+      const uint32_t flags = issue(T);
+      const uint4 lt = L.r.lat;
       if ((flags & F_MCLASS) && __popc(pending & ~(1u << lane)) >= 4) L.throttled++;
       if (flags & F_MEMOP) {
         L.has_prev = L.has_mem;
@@ -343,7 +368,6 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
         L.mem_at = T;
         L.mem_done = T + max(lt.x, lt.y);  // a load's result, a store's drain
       }
-      if (L.div) L.diverged++;
       const bool more = advance(true);
       if (flags & F_BAR) {
         L.state = ST_WAITING;
@@ -365,6 +389,40 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
       const uint32_t lo = c * S.wpc;
       const uint32_t slot_mask = (S.wpc >= 32u ? FULL : ((1u << S.wpc) - 1u)) << lo;
       m &= ~slot_mask;
+    }
+    // Run-ahead. In a kernel without barriers, once no CTA is left to reach
+    // this SM, a warp that is the only running one on its scheduler can be
+    // contested by nothing: no warp can join its scheduler and no release
+    // or dispatch depends on it. It issues on its own, at max(its scoreboard
+    // time, its scheduler's port), exactly the cycles the steps would give
+    // it, up to its next memory-class entry (whose throttle label counts the
+    // other warps' memory operations pending at its cycle, known only in
+    // step order) or its end.
+    if (RUN_AHEAD && run_ahead && (uint64_t)s_id + (uint64_t)next_cta_k * S.n_sm >= S.grid) {
+      const uint32_t busy = __ballot_sync(FULL, L.state == ST_RUNNING || L.state == ST_WAITING);
+      uint32_t fin = 0;
+      if (L.state == ST_RUNNING && __popc(busy & sched_lanes) == 1) {
+        for (;;) {
+          if (((L.r.q.w >> 8) & 0xFFu) & (F_MCLASS | F_BAR)) break;
+          const uint32_t T1 = max(L.e, port);
+          if (T1 >= CLOCK_LIMIT) break;  // the steps report it
+          issue(T1);
+          port = T1 + 1u;
+          if (!advance(true)) {
+            finish();
+            fin = 1;
+            break;
+          }
+          compute_e();
+        }
+      }
+      for (uint32_t m = __ballot_sync(FULL, fin != 0u); m;) {
+        const uint32_t c = (uint32_t)(__ffs(m) - 1) / S.wpc;
+        settle(c);
+        const uint32_t lo = c * S.wpc;
+        const uint32_t slot_mask = (S.wpc >= 32u ? FULL : ((1u << S.wpc) - 1u)) << lo;
+        m &= ~slot_mask;
+      }
     }
   }
 
@@ -398,6 +456,7 @@ int launch_sched(const KsLaunch& L, uint32_t n_rows, uint32_t n_sm, uint32_t cta
   S.pred_off = L.layout.pred_off;
   S.row_bytes = L.layout.row_bytes;
   S.split = L.layout.split;
+  S.cta_mode = L.cta_mode;
   for (int i = 0; i < KS_NUM_LAT_CLASSES; i++) S.lat[i] = L.lat[i];
   S.grid = L.grid;
   S.wpc = L.wpc;
@@ -410,10 +469,13 @@ int launch_sched(const KsLaunch& L, uint32_t n_rows, uint32_t n_sm, uint32_t cta
   S.warps_out = warps_out;
   S.sms_out = sms_out;
   const size_t smem = sched_smem_bytes(L.n_insn, n_rows);
-  cudaError_t e = cudaFuncSetAttribute(ks_sched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // every CTA on an SM at the start: grid <= simulated SMs x CTA slots
+  const bool run_ahead = !L.cta_mode && L.lat[KS_LAT_BAR] != 0u && (uint64_t)L.grid <= (uint64_t)n_sm * ctas_per_sm;
+  const void* fn = run_ahead ? (const void*)ks_sched_kernel<true> : (const void*)ks_sched_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  ks_sched_kernel<<<n_sm, 32, smem, (cudaStream_t)stream>>>(S);
-  return (int)cudaGetLastError();
+  void* args[] = {&S};
+  return (int)cudaLaunchKernel(fn, dim3(n_sm), dim3(32), args, smem, (cudaStream_t)stream);
 }
 
 }  // namespace ks
