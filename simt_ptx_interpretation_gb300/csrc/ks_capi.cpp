@@ -86,6 +86,82 @@ int pick_layout(const KsKernel& k, uint32_t flags) {
   if (pair) return 0;
   return (!k.cta_mode() && k.layout[0].region_bytes > SPLIT_REGION_MIN) ? 1 : 0;
 }
+
+int check_call(const KsKernel& k, uint32_t grid, uint32_t block, const void* params, size_t param_bytes,
+               const ks_buffer* bufs, uint32_t n_bufs, const void* trace_buf, size_t trace_bytes,
+               const void* stats_buf, size_t stats_bytes, const ks_config& cfg, int* lay) {
+  if (grid == 0 || block == 0 || block > 1024) return KS_ERR_ARG;
+  const uint64_t W = (uint64_t)grid * ((block + 31u) / 32u);
+  if (W >= (1ull << 31)) return KS_ERR_ARG;
+  if (param_bytes < k.param_bytes || param_bytes > KS_MAX_PARAM_BYTES) return KS_ERR_ARG;
+  if (k.param_bytes && !params) return KS_ERR_ARG;
+  if (n_bufs > KS_MAX_BUFFERS || (n_bufs && !bufs)) return KS_ERR_ARG;
+  for (uint32_t i = 0; i < n_bufs; i++) {
+    const ks_buffer& b = bufs[i];
+    if (b.sim_base % 4096 != 0 || b.bytes == 0 || !b.dev_ptr) return KS_ERR_ARG;
+    if (b.sim_base + b.bytes < b.sim_base) return KS_ERR_ARG;
+    for (uint32_t j = 0; j < i; j++) {
+      const ks_buffer& o = bufs[j];
+      if (!(b.sim_base + b.bytes <= o.sim_base || o.sim_base + o.bytes <= b.sim_base)) return KS_ERR_ARG;
+    }
+  }
+  if (!stats_buf || stats_bytes < W * sizeof(ks_warp_stats)) return KS_ERR_ARG;
+  if (cfg.simt_stack_depth == 0 || cfg.simt_stack_depth > KS_MAX_STACK) return KS_ERR_ARG;
+  if (cfg.max_ts_per_warp > (1u << 24)) return KS_ERR_ARG;
+  for (uint32_t i = 0; i < KS_NUM_LAT_CLASSES; i++)
+    if (cfg.lat[i] > KS_MAX_LATENCY) return KS_ERR_ARG;
+  if (trace_buf && trace_bytes < W * trace_slot_bytes(k, cfg)) return KS_ERR_ARG;
+  // shared memory / bar.sync: every warp of a CTA resident on one real CTA
+  if (k.cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
+  if (cfg.profile_buf && cfg.profile_bytes < k.code.size() * sizeof(ks_pc_profile)) return KS_ERR_ARG;
+  const int l = pick_layout(k, cfg.flags);
+  if (l < 0) return l;
+  *lay = l;
+  return KS_OK;
+}
+
+void fill_launch(const KsKernel& k, int lay, const void* image, uint32_t grid, uint32_t block, const void* params,
+                 size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf, void* stats_buf,
+                 const ks_config& cfg, KsLaunch* Lp) {
+  KsLaunch& L = *Lp;
+  std::memset(&L, 0, sizeof L);
+  L.image = static_cast<const uint8_t*>(image);
+  L.image_bytes = (uint32_t)k.image[lay].size();
+  L.prog_bytes = k.prog_bytes;
+  L.n_insn = (uint32_t)k.code.size();
+  L.n_slots = k.n_slots;
+  L.n_crows = k.layout[lay].n_crows;
+  L.layout = k.layout[lay];
+  L.grid = grid;
+  L.block = block;
+  L.wpc = (block + 31u) / 32u;
+  L.n_warps = grid * L.wpc;
+  L.shared_bytes = k.shared_bytes;
+  L.cta_mode = k.cta_mode() ? 1u : 0u;
+  {
+    const uint32_t lmax = std::max(std::max(cfg.lat[KS_LAT_ALU], cfg.lat[KS_LAT_FMA]), 1u);
+    L.fast_shift = 32u - (uint32_t)__builtin_clz(lmax);  // 2^shift > lmax
+  }
+  std::memcpy(L.lat, cfg.lat, sizeof L.lat);
+  L.max_ts = cfg.max_ts_per_warp;
+  L.rec_bytes = k.record_bytes;
+  L.stack_depth = cfg.simt_stack_depth;
+  L.step_limit = cfg.step_limit;
+  L.inject_warp = cfg.inject_warp;
+  L.inject_step = cfg.inject_step;
+  L.n_bufs = n_bufs;
+  for (uint32_t i = 0; i < n_bufs; i++) {
+    L.bufs[i].sim_base = bufs[i].sim_base;
+    L.bufs[i].bytes = bufs[i].bytes;
+    L.bufs[i].ptr = static_cast<uint8_t*>(bufs[i].dev_ptr);
+  }
+  L.trace = static_cast<uint8_t*>(trace_buf);
+  L.slot_bytes = trace_slot_bytes(k, cfg);
+  L.stats = static_cast<uint8_t*>(stats_buf);
+  L.param_bytes = (uint32_t)param_bytes;
+  if (param_bytes) std::memcpy(L.params, params, param_bytes);
+  L.profile = static_cast<ks_pc_profile*>(cfg.profile_buf);
+}
 }  // namespace ks
 
 extern "C" {
@@ -234,35 +310,10 @@ int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t 
   if (!k) return KS_ERR_NOT_FOUND;
   ks_config cfg;
   if (cfg_in) cfg = *cfg_in; else ks_config_default(&cfg);
-
-  // ---- argument checks ----
-  if (grid == 0 || block == 0 || block > 1024) return KS_ERR_ARG;
-  const uint64_t W = warps_of(grid, block);
-  if (W >= (1ull << 31)) return KS_ERR_ARG;
-  if (param_bytes < k->param_bytes || param_bytes > KS_MAX_PARAM_BYTES) return KS_ERR_ARG;
-  if (k->param_bytes && !params) return KS_ERR_ARG;
-  if (n_bufs > KS_MAX_BUFFERS || (n_bufs && !bufs)) return KS_ERR_ARG;
-  for (uint32_t i = 0; i < n_bufs; i++) {
-    const ks_buffer& b = bufs[i];
-    if (b.sim_base % 4096 != 0 || b.bytes == 0 || !b.dev_ptr) return KS_ERR_ARG;
-    if (b.sim_base + b.bytes < b.sim_base) return KS_ERR_ARG;
-    for (uint32_t j = 0; j < i; j++) {
-      const ks_buffer& o = bufs[j];
-      if (!(b.sim_base + b.bytes <= o.sim_base || o.sim_base + o.bytes <= b.sim_base)) return KS_ERR_ARG;
-    }
-  }
-  if (!stats_buf || stats_bytes < W * sizeof(ks_warp_stats)) return KS_ERR_ARG;
-  if (cfg.simt_stack_depth == 0 || cfg.simt_stack_depth > KS_MAX_STACK) return KS_ERR_ARG;
-  if (cfg.max_ts_per_warp > (1u << 24)) return KS_ERR_ARG;
-  for (uint32_t i = 0; i < KS_NUM_LAT_CLASSES; i++)
-    if (cfg.lat[i] > ks::KS_MAX_LATENCY) return KS_ERR_ARG;
-  const uint64_t slot = (16ull + (uint64_t)k->record_bytes * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
-  if (trace_buf && trace_bytes < W * slot) return KS_ERR_ARG;
-  // shared memory / bar.sync: every warp of a CTA resident on one real CTA
-  if (k->cta_mode() && block > KS_MAX_CTA_MODE_BLOCK) return KS_ERR_LIMIT;
-  if (cfg.profile_buf && cfg.profile_bytes < k->code.size() * sizeof(ks_pc_profile)) return KS_ERR_ARG;
-  const int lay = ks::pick_layout(*k, cfg.flags);
-  if (lay < 0) return lay;
+  int lay = 0;
+  const int rc = ks::check_call(*k, grid, block, params, param_bytes, bufs, n_bufs, trace_buf, trace_bytes, stats_buf,
+                                stats_bytes, cfg, &lay);
+  if (rc != KS_OK) return rc;
 
   if (host_checks_only) return KS_OK;
   DevInfo& di = *dip;
@@ -287,46 +338,7 @@ int prepare(const ks_module* mod_c, const char* kernel, uint32_t grid, uint32_t 
       image = it->second;
     }
   }
-
-  // ---- launch block ----
-  ks::KsLaunch& L = *Lp;
-  std::memset(&L, 0, sizeof L);
-  L.image = static_cast<const uint8_t*>(image);
-  L.image_bytes = (uint32_t)img.size();
-  L.prog_bytes = k->prog_bytes;
-  L.n_insn = (uint32_t)k->code.size();
-  L.n_slots = k->n_slots;
-  L.n_crows = k->layout[lay].n_crows;
-  L.layout = k->layout[lay];
-  L.grid = grid;
-  L.block = block;
-  L.wpc = (block + 31u) / 32u;
-  L.n_warps = (uint32_t)W;
-  L.shared_bytes = k->shared_bytes;
-  L.cta_mode = k->cta_mode() ? 1u : 0u;
-  {
-    const uint32_t lmax = std::max(std::max(cfg.lat[KS_LAT_ALU], cfg.lat[KS_LAT_FMA]), 1u);
-    L.fast_shift = 32u - (uint32_t)__builtin_clz(lmax);  // 2^shift > lmax
-  }
-  std::memcpy(L.lat, cfg.lat, sizeof L.lat);
-  L.max_ts = cfg.max_ts_per_warp;
-  L.rec_bytes = k->record_bytes;
-  L.stack_depth = cfg.simt_stack_depth;
-  L.step_limit = cfg.step_limit;
-  L.inject_warp = cfg.inject_warp;
-  L.inject_step = cfg.inject_step;
-  L.n_bufs = n_bufs;
-  for (uint32_t i = 0; i < n_bufs; i++) {
-    L.bufs[i].sim_base = bufs[i].sim_base;
-    L.bufs[i].bytes = bufs[i].bytes;
-    L.bufs[i].ptr = static_cast<uint8_t*>(bufs[i].dev_ptr);
-  }
-  L.trace = static_cast<uint8_t*>(trace_buf);
-  L.slot_bytes = slot;
-  L.stats = static_cast<uint8_t*>(stats_buf);
-  L.param_bytes = (uint32_t)param_bytes;
-  if (param_bytes) std::memcpy(L.params, params, param_bytes);
-  L.profile = static_cast<ks_pc_profile*>(cfg.profile_buf);
+  ks::fill_launch(*k, lay, image, grid, block, params, param_bytes, bufs, n_bufs, trace_buf, stats_buf, cfg, Lp);
   return KS_OK;
 }
 

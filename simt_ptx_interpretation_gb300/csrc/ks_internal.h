@@ -274,6 +274,23 @@ struct KsKernel {
 constexpr uint32_t SPLIT_REGION_MIN = 12u * 1024u;
 int pick_layout(const KsKernel& k, uint32_t flags);
 
+// Bytes of one warp's trace slot: align8(16-byte header + records).
+inline uint64_t trace_slot_bytes(const KsKernel& k, const ks_config& cfg) {
+  return (16ull + (uint64_t)k.record_bytes * cfg.max_ts_per_warp + 7ull) / 8ull * 8ull;
+}
+// The argument checks every simulation call makes (ks_simulate and the
+// static, cached and SM-model calls, ks_capi.cpp): KS_OK with the layout the
+// launch runs in (*lay), or the KS_ERR_* code of the first failed check.
+int check_call(const KsKernel& k, uint32_t grid, uint32_t block, const void* params, size_t param_bytes,
+               const ks_buffer* bufs, uint32_t n_bufs, const void* trace_buf, size_t trace_bytes,
+               const void* stats_buf, size_t stats_bytes, const ks_config& cfg, int* lay);
+struct KsLaunch;
+// The launch block of a checked call whose program image of layout `lay`
+// is at `image` (device memory).
+void fill_launch(const KsKernel& k, int lay, const void* image, uint32_t grid, uint32_t block, const void* params,
+                 size_t param_bytes, const ks_buffer* bufs, uint32_t n_bufs, void* trace_buf, void* stats_buf,
+                 const ks_config& cfg, KsLaunch* L);
+
 // Decoder entry point (ks_decode.cpp). Returns KS_OK or a KS_ERR_* code and
 // fills `err` with a message.
 int decode_module(const char* text, size_t len, std::vector<KsKernel>* out, std::string* err);
