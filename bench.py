@@ -461,6 +461,11 @@ def run_ours(args, world, rank, local):
                 "launch_ms_mean": [round(sum(x) / len(x), 4) for x in launch_ms],
                 "streams": n_streams, "batched": bool(batch or cache_batch),
                 "timed_over": "each step's span (its launches may overlap)"}
+    ncu = ncu_figures(config["workload"]) if args.scale == 1 and args.iters == 4096 and not (cache or sched) else None
+    if ncu:  # the interpreter's own instruction stream on this kernel source, per ncu
+        roofline["ncu"] = {k: v for k, v in ncu.items() if k != "dram_bytes"}
+        roofline["ncu"]["measure"] = ("sm__inst_issued.avg.pct_of_peak_sustained_active: the share of the SMs' issue "
+                                      "slots the interpreter's own instructions use")
     if cache:
         roofline["note"] = ("each call runs ks_interp_kernel twice plus the level kernels and radix sorts; "
                             "achieved counts both passes over the whole call's time")
