@@ -1320,6 +1320,16 @@ class Decoder {
         o.inc |= (next + 1u) << INC_RUN_SHIFT;
       }
     }
+    // Short fast runs (at most MID_FAST_RUN ops, e.g. one address mad or a
+    // hash step's mul and add between logic ops) run in the mid loop instead:
+    // between mid ops they would cut its run in three, each piece taking a
+    // dispatch, while the fast loop's pipelining only pays on long runs.
+    for (size_t i = 0; i < n; i++) {
+      if (!fast(i) || (i > 0 && fast(i - 1))) continue;  // the first op of a run
+      const uint32_t len = dev[i].inc >> INC_RUN_SHIFT;
+      if (len > MID_FAST_RUN) continue;
+      for (size_t j = i; j < i + len; j++) dev[j].inc = (dev[j].inc & ((1u << INC_RUN_SHIFT) - 1u)) | INC_MID;
+    }
     // forwarding flags between consecutive fast ops (read by the SPLIT fast
     // loop): inside a run the next op's operands and scoreboard terms are
     // loaded before this op's stores

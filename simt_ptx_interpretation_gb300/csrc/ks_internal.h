@@ -192,6 +192,9 @@ constexpr uint32_t RUN_DIVERGED = 1u << 15;
 // bits 16..31 of DevInsn::inc of a fast-path op: the number of consecutive
 // fast-path ops starting at it (a run's length, at most KS_MAX_INSNS)
 constexpr uint32_t INC_RUN_SHIFT = 16u;
+// Fast runs of at most this many ops carry INC_MID and a run length of 0: the
+// mid loop runs them (DOP_FPU / DOP_IMAD cases) with the ops around them.
+constexpr uint32_t MID_FAST_RUN = 2u;
 // INC_MID: unguarded register-to-register op with no predicate operand, no
 //          memory access and no control transfer (runs in the mid loop)
 // INC_PHAZ: has a predicate source or destination (its ready entries matter)

@@ -688,6 +688,8 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
 #define MB64() ((uint64_t)b0 | ((uint64_t)RG32(lv + B + RB) << 32))
 #define R64(v) do { const uint64_t v_ = (v); lo = (uint32_t)v_; hi = (uint32_t)(v_ >> 32); wide = true; } while (0)
           switch (__shfl_sync(FULL, ka.x, 0)) {
+            case DOP_FPU: lo = fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))); break;
+            case DOP_IMAD: lo = a0 * b0 + (c0 ^ aux); break;
             case DOP_MADI: lo = a0 * aux + c0; break;
             case DOP_MADII: lo = a0 * aux + mp[3].x; break;
             case OP_LDP32: lo = *reinterpret_cast<const uint32_t*>(s_params + aux); break;
