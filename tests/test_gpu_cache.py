@@ -24,19 +24,19 @@ def gpu():
     _build.build_native()
 
 
-def gpu_cached(ptx, kernel, grid, block, params, buffers, cache, max_ts=0, lat=ks.DEFAULT_LAT):
+def gpu_cached(ptx, kernel, grid, block, params, buffers, cache, max_ts=0, lat=ks.DEFAULT_LAT, layout="auto"):
     """buffers: [(sim_base, numpy array)] (copied to the device)."""
     mod = ks.Module(ptx)
     dev = [(base, torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).copy()).cuda()) for base, a in buffers]
-    r = ks.run(mod, kernel, grid, block, params, dev, config=ks.Config(lat=lat, max_ts=max_ts), trace=max_ts > 0,
-               cache=cache)
+    r = ks.run(mod, kernel, grid, block, params, dev, config=ks.Config(lat=lat, max_ts=max_ts, layout=layout),
+               trace=max_ts > 0, cache=cache)
     torch.cuda.synchronize()
     return r, [t.cpu().numpy() for _, t in dev]
 
 
-def check(ptx, kernel, grid, block, params, buffers, cache=None, max_ts=0, lat=ks.DEFAULT_LAT):
+def check(ptx, kernel, grid, block, params, buffers, cache=None, max_ts=0, lat=ks.DEFAULT_LAT, layout="auto"):
     cache = cache or ks.CacheConfig(max_accesses_per_warp=256)
-    g, gbufs = gpu_cached(ptx, kernel, grid, block, params, buffers, cache, max_ts, lat)
+    g, gbufs = gpu_cached(ptx, kernel, grid, block, params, buffers, cache, max_ts, lat, layout)
     obufs = [(base, np.ascontiguousarray(a).copy()) for base, a in buffers]
     o = oracle.run_cached(ptx, kernel, grid, block, params, obufs, lat=lat, max_ts=max_ts, trace=max_ts > 0,
                           l1_lines=cache.l1_lines, l2_lines=cache.l2_lines, lat_l1=cache.lat_l1,
@@ -87,9 +87,19 @@ def test_barrier_release_steps():
     check(ck.BARRIER_EXIT, "barrier_exit", 1, 64, ck.u64(ck.BASE_IN), [(ck.BASE_IN, np.zeros(64, np.float32))])
 
 
-def wl_check(w: wl.Workload, cache=None):
+def wl_check(w: wl.Workload, cache=None, layout="auto"):
     return check(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in w.fresh_buffers()],
-                 cache=cache, max_ts=w.max_ts)
+                 cache=cache, max_ts=w.max_ts, layout=layout)
+
+
+@pytest.mark.parametrize("layout", ["pair", "split"])
+@pytest.mark.parametrize("name", ["vector_add", "ffma8", "gather4", "divergent", "fuzz2"])
+def test_both_register_layouts(name, layout):
+    """The hit model's two passes in each register layout, forced."""
+    w = {"vector_add": lambda: wl.vector_add(), "ffma8": lambda: wl.ffma(acc=8, iters=8, grid=4, block=128),
+         "gather4": lambda: wl.gather(4, n_out=1 << 12), "divergent": lambda: wl.divergent(4, n=1 << 11),
+         "fuzz2": lambda: wl.fuzz(2, grid=4, block=64)}[name]()
+    wl_check(w, cache=ks.CacheConfig(max_accesses_per_warp=4096), layout=layout)
 
 
 def test_vector_add():

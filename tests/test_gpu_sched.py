@@ -24,11 +24,12 @@ def gpu():
     _build.build_native()
 
 
-def check(ptx, kernel, grid, block, params, buffers, n_sm, ctas_per_sm=0, schedulers=4, max_ts=0):
+def check(ptx, kernel, grid, block, params, buffers, n_sm, ctas_per_sm=0, schedulers=4, max_ts=0, layout="auto"):
     sc = ks.SchedConfig(n_sm=n_sm, ctas_per_sm=ctas_per_sm, schedulers_per_sm=schedulers)
     mod = ks.Module(ptx)
     dev = [(base, torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).copy()).cuda()) for base, a in buffers]
-    r = ks.run(mod, kernel, grid, block, params, dev, config=ks.Config(max_ts=max_ts), trace=max_ts > 0, sched=sc)
+    r = ks.run(mod, kernel, grid, block, params, dev, config=ks.Config(max_ts=max_ts, layout=layout), trace=max_ts > 0,
+               sched=sc)
     torch.cuda.synchronize()
     obufs = [(base, np.ascontiguousarray(a).copy()) for base, a in buffers]
     ow, osm = oracle.run_sched(ptx, kernel, grid, block, params, obufs, n_sm=n_sm, ctas_per_sm=ctas_per_sm,
@@ -160,3 +161,14 @@ def test_cta_warp_state_in_global_memory():
     w = wl.fuzz_shared(1, grid=3, block=1024)
     check(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in w.fresh_buffers()],
           n_sm=2, schedulers=4, max_ts=w.max_ts)
+
+
+@pytest.mark.parametrize("layout", ["pair", "split"])
+@pytest.mark.parametrize("name", ["vector_add", "ffma8", "divergent", "fuzz0"])
+def test_both_register_layouts(name, layout):
+    """The issue log and the replay in each register layout, forced (the
+    replay reads the decoded records of either layout)."""
+    w = {"vector_add": lambda: wl.vector_add(), "ffma8": lambda: wl.ffma(acc=8, iters=4, grid=6, block=128),
+         "divergent": lambda: wl.divergent(4, n=1 << 11), "fuzz0": lambda: wl.fuzz(0, grid=6, block=64)}[name]()
+    check(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in w.fresh_buffers()],
+          n_sm=3, schedulers=4, max_ts=w.max_ts, layout=layout)
