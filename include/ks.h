@@ -466,16 +466,32 @@ int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_tota
  * arrived or finished, and its warps issue again at the next step. Trace
  * pseudo-ops take no step.
  *
- * How it runs: the library interprets the launch twice on `stream`. The first
- * pass suppresses the simulated stores and logs every access (line, step) per
- * warp; two stable radix sorts of the log — by (L1 set, step, warp), then the
- * L1 misses by their L2 set — put each set's accesses in order, and an access
- * hits when the one before it in its set had the same line. The second pass
- * is the real run: stores land, loads take the logged level's latency, and
- * every access is checked against the log. If the addresses or the control
- * flow depend on a value that the launch itself stored, the first pass may
- * log other accesses than the second makes; such warps end with
- * KS_ST_CACHE_STREAM rather than a wrong result.
+ * How it runs (two forms on `stream`; both give the same results where
+ * both apply):
+ *  - Re-interpretation (max_runs_per_warp == 0, and every kernel with shared
+ *    memory or bar.sync): the library interprets the launch twice. The first
+ *    pass suppresses the simulated stores and logs every access (line, step)
+ *    per warp; two stable radix sorts of the log — by (L1 set, step, warp),
+ *    then the L1 misses by their L2 set — put each set's accesses in order,
+ *    and an access hits when the one before it in its set had the same line.
+ *    The second pass is the real run: stores land, loads take the logged
+ *    level's latency, and every access is checked against the log. If the
+ *    addresses or the control flow depend on a value that the launch itself
+ *    stored, the first pass may log other accesses than the second makes;
+ *    such warps end with KS_ST_CACHE_STREAM rather than a wrong result.
+ *  - Timing replay (max_runs_per_warp > 0, kernels without shared memory
+ *    or bar.sync): timing never changes what a warp executes, so the one
+ *    interpretation is the real run (stores land, loads read them) and also
+ *    logs each warp's issued runs of program entries (at most
+ *    max_runs_per_warp); after the same sorts, a replay kernel — one thread
+ *    per simulated warp, no values — recomputes every warp's scoreboard from
+ *    its runs with each load's level latency and rewrites what timing
+ *    decides: the cycles of the stats record and trace header, the trace
+ *    records' timestamps, the hit counts. About one interpretation instead
+ *    of two. A warp reading back its own stores gets the values it stored
+ *    (no KS_ST_CACHE_STREAM). A warp whose accesses or runs overflow their
+ *    logs ends with KS_ST_CACHE_LOG, its stores done, its cycles those of
+ *    DRAM latencies.
  */
 typedef struct {
   uint32_t l1_lines;              /* default 1024 (128 KB); 1..65536 */
@@ -483,7 +499,9 @@ typedef struct {
   uint32_t lat_l1;                /* default 28 cycles, <= 2^24 */
   uint32_t lat_l2;                /* default 150 cycles, <= 2^24 */
   uint32_t max_accesses_per_warp; /* log capacity per warp (default 1024) */
-  uint32_t reserved[3];
+  uint32_t max_runs_per_warp;     /* 0 (default): re-interpretation; > 0: timing replay with a run
+                                     log of this many runs per warp (see above) */
+  uint32_t reserved[2];
 } ks_cache_config;
 
 #define KS_CACHE_LINE_BYTES 128
@@ -513,7 +531,8 @@ void ks_cache_config_default(ks_cache_config* cc);
 
 /* Bytes of the caller-owned device workspace of ks_simulate_cached: W
  * ks_cache_warp records, W * max_accesses_per_warp ks_cache_access records,
- * then the sort's scratch (its size is asked of the current CUDA device).
+ * then the sort's scratch (its size is asked of the current CUDA device),
+ * then (max_runs_per_warp > 0) W run counts and W * max_runs_per_warp runs.
  * 0 when the configuration is invalid, when the log would hold 2^31 records
  * or more, or when no CUDA device can be queried. */
 size_t ks_cache_workspace_bytes(uint32_t grid, uint32_t block, const ks_cache_config* cc);

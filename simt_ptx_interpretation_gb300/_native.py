@@ -52,7 +52,7 @@ class KsOccupancy(ctypes.Structure):
 class KsCacheConfig(ctypes.Structure):
     _fields_ = [("l1_lines", ctypes.c_uint32), ("l2_lines", ctypes.c_uint32), ("lat_l1", ctypes.c_uint32),
                 ("lat_l2", ctypes.c_uint32), ("max_accesses_per_warp", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32 * 3)]
+                ("max_runs_per_warp", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 2)]
 
 
 class KsSchedConfig(ctypes.Structure):

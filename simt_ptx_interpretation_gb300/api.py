@@ -387,6 +387,9 @@ class CacheConfig:
     lat_l1: int = 28
     lat_l2: int = 150
     max_accesses_per_warp: int = 1024
+    # 0: the second pass interprets again; > 0: a timing replay over a log of
+    # this many issued runs per warp (kernels without shared memory / bar.sync)
+    max_runs_per_warp: int = 0
 
     def to_c(self) -> _native.KsCacheConfig:
         c = _native.KsCacheConfig()
@@ -394,6 +397,7 @@ class CacheConfig:
         c.l1_lines, c.l2_lines = self.l1_lines, self.l2_lines
         c.lat_l1, c.lat_l2 = self.lat_l1, self.lat_l2
         c.max_accesses_per_warp = self.max_accesses_per_warp
+        c.max_runs_per_warp = self.max_runs_per_warp
         return c
 
 

@@ -106,7 +106,7 @@ unsigned grid_for(uint64_t n) {
 
 }  // namespace
 
-int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out) {
+int cache_layout(uint64_t n_warps, uint32_t cap, uint32_t max_runs, CacheLayout* out) {
   const uint64_t n = n_warps * (uint64_t)cap;
   if (n == 0 || n >= (1ull << 31)) return KS_ERR_ARG;
   size_t t1 = 0, t2 = 0, t3 = 0;
@@ -130,7 +130,11 @@ int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out) {
   C.vals_b = C.vals_a + align256(n * 4);
   C.temp_off = C.vals_b + align256(n * 4);
   C.temp_bytes = align256(std::max(std::max(t1, t2), t3));
-  C.total = C.temp_off + C.temp_bytes;
+  C.runs_off = C.temp_off + C.temp_bytes;
+  C.runlog_off = C.runs_off + (max_runs ? align256(n_warps * 4) : 0);
+  const uint64_t nr = n_warps * (uint64_t)max_runs;
+  if (nr >= (1ull << 34)) return KS_ERR_ARG;
+  C.total = C.runlog_off + align256(nr * 4);
   *out = C;
   return KS_OK;
 }

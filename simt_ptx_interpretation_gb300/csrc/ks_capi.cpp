@@ -384,22 +384,34 @@ int cache_checks(const ks_cache_config* cc_in, const void* workspace, size_t wor
   const uint64_t W = warps_of(grid, block);
   if (bits_for(cc->l1_lines - 1u) + 32u + bits_for(W - 1u) > 64u) return KS_ERR_LIMIT;
   if (host_checks_only) return KS_OK;
-  const int lc = ks::cache_layout(W, cc->max_accesses_per_warp, C);
+  const int lc = ks::cache_layout(W, cc->max_accesses_per_warp, cc->max_runs_per_warp, C);
   if (lc != KS_OK) return lc;
   if (workspace_bytes < C->total) return KS_ERR_ARG;
   return KS_OK;
 }
 
-// Points a prepared launch at its cache-model workspace (first pass: the
-// accesses logged, stores suppressed, no profile).
-void cache_first_pass(ks::KsLaunch* L, const ks_cache_config& cc, uint8_t* ws, const ks::CacheLayout& C) {
+// Points a prepared launch at its cache-model workspace for its first pass
+// and returns whether the launch takes the timing-replay form: then the pass
+// is the real run (cache_pass 3: stores land, accesses and issued runs
+// logged, the profile collected); else the accesses are logged with the
+// stores suppressed and no profile (cache_pass 1), and a second
+// interpretation follows.
+bool cache_first_pass(ks::KsLaunch* L, const ks_cache_config& cc, uint8_t* ws, const ks::CacheLayout& C) {
   L->cache_cap = cc.max_accesses_per_warp;
   L->lat_l1 = cc.lat_l1;
   L->lat_l2 = cc.lat_l2;
   L->cache_warps = reinterpret_cast<ks_cache_warp*>(ws + C.warps_off);
   L->cache_log = reinterpret_cast<ks_cache_access*>(ws + C.log_off);
+  if (cc.max_runs_per_warp > 0 && !L->cta_mode) {
+    L->sched_runs = reinterpret_cast<uint32_t*>(ws + C.runs_off);
+    L->sched_log = reinterpret_cast<uint32_t*>(ws + C.runlog_off);
+    L->sched_cap = cc.max_runs_per_warp;
+    L->cache_pass = 3;
+    return true;
+  }
   L->profile = nullptr;
   L->cache_pass = 1;
+  return false;
 }
 
 // Launches prepared simulations as real grids of one instantiation each (mode,
@@ -566,7 +578,7 @@ size_t ks_cache_workspace_bytes(uint32_t grid, uint32_t block, const ks_cache_co
   if (cc_in) cc = *cc_in; else ks_cache_config_default(&cc);
   if (grid == 0 || block == 0 || block > 1024 || !cache_config_ok(cc)) return 0;
   ks::CacheLayout C;
-  if (ks::cache_layout(warps_of(grid, block), cc.max_accesses_per_warp, &C) != KS_OK) return 0;
+  if (ks::cache_layout(warps_of(grid, block), cc.max_accesses_per_warp, cc.max_runs_per_warp, &C) != KS_OK) return 0;
   return (size_t)C.total;
 }
 
@@ -585,10 +597,12 @@ int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, 
   if (rc != KS_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   ks_pc_profile* profile = L.profile;
-  cache_first_pass(&L, cc, ws, C);
+  const bool replay = cache_first_pass(&L, cc, ws, C);
+  if (replay && clear_profile(L, stream) != KS_OK) return KS_ERR_CUDA;
   rc = shape_and_launch(L, di, stream);
   if (rc != KS_OK) return rc;
   if (ks::launch_cache_levels(L, ws, C, cc.l1_lines, cc.l2_lines, stream) != 0) return KS_ERR_CUDA;
+  if (replay) return ks::launch_cache_replay(L, di.sms, di.max_smem, stream) != 0 ? KS_ERR_CUDA : KS_OK;
   L.cache_pass = 2;  // the real run, latencies from the levels
   L.profile = profile;
   if (clear_profile(L, stream) != KS_OK) return KS_ERR_CUDA;
@@ -622,9 +636,12 @@ int ks_simulate_cached_batch(const ks_cached_item* items, uint32_t n_items, void
     }
   }
   // first pass of every item, then every item's levels, then the second
+  // passes: timing replays, and the other items' interpretations batched
+  std::vector<char> replay(n_items, 0);
   for (uint32_t i = 0; i < n_items; i++) {
     profiles[i] = Ls[i].profile;
-    cache_first_pass(&Ls[i], ccs[i], static_cast<uint8_t*>(items[i].workspace), Cs[i]);
+    replay[i] = cache_first_pass(&Ls[i], ccs[i], static_cast<uint8_t*>(items[i].workspace), Cs[i]) ? 1 : 0;
+    if (replay[i] && clear_profile(Ls[i], stream) != KS_OK) return KS_ERR_CUDA;
   }
   int rc = launch_items(Ls, di, stream, n_launched);
   if (rc != KS_OK) return rc;
@@ -632,12 +649,19 @@ int ks_simulate_cached_batch(const ks_cached_item* items, uint32_t n_items, void
     if (ks::launch_cache_levels(Ls[i], static_cast<uint8_t*>(items[i].workspace), Cs[i], ccs[i].l1_lines,
                                 ccs[i].l2_lines, stream, n_launched) != 0)
       return KS_ERR_CUDA;
+  std::vector<ks::KsLaunch> second;
   for (uint32_t i = 0; i < n_items; i++) {
+    if (replay[i]) {
+      if (ks::launch_cache_replay(Ls[i], di.sms, di.max_smem, stream) != 0) return KS_ERR_CUDA;
+      if (n_launched) ++*n_launched;
+      continue;
+    }
     Ls[i].cache_pass = 2;
     Ls[i].profile = profiles[i];
     if (clear_profile(Ls[i], stream) != KS_OK) return KS_ERR_CUDA;
+    second.push_back(Ls[i]);
   }
-  return launch_items(Ls, di, stream, n_launched);
+  return second.empty() ? KS_OK : launch_items(second, di, stream, n_launched);
 }
 
 int ks_read_stats(const void* stats_buf, uint64_t n_warps, void* stream, ks_totals* out) {

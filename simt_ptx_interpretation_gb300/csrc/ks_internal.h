@@ -333,7 +333,9 @@ struct KsLaunch {
   uint64_t slot_bytes;
   uint8_t* stats;
   // L1/L2 hit model (ks_simulate_cached): 0 off; 1 first pass (stores
-  // suppressed, accesses logged); 2 second pass (levels from the log)
+  // suppressed, accesses logged); 2 second pass (levels from the log); 3 the
+  // one interpretation of the timing-replay form (stores land, accesses and
+  // issued runs logged; cache_replay_kernel then retimes every warp)
   uint32_t cache_pass;
   uint32_t cache_cap;             // log records per warp
   uint32_t lat_l1, lat_l2;        // load latency on an L1 / L2 hit
@@ -417,11 +419,19 @@ int launch_batch(KsGrid<KS_BATCH_ITEMS>* G, int sms, int max_smem, void* stream)
 // Workspace of the L1/L2 hit model (ks_cache.cu): per-warp counts, the log,
 // and the sort's buffers, each at a 256-byte boundary.
 struct CacheLayout {
-  uint64_t warps_off, log_off, logged_off, offsets_off, keys_a, keys_b, vals_a, vals_b, temp_off, temp_bytes, total;
+  uint64_t warps_off, log_off, logged_off, offsets_off, keys_a, keys_b, vals_a, vals_b, temp_off, temp_bytes;
+  uint64_t runs_off, runlog_off;  // timing replay (max_runs > 0): run counts, runs
+  uint64_t total;
 };
-// KS_OK, KS_ERR_ARG (log of 2^31 records or more) or KS_ERR_CUDA (the sort's
-// scratch size could not be queried: it needs a current CUDA device).
-int cache_layout(uint64_t n_warps, uint32_t cap, CacheLayout* out);
+// KS_OK, KS_ERR_ARG (a log of 2^31 records or more) or KS_ERR_CUDA (the
+// sort's scratch size could not be queried: it needs a current CUDA device).
+int cache_layout(uint64_t n_warps, uint32_t cap, uint32_t max_runs, CacheLayout* out);
+// The timing replay of the hit model (ks_cache_replay.cu): after the
+// logging interpretation (cache_pass 3) and the levels, every warp's timing
+// again from its logged runs and its accesses' levels -- the cycles of its
+// stats record and trace header, its trace timestamps and hit counts.
+// Returns a cudaError_t value.
+int launch_cache_replay(const KsLaunch& L, int sms, int max_smem, void* stream);
 // The hit computation between the two passes: the logged records packed,
 // sorted by (L1 set, step, warp), L1 hits, a stable sort of the misses by
 // their L2 set, L2 hits. Waits for the stream once (the sorts' length is the

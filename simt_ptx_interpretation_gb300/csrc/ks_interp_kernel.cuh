@@ -874,7 +874,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           int cst = 0;
           if (step >= 0xFFFFFFFFull) {
             cst = KS_ST_CACHE_LOG;
-          } else if (L.cache_pass == 1) {
+          } else if (L.cache_pass != 2u) {  // a logging pass (1, or 3: the timing replay's)
             if (c_k < L.cache_cap && lane == 0) {
               rec->line = line;
               rec->step = (uint32_t)step;
@@ -1373,9 +1373,11 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           n_runs++;
         }
         if (lane == 0) L.sched_runs[gw] = n_runs;
-        if (n_runs > L.sched_cap && status == 0) status = KS_ST_SCHED_LIMIT;
+        if (n_runs > L.sched_cap && status == 0) status = L.cache_pass == 3u ? KS_ST_CACHE_LOG : KS_ST_SCHED_LIMIT;
       }
       if (L.cache_pass == 2 && status == 0 && c_k != c_n) status = KS_ST_CACHE_STREAM;
+      // the timing replay needs every access's level
+      if (L.cache_pass == 3 && status == 0 && c_k > L.cache_cap) status = KS_ST_CACHE_LOG;
       if (L.cache_pass != 0u && lane == 0) {
         ks_cache_warp cw;
         cw.n_access = c_k;

@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "ks_internal.h"
+#include "ks_rec.cuh"
 
 namespace ks {
 namespace {
@@ -100,7 +101,8 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
   // interpreter patches its copy)
   for (uint32_t i = lane; i <= S.n_insn; i += 32) {
     const DevInsn d = reinterpret_cast<const DevInsn*>(S.image)[i];
-    const uint32_t f = d.wlat, cls = f & 0xFFu, lat = S.lat[cls];
+    const uint32_t f = d.wlat, cls = f & 0xFFu;
+    const EntryLat el = entry_lat(d, S.lat);
     const uint32_t kind = (cls == KS_LAT_LDG || cls == KS_LAT_LDS) ? K_MEM : cls == KS_LAT_SFU ? K_MATH : K_EXEC;
     uint32_t flags = 0;
     if (d.inc & INC_ISSUE) flags |= F_ISSUE;
@@ -110,33 +112,19 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     if (d.op == OP_BAR) flags |= F_BAR;
     if (d.inc & INC_MCLASS) flags |= F_MCLASS;
     if (d.inc & INC_MEMOP) flags |= F_MEMOP;
-    // predicate index of a predicate-table offset
-    auto pred = [&](uint32_t off) { return (off - S.pred_off) / 4u; };
     // the guard, the predicate sources and the predicate destination (31:
     // none), from either layout's record
-    uint32_t guard, pa, pb, pc, pd;
-    if (S.split) {  // hazard halfwords 4..7: guard, sources; 3: the destination's term
-      guard = pred(d.x[2] & 0xFFFFu);
-      pa = pred(d.x[2] >> 16);
-      pb = pred(d.x[3] & 0xFFFFu);
-      pc = pred(d.x[3] >> 16);
-      pd = (d.inc & INC_PDEST) ? pred(d.x[1] >> 16) : 31u;
-    } else {        // guard, gneg, ha, hb, hc, hd
-      guard = d.x[0];
-      pa = pred(d.x[2]);
-      pb = pred(d.x[3]);
-      pc = pred(d.x[4]);
-      pd = pred(d.x[5]);
-    }
+    const PredTerms pt = pred_terms(d, S.split, S.pred_off);
+    const uint32_t guard = pt.guard, pa = pt.pa, pb = pt.pb, pc = pt.pc, pd = pt.pd;
     const uint32_t RB = S.row_bytes;
     Rec r;
     r.q.x = (d.a / RB) | ((d.b / RB) << 16);
     r.q.y = (d.c / RB) | ((d.d / RB) << 16);
     r.q.z = guard | (pa << 8) | (pb << 16) | (pc << 24);
     r.q.w = pd | (flags << 8) | (kind << 16);
-    r.lat.x = (f & DEV_HAS_DEST) ? lat : 0u;
-    r.lat.y = (f & DEV_IS_STORE) ? lat : 0u;
-    r.lat.z = d.inc ? ((f & DEV_IS_CTRL) ? lat : 1u) : 0u;
+    r.lat.x = el.dest;
+    r.lat.y = el.store;
+    r.lat.z = el.next;
     r.lat.w = 0u;
     prog[i] = r;
   }
