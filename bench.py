@@ -9,10 +9,13 @@ kernel and one with 8 rotating accumulators), i.e. two interpreter launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload ffma_pair|vector_add|gather_sS|divergent_kK|fuzz|smem_reduce]
-                  [--cache [--cache-cap C]] [--sched [--sched-sms S]]
+                  [--cache [--cache-cap C] [--cache-form replay|reinterpret]]
+                  [--sched [--sched-sms S]]
 
 --cache runs every launch with the L1/L2 hit model (ks_simulate_cached: a
-logging pass, the sorted levels, the checked second pass); --sched with the
+logging pass, the sorted levels, then either a value-free replay of each
+warp's issued runs or, --cache-form reinterpret and kernels with shared
+memory, a checked second interpretation); --sched with the
 SM-level issue model (ks_simulate_sched: the interpreter logging each warp's
 issued runs, then one replay warp per simulated SM).
 
@@ -78,6 +81,11 @@ def parse_args():
     p.add_argument("--cache-cap", type=int, default=0,
                    help="logged global accesses per warp (--cache); 0: the largest count of a plain run, "
                         "rounded up to a power of two")
+    p.add_argument("--cache-form", choices=["replay", "reinterpret"], default="replay",
+                   help="second half of the hit model (--cache): replay the logged runs (kernels without shared "
+                        "memory; the run log is sized from an untimed logging run) or interpret again")
+    p.add_argument("--layout", choices=["auto", "pair", "split"], default="auto",
+                   help="register-file layout of every launch (auto: the library's choice per kernel)")
     p.add_argument("--sched", action="store_true", help="simulate with the SM-level issue model")
     p.add_argument("--sched-sms", type=int, default=152, help="simulated SMs (--sched)")
     p.add_argument("--streams", type=int, default=0,
@@ -252,6 +260,27 @@ def sm_peak_mhz():
 
 # ---------------------------------------------------------------- ours ----
 
+def most_runs(jobs, n_sm, dev, stream) -> int:
+    """The largest count of issued runs of any warp of the jobs, from one
+    untimed logging run of each (the SM model's issue log, whose runs the
+    hit model's replay form logs too), rounded up to a power of two."""
+    import simt_ptx_interpretation_gb300 as ks
+    import torch
+    runs = 1
+    for j in jobs:
+        w = j["w"]
+        probe = ks.SchedConfig(n_sm=n_sm, max_runs_per_warp=1 << 16)
+        tmp = torch.empty(ks.sched_workspace_bytes(w.grid, w.block, probe), dtype=torch.uint8, device=dev)
+        sw = torch.empty(w.warps * ks.SCHED_WARP_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+        ss = torch.empty(n_sm * 32, dtype=torch.uint8, device=dev)
+        ks.simulate_sched(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], sw, ss, tmp, j["tr"],
+                          j["cfg"], probe, stream)
+        torch.cuda.synchronize(dev)
+        runs = max(runs, int(tmp[:w.warps * 4].view(torch.int32).max().item()))
+        del tmp
+    return 1 << (runs - 1).bit_length()
+
+
 def run_ours(args, world, rank, local):
     import torch
     import simt_ptx_interpretation_gb300 as ks
@@ -270,11 +299,13 @@ def run_ours(args, world, rank, local):
         mod = ks.Module(w.ptx)
         host = [b.data for b in w.fresh_buffers()]
         bufs = [(b.sim_base, torch.from_numpy(h.view(np.uint8)).to(dev)) for b, h in zip(w.buffers, host)]
-        cfg = ks.Config(max_ts=w.max_ts)
+        cfg = ks.Config(max_ts=w.max_ts, layout=args.layout)
         st = torch.empty(ks.stats_bytes(w.grid, w.block), dtype=torch.uint8, device=dev)
         tr = (torch.empty(ks.trace_bytes(w.grid, w.block, w.max_ts, mod.record_bytes(w.kernel)), dtype=torch.uint8,
                           device=dev) if w.max_ts else None)
         jobs.append(dict(w=w, mod=mod, bufs=bufs, cfg=cfg, st=st, tr=tr))
+    if args.layout != "auto":
+        config = dict(config, layout=args.layout)
     # The step's launches are independent simulations (own buffers, stats and
     # trace). Plain runs go to the GPU as one batch (ks_simulate_batch: their
     # warps share one real grid). With the SM model, whose calls hold the
@@ -294,7 +325,10 @@ def run_ours(args, world, rank, local):
             a = ks.stats_array(j["st"])
             most = max(most, int((a["ld_req"] + a["st_req"]).max()))
         cap = 1 << (most - 1).bit_length()
-    cache = ks.CacheConfig(max_accesses_per_warp=cap) if args.cache else None
+    cache = None
+    if args.cache:
+        runs = most_runs(jobs, args.sched_sms, dev, stream) if args.cache_form == "replay" else 0
+        cache = ks.CacheConfig(max_accesses_per_warp=cap, max_runs_per_warp=runs)
     if cache:  # one workspace, sized for the largest grid
         wmax = max(jobs, key=lambda j: j["w"].warps)["w"]
         nbytes = ks.cache_workspace_bytes(wmax.grid, wmax.block, cache)
@@ -312,27 +346,18 @@ def run_ours(args, world, rank, local):
                             device=dev)) for j in jobs]
         config = dict(config, cache_model={"l1_lines": cache.l1_lines, "l2_lines": cache.l2_lines,
                                            "lat_l1": cache.lat_l1, "lat_l2": cache.lat_l2,
-                                           "max_accesses_per_warp": cache.max_accesses_per_warp})
+                                           "max_accesses_per_warp": cache.max_accesses_per_warp,
+                                           "form": args.cache_form + (" (kernels with shared memory or bar.sync: "
+                                                                      "reinterpret)" if args.cache_form == "replay"
+                                                                      else ""),
+                                           "max_runs_per_warp": cache.max_runs_per_warp})
 
     sched = ks.SchedConfig(n_sm=args.sched_sms) if args.sched else None
     if sched:
         if cache:
             raise SystemExit("--cache and --sched run separately")
         wmax = max(jobs, key=lambda j: j["w"].warps)["w"]
-        runs = 1
-        for j in jobs:  # size the issue log from an untimed logging run
-            w = j["w"]
-            probe = ks.SchedConfig(n_sm=args.sched_sms, max_runs_per_warp=1 << 16)
-            nb = ks.sched_workspace_bytes(w.grid, w.block, probe)
-            tmp = torch.empty(nb, dtype=torch.uint8, device=dev)
-            sw = torch.empty(w.warps * ks.SCHED_WARP_DTYPE.itemsize, dtype=torch.uint8, device=dev)
-            ss = torch.empty(args.sched_sms * 32, dtype=torch.uint8, device=dev)
-            ks.simulate_sched(j["mod"], w.kernel, w.grid, w.block, w.params, j["bufs"], j["st"], sw, ss, tmp, j["tr"],
-                              j["cfg"], probe, stream)
-            torch.cuda.synchronize(dev)
-            runs = max(runs, int(tmp[:w.warps * 4].view(torch.int32).max().item()))
-            del tmp
-        sched = ks.SchedConfig(n_sm=args.sched_sms, max_runs_per_warp=1 << (runs - 1).bit_length())
+        sched = ks.SchedConfig(n_sm=args.sched_sms, max_runs_per_warp=most_runs(jobs, args.sched_sms, dev, stream))
         nbytes = ks.sched_workspace_bytes(wmax.grid, wmax.block, sched)
         sched_ws = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
         sched_w = [torch.empty(wmax.warps * ks.SCHED_WARP_DTYPE.itemsize, dtype=torch.uint8, device=dev)
@@ -448,7 +473,8 @@ def run_ours(args, world, rank, local):
     span_s = sum(step_ms) / args.steps / 1e3
     # with the cache model a call interprets the launch twice (and sorts in
     # between): charge the whole call to the two interpreter passes
-    passes = 2 if cache else 1  # (the SM model's replay runs once per call)
+    # (the replay form and the SM model interpret once per call)
+    passes = 2 if cache and not cache.max_runs_per_warp else 1
     achieved = passes * insts / span_s / 1e9
     # the stored counters are for the full-size workloads only
     traffic = traffic_for(config["workload"]) if args.scale == 1 and args.iters == 4096 else None
@@ -466,7 +492,11 @@ def run_ours(args, world, rank, local):
         roofline["ncu"] = {k: v for k, v in ncu.items() if k != "dram_bytes"}
         roofline["ncu"]["measure"] = ("sm__inst_issued.avg.pct_of_peak_sustained_active: the share of the SMs' issue "
                                       "slots the interpreter's own instructions use")
-    if cache:
+    if cache and cache.max_runs_per_warp:
+        roofline["note"] = ("each call runs ks_interp_kernel once (logging accesses and issued runs), the level "
+                            "kernels and radix sorts, then cache_replay_kernel; achieved counts the simulated "
+                            "thread-instructions over the whole call's time")
+    elif cache:
         roofline["note"] = ("each call runs ks_interp_kernel twice plus the level kernels and radix sorts; "
                             "achieved counts both passes over the whole call's time")
     if sched:
@@ -487,9 +517,9 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32/u64 (simulated)", "data": "synthetic (seeded)",
         "config": dict(config, l2="flushed between steps (256 MiB write)", parallelism=f"replicas{world}",
                        streams=n_streams, batched=bool(batch or cache_batch)),
-        # our kernels per call: the interpreter, or (cache model) two interpreter
-        # passes and the four level kernels (the radix sorts and the scan are
-        # library code)
+        # our kernels per call: the interpreter, or (cache model) the four level
+        # kernels between either two interpreter passes or one pass and the
+        # replay (the radix sorts and the scan are library code)
         "roofline": roofline, "e2e": e2e,
         # (a batch call reports its real launches)
         "gpu_launches": args.steps * (batch_launches[0] if (batch or cache_batch)
