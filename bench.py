@@ -9,13 +9,14 @@ kernel and one with 8 rotating accumulators), i.e. two interpreter launches.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload ffma_pair|vector_add|gather_sS|divergent_kK|fuzz|smem_reduce]
-                  [--cache [--cache-cap C] [--cache-form replay|reinterpret]]
+                  [--cache [--cache-cap C] [--cache-form auto|replay|reinterpret]]
                   [--sched [--sched-sms S]]
 
 --cache runs every launch with the L1/L2 hit model (ks_simulate_cached: a
 logging pass, the sorted levels, then either a value-free replay of each
-warp's issued runs or, --cache-form reinterpret and kernels with shared
-memory, a checked second interpretation); --sched with the
+warp's issued runs or a checked second interpretation: the replay for large
+grids by default, the second interpretation for small grids, kernels with
+shared memory and --cache-form reinterpret); --sched with the
 SM-level issue model (ks_simulate_sched: the interpreter logging each warp's
 issued runs, then one replay warp per simulated SM).
 
@@ -81,9 +82,11 @@ def parse_args():
     p.add_argument("--cache-cap", type=int, default=0,
                    help="logged global accesses per warp (--cache); 0: the largest count of a plain run, "
                         "rounded up to a power of two")
-    p.add_argument("--cache-form", choices=["replay", "reinterpret"], default="replay",
+    p.add_argument("--cache-form", choices=["auto", "replay", "reinterpret"], default="auto",
                    help="second half of the hit model (--cache): replay the logged runs (kernels without shared "
-                        "memory; the run log is sized from an untimed logging run) or interpret again")
+                        "memory; the run log is sized from an untimed logging run) or interpret again; auto: "
+                        "replay when every launch of the step has at least 32 simulated warps per SM (the replay "
+                        "walks a warp's log with one thread, so a small grid leaves it few real warps)")
     p.add_argument("--layout", choices=["auto", "pair", "split"], default="auto",
                    help="register-file layout of every launch (auto: the library's choice per kernel)")
     p.add_argument("--sched", action="store_true", help="simulate with the SM-level issue model")
@@ -326,8 +329,12 @@ def run_ours(args, world, rank, local):
             most = max(most, int((a["ld_req"] + a["st_req"]).max()))
         cap = 1 << (most - 1).bit_length()
     cache = None
+    cache_form = args.cache_form
+    if args.cache and cache_form == "auto":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        cache_form = "replay" if all(j["w"].warps >= 32 * sms for j in jobs) else "reinterpret"
     if args.cache:
-        runs = most_runs(jobs, args.sched_sms, dev, stream) if args.cache_form == "replay" else 0
+        runs = most_runs(jobs, args.sched_sms, dev, stream) if cache_form == "replay" else 0
         cache = ks.CacheConfig(max_accesses_per_warp=cap, max_runs_per_warp=runs)
     if cache:  # one workspace, sized for the largest grid
         wmax = max(jobs, key=lambda j: j["w"].warps)["w"]
@@ -347,9 +354,8 @@ def run_ours(args, world, rank, local):
         config = dict(config, cache_model={"l1_lines": cache.l1_lines, "l2_lines": cache.l2_lines,
                                            "lat_l1": cache.lat_l1, "lat_l2": cache.lat_l2,
                                            "max_accesses_per_warp": cache.max_accesses_per_warp,
-                                           "form": args.cache_form + (" (kernels with shared memory or bar.sync: "
-                                                                      "reinterpret)" if args.cache_form == "replay"
-                                                                      else ""),
+                                           "form": cache_form + (" (kernels with shared memory or bar.sync: "
+                                                                 "reinterpret)" if cache_form == "replay" else ""),
                                            "max_runs_per_warp": cache.max_runs_per_warp})
 
     sched = ks.SchedConfig(n_sm=args.sched_sms) if args.sched else None

@@ -185,12 +185,16 @@ int launch_cache_replay(const KsLaunch& L, int sms, int max_smem, void* stream) 
   R.slot_bytes = L.slot_bytes;
   R.rec_bytes = L.rec_bytes;
   R.max_ts = L.max_ts;
-  // as many warps of threads per block as shared memory allows (records,
-  // then each thread's ready table), at most 8
+  // Warps of threads per block: as many as shared memory allows (records,
+  // then each thread's ready table), at most 8, and no more than it takes to
+  // spread the simulated warps over every SM (each thread walks one warp's
+  // whole issue log, so a small grid wants its threads on many SMs)
   const size_t prog = (size_t)(L.n_insn + 1u) * sizeof(RRec);
   const size_t per_warp = (size_t)(L.n_slots + 33u) * 32u * 8u;
   if (prog + per_warp > (size_t)max_smem) return (int)cudaErrorInvalidValue;
-  const uint32_t warps = (uint32_t)std::min<size_t>(8, ((size_t)max_smem - prog) / per_warp);
+  const uint64_t per_sm = (L.n_warps + (uint64_t)std::max(sms, 1) - 1u) / (uint64_t)std::max(sms, 1);
+  const uint32_t spread = (uint32_t)std::max<uint64_t>(1, std::min<uint64_t>(8, (per_sm + 31u) / 32u));
+  const uint32_t warps = (uint32_t)std::min<size_t>(spread, ((size_t)max_smem - prog) / per_warp);
   const size_t smem = prog + per_warp * warps;
   cudaError_t e = cudaFuncSetAttribute(cache_replay_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
