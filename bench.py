@@ -52,7 +52,8 @@ import numpy as np  # noqa: E402
 METRIC = "simulated thread-instructions/sec"
 UNIT = "thread-inst/s"
 KERNEL_SRC = [os.path.join(ROOT, "simt_ptx_interpretation_gb300", "csrc", f)
-              for f in ("ks_interp_kernel.cuh", "ks_interp.cu", "ks_batch.cu", "ks_interp_split.cu")]
+              for f in ("ks_interp_kernel.cuh", "ks_interp.cu", "ks_batch.cu", "ks_interp_split.cu", "ks_decode.cpp",
+                        "ks_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 NCU_FILE = os.path.join(ROOT, "profiles", "ncu_full_size.json")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
