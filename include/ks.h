@@ -421,7 +421,13 @@ typedef struct ks_batch_item {
  * grid the real CTAs are shared out in proportion to the items' simulated
  * warps (CTAs in CTA mode); when every simulated warp fits on the GPU at
  * once, the grid is a multiple of the SM count with the same number of real
- * warps on every SM. Items must not share
+ * warps on every SM. When the items take more than one real grid, the grids
+ * run side by side on up to four streams that the library creates once per
+ * device and keeps (one grid's last warps then overlap the next grid's work):
+ * they start after everything enqueued on `stream` before the call, and
+ * everything enqueued on `stream` after the call waits for all of them, as
+ * for a launch on `stream` itself. While `stream` is capturing a graph, every
+ * grid is launched on `stream`. Items must not share
  * output, trace, stats, profile or store-target buffers (they run at the same
  * time). *n_launched (if not NULL) receives the number of real kernel
  * launches enqueued. KS_ERR_ARG for items == NULL or n_items == 0, else the

@@ -414,13 +414,46 @@ bool cache_first_pass(ks::KsLaunch* L, const ks_cache_config& cc, uint8_t* ws, c
   return false;
 }
 
+// Helper streams of one device, created on first use and kept for the
+// library's lifetime: the grids of one call that do not share a real grid run
+// on them side by side, so that one grid's last warps overlap the next grid's
+// work instead of leaving SMs idle (the 64 fuzz kernels: 182 -> 166 ms a step
+// on four streams). They start when the caller's stream reaches the call and
+// the caller's stream waits for all of them, so the call keeps the ordering
+// of a single-stream launch.
+constexpr int FORK_STREAMS = 4;
+struct ForkPool {
+  cudaStream_t s[FORK_STREAMS];
+  cudaEvent_t fork, join[FORK_STREAMS];
+};
+std::mutex g_fork_mu;  // held while a call enqueues its fork and join
+std::map<int, ForkPool> g_fork;
+
+// The current device's pool, or null if it cannot be made (the call then
+// launches everything on the caller's stream). Needs g_fork_mu.
+ForkPool* fork_pool() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  auto it = g_fork.find(dev);
+  if (it != g_fork.end()) return &it->second;
+  ForkPool P;
+  if (cudaEventCreateWithFlags(&P.fork, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+  for (int j = 0; j < FORK_STREAMS; j++) {
+    if (cudaStreamCreateWithFlags(&P.s[j], cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&P.join[j], cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;  // (what was made stays unused)
+  }
+  return &g_fork.emplace(dev, P).first->second;
+}
+
 // Launches prepared simulations as real grids of one instantiation each (mode,
 // form, layout, and in CTA mode the block), in the order of their first items, at
 // most KS_BATCH_ITEMS and at most BATCH_WARPS_PER_SM simulated warps per SM
 // of them, so that a grid runs as one wave and ends with its slowest warp
 // (items are not weighted by their unknown cost per warp). An item larger
 // than that fills the GPU alone and is launched as ks_simulate launches it.
-// Adds the real launches to *n_launched (if not null).
+// Several grids go to the helper streams (above) unless the caller's stream
+// is capturing a graph. Adds the real launches to *n_launched (if not null).
 int launch_items(const std::vector<ks::KsLaunch>& Ls, const DevInfo& di, void* stream, uint32_t* n_launched) {
   constexpr uint64_t BATCH_WARPS_PER_SM = 16;
   const uint64_t budget = BATCH_WARPS_PER_SM * (uint64_t)std::max(di.sms, 1);
@@ -433,27 +466,64 @@ int launch_items(const std::vector<ks::KsLaunch>& Ls, const DevInfo& di, void* s
   auto alone = [&](const ks::KsLaunch& L) {
     return L.cta_mode && ks::cta_mode_smem(L) > (size_t)di.max_smem;
   };
+  // the real grids: the items of each, in call order
   const size_t n_items = Ls.size();
   std::vector<char> done(n_items, 0);
-  auto G = std::make_unique<ks::KsGrid<ks::KS_BATCH_ITEMS>>();
+  std::vector<std::vector<size_t>> grids;
   for (size_t i = 0; i < n_items; i++) {
     if (done[i]) continue;
-    G->n = 0;
+    std::vector<size_t> g;
     uint64_t warps = 0;
-    for (size_t j = i; j < n_items && G->n < ks::KS_BATCH_ITEMS; j++) {
-      if (done[j] || key(Ls[j]) != key(Ls[i]) || (G->n > 0 && (alone(Ls[i]) || alone(Ls[j])))) continue;
-      if (G->n > 0 && (Ls[j].n_warps > budget || warps + Ls[j].n_warps > budget)) continue;
-      G->item[G->n++] = Ls[j];
+    for (size_t j = i; j < n_items && g.size() < ks::KS_BATCH_ITEMS; j++) {
+      if (done[j] || key(Ls[j]) != key(Ls[i]) || (!g.empty() && (alone(Ls[i]) || alone(Ls[j])))) continue;
+      if (!g.empty() && (Ls[j].n_warps > budget || warps + Ls[j].n_warps > budget)) continue;
+      g.push_back(j);
       warps += Ls[j].n_warps;
       done[j] = 1;
       if (warps > budget) break;  // a large first item goes alone
     }
-    const int rc = G->n == 1 ? shape_and_launch(G->item[0], di, stream)
-                             : ks::launch_batch(G.get(), di.sms, di.max_smem, stream);
-    if (rc != KS_OK) return rc;
-    if (n_launched) ++*n_launched;
+    grids.push_back(std::move(g));
   }
-  return KS_OK;
+  auto G = std::make_unique<ks::KsGrid<ks::KS_BATCH_ITEMS>>();
+  auto launch = [&](const std::vector<size_t>& g, void* st) {
+    if (g.size() == 1) return shape_and_launch(Ls[g[0]], di, st);
+    G->n = 0;
+    for (size_t j : g) G->item[G->n++] = Ls[j];
+    return ks::launch_batch(G.get(), di.sms, di.max_smem, st);
+  };
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (grids.size() > 1 && cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return KS_ERR_CUDA;
+  std::unique_lock<std::mutex> lk(g_fork_mu, std::defer_lock);
+  ForkPool* P = nullptr;
+  if (grids.size() > 1 && cap == cudaStreamCaptureStatusNone) {
+    lk.lock();
+    P = fork_pool();
+    if (!P) lk.unlock();
+  }
+  if (!P) {
+    for (const auto& g : grids) {
+      const int rc = launch(g, stream);
+      if (rc != KS_OK) return rc;
+      if (n_launched) ++*n_launched;
+    }
+    return KS_OK;
+  }
+  const int used = (int)std::min<size_t>(grids.size(), FORK_STREAMS);
+  if (cudaEventRecord(P->fork, cs) != cudaSuccess) return KS_ERR_CUDA;
+  for (int j = 0; j < used; j++)
+    if (cudaStreamWaitEvent(P->s[j], P->fork, 0) != cudaSuccess) return KS_ERR_CUDA;
+  int rc = KS_OK;
+  for (size_t g = 0; g < grids.size() && rc == KS_OK; g++) {
+    rc = launch(grids[g], P->s[g % used]);
+    if (rc == KS_OK && n_launched) ++*n_launched;
+  }
+  // the caller's stream waits for every helper stream, whatever happened
+  for (int j = 0; j < used; j++) {
+    if (cudaEventRecord(P->join[j], P->s[j]) != cudaSuccess || cudaStreamWaitEvent(cs, P->join[j], 0) != cudaSuccess)
+      rc = rc == KS_OK ? KS_ERR_CUDA : rc;
+  }
+  return rc;
 }
 
 }  // namespace

@@ -201,3 +201,28 @@ def test_cta_mode_large_blocks(block):
     assert run_batch(jobs) == 1
     for j in jobs:
         j.check_oracle()
+
+
+def test_grids_on_helper_streams_keep_the_callers_order():
+    """Items that each take a real grid of their own run side by side on the
+    library's helper streams; what the caller enqueues on its own stream after
+    the call sees every grid's results: copies made there with no
+    synchronisation in between equal single launches."""
+    ws = [wl.divergent(k, n=2048 * 32) for k in (2, 4, 32, 2, 4)]  # 2,048 warps each: one grid apiece
+    jobs = [Job(w) for w in ws]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        n = ks.simulate_batch([j.item() for j in jobs], stream=s)
+        copies = [(j.stats.clone(), j.dev[1][1].clone()) for j in jobs]
+    torch.cuda.synchronize()
+    assert n == len(ws)
+    for k, w in enumerate(ws[:3]):
+        g = _parity.gpu_run(w)
+        for j in (k, k + 3) if k < 2 else (k,):
+            st, out = copies[j]
+            assert np.array_equal(ks.stats_array(st).view(np.uint8), g.stats.view(np.uint8)), j
+            assert np.array_equal(out.cpu().numpy(), g.buffers[1]), j
+    w = ws[0]
+    warps = _parity.sample_warps(w, n=24, seed=5)
+    jobs[0].check_oracle(warps=warps, out_words={"out": _parity.thread_ids(w, warps)})
