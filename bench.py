@@ -316,7 +316,8 @@ def run_ours(args, world, rank, local):
     # GPU with a small replay grid, they may be spread over streams forked
     # from and joined to `stream`.
     batch = not (args.cache or args.sched or args.no_batch) and len(jobs) > 1
-    cache_batch = None  # the cached batch's items (--cache, small grids)
+    cache_batch = None  # the cached batches' items (--cache, several launches a step)
+    cache_ws = None  # the workspaces of single cached calls (--cache, --no-batch or one launch a step)
     n_streams = args.streams if args.streams > 0 else (min(len(jobs), 8) if args.sched else 1)
     n_streams = max(1, min(n_streams, len(jobs)))
     streams = [stream] + [torch.cuda.Stream(dev) for _ in range(n_streams - 1)]
@@ -342,16 +343,19 @@ def run_ours(args, world, rank, local):
         nbytes = ks.cache_workspace_bytes(wmax.grid, wmax.block, cache)
         if nbytes == 0:
             raise SystemExit("invalid cache configuration")
-        cache_ws = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
-        # launches that fit one wave together go as one cached batch (their
-        # passes share real grids), each with a workspace of its own
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        if not args.no_batch and len(jobs) > 1 and sum(j["w"].warps for j in jobs) <= 16 * sms:
-            cache_batch = [ks.CachedBatchItem(
+        # a step of several launches goes as cached batches of at most 16
+        # items (their passes share real grids or run side by side, their
+        # replays too), each item with a workspace of its own; a single
+        # launch as one ks_simulate_cached call
+        if not args.no_batch and len(jobs) > 1:
+            items = [ks.CachedBatchItem(
                 ks.BatchItem(j["mod"], j["w"].kernel, j["w"].grid, j["w"].block, j["w"].params, j["bufs"], j["st"],
                              j["tr"], j["cfg"]), cache,
                 torch.empty(ks.cache_workspace_bytes(j["w"].grid, j["w"].block, cache), dtype=torch.uint8,
                             device=dev)) for j in jobs]
+            cache_batch = [items[i:i + 16] for i in range(0, len(items), 16)]
+        else:
+            cache_ws = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(n_streams)]
         config = dict(config, cache_model={"l1_lines": cache.l1_lines, "l2_lines": cache.l2_lines,
                                            "lat_l1": cache.lat_l1, "lat_l2": cache.lat_l2,
                                            "max_accesses_per_warp": cache.max_accesses_per_warp,
@@ -405,11 +409,14 @@ def run_ours(args, world, rank, local):
             [ks.BatchItem(j["mod"], j["w"].kernel, j["w"].grid, j["w"].block, j["w"].params, j["bufs"], j["st"],
                           j["tr"], j["cfg"]) for j in jobs], stream)
 
+    def launch_cached_batch():
+        batch_launches[0] = sum(ks.simulate_cached_batch(c, stream) for c in cache_batch)
+
     def step(lev=None):
         if cache_batch:
             if lev:
                 lev[0][0].record(stream)
-            batch_launches[0] = ks.simulate_cached_batch(cache_batch, stream)
+            launch_cached_batch()
             if lev:
                 lev[0][1].record(stream)
             return
@@ -513,7 +520,7 @@ def run_ours(args, world, rank, local):
     # end to end through the public API with pinned host buffers
     e2e = None if args.no_e2e else run_e2e(args, jobs, insts, dev, streams, launch, fork, join,
                                            launch_batch if batch else
-                                           (lambda: ks.simulate_cached_batch(cache_batch, stream)) if cache_batch
+                                           launch_cached_batch if cache_batch
                                            else None)
 
     line = {

@@ -566,7 +566,8 @@ int ks_simulate_cached(const ks_module* mod, const char* kernel, uint32_t grid, 
 /* Several cached simulations in one call (no counterpart on the pages), each
  * giving exactly ks_simulate_cached's outputs: the items' first passes run
  * as ks_simulate_batch runs its items (shared real grids), then each item's
- * levels (one stream wait each), then the second passes, again batched.
+ * levels (one stream wait each), then the second passes, again batched (the
+ * timing replays side by side on ks_simulate_batch's helper streams).
  * Each item has its own hit model: cache NULL means ks_cache_config_default,
  * and its workspace is sized by ks_cache_workspace_bytes. Checks, failed_item
  * and the no-launch guarantee are those of ks_simulate_batch, plus the

@@ -446,6 +446,42 @@ ForkPool* fork_pool() {
   return &g_fork.emplace(dev, P).first->second;
 }
 
+// Runs launch(k, stream) for k = 0 .. n-1: with n > 1 on the helper streams,
+// forked from and joined back to `stream` (unless it is capturing a graph,
+// or no pool can be made: then all on `stream`, in order). Returns the first
+// launch's error; the join is enqueued whatever happened.
+template <class F>
+int fork_launches(size_t n, void* stream, F&& launch) {
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (n > 1 && cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return KS_ERR_CUDA;
+  std::unique_lock<std::mutex> lk(g_fork_mu, std::defer_lock);
+  ForkPool* P = nullptr;
+  if (n > 1 && cap == cudaStreamCaptureStatusNone) {
+    lk.lock();
+    P = fork_pool();
+    if (!P) lk.unlock();
+  }
+  if (!P) {
+    for (size_t k = 0; k < n; k++) {
+      const int rc = launch(k, stream);
+      if (rc != KS_OK) return rc;
+    }
+    return KS_OK;
+  }
+  const int used = (int)std::min<size_t>(n, FORK_STREAMS);
+  if (cudaEventRecord(P->fork, cs) != cudaSuccess) return KS_ERR_CUDA;
+  for (int j = 0; j < used; j++)
+    if (cudaStreamWaitEvent(P->s[j], P->fork, 0) != cudaSuccess) return KS_ERR_CUDA;
+  int rc = KS_OK;
+  for (size_t k = 0; k < n && rc == KS_OK; k++) rc = launch(k, P->s[k % used]);
+  for (int j = 0; j < used; j++) {
+    if (cudaEventRecord(P->join[j], P->s[j]) != cudaSuccess || cudaStreamWaitEvent(cs, P->join[j], 0) != cudaSuccess)
+      rc = rc == KS_OK ? KS_ERR_CUDA : rc;
+  }
+  return rc;
+}
+
 // Launches prepared simulations as real grids of one instantiation each (mode,
 // form, layout, and in CTA mode the block), in the order of their first items, at
 // most KS_BATCH_ITEMS and at most BATCH_WARPS_PER_SM simulated warps per SM
@@ -491,39 +527,11 @@ int launch_items(const std::vector<ks::KsLaunch>& Ls, const DevInfo& di, void* s
     for (size_t j : g) G->item[G->n++] = Ls[j];
     return ks::launch_batch(G.get(), di.sms, di.max_smem, st);
   };
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (grids.size() > 1 && cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return KS_ERR_CUDA;
-  std::unique_lock<std::mutex> lk(g_fork_mu, std::defer_lock);
-  ForkPool* P = nullptr;
-  if (grids.size() > 1 && cap == cudaStreamCaptureStatusNone) {
-    lk.lock();
-    P = fork_pool();
-    if (!P) lk.unlock();
-  }
-  if (!P) {
-    for (const auto& g : grids) {
-      const int rc = launch(g, stream);
-      if (rc != KS_OK) return rc;
-      if (n_launched) ++*n_launched;
-    }
-    return KS_OK;
-  }
-  const int used = (int)std::min<size_t>(grids.size(), FORK_STREAMS);
-  if (cudaEventRecord(P->fork, cs) != cudaSuccess) return KS_ERR_CUDA;
-  for (int j = 0; j < used; j++)
-    if (cudaStreamWaitEvent(P->s[j], P->fork, 0) != cudaSuccess) return KS_ERR_CUDA;
-  int rc = KS_OK;
-  for (size_t g = 0; g < grids.size() && rc == KS_OK; g++) {
-    rc = launch(grids[g], P->s[g % used]);
+  return fork_launches(grids.size(), stream, [&](size_t g, void* st) {
+    const int rc = launch(grids[g], st);
     if (rc == KS_OK && n_launched) ++*n_launched;
-  }
-  // the caller's stream waits for every helper stream, whatever happened
-  for (int j = 0; j < used; j++) {
-    if (cudaEventRecord(P->join[j], P->s[j]) != cudaSuccess || cudaStreamWaitEvent(cs, P->join[j], 0) != cudaSuccess)
-      rc = rc == KS_OK ? KS_ERR_CUDA : rc;
-  }
-  return rc;
+    return rc;
+  });
 }
 
 }  // namespace
@@ -719,13 +727,19 @@ int ks_simulate_cached_batch(const ks_cached_item* items, uint32_t n_items, void
     if (ks::launch_cache_levels(Ls[i], static_cast<uint8_t*>(items[i].workspace), Cs[i], ccs[i].l1_lines,
                                 ccs[i].l2_lines, stream, n_launched) != 0)
       return KS_ERR_CUDA;
+  // the timing replays side by side (each fills few SMs)
+  std::vector<uint32_t> rep;
+  for (uint32_t i = 0; i < n_items; i++)
+    if (replay[i]) rep.push_back(i);
+  rc = fork_launches(rep.size(), stream, [&](size_t k, void* st) {
+    if (ks::launch_cache_replay(Ls[rep[k]], di.sms, di.max_smem, st) != 0) return (int)KS_ERR_CUDA;
+    if (n_launched) ++*n_launched;
+    return (int)KS_OK;
+  });
+  if (rc != KS_OK) return rc;
   std::vector<ks::KsLaunch> second;
   for (uint32_t i = 0; i < n_items; i++) {
-    if (replay[i]) {
-      if (ks::launch_cache_replay(Ls[i], di.sms, di.max_smem, stream) != 0) return KS_ERR_CUDA;
-      if (n_launched) ++*n_launched;
-      continue;
-    }
+    if (replay[i]) continue;
     Ls[i].cache_pass = 2;
     Ls[i].profile = profiles[i];
     if (clear_profile(Ls[i], stream) != KS_OK) return KS_ERR_CUDA;
