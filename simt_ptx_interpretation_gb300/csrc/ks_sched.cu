@@ -324,6 +324,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
     }
     const bool at_T = cand == T;
     bool win;
+    bool sched_won = false;  // (not one at a time) my scheduler issues at T
     if (one_at_a_time) {
       win = at_T && L.gw == __reduce_min_sync(FULL, at_T ? L.gw : NEVER);
     } else {
@@ -340,6 +341,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
       const uint32_t all = __reduce_or_sync(FULL, at_T ? 1u << (my_sched * per + L.rank) : 0u);
       const uint32_t mine_bits = per == 32u ? all : (all >> (my_sched * per)) & ((1u << per) - 1u);
       win = at_T && (uint32_t)(__ffs(mine_bits) - 1) == L.rank;
+      sched_won = mine_bits != 0u;
     }
     // warps of this SM with a memory operation pending at T (issued earlier,
     // not yet complete), for the memory-throttle label
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(32) ks_sched_kernel(const __grid_constant__ Sc
       }
     }
     // the winning schedulers' ports move on
-    if (__ballot_sync(FULL, win) & sched_lanes) port = T + 1u;
+    if (one_at_a_time ? (__ballot_sync(FULL, win) & sched_lanes) != 0u : sched_won) port = T + 1u;
     // settle every CTA slot in which a warp arrived or finished
     for (uint32_t m = __ballot_sync(FULL, ev != 0u); m;) {
       const uint32_t c = (uint32_t)(__ffs(m) - 1) / S.wpc;
