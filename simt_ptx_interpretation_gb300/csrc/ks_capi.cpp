@@ -136,6 +136,7 @@ void fill_launch(const KsKernel& k, int lay, const void* image, uint32_t grid, u
   L.block = block;
   L.wpc = (block + 31u) / 32u;
   L.n_warps = grid * L.wpc;
+  std::memcpy(L.live_in, k.live_in, sizeof L.live_in);
   L.shared_bytes = k.shared_bytes;
   L.cta_mode = k.cta_mode() ? 1u : 0u;
   {

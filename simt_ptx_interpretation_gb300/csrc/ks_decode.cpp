@@ -12,6 +12,7 @@
 // consecutive slots; slots and predicate indices are assigned in order of
 // first use. Immediates go to a per-kernel constant pool.
 #include <algorithm>
+#include <array>
 #include <cctype>
 #include <cstring>
 #include <map>
@@ -1478,6 +1479,52 @@ class Decoder {
     }
     // one program image per layout
     for (uint32_t split = 0; split < 2; split++) resolve_image(split, route, madi, madi_c, crow, rowval);
+    live_in_slots();
+  }
+
+  // The register slots that some path from the entry may read before writing
+  // them (backward liveness over the program's control flow; a guarded write
+  // kills nothing, since some lanes may skip it). Only these must start at 0
+  // in each simulated warp; every other slot is written before it is read.
+  void live_in_slots() {
+    const size_t n = K.code.size();
+    using Set = std::array<uint64_t, 2>;  // KS_MAX_SLOTS <= 128 bits
+    auto add = [](Set& x, unsigned s, unsigned w) {
+      for (unsigned k = 0; k < (w == 64 ? 2u : 1u) && s + k < KS_MAX_SLOTS; k++) x[(s + k) >> 6] |= 1ull << ((s + k) & 63);
+    };
+    std::vector<Set> use(n, Set{0, 0}), kill(n, Set{0, 0}), in(n + 1, Set{0, 0});
+    for (size_t i = 0; i < n; i++) {
+      const KsInsn& k = K.code[i];
+      const uint8_t ops[3] = {k.a, k.b, k.c};
+      for (int p = 0; p < 3; p++) {
+        const unsigned w = row_width(k, p);
+        if (w && ops[p] < KS_MAX_SLOTS) add(use[i], ops[p], w);
+      }
+      const unsigned wd = row_width(k, 3);
+      if (wd && k.d < KS_MAX_SLOTS && k.guard == KS_NO_GUARD) add(kill[i], k.d, wd);
+    }
+    // successors: the next entry unless an unguarded bra or ret ends the
+    // path here; a bra's target
+    for (bool changed = true; changed;) {
+      changed = false;
+      for (size_t i = n; i-- > 0;) {
+        const KsInsn& k = K.code[i];
+        const bool ends = (k.op == OP_BRA || k.op == OP_RET) && k.guard == KS_NO_GUARD;
+        Set out{0, 0};
+        if (!ends) out = in[i + 1];
+        if (k.op == OP_BRA && k.target <= n) {
+          out[0] |= in[k.target][0];
+          out[1] |= in[k.target][1];
+        }
+        const Set v{use[i][0] | (out[0] & ~kill[i][0]), use[i][1] | (out[1] & ~kill[i][1])};
+        if (v != in[i]) {
+          in[i] = v;
+          changed = true;
+        }
+      }
+    }
+    const Set& e = n ? in[0] : in[n];
+    for (int w = 0; w < 4; w++) K.live_in[w] = (uint32_t)(e[w >> 1] >> (32 * (w & 1)));
   }
 };
 

@@ -266,6 +266,7 @@ struct KsKernel {
   std::vector<uint8_t> image[2];
   DevLayout layout[2]{};
   uint32_t prog_bytes = 0;  // DevInsn part of an image
+  uint32_t live_in[4]{};    // bit s: slot s may be read before it is written (starts at 0)
 };
 
 // The layout a launch of `k` runs in: forced by KS_FLAG_LAYOUT_PAIR /
@@ -304,7 +305,7 @@ struct KsBufDev {
   uint8_t* ptr;
 };
 
-// Everything one interpreter launch needs (720 bytes), passed by value in the
+// Everything one interpreter launch needs (736 bytes), passed by value in the
 // kernel argument (KsGrid).
 struct KsLaunch {
   const uint8_t* image;  // device: DevInsn program then constant row values
@@ -319,6 +320,7 @@ struct KsLaunch {
   uint32_t cta_mode;          // 1: one real CTA per simulated CTA, one real warp per simulated warp
   uint32_t fast_shift;        // 2^fast_shift > the largest fast-path (ALU, FMA) latency
   uint32_t n_warps;           // grid * wpc
+  uint32_t live_in[4];        // KsKernel::live_in
   uint32_t lat[KS_NUM_LAT_CLASSES];
   uint32_t max_ts;
   uint32_t rec_bytes;  // trace record size (4, 8 or 16)

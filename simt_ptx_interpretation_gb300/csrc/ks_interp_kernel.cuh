@@ -352,6 +352,17 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
   uint32_t cta = (cta_x * nwarps + wid) / L.wpc;
   uint32_t wic = (cta_x * nwarps + wid) - cta * L.wpc;
   uint32_t hint = 0;  // buffer of the last simulated access (tried first)
+  // Outside CTA mode a real warp runs its simulated warps one after another
+  // in one region. In the PAIR layout the first starts from a zeroed region
+  // at clock 0; each later one zeroes only the slots it may read before
+  // writing (the decoder's live-in set) and starts its clock at t_floor, the
+  // latest time the region holds (every ready time left behind is at most
+  // that, so none delays it), with its epoch at -t_floor so that its cycles
+  // and timestamps still count from its own start. (The SPLIT form zeroes
+  // every warp's region: the floor's registers would cost it resident warps.)
+  constexpr bool FLOOR = !CTA && !SPLIT;
+  bool region_fresh = false;
+  uint32_t t_floor = 0;
 
   for (uint32_t gw = cta_x * nwarps + wid; gw < L.n_warps;
        gw += gw_stride, cta += step_cta, wic += step_wic, cta += (wic >= L.wpc), wic -= (wic >= L.wpc) ? L.wpc : 0u) {
@@ -372,12 +383,19 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
     }
 
     // ---- warp set-up (a1): registers zero, predicates false, clock 0 ----
-    if constexpr (SPLIT) {
-      for (uint32_t s = 0; s < Y.n_slots; s++) RG32(lv + s * RB) = 0u;
-      for (uint32_t i = lane; i < Y.n_ready; i += 32u) RG32(wb + Y.ready_off + 4u * i) = 0u;
+    if (!FLOOR || !region_fresh) {
+      if constexpr (SPLIT) {
+        for (uint32_t s = 0; s < Y.n_slots; s++) RG32(lv + s * RB) = 0u;
+        for (uint32_t i = lane; i < Y.n_ready; i += 32u) RG32(wb + Y.ready_off + 4u * i) = 0u;
+      } else {
+        for (uint32_t s = 0; s < Y.n_slots; s++) RG64(lv + s * RB) = 0ull;
+        RG32(pg + lane * 4u) = 0u;
+      }
+      region_fresh = true;
+      t_floor = 0;
     } else {
-      for (uint32_t s = 0; s < Y.n_slots; s++) RG64(lv + s * RB) = 0ull;
-      RG32(pg + lane * 4u) = 0u;
+      for (uint32_t w = 0; w < 4u; w++)
+        for (uint32_t m = L.live_in[w]; m; m &= m - 1u) RG32(lv + (32u * w + (uint32_t)(__ffs(m) - 1)) * RB) = 0u;
     }
     __syncwarp();
     uint32_t my_pred = (lane == 31u) ? 0xFFFFFFFFu : 0u;  // predicate 31 is always true
@@ -387,8 +405,8 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
     uint64_t sh_req = 0, sh_wf = 0;  // shared requests, their bank-conflict degrees
     bool at_bar = false, finished = false;
     uint64_t cyc_floor = 0;           // cycles owed to before a barrier's epoch move
-    uint64_t epoch = 0;
-    uint32_t t_next = 0, t_last = 0, max_ready = 0, drain = 0;
+    uint64_t epoch = 0ull - (uint64_t)t_floor;
+    uint32_t t_next = t_floor, t_last = t_floor, max_ready = t_floor, drain = t_floor;
     uint64_t thread_insts = 0;
     uint64_t ld_req = 0, ld_sec = 0, st_req = 0, st_sec = 0, ld_lin = 0, st_lin = 0;
     uint32_t n_events = 0, n_rec = 0, n_dropped = 0;
@@ -1411,6 +1429,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       }
       for (uint32_t i = 4 + n_rec * (L.rec_bytes / 4u) + lane; i < words; i += 32) sw[i] = 0u;
     }
+    if constexpr (FLOOR) t_floor = max(max(t_next, t_last + 1u), max(max_ready, drain));
     __syncwarp();
   }
   // Leave no copy in flight: if staging timed out, wait once more (bounded).
