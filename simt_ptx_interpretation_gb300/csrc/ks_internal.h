@@ -305,7 +305,7 @@ struct KsBufDev {
   uint8_t* ptr;
 };
 
-// Everything one interpreter launch needs (736 bytes), passed by value in the
+// Everything one interpreter launch needs (752 bytes), passed by value in the
 // kernel argument (KsGrid).
 struct KsLaunch {
   const uint8_t* image;  // device: DevInsn program then constant row values
