@@ -226,3 +226,34 @@ def test_grids_on_helper_streams_keep_the_callers_order():
     w = ws[0]
     warps = _parity.sample_warps(w, n=24, seed=5)
     jobs[0].check_oracle(warps=warps, out_words={"out": _parity.thread_ids(w, warps)})
+
+
+def test_two_host_threads_fork_at_once():
+    """Two host threads, each with its own stream, issue batches that take
+    several real grids at the same time: the helper streams are shared under
+    the library's lock, and every item equals its single launch."""
+    import threading
+    ws = [wl.divergent(k, n=2048 * 32) for k in (2, 4, 32)]
+    refs = [_parity.gpu_run(w) for w in ws]
+    results = {}
+
+    def worker(t):
+        s = torch.cuda.Stream()
+        jobs = [Job(w) for w in ws]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                ks.simulate_batch([j.item() for j in jobs], stream=s)
+        s.synchronize()
+        results[t] = jobs
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert sorted(results) == [0, 1]
+    for jobs in results.values():
+        for j, g in zip(jobs, refs):
+            assert np.array_equal(ks.stats_array(j.stats).view(np.uint8), g.stats.view(np.uint8))
+            assert np.array_equal(j.dev[1][1].cpu().numpy(), g.buffers[1])

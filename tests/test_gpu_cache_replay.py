@@ -177,3 +177,24 @@ def test_gather_full_size_all_misses():
     assert (r.cache_warps["n_access"] == 2).all() and (r.cache_warps["dram"] == 2).all()
     assert np.array_equal(ks.stats_array(r.stats), ks.stats_array(p.stats))
     assert torch.equal(dev[1][1], p.buffers[1][1])
+
+
+def test_forked_replays_keep_the_callers_order():
+    """A cached batch's replays run side by side on the library's helper
+    streams; copies of the outputs made on the caller's stream right after the
+    call, with no synchronisation in between, equal single cached calls."""
+    ws = [(wl.divergent(k, n=1 << 14), replay(64, 2048)) for k in (2, 4, 32, 2)]
+    jobs = [tgc._cached_job(w, c) for w, c in ws]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ks.simulate_cached_batch(jobs, stream=s)
+        copies = [(j.item.stats.clone(), j.item.trace.clone(), j.workspace[:w.warps * 16].clone())
+                  for (w, _), j in zip(ws, jobs)]
+    torch.cuda.synchronize()
+    for (w, c), (st, tr, cw) in zip(ws, copies):
+        g, _ = tgc.gpu_cached(w.ptx, w.kernel, w.grid, w.block, w.params, [(b.sim_base, b.data) for b in w.buffers],
+                              c, max_ts=w.max_ts)
+        assert np.array_equal(st.cpu().numpy(), g.stats.cpu().numpy()), w.name
+        assert np.array_equal(tr.cpu().numpy(), g.trace.cpu().numpy()), w.name
+        assert np.array_equal(cw.cpu().numpy().view(ks.api.CACHE_WARP_DTYPE), g.cache_warps), w.name
