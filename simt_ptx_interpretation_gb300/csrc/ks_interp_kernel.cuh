@@ -116,6 +116,14 @@ __device__ __forceinline__ uint32_t fbits(float f) {
   return (f != f) ? 0x7FFFFFFFu : __float_as_uint(f);  // canonical NaN
 }
 
+// The bits of an f32 result of one hardware FFMA / FADD / FMUL: every NaN
+// such an instruction writes on this GPU is already the canonical 0x7FFFFFFF,
+// whatever NaNs its operands hold (payloads, either sign, quiet or
+// signalling), so the canonical-NaN rule costs no compare and select on the
+// datapaths' chains (held by parity tests with NaN-payload operands in the
+// fast, mid and general paths). Division and square root keep fbits.
+__device__ __forceinline__ uint32_t fbits_hw(float f) { return __float_as_uint(f); }
+
 __device__ __forceinline__ uint64_t f2i(float f, uint32_t flags) {
   if (f != f) return 0;
   const uint32_t rnd = flags >> 4, kind = flags & 15;
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             max_ready = max(max_ready, wr);
             t_next = t + 1u;
             const uint32_t cx = c ^ ka.z;
-            const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a), __uint_as_float(b), __uint_as_float(cx)));
+            const uint32_t rf = fbits_hw(__fmaf_rn(__uint_as_float(a), __uint_as_float(b), __uint_as_float(cx)));
             const uint32_t ri = a * b + cx;
             const uint32_t res = ka.x == DOP_FPU ? rf : ri;
             ST_LANE_IF(on_all, ka.w, res);
@@ -633,7 +641,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             max_ready = max(max_ready, wr);
             t_next = t + 1u;
             const uint32_t cx = c.x ^ ka.z;
-            const uint32_t rf = fbits(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
+            const uint32_t rf = fbits_hw(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
             const uint32_t ri = a.x * b.x + cx;
             const uint32_t res = ka.x == DOP_FPU ? rf : ri;
             ST_LANE_PAIR(on_all, ka.w, res, wr);
@@ -706,7 +714,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
 #define MB64() ((uint64_t)b0 | ((uint64_t)RG32(lv + B + RB) << 32))
 #define R64(v) do { const uint64_t v_ = (v); lo = (uint32_t)v_; hi = (uint32_t)(v_ >> 32); wide = true; } while (0)
           switch (__shfl_sync(FULL, ka.x, 0)) {
-            case DOP_FPU: lo = fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))); break;
+            case DOP_FPU: lo = fbits_hw(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))); break;
             case DOP_IMAD: lo = a0 * b0 + (c0 ^ aux); break;
             case DOP_MADI: lo = a0 * aux + c0; break;
             case DOP_MADII: lo = a0 * aux + mp[3].x; break;
@@ -1126,7 +1134,7 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
       else switch (op) {
         // ---- the routed datapaths (guarded, or outside a fast run) ----
         case DOP_FPU: case DOP_FPU | DOP_GUARDED:
-          W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))));
+          W32(fbits_hw(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0 ^ aux))));
           pc++;
           break;
         case DOP_IMAD: case DOP_IMAD | DOP_GUARDED:
@@ -1256,11 +1264,11 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           break;
         }
         // ---- f32 (a4), IEEE round-to-nearest-even, canonical NaN ----
-        case OP_FADD: W32(fbits(__fadd_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
-        case OP_FSUB: W32(fbits(__fsub_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
-        case OP_FMUL: W32(fbits(__fmul_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
+        case OP_FADD: W32(fbits_hw(__fadd_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
+        case OP_FSUB: W32(fbits_hw(__fsub_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
+        case OP_FMUL: W32(fbits_hw(__fmul_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;
         case OP_FFMA:
-          W32(fbits(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0))));
+          W32(fbits_hw(__fmaf_rn(__uint_as_float(a0), __uint_as_float(b0), __uint_as_float(c0))));
           pc++;
           break;
         case OP_FDIV: W32(fbits(__fdiv_rn(__uint_as_float(a0), __uint_as_float(b0)))); pc++; break;

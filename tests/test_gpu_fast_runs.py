@@ -95,13 +95,18 @@ def runs_kernel(name, seed, nf, nr, run_len, iters, diverge=0, mid_entry=False):
     return wl.HEADER + "\n".join(L)
 
 
-def runs_workload(seed, nf, nr, run_len, iters, grid=3, block=96, **kw):
+def runs_workload(seed, nf, nr, run_len, iters, grid=3, block=96, fbits=None, **kw):
+    """fbits: bit patterns the f32 inputs are drawn from (default: values in
+    [0.25, 1.5))."""
     name = f"rs{seed}"
     n = nf + nr
     rng = np.random.default_rng(1000 + seed)
     threads = grid * block
     inp = np.empty((threads, n), dtype=np.uint32)
-    inp[:, :nf] = rng.uniform(0.25, 1.5, size=(threads, nf)).astype(np.float32).view(np.uint32)
+    if fbits is None:
+        inp[:, :nf] = rng.uniform(0.25, 1.5, size=(threads, nf)).astype(np.float32).view(np.uint32)
+    else:
+        inp[:, :nf] = rng.choice(np.asarray(fbits, dtype=np.uint32), size=(threads, nf))
     inp[:, nf:] = rng.integers(0, 1 << 32, size=(threads, nr), dtype=np.uint64).astype(np.uint32)
     out = np.zeros((threads, n), dtype=np.uint32)
     bufs = wl.place([("out", out, True), ("inp", inp, False)])
@@ -130,6 +135,91 @@ def test_runs_match_oracle(name, layout):
     for seed in range(3):
         w = runs_workload(seed * 17 + len(name), nf, nr, run_len, iters, **extra)
         _parity.assert_parity(w, cfg=ks.Config(layout=layout))
+
+
+# NaNs with payloads and either sign, signalling NaNs, infinities, zeros,
+# subnormals and ordinary values: IEEE-754 binary32 patterns
+SPECIAL_F32 = [0x7FC00000, 0xFFC00000, 0x7FC12345, 0xFFE00001, 0x7F800001, 0xFF800001, 0x7F800000, 0xFF800000, 0x00000000, 0x80000000, 0x00000001, 0x807FFFFF, 0x7F7FFFFF,
+               0x3F800000, 0xBF400000, 0x3F000000, 0x40490FDB]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_runs_with_nan_payload_inputs(layout):
+    """f32 fast runs whose inputs hold NaNs with payloads (quiet and
+    signalling, either sign), infinities, signed zeros and subnormals: every
+    NaN result is stored as the canonical 0x7FFFFFFF (which no input holds),
+    as the oracle stores it, and every other result bit for bit."""
+    for seed in range(4):
+        w = runs_workload(40 + seed, 6, 1, 24, 2, fbits=SPECIAL_F32)
+        g, _ = _parity.assert_parity(w, cfg=ks.Config(layout=layout))
+        assert (g.buffers[0].view(np.uint32) == 0x7FFFFFFF).any()
+
+
+def guarded_f32_workload(seed):
+    """Guarded f32 add / sub / mul / fma (the general path) and the same ops
+    unguarded and alone between integer ops (the mid loop), on operands drawn
+    from SPECIAL_F32."""
+    ptx = wl.HEADER + """.visible .entry gf(.param .u64 gf_out, .param .u64 gf_inp)
+{
+    .reg .pred %p<3>;
+    .reg .f32 %f<12>;
+    .reg .b32 %r<8>;
+    .reg .b64 %rd<6>;
+    ld.param.u64 %rd1, [gf_out];
+    ld.param.u64 %rd2, [gf_inp];
+    mov.u32 %r1, %ctaid.x;
+    mov.u32 %r2, %ntid.x;
+    mov.u32 %r3, %tid.x;
+    mad.lo.s32 %r4, %r1, %r2, %r3;
+    mul.lo.u32 %r5, %r4, 32;
+    cvt.u64.u32 %rd3, %r5;
+    add.s64 %rd4, %rd2, %rd3;
+    add.s64 %rd5, %rd1, %rd3;
+    ld.global.f32 %f1, [%rd4];
+    ld.global.f32 %f2, [%rd4+4];
+    ld.global.f32 %f3, [%rd4+8];
+    and.b32 %r6, %r3, 1;
+    setp.ne.u32 %p1, %r6, 0;
+    mov.f32 %f4, 0f00000000;
+    mov.f32 %f5, 0f00000000;
+    mov.f32 %f6, 0f00000000;
+    mov.f32 %f7, 0f00000000;
+    @%p1 add.rn.f32 %f4, %f1, %f2;
+    @!%p1 sub.rn.f32 %f5, %f2, %f3;
+    @%p1 mul.rn.f32 %f6, %f3, %f1;
+    @!%p1 fma.rn.f32 %f7, %f1, %f2, %f3;
+    add.rn.f32 %f8, %f1, %f3;
+    xor.b32 %r7, %r6, 1;
+    mul.rn.f32 %f9, %f2, %f2;
+    xor.b32 %r7, %r7, 3;
+    fma.rn.f32 %f10, %f3, %f2, %f1;
+    st.global.f32 [%rd5], %f4;
+    st.global.f32 [%rd5+4], %f5;
+    st.global.f32 [%rd5+8], %f6;
+    st.global.f32 [%rd5+12], %f7;
+    st.global.f32 [%rd5+16], %f8;
+    st.global.f32 [%rd5+20], %f9;
+    st.global.f32 [%rd5+24], %f10;
+    st.global.u32 [%rd5+28], %r7;
+    ret;
+}
+"""
+    grid, block = 2, 128
+    rng = np.random.default_rng(2000 + seed)
+    inp = np.zeros((grid * block, 8), dtype=np.uint32)
+    inp[:, :3] = rng.choice(np.asarray(SPECIAL_F32, dtype=np.uint32), size=(grid * block, 3))
+    out = np.zeros((grid * block, 8), dtype=np.uint32)
+    bufs = wl.place([("out", out, True), ("inp", inp, False)])
+    params = wl.pack_params([("u64", bufs[0].sim_base), ("u64", bufs[1].sim_base)])
+    return wl.Workload(f"gf{seed}", ptx, "gf", grid, block, params, bufs, max_ts=0)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_guarded_and_lone_f32_ops_with_nan_payload_inputs(layout):
+    for seed in range(3):
+        w = guarded_f32_workload(seed)
+        g, _ = _parity.assert_parity(w, cfg=ks.Config(layout=layout))
+        assert (g.buffers[0].view(np.uint32) == 0x7FFFFFFF).any()
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)
