@@ -1343,6 +1343,14 @@ class Decoder {
       if (o.c == pd) o.inc |= INC_FWD_C;
       if (o.a == pd || o.b == pd || o.c == pd || o.d == pd) o.inc |= INC_FWD_T;
     }
+    // runs (from each op to the run's end) whose ops all write a row they read
+    for (size_t i = n; i-- > 0;) {
+      DevInsn& o = dev[i];
+      if ((o.inc >> INC_RUN_SHIFT) == 0u) continue;  // not in a fast run
+      const bool own = o.d == o.a || o.d == o.b || o.d == o.c;
+      const bool rest = (o.inc >> INC_RUN_SHIFT) == 1u || (dev[i + 1].inc & INC_OWN_D) != 0u;
+      if (own && rest) o.inc |= INC_OWN_D;
+    }
     K.prog_bytes = (uint32_t)((n + 1) * sizeof(DevInsn));
     const size_t cb = rowval.size() * 4;
     std::vector<uint8_t>& img = K.image[split];

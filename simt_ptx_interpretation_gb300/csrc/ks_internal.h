@@ -204,6 +204,10 @@ constexpr uint32_t INC_MID = 8u, INC_PHAZ = 16u;
 // INC_FWD_A/B/C, operand a / b / c is the previous entry's destination;
 // INC_FWD_T, one of its scoreboard terms is that destination's ready word.
 constexpr uint32_t INC_FWD_A = 1u << 9, INC_FWD_B = 1u << 10, INC_FWD_C = 1u << 11, INC_FWD_T = 1u << 12;
+// INC_OWN_D: this fast op and every op after it in its run write a row they
+// also read (d is a, b or c), so the destination's ready time is already one
+// of the op's scoreboard terms (the PAIR fast loop then skips its load)
+constexpr uint32_t INC_OWN_D = 1u << 13;
 constexpr uint32_t OP_EXIT = 0xFE;  // sentinel at index n_insn: the remaining lanes finish
 // Unified datapaths selected at resolve time (DevInsn::op only):
 //   DOP_FPU:  d = fma.rn(a, b, c ^ aux)      add: b = 1.0, c = y;  sub: b = 1.0, c = y, aux = sign bit;

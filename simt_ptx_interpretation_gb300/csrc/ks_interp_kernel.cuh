@@ -57,6 +57,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 
 #include "ks_internal.h"
 
@@ -623,51 +624,63 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           if constexpr (RUNLOG) run_next = pc;
           continue;
         } else {
-          uint32_t n = run_n;
-          const bool on_all = (mask >> lane) & 1u;
-          // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
-          uint4 ka = q0, kb = q1;
-          uint2 a = RG2(lv + kb.x), b = RG2(lv + kb.y), c = RG2(lv + kb.z);
-          uint32_t rd = RG32(rdb + ka.w + 4u);
-          // instruction k+1 (the last instruction is never a fast op, so k+1 and
-          // k+2 stay within the program and its exit sentinel)
-          uint4 na = ip[4], nb = ip[5];
-          for (;;) {
-            uint2 a1 = RG2(lv + nb.x), b1 = RG2(lv + nb.y), c1 = RG2(lv + nb.z);
-            uint32_t rd1 = RG32(rdb + na.w + 4u);
-            const uint4 ma = ip[8], mb = ip[9];
-            const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));
-            const uint32_t wr = t + ka.y;
-            max_ready = max(max_ready, wr);
-            t_next = t + 1u;
-            const uint32_t cx = c.x ^ ka.z;
-            const uint32_t rf = fbits_hw(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
-            const uint32_t ri = a.x * b.x + cx;
-            const uint32_t res = ka.x == DOP_FPU ? rf : ri;
-            ST_LANE_PAIR(on_all, ka.w, res, wr);
-            // forward k into k+1 (the decoder's INC_FWD_* flags of k+1): the
-            // value into each operand that is k's destination -- in every
-            // lane: a lane outside the mask stores nothing during the run, so
-            // what it computes from a forwarded value is never seen -- and
-            // k's ready time into k+1's scoreboard, through the destination
-            // term (every term of k+1 is maxed together, and a stale entry of
-            // k's destination is never later than k's own ready time)
-            const uint32_t f = nb.w;
-            a1.x = (f & INC_FWD_A) ? res : a1.x;
-            b1.x = (f & INC_FWD_B) ? res : b1.x;
-            c1.x = (f & INC_FWD_C) ? res : c1.x;
-            rd1 = (f & INC_FWD_T) ? max(rd1, wr) : rd1;
-            ka = na;
-            kb = nb;
-            na = ma;
-            nb = mb;
-            a = a1;
-            b = b1;
-            c = c1;
-            rd = rd1;
-            ip += 4;
-            if (--n == 0u) break;  // uniform in value
-          }
+          // The loop in two forms: with the destination's ready word as a
+          // scoreboard term, and (runs whose every op writes a row it reads,
+          // INC_OWN_D) without it, that term being one of the rows'. The
+          // register-capped forms keep the first only (their launches are
+          // bound by registers, which the second copy would raise).
+          auto pair_run = [&](auto with_rd) {
+            constexpr bool RD = decltype(with_rd)::value;
+            uint32_t n = run_n;
+            const bool on_all = (mask >> lane) & 1u;
+            // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
+            uint4 ka = q0, kb = q1;
+            uint2 a = RG2(lv + kb.x), b = RG2(lv + kb.y), c = RG2(lv + kb.z);
+            uint32_t rd = RD ? RG32(rdb + ka.w + 4u) : 0u;
+            // instruction k+1 (the last instruction is never a fast op, so k+1
+            // and k+2 stay within the program and its exit sentinel)
+            uint4 na = ip[4], nb = ip[5];
+            for (;;) {
+              uint2 a1 = RG2(lv + nb.x), b1 = RG2(lv + nb.y), c1 = RG2(lv + nb.z);
+              uint32_t rd1 = RD ? RG32(rdb + na.w + 4u) : 0u;
+              const uint4 ma = ip[8], mb = ip[9];
+              const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));
+              const uint32_t wr = t + ka.y;
+              max_ready = max(max_ready, wr);
+              t_next = t + 1u;
+              const uint32_t cx = c.x ^ ka.z;
+              const uint32_t rf = fbits_hw(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
+              const uint32_t ri = a.x * b.x + cx;
+              const uint32_t res = ka.x == DOP_FPU ? rf : ri;
+              ST_LANE_PAIR(on_all, ka.w, res, wr);
+              // forward k into k+1 (the decoder's INC_FWD_* flags of k+1): the
+              // value into each operand that is k's destination -- in every
+              // lane: a lane outside the mask stores nothing during the run,
+              // so what it computes from a forwarded value is never seen --
+              // and k's ready time into k+1's scoreboard, through the
+              // destination term (every term of k+1 is maxed together, and a
+              // stale entry of k's destination is never later than k's own
+              // ready time)
+              const uint32_t f = nb.w;
+              a1.x = (f & INC_FWD_A) ? res : a1.x;
+              b1.x = (f & INC_FWD_B) ? res : b1.x;
+              c1.x = (f & INC_FWD_C) ? res : c1.x;
+              if constexpr (RD) rd1 = (f & INC_FWD_T) ? max(rd1, wr) : rd1;
+              else rd1 = (f & INC_FWD_T) ? wr : 0u;
+              ka = na;
+              kb = nb;
+              na = ma;
+              nb = mb;
+              a = a1;
+              b = b1;
+              c = c1;
+              rd = rd1;
+              ip += 4;
+              if (--n == 0u) break;  // uniform in value
+            }
+          };
+          if (!CAP && (q1.w & INC_OWN_D)) pair_run(std::false_type{});
+          else pair_run(std::true_type{});
           pc += run_n;
           budget -= run_n;
           t_last = t_next - 1u;
