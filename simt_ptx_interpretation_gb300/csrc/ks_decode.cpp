@@ -1351,6 +1351,22 @@ class Decoder {
       const bool rest = (o.inc >> INC_RUN_SHIFT) == 1u || (dev[i + 1].inc & INC_OWN_D) != 0u;
       if (own && rest) o.inc |= INC_OWN_D;
     }
+    // PAIR: how many ops from each run op on keep reading its b and c rows
+    // (rows the op before does not write), in x[4] (hc: fast ops have no
+    // predicate operands)
+    if (!split) {
+      for (size_t i = n; i-- > 0;) {
+        DevInsn& o = dev[i];
+        const uint32_t len = o.inc >> INC_RUN_SHIFT;
+        if (len == 0u) continue;
+        uint32_t keep = 1u;
+        if (len > 1u) {
+          const DevInsn& x = dev[i + 1];
+          if (x.b == o.b && x.c == o.c && o.b != o.d && o.c != o.d) keep = 1u + x.x[4];
+        }
+        o.x[4] = keep;
+      }
+    }
     K.prog_bytes = (uint32_t)((n + 1) * sizeof(DevInsn));
     const size_t cb = rowval.size() * 4;
     std::vector<uint8_t>& img = K.image[split];

@@ -149,7 +149,10 @@ struct alignas(16) DevInsn {
   // q2, q3 by layout (x[6] = dlat and x[7] = nlat in both):
   //   PAIR:  guard, gneg, ha, hb, hc, hd, dlat, nlat
   //          ha/hb/hc/hd: predicate-table offsets of predicate sources /
-  //          destination (entry 31 if absent); DOP_MADII: hc = its immediate
+  //          destination (entry 31 if absent); DOP_MADII: hc = its immediate;
+  //          a fast op in a run: hc = the ops from it on (itself included)
+  //          that read the same b and c rows as it, which none of them but
+  //          the last writes (the fast loop then loads those rows once)
   //   SPLIT: hz[0..3], guard, gneg, dlat, nlat
   //          hz: ready-word offsets (16 bits each, region-relative) of the
   //          scoreboard terms: halfwords 0..3 = rows a, b, c and the

@@ -629,12 +629,12 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           // INC_OWN_D) without it, that term being one of the rows'. The
           // register-capped forms keep the first only (their launches are
           // bound by registers, which the second copy would raise).
-          auto pair_run = [&](auto with_rd) {
+          const bool on_all = (mask >> lane) & 1u;
+          // n ops from ip on, the first one's record halves k0, k1
+          auto pair_run = [&](auto with_rd, uint32_t n, const uint4 k0, const uint4 k1) {
             constexpr bool RD = decltype(with_rd)::value;
-            uint32_t n = run_n;
-            const bool on_all = (mask >> lane) & 1u;
             // instruction k: {op, wlat, aux, d}, {a, b, c, inc}; its rows
-            uint4 ka = q0, kb = q1;
+            uint4 ka = k0, kb = k1;
             uint2 a = RG2(lv + kb.x), b = RG2(lv + kb.y), c = RG2(lv + kb.z);
             uint32_t rd = RD ? RG32(rdb + ka.w + 4u) : 0u;
             // instruction k+1 (the last instruction is never a fast op, so k+1
@@ -679,8 +679,51 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
               if (--n == 0u) break;  // uniform in value
             }
           };
-          if (!CAP && (q1.w & INC_OWN_D)) pair_run(std::false_type{});
-          else pair_run(std::true_type{});
+          if (CAP || !(q1.w & INC_OWN_D)) {
+            pair_run(std::true_type{}, run_n, q0, q1);
+          } else {
+            // A run prefix whose ops read the same b and c rows (q3.x: hc of
+            // a fast op), which no op of it but the last writes: those rows
+            // are loaded once, and only a, the record and the result move
+            // per op (then the rest of the run, its rows loaded afresh).
+            const uint32_t keep = min(run_n, q3.x);
+            if (keep < 2u) {
+              pair_run(std::false_type{}, run_n, q0, q1);
+            } else {
+              uint32_t n = keep;
+              uint4 ka = q0, kb = q1;
+              uint2 a = RG2(lv + kb.x);
+              const uint2 b = RG2(lv + kb.y), c = RG2(lv + kb.z);
+              uint32_t rd = 0;
+              uint4 na = ip[4], nb = ip[5];
+              for (;;) {
+                uint2 a1 = RG2(lv + nb.x);
+                const uint4 ma = ip[8], mb = ip[9];
+                const uint32_t t = max(max(t_next, a.y), max(max(b.y, c.y), rd));
+                const uint32_t wr = t + ka.y;
+                max_ready = max(max_ready, wr);
+                t_next = t + 1u;
+                const uint32_t cx = c.x ^ ka.z;
+                const uint32_t rf =
+                    fbits_hw(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
+                const uint32_t ri = a.x * b.x + cx;
+                const uint32_t res = ka.x == DOP_FPU ? rf : ri;
+                ST_LANE_PAIR(on_all, ka.w, res, wr);
+                // forward k into k+1 (its b and c are not k's destination)
+                const uint32_t f = nb.w;
+                a1.x = (f & INC_FWD_A) ? res : a1.x;
+                rd = (f & INC_FWD_T) ? wr : 0u;
+                ka = na;
+                kb = nb;
+                na = ma;
+                nb = mb;
+                a = a1;
+                ip += 4;
+                if (--n == 0u) break;  // uniform in value
+              }
+              if (run_n > keep) pair_run(std::false_type{}, run_n - keep, ip[0], ip[1]);
+            }
+          }
           pc += run_n;
           budget -= run_n;
           t_last = t_next - 1u;
