@@ -624,11 +624,13 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
           if constexpr (RUNLOG) run_next = pc;
           continue;
         } else {
-          // The loop in two forms: with the destination's ready word as a
-          // scoreboard term, and (runs whose every op writes a row it reads,
-          // INC_OWN_D) without it, that term being one of the rows'. The
-          // register-capped forms keep the first only (their launches are
-          // bound by registers, which the second copy would raise).
+          // The loop in three forms: with the destination's ready word as a
+          // scoreboard term; without it (runs whose every op writes a row it
+          // reads, INC_OWN_D: that term is one of the rows'); and, in such
+          // runs, for a prefix that keeps reading the same b and c rows,
+          // without their loads either (below). The register-capped forms
+          // keep the first only (their launches are bound by registers,
+          // which the other copies would raise).
           const bool on_all = (mask >> lane) & 1u;
           // n ops from ip on, the first one's record halves k0, k1
           auto pair_run = [&](auto with_rd, uint32_t n, const uint4 k0, const uint4 k1) {
