@@ -283,6 +283,18 @@ int ks_kernel_event(const ks_module* mod, const char* kernel, uint32_t id, uint3
  * (instructions and pseudo-ops in order); the virtual exit is *n_out. */
 int ks_kernel_ipdom(const ks_module* mod, const char* kernel, int32_t* out, uint32_t cap,
                     uint32_t* n_out);
+/* The interpreter's fast-path runs in the PAIR register layout, per program
+ * entry (order of ks_kernel_ipdom), three words each (no counterpart on the
+ * pages: it describes how this library runs the kernel, not what it
+ * computes): out[3i] = the consecutive unguarded FMA / IMAD-type ops from
+ * entry i to the end of its run in the fast loop (0: entry i is not in
+ * one); out[3i+1] = 1 when every one of them writes a row it also reads
+ * (the loop then skips the destination's ready-time load); out[3i+2] = how
+ * many of them, from i on, read entry i's b and c rows while none of them
+ * but the last writes those (loaded once for all of them). cap is in
+ * entries; *n_out receives the number of entries. */
+int ks_kernel_fast_runs(const ks_module* mod, const char* kernel, uint32_t* out, uint32_t cap,
+                        uint32_t* n_out);
 /* The register-file layout a launch of `kernel` with these ks_config.flags
  * runs in (*split: 0 PAIR, 1 SPLIT; see KS_FLAG_LAYOUT_*) and the shared
  * memory each simulated warp's state takes in it (*region_bytes). Errors are

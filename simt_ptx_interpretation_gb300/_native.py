@@ -92,6 +92,8 @@ EXPORTS = {
                                        ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_char_p)]),
     "ks_kernel_ipdom": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                        ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
+    "ks_kernel_fast_runs": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.POINTER(ctypes.c_uint32),
+                                           ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
     "ks_kernel_layout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint32,
                                         ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)]),
     "ks_trace_bytes": (ctypes.c_size_t, [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]),

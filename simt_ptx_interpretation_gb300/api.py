@@ -178,6 +178,16 @@ class Module:
         _check(_native.lib().ks_kernel_ipdom(self._h, kernel.encode(), arr, n, ctypes.byref(cnt)))
         return [arr[i] for i in range(cnt.value)]
 
+    def fast_runs(self, kernel: str) -> list[tuple[int, bool, int]]:
+        """Per program entry: (ops from it to the end of its fast-loop run,
+        0 outside one; whether every one of them writes a row it reads; how
+        many of them keep reading its b and c rows), PAIR layout."""
+        n = self.info(kernel)["n_insns"]
+        arr = (ctypes.c_uint32 * max(1, 3 * n))()
+        cnt = ctypes.c_uint32()
+        _check(_native.lib().ks_kernel_fast_runs(self._h, kernel.encode(), arr, n, ctypes.byref(cnt)))
+        return [(arr[3 * i], bool(arr[3 * i + 1]), arr[3 * i + 2]) for i in range(cnt.value)]
+
     def layout(self, kernel: str, layout: str = "auto") -> tuple[str, int]:
         """The register-file layout a launch with Config(layout=layout) runs
         in ("pair" or "split") and the shared memory per simulated warp."""

@@ -252,6 +252,23 @@ int ks_kernel_ipdom(const ks_module* mod, const char* kernel, int32_t* out, uint
   return KS_OK;
 }
 
+int ks_kernel_fast_runs(const ks_module* mod, const char* kernel, uint32_t* out, uint32_t cap, uint32_t* n_out) {
+  const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);
+  if (!k) return mod && kernel ? KS_ERR_NOT_FOUND : KS_ERR_ARG;
+  const size_t n = k->code.size();
+  if (n_out) *n_out = (uint32_t)n;
+  if (out) {
+    const ks::DevInsn* d = reinterpret_cast<const ks::DevInsn*>(k->image[0].data());
+    for (size_t i = 0; i < n && i < cap; i++) {
+      const uint32_t len = d[i].inc >> ks::INC_RUN_SHIFT;
+      out[3 * i] = len;
+      out[3 * i + 1] = (len && (d[i].inc & ks::INC_OWN_D)) ? 1u : 0u;
+      out[3 * i + 2] = len ? d[i].x[4] : 0u;
+    }
+  }
+  return KS_OK;
+}
+
 int ks_kernel_layout(const ks_module* mod, const char* kernel, uint32_t flags, uint32_t* split,
                      uint32_t* region_bytes) {
   const ks::KsKernel* k = find_kernel(mod, kernel, nullptr);

@@ -312,3 +312,44 @@ def test_register_layout_choice():
     assert lib.ks_kernel_layout(v._h, b"vector_add", 3, ctypes.byref(sp), ctypes.byref(rb)) == -3  # both flags
     assert lib.ks_kernel_layout(v._h, b"vector_add", 4, ctypes.byref(sp), ctypes.byref(rb)) == -3  # unknown bit
     assert lib.ks_kernel_layout(v._h, b"nope", 0, ctypes.byref(sp), ctypes.byref(rb)) == -5
+
+
+def test_fast_runs_follow_the_programs_shape():
+    """ks_kernel_fast_runs reports the decoder's fast-loop runs (PAIR layout):
+    their lengths, whether every op of a run's rest writes a row it reads,
+    and how far each op's b and c rows keep being read unwritten. Pinned on
+    the FFMA probe (32 `fma acc, acc, m, add` and the counter's add in one
+    run) and on hand-made runs where a row stops being kept."""
+    for acc in (1, 8):
+        w = wl.ffma(acc=acc, iters=16, per_iter=32)
+        runs = ks.Module(w.ptx).fast_runs(w.kernel)
+        starts = [i for i, (n, _, _) in enumerate(runs) if n == 33]
+        assert len(starts) == 1, runs
+        s = starts[0]
+        for j in range(33):
+            n, own, keep = runs[s + j]
+            assert n == 33 - j and own
+            # the 32 FMAs keep m and add; the counter's add reads other rows
+            assert keep == (32 - j if j < 32 else 1)
+    body = "\n".join([
+        "    fma.rn.f32 %f1, %f1, %f2, %f3;",   # keeps f2, f3 into the next op
+        "    fma.rn.f32 %f2, %f1, %f2, %f3;",   # writes its own b: the next op reloads
+        "    fma.rn.f32 %f3, %f1, %f2, %f3;",
+        "    fma.rn.f32 %f5, %f1, %f2, %f4;",   # writes a row it does not read
+        "    fma.rn.f32 %f1, %f1, %f2, %f4;",
+        "    fma.rn.f32 %f1, %f1, %f2, %f4;",
+    ])
+    ptx = (wl.HEADER + ".visible .entry fr(.param .u64 fr_out)\n{\n    .reg .f32 %f<6>;\n    .reg .b64 %rd<2>;\n"
+           "    ld.param.u64 %rd1, [fr_out];\n    ld.global.f32 %f1, [%rd1];\n    ld.global.f32 %f2, [%rd1+4];\n"
+           "    ld.global.f32 %f3, [%rd1+8];\n    ld.global.f32 %f4, [%rd1+12];\n" + body + "\n"
+           "    st.global.f32 [%rd1], %f1;\n    st.global.f32 [%rd1+4], %f5;\n    ret;\n}\n")
+    runs = ks.Module(ptx).fast_runs("fr")
+    first = next(i for i, (n, _, _) in enumerate(runs) if n)
+    got = runs[first:first + 6]
+    assert [n for n, _, _ in got] == [6, 5, 4, 3, 2, 1]
+    # the op writing %f5 (not among its sources) clears the flag for it and
+    # every op before it in the run
+    assert [own for _, own, _ in got] == [False, False, False, False, True, True]
+    # f2, f3 kept into the op that writes f2; f2, f4 kept from the %f5 op on
+    assert [keep for _, _, keep in got] == [2, 1, 1, 3, 2, 1]
+    assert all(r == (0, False, 0) for i, r in enumerate(runs) if not first <= i < first + 6)
