@@ -263,7 +263,7 @@ int ks_kernel_fast_runs(const ks_module* mod, const char* kernel, uint32_t* out,
       const uint32_t len = d[i].inc >> ks::INC_RUN_SHIFT;
       out[3 * i] = len;
       out[3 * i + 1] = (len && (d[i].inc & ks::INC_OWN_D)) ? 1u : 0u;
-      out[3 * i + 2] = len ? d[i].x[4] : 0u;
+      out[3 * i + 2] = len ? (d[i].x[4] & ks::KEEP_COUNT) : 0u;
     }
   }
   return KS_OK;

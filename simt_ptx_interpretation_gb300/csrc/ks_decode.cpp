@@ -1352,19 +1352,23 @@ class Decoder {
       if (own && rest) o.inc |= INC_OWN_D;
     }
     // PAIR: how many ops from each run op on keep reading its b and c rows
-    // (rows the op before does not write), in x[4] (hc: fast ops have no
-    // predicate operands)
+    // (rows the op before does not write), and whether all of them are f32
+    // ops, in x[4] (hc: fast ops have no predicate operands)
     if (!split) {
       for (size_t i = n; i-- > 0;) {
         DevInsn& o = dev[i];
         const uint32_t len = o.inc >> INC_RUN_SHIFT;
         if (len == 0u) continue;
         uint32_t keep = 1u;
+        bool fpu = o.op == DOP_FPU;
         if (len > 1u) {
           const DevInsn& x = dev[i + 1];
-          if (x.b == o.b && x.c == o.c && o.b != o.d && o.c != o.d) keep = 1u + x.x[4];
+          if (x.b == o.b && x.c == o.c && o.b != o.d && o.c != o.d) {
+            keep = 1u + (x.x[4] & KEEP_COUNT);
+            fpu = fpu && (x.x[4] & KEEP_FPU) != 0u;
+          }
         }
-        o.x[4] = keep;
+        o.x[4] = keep | (fpu ? KEEP_FPU : 0u);
       }
     }
     K.prog_bytes = (uint32_t)((n + 1) * sizeof(DevInsn));

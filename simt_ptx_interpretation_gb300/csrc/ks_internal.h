@@ -152,7 +152,8 @@ struct alignas(16) DevInsn {
   //          destination (entry 31 if absent); DOP_MADII: hc = its immediate;
   //          a fast op in a run: hc = the ops from it on (itself included)
   //          that read the same b and c rows as it, which none of them but
-  //          the last writes (the fast loop then loads those rows once)
+  //          the last writes (the fast loop then loads those rows once), in
+  //          KEEP_COUNT, and KEEP_FPU when all of them are DOP_FPU
   //   SPLIT: hz[0..3], guard, gneg, dlat, nlat
   //          hz: ready-word offsets (16 bits each, region-relative) of the
   //          scoreboard terms: halfwords 0..3 = rows a, b, c and the
@@ -211,6 +212,8 @@ constexpr uint32_t INC_FWD_A = 1u << 9, INC_FWD_B = 1u << 10, INC_FWD_C = 1u << 
 // also read (d is a, b or c), so the destination's ready time is already one
 // of the op's scoreboard terms (the PAIR fast loop then skips its load)
 constexpr uint32_t INC_OWN_D = 1u << 13;
+// the fields of a PAIR fast op's hc word (DevInsn::x[4])
+constexpr uint32_t KEEP_COUNT = 0xFFFFu, KEEP_FPU = 1u << 31;
 constexpr uint32_t OP_EXIT = 0xFE;  // sentinel at index n_insn: the remaining lanes finish
 // Unified datapaths selected at resolve time (DevInsn::op only):
 //   DOP_FPU:  d = fma.rn(a, b, c ^ aux)      add: b = 1.0, c = y;  sub: b = 1.0, c = y, aux = sign bit;

@@ -688,10 +688,10 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
             // a fast op), which no op of it but the last writes: those rows
             // are loaded once, and only a, the record and the result move
             // per op (then the rest of the run, its rows loaded afresh).
-            const uint32_t keep = min(run_n, q3.x);
-            if (keep < 2u) {
-              pair_run(std::false_type{}, run_n, q0, q1);
-            } else {
+            const uint32_t keep = min(run_n, q3.x & KEEP_COUNT);
+            // FPU: every op of the prefix is an f32 op (no integer datapath)
+            auto keep_run = [&](auto fpu_only) {
+              constexpr bool FPU = decltype(fpu_only)::value;
               uint32_t n = keep;
               uint4 ka = q0, kb = q1;
               uint2 a = RG2(lv + kb.x);
@@ -708,8 +708,8 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
                 const uint32_t cx = c.x ^ ka.z;
                 const uint32_t rf =
                     fbits_hw(__fmaf_rn(__uint_as_float(a.x), __uint_as_float(b.x), __uint_as_float(cx)));
-                const uint32_t ri = a.x * b.x + cx;
-                const uint32_t res = ka.x == DOP_FPU ? rf : ri;
+                uint32_t res = rf;
+                if constexpr (!FPU) res = ka.x == DOP_FPU ? rf : a.x * b.x + cx;
                 ST_LANE_PAIR(on_all, ka.w, res, wr);
                 // forward k into k+1 (its b and c are not k's destination)
                 const uint32_t f = nb.w;
@@ -723,6 +723,12 @@ __global__ void __launch_bounds__(CAP ? (CTA ? 256 : 320) : (BIG ? 1024 : (CTA ?
                 ip += 4;
                 if (--n == 0u) break;  // uniform in value
               }
+            };
+            if (keep < 2u) {
+              pair_run(std::false_type{}, run_n, q0, q1);
+            } else {
+              if (q3.x & KEEP_FPU) keep_run(std::true_type{});
+              else keep_run(std::false_type{});
               if (run_n > keep) pair_run(std::false_type{}, run_n - keep, ip[0], ip[1]);
             }
           }
