@@ -353,3 +353,25 @@ def test_fast_runs_follow_the_programs_shape():
     # f2, f3 kept into the op that writes f2; f2, f4 kept from the %f5 op on
     assert [keep for _, _, keep in got] == [2, 1, 1, 3, 2, 1]
     assert all(r == (0, False, 0) for i, r in enumerate(runs) if not first <= i < first + 6)
+
+
+def test_fast_runs_are_consistent_on_every_workload():
+    """Over every benchmark kernel (and the fuzz corpus): a run's length
+    drops by one per entry; the own-destination flag, once set, holds to the
+    run's end; a kept-rows count never exceeds the run and counts down along
+    its prefix."""
+    ws = [wl.vector_add(), wl.ffma(acc=1), wl.ffma(acc=8), wl.gather(8), wl.divergent(4), wl.smem_reduce()]
+    ws += [wl.fuzz(i) for i in range(0, 64, 4)]
+    for w in ws:
+        runs = ks.Module(w.ptx).fast_runs(w.kernel)
+        for i, (n, own, keep) in enumerate(runs):
+            if n == 0:
+                assert (own, keep) == (False, 0), (w.name, i)
+                continue
+            assert 1 <= keep <= n, (w.name, i)
+            if n > 1:
+                n1, own1, keep1 = runs[i + 1]
+                assert n1 == n - 1, (w.name, i)
+                assert own1 or not own, (w.name, i)
+                if keep > 1:
+                    assert keep1 == keep - 1, (w.name, i)
