@@ -353,6 +353,16 @@ def test_fast_runs_follow_the_programs_shape():
     # f2, f3 kept into the op that writes f2; f2, f4 kept from the %f5 op on
     assert [keep for _, _, keep in got] == [2, 1, 1, 3, 2, 1]
     assert all(r == (0, False, 0) for i, r in enumerate(runs) if not first <= i < first + 6)
+    # argument errors; a short buffer receives what fits, n_out the whole count
+    lib = _native.lib()
+    m = ks.Module(ptx)
+    cnt = ctypes.c_uint32()
+    assert lib.ks_kernel_fast_runs(None, b"fr", None, 0, ctypes.byref(cnt)) == -3
+    assert lib.ks_kernel_fast_runs(m._h, b"nope", None, 0, ctypes.byref(cnt)) == -5
+    short = (ctypes.c_uint32 * 6)(*([0xDEADBEEF] * 6))
+    assert lib.ks_kernel_fast_runs(m._h, b"fr", short, 1, ctypes.byref(cnt)) == 0
+    assert cnt.value == len(runs)
+    assert tuple(short[:3]) == (runs[0][0], int(runs[0][1]), runs[0][2]) and short[3] == 0xDEADBEEF
 
 
 def test_fast_runs_are_consistent_on_every_workload():
